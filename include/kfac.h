@@ -1,0 +1,211 @@
+/*
+ * kfac.h -- C ABI of the GB300 (sm_103a) K-FAC preconditioning step.
+ *
+ * The step follows "Accelerating Distributed K-FAC with Smart Parallelism of
+ * Computing and Communication Tasks" (SPD-KFAC):
+ *   1. kfac_factors        per-worker Kronecker factors A^p = a_p^T a_p / rows_p
+ *                          and G^p = g_p^T g_p / rows_p            (§II-B, Eq. (7), (8))
+ *   2. kfac_update_running mean over the P workers (the D-KFAC aggregation,
+ *                          §II-C), running average over steps, Tikhonov
+ *                          damping R + gamma*I                      (§II-B damped update rule)
+ *   3. kfac_damped_inverse (A + gamma I)^-1, (G + gamma I)^-1 through a
+ *                          Cholesky decomposition                   (§III-B, §IV)
+ *   4. kfac_precondition   (G + gamma I)^-1 grad (A + gamma I)^-1   (§II-B damped update rule)
+ *
+ * Conventions shared by every call
+ *   - All matrices are row-major.  "ld" is the leading dimension in elements.
+ *   - Every data pointer is a DEVICE pointer, 16-byte aligned.  Every array of
+ *     argument structs is a HOST array that is read during the call only.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream), never synchronise the host, and never
+ *     allocate device memory.  Scratch memory is caller-provided ("workspace")
+ *     and sized by the matching *_workspace query.
+ *   - The caller owns every buffer.  Nothing is retained between calls, so the
+ *     K-FAC state (the running factors) lives in caller buffers.
+ *   - Argument errors are detected on the host before any launch and return
+ *     KFAC_ERR_INVALID_ARG; a failed launch returns KFAC_ERR_CUDA.  Numerical
+ *     failure of an inverse is reported per matrix in a device `info` array.
+ *   - Symmetric factors are produced and consumed as UPPER TILES: with the
+ *     128-row tile grid, element (r, c) belongs to an upper tile when
+ *     c >= 128 * floor(r / 128).  Elements of lower tiles are not written by
+ *     kfac_factors / kfac_update_running (unless `mirror` is set) and are
+ *     never read by kfac_update_running / kfac_damped_inverse.
+ *   - Device kernels never trap.  A device-side wait that runs past its limit
+ *     (a scheduling bug, never expected) records KFAC_ERR_TIMEOUT in a device
+ *     status word, read and cleared with kfac_device_status().
+ *
+ * Not thread-safe for concurrent calls on the same stream's buffers (the
+ * caller orders its own buffers); calls on independent buffers may run on
+ * different streams.
+ */
+#ifndef KFAC_GB300_H
+#define KFAC_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status */
+enum kfac_status {
+  KFAC_OK = 0,
+  KFAC_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or parameter      */
+  KFAC_ERR_NOT_SPD = 2,     /* only as a value of info[] semantics, see below */
+  KFAC_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed    */
+  KFAC_ERR_UNSUPPORTED = 4, /* device is not sm_103 / feature unavailable     */
+  KFAC_ERR_TIMEOUT = 5,     /* a bounded device wait gave up (device status)  */
+  KFAC_ERR_WORKSPACE = 6    /* workspace NULL or smaller than the query       */
+};
+
+enum kfac_dtype { KFAC_BF16 = 0, KFAC_FP32 = 1 };
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* kfac_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int kfac_version(void);
+
+/* Number of CUDA kernels this library has launched in this process so far
+ * (all devices, all streams).  For accounting only; host only. */
+unsigned long long kfac_launch_count(void);
+
+/* Read the device status word (KFAC_OK or KFAC_ERR_TIMEOUT) recorded by any
+ * kernel of this library on the current device; clears it when `clear` != 0.
+ * Synchronises `stream`. */
+int kfac_device_status(int* status_out, int clear, void* stream);
+
+/* -------------------------------------------------------- 1. factors (a1, a2)
+ * Per-worker Kronecker factors (§II-B, Eq. (7)/(8); §II-C local factors).
+ * For each problem, x holds `rows` rows split into P equal contiguous shards
+ * of rows_p = rows / P rows (worker p owns rows [p*rows_p, (p+1)*rows_p)):
+ *
+ *     out[p] = scale * x_p^T x_p          (d x d, fp32, p = 0..P-1)
+ *
+ * with out[p] = out + p * stride_out.  Use scale = 1/rows_p for the mean of
+ * the paper's factors.  Only upper tiles are written (see conventions); with
+ * mirror != 0 the lower tiles are written too, giving full symmetric output.
+ *
+ * x: KFAC_BF16 -> tcgen05 tensor cores (bf16 products, fp32 accumulation),
+ *               ld_x % 8 == 0;
+ *    KFAC_FP32 -> fp32 CUDA-core path (exact fp32 products), ld_x % 4 == 0.
+ * out: ld_out % 4 == 0, ld_out >= d, stride_out >= d * ld_out (or 0 if P == 1).
+ * Limits per call: n <= 4096 problems, 1 <= d <= 65536, rows % P == 0.
+ */
+typedef struct {
+  const void* x;       /* device, rows x d, element type = dtype */
+  int64_t rows;        /* total rows of all P shards             */
+  int64_t d;           /* factor dimension                       */
+  int64_t ld_x;        /* leading dimension of x (elements)      */
+  float* out;          /* device, P fp32 matrices d x d          */
+  int64_t ld_out;      /* leading dimension of out (elements)    */
+  int64_t stride_out;  /* elements between out[p] and out[p+1]   */
+  float scale;         /* multiplies x_p^T x_p                   */
+} kfac_factor_args;
+
+int kfac_factors(int n, const kfac_factor_args* args, int dtype, int P,
+                 int mirror, void* stream);
+
+/* Conv helper for the G factor of a conv layer (the pages do not describe
+ * conv factors; the per-sample spatial sum is the reading taken):
+ *     gs[b, c] = sum_{s < hw} g[b*hw + s, c]     (fp32 accumulate and out)
+ * g: batch*hw x C, dtype bf16 (ld_g % 8 == 0) or fp32 (ld_g % 4 == 0);
+ * gs: batch x C fp32, ld_gs % 4 == 0.                                       */
+int kfac_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw,
+                     int64_t C, int64_t ld_g, float* gs, int64_t ld_gs,
+                     void* stream);
+
+/* --------------------------------------- 2. reduce + running average + damp (a3)
+ * One fused pass over the upper tiles of each factor (§II-C aggregation,
+ * §II-B damping):
+ *     F = (1/P) sum_p shards[p]
+ *     running = first_step ? F : decay * running + (1 - decay) * F
+ *     damped  = running + gamma * I
+ * shards[p] = shards + p * stride_shard.  shards, running and damped share
+ * `ld` (ld % 4 == 0, ld >= d).  running is read only when first_step == 0.
+ * 0 <= decay < 1, gamma >= 0.  n <= 4096.                                    */
+typedef struct {
+  const float* shards;  /* device, P fp32 d x d matrices (upper tiles read) */
+  int64_t stride_shard; /* elements between shards[p] and shards[p+1]       */
+  float* running;       /* device, in/out running average (upper tiles)     */
+  float* damped;        /* device, out running + gamma I (upper tiles)      */
+  int64_t d;
+  int64_t ld;
+} kfac_running_args;
+
+int kfac_update_running(int n, const kfac_running_args* args, int P,
+                        float decay, float gamma, int first_step, void* stream);
+
+/* ------------------------------------------------------ 3. damped inverse (a4)
+ * Batched inverse of damped SPD factors through a Cholesky decomposition
+ * (§IV: cuSolver-style Cholesky-based inverse; §III-B: the damped inverses):
+ *     D_i + gamma_extra * I = L L^T,   inv_i = L^-T L^-1
+ * computed with a blocked right-looking Cholesky (128-wide panels) fused with
+ * the blocked triangular inverse, then inv = W^T W with W = L^-1.  Only the
+ * upper triangle (incl. diagonal) of D_i is read.  inv_i is written as a full,
+ * exactly symmetric matrix (§IV: the inverse of a symmetric factor is
+ * symmetric).  Matrices may have different sizes.
+ *
+ * refine: KFAC_REFINE_NONE   fp32 arithmetic for every matrix;
+ *         KFAC_REFINE_AUTO   fp32, then matrices whose condition estimate
+ *                            ||D||_1 / min_j L_jj^2 exceeds 1e5 (or whose fp32
+ *                            factorisation failed) are recomputed in fp64;
+ *         KFAC_REFINE_ALWAYS fp64 arithmetic for every matrix.
+ * info: device int[n]; info[i] = 0 on success, k > 0 when the k-th pivot
+ *       (1-based) is not positive (LAPACK potrf convention); inv_i is then
+ *       unspecified.  route (device int[n], may be NULL): 0 when inv_i came
+ *       from the fp32 pass, 1 from the fp64 pass.
+ * ld_in, ld_out % 4 == 0.  n <= 4096, 1 <= d <= 65536.
+ * Workspace: kfac_damped_inverse_workspace(n, args, refine) bytes, 256-byte
+ * aligned, fully overwritten (no initialisation needed).                     */
+enum kfac_refine { KFAC_REFINE_NONE = 0, KFAC_REFINE_AUTO = 1, KFAC_REFINE_ALWAYS = 2 };
+
+typedef struct {
+  const float* damped;  /* device, d x d fp32 (upper triangle read) */
+  float* inv;           /* device, d x d fp32 out (full symmetric)  */
+  int64_t d;
+  int64_t ld_in;
+  int64_t ld_out;
+} kfac_inverse_args;
+
+size_t kfac_damped_inverse_workspace(int n, const kfac_inverse_args* args, int refine);
+
+int kfac_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra,
+                        int refine, int* info, int* route, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* -------------------------------------------------------- 4. precondition (a5)
+ * Preconditioned gradient of each layer (§II-B damped update rule):
+ *     out = inv_g * grad * inv_a        (d_out x d_out)(d_out x d_in)(d_in x d_in)
+ * inv_g and inv_a must be full symmetric matrices (as kfac_damped_inverse
+ * writes them).  All fp32; every ld % 4 == 0.  out must not alias an input.
+ * Workspace: kfac_precondition_workspace(n, args) bytes (holds grad * inv_a). */
+typedef struct {
+  const float* inv_g;  int64_t ld_g;
+  const float* grad;   int64_t ld_grad;
+  const float* inv_a;  int64_t ld_a;
+  float* out;          int64_t ld_out;
+  int64_t d_out;
+  int64_t d_in;
+} kfac_precond_args;
+
+size_t kfac_precondition_workspace(int n, const kfac_precond_args* args);
+
+int kfac_precondition(int n, const kfac_precond_args* args, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------- index tables
+ * The work units kfac_factors uses to cover the upper tiles of a d x d factor
+ * on the tensor-core path: for every 128-row block i, the columns
+ * [128 i, d) cut into chunks of at most 256.  Unit u is
+ * (row_block[u], col_start[u], width[u]).  Writes min(count, capacity)
+ * entries and returns the total count in *count.  Host only.                 */
+int kfac_factor_tile_map(int64_t d, int64_t capacity, int32_t* row_block,
+                         int64_t* col_start, int32_t* width, int64_t* count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KFAC_GB300_H */

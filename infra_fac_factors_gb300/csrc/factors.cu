@@ -1,0 +1,433 @@
+// Kronecker factors of P emulated workers (SPD-KFAC §II-B, Eq. (7)/(8);
+// §II-C: each worker p forms its local factor from its own rows):
+//
+//     out[p] = scale * x_p^T x_p,   x_p = rows [p*rows_p, (p+1)*rows_p) of x
+//
+// bf16 inputs: tcgen05 tensor cores.  The operand tiles are x[k0:k0+64,
+// i0:i0+128] and x[k0:k0+64, j0:j0+N]; both are MN-major in shared memory
+// (x is row-major, so the factor's row index m is the contiguous one), loaded
+// by TMA with the 128-byte swizzle from a 3-D tensor map {d, rows_p, P}, so the
+// tail of each worker's rows and of the columns reads as zero.
+//
+// Kernel roles (192 threads, one CTA per SM, persistent over work units):
+//   warp 0   TMA producer (one thread), 4-stage shared-memory ring;
+//   warp 1   TMEM allocation and the MMA issuer (one thread);
+//   warps 2-5 epilogue: TMEM -> registers -> scale -> global fp32 stores.
+// Two 128 x 256 fp32 accumulators in TMEM (all 512 columns) let the epilogue
+// of one unit overlap the main loop of the next.
+//
+// fp32 inputs: exact fp32 products on CUDA cores (simt.cuh).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "simt.cuh"
+#include "tilemap.cuh"
+
+namespace kfac {
+
+// Device status word (KFAC_OK or KFAC_ERR_TIMEOUT) of this library.
+__device__ int g_device_status = 0;
+
+int* device_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+// ------------------------------------------------------------------ tcgen05 SYRK
+constexpr int kSyBK = 64;                      // rows (k) per stage
+constexpr int kSyStages = 4;
+constexpr int kSyBox = 64 * kSyBK * 2;         // one 64-column x 64-row bf16 box: 8 KB
+constexpr int kSyABytes = 2 * kSyBox;          // 128 columns
+constexpr int kSyBBytes = 4 * kSyBox;          // up to 256 columns
+constexpr int kSyStageBytes = kSyABytes + kSyBBytes;
+constexpr int kSyMaxProbs = 96;
+constexpr int kSySmem = kSyStages * kSyStageBytes + 1024 + 256;
+
+struct SyProb {
+  float* out;
+  long long ld_out, stride_out;
+  long long unit_begin;
+  int d, rows_p, units_per_shard;
+  float scale;
+};
+
+struct SyParams {  // 128-byte aligned through CUtensorMap
+  CUtensorMap maps[kSyMaxProbs];
+  SyProb probs[kSyMaxProbs];
+  long long total_units;
+  int* status;
+  int n_probs, P, mirror;
+};
+
+struct SyUnit {
+  int prob, p, i, w;
+  int64_t j0;
+};
+
+__device__ __forceinline__ SyUnit sy_decode(const SyParams& prm, long long u) {
+  SyUnit r;
+  int pi = 0;
+  while (pi + 1 < prm.n_probs && prm.probs[pi + 1].unit_begin <= u) ++pi;
+  const SyProb& pr = prm.probs[pi];
+  const long long local = u - pr.unit_begin;
+  r.prob = pi;
+  r.p = (int)(local / pr.units_per_shard);
+  const long long t = local % pr.units_per_shard;
+  factor_unit(pr.d, t, r.i, r.j0, r.w);
+  return r;
+}
+
+__global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__ SyParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSyStages * kSyStageBytes);
+  uint64_t* empty = full + kSyStages;
+  uint64_t* acc_full = empty + kSyStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done_bar = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSyStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tc_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      for (long long u = blockIdx.x; u < prm.total_units && !*abort_flag; u += gridDim.x) {
+        const SyUnit un = sy_decode(prm, u);
+        const SyProb& pr = prm.probs[un.prob];
+        const CUtensorMap* map = &prm.maps[un.prob];
+        const int nb = (un.w + 63) / 64;
+        const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
+          uint8_t* sa = smem + stage * kSyStageBytes;
+          uint8_t* sb = sa + kSyABytes;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)((2 + nb) * kSyBox));
+          tma_load_3d(sa, map, un.i * 128, kb * kSyBK, un.p, &full[stage]);
+          tma_load_3d(sa + kSyBox, map, un.i * 128 + 64, kb * kSyBK, un.p, &full[stage]);
+          for (int q = 0; q < nb; ++q)
+            tma_load_3d(sb + q * kSyBox, map, (int)un.j0 + 64 * q, kb * kSyBK, un.p, &full[stage]);
+          if (++stage == kSyStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (long long u = blockIdx.x; u < prm.total_units && ok; u += gridDim.x) {
+        const SyUnit un = sy_decode(prm, u);
+        const SyProb& pr = prm.probs[un.prob];
+        const int nb = (un.w + 63) / 64;
+        const uint32_t idesc = idesc_bf16_f32(nb * 64, true, true);
+        const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * 256;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, prm.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + stage * kSyStageBytes);
+          const uint32_t b0 = a0 + kSyABytes;
+#pragma unroll
+          for (int kk = 0; kk < kSyBK / 16; ++kk) {
+            // 16 rows of k = two 8-row groups of 1024 B; 64-column blocks are kSyBox apart.
+            const uint64_t ad = smem_desc_sw128(a0 + kk * 2048, kSyBox, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kSyBox, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kSyStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      // Every MMA issued above has completed once done_bar flips.
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0, abort_flag, prm.status);
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t acc = 0, acc_phase = 0;
+    for (long long u = blockIdx.x; u < prm.total_units; u += gridDim.x) {
+      const SyUnit un = sy_decode(prm, u);
+      const SyProb& pr = prm.probs[un.prob];
+      const int nb = (un.w + 63) / 64;
+      if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) break;
+      tc_fence_after();
+      const int r = un.i * 128 + q * 32 + lane;
+      float* outp = pr.out + (long long)un.p * pr.stride_out;
+      float* orow = outp + (long long)r * pr.ld_out;
+      const long long jend = un.j0 + un.w;
+      for (int c = 0; c < nb * 2; ++c) {
+        uint32_t v[32];
+        tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
+        tc_wait_ld();
+        const long long col0 = un.j0 + c * 32;
+        if (r < pr.d && col0 < jend) {
+          if (col0 + 32 <= jend) {
+#pragma unroll
+            for (int t = 0; t < 32; t += 4) {
+              float4 o;
+              o.x = __uint_as_float(v[t]) * pr.scale;
+              o.y = __uint_as_float(v[t + 1]) * pr.scale;
+              o.z = __uint_as_float(v[t + 2]) * pr.scale;
+              o.w = __uint_as_float(v[t + 3]) * pr.scale;
+              *reinterpret_cast<float4*>(orow + col0 + t) = o;
+            }
+          } else {
+            for (int t = 0; t < 32; ++t)
+              if (col0 + t < jend) orow[col0 + t] = __uint_as_float(v[t]) * pr.scale;
+          }
+          if (prm.mirror) {
+            const long long lower_from = (long long)(un.i + 1) * 128;  // columns in lower-tile territory
+            for (int t = 0; t < 32; ++t) {
+              const long long col = col0 + t;
+              if (col < jend && col >= lower_from) outp[col * pr.ld_out + r] = __uint_as_float(v[t]) * pr.scale;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tc_dealloc(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------------------------ fp32 (CUDA-core) factors
+constexpr int kSmMaxProbs = 128;
+struct SmProb {
+  const void* x;
+  float* out;
+  long long ld_x, ld_out, stride_out;
+  long long tile_begin;
+  int d, rows_p, tiles_per_shard;
+  float scale;
+};
+struct SmParams {
+  SmProb probs[kSmMaxProbs];
+  long long total_tiles;
+  int n_probs, P, mirror;
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(256) syrk_simt_kernel(const __grid_constant__ SmParams prm) {
+  __shared__ __align__(16) float smem[simt_smem_bytes<float>() / sizeof(float)];
+  for (long long u = blockIdx.x; u < prm.total_tiles; u += gridDim.x) {
+    int pi = 0;
+    while (pi + 1 < prm.n_probs && prm.probs[pi + 1].tile_begin <= u) ++pi;
+    const SmProb& pr = prm.probs[pi];
+    const long long local = u - pr.tile_begin;
+    const int p = (int)(local / pr.tiles_per_shard);
+    int t = (int)(local % pr.tiles_per_shard);
+    // upper tile (i, j) of the 128-grid, row-major over i
+    const int T = (pr.d + 127) / 128;
+    int i = 0;
+    while (t >= T - i) {
+      t -= T - i;
+      ++i;
+    }
+    const int j = i + t;
+    const Tin* xs = static_cast<const Tin*>(pr.x) + (long long)p * pr.rows_p * pr.ld_x;
+    Opnd<Tin> A{xs + i * 128, 1, pr.ld_x, min(128, pr.d - i * 128)};
+    Opnd<Tin> B{xs + j * 128, 1, pr.ld_x, min(128, pr.d - j * 128)};
+    float acc[8][8];
+    zero_acc(acc);
+    simt_tile<float, Tin, Tin>(acc, A, B, pr.rows_p, smem);
+    float* outp = pr.out + (long long)p * pr.stride_out;
+    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+      const int r = i * 128 + ty * 8 + a;
+      if (r >= pr.d) continue;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int c = j * 128 + tx * 8 + b;
+        if (c >= pr.d) continue;
+        const float v = acc[a][b] * pr.scale;
+        outp[(long long)r * pr.ld_out + c] = v;
+        if (prm.mirror && j > i) outp[(long long)c * pr.ld_out + r] = v;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ spatial sum (conv G helper)
+template <typename Tin>
+__global__ void __launch_bounds__(256) spatial_sum_kernel(const Tin* __restrict__ g, long long hw, long long C,
+                                                          long long ld_g, float* __restrict__ gs, long long ld_gs) {
+  // block: 64 channels x 4 position lanes; grid: (ceil(C/64), batch)
+  __shared__ float red[4][64];
+  const int cl = threadIdx.x % 64, sl = threadIdx.x / 64;
+  const long long c = (long long)blockIdx.x * 64 + cl;
+  const long long b = blockIdx.y;
+  float acc = 0.f;
+  if (c < C) {
+    const Tin* base = g + (b * hw) * ld_g + c;
+    for (long long s = sl; s < hw; s += 4) acc += load_as<float, Tin>(base + s * ld_g);
+  }
+  red[sl][cl] = acc;
+  __syncthreads();
+  if (sl == 0 && c < C) gs[b * ld_gs + c] = (red[0][cl] + red[1][cl]) + (red[2][cl] + red[3][cl]);
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirror, cudaStream_t stream) {
+  if (dtype == KFAC_BF16) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return KFAC_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+    const int sms = device_sm_count(dev);
+    if (sms <= 0) return KFAC_ERR_CUDA;
+    if (!ensure_smem_attr(dev, (const void*)syrk_tc_kernel, kSySmem)) return KFAC_ERR_CUDA;
+    for (int base = 0; base < n; base += kSyMaxProbs) {
+      const int cnt = n - base < kSyMaxProbs ? n - base : kSyMaxProbs;
+      SyParams prm;
+      memset(&prm, 0, sizeof(prm));
+      long long units = 0;
+      for (int k = 0; k < cnt; ++k) {
+        const kfac_factor_args& a = args[base + k];
+        const long long rows_p = a.rows / P;
+        cuuint64_t gdim[3] = {(cuuint64_t)a.d, (cuuint64_t)rows_p, (cuuint64_t)P};
+        cuuint64_t gstride[2] = {(cuuint64_t)a.ld_x * 2, (cuuint64_t)(rows_p * a.ld_x * 2)};
+        cuuint32_t box[3] = {64, kSyBK, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        CUresult cr = enc(&prm.maps[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.x), gdim, gstride,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return KFAC_ERR_INVALID_ARG;
+        SyProb& pr = prm.probs[k];
+        pr.out = a.out;
+        pr.ld_out = a.ld_out;
+        pr.stride_out = a.stride_out;
+        pr.d = (int)a.d;
+        pr.rows_p = (int)rows_p;
+        pr.units_per_shard = (int)factor_units(a.d);
+        pr.unit_begin = units;
+        pr.scale = a.scale;
+        units += (long long)pr.units_per_shard * P;
+      }
+      prm.n_probs = cnt;
+      prm.P = P;
+      prm.mirror = mirror;
+      prm.total_units = units;
+      prm.status = device_status_ptr();
+      if (!prm.status) return KFAC_ERR_CUDA;
+      if (units == 0) continue;
+      const int grid = (int)(units < sms ? units : sms);
+      syrk_tc_kernel<<<grid, 192, kSySmem, stream>>>(prm);
+      count_launch();
+      if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
+    }
+    return KFAC_OK;
+  }
+  // fp32 inputs on CUDA cores
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  for (int base = 0; base < n; base += kSmMaxProbs) {
+    const int cnt = n - base < kSmMaxProbs ? n - base : kSmMaxProbs;
+    SmParams prm;
+    memset(&prm, 0, sizeof(prm));
+    long long tiles = 0;
+    for (int k = 0; k < cnt; ++k) {
+      const kfac_factor_args& a = args[base + k];
+      SmProb& pr = prm.probs[k];
+      const long long T = (a.d + 127) / 128;
+      pr.x = a.x;
+      pr.out = a.out;
+      pr.ld_x = a.ld_x;
+      pr.ld_out = a.ld_out;
+      pr.stride_out = a.stride_out;
+      pr.d = (int)a.d;
+      pr.rows_p = (int)(a.rows / P);
+      pr.tiles_per_shard = (int)(T * (T + 1) / 2);
+      pr.tile_begin = tiles;
+      pr.scale = a.scale;
+      tiles += (long long)pr.tiles_per_shard * P;
+    }
+    prm.n_probs = cnt;
+    prm.P = P;
+    prm.mirror = mirror;
+    prm.total_tiles = tiles;
+    if (tiles == 0) continue;
+    const long long cap = (long long)sms * 4;
+    const int grid = (int)(tiles < cap ? tiles : cap);
+    syrk_simt_kernel<float><<<grid, 256, 0, stream>>>(prm);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
+  }
+  return KFAC_OK;
+}
+
+int launch_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw, int64_t C, int64_t ld_g, float* gs,
+                       int64_t ld_gs, cudaStream_t stream) {
+  dim3 grid((unsigned)((C + 63) / 64), (unsigned)batch);
+  if (dtype == KFAC_BF16)
+    spatial_sum_kernel<uint16_t><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(g), hw, C, ld_g, gs, ld_gs);
+  else
+    spatial_sum_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(g), hw, C, ld_g, gs, ld_gs);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
+}  // namespace kfac

@@ -1,0 +1,563 @@
+// Batched inverse of damped SPD factors through a Cholesky decomposition
+// (SPD-KFAC §IV: the inverse is computed through a Cholesky decomposition;
+// §III-B: the damped inverses (A + lambda I)^-1, (G + lambda I)^-1).
+//
+// For each matrix (size d, T = ceil(d/128) tile rows, n_pad = 128 T):
+//   L-buffer  n_pad x n_pad, lower tiles = D (+ gamma_extra on the diagonal),
+//             padded with the identity, so every tile operation is full size
+//             (the padded matrix is diag(D, I); its inverse is diag(D^-1, I)).
+//   W-buffer  n_pad x n_pad, lower tiles end up as W = L^-1.
+// Right-looking blocked sweep over the 128-wide block columns k = 0..T-1:
+//   diag(k)   L_kk = chol(A_kk) and Winv_k = L_kk^-1 in shared memory;
+//             Winv_k is stored as W_kk.
+//   panel(k)  L_rk = A_rk Winv_k^T            for r > k
+//             W_kc = Winv_k C_kc              for c < k
+//   update(k) A_rc -= L_rk L_ck^T             for r >= c > k   (Cholesky)
+//             C_rc  = [c<k] C_rc - L_rk W_kc  for r > k >= c   (forward
+//             substitution on I: row block r of L W = I)
+// and finally X = W^T W, formed for the upper tiles and mirrored, so X is
+// exactly symmetric.  The same kernels run in fp32 and fp64 (templates).
+//
+// refine = AUTO: the fp32 pass also records ||D||_1 (row abs sums) and the
+// smallest pivot L_jj^2; matrices with ||D||_1 / min L_jj^2 > 1e5, or whose
+// fp32 factorisation failed, are redone in fp64 (the fp64 kernels of the other
+// matrices exit at once).
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "simt.cuh"
+
+namespace kfac {
+
+constexpr int kInvMaxGroup = 256;
+constexpr float kAutoKappa = 1e5f;
+
+struct InvMat {
+  const float* D;
+  float* X;
+  long long ld_in, ld_out;
+  long long off_buf;     // byte offset of the L/W buffers in the workspace
+  long long off_rowsum;  // float index of this matrix's row sums
+  int d, T, pad0, pad1;
+};
+
+struct InvState {
+  int info32, info64, failed, use64;
+  float min_piv, kappa;
+  int pad0, pad1;
+};
+
+struct InvSetup {
+  InvMat mats[kInvMaxGroup];
+  int n, mode;
+  long long rowsum_total;
+};
+
+struct InvCtx {
+  uint8_t* ws;
+  const InvMat* mats;
+  InvState* st;
+  float* rowsum;
+  float gamma_extra;
+  int pass64;  // 0: fp32 pass, 1: fp64 pass
+  int want_rowsum;
+};
+
+template <typename T>
+__device__ __forceinline__ T* lbuf(const InvCtx& c, const InvMat& m) {
+  return reinterpret_cast<T*>(c.ws + m.off_buf);
+}
+template <typename T>
+__device__ __forceinline__ T* wbuf(const InvCtx& c, const InvMat& m) {
+  return lbuf<T>(c, m) + (long long)m.T * 128 * m.T * 128;
+}
+
+// Whether matrix `mi` takes part in the current pass (and has not failed in it).
+__device__ __forceinline__ bool inv_active(const InvCtx& c, int mi, bool need_ok) {
+  const InvState& s = c.st[mi];
+  if (c.pass64 ? !s.use64 : s.use64) return false;
+  if (need_ok && s.failed) return false;
+  return true;
+}
+
+__host__ __device__ inline long long tri(long long t) { return t * (t + 1) / 2; }
+// largest r with r(r+1)/2 <= q
+__device__ __forceinline__ int tri_root(long long q) {
+  int r = (int)((sqrt(8.0 * (double)q + 1.0) - 1.0) * 0.5);
+  while (tri(r + 1) <= q) ++r;
+  while (tri(r) > q) --r;
+  return r;
+}
+
+// ------------------------------------------------------------------ setup
+__global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, uint8_t* ws, InvMat* mats, InvState* st,
+                                 float* rowsum) {
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nth = (long long)gridDim.x * blockDim.x;
+  for (long long e = tid; e < prm.n; e += nth) {
+    mats[e] = prm.mats[e];
+    InvState s;
+    s.info32 = 0;
+    s.info64 = 0;
+    s.failed = 0;
+    s.use64 = prm.mode == KFAC_REFINE_ALWAYS ? 1 : 0;
+    s.min_piv = 3.0e38f;
+    s.kappa = 0.f;
+    s.pad0 = s.pad1 = 0;
+    st[e] = s;
+  }
+  for (long long e = tid; e < prm.rowsum_total; e += nth) rowsum[e] = 0.f;
+}
+
+// ------------------------------------------------------------------ load D into the L-buffer
+template <typename T>
+__global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, false)) return;
+  const InvMat m = c.mats[mi];
+  const long long q = blockIdx.x;
+  if (q >= tri(m.T)) return;
+  if (threadIdx.x == 0 && c.pass64) c.st[mi].failed = 0;
+  const int R = tri_root(q), C = (int)(q - tri(R));  // lower tile (R, C), R >= C
+  const long long np = (long long)m.T * 128;
+  T* L = lbuf<T>(c, m);
+  __shared__ float sub[32][33];
+  __shared__ float rs_row[128], rs_col[128];
+  if (threadIdx.x < 128) {
+    rs_row[threadIdx.x] = 0.f;
+    rs_col[threadIdx.x] = 0.f;
+  }
+  __syncthreads();
+  const int lx = threadIdx.x % 32, ly = threadIdx.x / 32;  // 32 x 8
+  for (int sb = 0; sb < 16; ++sb) {
+    const int bm = (sb / 4) * 32, bn = (sb % 4) * 32;  // sub-block rows (mm) / cols (nn) of the L tile
+    // read D[C*128 + bn + y][R*128 + bm + x] (coalesced along x), store sub[y][x]
+    for (int y = ly; y < 32; y += 8) {
+      const long long gc = (long long)C * 128 + bn + y;   // D row   = L column
+      const long long gr = (long long)R * 128 + bm + lx;  // D column = L row
+      float v = 0.f;
+      if (gc < m.d && gr < m.d && gr >= gc) v = m.D[gc * m.ld_in + gr];
+      sub[y][lx] = v;
+    }
+    __syncthreads();
+    // write L[R*128 + bm + y][C*128 + bn + x] = sub[x][y]
+    for (int y = ly; y < 32; y += 8) {
+      const long long gr = (long long)R * 128 + bm + y;
+      const long long gc = (long long)C * 128 + bn + lx;
+      float v = sub[lx][y];
+      T out;
+      if (gr >= m.d || gc >= m.d) {
+        out = (gr == gc) ? T(1) : T(0);
+      } else if (gr < gc) {
+        out = T(0);
+      } else {
+        if (c.want_rowsum) {
+          const float a = fabsf(v);
+          atomicAdd(&rs_row[bm + y], a);
+          if (gr != gc) atomicAdd(&rs_col[bn + lx], a);
+        }
+        out = (T)v;
+        if (gr == gc) out += (T)c.gamma_extra;
+      }
+      L[gr * np + gc] = out;
+    }
+    __syncthreads();
+  }
+  if (c.want_rowsum && threadIdx.x < 128) {
+    const long long gr = (long long)R * 128 + threadIdx.x;
+    const long long gc = (long long)C * 128 + threadIdx.x;
+    if (gr < m.d && rs_row[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gr], rs_row[threadIdx.x]);
+    if (gc < m.d && rs_col[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gc], rs_col[threadIdx.x]);
+  }
+}
+
+// ------------------------------------------------------------------ diagonal block
+template <typename T>
+__device__ __forceinline__ T dev_sqrt(T v);
+template <>
+__device__ __forceinline__ float dev_sqrt<float>(float v) { return __fsqrt_rn(v); }
+template <>
+__device__ __forceinline__ double dev_sqrt<double>(double v) { return sqrt(v); }
+template <typename T>
+__device__ __forceinline__ T dev_rcp(T v);
+template <>
+__device__ __forceinline__ float dev_rcp<float>(float v) { return __frcp_rn(v); }
+template <>
+__device__ __forceinline__ double dev_rcp<double>(double v) { return 1.0 / v; }
+
+constexpr int kDiagPitch = 129;
+template <typename T>
+constexpr int diag_smem_bytes() {
+  return 128 * kDiagPitch * (int)sizeof(T);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) inv_diag_kernel(InvCtx c, int k) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, true)) return;
+  const InvMat m = c.mats[mi];
+  if (k >= m.T) return;
+  extern __shared__ __align__(16) uint8_t diag_smem[];
+  T* a = reinterpret_cast<T*>(diag_smem);
+  const long long np = (long long)m.T * 128;
+  const T* src = lbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
+  const int t = threadIdx.x;
+  for (int r = 0; r < 128; ++r) a[r * kDiagPitch + t] = (t <= r) ? src[(long long)r * np + t] : T(0);
+  __syncthreads();
+
+  // Cholesky, right-looking; column j is scaled by 1/sqrt(pivot) one iteration
+  // later, when no thread reads it any more, so each column costs one barrier.
+  int fail = -1;
+  T min_piv = T(3.0e38);
+  T prev_rs = T(0);
+  for (int j = 0; j < 128; ++j) {
+    const T piv = a[j * kDiagPitch + j];
+    if (!(piv > T(0))) {  // also catches NaN
+      fail = j;
+      break;
+    }
+    if (k * 128 + j < m.d && piv < min_piv) min_piv = piv;
+    if (j > 0) {
+      const int r = j + t;  // rows j .. 127 of column j-1
+      if (r < 128) a[r * kDiagPitch + (j - 1)] *= prev_rs;
+      if (t == 0) a[(j - 1) * kDiagPitch + (j - 1)] = dev_sqrt<T>(a[(j - 1) * kDiagPitch + (j - 1)]);
+    }
+    const T ip = dev_rcp<T>(piv);
+    prev_rs = dev_rcp<T>(dev_sqrt<T>(piv));
+    const int col = t;
+    if (col > j) {
+      const T f = a[col * kDiagPitch + j] * ip;
+      for (int r = col; r < 128; ++r) a[r * kDiagPitch + col] -= a[r * kDiagPitch + j] * f;
+    }
+    __syncthreads();
+  }
+  if (fail >= 0) {
+    if (t == 0) {
+      InvState& s = c.st[mi];
+      s.failed = 1;
+      const int idx = k * 128 + fail + 1;
+      if (c.pass64)
+        s.info64 = idx;
+      else
+        s.info32 = idx;
+    }
+    return;
+  }
+  // last column: only its diagonal is left
+  if (t == 0) a[127 * kDiagPitch + 127] = dev_sqrt<T>(a[127 * kDiagPitch + 127]);
+  __syncthreads();
+  if (t == 0) {
+    // positive floats order like their bit patterns
+    const float mp = (float)min_piv;
+    atomicMin(reinterpret_cast<int*>(&c.st[mi].min_piv), __float_as_int(mp));
+  }
+
+  // In-place inverse of the lower-triangular block, column by column from the
+  // right: W_jj = 1/L_jj, W_rj = -(sum_{j<s<=r} W_rs L_sj) / L_jj.
+  for (int j = 127; j >= 0; --j) {
+    const T ljj = a[j * kDiagPitch + j];
+    T s = T(0);
+    const int r = t;
+    if (r > j)
+      for (int q = j + 1; q <= r; ++q) s += a[r * kDiagPitch + q] * a[q * kDiagPitch + j];
+    __syncthreads();
+    if (r > j) a[r * kDiagPitch + j] = -s / ljj;
+    if (r == j) a[j * kDiagPitch + j] = dev_rcp<T>(ljj);
+    __syncthreads();
+  }
+  T* dst = wbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
+  for (int r = 0; r < 128; ++r) dst[(long long)r * np + t] = (t <= r) ? a[r * kDiagPitch + t] : T(0);
+}
+
+// ------------------------------------------------------------------ tile epilogues
+template <typename T>
+__device__ __forceinline__ void tile_store(T* dst, long long ld, const T (&acc)[8][8], int mode) {
+  // mode 0: dst = acc, 1: dst -= acc, 2: dst = -acc
+  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    T* row = dst + (long long)(ty * 8 + a) * ld + tx * 8;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (mode == 0)
+        row[b] = acc[a][b];
+      else if (mode == 1)
+        row[b] -= acc[a][b];
+      else
+        row[b] = -acc[a][b];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ panel
+template <typename T>
+__global__ void __launch_bounds__(256) inv_panel_kernel(InvCtx c, int k) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, true)) return;
+  const InvMat m = c.mats[mi];
+  if (k >= m.T) return;
+  const int nr = m.T - 1 - k;
+  const int q = blockIdx.x;
+  if (q >= nr + k) return;
+  __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
+  const long long np = (long long)m.T * 128;
+  T* L = lbuf<T>(c, m);
+  T* W = wbuf<T>(c, m);
+  const T* winv = W + (long long)k * 128 * np + (long long)k * 128;
+  T acc[8][8];
+  zero_acc(acc);
+  if (q < nr) {
+    const int r = k + 1 + q;
+    T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
+    Opnd<T> A{Lrk, np, 1, 128};
+    Opnd<T> B{winv, np, 1, 128};
+    simt_tile<T, T, T>(acc, A, B, 128, smem);
+    tile_store(Lrk, np, acc, 0);
+  } else {
+    const int cc = q - nr;
+    T* Ckc = W + (long long)k * 128 * np + (long long)cc * 128;
+    Opnd<T> A{winv, np, 1, 128};
+    Opnd<T> B{Ckc, 1, np, 128};
+    simt_tile<T, T, T>(acc, A, B, 128, smem);
+    tile_store(Ckc, np, acc, 0);
+  }
+}
+
+// ------------------------------------------------------------------ trailing update
+template <typename T>
+__global__ void __launch_bounds__(256) inv_update_kernel(InvCtx c, int k) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, true)) return;
+  const InvMat m = c.mats[mi];
+  if (k + 1 >= m.T) return;
+  const long long q = blockIdx.x;
+  if (q >= tri(m.T) - tri(k + 1)) return;
+  const long long qq = q + tri(k + 1);
+  const int r = tri_root(qq);
+  const int cc = (int)(qq - tri(r));
+  __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
+  const long long np = (long long)m.T * 128;
+  T* L = lbuf<T>(c, m);
+  T* W = wbuf<T>(c, m);
+  const T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
+  T acc[8][8];
+  zero_acc(acc);
+  Opnd<T> A{Lrk, np, 1, 128};
+  if (cc > k) {
+    Opnd<T> B{L + (long long)cc * 128 * np + (long long)k * 128, np, 1, 128};
+    simt_tile<T, T, T>(acc, A, B, 128, smem);
+    tile_store(L + (long long)r * 128 * np + (long long)cc * 128, np, acc, 1);
+  } else {
+    Opnd<T> B{W + (long long)k * 128 * np + (long long)cc * 128, 1, np, 128};
+    simt_tile<T, T, T>(acc, A, B, 128, smem);
+    tile_store(W + (long long)r * 128 * np + (long long)cc * 128, np, acc, cc == k ? 2 : 1);
+  }
+}
+
+// ------------------------------------------------------------------ X = W^T W
+template <typename T>
+__global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, true)) return;
+  const InvMat m = c.mats[mi];
+  const long long q = blockIdx.x;
+  if (q >= tri(m.T)) return;
+  const int j = tri_root(q);
+  const int i = (int)(q - tri(j));  // i <= j
+  __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
+  const long long np = (long long)m.T * 128;
+  const T* W = wbuf<T>(c, m);
+  T acc[8][8];
+  zero_acc(acc);
+  Opnd<T> A{W + (long long)j * 128 * np + (long long)i * 128, 1, np, 128};
+  Opnd<T> B{W + (long long)j * 128 * np + (long long)j * 128, 1, np, 128};
+  simt_tile<T, T, T>(acc, A, B, (int)(np - (long long)j * 128), smem);
+  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    const int mm = ty * 8 + a;
+    const long long row = (long long)i * 128 + mm;
+    if (row >= m.d) continue;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int nn = tx * 8 + b;
+      const long long col = (long long)j * 128 + nn;
+      if (col >= m.d) continue;
+      if (i == j && mm > nn) continue;
+      const float v = (float)acc[a][b];
+      m.X[row * m.ld_out + col] = v;
+      m.X[col * m.ld_out + row] = v;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ AUTO decision
+__global__ void __launch_bounds__(128) inv_flag_kernel(InvCtx c) {
+  const int mi = blockIdx.x;
+  const InvMat m = c.mats[mi];
+  __shared__ float red[128];
+  float mx = 0.f;
+  for (int r = threadIdx.x; r < m.d; r += 128) mx = fmaxf(mx, c.rowsum[m.off_rowsum + r]);
+  red[threadIdx.x] = mx;
+  __syncthreads();
+  for (int s = 64; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + s]);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    InvState& s = c.st[mi];
+    const float kappa = s.min_piv > 0.f ? red[0] / s.min_piv : 3.0e38f;
+    s.kappa = kappa;
+    s.use64 = (s.failed || !(kappa <= kAutoKappa)) ? 1 : 0;
+  }
+}
+
+__global__ void inv_finish_kernel(InvCtx c, int n, int* info, int* route) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const InvState s = c.st[i];
+  info[i] = s.use64 ? s.info64 : s.info32;
+  if (route) route[i] = s.use64;
+}
+
+// ------------------------------------------------------------------ host side
+struct InvLayout {
+  size_t mats_off, st_off, rowsum_off, buf_off, total;
+};
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+static InvLayout inv_layout(int n, const kfac_inverse_args* args, int refine, long long* rowsum_total,
+                            InvMat* mats /* may be null */) {
+  InvLayout L;
+  L.mats_off = 0;
+  L.st_off = align256(sizeof(InvMat) * (size_t)n);
+  L.rowsum_off = L.st_off + align256(sizeof(InvState) * (size_t)n);
+  long long rs = 0;
+  for (int i = 0; i < n; ++i) {
+    if (mats) mats[i].off_rowsum = rs;
+    rs += (args[i].d + 127) / 128 * 128;
+  }
+  *rowsum_total = rs;
+  L.buf_off = L.rowsum_off + align256(sizeof(float) * (size_t)rs);
+  size_t off = L.buf_off;
+  const size_t elem = refine == KFAC_REFINE_NONE ? 4 : 8;
+  for (int i = 0; i < n; ++i) {
+    const size_t np = (size_t)((args[i].d + 127) / 128) * 128;
+    if (mats) mats[i].off_buf = (long long)off;
+    off += align256(2 * np * np * elem);
+  }
+  L.total = off;
+  return L;
+}
+
+size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine) {
+  // groups of kInvMaxGroup run one after the other and reuse the workspace
+  size_t best = 0;
+  for (int base = 0; base < n; base += kInvMaxGroup) {
+    const int cnt = n - base < kInvMaxGroup ? n - base : kInvMaxGroup;
+    long long rs;
+    const InvLayout L = inv_layout(cnt, args + base, refine, &rs, nullptr);
+    if (L.total > best) best = L.total;
+  }
+  return best;
+}
+
+template <typename T>
+static int run_pass(const InvCtx& ctx, int cnt, int Tmax, const int* Ts, cudaStream_t stream) {
+  const int dsm = diag_smem_bytes<T>();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  if (!ensure_smem_attr(dev, (const void*)inv_diag_kernel<T>, dsm)) return KFAC_ERR_CUDA;
+  inv_load_kernel<T><<<dim3((unsigned)tri(Tmax), cnt), 256, 0, stream>>>(ctx);
+  count_launch();
+  for (int k = 0; k < Tmax; ++k) {
+    inv_diag_kernel<T><<<dim3(1, cnt), 128, dsm, stream>>>(ctx, k);
+    count_launch();
+    if (Tmax > 1) {
+      inv_panel_kernel<T><<<dim3((unsigned)(Tmax - 1), cnt), 256, 0, stream>>>(ctx, k);
+      count_launch();
+    }
+    long long upd = 0;
+    for (int i = 0; i < cnt; ++i)
+      if (Ts[i] > k + 1) {
+        const long long u = tri(Ts[i]) - tri(k + 1);
+        if (u > upd) upd = u;
+      }
+    if (upd > 0) {
+      inv_update_kernel<T><<<dim3((unsigned)upd, cnt), 256, 0, stream>>>(ctx, k);
+      count_launch();
+    }
+  }
+  inv_lauum_kernel<T><<<dim3((unsigned)tri(Tmax), cnt), 256, 0, stream>>>(ctx);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
+int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra, int refine, int* info, int* route,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (workspace_bytes < inverse_workspace(n, args, refine) || workspace == nullptr) return KFAC_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  static InvSetup prm;  // large; host-side staging only
+  int Ts[kInvMaxGroup];
+  for (int base = 0; base < n; base += kInvMaxGroup) {
+    const int cnt = n - base < kInvMaxGroup ? n - base : kInvMaxGroup;
+    memset(&prm, 0, sizeof(prm));
+    long long rs_total = 0;
+    const InvLayout L = inv_layout(cnt, args + base, refine, &rs_total, prm.mats);
+    int Tmax = 0;
+    for (int i = 0; i < cnt; ++i) {
+      const kfac_inverse_args& a = args[base + i];
+      InvMat& m = prm.mats[i];
+      m.D = a.damped;
+      m.X = a.inv;
+      m.ld_in = a.ld_in;
+      m.ld_out = a.ld_out;
+      m.d = (int)a.d;
+      m.T = (int)((a.d + 127) / 128);
+      Ts[i] = m.T;
+      if (m.T > Tmax) Tmax = m.T;
+    }
+    prm.n = cnt;
+    prm.mode = refine;
+    prm.rowsum_total = rs_total;
+    InvCtx ctx;
+    ctx.ws = ws;
+    ctx.mats = reinterpret_cast<const InvMat*>(ws + L.mats_off);
+    ctx.st = reinterpret_cast<InvState*>(ws + L.st_off);
+    ctx.rowsum = reinterpret_cast<float*>(ws + L.rowsum_off);
+    ctx.gamma_extra = gamma_extra;
+    ctx.want_rowsum = refine == KFAC_REFINE_AUTO;
+    {
+      const long long work = rs_total > cnt ? rs_total : cnt;
+      long long blocks = (work + 255) / 256;
+      if (blocks > 1024) blocks = 1024;
+      inv_setup_kernel<<<(unsigned)blocks, 256, 0, stream>>>(prm, ws, const_cast<InvMat*>(ctx.mats), ctx.st,
+                                                             ctx.rowsum);
+      count_launch();
+    }
+    int rc;
+    if (refine != KFAC_REFINE_ALWAYS) {
+      ctx.pass64 = 0;
+      rc = run_pass<float>(ctx, cnt, Tmax, Ts, stream);
+      if (rc != KFAC_OK) return rc;
+    }
+    if (refine == KFAC_REFINE_AUTO) {
+      inv_flag_kernel<<<cnt, 128, 0, stream>>>(ctx);
+      count_launch();
+    }
+    if (refine != KFAC_REFINE_NONE) {
+      ctx.pass64 = 1;
+      ctx.want_rowsum = 0;
+      rc = run_pass<double>(ctx, cnt, Tmax, Ts, stream);
+      if (rc != KFAC_OK) return rc;
+    }
+    inv_finish_kernel<<<(cnt + 255) / 256, 256, 0, stream>>>(ctx, cnt, info + base, route ? route + base : nullptr);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
+  }
+  return KFAC_OK;
+}
+
+}  // namespace kfac

@@ -1,0 +1,30 @@
+// Internal launchers (host side) behind the C ABI of kfac.h.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "kfac.h"
+
+namespace kfac {
+
+int device_sm_count(int dev);
+int* device_status_ptr();
+// Counts every kernel launch of the library (reported by kfac_launch_count).
+void count_launch();
+bool ensure_smem_attr(int dev, const void* fn, int bytes);
+
+int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirror, cudaStream_t stream);
+int launch_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw, int64_t C, int64_t ld_g, float* gs,
+                       int64_t ld_gs, cudaStream_t stream);
+int launch_update_running(int n, const kfac_running_args* args, int P, float decay, float gamma, int first_step,
+                          cudaStream_t stream);
+size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine);
+int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra, int refine, int* info, int* route,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+size_t precondition_workspace(int n, const kfac_precond_args* args);
+int launch_precondition(int n, const kfac_precond_args* args, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+}  // namespace kfac

@@ -1,0 +1,151 @@
+// Fused aggregation + running average + damping, one pass over the upper
+// tiles of every factor (SPD-KFAC §II-C: the P workers' local factors are
+// aggregated before inverting; §II-B: Tikhonov damping):
+//
+//   F       = (1/P) sum_p shards[p]
+//   running = first_step ? F : decay * running + (1 - decay) * F
+//   damped  = running + gamma * I
+//
+// HBM-bound: per element P (+1) fp32 reads and 2 fp32 writes.  One warp streams
+// one row segment [128*floor(r/128), d) with 16-byte loads; all P shard loads
+// of an iteration are issued before they are summed.
+#include "common.cuh"
+#include "launch.h"
+
+namespace kfac {
+
+constexpr int kRunMaxProbs = 256;
+
+struct RunProb {
+  const float* shards;
+  float* running;
+  float* damped;
+  long long stride, ld, row_begin;
+  int d;
+};
+struct RunParams {
+  RunProb probs[kRunMaxProbs];
+  long long total_rows;
+  int n_probs, P, first_step;
+  float decay, gamma, inv_p;
+};
+
+template <int PC>
+__device__ __forceinline__ float4 sum_shards(const float* base, long long stride, int P) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // PC shards per batch of independent loads
+  for (int p0 = 0; p0 < P; p0 += PC) {
+    float4 v[PC];
+#pragma unroll
+    for (int q = 0; q < PC; ++q)
+      if (p0 + q < P) v[q] = __ldcs(reinterpret_cast<const float4*>(base + (long long)(p0 + q) * stride));
+#pragma unroll
+    for (int q = 0; q < PC; ++q)
+      if (p0 + q < P) {
+        acc.x += v[q].x;
+        acc.y += v[q].y;
+        acc.z += v[q].z;
+        acc.w += v[q].w;
+      }
+  }
+  return acc;
+}
+
+__global__ void __launch_bounds__(256) update_running_kernel(const __grid_constant__ RunParams prm) {
+  const int lane = threadIdx.x % 32;
+  const long long warp_global = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) / 32;
+  const float decay = prm.decay, keep = 1.f - prm.decay;
+  for (long long g = warp_global; g < prm.total_rows; g += nwarps) {
+    int pi = 0;
+    while (pi + 1 < prm.n_probs && prm.probs[pi + 1].row_begin <= g) ++pi;
+    const RunProb& pr = prm.probs[pi];
+    const long long r = g - pr.row_begin;
+    const long long c_begin = (r / 128) * 128;
+    const long long off_row = r * pr.ld;
+    // vector part
+    const long long c_vec_end = c_begin + ((pr.d - c_begin) / 4) * 4;
+    for (long long c = c_begin + lane * 4; c < c_vec_end; c += 128) {
+      const long long off = off_row + c;
+      float4 f = sum_shards<8>(pr.shards + off, pr.stride, prm.P);
+      f.x *= prm.inv_p;
+      f.y *= prm.inv_p;
+      f.z *= prm.inv_p;
+      f.w *= prm.inv_p;
+      float4 rn;
+      if (prm.first_step) {
+        rn = f;
+      } else {
+        const float4 old = *reinterpret_cast<const float4*>(pr.running + off);
+        rn.x = fmaf(decay, old.x, keep * f.x);
+        rn.y = fmaf(decay, old.y, keep * f.y);
+        rn.z = fmaf(decay, old.z, keep * f.z);
+        rn.w = fmaf(decay, old.w, keep * f.w);
+      }
+      float4 dm = rn;
+      if (r >= c && r < c + 4) {
+        const int k = (int)(r - c);
+        if (k == 0) dm.x += prm.gamma;
+        if (k == 1) dm.y += prm.gamma;
+        if (k == 2) dm.z += prm.gamma;
+        if (k == 3) dm.w += prm.gamma;
+      }
+      *reinterpret_cast<float4*>(pr.running + off) = rn;
+      __stcs(reinterpret_cast<float4*>(pr.damped + off), dm);
+    }
+    // scalar tail (d not a multiple of 4)
+    const long long c = c_vec_end + lane;
+    if (c < pr.d) {
+      const long long off = off_row + c;
+      float f = 0.f;
+      for (int p = 0; p < prm.P; ++p) f += pr.shards[off + (long long)p * pr.stride];
+      f *= prm.inv_p;
+      const float rn = prm.first_step ? f : fmaf(decay, pr.running[off], keep * f);
+      pr.running[off] = rn;
+      pr.damped[off] = (c == r) ? rn + prm.gamma : rn;
+    }
+  }
+}
+
+int launch_update_running(int n, const kfac_running_args* args, int P, float decay, float gamma, int first_step,
+                          cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return KFAC_ERR_CUDA;
+  for (int base = 0; base < n; base += kRunMaxProbs) {
+    const int cnt = n - base < kRunMaxProbs ? n - base : kRunMaxProbs;
+    RunParams prm;
+    memset(&prm, 0, sizeof(prm));
+    long long rows = 0;
+    for (int k = 0; k < cnt; ++k) {
+      const kfac_running_args& a = args[base + k];
+      RunProb& pr = prm.probs[k];
+      pr.shards = a.shards;
+      pr.running = a.running;
+      pr.damped = a.damped;
+      pr.stride = a.stride_shard;
+      pr.ld = a.ld;
+      pr.d = (int)a.d;
+      pr.row_begin = rows;
+      rows += a.d;
+    }
+    prm.n_probs = cnt;
+    prm.P = P;
+    prm.first_step = first_step;
+    prm.decay = decay;
+    prm.gamma = gamma;
+    prm.inv_p = 1.0f / (float)P;
+    prm.total_rows = rows;
+    if (rows == 0) continue;
+    const long long want = (rows + 7) / 8;  // 8 warps per block, one row per warp
+    const long long cap = (long long)sms * 8;
+    const int grid = (int)(want < cap ? want : cap);
+    update_running_kernel<<<grid, 256, 0, stream>>>(prm);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
+  }
+  return KFAC_OK;
+}
+
+}  // namespace kfac

@@ -1,0 +1,189 @@
+"""One K-FAC preconditioning step over a list of layers, through the C ABI.
+
+``KFACStep`` owns the device buffers of every layer (PyTorch allocates them;
+nothing else of PyTorch is used) and issues, per step, the library calls of
+the step in order (SPD-KFAC §II-B/§II-C):
+
+  1. kfac_spatial_sum       (conv layers: per-sample sum of g over H*W)
+  2. kfac_factors           per-worker factors A^p, G^p of all layers
+  3. kfac_update_running    mean over workers, running average, damping
+  4. kfac_damped_inverse    (A + gamma I)^-1, (G + gamma I)^-1 of all factors
+  5. kfac_precondition      (G + gamma I)^-1 grad (A + gamma I)^-1 of all layers
+
+Buffers are row-major with leading dimensions padded to 16-byte multiples
+(bf16 inputs) or 128-byte multiples (fp32 factor matrices).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import capi
+
+
+def _pad(v: int, m: int) -> int:
+    return (v + m - 1) // m * m
+
+
+@dataclasses.dataclass
+class LayerSpec:
+    d_in: int            # factor A dimension (incl. bias column)
+    d_out: int           # factor G dimension
+    rows: int            # rows of a and g per step
+    batch: int           # samples per step (conv: rows = batch * hw)
+    hw: int = 1          # spatial positions (1 for linear layers)
+
+
+class FactorBufs:
+    def __init__(self, d: int, P: int, device):
+        self.d = d
+        self.ld = _pad(d, 32)
+        self.P = P
+        self.stride = d * self.ld
+        self.shards = torch.zeros((P, d, self.ld), dtype=torch.float32, device=device)
+        self.running = torch.zeros((d, self.ld), dtype=torch.float32, device=device)
+        self.damped = torch.zeros((d, self.ld), dtype=torch.float32, device=device)
+        self.inv = torch.zeros((d, self.ld), dtype=torch.float32, device=device)
+
+
+class KFACStep:
+    def __init__(self, layers: Sequence[LayerSpec], P: int, gamma: float, decay: float, in_dtype: str,
+                 refine: int = capi.KFAC_REFINE_AUTO, device="cuda"):
+        self.layers = list(layers)
+        self.P = P
+        self.gamma = float(gamma)
+        self.decay = float(decay)
+        self.in_dtype = in_dtype
+        self.refine = refine
+        self.device = torch.device(device)
+        tdt = torch.bfloat16 if in_dtype == "bf16" else torch.float32
+        self.kdt = capi.KFAC_BF16 if in_dtype == "bf16" else capi.KFAC_FP32
+        vec = 8 if in_dtype == "bf16" else 4
+        dev = self.device
+        self.a, self.g, self.gs, self.grad, self.out = [], [], [], [], []
+        self.fa: List[FactorBufs] = []
+        self.fg: List[FactorBufs] = []
+        for L in self.layers:
+            if L.rows % P:
+                raise ValueError("rows must split into P equal shards")
+            self.a.append(torch.zeros((L.rows, _pad(L.d_in, vec)), dtype=tdt, device=dev))
+            self.g.append(torch.zeros((L.rows, _pad(L.d_out, vec)), dtype=tdt, device=dev))
+            if L.hw > 1:
+                if L.batch % P:
+                    raise ValueError("conv layers need batch % P == 0")
+                self.gs.append(torch.zeros((L.batch, _pad(L.d_out, 4)), dtype=torch.float32, device=dev))
+            else:
+                self.gs.append(None)
+            self.grad.append(torch.zeros((L.d_out, _pad(L.d_in, 32)), dtype=torch.float32, device=dev))
+            self.out.append(torch.zeros((L.d_out, _pad(L.d_in, 32)), dtype=torch.float32, device=dev))
+            self.fa.append(FactorBufs(L.d_in, P, dev))
+            self.fg.append(FactorBufs(L.d_out, P, dev))
+        nf = 2 * len(self.layers)
+        self.info = torch.zeros(nf, dtype=torch.int32, device=dev)
+        self.route = torch.zeros(nf, dtype=torch.int32, device=dev)
+        self._build_args()
+        self.inv_ws_bytes = capi.kfac_damped_inverse_workspace(self._inv_args, refine)
+        self.pc_ws_bytes = capi.kfac_precondition_workspace(self._pc_args)
+        if self.inv_ws_bytes == 0 or self.pc_ws_bytes == 0:
+            raise ValueError("workspace query rejected the arguments")
+        self.inv_ws = torch.empty(self.inv_ws_bytes, dtype=torch.uint8, device=dev)
+        self.pc_ws = torch.empty(self.pc_ws_bytes, dtype=torch.uint8, device=dev)
+
+    # ------------------------------------------------------------------ argument arrays
+    def factor_list(self):
+        """All factors in call order: A of every layer, then G of every layer."""
+        return self.fa + self.fg
+
+    def _build_args(self):
+        P = self.P
+        fa_main, fa_fp32 = [], []   # factors from a (dtype of a), factors from fp32 spatial sums
+        for li, L in enumerate(self.layers):
+            A = self.fa[li]
+            fa_main.append(capi.kfac_factor_args(self.a[li].data_ptr(), L.rows, L.d_in, self.a[li].shape[1],
+                                                 A.shards.data_ptr(), A.ld, A.stride, 1.0 / (L.rows // P)))
+        for li, L in enumerate(self.layers):
+            G = self.fg[li]
+            if L.hw > 1:
+                gs = self.gs[li]
+                fa_fp32.append(capi.kfac_factor_args(gs.data_ptr(), L.batch, L.d_out, gs.shape[1],
+                                                     G.shards.data_ptr(), G.ld, G.stride, 1.0 / (L.batch // P)))
+            else:
+                fa_main.append(capi.kfac_factor_args(self.g[li].data_ptr(), L.rows, L.d_out, self.g[li].shape[1],
+                                                     G.shards.data_ptr(), G.ld, G.stride, 1.0 / (L.rows // P)))
+        self._fac_main = fa_main
+        self._fac_fp32 = fa_fp32
+        self._run_args = [capi.kfac_running_args(F.shards.data_ptr(), F.stride, F.running.data_ptr(),
+                                                 F.damped.data_ptr(), F.d, F.ld) for F in self.factor_list()]
+        self._inv_args = [capi.kfac_inverse_args(F.damped.data_ptr(), F.inv.data_ptr(), F.d, F.ld, F.ld)
+                          for F in self.factor_list()]
+        self._pc_args = []
+        for li, L in enumerate(self.layers):
+            A, G = self.fa[li], self.fg[li]
+            self._pc_args.append(capi.kfac_precond_args(
+                G.inv.data_ptr(), G.ld, self.grad[li].data_ptr(), self.grad[li].shape[1],
+                A.inv.data_ptr(), A.ld, self.out[li].data_ptr(), self.out[li].shape[1], L.d_out, L.d_in))
+
+    # ------------------------------------------------------------------ inputs
+    def set_layer_inputs(self, li: int, a: torch.Tensor, g: torch.Tensor, grad: torch.Tensor,
+                         non_blocking: bool = False):
+        """Copy one layer's inputs (any device) into the padded device buffers."""
+        L = self.layers[li]
+        self.a[li][:, :L.d_in].copy_(a, non_blocking=non_blocking)
+        self.g[li][:, :L.d_out].copy_(g, non_blocking=non_blocking)
+        self.grad[li][:, :L.d_in].copy_(grad, non_blocking=non_blocking)
+
+    # ------------------------------------------------------------------ the step
+    def stream_handle(self, stream: Optional[torch.cuda.Stream] = None) -> int:
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        return s.cuda_stream
+
+    def factors(self, stream: int):
+        P = self.P
+        for li, L in enumerate(self.layers):
+            if L.hw > 1:
+                gs = self.gs[li]
+                capi.kfac_spatial_sum(self.g[li].data_ptr(), self.kdt, L.batch, L.hw, L.d_out,
+                                      self.g[li].shape[1], gs.data_ptr(), gs.shape[1], stream)
+        if self._fac_main:
+            capi.kfac_factors(self._fac_main, self.kdt, P, 0, stream)
+        if self._fac_fp32:
+            capi.kfac_factors(self._fac_fp32, capi.KFAC_FP32, P, 0, stream)
+
+    def update_running(self, first_step: bool, stream: int):
+        decay = 0.0 if first_step else self.decay
+        capi.kfac_update_running(self._run_args, self.P, decay, self.gamma, first_step, stream)
+
+    def inverse(self, stream: int):
+        capi.kfac_damped_inverse(self._inv_args, 0.0, self.refine, self.info.data_ptr(), self.route.data_ptr(),
+                                 self.inv_ws.data_ptr(), self.inv_ws_bytes, stream)
+
+    def precondition(self, stream: int):
+        capi.kfac_precondition(self._pc_args, self.pc_ws.data_ptr(), self.pc_ws_bytes, stream)
+
+    def step(self, first_step: bool, stream: Optional[torch.cuda.Stream] = None):
+        s = self.stream_handle(stream)
+        self.factors(s)
+        self.update_running(first_step, s)
+        self.inverse(s)
+        self.precondition(s)
+
+    # ------------------------------------------------------------------ counts
+    def algorithmic_work(self):
+        """Per-step algorithmic work of each stage (upper-triangle convention).
+
+        factor flops: 2 * rows * d(d+1)/2 per factor; update bytes: (P + 1 reads
+        + 2 writes) * 4 * d(d+1)/2 per factor (P + 2 accesses on a first step);
+        inverse flops: d^3 per factor; precondition flops: 2 d_out d_in (d_out + d_in).
+        """
+        fac = upd = inv = pc = 0
+        for li, L in enumerate(self.layers):
+            rows_g = L.batch if L.hw > 1 else L.rows
+            for d, rows in ((L.d_in, L.rows), (L.d_out, rows_g)):
+                tri = d * (d + 1) // 2
+                fac += 2 * rows * tri
+                upd += (self.P + 3) * 4 * tri
+                inv += d ** 3
+            pc += 2 * L.d_out * L.d_in * (L.d_out + L.d_in)
+        return dict(factor_flops=fac, update_bytes=upd, inverse_flops=inv, precond_flops=pc)

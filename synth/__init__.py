@@ -158,6 +158,38 @@ def _round(cfg: Config, x: np.ndarray) -> np.ndarray:
     return round_bf16(x32) if cfg.in_dtype == "bf16" else x32
 
 
+def torch_seed(*keys) -> int:
+    h = hashlib.sha256(repr(("torch",) + keys).encode()).digest()
+    return int.from_bytes(h[:8], "little") & ((1 << 63) - 1)
+
+
+def device_layer_inputs(cfg: Config, step: int, layer_index: int, device="cuda"):
+    """Same shapes and distributions as ``layer_inputs``, drawn on the device
+    from seeded torch generators (for sizes where host generation is slow).
+    Supports the "normal" and "relu_normal" workloads.  The weight gradient
+    is g^T a / B in float32 (an input of the step, made outside it)."""
+    import torch
+
+    if cfg.a_dist == "mlp":
+        raise ValueError("the MLP workload is generated on the host (layer_inputs)")
+    layer = cfg.layers[layer_index]
+    rows = cfg.rows(layer)
+    dt = torch.bfloat16 if cfg.in_dtype == "bf16" else torch.float32
+    gen = torch.Generator(device=device)
+    gen.manual_seed(torch_seed(cfg.key, step, layer_index, "a"))
+    body = torch.randn((rows, layer.d_in - 1), generator=gen, device=device, dtype=torch.float32) * cfg.a_sigma
+    if cfg.a_dist == "relu_normal":
+        body.clamp_(min=0.0)
+    a = torch.empty((rows, layer.d_in), dtype=dt, device=device)
+    a[:, :-1] = body.to(dt)
+    a[:, -1] = 1.0
+    del body
+    gen.manual_seed(torch_seed(cfg.key, step, layer_index, "g"))
+    g = (torch.randn((rows, layer.d_out), generator=gen, device=device, dtype=torch.float32) * cfg.g_sigma).to(dt)
+    grad = (g.float().t() @ a.float()) / cfg.batch
+    return {"a": a, "g": g, "grad": grad}
+
+
 def layer_inputs(cfg: Config, step: int, layer_index: int, with_grad: bool = True):
     """Inputs of one layer at one step, as float32 arrays holding the exact
     values given to the GPU (bf16-representable when ``cfg.in_dtype`` is bf16).

@@ -1,0 +1,179 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol kfac.h
+declares, its struct layouts agree with a C compiler's, its tile map equals
+the oracle's enumeration bit for bit, and invalid arguments are rejected on
+the host before any launch."""
+import ctypes as C
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from infra_fac_factors_gb300 import build, capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kfac.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    build.build()
+    return capi.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kfac_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function():
+    names = declared_functions()
+    assert len(names) == 12
+    out = subprocess.run(["nm", "-D", "--defined-only", capi.library_path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (kfac_[a-z_0-9]+)$", out, flags=re.M))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(capi.lib(), n)
+    assert set(names) == set(capi.exported_symbols)
+
+
+def test_struct_layouts_match_c_compiler():
+    src = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "kfac.h"
+#define S(t) printf(#t " %zu\n", sizeof(t));
+#define O(t, f) printf(#t "." #f " %zu\n", offsetof(t, f));
+int main(void) {
+  S(kfac_factor_args) O(kfac_factor_args, out) O(kfac_factor_args, scale)
+  S(kfac_running_args) O(kfac_running_args, damped) O(kfac_running_args, ld)
+  S(kfac_inverse_args) O(kfac_inverse_args, ld_out)
+  S(kfac_precond_args) O(kfac_precond_args, out) O(kfac_precond_args, d_in)
+  return 0;
+}
+"""
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "l.c")
+        exe = os.path.join(td, "l")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-I", os.path.dirname(HEADER), c, "-o", exe], check=True)
+        lines = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(l.split() for l in lines if l)
+    for name, st in (("kfac_factor_args", capi.kfac_factor_args), ("kfac_running_args", capi.kfac_running_args),
+                     ("kfac_inverse_args", capi.kfac_inverse_args), ("kfac_precond_args", capi.kfac_precond_args)):
+        assert int(got[name]) == C.sizeof(st), name
+        for key, val in got.items():
+            if key.startswith(name + "."):
+                field = key.split(".")[1]
+                assert getattr(st, field).offset == int(val), key
+
+
+@pytest.mark.parametrize("d", [1, 2, 10, 64, 127, 128, 129, 255, 256, 257, 385, 577, 1025, 1153, 2305, 3072,
+                               4096, 4097, 4609])
+def test_factor_tile_map_bit_exact(d):
+    assert capi.kfac_factor_tile_map(d) == oracle.factor_tile_units(d, 128, 256)
+
+
+def test_status_strings_and_version():
+    assert capi.kfac_status_string(0) == "KFAC_OK"
+    assert capi.kfac_status_string(5) == "KFAC_ERR_TIMEOUT"
+    assert capi.kfac_status_string(99) == "KFAC_ERR_UNKNOWN"
+    assert capi.kfac_version() >= 100
+
+
+# Fake (never dereferenced) device addresses: validation rejects before any CUDA call.
+A16 = 1 << 20
+
+
+def fa(**kw):
+    base = dict(x=A16, rows=64, d=10, ld_x=16, out=A16 * 2, ld_out=16, stride_out=160, scale=1 / 32)
+    base.update(kw)
+    return capi.kfac_factor_args(**base)
+
+
+@pytest.mark.parametrize("kw,dtype,P", [
+    (dict(x=None), capi.KFAC_BF16, 2),
+    (dict(x=A16 + 2), capi.KFAC_BF16, 2),          # misaligned base
+    (dict(rows=63), capi.KFAC_BF16, 2),            # rows % P
+    (dict(d=0), capi.KFAC_BF16, 2),
+    (dict(ld_x=12), capi.KFAC_BF16, 2),            # bf16 ld not a multiple of 8
+    (dict(ld_x=8), capi.KFAC_BF16, 2),             # ld < d
+    (dict(ld_out=18), capi.KFAC_BF16, 2),          # fp32 ld not a multiple of 4
+    (dict(stride_out=100), capi.KFAC_BF16, 2),     # shards overlap
+    (dict(scale=float("nan")), capi.KFAC_BF16, 2),
+    (dict(), 7, 2),                                # dtype
+    (dict(), capi.KFAC_BF16, 0),                   # P
+])
+def test_factors_rejects_invalid(kw, dtype, P):
+    assert capi.kfac_factors([fa(**kw)], dtype, P, check=False) == capi.KFAC_ERR_INVALID_ARG
+
+
+def ra(**kw):
+    base = dict(shards=A16, stride_shard=16 * 16, running=A16 * 2, damped=A16 * 3, d=16, ld=16)
+    base.update(kw)
+    return capi.kfac_running_args(**base)
+
+
+@pytest.mark.parametrize("kw,decay,gamma,P", [
+    (dict(), 1.0, 1e-3, 2), (dict(), -0.1, 1e-3, 2), (dict(), 0.9, -1e-3, 2),
+    (dict(), 0.9, float("inf"), 2), (dict(damped=A16 * 2), 0.9, 1e-3, 2),
+    (dict(ld=14), 0.9, 1e-3, 2), (dict(stride_shard=16), 0.9, 1e-3, 2), (dict(shards=None), 0.9, 1e-3, 2),
+    (dict(), 0.9, 1e-3, 0),
+])
+def test_update_running_rejects_invalid(kw, decay, gamma, P):
+    assert capi.kfac_update_running([ra(**kw)], P, decay, gamma, False, check=False) == capi.KFAC_ERR_INVALID_ARG
+
+
+def ia(**kw):
+    base = dict(damped=A16, inv=A16 * 2, d=8, ld_in=8, ld_out=8)
+    base.update(kw)
+    return capi.kfac_inverse_args(**base)
+
+
+def test_inverse_rejects_invalid():
+    ok = [ia()]
+    ws = capi.kfac_damped_inverse_workspace(ok, capi.KFAC_REFINE_AUTO)
+    assert ws > 0
+    assert capi.kfac_damped_inverse_workspace(ok, capi.KFAC_REFINE_NONE) < ws
+    for bad in (ia(d=0), ia(ld_in=6), ia(inv=A16), ia(ld_out=7), ia(damped=None)):
+        assert capi.kfac_damped_inverse_workspace([bad], 1) == 0
+        assert capi.kfac_damped_inverse([bad], 0.0, 1, A16, 0, A16 * 4, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_damped_inverse(ok, 0.0, 3, A16, 0, A16 * 4, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_damped_inverse(ok, -1.0, 1, A16, 0, A16 * 4, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_damped_inverse(ok, 0.0, 1, 0, 0, A16 * 4, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_damped_inverse(ok, 0.0, 1, A16, 0, A16 * 4, ws - 1, check=False) == capi.KFAC_ERR_WORKSPACE
+    assert capi.kfac_damped_inverse(ok, 0.0, 1, A16, 0, A16 * 4 + 16, ws, check=False) == capi.KFAC_ERR_WORKSPACE
+    assert capi.kfac_damped_inverse(ok, 0.0, 1, A16, 0, 0, ws, check=False) == capi.KFAC_ERR_WORKSPACE
+
+
+def pa(**kw):
+    base = dict(inv_g=A16, ld_g=8, grad=A16 * 2, ld_grad=12, inv_a=A16 * 3, ld_a=12, out=A16 * 4, ld_out=12,
+                d_out=8, d_in=12)
+    base.update(kw)
+    return capi.kfac_precond_args(**base)
+
+
+def test_precondition_rejects_invalid():
+    ws = capi.kfac_precondition_workspace([pa()])
+    assert ws == 8 * 12 * 4
+    for bad in (pa(d_in=0), pa(ld_g=4), pa(ld_grad=10), pa(out=A16 * 2), pa(inv_a=A16 + 4)):
+        assert capi.kfac_precondition_workspace([bad]) == 0
+        assert capi.kfac_precondition([bad], A16 * 5, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_precondition([pa()], A16 * 5, ws - 4, check=False) == capi.KFAC_ERR_WORKSPACE
+
+
+def test_spatial_sum_rejects_invalid():
+    f = capi.kfac_spatial_sum
+    assert f(0, 0, 2, 4, 8, 8, A16, 8, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert f(A16, 0, 2, 4, 8, 4, A16, 8, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert f(A16, 0, 0, 4, 8, 8, A16, 8, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert f(A16, 1, 2, 4, 8, 8, A16, 6, check=False) == capi.KFAC_ERR_INVALID_ARG
+
+
+def test_empty_calls_are_no_ops():
+    assert capi.kfac_factors([], capi.KFAC_BF16, 1, check=False) == capi.KFAC_OK
+    assert capi.kfac_update_running([], 1, 0.5, 0.0, True, check=False) == capi.KFAC_OK
+    assert capi.kfac_precondition([], 0, 0, check=False) == capi.KFAC_OK
