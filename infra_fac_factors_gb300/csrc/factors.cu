@@ -45,6 +45,10 @@ constexpr int kSyBBytes = 4 * kSyBox;          // up to 256 columns
 constexpr int kSyStageBytes = kSyABytes + kSyBBytes;
 constexpr int kSyMaxProbs = 96;
 constexpr int kSySmem = kSyStages * kSyStageBytes + 1024 + 256;
+// The TMEM accumulator is restarted every kSyChunkKB stages (1024 rows) and the
+// partial products are summed in fp32 by the epilogue: long worker shards
+// (12544 rows in the ResNet workload) then keep ~1e-6 relative accuracy.
+constexpr int kSyChunkKB = 16;
 
 struct SyProb {
   float* out;
@@ -146,34 +150,40 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
         const int nb = (un.w + 63) / 64;
         const uint32_t idesc = idesc_bf16_f32(nb * 64, true, true);
         const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * 256;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, prm.status)) {
+        for (int kc = 0; kc < nk && ok; kc += kSyChunkKB) {
+          const int kend = kc + kSyChunkKB < nk ? kc + kSyChunkKB : nk;
+          if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + stage * kSyStageBytes);
-          const uint32_t b0 = a0 + kSyABytes;
+          const uint32_t d_tmem = tmem_base + acc * 256;
+          for (int kb = kc; kb < kend; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, prm.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem + stage * kSyStageBytes);
+            const uint32_t b0 = a0 + kSyABytes;
 #pragma unroll
-          for (int kk = 0; kk < kSyBK / 16; ++kk) {
-            // 16 rows of k = two 8-row groups of 1024 B; 64-column blocks are kSyBox apart.
-            const uint64_t ad = smem_desc_sw128(a0 + kk * 2048, kSyBox, 1024);
-            const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kSyBox, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < kSyBK / 16; ++kk) {
+              // 16 rows of k = two 8-row groups of 1024 B; 64-column blocks are kSyBox apart.
+              const uint64_t ad = smem_desc_sw128(a0 + kk * 2048, kSyBox, 1024);
+              const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kSyBox, 1024);
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb != kc || kk != 0) ? 1u : 0u);
+            }
+            tc_commit(&empty[stage]);
+            if (++stage == kSyStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          tc_commit(&empty[stage]);
-          if (++stage == kSyStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (!ok) break;
+          tc_commit(&acc_full[acc]);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
         }
-        if (!ok) break;
-        tc_commit(&acc_full[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
       }
       // Every MMA issued above has completed once done_bar flips.
       tc_commit(done_bar);
@@ -182,50 +192,68 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint32_t acc = 0, acc_phase = 0;
-    for (long long u = blockIdx.x; u < prm.total_units; u += gridDim.x) {
+    bool ok = true;
+    for (long long u = blockIdx.x; u < prm.total_units && ok; u += gridDim.x) {
       const SyUnit un = sy_decode(prm, u);
       const SyProb& pr = prm.probs[un.prob];
       const int nb = (un.w + 63) / 64;
-      if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) break;
-      tc_fence_after();
+      const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
+      const int nchunks = (nk + kSyChunkKB - 1) / kSyChunkKB;
       const int r = un.i * 128 + q * 32 + lane;
       float* outp = pr.out + (long long)un.p * pr.stride_out;
       float* orow = outp + (long long)r * pr.ld_out;
       const long long jend = un.j0 + un.w;
-      for (int c = 0; c < nb * 2; ++c) {
-        uint32_t v[32];
-        tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
-        tc_wait_ld();
-        const long long col0 = un.j0 + c * 32;
-        if (r < pr.d && col0 < jend) {
-          if (col0 + 32 <= jend) {
+      const long long lower_from = (long long)(un.i + 1) * 128;  // columns in lower-tile territory
+      for (int ch = 0; ch < nchunks; ++ch) {
+        if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const bool first = ch == 0, last = ch == nchunks - 1;
+        for (int c = 0; c < nb * 2; ++c) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
+          tc_wait_ld();
+          const long long col0 = un.j0 + c * 32;
+          if (r < pr.d && col0 < jend) {
+            float o[32];
 #pragma unroll
-            for (int t = 0; t < 32; t += 4) {
-              float4 o;
-              o.x = __uint_as_float(v[t]) * pr.scale;
-              o.y = __uint_as_float(v[t + 1]) * pr.scale;
-              o.z = __uint_as_float(v[t + 2]) * pr.scale;
-              o.w = __uint_as_float(v[t + 3]) * pr.scale;
-              *reinterpret_cast<float4*>(orow + col0 + t) = o;
+            for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(v[t]) * pr.scale;
+            if (col0 + 32 <= jend) {
+#pragma unroll
+              for (int t = 0; t < 32; t += 4) {
+                float4* dst = reinterpret_cast<float4*>(orow + col0 + t);
+                if (!first) {
+                  const float4 prev = *dst;
+                  o[t] += prev.x;
+                  o[t + 1] += prev.y;
+                  o[t + 2] += prev.z;
+                  o[t + 3] += prev.w;
+                }
+                *dst = make_float4(o[t], o[t + 1], o[t + 2], o[t + 3]);
+              }
+            } else {
+              for (int t = 0; t < 32; ++t)
+                if (col0 + t < jend) {
+                  if (!first) o[t] += orow[col0 + t];
+                  orow[col0 + t] = o[t];
+                }
             }
-          } else {
-            for (int t = 0; t < 32; ++t)
-              if (col0 + t < jend) orow[col0 + t] = __uint_as_float(v[t]) * pr.scale;
-          }
-          if (prm.mirror) {
-            const long long lower_from = (long long)(un.i + 1) * 128;  // columns in lower-tile territory
-            for (int t = 0; t < 32; ++t) {
-              const long long col = col0 + t;
-              if (col < jend && col >= lower_from) outp[col * pr.ld_out + r] = __uint_as_float(v[t]) * pr.scale;
+            if (prm.mirror && last) {
+              for (int t = 0; t < 32; ++t) {
+                const long long col = col0 + t;
+                if (col < jend && col >= lower_from) outp[col * pr.ld_out + r] = o[t];
+              }
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
     }
   }
   __syncthreads();

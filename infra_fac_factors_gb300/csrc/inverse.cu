@@ -18,10 +18,12 @@
 // and finally X = W^T W, formed for the upper tiles and mirrored, so X is
 // exactly symmetric.  The same kernels run in fp32 and fp64 (templates).
 //
-// refine = AUTO: the fp32 pass also records ||D||_1 (row abs sums) and the
-// smallest pivot L_jj^2; matrices with ||D||_1 / min L_jj^2 > 1e5, or whose
-// fp32 factorisation failed, are redone in fp64 (the fp64 kernels of the other
-// matrices exit at once).
+// refine = AUTO: the fp32 pass also records ||D||_1 (row abs sums), the
+// smallest pivot L_jj^2 and ||X||_F.  The residual of an fp32 inverse behaves
+// like u ||D|| ||X||_F / sqrt(d) (u = 2^-24): matrices for which
+// u ||D||_1 ||X||_F / sqrt(d) > 1e-4 (ten times below the 1e-3 residual
+// target), or ||D||_1 / min L_jj^2 > 3e5, or whose fp32 factorisation failed,
+// are redone in fp64; the fp64 kernels of the other matrices exit at once.
 #include <math.h>
 
 #include "common.cuh"
@@ -31,7 +33,9 @@
 namespace kfac {
 
 constexpr int kInvMaxGroup = 256;
-constexpr float kAutoKappa = 1e5f;
+constexpr float kAutoKappa = 3e5f;
+constexpr float kAutoResidual = 1e-4f;
+constexpr float kUnitRoundoff32 = 5.9604645e-8f;  // 2^-24
 
 struct InvMat {
   const float* D;
@@ -45,7 +49,7 @@ struct InvMat {
 struct InvState {
   int info32, info64, failed, use64;
   float min_piv, kappa;
-  int pad0, pad1;
+  float xnorm2, est_res;  // ||X||_F^2 of the fp32 pass, predicted fp32 residual
 };
 
 struct InvSetup {
@@ -104,7 +108,8 @@ __global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, uint8_t* 
     s.use64 = prm.mode == KFAC_REFINE_ALWAYS ? 1 : 0;
     s.min_piv = 3.0e38f;
     s.kappa = 0.f;
-    s.pad0 = s.pad1 = 0;
+    s.xnorm2 = 0.f;
+    s.est_res = 0.f;
     st[e] = s;
   }
   for (long long e = tid; e < prm.rowsum_total; e += nth) rowsum[e] = 0.f;
@@ -374,6 +379,7 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
   Opnd<T> B{W + (long long)j * 128 * np + (long long)j * 128, 1, np, 128};
   simt_tile<T, T, T>(acc, A, B, (int)(np - (long long)j * 128), smem);
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  float sq = 0.f;  // this thread's share of ||X||_F^2
 #pragma unroll
   for (int a = 0; a < 8; ++a) {
     const int mm = ty * 8 + a;
@@ -388,7 +394,12 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
       const float v = (float)acc[a][b];
       m.X[row * m.ld_out + col] = v;
       m.X[col * m.ld_out + row] = v;
+      sq += (row == col ? 1.f : 2.f) * v * v;
     }
+  }
+  if (c.want_rowsum) {
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&c.st[mi].xnorm2, sq);
   }
 }
 
@@ -407,9 +418,12 @@ __global__ void __launch_bounds__(128) inv_flag_kernel(InvCtx c) {
   }
   if (threadIdx.x == 0) {
     InvState& s = c.st[mi];
-    const float kappa = s.min_piv > 0.f ? red[0] / s.min_piv : 3.0e38f;
+    const float norm1 = red[0];
+    const float kappa = s.min_piv > 0.f ? norm1 / s.min_piv : 3.0e38f;
+    const float est = kUnitRoundoff32 * norm1 * sqrtf(s.xnorm2) / sqrtf((float)m.d);
     s.kappa = kappa;
-    s.use64 = (s.failed || !(kappa <= kAutoKappa)) ? 1 : 0;
+    s.est_res = est;
+    s.use64 = (s.failed || !(kappa <= kAutoKappa) || !(est <= kAutoResidual)) ? 1 : 0;
   }
 }
 
@@ -499,7 +513,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (workspace_bytes < inverse_workspace(n, args, refine) || workspace == nullptr) return KFAC_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  static InvSetup prm;  // large; host-side staging only
+  InvSetup prm;  // 16 KB of kernel parameters, staged on the host stack
   int Ts[kInvMaxGroup];
   for (int base = 0; base < n; base += kInvMaxGroup) {
     const int cnt = n - base < kInvMaxGroup ? n - base : kInvMaxGroup;

@@ -195,7 +195,10 @@ def test_damped_inverse_batched_variable_sizes(refine):
     Ds = [spd_case(d, rng) for d in SIZES]
     Xs, info, route = run_inverse(Ds, refine)
     assert (info == 0).all()
-    assert (route == (1 if refine == capi.KFAC_REFINE_ALWAYS else 0)).all(), route
+    if refine == capi.KFAC_REFINE_AUTO:
+        assert set(route.tolist()) <= {0, 1}, route
+    else:
+        assert (route == (1 if refine == capi.KFAC_REFINE_ALWAYS else 0)).all(), route
     for D, X in zip(Ds, Xs):
         ref, i = oracle.spd_inverse(D.astype(np.float64))
         assert i == 0
@@ -286,7 +289,7 @@ def snapshot(step, li):
                 XA=f(A.inv)[:, :A.d], XG=f(G.inv)[:, :G.d])
 
 
-def check_config(key, steps, check_layers=None, e2e_tol=None):
+def check_config(key, steps, check_layers=None, inv_steps=None):
     cfg = synth.config(key)
     specs = layer_specs(cfg)
     step = KFACStep(specs, cfg.P, cfg.gamma, cfg.decay or 0.0, cfg.in_dtype, refine=capi.KFAC_REFINE_AUTO)
@@ -308,7 +311,7 @@ def check_config(key, steps, check_layers=None, e2e_tol=None):
         sync()
         info = step.info.cpu().numpy()
         assert (info == 0).all(), info
-        last = t == steps - 1
+        last = t in (inv_steps if inv_steps is not None else (steps - 1,))
         for li in check_layers:
             L = specs[li]
             snap = snapshot(step, li)
@@ -359,7 +362,8 @@ def test_config_single_linear_with_bruteforce_end_to_end():
 
 
 def test_config_mlp_ten_steps():
-    check_config("mlp", 10)
+    # every step: the first steps see rank-deficient factors (256 samples, 785/1025 inputs)
+    check_config("mlp", 10, inv_steps=range(10))
 
 
 def test_config_resnet_conv_one_step():
@@ -367,4 +371,4 @@ def test_config_resnet_conv_one_step():
 
 
 def test_config_bert_layer_three_steps():
-    check_config("bert_layer", 3)
+    check_config("bert_layer", 3, inv_steps=(0, 2))
