@@ -18,12 +18,15 @@
 // and finally X = W^T W, formed for the upper tiles and mirrored, so X is
 // exactly symmetric.  The same kernels run in fp32 and fp64 (templates).
 //
-// refine = AUTO: the fp32 pass also records ||D||_1 (row abs sums), the
-// smallest pivot L_jj^2 and ||X||_F.  The residual of an fp32 inverse behaves
-// like u ||D|| ||X||_F / sqrt(d) (u = 2^-24): matrices for which
-// u ||D||_1 ||X||_F / sqrt(d) > 1e-4 (ten times below the 1e-3 residual
-// target), or ||D||_1 / min L_jj^2 > 3e5, or whose fp32 factorisation failed,
-// are redone in fp64; the fp64 kernels of the other matrices exit at once.
+// refine = AUTO: the fp32 pass measures its own residual.  With kProbes
+// Rademacher vectors v (+-1 entries), w = D v is accumulated in fp64 while D
+// is loaded, and y = X w while X is written, so ||y - v||^2 averaged over the
+// probes is an unbiased estimate of ||X D - I||_F^2 at no extra HBM traffic
+// (products of fp32 values are exact in fp64).  Matrices whose estimated
+// residual ||X D - I||_F / sqrt(d) exceeds 2.5e-4 (four times below the 1e-3
+// target), whose ||D||_1 / min L_jj^2 exceeds 3e5 (a guard on the relative
+// error), or whose fp32 factorisation failed, are redone in fp64; the fp64
+// kernels of the other matrices exit at once.
 #include <math.h>
 
 #include "common.cuh"
@@ -34,8 +37,8 @@ namespace kfac {
 
 constexpr int kInvMaxGroup = 256;
 constexpr float kAutoKappa = 3e5f;
-constexpr float kAutoResidual = 1e-4f;
-constexpr float kUnitRoundoff32 = 5.9604645e-8f;  // 2^-24
+constexpr double kAutoResidual = 2.5e-4;
+constexpr int kProbes = 4;
 
 struct InvMat {
   const float* D;
@@ -43,19 +46,29 @@ struct InvMat {
   long long ld_in, ld_out;
   long long off_buf;     // byte offset of the L/W buffers in the workspace
   long long off_rowsum;  // float index of this matrix's row sums
-  int d, T, pad0, pad1;
+  long long off_probe;   // double index of this matrix's probe vectors w, y
+  int d, T;
 };
 
 struct InvState {
   int info32, info64, failed, use64;
   float min_piv, kappa;
-  float xnorm2, est_res;  // ||X||_F^2 of the fp32 pass, predicted fp32 residual
+  float xnorm2, est_res;  // ||X||_F^2 and the estimated residual of the fp32 pass
 };
+
+// Rademacher probe entry v_p(i) in {-1, +1} (splitmix64 finaliser of (i, p)).
+__device__ __forceinline__ double probe_sign(long long i, int p) {
+  unsigned long long z = (unsigned long long)(i * kProbes + p) + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return (z & 1ull) ? 1.0 : -1.0;
+}
 
 struct InvSetup {
   InvMat mats[kInvMaxGroup];
   int n, mode;
-  long long rowsum_total;
+  long long rowsum_total, probe_total;
 };
 
 struct InvCtx {
@@ -63,9 +76,10 @@ struct InvCtx {
   const InvMat* mats;
   InvState* st;
   float* rowsum;
+  double* probe;  // per matrix: w[kProbes][n_pad] then y[kProbes][n_pad]
   float gamma_extra;
   int pass64;  // 0: fp32 pass, 1: fp64 pass
-  int want_rowsum;
+  int want_rowsum;  // fp32 pass of AUTO: record norms and probes
 };
 
 template <typename T>
@@ -96,7 +110,7 @@ __device__ __forceinline__ int tri_root(long long q) {
 
 // ------------------------------------------------------------------ setup
 __global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, uint8_t* ws, InvMat* mats, InvState* st,
-                                 float* rowsum) {
+                                 float* rowsum, double* probe) {
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nth = (long long)gridDim.x * blockDim.x;
   for (long long e = tid; e < prm.n; e += nth) {
@@ -113,6 +127,7 @@ __global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, uint8_t* 
     st[e] = s;
   }
   for (long long e = tid; e < prm.rowsum_total; e += nth) rowsum[e] = 0.f;
+  for (long long e = tid; e < prm.probe_total; e += nth) probe[e] = 0.0;
 }
 
 // ------------------------------------------------------------------ load D into the L-buffer
@@ -129,9 +144,12 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
   T* L = lbuf<T>(c, m);
   __shared__ float sub[32][33];
   __shared__ float rs_row[128], rs_col[128];
+  __shared__ double pw_row[kProbes][128], pw_col[kProbes][128];  // partial w = D v
   if (threadIdx.x < 128) {
     rs_row[threadIdx.x] = 0.f;
     rs_col[threadIdx.x] = 0.f;
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) pw_row[p][threadIdx.x] = pw_col[p][threadIdx.x] = 0.0;
   }
   __syncthreads();
   const int lx = threadIdx.x % 32, ly = threadIdx.x / 32;  // 32 x 8
@@ -157,13 +175,19 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
       } else if (gr < gc) {
         out = T(0);
       } else {
+        out = (T)v;
+        if (gr == gc) out += (T)c.gamma_extra;
         if (c.want_rowsum) {
           const float a = fabsf(v);
           atomicAdd(&rs_row[bm + y], a);
           if (gr != gc) atomicAdd(&rs_col[bn + lx], a);
+          const double x = (double)out;  // the matrix being inverted, as stored
+#pragma unroll
+          for (int p = 0; p < kProbes; ++p) {
+            atomicAdd(&pw_row[p][bm + y], x * probe_sign(gc, p));
+            if (gr != gc) atomicAdd(&pw_col[p][bn + lx], x * probe_sign(gr, p));
+          }
         }
-        out = (T)v;
-        if (gr == gc) out += (T)c.gamma_extra;
       }
       L[gr * np + gc] = out;
     }
@@ -174,6 +198,12 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
     const long long gc = (long long)C * 128 + threadIdx.x;
     if (gr < m.d && rs_row[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gr], rs_row[threadIdx.x]);
     if (gc < m.d && rs_col[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gc], rs_col[threadIdx.x]);
+    double* w = c.probe + m.off_probe;
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) {
+      if (gr < m.d) atomicAdd(&w[p * np + gr], pw_row[p][threadIdx.x]);
+      if (gc < m.d) atomicAdd(&w[p * np + gc], pw_col[p][threadIdx.x]);
+    }
   }
 }
 
@@ -379,6 +409,15 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
   Opnd<T> B{W + (long long)j * 128 * np + (long long)j * 128, 1, np, 128};
   simt_tile<T, T, T>(acc, A, B, (int)(np - (long long)j * 128), smem);
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  const bool probe = c.want_rowsum;
+  __shared__ double py_row[kProbes][128], py_col[kProbes][128];  // partial y = X w
+  const double* w = c.probe + m.off_probe;
+  if (probe) {
+    if (threadIdx.x < 128)
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p) py_row[p][threadIdx.x] = py_col[p][threadIdx.x] = 0.0;
+    __syncthreads();
+  }
   float sq = 0.f;  // this thread's share of ||X||_F^2
 #pragma unroll
   for (int a = 0; a < 8; ++a) {
@@ -395,11 +434,31 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
       m.X[row * m.ld_out + col] = v;
       m.X[col * m.ld_out + row] = v;
       sq += (row == col ? 1.f : 2.f) * v * v;
+      if (probe) {
+        // the stored value X[row][col] = X[col][row] contributes to y[row] and y[col]
+        const double x = (double)v;
+#pragma unroll
+        for (int p = 0; p < kProbes; ++p) {
+          atomicAdd(&py_row[p][mm], x * w[p * np + col]);
+          if (row != col) atomicAdd(&py_col[p][nn], x * w[p * np + row]);
+        }
+      }
     }
   }
-  if (c.want_rowsum) {
+  if (probe) {
     for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
     if ((threadIdx.x & 31) == 0) atomicAdd(&c.st[mi].xnorm2, sq);
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      double* y = c.probe + m.off_probe + (long long)kProbes * np;
+      const long long row = (long long)i * 128 + threadIdx.x;
+      const long long col = (long long)j * 128 + threadIdx.x;
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p) {
+        if (row < m.d) atomicAdd(&y[p * np + row], py_row[p][threadIdx.x]);
+        if (col < m.d) atomicAdd(&y[p * np + col], py_col[p][threadIdx.x]);
+      }
+    }
   }
 }
 
@@ -408,21 +467,37 @@ __global__ void __launch_bounds__(128) inv_flag_kernel(InvCtx c) {
   const int mi = blockIdx.x;
   const InvMat m = c.mats[mi];
   __shared__ float red[128];
+  __shared__ double red2[128];
+  const long long np = (long long)m.T * 128;
+  const double* y = c.probe + m.off_probe + (long long)kProbes * np;
   float mx = 0.f;
-  for (int r = threadIdx.x; r < m.d; r += 128) mx = fmaxf(mx, c.rowsum[m.off_rowsum + r]);
+  double e2 = 0.0;  // sum over probes of ||X (D v) - v||^2
+  for (int r = threadIdx.x; r < m.d; r += 128) {
+    mx = fmaxf(mx, c.rowsum[m.off_rowsum + r]);
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) {
+      const double e = y[p * np + r] - probe_sign(r, p);
+      e2 += e * e;
+    }
+  }
   red[threadIdx.x] = mx;
+  red2[threadIdx.x] = e2;
   __syncthreads();
   for (int s = 64; s > 0; s >>= 1) {
-    if (threadIdx.x < s) red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + s]);
+    if (threadIdx.x < s) {
+      red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + s]);
+      red2[threadIdx.x] += red2[threadIdx.x + s];
+    }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
     InvState& s = c.st[mi];
     const float norm1 = red[0];
     const float kappa = s.min_piv > 0.f ? norm1 / s.min_piv : 3.0e38f;
-    const float est = kUnitRoundoff32 * norm1 * sqrtf(s.xnorm2) / sqrtf((float)m.d);
+    // E||(XD - I) v||^2 = ||XD - I||_F^2 for Rademacher v
+    const double est = sqrt(red2[0] / kProbes / (double)m.d);
     s.kappa = kappa;
-    s.est_res = est;
+    s.est_res = (float)est;
     s.use64 = (s.failed || !(kappa <= kAutoKappa) || !(est <= kAutoResidual)) ? 1 : 0;
   }
 }
@@ -437,24 +512,29 @@ __global__ void inv_finish_kernel(InvCtx c, int n, int* info, int* route) {
 
 // ------------------------------------------------------------------ host side
 struct InvLayout {
-  size_t mats_off, st_off, rowsum_off, buf_off, total;
+  size_t mats_off, st_off, rowsum_off, probe_off, buf_off, total;
 };
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 static InvLayout inv_layout(int n, const kfac_inverse_args* args, int refine, long long* rowsum_total,
-                            InvMat* mats /* may be null */) {
+                            long long* probe_total, InvMat* mats /* may be null */) {
   InvLayout L;
   L.mats_off = 0;
   L.st_off = align256(sizeof(InvMat) * (size_t)n);
   L.rowsum_off = L.st_off + align256(sizeof(InvState) * (size_t)n);
   long long rs = 0;
   for (int i = 0; i < n; ++i) {
-    if (mats) mats[i].off_rowsum = rs;
+    if (mats) {
+      mats[i].off_rowsum = rs;
+      mats[i].off_probe = 2 * kProbes * rs;
+    }
     rs += (args[i].d + 127) / 128 * 128;
   }
   *rowsum_total = rs;
-  L.buf_off = L.rowsum_off + align256(sizeof(float) * (size_t)rs);
+  *probe_total = 2 * kProbes * rs;
+  L.probe_off = L.rowsum_off + align256(sizeof(float) * (size_t)rs);
+  L.buf_off = L.probe_off + align256(sizeof(double) * (size_t)(2 * kProbes * rs));
   size_t off = L.buf_off;
   const size_t elem = refine == KFAC_REFINE_NONE ? 4 : 8;
   for (int i = 0; i < n; ++i) {
@@ -471,8 +551,8 @@ size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine) {
   size_t best = 0;
   for (int base = 0; base < n; base += kInvMaxGroup) {
     const int cnt = n - base < kInvMaxGroup ? n - base : kInvMaxGroup;
-    long long rs;
-    const InvLayout L = inv_layout(cnt, args + base, refine, &rs, nullptr);
+    long long rs, pt;
+    const InvLayout L = inv_layout(cnt, args + base, refine, &rs, &pt, nullptr);
     if (L.total > best) best = L.total;
   }
   return best;
@@ -518,8 +598,8 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
   for (int base = 0; base < n; base += kInvMaxGroup) {
     const int cnt = n - base < kInvMaxGroup ? n - base : kInvMaxGroup;
     memset(&prm, 0, sizeof(prm));
-    long long rs_total = 0;
-    const InvLayout L = inv_layout(cnt, args + base, refine, &rs_total, prm.mats);
+    long long rs_total = 0, probe_total = 0;
+    const InvLayout L = inv_layout(cnt, args + base, refine, &rs_total, &probe_total, prm.mats);
     int Tmax = 0;
     for (int i = 0; i < cnt; ++i) {
       const kfac_inverse_args& a = args[base + i];
@@ -536,19 +616,21 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
     prm.n = cnt;
     prm.mode = refine;
     prm.rowsum_total = rs_total;
+    prm.probe_total = refine == KFAC_REFINE_AUTO ? probe_total : 0;
     InvCtx ctx;
     ctx.ws = ws;
     ctx.mats = reinterpret_cast<const InvMat*>(ws + L.mats_off);
     ctx.st = reinterpret_cast<InvState*>(ws + L.st_off);
     ctx.rowsum = reinterpret_cast<float*>(ws + L.rowsum_off);
+    ctx.probe = reinterpret_cast<double*>(ws + L.probe_off);
     ctx.gamma_extra = gamma_extra;
     ctx.want_rowsum = refine == KFAC_REFINE_AUTO;
     {
-      const long long work = rs_total > cnt ? rs_total : cnt;
+      const long long work = probe_total > cnt ? probe_total : cnt;
       long long blocks = (work + 255) / 256;
       if (blocks > 1024) blocks = 1024;
       inv_setup_kernel<<<(unsigned)blocks, 256, 0, stream>>>(prm, ws, const_cast<InvMat*>(ctx.mats), ctx.st,
-                                                             ctx.rowsum);
+                                                             ctx.rowsum, ctx.probe);
       count_launch();
     }
     int rc;

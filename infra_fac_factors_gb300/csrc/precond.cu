@@ -1,127 +1,78 @@
 // Preconditioned gradient of each layer (SPD-KFAC §II-B, the damped update
-// rule):  out = inv_g * grad * inv_a.
-// Two grouped GEMM launches over all layers: tmp = grad * inv_a, then
-// out = inv_g * tmp.  fp32 operands, fp32 products and accumulation on CUDA
-// cores (simt.cuh).
+// rule):  out = inv_g * grad * inv_a, on tcgen05 tensor cores.
+//
+// The fp32 operands are carried as split-bf16 pairs (x = hi + lo, three
+// products per multiply-add; gemm_tc.cu), which keeps ~2^-16 relative error per
+// product: plain bf16 operands would not do, because grad lies in the row
+// space of the layer input while inv_a amplifies the other directions by up to
+// 1/gamma, magnifying operand rounding.
+//   1. split      grad, inv_a, inv_g -> bf16 (hi, lo) slices   (one launch)
+//   2. GEMM 1     tmp^T = inv_a * grad^T   (d_in x d_out), written as slices
+//   3. GEMM 2     out   = inv_g * tmp      (= inv_g * (tmp^T)^T), fp32
+// inv_a and inv_g are symmetric, so their rows serve as the K-major operands.
 #include "common.cuh"
+#include "gemm_tc.h"
 #include "launch.h"
-#include "simt.cuh"
 
 namespace kfac {
 
-constexpr int kPcMaxProbs = 256;
+static long long pad8(long long v) { return (v + 7) / 8 * 8; }
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-struct GemmProb {
-  const float* A;  // M x K, row-major (K contiguous)
-  const float* B;  // K x N, row-major (N contiguous)
-  float* C;        // M x N
-  long long lda, ldb, ldc, tile_begin;
-  int M, N, K, tiles_n;
-};
-struct GemmParams {
-  GemmProb probs[kPcMaxProbs];
-  long long total_tiles;
-  int n_probs;
+struct PcLayout {
+  size_t grad, inv_a, inv_g, tmp, end;
 };
 
-__global__ void __launch_bounds__(256) gemm_nn_kernel(const __grid_constant__ GemmParams prm) {
-  __shared__ __align__(16) float smem[simt_smem_bytes<float>() / sizeof(float)];
-  for (long long u = blockIdx.x; u < prm.total_tiles; u += gridDim.x) {
-    int pi = 0;
-    while (pi + 1 < prm.n_probs && prm.probs[pi + 1].tile_begin <= u) ++pi;
-    const GemmProb& g = prm.probs[pi];
-    const long long t = u - g.tile_begin;
-    const int tm = (int)(t / g.tiles_n), tn = (int)(t % g.tiles_n);
-    Opnd<float> A{g.A + (long long)tm * 128 * g.lda, g.lda, 1, min(128, g.M - tm * 128)};
-    Opnd<float> B{g.B + (long long)tn * 128, 1, g.ldb, min(128, g.N - tn * 128)};
-    float acc[8][8];
-    zero_acc(acc);
-    simt_tile<float, float, float>(acc, A, B, g.K, smem);
-    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-      const int r = tm * 128 + ty * 8 + a;
-      if (r >= g.M) continue;
-      float* crow = g.C + (long long)r * g.ldc;
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        const int cidx = tn * 128 + tx * 8 + b;
-        if (cidx < g.N) crow[cidx] = acc[a][b];
-      }
-    }
-  }
+// Workspace of layer i starting at byte `off`: four bf16 slice pairs.
+static PcLayout pc_layout(const kfac_precond_args& a, size_t off) {
+  PcLayout L;
+  L.grad = off;
+  off += align256(2 * a.d_out * pad8(a.d_in) * sizeof(uint16_t));
+  L.inv_a = off;
+  off += align256(2 * a.d_in * pad8(a.d_in) * sizeof(uint16_t));
+  L.inv_g = off;
+  off += align256(2 * a.d_out * pad8(a.d_out) * sizeof(uint16_t));
+  L.tmp = off;
+  off += align256(2 * a.d_in * pad8(a.d_out) * sizeof(uint16_t));
+  L.end = off;
+  return L;
 }
-
-static long long pad4(long long v) { return (v + 3) / 4 * 4; }
 
 size_t precondition_workspace(int n, const kfac_precond_args* args) {
-  size_t total = 0;
-  for (int i = 0; i < n; ++i) total += (size_t)args[i].d_out * pad4(args[i].d_in) * sizeof(float);
-  return total;
-}
-
-static int run_gemms(const GemmProb* probs, int n, cudaStream_t stream, int sms) {
-  for (int base = 0; base < n; base += kPcMaxProbs) {
-    const int cnt = n - base < kPcMaxProbs ? n - base : kPcMaxProbs;
-    GemmParams prm;
-    memset(&prm, 0, sizeof(prm));
-    long long tiles = 0;
-    for (int k = 0; k < cnt; ++k) {
-      prm.probs[k] = probs[base + k];
-      GemmProb& g = prm.probs[k];
-      g.tiles_n = (g.N + 127) / 128;
-      g.tile_begin = tiles;
-      tiles += (long long)((g.M + 127) / 128) * g.tiles_n;
-    }
-    prm.n_probs = cnt;
-    prm.total_tiles = tiles;
-    if (tiles == 0) continue;
-    const long long cap = (long long)sms * 4;
-    gemm_nn_kernel<<<(unsigned)(tiles < cap ? tiles : cap), 256, 0, stream>>>(prm);
-    count_launch();
-    if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
-  }
-  return KFAC_OK;
+  size_t off = 0;
+  for (int i = 0; i < n; ++i) off = pc_layout(args[i], off).end;
+  return off;
 }
 
 int launch_precondition(int n, const kfac_precond_args* args, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream) {
   if (workspace_bytes < precondition_workspace(n, args) || (workspace == nullptr && n > 0)) return KFAC_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
-  const int sms = device_sm_count(dev);
-  GemmProb* g1 = new GemmProb[n > 0 ? n : 1];
-  GemmProb* g2 = new GemmProb[n > 0 ? n : 1];
-  float* tmp = static_cast<float*>(workspace);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SplitItem* items = new SplitItem[3 * (size_t)n];
+  GtOperand* g1 = new GtOperand[n];
+  GtOperand* g2 = new GtOperand[n];
+  size_t off = 0;
   for (int i = 0; i < n; ++i) {
     const kfac_precond_args& a = args[i];
-    const long long ldt = pad4(a.d_in);
-    GemmProb& p1 = g1[i];
-    memset(&p1, 0, sizeof(p1));
-    p1.A = a.grad;
-    p1.lda = a.ld_grad;
-    p1.B = a.inv_a;
-    p1.ldb = a.ld_a;
-    p1.C = tmp;
-    p1.ldc = ldt;
-    p1.M = (int)a.d_out;
-    p1.N = (int)a.d_in;
-    p1.K = (int)a.d_in;
-    GemmProb& p2 = g2[i];
-    memset(&p2, 0, sizeof(p2));
-    p2.A = a.inv_g;
-    p2.lda = a.ld_g;
-    p2.B = tmp;
-    p2.ldb = ldt;
-    p2.C = a.out;
-    p2.ldc = a.ld_out;
-    p2.M = (int)a.d_out;
-    p2.N = (int)a.d_in;
-    p2.K = (int)a.d_out;
-    tmp += a.d_out * ldt;
+    const PcLayout L = pc_layout(a, off);
+    off = L.end;
+    uint16_t* s_grad = reinterpret_cast<uint16_t*>(ws + L.grad);
+    uint16_t* s_ia = reinterpret_cast<uint16_t*>(ws + L.inv_a);
+    uint16_t* s_ig = reinterpret_cast<uint16_t*>(ws + L.inv_g);
+    uint16_t* s_tmp = reinterpret_cast<uint16_t*>(ws + L.tmp);
+    const long long ldi = pad8(a.d_in), ldo = pad8(a.d_out);
+    items[3 * i + 0] = SplitItem{a.grad, s_grad, a.d_out, a.d_in, a.ld_grad, ldi, a.d_out * ldi, 0};
+    items[3 * i + 1] = SplitItem{a.inv_a, s_ia, a.d_in, a.d_in, a.ld_a, ldi, a.d_in * ldi, 0};
+    items[3 * i + 2] = SplitItem{a.inv_g, s_ig, a.d_out, a.d_out, a.ld_g, ldo, a.d_out * ldo, 0};
+    // tmp^T[n][m] = sum_k inv_a[n][k] grad[m][k]: M = d_in, N = d_out, K = d_in
+    g1[i] = GtOperand{s_ia, s_grad, a.d_in, a.d_out, a.d_in, ldi, ldi, s_tmp, ldo, a.d_in * ldo, 1, 1.0f};
+    // out[m][n] = sum_k inv_g[m][k] tmp^T[n][k]: M = d_out, N = d_in, K = d_out
+    g2[i] = GtOperand{s_ig, s_tmp, a.d_out, a.d_in, a.d_out, ldo, ldo, a.out, a.ld_out, 0, 0, 1.0f};
   }
-  int rc = run_gemms(g1, n, stream, sms);
-  if (rc == KFAC_OK) rc = run_gemms(g2, n, stream, sms);
+  int rc = launch_split(items, 3 * n, stream);
+  if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, stream);
+  if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, stream);
+  delete[] items;
   delete[] g1;
   delete[] g2;
   return rc;
