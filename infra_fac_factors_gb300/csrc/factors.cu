@@ -44,7 +44,11 @@ constexpr int kSyABytes = 2 * kSyBox;          // 128 columns
 constexpr int kSyBBytes = 4 * kSyBox;          // up to 256 columns
 constexpr int kSyStageBytes = kSyABytes + kSyBBytes;
 constexpr int kSyMaxProbs = 96;
-constexpr int kSySmem = kSyStages * kSyStageBytes + 1024 + 256;
+// Epilogue staging: per epilogue warp two 32 x 32 fp32 blocks (4 KB each,
+// 128-byte swizzled), written to global memory by TMA stores.
+constexpr int kSyStageOut = 4096;
+constexpr int kSyOutBytes = 4 * 2 * kSyStageOut;
+constexpr int kSySmem = kSyStages * kSyStageBytes + kSyOutBytes + 1024 + 256;
 // The TMEM accumulator is restarted every kSyChunkKB stages (1024 rows) and the
 // partial products are summed in fp32 by the epilogue: long worker shards
 // (12544 rows in the ResNet workload) then keep ~1e-6 relative accuracy.
@@ -59,7 +63,8 @@ struct SyProb {
 };
 
 struct SyParams {  // 128-byte aligned through CUtensorMap
-  CUtensorMap maps[kSyMaxProbs];
+  CUtensorMap maps[kSyMaxProbs];   // inputs  {d, rows_p, P} bf16, box 64 x 64
+  CUtensorMap omaps[kSyMaxProbs];  // outputs {d, d, P} fp32, box 32 x 32, swizzled
   SyProb probs[kSyMaxProbs];
   long long total_units;
   int* status;
@@ -87,7 +92,8 @@ __device__ __forceinline__ SyUnit sy_decode(const SyParams& prm, long long u) {
 __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__ SyParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSyStages * kSyStageBytes);
+  uint8_t* out_stage = smem + kSyStages * kSyStageBytes;  // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + kSyOutBytes);
   uint64_t* empty = full + kSyStages;
   uint64_t* acc_full = empty + kSyStages;
   uint64_t* acc_empty = acc_full + 2;
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint32_t acc = 0, acc_phase = 0;
+    int obuf = 0;  // staging buffer of this warp in use
     bool ok = true;
     for (long long u = blockIdx.x; u < prm.total_units && ok; u += gridDim.x) {
       const SyUnit un = sy_decode(prm, u);
@@ -211,6 +218,40 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
         }
         tc_fence_after();
         const bool first = ch == 0, last = ch == nchunks - 1;
+        if (!prm.mirror) {
+          // Stage each 32 x 32 block in shared memory (128-byte swizzle: chunk j
+          // of row t lands at chunk j ^ (t & 7), conflict-free) and write it with
+          // a TMA store; later K-chunks of the same unit add with a TMA reduce.
+          if (!first && lane == 0) bulk_wait<0>();  // earlier writes of this unit are done
+          const int r0 = un.i * 128 + q * 32;
+          for (int c = 0; c < nb * 2; ++c) {
+            uint32_t v[32];
+            tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
+            tc_wait_ld();
+            const long long col0 = un.j0 + c * 32;
+            if (col0 >= jend || r0 >= pr.d) continue;  // uniform over the warp
+            uint8_t* buf = out_stage + (q * 2 + obuf) * kSyStageOut;
+            if (lane == 0) bulk_wait_read<1>();  // the store that last used `buf` has read it
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float4 o = make_float4(__uint_as_float(v[4 * j]) * pr.scale, __uint_as_float(v[4 * j + 1]) * pr.scale,
+                                     __uint_as_float(v[4 * j + 2]) * pr.scale,
+                                     __uint_as_float(v[4 * j + 3]) * pr.scale);
+              *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (first)
+                tma_store_3d(&prm.omaps[un.prob], buf, (int)col0, r0, un.p);
+              else
+                tma_reduce_add_3d(&prm.omaps[un.prob], buf, (int)col0, r0, un.p);
+              bulk_commit();
+            }
+            obuf ^= 1;
+          }
+        } else
         for (int c = 0; c < nb * 2; ++c) {
           uint32_t v[32];
           tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
@@ -255,6 +296,8 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
         if (acc == 0) acc_phase ^= 1;
       }
     }
+    if (lane == 0) bulk_wait<0>();  // all TMA stores of this warp complete before exit
+    __syncwarp();
   }
   __syncthreads();
   if (warp == 1) {
@@ -382,6 +425,14 @@ int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mi
         CUresult cr = enc(&prm.maps[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.x), gdim, gstride,
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (cr != CUDA_SUCCESS) return KFAC_ERR_INVALID_ARG;
+        const long long so = P > 1 ? a.stride_out : a.d * a.ld_out;
+        cuuint64_t odim[3] = {(cuuint64_t)a.d, (cuuint64_t)a.d, (cuuint64_t)P};
+        cuuint64_t ostride[2] = {(cuuint64_t)a.ld_out * 4, (cuuint64_t)so * 4};
+        cuuint32_t obox[3] = {32, 32, 1};
+        cr = enc(&prm.omaps[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.out, odim, ostride, obox, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) return KFAC_ERR_INVALID_ARG;
         SyProb& pr = prm.probs[k];
         pr.out = a.out;

@@ -2,18 +2,21 @@
 //
 //     C[m, n] = alpha * sum_k A[m, k] B[n, k]        (A: M x K, B: N x K)
 //
-// Every fp32 operand x is carried as two bf16 slices x = hi + lo with
-// hi = bf16(x), lo = bf16(x - hi) (16 significant bits), and the three
-// products hi*hi + hi*lo + lo*hi are accumulated in one fp32 TMEM accumulator
-// (the dropped lo*lo term is below 2^-16 of the product).  The two slices of
-// an operand are the z = 0 / 1 planes of one row-major buffer [2][rows][ld],
-// read by TMA with the 128-byte swizzle (K-major, 64 values of k per row).
+// Every fp32 operand x is carried as NS bf16 slices whose sum is x:
+//   NS = 2: x = hi + lo (16 significant bits); products hi*hi + hi*lo + lo*hi;
+//   NS = 3: x = hi + mid + lo (24 bits, all of fp32); products hi*hi + hi*mid +
+//           mid*hi + hi*lo + lo*hi + mid*mid (the dropped terms are below 2^-24
+//           of the product).
+// All products of a tile go into one fp32 TMEM accumulator.  The slices of an
+// operand are the z-planes of one row-major buffer [NS][rows][ld], read by TMA
+// K-major with a swizzle as wide as one stage row (NS = 2: 64 values of k,
+// 128-byte swizzle; NS = 3: 32 values of k, 64-byte swizzle, so that three
+// stages of all six tiles fit in shared memory).
 //
 // Kernel roles (192 threads, one CTA per SM, persistent over 128 x 256 tiles):
-//   warp 0: TMA producer, 2 stages of {A_hi, A_lo, B_hi, B_lo} (96 KB each);
-//   warp 1: TMEM allocation + MMA issuer; warps 2-5: epilogue.
-// The epilogue writes either fp32 C or C split again into bf16 hi/lo slices
-// (so one GEMM can feed the next one directly).
+//   warp 0: TMA producer; warp 1: TMEM allocation + MMA issuer;
+//   warps 2-5: epilogue (fp32 C, or C split again into NS bf16 slices so one
+//   GEMM feeds the next directly).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -26,12 +29,24 @@
 
 namespace kfac {
 
-constexpr int kGtBK = 64;
-constexpr int kGtStages = 2;
-constexpr int kGtABytes = 128 * kGtBK * 2;  // one slice of the A tile: 16 KB
-constexpr int kGtBBytes = 256 * kGtBK * 2;  // one slice of the B tile: 32 KB
-constexpr int kGtStageBytes = 2 * kGtABytes + 2 * kGtBBytes;
-constexpr int kGtSmem = kGtStages * kGtStageBytes + 1024 + 256;
+template <int NS>
+struct GtCfg;
+template <>
+struct GtCfg<2> {
+  static constexpr int BK = 64, STAGES = 2, SWZ = 2 /*128 B*/, ROWB = 128, NPROD = 3;
+};
+template <>
+struct GtCfg<3> {
+  static constexpr int BK = 32, STAGES = 3, SWZ = 4 /*64 B*/, ROWB = 64, NPROD = 6;
+};
+template <int NS>
+struct GtLayout {
+  static constexpr int BK = GtCfg<NS>::BK;
+  static constexpr int A = 128 * BK * 2;  // one slice of the A tile
+  static constexpr int B = 256 * BK * 2;  // one slice of the B tile
+  static constexpr int STAGE = NS * (A + B);
+  static constexpr int SMEM = GtCfg<NS>::STAGES * STAGE + 1024 + 256;
+};
 
 struct GtParams {
   CUtensorMap mapA[kGtMaxProbs];
@@ -43,7 +58,7 @@ struct GtParams {
 };
 
 struct GtTile {
-  int prob, m0, n0, n_valid, n_mma, K;
+  int prob, m0, n0, n_mma, K;
 };
 
 __device__ __forceinline__ GtTile gt_decode(const GtParams& prm, long long u) {
@@ -55,23 +70,66 @@ __device__ __forceinline__ GtTile gt_decode(const GtParams& prm, long long u) {
   r.prob = pi;
   r.m0 = (int)(t / p.tiles_n) * 128;
   r.n0 = (int)(t % p.tiles_n) * 256;
-  r.n_valid = min(256, p.N - r.n0);
-  r.n_mma = (r.n_valid + 15) / 16 * 16;
+  r.n_mma = (min(256, p.N - r.n0) + 15) / 16 * 16;
   r.K = p.K;
   return r;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&v);
+// K-major shared-memory descriptor for the NS configuration (SBO = 8 rows).
+template <int NS>
+__device__ __forceinline__ uint64_t gt_desc(uint32_t saddr) {
+  constexpr int ROWB = GtCfg<NS>::ROWB;
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(16 >> 4) << 16;
+  d |= (uint64_t)((8 * ROWB) >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)GtCfg<NS>::SWZ << 61;
+  return d;
 }
 
+// x -> NS bf16 slices (each slice carries the remainder of the previous ones)
+template <int NS>
+__device__ __forceinline__ void split_value(float x, __nv_bfloat16 (&s)[NS]) {
+  float r = x;
+#pragma unroll
+  for (int k = 0; k < NS; ++k) {
+    s[k] = __float2bfloat16_rn(r);
+    r = r - __bfloat162float(s[k]);
+  }
+}
+
+template <int NS>
+__device__ __forceinline__ void split8_store(const float (&x)[8], uint16_t* dst, long long slice_stride) {
+  uint32_t w[NS][4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    __nv_bfloat16 a[NS], b[NS];
+    split_value<NS>(x[2 * e], a);
+    split_value<NS>(x[2 * e + 1], b);
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      __nv_bfloat162 p;
+      p.x = a[k];
+      p.y = b[k];
+      w[k][e] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NS; ++k)
+    *reinterpret_cast<uint4*>(dst + k * slice_stride) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+}
+
+template <int NS>
 __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ GtParams prm) {
+  using Lay = GtLayout<NS>;
+  constexpr int STAGES = GtCfg<NS>::STAGES;
+  constexpr int BK = Lay::BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGtStages * kGtStageBytes);
-  uint64_t* empty = full + kGtStages;
-  uint64_t* acc_full = empty + kGtStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Lay::STAGE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -79,7 +137,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGtStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -104,16 +162,17 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         const GtTile tl = gt_decode(prm, u);
         const CUtensorMap* ma = &prm.mapA[tl.prob];
         const CUtensorMap* mb = &prm.mapB[tl.prob];
-        const int nk = (tl.K + kGtBK - 1) / kGtBK;
+        const int nk = (tl.K + BK - 1) / BK;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
-          uint8_t* s0 = smem + stage * kGtStageBytes;
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)kGtStageBytes);
-          tma_load_3d(s0, ma, kb * kGtBK, tl.m0, 0, &full[stage]);
-          tma_load_3d(s0 + kGtABytes, ma, kb * kGtBK, tl.m0, 1, &full[stage]);
-          tma_load_3d(s0 + 2 * kGtABytes, mb, kb * kGtBK, tl.n0, 0, &full[stage]);
-          tma_load_3d(s0 + 2 * kGtABytes + kGtBBytes, mb, kb * kGtBK, tl.n0, 1, &full[stage]);
-          if (++stage == kGtStages) {
+          uint8_t* s0 = smem + stage * Lay::STAGE;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)Lay::STAGE);
+#pragma unroll
+          for (int s = 0; s < NS; ++s) {
+            tma_load_3d(s0 + s * Lay::A, ma, kb * BK, tl.m0, s, &full[stage]);
+            tma_load_3d(s0 + NS * Lay::A + s * Lay::B, mb, kb * BK, tl.n0, s, &full[stage]);
+          }
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
@@ -127,7 +186,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       for (long long u = blockIdx.x; u < prm.total_tiles && ok; u += gridDim.x) {
         const GtTile tl = gt_decode(prm, u);
         const uint32_t idesc = idesc_bf16_f32(tl.n_mma, false, false);
-        const int nk = (tl.K + kGtBK - 1) / kGtBK;
+        const int nk = (tl.K + BK - 1) / BK;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * 256;
@@ -137,25 +196,29 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             break;
           }
           tc_fence_after();
-          const uint32_t a_hi = smem_u32(smem + stage * kGtStageBytes);
-          const uint32_t a_lo = a_hi + kGtABytes;
-          const uint32_t b_hi = a_hi + 2 * kGtABytes;
-          const uint32_t b_lo = b_hi + kGtBBytes;
+          const uint32_t a0 = smem_u32(smem + stage * Lay::STAGE);
+          const uint32_t b0 = a0 + NS * Lay::A;
 #pragma unroll
-          for (int kk = 0; kk < kGtBK / 16; ++kk) {
-            // K-major, 128-byte swizzle: 16 values of k = 32 bytes along the row;
-            // 8-row groups are 1024 bytes apart.
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // 16 values of k = 32 bytes along the swizzled row
             const uint32_t off = kk * 32;
-            const uint64_t dah = smem_desc_sw128(a_hi + off, 16, 1024);
-            const uint64_t dal = smem_desc_sw128(a_lo + off, 16, 1024);
-            const uint64_t dbh = smem_desc_sw128(b_hi + off, 16, 1024);
-            const uint64_t dbl = smem_desc_sw128(b_lo + off, 16, 1024);
-            tc_mma_bf16(d_tmem, dah, dbh, idesc, (kb | kk) != 0);
-            tc_mma_bf16(d_tmem, dah, dbl, idesc, 1u);
-            tc_mma_bf16(d_tmem, dal, dbh, idesc, 1u);
+            uint64_t da[NS], db[NS];
+#pragma unroll
+            for (int s = 0; s < NS; ++s) {
+              da[s] = gt_desc<NS>(a0 + s * Lay::A + off);
+              db[s] = gt_desc<NS>(b0 + s * Lay::B + off);
+            }
+            tc_mma_bf16(d_tmem, da[0], db[0], idesc, (kb | kk) != 0);
+            tc_mma_bf16(d_tmem, da[0], db[1], idesc, 1u);
+            tc_mma_bf16(d_tmem, da[1], db[0], idesc, 1u);
+            if constexpr (NS == 3) {
+              tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
+              tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
+              tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
+            }
           }
           tc_commit(&empty[stage]);
-          if (++stage == kGtStages) {
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
@@ -177,7 +240,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) break;
       tc_fence_after();
       const int r = tl.m0 + q * 32 + lane;
-      const int nchunk = tl.n_mma / 32 + ((tl.n_mma % 32) ? 1 : 0);
+      const int nchunk = (tl.n_mma + 31) / 32;
       for (int c = 0; c < nchunk; ++c) {
         uint32_t v[32];
         tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
@@ -199,30 +262,22 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
               if (col0 + t < pr.N) dst[t] = o[t];
           }
         } else {
-          uint16_t* hi = static_cast<uint16_t*>(pr.out) + (long long)r * pr.ldc + col0;
-          uint16_t* lo = hi + pr.out_slice_stride;
+          uint16_t* dst = static_cast<uint16_t*>(pr.out) + (long long)r * pr.ldc + col0;
           if (fullc) {
 #pragma unroll
             for (int t = 0; t < 32; t += 8) {
-              uint32_t h[4], l[4];
+              float x8[8];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float x0 = o[t + 2 * e], x1 = o[t + 2 * e + 1];
-                const __nv_bfloat162 hb = __floats2bfloat162_rn(x0, x1);
-                const float2 hf = __bfloat1622float2(hb);
-                h[e] = *reinterpret_cast<const uint32_t*>(&hb);
-                l[e] = pack_bf16x2(x0 - hf.x, x1 - hf.y);
-              }
-              *reinterpret_cast<uint4*>(hi + t) = make_uint4(h[0], h[1], h[2], h[3]);
-              *reinterpret_cast<uint4*>(lo + t) = make_uint4(l[0], l[1], l[2], l[3]);
+              for (int e = 0; e < 8; ++e) x8[e] = o[t + e];
+              split8_store<NS>(x8, dst + t, pr.out_slice_stride);
             }
           } else {
             for (int t = 0; t < 32; ++t)
               if (col0 + t < pr.N) {
-                const __nv_bfloat16 hb = __float2bfloat16_rn(o[t]);
-                const __nv_bfloat16 lb = __float2bfloat16_rn(o[t] - __bfloat162float(hb));
-                hi[t] = *reinterpret_cast<const uint16_t*>(&hb);
-                lo[t] = *reinterpret_cast<const uint16_t*>(&lb);
+                __nv_bfloat16 s[NS];
+                split_value<NS>(o[t], s);
+#pragma unroll
+                for (int k = 0; k < NS; ++k) dst[t + k * pr.out_slice_stride] = *reinterpret_cast<uint16_t*>(&s[k]);
               }
           }
         }
@@ -241,7 +296,8 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
   }
 }
 
-// ------------------------------------------------------------------ fp32 -> (hi, lo) bf16 slices
+// ------------------------------------------------------------------ fp32 -> bf16 slices
+template <int NS>
 __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitParams prm) {
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nth = (long long)gridDim.x * blockDim.x;
@@ -265,17 +321,7 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = (c0 + e < it.cols) ? src[e] : 0.f;
     }
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-      const float2 hf = __bfloat1622float2(hb);
-      h[e] = *reinterpret_cast<const uint32_t*>(&hb);
-      l[e] = pack_bf16x2(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
-    }
-    uint16_t* dst = it.dst + r * it.ld_dst + c0;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(dst + it.slice_stride) = make_uint4(l[0], l[1], l[2], l[3]);
+    split8_store<NS>(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
   }
 }
 
@@ -297,19 +343,22 @@ static EncodeTiledFn gt_encode_fn() {
   return fn;
 }
 
-// Slices of one operand: [2][rows][ld] bf16, K = inner extent, box rows = box_rows.
-static bool encode_slices(EncodeTiledFn enc, CUtensorMap* map, const uint16_t* base, long long rows, long long K,
-                          long long ld, int box_rows) {
-  cuuint64_t gdim[3] = {(cuuint64_t)K, (cuuint64_t)rows, 2};
+// Slices of one operand: [NS][rows][ld] bf16, K = inner extent.
+static bool encode_slices(EncodeTiledFn enc, int NS, CUtensorMap* map, const uint16_t* base, long long rows,
+                          long long K, long long ld, int box_rows) {
+  const int bk = NS == 3 ? GtCfg<3>::BK : GtCfg<2>::BK;
+  cuuint64_t gdim[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)NS};
   cuuint64_t gstride[2] = {(cuuint64_t)ld * 2, (cuuint64_t)(rows * ld * 2)};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t box[3] = {(cuuint32_t)bk, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz = NS == 3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), gdim, gstride, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int launch_split(const SplitItem* items, int n, cudaStream_t stream) {
+int launch_split(const SplitItem* items, int n, int NS, cudaStream_t stream) {
+  if (NS != 2 && NS != 3) return KFAC_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
@@ -327,44 +376,52 @@ int launch_split(const SplitItem* items, int n, cudaStream_t stream) {
     prm.total_items = total;
     if (total == 0) continue;
     const long long want = (total + 255) / 256, cap = (long long)sms * 16;
-    split_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(prm);
+    const unsigned grid = (unsigned)(want < cap ? want : cap);
+    if (NS == 3)
+      split_kernel<3><<<grid, 256, 0, stream>>>(prm);
+    else
+      split_kernel<2><<<grid, 256, 0, stream>>>(prm);
     count_launch();
     if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
   }
   return KFAC_OK;
 }
 
-int launch_gemm_tc(const GtOperand* ops_in, int n, cudaStream_t stream) {
+int launch_gemm_tc(const GtOperand* ops_in, int n, int NS, cudaStream_t stream) {
   // longest K first: tiles are dealt round-robin to a persistent grid
   GtOperand* ops = new GtOperand[n > 0 ? n : 1];
   std::copy(ops_in, ops_in + n, ops);
   std::stable_sort(ops, ops + n, [](const GtOperand& x, const GtOperand& y) { return x.K > y.K; });
-  const int rc = launch_gemm_tc_sorted(ops, n, stream);
+  const int rc = launch_gemm_tc_sorted(ops, n, NS, stream);
   delete[] ops;
   return rc;
 }
 
-int launch_gemm_tc_sorted(const GtOperand* ops, int n, cudaStream_t stream) {
+int launch_gemm_tc_sorted(const GtOperand* ops, int n, int NS, cudaStream_t stream) {
+  if (NS != 2 && NS != 3) return KFAC_ERR_INVALID_ARG;
   EncodeTiledFn enc = gt_encode_fn();
   if (!enc) return KFAC_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return KFAC_ERR_CUDA;
-  if (!ensure_smem_attr(dev, (const void*)gemm_tc_kernel, kGtSmem)) return KFAC_ERR_CUDA;
+  const void* fn = NS == 3 ? (const void*)gemm_tc_kernel<3> : (const void*)gemm_tc_kernel<2>;
+  const int smem = NS == 3 ? GtLayout<3>::SMEM : GtLayout<2>::SMEM;
+  if (!ensure_smem_attr(dev, fn, smem)) return KFAC_ERR_CUDA;
   int* status = device_status_ptr();
   if (!status) return KFAC_ERR_CUDA;
-  for (int base = 0; base < n; base += kGtMaxProbs) {
+  GtParams* prm = new GtParams;
+  int rc = KFAC_OK;
+  for (int base = 0; base < n && rc == KFAC_OK; base += kGtMaxProbs) {
     const int cnt = n - base < kGtMaxProbs ? n - base : kGtMaxProbs;
-    GtParams* prm = new GtParams;
     memset(prm, 0, sizeof(GtParams));
     long long tiles = 0;
-    for (int i = 0; i < cnt; ++i) {
+    for (int i = 0; i < cnt && rc == KFAC_OK; ++i) {
       const GtOperand& o = ops[base + i];
-      if (!encode_slices(enc, &prm->mapA[i], o.a, o.M, o.K, o.lda, 128) ||
-          !encode_slices(enc, &prm->mapB[i], o.b, o.N, o.K, o.ldb, 256)) {
-        delete prm;
-        return KFAC_ERR_INVALID_ARG;
+      if (!encode_slices(enc, NS, &prm->mapA[i], o.a, o.M, o.K, o.lda, 128) ||
+          !encode_slices(enc, NS, &prm->mapB[i], o.b, o.N, o.K, o.ldb, 256)) {
+        rc = KFAC_ERR_INVALID_ARG;
+        break;
       }
       GtProb& p = prm->probs[i];
       p.out = o.out;
@@ -379,18 +436,22 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, cudaStream_t stream) {
       p.tile_begin = tiles;
       tiles += (long long)((o.M + 127) / 128) * p.tiles_n;
     }
+    if (rc != KFAC_OK) break;
     prm->n_probs = cnt;
     prm->total_tiles = tiles;
     prm->status = status;
     if (tiles > 0) {
       const int grid = (int)(tiles < sms ? tiles : sms);
-      gemm_tc_kernel<<<grid, 192, kGtSmem, stream>>>(*prm);
+      if (NS == 3)
+        gemm_tc_kernel<3><<<grid, 192, smem, stream>>>(*prm);
+      else
+        gemm_tc_kernel<2><<<grid, 192, smem, stream>>>(*prm);
       count_launch();
+      if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
     }
-    delete prm;
-    if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
   }
-  return KFAC_OK;
+  delete prm;
+  return rc;
 }
 
 }  // namespace kfac

@@ -153,6 +153,11 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
   }
   __syncthreads();
   const int lx = threadIdx.x % 32, ly = threadIdx.x / 32;  // 32 x 8
+  double wcol[4][kProbes];  // partial w for column bn + lx, one per column block bn
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) wcol[q4][p] = 0.0;
   for (int sb = 0; sb < 16; ++sb) {
     const int bm = (sb / 4) * 32, bn = (sb % 4) * 32;  // sub-block rows (mm) / cols (nn) of the L tile
     // read D[C*128 + bn + y][R*128 + bm + x] (coalesced along x), store sub[y][x]
@@ -165,11 +170,16 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
     }
     __syncthreads();
     // write L[R*128 + bm + y][C*128 + bn + x] = sub[x][y]
+    const long long gc = (long long)C * 128 + bn + lx;
+    double vc[kProbes];
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) vc[p] = probe_sign(gc, p);
     for (int y = ly; y < 32; y += 8) {
       const long long gr = (long long)R * 128 + bm + y;
-      const long long gc = (long long)C * 128 + bn + lx;
       float v = sub[lx][y];
       T out;
+      double x = 0.0;  // contribution of this stored element to w = D v
+      bool inside = false;
       if (gr >= m.d || gc >= m.d) {
         out = (gr == gc) ? T(1) : T(0);
       } else if (gr < gc) {
@@ -177,20 +187,33 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
       } else {
         out = (T)v;
         if (gr == gc) out += (T)c.gamma_extra;
-        if (c.want_rowsum) {
-          const float a = fabsf(v);
-          atomicAdd(&rs_row[bm + y], a);
-          if (gr != gc) atomicAdd(&rs_col[bn + lx], a);
-          const double x = (double)out;  // the matrix being inverted, as stored
-#pragma unroll
-          for (int p = 0; p < kProbes; ++p) {
-            atomicAdd(&pw_row[p][bm + y], x * probe_sign(gc, p));
-            if (gr != gc) atomicAdd(&pw_col[p][bn + lx], x * probe_sign(gr, p));
-          }
-        }
+        x = (double)out;  // the matrix being inverted, as stored
+        inside = true;
       }
       L[gr * np + gc] = out;
+      if (c.want_rowsum) {  // uniform over the block
+        const float a = inside ? fabsf(v) : 0.f;
+        float ra = a;
+        for (int o = 16; o > 0; o >>= 1) ra += __shfl_xor_sync(0xffffffffu, ra, o);
+        if (lx == 0) rs_row[bm + y] += ra;  // row bm + y belongs to this warp alone
+#pragma unroll
+        for (int p = 0; p < kProbes; ++p) {
+          double s = x * vc[p];
+          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          if (lx == 0) pw_row[p][bm + y] += s;
+          if (inside && gr != gc) wcol[bn / 32][p] += x * probe_sign(gr, p);
+        }
+        if (inside && gr != gc) atomicAdd(&rs_col[bn + lx], a);
+      }
     }
+    __syncthreads();
+  }
+  if (c.want_rowsum) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p)
+        if (wcol[q4][p] != 0.0) atomicAdd(&pw_col[p][q4 * 32 + lx], wcol[q4][p]);
     __syncthreads();
   }
   if (c.want_rowsum && threadIdx.x < 128) {
@@ -419,17 +442,23 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
     __syncthreads();
   }
   float sq = 0.f;  // this thread's share of ||X||_F^2
+  double ycol[8][kProbes];  // this thread's partial y for its 8 columns
+#pragma unroll
+  for (int b = 0; b < 8; ++b)
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) ycol[b][p] = 0.0;
 #pragma unroll
   for (int a = 0; a < 8; ++a) {
     const int mm = ty * 8 + a;
     const long long row = (long long)i * 128 + mm;
-    if (row >= m.d) continue;
+    double yrow[kProbes];
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) yrow[p] = 0.0;
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       const int nn = tx * 8 + b;
       const long long col = (long long)j * 128 + nn;
-      if (col >= m.d) continue;
-      if (i == j && mm > nn) continue;
+      if (row >= m.d || col >= m.d || (i == j && mm > nn)) continue;
       const float v = (float)acc[a][b];
       m.X[row * m.ld_out + col] = v;
       m.X[col * m.ld_out + row] = v;
@@ -439,13 +468,27 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
         const double x = (double)v;
 #pragma unroll
         for (int p = 0; p < kProbes; ++p) {
-          atomicAdd(&py_row[p][mm], x * w[p * np + col]);
-          if (row != col) atomicAdd(&py_col[p][nn], x * w[p * np + row]);
+          yrow[p] += x * w[p * np + col];
+          if (row != col) ycol[b][p] += x * w[p * np + row];
         }
+      }
+    }
+    if (probe) {
+      // the 16 threads of a row (same ty) are 16 consecutive lanes of one warp
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p) {
+        double s = yrow[p];
+        for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (tx == 0) py_row[p][mm] = s;
       }
     }
   }
   if (probe) {
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p)
+        if (ycol[b][p] != 0.0) atomicAdd(&py_col[p][tx * 8 + b], ycol[b][p]);
     for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
     if ((threadIdx.x & 31) == 0) atomicAdd(&c.st[mi].xnorm2, sq);
     __syncthreads();

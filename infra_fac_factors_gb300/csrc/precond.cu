@@ -1,12 +1,13 @@
 // Preconditioned gradient of each layer (SPD-KFAC §II-B, the damped update
 // rule):  out = inv_g * grad * inv_a, on tcgen05 tensor cores.
 //
-// The fp32 operands are carried as split-bf16 pairs (x = hi + lo, three
-// products per multiply-add; gemm_tc.cu), which keeps ~2^-16 relative error per
-// product: plain bf16 operands would not do, because grad lies in the row
-// space of the layer input while inv_a amplifies the other directions by up to
-// 1/gamma, magnifying operand rounding.
-//   1. split      grad, inv_a, inv_g -> bf16 (hi, lo) slices   (one launch)
+// The fp32 operands are carried as three bf16 slices (x = hi + mid + lo, all 24
+// bits of fp32; six products per multiply-add, gemm_tc.cu).  Fewer bits do not
+// do: grad lies in the row space of the layer input while inv_a has gain up to
+// 1/gamma on the other directions, so the rounding of either operand is
+// amplified ~1/gamma-fold (two slices, 16 bits, gave 1e-2 relative error on the
+// first steps of the MLP workload, where 529 of 785 directions have gain 1000).
+//   1. split      grad, inv_a, inv_g -> bf16 slices               (one launch)
 //   2. GEMM 1     tmp^T = inv_a * grad^T   (d_in x d_out), written as slices
 //   3. GEMM 2     out   = inv_g * tmp      (= inv_g * (tmp^T)^T), fp32
 // inv_a and inv_g are symmetric, so their rows serve as the K-major operands.
@@ -16,6 +17,8 @@
 
 namespace kfac {
 
+constexpr int kPcSlices = 3;
+
 static long long pad8(long long v) { return (v + 7) / 8 * 8; }
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -23,17 +26,18 @@ struct PcLayout {
   size_t grad, inv_a, inv_g, tmp, end;
 };
 
-// Workspace of layer i starting at byte `off`: four bf16 slice pairs.
+// Workspace of layer i starting at byte `off`: four sliced operands.
 static PcLayout pc_layout(const kfac_precond_args& a, size_t off) {
+  const size_t s = kPcSlices * sizeof(uint16_t);
   PcLayout L;
   L.grad = off;
-  off += align256(2 * a.d_out * pad8(a.d_in) * sizeof(uint16_t));
+  off += align256(s * a.d_out * pad8(a.d_in));
   L.inv_a = off;
-  off += align256(2 * a.d_in * pad8(a.d_in) * sizeof(uint16_t));
+  off += align256(s * a.d_in * pad8(a.d_in));
   L.inv_g = off;
-  off += align256(2 * a.d_out * pad8(a.d_out) * sizeof(uint16_t));
+  off += align256(s * a.d_out * pad8(a.d_out));
   L.tmp = off;
-  off += align256(2 * a.d_in * pad8(a.d_out) * sizeof(uint16_t));
+  off += align256(s * a.d_in * pad8(a.d_out));
   L.end = off;
   return L;
 }
@@ -69,9 +73,9 @@ int launch_precondition(int n, const kfac_precond_args* args, void* workspace, s
     // out[m][n] = sum_k inv_g[m][k] tmp^T[n][k]: M = d_out, N = d_in, K = d_out
     g2[i] = GtOperand{s_ig, s_tmp, a.d_out, a.d_in, a.d_out, ldo, ldo, a.out, a.ld_out, 0, 0, 1.0f};
   }
-  int rc = launch_split(items, 3 * n, stream);
-  if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, stream);
-  if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, stream);
+  int rc = launch_split(items, 3 * n, kPcSlices, stream);
+  if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, kPcSlices, stream);
+  if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, kPcSlices, stream);
   delete[] items;
   delete[] g1;
   delete[] g2;

@@ -158,8 +158,8 @@ def pa(**kw):
 
 def test_precondition_rejects_invalid():
     ws = capi.kfac_precondition_workspace([pa()])
-    # four (hi, lo) bf16 slice pairs: grad 8x16, inv_a 12x16, inv_g 8x8, tmp^T 12x8, each 256-B aligned
-    assert ws == 512 + 768 + 256 + 512
+    # four operands as three bf16 slices: grad 8x16, inv_a 12x16, inv_g 8x8, tmp^T 12x8, each 256-B aligned
+    assert ws == 768 + 1280 + 512 + 768
     for bad in (pa(d_in=0), pa(ld_g=4), pa(ld_grad=10), pa(out=A16 * 2), pa(inv_a=A16 + 4)):
         assert capi.kfac_precondition_workspace([bad]) == 0
         assert capi.kfac_precondition([bad], A16 * 5, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
