@@ -223,13 +223,28 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
           // of row t lands at chunk j ^ (t & 7), conflict-free) and write it with
           // a TMA store; later K-chunks of the same unit add with a TMA reduce.
           if (!first && lane == 0) bulk_wait<0>();  // earlier writes of this unit are done
+          __syncwarp();
           const int r0 = un.i * 128 + q * 32;
+          // TMA writes whole 16-byte groups at the inner edge: a chunk reaching
+          // past the last full group (d rounded down to 4) is stored directly.
+          const long long d4 = (long long)(pr.d / 4) * 4;
           for (int c = 0; c < nb * 2; ++c) {
             uint32_t v[32];
             tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
             tc_wait_ld();
             const long long col0 = un.j0 + c * 32;
             if (col0 >= jend || r0 >= pr.d) continue;  // uniform over the warp
+            if (col0 + 32 > d4 && d4 != pr.d) {
+              if (r < pr.d)
+                for (int t = 0; t < 32; ++t) {
+                  const long long col = col0 + t;
+                  if (col >= jend) break;
+                  float o = __uint_as_float(v[t]) * pr.scale;
+                  if (!first) o += orow[col];
+                  orow[col] = o;
+                }
+              continue;
+            }
             uint8_t* buf = out_stage + (q * 2 + obuf) * kSyStageOut;
             if (lane == 0) bulk_wait_read<1>();  // the store that last used `buf` has read it
             __syncwarp();

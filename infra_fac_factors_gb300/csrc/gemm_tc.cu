@@ -2,21 +2,26 @@
 //
 //     C[m, n] = alpha * sum_k A[m, k] B[n, k]        (A: M x K, B: N x K)
 //
-// Every fp32 operand x is carried as NS bf16 slices whose sum is x:
-//   NS = 2: x = hi + lo (16 significant bits); products hi*hi + hi*lo + lo*hi;
-//   NS = 3: x = hi + mid + lo (24 bits, all of fp32); products hi*hi + hi*mid +
-//           mid*hi + hi*lo + lo*hi + mid*mid (the dropped terms are below 2^-24
-//           of the product).
-// All products of a tile go into one fp32 TMEM accumulator.  The slices of an
-// operand are the z-planes of one row-major buffer [NS][rows][ld], read by TMA
-// K-major with a swizzle as wide as one stage row (NS = 2: 64 values of k,
-// 128-byte swizzle; NS = 3: 32 values of k, 64-byte swizzle, so that three
-// stages of all six tiles fit in shared memory).
+// Every fp32 operand x is carried as three bf16 slices x = hi + mid + lo (all
+// 24 bits of fp32), and each 16-wide k-step issues six MMAs: hi*hi + hi*mid +
+// mid*hi + hi*lo + lo*hi + mid*mid (the dropped terms are below 2^-24 of the
+// product).  The slices of an operand are the z-planes of one row-major
+// buffer [3][rows][ld], read by TMA K-major (32 values of k per stage row,
+// 64-byte swizzle, three stages of all six tiles in shared memory).
 //
-// Kernel roles (192 threads, one CTA per SM, persistent over 128 x 256 tiles):
+// Accumulation.  The products the K-FAC step multiplies cancel heavily (the
+// preconditioner has gain up to 1/gamma on directions the gradient does not
+// occupy: |grad| |inv_a| can be 6e3 times |grad inv_a|).  The tensor-core
+// accumulator does not round to nearest, and its error grows with the number
+// of accumulations, so each k-step goes to a fresh TMEM accumulator (two,
+// ping-pong) and the epilogue warps add it into fp32 registers with
+// round-to-nearest: the result has the accuracy of an fp32 FMA loop.
+//
+// Kernel roles (320 threads, one CTA per SM, persistent over 128 x 256 tiles):
 //   warp 0: TMA producer; warp 1: TMEM allocation + MMA issuer;
-//   warps 2-5: epilogue (fp32 C, or C split again into NS bf16 slices so one
-//   GEMM feeds the next directly).
+//   warps 2-9: epilogue; warp w reads TMEM lanes 32*(w%4).. and columns
+//   128*((w-2)/4) .. +127 of the tile.  The epilogue writes fp32 C, or C split
+//   again into three bf16 slices so one GEMM feeds the next directly.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -29,24 +34,15 @@
 
 namespace kfac {
 
-template <int NS>
-struct GtCfg;
-template <>
-struct GtCfg<2> {
-  static constexpr int BK = 64, STAGES = 2, SWZ = 2 /*128 B*/, ROWB = 128, NPROD = 3;
-};
-template <>
-struct GtCfg<3> {
-  static constexpr int BK = 32, STAGES = 3, SWZ = 4 /*64 B*/, ROWB = 64, NPROD = 6;
-};
-template <int NS>
-struct GtLayout {
-  static constexpr int BK = GtCfg<NS>::BK;
-  static constexpr int A = 128 * BK * 2;  // one slice of the A tile
-  static constexpr int B = 256 * BK * 2;  // one slice of the B tile
-  static constexpr int STAGE = NS * (A + B);
-  static constexpr int SMEM = GtCfg<NS>::STAGES * STAGE + 1024 + 256;
-};
+constexpr int kGtBK = 32;
+constexpr int kGtStages = 3;
+constexpr int kGtNS = 3;
+constexpr int kGtA = 128 * kGtBK * 2;  // one slice of the A tile (8 KB)
+constexpr int kGtB = 256 * kGtBK * 2;  // one slice of the B tile (16 KB)
+constexpr int kGtStage = kGtNS * (kGtA + kGtB);
+constexpr int kGtSmem = kGtStages * kGtStage + 1024 + 256;
+constexpr int kGtThreads = 320;
+constexpr int kGtEpiWarps = 8;
 
 struct GtParams {
   CUtensorMap mapA[kGtMaxProbs];
@@ -75,40 +71,37 @@ __device__ __forceinline__ GtTile gt_decode(const GtParams& prm, long long u) {
   return r;
 }
 
-// K-major shared-memory descriptor for the NS configuration (SBO = 8 rows).
-template <int NS>
+// K-major shared-memory descriptor, 64-byte swizzle: rows of 64 B, 8-row
+// groups 512 B apart (layout type 4 at bits 61..63).
 __device__ __forceinline__ uint64_t gt_desc(uint32_t saddr) {
-  constexpr int ROWB = GtCfg<NS>::ROWB;
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
   d |= (uint64_t)(16 >> 4) << 16;
-  d |= (uint64_t)((8 * ROWB) >> 4) << 32;
+  d |= (uint64_t)(512 >> 4) << 32;
   d |= (uint64_t)1 << 46;
-  d |= (uint64_t)GtCfg<NS>::SWZ << 61;
+  d |= (uint64_t)4 << 61;
   return d;
 }
 
-// x -> NS bf16 slices (each slice carries the remainder of the previous ones)
-template <int NS>
-__device__ __forceinline__ void split_value(float x, __nv_bfloat16 (&s)[NS]) {
+// x -> three bf16 slices, each carrying the remainder of the previous ones
+__device__ __forceinline__ void split_value(float x, __nv_bfloat16 (&s)[kGtNS]) {
   float r = x;
 #pragma unroll
-  for (int k = 0; k < NS; ++k) {
+  for (int k = 0; k < kGtNS; ++k) {
     s[k] = __float2bfloat16_rn(r);
     r = r - __bfloat162float(s[k]);
   }
 }
 
-template <int NS>
 __device__ __forceinline__ void split8_store(const float (&x)[8], uint16_t* dst, long long slice_stride) {
-  uint32_t w[NS][4];
+  uint32_t w[kGtNS][4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    __nv_bfloat16 a[NS], b[NS];
-    split_value<NS>(x[2 * e], a);
-    split_value<NS>(x[2 * e + 1], b);
+    __nv_bfloat16 a[kGtNS], b[kGtNS];
+    split_value(x[2 * e], a);
+    split_value(x[2 * e + 1], b);
 #pragma unroll
-    for (int k = 0; k < NS; ++k) {
+    for (int k = 0; k < kGtNS; ++k) {
       __nv_bfloat162 p;
       p.x = a[k];
       p.y = b[k];
@@ -116,20 +109,16 @@ __device__ __forceinline__ void split8_store(const float (&x)[8], uint16_t* dst,
     }
   }
 #pragma unroll
-  for (int k = 0; k < NS; ++k)
+  for (int k = 0; k < kGtNS; ++k)
     *reinterpret_cast<uint4*>(dst + k * slice_stride) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
 }
 
-template <int NS>
-__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ GtParams prm) {
-  using Lay = GtLayout<NS>;
-  constexpr int STAGES = GtCfg<NS>::STAGES;
-  constexpr int BK = Lay::BK;
+__global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_constant__ GtParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Lay::STAGE);
-  uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGtStages * kGtStage);
+  uint64_t* empty = full + kGtStages;
+  uint64_t* acc_full = empty + kGtStages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -137,13 +126,13 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < kGtStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
+      mbar_init(&acc_empty[a], kGtEpiWarps);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -162,17 +151,17 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         const GtTile tl = gt_decode(prm, u);
         const CUtensorMap* ma = &prm.mapA[tl.prob];
         const CUtensorMap* mb = &prm.mapB[tl.prob];
-        const int nk = (tl.K + BK - 1) / BK;
+        const int nk = (tl.K + kGtBK - 1) / kGtBK;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
-          uint8_t* s0 = smem + stage * Lay::STAGE;
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)Lay::STAGE);
+          uint8_t* s0 = smem + stage * kGtStage;
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)kGtStage);
 #pragma unroll
-          for (int s = 0; s < NS; ++s) {
-            tma_load_3d(s0 + s * Lay::A, ma, kb * BK, tl.m0, s, &full[stage]);
-            tma_load_3d(s0 + NS * Lay::A + s * Lay::B, mb, kb * BK, tl.n0, s, &full[stage]);
+          for (int s = 0; s < kGtNS; ++s) {
+            tma_load_3d(s0 + s * kGtA, ma, kb * kGtBK, tl.m0, s, &full[stage]);
+            tma_load_3d(s0 + kGtNS * kGtA + s * kGtB, mb, kb * kGtBK, tl.n0, s, &full[stage]);
           }
-          if (++stage == STAGES) {
+          if (++stage == kGtStages) {
             stage = 0;
             phase ^= 1;
           }
@@ -186,107 +175,128 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       for (long long u = blockIdx.x; u < prm.total_tiles && ok; u += gridDim.x) {
         const GtTile tl = gt_decode(prm, u);
         const uint32_t idesc = idesc_bf16_f32(tl.n_mma, false, false);
-        const int nk = (tl.K + BK - 1) / BK;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * 256;
-        for (int kb = 0; kb < nk; ++kb) {
+        const int nk = (tl.K + kGtBK - 1) / kGtBK;
+        for (int kb = 0; kb < nk && ok; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, prm.status)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + stage * Lay::STAGE);
-          const uint32_t b0 = a0 + NS * Lay::A;
+          const uint32_t a0 = smem_u32(smem + stage * kGtStage);
+          const uint32_t b0 = a0 + kGtNS * kGtA;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // 16 values of k = 32 bytes along the swizzled row
-            const uint32_t off = kk * 32;
-            uint64_t da[NS], db[NS];
-#pragma unroll
-            for (int s = 0; s < NS; ++s) {
-              da[s] = gt_desc<NS>(a0 + s * Lay::A + off);
-              db[s] = gt_desc<NS>(b0 + s * Lay::B + off);
+          for (int kk = 0; kk < kGtBK / 16; ++kk) {
+            if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) {
+              ok = false;
+              break;
             }
-            tc_mma_bf16(d_tmem, da[0], db[0], idesc, (kb | kk) != 0);
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * 256;
+            const uint32_t off = kk * 32;  // 16 values of k = 32 bytes along the swizzled row
+            uint64_t da[kGtNS], db[kGtNS];
+#pragma unroll
+            for (int s = 0; s < kGtNS; ++s) {
+              da[s] = gt_desc(a0 + s * kGtA + off);
+              db[s] = gt_desc(b0 + s * kGtB + off);
+            }
+            tc_mma_bf16(d_tmem, da[0], db[0], idesc, 0u);
             tc_mma_bf16(d_tmem, da[0], db[1], idesc, 1u);
             tc_mma_bf16(d_tmem, da[1], db[0], idesc, 1u);
-            if constexpr (NS == 3) {
-              tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
-              tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
-              tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
-            }
+            tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
+            tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
+            tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
+            tc_commit(&acc_full[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
           }
           tc_commit(&empty[stage]);
-          if (++stage == STAGES) {
+          if (++stage == kGtStages) {
             stage = 0;
             phase ^= 1;
           }
         }
-        if (!ok) break;
-        tc_commit(&acc_full[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
       }
       tc_commit(done_bar);
       mbar_wait(done_bar, 0, abort_flag, prm.status);
     }
   } else {
-    const int q = warp & 3;
+    const int e = warp - 2;
+    const int q = warp & 3;           // TMEM lane quarter
+    const int h = e / 4;              // column half of the 256-wide tile
     uint32_t acc = 0, acc_phase = 0;
-    for (long long u = blockIdx.x; u < prm.total_tiles; u += gridDim.x) {
+    bool ok = true;
+    for (long long u = blockIdx.x; u < prm.total_tiles && ok; u += gridDim.x) {
       const GtTile tl = gt_decode(prm, u);
       const GtProb& pr = prm.probs[tl.prob];
-      if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) break;
-      tc_fence_after();
+      const int nsteps = (tl.K + kGtBK - 1) / kGtBK * (kGtBK / 16);
+      float run[128];
+#pragma unroll
+      for (int t = 0; t < 128; ++t) run[t] = 0.f;
+      for (int st = 0; st < nsteps; ++st) {
+        if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + h * 128;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t v[32];
+          tc_ld_32x32b_x32(base + g * 32, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) run[g * 32 + t] += __uint_as_float(v[t]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok) break;
       const int r = tl.m0 + q * 32 + lane;
-      const int nchunk = (tl.n_mma + 31) / 32;
-      for (int c = 0; c < nchunk; ++c) {
-        uint32_t v[32];
-        tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
-        tc_wait_ld();
-        const int col0 = tl.n0 + c * 32;
-        if (r >= pr.M || col0 >= pr.N) continue;
-        const bool fullc = col0 + 32 <= pr.N;
-        float o[32];
+      if (r < pr.M) {
 #pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(v[t]) * pr.alpha;
-        if (!pr.out_split) {
-          float* dst = static_cast<float*>(pr.out) + (long long)r * pr.ldc + col0;
-          if (fullc) {
+        for (int g = 0; g < 4; ++g) {
+          const int col0 = tl.n0 + h * 128 + g * 32;
+          if (col0 >= pr.N) continue;
+          const bool fullc = col0 + 32 <= pr.N;
+          if (!pr.out_split) {
+            float* dst = static_cast<float*>(pr.out) + (long long)r * pr.ldc + col0;
+            if (fullc) {
 #pragma unroll
-            for (int t = 0; t < 32; t += 4)
-              *reinterpret_cast<float4*>(dst + t) = make_float4(o[t], o[t + 1], o[t + 2], o[t + 3]);
-          } else {
-            for (int t = 0; t < 32; ++t)
-              if (col0 + t < pr.N) dst[t] = o[t];
-          }
-        } else {
-          uint16_t* dst = static_cast<uint16_t*>(pr.out) + (long long)r * pr.ldc + col0;
-          if (fullc) {
+              for (int t = 0; t < 32; t += 4)
+                *reinterpret_cast<float4*>(dst + t) =
+                    make_float4(run[g * 32 + t] * pr.alpha, run[g * 32 + t + 1] * pr.alpha,
+                                run[g * 32 + t + 2] * pr.alpha, run[g * 32 + t + 3] * pr.alpha);
+            } else {
 #pragma unroll
-            for (int t = 0; t < 32; t += 8) {
-              float x8[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) x8[e] = o[t + e];
-              split8_store<NS>(x8, dst + t, pr.out_slice_stride);
+              for (int t = 0; t < 32; ++t)
+                if (col0 + t < pr.N) dst[t] = run[g * 32 + t] * pr.alpha;
             }
           } else {
-            for (int t = 0; t < 32; ++t)
-              if (col0 + t < pr.N) {
-                __nv_bfloat16 s[NS];
-                split_value<NS>(o[t], s);
+            uint16_t* dst = static_cast<uint16_t*>(pr.out) + (long long)r * pr.ldc + col0;
+            if (fullc) {
 #pragma unroll
-                for (int k = 0; k < NS; ++k) dst[t + k * pr.out_slice_stride] = *reinterpret_cast<uint16_t*>(&s[k]);
+              for (int t = 0; t < 32; t += 8) {
+                float x8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x8[k] = run[g * 32 + t + k] * pr.alpha;
+                split8_store(x8, dst + t, pr.out_slice_stride);
               }
+            } else {
+#pragma unroll
+              for (int t = 0; t < 32; ++t)
+                if (col0 + t < pr.N) {
+                  __nv_bfloat16 s[kGtNS];
+                  split_value(run[g * 32 + t] * pr.alpha, s);
+#pragma unroll
+                  for (int k = 0; k < kGtNS; ++k)
+                    dst[t + k * pr.out_slice_stride] = *reinterpret_cast<uint16_t*>(&s[k]);
+                }
+            }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
     }
   }
   __syncthreads();
@@ -297,7 +307,6 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
 }
 
 // ------------------------------------------------------------------ fp32 -> bf16 slices
-template <int NS>
 __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitParams prm) {
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nth = (long long)gridDim.x * blockDim.x;
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = (c0 + e < it.cols) ? src[e] : 0.f;
     }
-    split8_store<NS>(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
+    split8_store(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
   }
 }
 
@@ -343,22 +352,19 @@ static EncodeTiledFn gt_encode_fn() {
   return fn;
 }
 
-// Slices of one operand: [NS][rows][ld] bf16, K = inner extent.
-static bool encode_slices(EncodeTiledFn enc, int NS, CUtensorMap* map, const uint16_t* base, long long rows,
-                          long long K, long long ld, int box_rows) {
-  const int bk = NS == 3 ? GtCfg<3>::BK : GtCfg<2>::BK;
-  cuuint64_t gdim[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)NS};
+// Slices of one operand: [3][rows][ld] bf16, K = inner extent.
+static bool encode_slices(EncodeTiledFn enc, CUtensorMap* map, const uint16_t* base, long long rows, long long K,
+                          long long ld, int box_rows) {
+  cuuint64_t gdim[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)kGtNS};
   cuuint64_t gstride[2] = {(cuuint64_t)ld * 2, (cuuint64_t)(rows * ld * 2)};
-  cuuint32_t box[3] = {(cuuint32_t)bk, (cuuint32_t)box_rows, 1};
+  cuuint32_t box[3] = {(cuuint32_t)kGtBK, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapSwizzle swz = NS == 3 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), gdim, gstride, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int launch_split(const SplitItem* items, int n, int NS, cudaStream_t stream) {
-  if (NS != 2 && NS != 3) return KFAC_ERR_INVALID_ARG;
+int launch_split(const SplitItem* items, int n, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
@@ -376,38 +382,31 @@ int launch_split(const SplitItem* items, int n, int NS, cudaStream_t stream) {
     prm.total_items = total;
     if (total == 0) continue;
     const long long want = (total + 255) / 256, cap = (long long)sms * 16;
-    const unsigned grid = (unsigned)(want < cap ? want : cap);
-    if (NS == 3)
-      split_kernel<3><<<grid, 256, 0, stream>>>(prm);
-    else
-      split_kernel<2><<<grid, 256, 0, stream>>>(prm);
+    split_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(prm);
     count_launch();
     if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
   }
   return KFAC_OK;
 }
 
-int launch_gemm_tc(const GtOperand* ops_in, int n, int NS, cudaStream_t stream) {
+int launch_gemm_tc(const GtOperand* ops_in, int n, cudaStream_t stream) {
   // longest K first: tiles are dealt round-robin to a persistent grid
   GtOperand* ops = new GtOperand[n > 0 ? n : 1];
   std::copy(ops_in, ops_in + n, ops);
   std::stable_sort(ops, ops + n, [](const GtOperand& x, const GtOperand& y) { return x.K > y.K; });
-  const int rc = launch_gemm_tc_sorted(ops, n, NS, stream);
+  const int rc = launch_gemm_tc_sorted(ops, n, stream);
   delete[] ops;
   return rc;
 }
 
-int launch_gemm_tc_sorted(const GtOperand* ops, int n, int NS, cudaStream_t stream) {
-  if (NS != 2 && NS != 3) return KFAC_ERR_INVALID_ARG;
+int launch_gemm_tc_sorted(const GtOperand* ops, int n, cudaStream_t stream) {
   EncodeTiledFn enc = gt_encode_fn();
   if (!enc) return KFAC_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return KFAC_ERR_CUDA;
-  const void* fn = NS == 3 ? (const void*)gemm_tc_kernel<3> : (const void*)gemm_tc_kernel<2>;
-  const int smem = NS == 3 ? GtLayout<3>::SMEM : GtLayout<2>::SMEM;
-  if (!ensure_smem_attr(dev, fn, smem)) return KFAC_ERR_CUDA;
+  if (!ensure_smem_attr(dev, (const void*)gemm_tc_kernel, kGtSmem)) return KFAC_ERR_CUDA;
   int* status = device_status_ptr();
   if (!status) return KFAC_ERR_CUDA;
   GtParams* prm = new GtParams;
@@ -418,8 +417,8 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, int NS, cudaStream_t stre
     long long tiles = 0;
     for (int i = 0; i < cnt && rc == KFAC_OK; ++i) {
       const GtOperand& o = ops[base + i];
-      if (!encode_slices(enc, NS, &prm->mapA[i], o.a, o.M, o.K, o.lda, 128) ||
-          !encode_slices(enc, NS, &prm->mapB[i], o.b, o.N, o.K, o.ldb, 256)) {
+      if (!encode_slices(enc, &prm->mapA[i], o.a, o.M, o.K, o.lda, 128) ||
+          !encode_slices(enc, &prm->mapB[i], o.b, o.N, o.K, o.ldb, 256)) {
         rc = KFAC_ERR_INVALID_ARG;
         break;
       }
@@ -442,10 +441,7 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, int NS, cudaStream_t stre
     prm->status = status;
     if (tiles > 0) {
       const int grid = (int)(tiles < sms ? tiles : sms);
-      if (NS == 3)
-        gemm_tc_kernel<3><<<grid, 192, smem, stream>>>(*prm);
-      else
-        gemm_tc_kernel<2><<<grid, 192, smem, stream>>>(*prm);
+      gemm_tc_kernel<<<grid, kGtThreads, kGtSmem, stream>>>(*prm);
       count_launch();
       if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
     }

@@ -38,9 +38,9 @@ struct SplitParams {
   int n;
 };
 
-// NS = 2 or 3 bf16 slices per fp32 value (see gemm_tc.cu).
-int launch_split(const SplitItem* items, int n, int NS, cudaStream_t stream);
-int launch_gemm_tc(const GtOperand* ops, int n, int NS, cudaStream_t stream);         // sorts by K
-int launch_gemm_tc_sorted(const GtOperand* ops, int n, int NS, cudaStream_t stream);  // as given
+// Three bf16 slices per fp32 value (see gemm_tc.cu).
+int launch_split(const SplitItem* items, int n, cudaStream_t stream);
+int launch_gemm_tc(const GtOperand* ops, int n, cudaStream_t stream);         // sorts by K
+int launch_gemm_tc_sorted(const GtOperand* ops, int n, cudaStream_t stream);  // as given
 
 }  // namespace kfac

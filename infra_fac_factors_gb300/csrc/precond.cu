@@ -2,11 +2,13 @@
 // rule):  out = inv_g * grad * inv_a, on tcgen05 tensor cores.
 //
 // The fp32 operands are carried as three bf16 slices (x = hi + mid + lo, all 24
-// bits of fp32; six products per multiply-add, gemm_tc.cu).  Fewer bits do not
+// bits of fp32; six products per multiply-add, gemm_tc.cu), and every 16-wide
+// k-step is summed into fp32 registers with round-to-nearest.  Less does not
 // do: grad lies in the row space of the layer input while inv_a has gain up to
-// 1/gamma on the other directions, so the rounding of either operand is
-// amplified ~1/gamma-fold (two slices, 16 bits, gave 1e-2 relative error on the
-// first steps of the MLP workload, where 529 of 785 directions have gain 1000).
+// 1/gamma on the other directions, so operand rounding and accumulation error
+// are amplified ~1/gamma-fold (two slices, 16 bits, gave 1e-2 relative error on
+// the first steps of the MLP workload, where 529 of 785 directions have gain
+// 1000; one tensor-core accumulator over the whole K gave 5e-3).
 //   1. split      grad, inv_a, inv_g -> bf16 slices               (one launch)
 //   2. GEMM 1     tmp^T = inv_a * grad^T   (d_in x d_out), written as slices
 //   3. GEMM 2     out   = inv_g * tmp      (= inv_g * (tmp^T)^T), fp32
@@ -73,9 +75,9 @@ int launch_precondition(int n, const kfac_precond_args* args, void* workspace, s
     // out[m][n] = sum_k inv_g[m][k] tmp^T[n][k]: M = d_out, N = d_in, K = d_out
     g2[i] = GtOperand{s_ig, s_tmp, a.d_out, a.d_in, a.d_out, ldo, ldo, a.out, a.ld_out, 0, 0, 1.0f};
   }
-  int rc = launch_split(items, 3 * n, kPcSlices, stream);
-  if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, kPcSlices, stream);
-  if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, kPcSlices, stream);
+  int rc = launch_split(items, 3 * n, stream);
+  if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, stream);
+  if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, stream);
   delete[] items;
   delete[] g1;
   delete[] g2;

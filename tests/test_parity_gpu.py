@@ -252,6 +252,42 @@ def test_damped_inverse_reports_first_bad_pivot():
 
 
 # ------------------------------------------------------------------ a5: precondition
+def run_precondition(XG, grad, XA):
+    d_out, d_in = grad.shape
+    ldg, lda, ldw, ldo = pad(d_out, 4), pad(d_in, 4) + 4, pad(d_in, 4), pad(d_in, 4) + 8
+    tg = to_dev(XG, capi.KFAC_FP32, ldg)
+    ta = to_dev(XA, capi.KFAC_FP32, lda)
+    tw = to_dev(grad, capi.KFAC_FP32, ldw)
+    out = torch.full((d_out, ldo), float("nan"), device="cuda")
+    args = [capi.kfac_precond_args(tg.data_ptr(), ldg, tw.data_ptr(), ldw, ta.data_ptr(), lda, out.data_ptr(), ldo,
+                                   d_out, d_in)]
+    wsb = capi.kfac_precondition_workspace(args)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    capi.kfac_precondition(args, ws.data_ptr(), wsb, stream())
+    sync()
+    return out.cpu().numpy()
+
+
+def test_precondition_identity_is_exact():
+    # every partial sum is exactly representable: the three bf16 slices must reassemble grad bit for bit
+    rng = np.random.default_rng(21)
+    d_out, d_in = 200, 300
+    grad = rng.standard_normal((d_out, d_in)).astype(np.float32)
+    got = run_precondition(np.eye(d_out, dtype=np.float32), grad, np.eye(d_in, dtype=np.float32))
+    assert np.array_equal(got[:, :d_in], grad)
+
+
+def test_precondition_diagonal_uses_all_24_bits():
+    # single-term sums: the result is the fp32 product up to the dropped slice terms (< 2^-23)
+    rng = np.random.default_rng(22)
+    d_out, d_in = 130, 257
+    grad = rng.standard_normal((d_out, d_in)).astype(np.float32)
+    s = (rng.random(d_in) + 0.5).astype(np.float32)
+    got = run_precondition(np.eye(d_out, dtype=np.float32), grad, np.diag(s))
+    ref = grad.astype(np.float64) * s.astype(np.float64)[None, :]
+    assert np.abs(got[:, :d_in] - ref).max() <= 3e-7 * np.abs(ref).max()
+
+
 @pytest.mark.parametrize("d_out,d_in", [(3, 4), (32, 65), (129, 300), (10, 1025), (300, 129)])
 def test_precondition(d_out, d_in):
     rng = np.random.default_rng(d_out * 7 + d_in)
