@@ -31,6 +31,7 @@
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "launch.h"
+#include "split.cuh"
 
 namespace kfac {
 
@@ -81,36 +82,6 @@ __device__ __forceinline__ uint64_t gt_desc(uint32_t saddr) {
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)4 << 61;
   return d;
-}
-
-// x -> three bf16 slices, each carrying the remainder of the previous ones
-__device__ __forceinline__ void split_value(float x, __nv_bfloat16 (&s)[kGtNS]) {
-  float r = x;
-#pragma unroll
-  for (int k = 0; k < kGtNS; ++k) {
-    s[k] = __float2bfloat16_rn(r);
-    r = r - __bfloat162float(s[k]);
-  }
-}
-
-__device__ __forceinline__ void split8_store(const float (&x)[8], uint16_t* dst, long long slice_stride) {
-  uint32_t w[kGtNS][4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    __nv_bfloat16 a[kGtNS], b[kGtNS];
-    split_value(x[2 * e], a);
-    split_value(x[2 * e + 1], b);
-#pragma unroll
-    for (int k = 0; k < kGtNS; ++k) {
-      __nv_bfloat162 p;
-      p.x = a[k];
-      p.y = b[k];
-      w[k][e] = *reinterpret_cast<const uint32_t*>(&p);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < kGtNS; ++k)
-    *reinterpret_cast<uint4*>(dst + k * slice_stride) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
 }
 
 __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_constant__ GtParams prm) {
@@ -287,7 +258,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
               for (int t = 0; t < 32; ++t)
                 if (col0 + t < pr.N) {
-                  __nv_bfloat16 s[kGtNS];
+                  __nv_bfloat16 s[kSlices];
                   split_value(run[g * 32 + t] * pr.alpha, s);
 #pragma unroll
                   for (int k = 0; k < kGtNS; ++k)

@@ -2,21 +2,22 @@
 // (SPD-KFAC §IV: the inverse is computed through a Cholesky decomposition;
 // §III-B: the damped inverses (A + lambda I)^-1, (G + lambda I)^-1).
 //
-// For each matrix (size d, T = ceil(d/128) tile rows, n_pad = 128 T):
-//   L-buffer  n_pad x n_pad, lower tiles = D (+ gamma_extra on the diagonal),
-//             padded with the identity, so every tile operation is full size
-//             (the padded matrix is diag(D, I); its inverse is diag(D^-1, I)).
-//   W-buffer  n_pad x n_pad, lower tiles end up as W = L^-1.
-// Right-looking blocked sweep over the 128-wide block columns k = 0..T-1:
-//   diag(k)   L_kk = chol(A_kk) and Winv_k = L_kk^-1 in shared memory;
-//             Winv_k is stored as W_kk.
-//   panel(k)  L_rk = A_rk Winv_k^T            for r > k
-//             W_kc = Winv_k C_kc              for c < k
-//   update(k) A_rc -= L_rk L_ck^T             for r >= c > k   (Cholesky)
-//             C_rc  = [c<k] C_rc - L_rk W_kc  for r > k >= c   (forward
-//             substitution on I: row block r of L W = I)
-// and finally X = W^T W, formed for the upper tiles and mirrored, so X is
-// exactly symmetric.  The same kernels run in fp32 and fp64 (templates).
+// Algorithm, per matrix (size d, T = ceil(d/128) block rows, n_pad = 128 T,
+// padded with the identity so every tile operation is full size: the padded
+// matrix is diag(D, I) and its inverse diag(D^-1, I)).  Right-looking blocked
+// sweep over the 128-wide block columns k = 0..T-1, Cholesky fused with the
+// blocked forward substitution L W = I (W = L^-1):
+//   diag(k)   L_kk = chol(A_kk), Winv_k = L_kk^-1 in shared memory (= W_kk)
+//   panel(k)  L_rk = A_rk Winv_k^T   for r > k;   W_kc = Winv_k C_kc  for c < k
+//   update(k) A_rc -= L_rk L_ck^T    for r >= c > k  (Schur complement)
+//             C_rc  = [c<k] C_rc - L_rk W_kc  for r > k >= c  (block row r of L W = I)
+// then X = W^T W, formed for the upper tiles and mirrored: X is exactly symmetric.
+//
+// Two passes run these steps:
+//   * fp32 on tcgen05 tensor cores (inverse_tc.cu): every tile product with
+//     three-slice bf16 operands, drained per k-step into fp32;
+//   * fp64 on CUDA cores (this file), for the matrices the fp32 pass routes
+//     to it (refine = AUTO) or for all of them (refine = ALWAYS).
 //
 // refine = AUTO: the fp32 pass measures its own residual.  With kProbes
 // Rademacher vectors v (+-1 entries), w = D v is accumulated in fp64 while D
@@ -30,83 +31,11 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "inverse_common.cuh"
 #include "launch.h"
 #include "simt.cuh"
 
 namespace kfac {
-
-constexpr int kInvMaxGroup = 256;
-constexpr float kAutoKappa = 3e5f;
-constexpr double kAutoResidual = 2.5e-4;
-constexpr int kProbes = 4;
-
-struct InvMat {
-  const float* D;
-  float* X;
-  long long ld_in, ld_out;
-  long long off_buf;     // byte offset of the L/W buffers in the workspace
-  long long off_rowsum;  // float index of this matrix's row sums
-  long long off_probe;   // double index of this matrix's probe vectors w, y
-  int d, T;
-};
-
-struct InvState {
-  int info32, info64, failed, use64;
-  float min_piv, kappa;
-  float xnorm2, est_res;  // ||X||_F^2 and the estimated residual of the fp32 pass
-};
-
-// Rademacher probe entry v_p(i) in {-1, +1} (splitmix64 finaliser of (i, p)).
-__device__ __forceinline__ double probe_sign(long long i, int p) {
-  unsigned long long z = (unsigned long long)(i * kProbes + p) + 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  z ^= z >> 31;
-  return (z & 1ull) ? 1.0 : -1.0;
-}
-
-struct InvSetup {
-  InvMat mats[kInvMaxGroup];
-  int n, mode;
-  long long rowsum_total, probe_total;
-};
-
-struct InvCtx {
-  uint8_t* ws;
-  const InvMat* mats;
-  InvState* st;
-  float* rowsum;
-  double* probe;  // per matrix: w[kProbes][n_pad] then y[kProbes][n_pad]
-  float gamma_extra;
-  int pass64;  // 0: fp32 pass, 1: fp64 pass
-  int want_rowsum;  // fp32 pass of AUTO: record norms and probes
-};
-
-template <typename T>
-__device__ __forceinline__ T* lbuf(const InvCtx& c, const InvMat& m) {
-  return reinterpret_cast<T*>(c.ws + m.off_buf);
-}
-template <typename T>
-__device__ __forceinline__ T* wbuf(const InvCtx& c, const InvMat& m) {
-  return lbuf<T>(c, m) + (long long)m.T * 128 * m.T * 128;
-}
-
-// Whether matrix `mi` takes part in the current pass (and has not failed in it).
-__device__ __forceinline__ bool inv_active(const InvCtx& c, int mi, bool need_ok) {
-  const InvState& s = c.st[mi];
-  if (c.pass64 ? !s.use64 : s.use64) return false;
-  if (need_ok && s.failed) return false;
-  return true;
-}
-
-__host__ __device__ inline long long tri(long long t) { return t * (t + 1) / 2; }
-// largest r with r(r+1)/2 <= q
-__device__ __forceinline__ int tri_root(long long q) {
-  int r = (int)((sqrt(8.0 * (double)q + 1.0) - 1.0) * 0.5);
-  while (tri(r + 1) <= q) ++r;
-  while (tri(r) > q) --r;
-  return r;
-}
 
 // ------------------------------------------------------------------ setup
 __global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, uint8_t* ws, InvMat* mats, InvState* st,
@@ -130,7 +59,7 @@ __global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, uint8_t* 
   for (long long e = tid; e < prm.probe_total; e += nth) probe[e] = 0.0;
 }
 
-// ------------------------------------------------------------------ load D into the L-buffer
+// ------------------------------------------------------------------ fp64 pass: load D into the L-buffer
 template <typename T>
 __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
   const int mi = blockIdx.y;
@@ -138,26 +67,12 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
   const InvMat m = c.mats[mi];
   const long long q = blockIdx.x;
   if (q >= tri(m.T)) return;
-  if (threadIdx.x == 0 && c.pass64) c.st[mi].failed = 0;
+  if (threadIdx.x == 0) c.st[mi].failed = 0;
   const int R = tri_root(q), C = (int)(q - tri(R));  // lower tile (R, C), R >= C
   const long long np = (long long)m.T * 128;
   T* L = lbuf<T>(c, m);
   __shared__ float sub[32][33];
-  __shared__ float rs_row[128], rs_col[128];
-  __shared__ double pw_row[kProbes][128], pw_col[kProbes][128];  // partial w = D v
-  if (threadIdx.x < 128) {
-    rs_row[threadIdx.x] = 0.f;
-    rs_col[threadIdx.x] = 0.f;
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) pw_row[p][threadIdx.x] = pw_col[p][threadIdx.x] = 0.0;
-  }
-  __syncthreads();
   const int lx = threadIdx.x % 32, ly = threadIdx.x / 32;  // 32 x 8
-  double wcol[4][kProbes];  // partial w for column bn + lx, one per column block bn
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) wcol[q4][p] = 0.0;
   for (int sb = 0; sb < 16; ++sb) {
     const int bm = (sb / 4) * 32, bn = (sb % 4) * 32;  // sub-block rows (mm) / cols (nn) of the L tile
     // read D[C*128 + bn + y][R*128 + bm + x] (coalesced along x), store sub[y][x]
@@ -169,87 +84,23 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
       sub[y][lx] = v;
     }
     __syncthreads();
-    // write L[R*128 + bm + y][C*128 + bn + x] = sub[x][y]
-    const long long gc = (long long)C * 128 + bn + lx;
-    double vc[kProbes];
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) vc[p] = probe_sign(gc, p);
     for (int y = ly; y < 32; y += 8) {
       const long long gr = (long long)R * 128 + bm + y;
-      float v = sub[lx][y];
+      const long long gc = (long long)C * 128 + bn + lx;
       T out;
-      double x = 0.0;  // contribution of this stored element to w = D v
-      bool inside = false;
-      if (gr >= m.d || gc >= m.d) {
+      if (gr >= m.d || gc >= m.d)
         out = (gr == gc) ? T(1) : T(0);
-      } else if (gr < gc) {
+      else if (gr < gc)
         out = T(0);
-      } else {
-        out = (T)v;
-        if (gr == gc) out += (T)c.gamma_extra;
-        x = (double)out;  // the matrix being inverted, as stored
-        inside = true;
-      }
+      else
+        out = (T)sub[lx][y] + ((gr == gc) ? (T)c.gamma_extra : T(0));
       L[gr * np + gc] = out;
-      if (c.want_rowsum) {  // uniform over the block
-        const float a = inside ? fabsf(v) : 0.f;
-        float ra = a;
-        for (int o = 16; o > 0; o >>= 1) ra += __shfl_xor_sync(0xffffffffu, ra, o);
-        if (lx == 0) rs_row[bm + y] += ra;  // row bm + y belongs to this warp alone
-#pragma unroll
-        for (int p = 0; p < kProbes; ++p) {
-          double s = x * vc[p];
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (lx == 0) pw_row[p][bm + y] += s;
-          if (inside && gr != gc) wcol[bn / 32][p] += x * probe_sign(gr, p);
-        }
-        if (inside && gr != gc) atomicAdd(&rs_col[bn + lx], a);
-      }
     }
     __syncthreads();
   }
-  if (c.want_rowsum) {
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-      for (int p = 0; p < kProbes; ++p)
-        if (wcol[q4][p] != 0.0) atomicAdd(&pw_col[p][q4 * 32 + lx], wcol[q4][p]);
-    __syncthreads();
-  }
-  if (c.want_rowsum && threadIdx.x < 128) {
-    const long long gr = (long long)R * 128 + threadIdx.x;
-    const long long gc = (long long)C * 128 + threadIdx.x;
-    if (gr < m.d && rs_row[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gr], rs_row[threadIdx.x]);
-    if (gc < m.d && rs_col[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gc], rs_col[threadIdx.x]);
-    double* w = c.probe + m.off_probe;
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) {
-      if (gr < m.d) atomicAdd(&w[p * np + gr], pw_row[p][threadIdx.x]);
-      if (gc < m.d) atomicAdd(&w[p * np + gc], pw_col[p][threadIdx.x]);
-    }
-  }
 }
 
-// ------------------------------------------------------------------ diagonal block
-template <typename T>
-__device__ __forceinline__ T dev_sqrt(T v);
-template <>
-__device__ __forceinline__ float dev_sqrt<float>(float v) { return __fsqrt_rn(v); }
-template <>
-__device__ __forceinline__ double dev_sqrt<double>(double v) { return sqrt(v); }
-template <typename T>
-__device__ __forceinline__ T dev_rcp(T v);
-template <>
-__device__ __forceinline__ float dev_rcp<float>(float v) { return __frcp_rn(v); }
-template <>
-__device__ __forceinline__ double dev_rcp<double>(double v) { return 1.0 / v; }
-
-constexpr int kDiagPitch = 129;
-template <typename T>
-constexpr int diag_smem_bytes() {
-  return 128 * kDiagPitch * (int)sizeof(T);
-}
-
+// ------------------------------------------------------------------ fp64 pass: diagonal block
 template <typename T>
 __global__ void __launch_bounds__(128) inv_diag_kernel(InvCtx c, int k) {
   const int mi = blockIdx.y;
@@ -263,66 +114,14 @@ __global__ void __launch_bounds__(128) inv_diag_kernel(InvCtx c, int k) {
   const int t = threadIdx.x;
   for (int r = 0; r < 128; ++r) a[r * kDiagPitch + t] = (t <= r) ? src[(long long)r * np + t] : T(0);
   __syncthreads();
-
-  // Cholesky, right-looking; column j is scaled by 1/sqrt(pivot) one iteration
-  // later, when no thread reads it any more, so each column costs one barrier.
-  int fail = -1;
-  T min_piv = T(3.0e38);
-  T prev_rs = T(0);
-  for (int j = 0; j < 128; ++j) {
-    const T piv = a[j * kDiagPitch + j];
-    if (!(piv > T(0))) {  // also catches NaN
-      fail = j;
-      break;
-    }
-    if (k * 128 + j < m.d && piv < min_piv) min_piv = piv;
-    if (j > 0) {
-      const int r = j + t;  // rows j .. 127 of column j-1
-      if (r < 128) a[r * kDiagPitch + (j - 1)] *= prev_rs;
-      if (t == 0) a[(j - 1) * kDiagPitch + (j - 1)] = dev_sqrt<T>(a[(j - 1) * kDiagPitch + (j - 1)]);
-    }
-    const T ip = dev_rcp<T>(piv);
-    prev_rs = dev_rcp<T>(dev_sqrt<T>(piv));
-    const int col = t;
-    if (col > j) {
-      const T f = a[col * kDiagPitch + j] * ip;
-      for (int r = col; r < 128; ++r) a[r * kDiagPitch + col] -= a[r * kDiagPitch + j] * f;
-    }
-    __syncthreads();
-  }
+  T min_piv;
+  const int fail = block_chol_inv<T>(a, m.d - k * 128, min_piv);
   if (fail >= 0) {
     if (t == 0) {
-      InvState& s = c.st[mi];
-      s.failed = 1;
-      const int idx = k * 128 + fail + 1;
-      if (c.pass64)
-        s.info64 = idx;
-      else
-        s.info32 = idx;
+      c.st[mi].failed = 1;
+      c.st[mi].info64 = k * 128 + fail + 1;
     }
     return;
-  }
-  // last column: only its diagonal is left
-  if (t == 0) a[127 * kDiagPitch + 127] = dev_sqrt<T>(a[127 * kDiagPitch + 127]);
-  __syncthreads();
-  if (t == 0) {
-    // positive floats order like their bit patterns
-    const float mp = (float)min_piv;
-    atomicMin(reinterpret_cast<int*>(&c.st[mi].min_piv), __float_as_int(mp));
-  }
-
-  // In-place inverse of the lower-triangular block, column by column from the
-  // right: W_jj = 1/L_jj, W_rj = -(sum_{j<s<=r} W_rs L_sj) / L_jj.
-  for (int j = 127; j >= 0; --j) {
-    const T ljj = a[j * kDiagPitch + j];
-    T s = T(0);
-    const int r = t;
-    if (r > j)
-      for (int q = j + 1; q <= r; ++q) s += a[r * kDiagPitch + q] * a[q * kDiagPitch + j];
-    __syncthreads();
-    if (r > j) a[r * kDiagPitch + j] = -s / ljj;
-    if (r == j) a[j * kDiagPitch + j] = dev_rcp<T>(ljj);
-    __syncthreads();
   }
   T* dst = wbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
   for (int r = 0; r < 128; ++r) dst[(long long)r * np + t] = (t <= r) ? a[r * kDiagPitch + t] : T(0);
@@ -348,7 +147,7 @@ __device__ __forceinline__ void tile_store(T* dst, long long ld, const T (&acc)[
   }
 }
 
-// ------------------------------------------------------------------ panel
+// ------------------------------------------------------------------ fp64 pass: panel
 template <typename T>
 __global__ void __launch_bounds__(256) inv_panel_kernel(InvCtx c, int k) {
   const int mi = blockIdx.y;
@@ -382,7 +181,7 @@ __global__ void __launch_bounds__(256) inv_panel_kernel(InvCtx c, int k) {
   }
 }
 
-// ------------------------------------------------------------------ trailing update
+// ------------------------------------------------------------------ fp64 pass: trailing update
 template <typename T>
 __global__ void __launch_bounds__(256) inv_update_kernel(InvCtx c, int k) {
   const int mi = blockIdx.y;
@@ -413,7 +212,7 @@ __global__ void __launch_bounds__(256) inv_update_kernel(InvCtx c, int k) {
   }
 }
 
-// ------------------------------------------------------------------ X = W^T W
+// ------------------------------------------------------------------ fp64 pass: X = W^T W
 template <typename T>
 __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
   const int mi = blockIdx.y;
@@ -432,28 +231,10 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
   Opnd<T> B{W + (long long)j * 128 * np + (long long)j * 128, 1, np, 128};
   simt_tile<T, T, T>(acc, A, B, (int)(np - (long long)j * 128), smem);
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-  const bool probe = c.want_rowsum;
-  __shared__ double py_row[kProbes][128], py_col[kProbes][128];  // partial y = X w
-  const double* w = c.probe + m.off_probe;
-  if (probe) {
-    if (threadIdx.x < 128)
-#pragma unroll
-      for (int p = 0; p < kProbes; ++p) py_row[p][threadIdx.x] = py_col[p][threadIdx.x] = 0.0;
-    __syncthreads();
-  }
-  float sq = 0.f;  // this thread's share of ||X||_F^2
-  double ycol[8][kProbes];  // this thread's partial y for its 8 columns
-#pragma unroll
-  for (int b = 0; b < 8; ++b)
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) ycol[b][p] = 0.0;
 #pragma unroll
   for (int a = 0; a < 8; ++a) {
     const int mm = ty * 8 + a;
     const long long row = (long long)i * 128 + mm;
-    double yrow[kProbes];
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) yrow[p] = 0.0;
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       const int nn = tx * 8 + b;
@@ -462,45 +243,6 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
       const float v = (float)acc[a][b];
       m.X[row * m.ld_out + col] = v;
       m.X[col * m.ld_out + row] = v;
-      sq += (row == col ? 1.f : 2.f) * v * v;
-      if (probe) {
-        // the stored value X[row][col] = X[col][row] contributes to y[row] and y[col]
-        const double x = (double)v;
-#pragma unroll
-        for (int p = 0; p < kProbes; ++p) {
-          yrow[p] += x * w[p * np + col];
-          if (row != col) ycol[b][p] += x * w[p * np + row];
-        }
-      }
-    }
-    if (probe) {
-      // the 16 threads of a row (same ty) are 16 consecutive lanes of one warp
-#pragma unroll
-      for (int p = 0; p < kProbes; ++p) {
-        double s = yrow[p];
-        for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (tx == 0) py_row[p][mm] = s;
-      }
-    }
-  }
-  if (probe) {
-#pragma unroll
-    for (int b = 0; b < 8; ++b)
-#pragma unroll
-      for (int p = 0; p < kProbes; ++p)
-        if (ycol[b][p] != 0.0) atomicAdd(&py_col[p][tx * 8 + b], ycol[b][p]);
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if ((threadIdx.x & 31) == 0) atomicAdd(&c.st[mi].xnorm2, sq);
-    __syncthreads();
-    if (threadIdx.x < 128) {
-      double* y = c.probe + m.off_probe + (long long)kProbes * np;
-      const long long row = (long long)i * 128 + threadIdx.x;
-      const long long col = (long long)j * 128 + threadIdx.x;
-#pragma unroll
-      for (int p = 0; p < kProbes; ++p) {
-        if (row < m.d) atomicAdd(&y[p * np + row], py_row[p][threadIdx.x]);
-        if (col < m.d) atomicAdd(&y[p * np + col], py_col[p][threadIdx.x]);
-      }
     }
   }
 }
@@ -555,7 +297,8 @@ __global__ void inv_finish_kernel(InvCtx c, int n, int* info, int* route) {
 
 // ------------------------------------------------------------------ host side
 struct InvLayout {
-  size_t mats_off, st_off, rowsum_off, probe_off, buf_off, total;
+  size_t mats_off, st_off, rowsum_off, probe_off, region_off, total;
+  TcLayout tc;
 };
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -567,25 +310,32 @@ static InvLayout inv_layout(int n, const kfac_inverse_args* args, int refine, lo
   L.st_off = align256(sizeof(InvMat) * (size_t)n);
   L.rowsum_off = L.st_off + align256(sizeof(InvState) * (size_t)n);
   long long rs = 0;
+  int Ts[kInvMaxGroup];
   for (int i = 0; i < n; ++i) {
     if (mats) {
       mats[i].off_rowsum = rs;
       mats[i].off_probe = 2 * kProbes * rs;
+      mats[i].row_off = rs;
     }
-    rs += (args[i].d + 127) / 128 * 128;
+    Ts[i] = (int)((args[i].d + 127) / 128);
+    rs += (long long)Ts[i] * 128;
   }
   *rowsum_total = rs;
   *probe_total = 2 * kProbes * rs;
   L.probe_off = L.rowsum_off + align256(sizeof(float) * (size_t)rs);
-  L.buf_off = L.probe_off + align256(sizeof(double) * (size_t)(2 * kProbes * rs));
-  size_t off = L.buf_off;
-  const size_t elem = refine == KFAC_REFINE_NONE ? 4 : 8;
-  for (int i = 0; i < n; ++i) {
-    const size_t np = (size_t)((args[i].d + 127) / 128) * 128;
-    if (mats) mats[i].off_buf = (long long)off;
-    off += align256(2 * np * np * elem);
-  }
-  L.total = off;
+  L.region_off = L.probe_off + align256(sizeof(double) * (size_t)(2 * kProbes * rs));
+  // the fp32 tensor-core pass and the fp64 pass run one after the other and
+  // share the work region
+  size_t fp64 = 0;
+  if (refine != KFAC_REFINE_NONE)
+    for (int i = 0; i < n; ++i) {
+      const size_t np = (size_t)Ts[i] * 128;
+      if (mats) mats[i].off_buf = (long long)fp64;
+      fp64 += align256(2 * np * np * sizeof(double));
+    }
+  L.tc = tc_layout(n, Ts);
+  const size_t fp32 = refine != KFAC_REFINE_ALWAYS ? L.tc.bytes : 0;
+  L.total = L.region_off + (fp64 > fp32 ? fp64 : fp32);
   return L;
 }
 
@@ -601,19 +351,18 @@ size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine) {
   return best;
 }
 
-template <typename T>
-static int run_pass(const InvCtx& ctx, int cnt, int Tmax, const int* Ts, cudaStream_t stream) {
-  const int dsm = diag_smem_bytes<T>();
+static int run_fp64_pass(const InvCtx& ctx, int cnt, int Tmax, const int* Ts, cudaStream_t stream) {
+  const int dsm = diag_smem_bytes<double>();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
-  if (!ensure_smem_attr(dev, (const void*)inv_diag_kernel<T>, dsm)) return KFAC_ERR_CUDA;
-  inv_load_kernel<T><<<dim3((unsigned)tri(Tmax), cnt), 256, 0, stream>>>(ctx);
+  if (!ensure_smem_attr(dev, (const void*)inv_diag_kernel<double>, dsm)) return KFAC_ERR_CUDA;
+  inv_load_kernel<double><<<dim3((unsigned)tri(Tmax), cnt), 256, 0, stream>>>(ctx);
   count_launch();
   for (int k = 0; k < Tmax; ++k) {
-    inv_diag_kernel<T><<<dim3(1, cnt), 128, dsm, stream>>>(ctx, k);
+    inv_diag_kernel<double><<<dim3(1, cnt), 128, dsm, stream>>>(ctx, k);
     count_launch();
     if (Tmax > 1) {
-      inv_panel_kernel<T><<<dim3((unsigned)(Tmax - 1), cnt), 256, 0, stream>>>(ctx, k);
+      inv_panel_kernel<double><<<dim3((unsigned)(Tmax - 1), cnt), 256, 0, stream>>>(ctx, k);
       count_launch();
     }
     long long upd = 0;
@@ -623,11 +372,11 @@ static int run_pass(const InvCtx& ctx, int cnt, int Tmax, const int* Ts, cudaStr
         if (u > upd) upd = u;
       }
     if (upd > 0) {
-      inv_update_kernel<T><<<dim3((unsigned)upd, cnt), 256, 0, stream>>>(ctx, k);
+      inv_update_kernel<double><<<dim3((unsigned)upd, cnt), 256, 0, stream>>>(ctx, k);
       count_launch();
     }
   }
-  inv_lauum_kernel<T><<<dim3((unsigned)tri(Tmax), cnt), 256, 0, stream>>>(ctx);
+  inv_lauum_kernel<double><<<dim3((unsigned)tri(Tmax), cnt), 256, 0, stream>>>(ctx);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
@@ -636,7 +385,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (workspace_bytes < inverse_workspace(n, args, refine) || workspace == nullptr) return KFAC_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  InvSetup prm;  // 16 KB of kernel parameters, staged on the host stack
+  InvSetup prm;  // 18 KB of kernel parameters, staged on the host stack
   int Ts[kInvMaxGroup];
   for (int base = 0; base < n; base += kInvMaxGroup) {
     const int cnt = n - base < kInvMaxGroup ? n - base : kInvMaxGroup;
@@ -666,6 +415,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
     ctx.st = reinterpret_cast<InvState*>(ws + L.st_off);
     ctx.rowsum = reinterpret_cast<float*>(ws + L.rowsum_off);
     ctx.probe = reinterpret_cast<double*>(ws + L.probe_off);
+    ctx.region = ws + L.region_off;
     ctx.gamma_extra = gamma_extra;
     ctx.want_rowsum = refine == KFAC_REFINE_AUTO;
     {
@@ -679,7 +429,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
     int rc;
     if (refine != KFAC_REFINE_ALWAYS) {
       ctx.pass64 = 0;
-      rc = run_pass<float>(ctx, cnt, Tmax, Ts, stream);
+      rc = run_tc_pass(ctx, prm.mats, cnt, Tmax, Ts, L.tc, stream);
       if (rc != KFAC_OK) return rc;
     }
     if (refine == KFAC_REFINE_AUTO) {
@@ -689,7 +439,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
     if (refine != KFAC_REFINE_NONE) {
       ctx.pass64 = 1;
       ctx.want_rowsum = 0;
-      rc = run_pass<double>(ctx, cnt, Tmax, Ts, stream);
+      rc = run_fp64_pass(ctx, cnt, Tmax, Ts, stream);
       if (rc != KFAC_OK) return rc;
     }
     inv_finish_kernel<<<(cnt + 255) / 256, 256, 0, stream>>>(ctx, cnt, info + base, route ? route + base : nullptr);

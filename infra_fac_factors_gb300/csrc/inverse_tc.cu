@@ -1,0 +1,750 @@
+// fp32 pass of the batched damped inverse on tcgen05 tensor cores (the
+// algorithm is described in inverse.cu).  Every tile product is a split-bf16
+// NT GEMM (three slices per fp32 value, six MMAs per 16-wide k-step, each
+// k-step drained into round-to-nearest fp32 sums, as in gemm_tc.cu), so the
+// arithmetic has fp32 accuracy.
+//
+// To make every product NT with K-major operands, the blocked inverse
+// W = L^-1 is kept transposed, U = W^T (block upper triangular), and so are
+// the forward-substitution accumulators C:
+//   panel(k)   L_rk = A_rk Winv_k^T                 (r > k)
+//              U_rk = C'_rk Winv_k^T                 (r < k)     [C'_rk = C_kr^T]
+//   update(k)  A_rc  -= L_rk L_ck^T                  (r >= c > k)
+//              C'_cr -= U_ck L_rk^T, first time =    (c <= k < r)
+//   X_ij = sum_{t >= j} U_it U_jt^T                  (i <= j), mirrored.
+// Work buffers, stacked over the matrices of a group (matrix m owns rows
+// [row_off, row_off + n_pad) of each, with one leading dimension LD = max n_pad):
+//   Acc   fp32 [R][LD]  lower blocks: A (Schur complements), upper blocks: C'
+//   U     bf16 [3][R][LD]   slices of U
+//   P     bf16 [3][R][128]  slices of block column k of Acc (the panel inputs)
+//   Lp    bf16 [3][R][128]  slices of L_rk, the current panel column
+//   Winv  bf16 [3][n*128][128]
+// so that one tensor map per buffer serves every matrix.  Updates land in Acc
+// through TMA add-reductions (no read-modify-write in the kernel).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "inverse_common.cuh"
+#include "launch.h"
+#include "split.cuh"
+
+namespace kfac {
+
+constexpr int kItBK = 32;
+constexpr int kItStages = 2;
+constexpr int kItA = 128 * kItBK * 2;  // one slice of the A tile (8 KB)
+constexpr int kItB = 256 * kItBK * 2;  // one slice of the B tile (16 KB, 128-row boxes use half)
+constexpr int kItStage = kSlices * (kItA + kItB);
+constexpr int kItOutBlock = 4096;  // one 32 x 32 fp32 block
+constexpr int kItOut = 8 * 2 * kItOutBlock;
+constexpr int kItSmem = kItStages * kItStage + kItOut + 1024 + 256;
+constexpr int kItThreads = 320;
+
+enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
+
+struct TcBufs {
+  float* acc;
+  uint16_t* u;
+  uint16_t* p;
+  uint16_t* lp;
+  uint16_t* winv;
+  long long R, LD;
+  int n;
+};
+
+struct ItParams {
+  CUtensorMap mUA, mUB, mP, mLA, mLB, mW, mAcc;
+  long long ro[kInvMaxGroup];
+  int T[kInvMaxGroup];
+  int job_begin[kInvMaxGroup + 1];
+  TcBufs b;
+  const InvMat* mats;
+  InvState* st;
+  int* status;
+  long long total_jobs;
+  int n, k;
+};
+
+struct ItJob {
+  int m, valid;
+  const CUtensorMap* ma;
+  const CUtensorMap* mb;
+  int a_y, a_x0, b_y, b_x0, b_box, K, n_mma;
+  int o_y, o_x, mode;  // output rows/cols; panel: 0 -> Lp, 1 -> U; update: 0 add, 1 store
+  int i, j;            // X tile (i, j) of the pair j, j+1 (lauum)
+};
+
+// jobs of the update at step k for a matrix of T block rows: rows r > k pair
+// their columns c in (k, r]; columns c <= k pair their rows r > k
+__host__ __device__ inline long long it_pairs(long long R) { return ((R + 1) / 2) * ((R + 2) / 2); }
+
+template <int KIND>
+__device__ ItJob it_decode(const ItParams& prm, long long u) {
+  int lo = 0, hi = prm.n;  // find m with job_begin[m] <= u < job_begin[m+1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (prm.job_begin[mid] <= u)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  ItJob J;
+  const int m = lo;
+  const long long q = u - prm.job_begin[m];
+  const long long ro = prm.ro[m];
+  const int T = prm.T[m];
+  const int k = prm.k;
+  J.m = m;
+  J.valid = !prm.st[m].failed;
+  J.i = J.j = 0;
+  J.mode = 0;
+  if (KIND == kItPanel) {
+    const int r = q < k ? (int)q : (int)q + 1;
+    J.ma = &prm.mP;
+    J.a_y = (int)(ro + r * 128);
+    J.a_x0 = 0;
+    J.mb = &prm.mW;
+    J.b_y = m * 128;
+    J.b_x0 = 0;
+    J.b_box = 128;
+    J.K = 128;
+    J.n_mma = 128;
+    J.o_y = (int)(ro + r * 128);
+    J.o_x = k * 128;
+    J.mode = r > k ? 0 : 1;
+  } else if (KIND == kItUpdate) {
+    const int R = T - k - 1;
+    const long long ni = it_pairs(R);
+    J.K = 128;
+    J.mb = &prm.mLB;
+    J.b_x0 = 0;
+    J.b_box = 256;
+    if (q < ni) {
+      int jrow = 1;
+      while (it_pairs(jrow) <= q) ++jrow;  // rows r = k + jrow
+      const int cp = (int)(q - it_pairs(jrow - 1));
+      const int r = k + jrow, c = k + 1 + 2 * cp;
+      const int w = min(2, r - c + 1);
+      J.ma = &prm.mLA;
+      J.a_y = (int)(ro + r * 128);
+      J.a_x0 = 0;
+      J.b_y = (int)(ro + c * 128);
+      J.n_mma = 128 * w;
+      J.o_y = (int)(ro + r * 128);
+      J.o_x = c * 128;
+      J.mode = 0;
+    } else {
+      const long long q2 = q - ni;
+      const int hp = (R + 1) / 2;
+      const int c = (int)(q2 / hp), rp = (int)(q2 % hp);
+      const int r = k + 1 + 2 * rp;
+      const int w = min(2, T - r);
+      J.ma = &prm.mUA;
+      J.a_y = (int)(ro + c * 128);
+      J.a_x0 = k * 128;
+      J.b_y = (int)(ro + r * 128);
+      J.n_mma = 128 * w;
+      J.o_y = (int)(ro + c * 128);
+      J.o_x = r * 128;
+      J.mode = c == k ? 1 : 0;
+    }
+  } else {
+    int i = 0;
+    long long qq = q;
+    while (qq >= (T - i + 1) / 2) {
+      qq -= (T - i + 1) / 2;
+      ++i;
+    }
+    const int j = i + 2 * (int)qq;
+    const int w = min(2, T - j);
+    J.i = i;
+    J.j = j;
+    J.ma = &prm.mUA;
+    J.a_y = (int)(ro + i * 128);
+    J.a_x0 = j * 128;
+    J.mb = &prm.mUB;
+    J.b_y = (int)(ro + j * 128);
+    J.b_x0 = j * 128;
+    J.b_box = 256;
+    J.K = (T - j) * 128;
+    J.n_mma = 128 * w;
+  }
+  return J;
+}
+
+// K-major shared-memory descriptor, 64-byte swizzle (as in gemm_tc.cu)
+__device__ __forceinline__ uint64_t it_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(16 >> 4) << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_constant__ ItParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* out_stage = smem + kItStages * kItStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + kItOut);
+  uint64_t* empty = full + kItStages;
+  uint64_t* acc_full = empty + kItStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done_bar = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kItStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 8);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tc_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      for (long long u = blockIdx.x; u < prm.total_jobs && !*abort_flag; u += gridDim.x) {
+        const ItJob J = it_decode<KIND>(prm, u);
+        if (!J.valid) continue;
+        const uint32_t bytes = kSlices * (kItA + J.b_box * kItBK * 2);
+        for (int kb = 0; kb < J.K / kItBK; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
+          uint8_t* s0 = smem + stage * kItStage;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+#pragma unroll
+          for (int s = 0; s < kSlices; ++s) {
+            tma_load_3d(s0 + s * kItA, J.ma, J.a_x0 + kb * kItBK, J.a_y, s, &full[stage]);
+            tma_load_3d(s0 + kSlices * kItA + s * kItB, J.mb, J.b_x0 + kb * kItBK, J.b_y, s, &full[stage]);
+          }
+          if (++stage == kItStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (long long u = blockIdx.x; u < prm.total_jobs && ok; u += gridDim.x) {
+        const ItJob J = it_decode<KIND>(prm, u);
+        if (!J.valid) continue;
+        const uint32_t idesc = idesc_bf16_f32(J.n_mma, false, false);
+        for (int kb = 0; kb < J.K / kItBK && ok; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, prm.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a0 = smem_u32(smem + stage * kItStage);
+          const uint32_t b0 = a0 + kSlices * kItA;
+#pragma unroll
+          for (int kk = 0; kk < kItBK / 16; ++kk) {
+            if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * 256;
+            const uint32_t off = kk * 32;
+            uint64_t da[kSlices], db[kSlices];
+#pragma unroll
+            for (int s = 0; s < kSlices; ++s) {
+              da[s] = it_desc(a0 + s * kItA + off);
+              db[s] = it_desc(b0 + s * kItB + off);
+            }
+            tc_mma_bf16(d_tmem, da[0], db[0], idesc, 0u);
+            tc_mma_bf16(d_tmem, da[0], db[1], idesc, 1u);
+            tc_mma_bf16(d_tmem, da[1], db[0], idesc, 1u);
+            tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
+            tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
+            tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
+            tc_commit(&acc_full[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kItStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0, abort_flag, prm.status);
+    }
+  } else {
+    const int e = warp - 2;
+    const int q = warp & 3;  // TMEM lane quarter
+    const int h = e / 4;     // column half of the 256-wide tile
+    uint32_t acc = 0, acc_phase = 0;
+    int obuf = 0;
+    bool ok = true;
+    for (long long u = blockIdx.x; u < prm.total_jobs && ok; u += gridDim.x) {
+      const ItJob J = it_decode<KIND>(prm, u);
+      if (!J.valid) continue;
+      const bool mine = h * 128 < J.n_mma;  // this warp's 128 columns exist
+      float run[128];
+#pragma unroll
+      for (int t = 0; t < 128; ++t) run[t] = 0.f;
+      const int nsteps = J.K / 16;
+      for (int st = 0; st < nsteps; ++st) {
+        if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (mine) {
+          const uint32_t base = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + h * 128;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
+            tc_ld_32x32b_x32(base + g * 32, v);
+            tc_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) run[g * 32 + t] += __uint_as_float(v[t]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok || !mine) continue;
+      const int mrow = q * 32 + lane;  // row of the 128-row output tile
+      if (KIND == kItPanel) {
+        // L_rk (r > k) into Lp, or U_rk (r < k) into U, as three bf16 slices
+        uint16_t* dst;
+        long long sstride;
+        if (J.mode == 0) {
+          dst = prm.b.lp + (long long)(J.o_y + mrow) * 128;
+          sstride = prm.b.R * 128;
+        } else {
+          dst = prm.b.u + (long long)(J.o_y + mrow) * prm.b.LD + J.o_x;
+          sstride = prm.b.R * prm.b.LD;
+        }
+#pragma unroll
+        for (int t = 0; t < 128; t += 8) {
+          float x8[8];
+#pragma unroll
+          for (int e8 = 0; e8 < 8; ++e8) x8[e8] = run[t + e8];
+          split8_store(x8, dst + t, sstride);
+        }
+      } else if (KIND == kItUpdate) {
+        // -acc into Acc through 32 x 32 TMA add-reductions (or stores, first time)
+        for (int g = 0; g < 4; ++g) {
+          uint8_t* buf = out_stage + (e * 2 + obuf) * kItOutBlock;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const float4 o = make_float4(-run[g * 32 + 4 * jj], -run[g * 32 + 4 * jj + 1], -run[g * 32 + 4 * jj + 2],
+                                         -run[g * 32 + 4 * jj + 3]);
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((jj ^ (lane & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int cx = J.o_x + h * 128 + g * 32, cy = J.o_y + q * 32;
+            if (J.mode == 1)
+              tma_store_2d(&prm.mAcc, buf, cx, cy);
+            else
+              tma_reduce_add_2d(&prm.mAcc, buf, cx, cy);
+            bulk_commit();
+          }
+          obuf ^= 1;
+        }
+      } else {
+        // X tile (i, j + h) of the pair: write it and its mirror
+        const InvMat mt = prm.mats[J.m];
+        const int jt = J.j + h;
+        const long long row = (long long)J.i * 128 + mrow;
+        if (row < mt.d) {
+#pragma unroll
+          for (int t = 0; t < 128; ++t) {
+            const long long col = (long long)jt * 128 + t;
+            if (col < mt.d && (J.i != jt || mrow <= t)) {
+              const float v = run[t];
+              mt.X[row * mt.ld_out + col] = v;
+              mt.X[col * mt.ld_out + row] = v;
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tc_dealloc(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------------------------ D -> Acc (lower blocks)
+__global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, false)) return;
+  const InvMat m = c.mats[mi];
+  const long long q = blockIdx.x;
+  if (q >= tri(m.T)) return;
+  const int R = tri_root(q), C = (int)(q - tri(R));  // lower tile (R, C), R >= C
+  const long long np = (long long)m.T * 128;
+  float* A = b.acc + m.row_off * b.LD;
+  __shared__ float sub[32][33];
+  __shared__ float rs_row[128], rs_col[128];
+  __shared__ double pw_row[kProbes][128], pw_col[kProbes][128];  // partial w = D v
+  if (threadIdx.x < 128) {
+    rs_row[threadIdx.x] = 0.f;
+    rs_col[threadIdx.x] = 0.f;
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) pw_row[p][threadIdx.x] = pw_col[p][threadIdx.x] = 0.0;
+  }
+  __syncthreads();
+  const int lx = threadIdx.x % 32, ly = threadIdx.x / 32;  // 32 x 8
+  double wcol[4][kProbes];  // partial w for column bn + lx, per column block bn
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) wcol[q4][p] = 0.0;
+  for (int sb = 0; sb < 16; ++sb) {
+    const int bm = (sb / 4) * 32, bn = (sb % 4) * 32;  // sub-block rows (mm) / cols (nn) of the tile
+    for (int y = ly; y < 32; y += 8) {
+      const long long gc = (long long)C * 128 + bn + y;   // D row   = tile column
+      const long long gr = (long long)R * 128 + bm + lx;  // D column = tile row
+      float v = 0.f;
+      if (gc < m.d && gr < m.d && gr >= gc) v = m.D[gc * m.ld_in + gr];
+      sub[y][lx] = v;
+    }
+    __syncthreads();
+    const long long gc = (long long)C * 128 + bn + lx;
+    double vc[kProbes];
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) vc[p] = probe_sign(gc, p);
+    for (int y = ly; y < 32; y += 8) {
+      const long long gr = (long long)R * 128 + bm + y;
+      const float v = sub[lx][y];
+      float out;
+      bool inside = false;
+      if (gr >= m.d || gc >= m.d) {
+        out = (gr == gc) ? 1.f : 0.f;
+      } else if (gr < gc) {
+        out = 0.f;
+      } else {
+        out = v + ((gr == gc) ? c.gamma_extra : 0.f);
+        inside = true;
+      }
+      A[gr * b.LD + gc] = out;
+      if (c.want_rowsum) {  // uniform over the block
+        const float a = inside ? fabsf(v) : 0.f;
+        float ra = a;
+        for (int o = 16; o > 0; o >>= 1) ra += __shfl_xor_sync(0xffffffffu, ra, o);
+        if (lx == 0) rs_row[bm + y] += ra;  // row bm + y belongs to this warp alone
+        const double x = inside ? (double)out : 0.0;  // the matrix being inverted, as stored
+#pragma unroll
+        for (int p = 0; p < kProbes; ++p) {
+          double s = x * vc[p];
+          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          if (lx == 0) pw_row[p][bm + y] += s;
+          if (inside && gr != gc) wcol[bn / 32][p] += x * probe_sign(gr, p);
+        }
+        if (inside && gr != gc) atomicAdd(&rs_col[bn + lx], a);
+      }
+    }
+    __syncthreads();
+  }
+  // zero the sub-diagonal U block (R, R-1): the X = U U^T products read it when they pair block rows
+  if (R == C + 1) {
+    const long long ss = b.R * b.LD;
+    for (int e = threadIdx.x; e < 128 * 16; e += 256) {
+      const int rr = e / 16, cc = (e % 16) * 8;
+      uint16_t* dst = b.u + (m.row_off + (long long)R * 128 + rr) * b.LD + (long long)C * 128 + cc;
+#pragma unroll
+      for (int s = 0; s < kSlices; ++s) *reinterpret_cast<uint4*>(dst + s * ss) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  if (c.want_rowsum) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p)
+        if (wcol[q4][p] != 0.0) atomicAdd(&pw_col[p][q4 * 32 + lx], wcol[q4][p]);
+    __syncthreads();
+    if (threadIdx.x < 128) {
+      const long long gr = (long long)R * 128 + threadIdx.x;
+      const long long gcc = (long long)C * 128 + threadIdx.x;
+      if (gr < m.d && rs_row[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gr], rs_row[threadIdx.x]);
+      if (gcc < m.d && rs_col[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gcc], rs_col[threadIdx.x]);
+      double* w = c.probe + m.off_probe;
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p) {
+        if (gr < m.d) atomicAdd(&w[p * np + gr], pw_row[p][threadIdx.x]);
+        if (gcc < m.d) atomicAdd(&w[p * np + gcc], pw_col[p][threadIdx.x]);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ step k: slices of block column k + diagonal block
+// blockIdx.x == 0: Cholesky and inverse of the diagonal block; blockIdx.x = x >= 1:
+// tile row r (the x-th row other than k) of block column k -> P slices.
+__global__ void __launch_bounds__(128) tc_prep_diag_kernel(InvCtx c, TcBufs b, int k) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, true)) return;
+  const InvMat m = c.mats[mi];
+  if (k >= m.T) return;
+  const int t = threadIdx.x;
+  const float* A = b.acc + m.row_off * b.LD;
+  if (blockIdx.x > 0) {
+    const int x = blockIdx.x - 1;
+    const int r = x < k ? x : x + 1;
+    if (r >= m.T) return;
+    const float* src = A + ((long long)r * 128 + t) * b.LD + (long long)k * 128;
+    uint16_t* dst = b.p + (m.row_off + (long long)r * 128 + t) * 128;
+    for (int c8 = 0; c8 < 128; c8 += 8) {
+      const float4 u0 = *reinterpret_cast<const float4*>(src + c8);
+      const float4 u1 = *reinterpret_cast<const float4*>(src + c8 + 4);
+      const float x8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      split8_store(x8, dst + c8, b.R * 128);
+    }
+    return;
+  }
+  extern __shared__ __align__(16) uint8_t diag_smem[];
+  float* a = reinterpret_cast<float*>(diag_smem);
+  const float* src = A + (long long)k * 128 * b.LD + (long long)k * 128;
+  for (int r = 0; r < 128; ++r) a[r * kDiagPitch + t] = (t <= r) ? src[(long long)r * b.LD + t] : 0.f;
+  __syncthreads();
+  float min_piv;
+  const int fail = block_chol_inv<float>(a, m.d - k * 128, min_piv);
+  if (fail >= 0) {
+    if (t == 0) {
+      c.st[mi].failed = 1;
+      c.st[mi].info32 = k * 128 + fail + 1;
+    }
+    return;
+  }
+  if (t == 0) atomicMin(reinterpret_cast<int*>(&c.st[mi].min_piv), __float_as_int(min_piv));
+  // Winv_k rows (the panel's B operand) and U_kk = Winv_k^T rows, as slices
+  uint16_t* wdst = b.winv + ((long long)mi * 128 + t) * 128;
+  uint16_t* udst = b.u + (m.row_off + (long long)k * 128 + t) * b.LD + (long long)k * 128;
+  for (int c8 = 0; c8 < 128; c8 += 8) {
+    float w8[8], u8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      w8[e] = a[t * kDiagPitch + c8 + e];  // Winv[t][c]  (zero above the diagonal)
+      u8[e] = a[(c8 + e) * kDiagPitch + t];  // Winv[c][t]
+    }
+    split8_store(w8, wdst + c8, (long long)b.n * 128 * 128);
+    split8_store(u8, udst + c8, b.R * b.LD);
+  }
+}
+
+// ------------------------------------------------------------------ residual probe y = X w, ||X||_F^2
+// one warp per row of X (full symmetric, as written by the lauum step)
+__global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c, int n) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, true)) return;
+  const InvMat m = c.mats[mi];
+  const int lane = threadIdx.x % 32;
+  const long long np = (long long)m.T * 128;
+  const double* w = c.probe + m.off_probe;
+  double* y = c.probe + m.off_probe + (long long)kProbes * np;
+  float sq = 0.f;
+  for (long long r = (long long)blockIdx.x * 8 + threadIdx.x / 32; r < m.d; r += (long long)gridDim.x * 8) {
+    double acc[kProbes] = {0.0, 0.0, 0.0, 0.0};
+    const float* xr = m.X + r * m.ld_out;
+    for (long long col = lane; col < m.d; col += 32) {
+      const float v = xr[col];
+      sq += v * v;
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p) acc[p] += (double)v * w[p * np + col];
+    }
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) {
+      double s = acc[p];
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) y[p * np + r] = s;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  if (lane == 0) atomicAdd(&c.st[mi].xnorm2, sq);
+}
+
+// ------------------------------------------------------------------ host side
+static size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+TcLayout tc_layout(int n, const int* T) {
+  TcLayout L;
+  long long R = 0, LD = 128;
+  for (int i = 0; i < n; ++i) {
+    R += (long long)T[i] * 128;
+    if ((long long)T[i] * 128 > LD) LD = (long long)T[i] * 128;
+  }
+  L.R_tot = R;
+  L.LD = LD;
+  size_t off = 0;
+  L.acc = off;
+  off += al256((size_t)R * LD * 4);
+  L.u = off;
+  off += al256((size_t)kSlices * R * LD * 2);
+  L.p = off;
+  off += al256((size_t)kSlices * R * 128 * 2);
+  L.lp = off;
+  off += al256((size_t)kSlices * R * 128 * 2);
+  L.winv = off;
+  off += al256((size_t)kSlices * n * 128 * 128 * 2);
+  L.bytes = off;
+  return L;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn it_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// slices [3][rows][cols] bf16, K-major boxes {32, box_rows}
+static bool enc_slices(EncodeTiledFn enc, CUtensorMap* map, uint16_t* base, long long rows, long long cols,
+                       int box_rows) {
+  cuuint64_t gdim[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)kSlices};
+  cuuint64_t gstride[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows * cols * 2)};
+  cuuint32_t box[3] = {(cuuint32_t)kItBK, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND>
+static int launch_it(ItParams* prm, const int* Ts, int n, int k, int sms, cudaStream_t stream) {
+  long long jobs = 0;
+  for (int i = 0; i < n; ++i) {
+    prm->job_begin[i] = (int)jobs;
+    long long cnt = 0;
+    const int T = Ts[i];
+    if (KIND == kItPanel) {
+      cnt = T > k ? T - 1 : 0;
+    } else if (KIND == kItUpdate) {
+      const int R = T - k - 1;
+      cnt = R > 0 ? it_pairs(R) + (long long)(k + 1) * ((R + 1) / 2) : 0;
+    } else {
+      cnt = it_pairs(T);
+    }
+    jobs += cnt;
+  }
+  prm->job_begin[n] = (int)jobs;
+  prm->total_jobs = jobs;
+  prm->k = k;
+  if (jobs == 0) return KFAC_OK;
+  const int grid = (int)(jobs < sms ? jobs : sms);
+  inv_tc_kernel<KIND><<<grid, kItThreads, kItSmem, stream>>>(*prm);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
+int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, const int* Ts, const TcLayout& L,
+                cudaStream_t stream) {
+  EncodeTiledFn enc = it_encode_fn();
+  if (!enc) return KFAC_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return KFAC_ERR_CUDA;
+  if (!ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItPanel>, kItSmem) ||
+      !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItUpdate>, kItSmem) ||
+      !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItLauum>, kItSmem) ||
+      !ensure_smem_attr(dev, (const void*)tc_prep_diag_kernel, diag_smem_bytes<float>()))
+    return KFAC_ERR_CUDA;
+  int* status = device_status_ptr();
+  if (!status) return KFAC_ERR_CUDA;
+
+  TcBufs b;
+  b.acc = reinterpret_cast<float*>(ctx.region + L.acc);
+  b.u = reinterpret_cast<uint16_t*>(ctx.region + L.u);
+  b.p = reinterpret_cast<uint16_t*>(ctx.region + L.p);
+  b.lp = reinterpret_cast<uint16_t*>(ctx.region + L.lp);
+  b.winv = reinterpret_cast<uint16_t*>(ctx.region + L.winv);
+  b.R = L.R_tot;
+  b.LD = L.LD;
+  b.n = n;
+
+  ItParams* prm = new ItParams;
+  memset(prm, 0, sizeof(ItParams));
+  bool ok = enc_slices(enc, &prm->mUA, b.u, b.R, b.LD, 128) && enc_slices(enc, &prm->mUB, b.u, b.R, b.LD, 256) &&
+            enc_slices(enc, &prm->mP, b.p, b.R, 128, 128) && enc_slices(enc, &prm->mLA, b.lp, b.R, 128, 128) &&
+            enc_slices(enc, &prm->mLB, b.lp, b.R, 128, 256) &&
+            enc_slices(enc, &prm->mW, b.winv, (long long)n * 128, 128, 128);
+  {
+    cuuint64_t gdim[2] = {(cuuint64_t)b.LD, (cuuint64_t)b.R};
+    cuuint64_t gstride[1] = {(cuuint64_t)b.LD * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    ok = ok && enc(&prm->mAcc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, b.acc, gdim, gstride, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  if (!ok) {
+    delete prm;
+    return KFAC_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n; ++i) {
+    prm->ro[i] = host_mats[i].row_off;
+    prm->T[i] = Ts[i];
+  }
+  prm->b = b;
+  prm->mats = ctx.mats;
+  prm->st = ctx.st;
+  prm->status = status;
+  prm->n = n;
+
+  int rc = KFAC_OK;
+  tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, 0, stream>>>(ctx, b);
+  count_launch();
+  for (int k = 0; k < Tmax && rc == KFAC_OK; ++k) {
+    tc_prep_diag_kernel<<<dim3((unsigned)Tmax, n), 128, diag_smem_bytes<float>(), stream>>>(ctx, b, k);
+    count_launch();
+    rc = launch_it<kItPanel>(prm, Ts, n, k, sms, stream);
+    if (rc == KFAC_OK) rc = launch_it<kItUpdate>(prm, Ts, n, k, sms, stream);
+  }
+  if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, stream);
+  if (rc == KFAC_OK && ctx.want_rowsum) {
+    tc_probe_kernel<<<dim3(64, n), 256, 0, stream>>>(ctx, n);
+    count_launch();
+  }
+  delete prm;
+  if (rc == KFAC_OK && cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
+  return rc;
+}
+
+}  // namespace kfac
