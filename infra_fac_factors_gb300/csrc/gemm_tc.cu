@@ -278,16 +278,25 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
 }
 
 // ------------------------------------------------------------------ fp32 -> bf16 slices
+constexpr int kSplitChunk = 2048;  // work items (8 values each) per block iteration
+
 __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitParams prm) {
-  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long nth = (long long)gridDim.x * blockDim.x;
-  // work item = 8 consecutive columns of one row
-  for (long long g = tid; g < prm.total_items; g += nth) {
-    int pi = 0;
-    while (pi + 1 < prm.n && prm.items[pi + 1].item_begin <= g) ++pi;
-    const SplitItem& it = prm.items[pi];
-    const long long local = g - it.item_begin;
+  // work item = 8 consecutive columns of one row; chunks of kSplitChunk work
+  // items never straddle two matrices, so the matrix lookup is block-uniform
+  for (long long ch = blockIdx.x; ch < prm.total_items; ch += gridDim.x) {
+    int lo = 0, hi = prm.n;  // matrix with item_begin (in chunks) <= ch
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prm.items[mid].item_begin <= ch)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const SplitItem& it = prm.items[lo];
     const long long per_row = (it.cols + 7) / 8;
+    const long long work = it.rows * per_row;
+    const long long w0 = (ch - it.item_begin) * kSplitChunk;
+    for (long long local = w0 + threadIdx.x; local < w0 + kSplitChunk && local < work; local += blockDim.x) {
     const long long r = local / per_row;
     const long long c0 = (local % per_row) * 8;
     const float* src = it.src + r * it.ld_src + c0;
@@ -302,6 +311,7 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
       for (int e = 0; e < 8; ++e) x[e] = (c0 + e < it.cols) ? src[e] : 0.f;
     }
     split8_store(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
+    }
   }
 }
 
@@ -346,14 +356,15 @@ int launch_split(const SplitItem* items, int n, cudaStream_t stream) {
     long long total = 0;
     for (int i = 0; i < cnt; ++i) {
       prm.items[i] = items[base + i];
-      prm.items[i].item_begin = total;
-      total += prm.items[i].rows * ((prm.items[i].cols + 7) / 8);
+      prm.items[i].item_begin = total;  // in chunks of kSplitChunk work items
+      const long long work = prm.items[i].rows * ((prm.items[i].cols + 7) / 8);
+      total += (work + kSplitChunk - 1) / kSplitChunk;
     }
     prm.n = cnt;
     prm.total_items = total;
     if (total == 0) continue;
-    const long long want = (total + 255) / 256, cap = (long long)sms * 16;
-    split_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(prm);
+    const long long cap = (long long)sms * 8;
+    split_kernel<<<(unsigned)(total < cap ? total : cap), 256, 0, stream>>>(prm);
     count_launch();
     if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
   }

@@ -20,10 +20,10 @@
 //     to it (refine = AUTO) or for all of them (refine = ALWAYS).
 //
 // refine = AUTO: the fp32 pass measures its own residual.  With kProbes
-// Rademacher vectors v (+-1 entries), w = D v is accumulated in fp64 while D
-// is loaded, and y = X w while X is written, so ||y - v||^2 averaged over the
-// probes is an unbiased estimate of ||X D - I||_F^2 at no extra HBM traffic
-// (products of fp32 values are exact in fp64).  Matrices whose estimated
+// Rademacher vectors v (+-1 entries), w = D v and then y = X w are formed in
+// double-float arithmetic (fp32 pairs, ~48 bits), so ||y - v||^2 averaged over
+// the probes is an unbiased estimate of ||X D - I||_F^2 (inverse_tc.cu:
+// tc_norms_kernel, tc_probe_kernel).  Matrices whose estimated
 // residual ||X D - I||_F / sqrt(d) exceeds 2.5e-4 (four times below the 1e-3
 // target), whose ||D||_1 / min L_jj^2 exceeds 3e5 (a guard on the relative
 // error), or whose fp32 factorisation failed, are redone in fp64; the fp64
@@ -38,93 +38,103 @@
 namespace kfac {
 
 // ------------------------------------------------------------------ setup
-__global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, uint8_t* ws, InvMat* mats, InvState* st,
-                                 float* rowsum, double* probe) {
+__global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, InvCtx c) {
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nth = (long long)gridDim.x * blockDim.x;
+  const bool all64 = prm.mode == KFAC_REFINE_ALWAYS;
   for (long long e = tid; e < prm.n; e += nth) {
-    mats[e] = prm.mats[e];
+    const_cast<InvMat*>(c.mats)[e] = prm.mats[e];
     InvState s;
     s.info32 = 0;
     s.info64 = 0;
     s.failed = 0;
-    s.use64 = prm.mode == KFAC_REFINE_ALWAYS ? 1 : 0;
+    s.use64 = all64 ? 1 : 0;
     s.min_piv = 3.0e38f;
     s.kappa = 0.f;
     s.xnorm2 = 0.f;
     s.est_res = 0.f;
-    st[e] = s;
+    c.st[e] = s;
+    c.flagged[e] = (int)e;
   }
-  for (long long e = tid; e < prm.rowsum_total; e += nth) rowsum[e] = 0.f;
-  for (long long e = tid; e < prm.probe_total; e += nth) probe[e] = 0.0;
+  if (tid == 0) *c.nflagged = all64 ? prm.n : 0;
+  for (long long e = tid; e < prm.rowsum_total; e += nth) c.rowsum[e] = 0.f;
+  for (long long e = tid; e < prm.probe_total; e += nth) c.probe[e] = make_float2(0.f, 0.f);
 }
+
+// The fp64 pass kernels run a persistent 1-D grid over the matrices in the
+// flagged list (tiles of one matrix spread over the grid), so that when the
+// fp32 pass routes nothing to fp64 every launch ends at once.
 
 // ------------------------------------------------------------------ fp64 pass: load D into the L-buffer
 template <typename T>
 __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
-  const int mi = blockIdx.y;
-  if (!inv_active(c, mi, false)) return;
-  const InvMat m = c.mats[mi];
-  const long long q = blockIdx.x;
-  if (q >= tri(m.T)) return;
-  if (threadIdx.x == 0) c.st[mi].failed = 0;
-  const int R = tri_root(q), C = (int)(q - tri(R));  // lower tile (R, C), R >= C
-  const long long np = (long long)m.T * 128;
-  T* L = lbuf<T>(c, m);
   __shared__ float sub[32][33];
+  const int nf = *c.nflagged;
   const int lx = threadIdx.x % 32, ly = threadIdx.x / 32;  // 32 x 8
-  for (int sb = 0; sb < 16; ++sb) {
-    const int bm = (sb / 4) * 32, bn = (sb % 4) * 32;  // sub-block rows (mm) / cols (nn) of the L tile
-    // read D[C*128 + bn + y][R*128 + bm + x] (coalesced along x), store sub[y][x]
-    for (int y = ly; y < 32; y += 8) {
-      const long long gc = (long long)C * 128 + bn + y;   // D row   = L column
-      const long long gr = (long long)R * 128 + bm + lx;  // D column = L row
-      float v = 0.f;
-      if (gc < m.d && gr < m.d && gr >= gc) v = m.D[gc * m.ld_in + gr];
-      sub[y][lx] = v;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = c.flagged[f];
+    const InvMat m = c.mats[mi];
+    const long long np = (long long)m.T * 128;
+    T* L = lbuf<T>(c, m);
+    for (long long q = blockIdx.x; q < tri(m.T); q += gridDim.x) {
+      const int R = tri_root(q), C = (int)(q - tri(R));  // lower tile (R, C), R >= C
+      for (int sb = 0; sb < 16; ++sb) {
+        const int bm = (sb / 4) * 32, bn = (sb % 4) * 32;  // sub-block rows (mm) / cols (nn) of the L tile
+        // read D[C*128 + bn + y][R*128 + bm + x] (coalesced along x), store sub[y][x]
+        for (int y = ly; y < 32; y += 8) {
+          const long long gc = (long long)C * 128 + bn + y;   // D row   = L column
+          const long long gr = (long long)R * 128 + bm + lx;  // D column = L row
+          float v = 0.f;
+          if (gc < m.d && gr < m.d && gr >= gc) v = m.D[gc * m.ld_in + gr];
+          sub[y][lx] = v;
+        }
+        __syncthreads();
+        for (int y = ly; y < 32; y += 8) {
+          const long long gr = (long long)R * 128 + bm + y;
+          const long long gc = (long long)C * 128 + bn + lx;
+          T out;
+          if (gr >= m.d || gc >= m.d)
+            out = (gr == gc) ? T(1) : T(0);
+          else if (gr < gc)
+            out = T(0);
+          else
+            out = (T)sub[lx][y] + ((gr == gc) ? (T)c.gamma_extra : T(0));
+          L[gr * np + gc] = out;
+        }
+        __syncthreads();
+      }
     }
-    __syncthreads();
-    for (int y = ly; y < 32; y += 8) {
-      const long long gr = (long long)R * 128 + bm + y;
-      const long long gc = (long long)C * 128 + bn + lx;
-      T out;
-      if (gr >= m.d || gc >= m.d)
-        out = (gr == gc) ? T(1) : T(0);
-      else if (gr < gc)
-        out = T(0);
-      else
-        out = (T)sub[lx][y] + ((gr == gc) ? (T)c.gamma_extra : T(0));
-      L[gr * np + gc] = out;
-    }
-    __syncthreads();
   }
 }
 
 // ------------------------------------------------------------------ fp64 pass: diagonal block
 template <typename T>
 __global__ void __launch_bounds__(128) inv_diag_kernel(InvCtx c, int k) {
-  const int mi = blockIdx.y;
-  if (!inv_active(c, mi, true)) return;
-  const InvMat m = c.mats[mi];
-  if (k >= m.T) return;
   extern __shared__ __align__(16) uint8_t diag_smem[];
   T* a = reinterpret_cast<T*>(diag_smem);
-  const long long np = (long long)m.T * 128;
-  const T* src = lbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
+  const int nf = *c.nflagged;
   const int t = threadIdx.x;
-  for (int r = 0; r < 128; ++r) a[r * kDiagPitch + t] = (t <= r) ? src[(long long)r * np + t] : T(0);
-  __syncthreads();
-  T min_piv;
-  const int fail = block_chol_inv<T>(a, m.d - k * 128, min_piv);
-  if (fail >= 0) {
-    if (t == 0) {
-      c.st[mi].failed = 1;
-      c.st[mi].info64 = k * 128 + fail + 1;
+  for (int f = blockIdx.x; f < nf; f += gridDim.x) {
+    const int mi = c.flagged[f];
+    const InvMat m = c.mats[mi];
+    if (k >= m.T || c.st[mi].failed) continue;
+    const long long np = (long long)m.T * 128;
+    const T* src = lbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
+    for (int r = 0; r < 128; ++r) a[r * kDiagPitch + t] = (t <= r) ? src[(long long)r * np + t] : T(0);
+    __syncthreads();
+    T min_piv;
+    const int fail = block_chol_inv<T>(a, m.d - k * 128, min_piv);
+    if (fail >= 0) {
+      if (t == 0) {
+        c.st[mi].failed = 1;
+        c.st[mi].info64 = k * 128 + fail + 1;
+      }
+    } else {
+      T* dst = wbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
+      for (int r = 0; r < 128; ++r) dst[(long long)r * np + t] = (t <= r) ? a[r * kDiagPitch + t] : T(0);
     }
-    return;
+    __syncthreads();
   }
-  T* dst = wbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
-  for (int r = 0; r < 128; ++r) dst[(long long)r * np + t] = (t <= r) ? a[r * kDiagPitch + t] : T(0);
 }
 
 // ------------------------------------------------------------------ tile epilogues
@@ -150,99 +160,106 @@ __device__ __forceinline__ void tile_store(T* dst, long long ld, const T (&acc)[
 // ------------------------------------------------------------------ fp64 pass: panel
 template <typename T>
 __global__ void __launch_bounds__(256) inv_panel_kernel(InvCtx c, int k) {
-  const int mi = blockIdx.y;
-  if (!inv_active(c, mi, true)) return;
-  const InvMat m = c.mats[mi];
-  if (k >= m.T) return;
-  const int nr = m.T - 1 - k;
-  const int q = blockIdx.x;
-  if (q >= nr + k) return;
   __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
-  const long long np = (long long)m.T * 128;
-  T* L = lbuf<T>(c, m);
-  T* W = wbuf<T>(c, m);
-  const T* winv = W + (long long)k * 128 * np + (long long)k * 128;
-  T acc[8][8];
-  zero_acc(acc);
-  if (q < nr) {
-    const int r = k + 1 + q;
-    T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
-    Opnd<T> A{Lrk, np, 1, 128};
-    Opnd<T> B{winv, np, 1, 128};
-    simt_tile<T, T, T>(acc, A, B, 128, smem);
-    tile_store(Lrk, np, acc, 0);
-  } else {
-    const int cc = q - nr;
-    T* Ckc = W + (long long)k * 128 * np + (long long)cc * 128;
-    Opnd<T> A{winv, np, 1, 128};
-    Opnd<T> B{Ckc, 1, np, 128};
-    simt_tile<T, T, T>(acc, A, B, 128, smem);
-    tile_store(Ckc, np, acc, 0);
+  const int nf = *c.nflagged;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = c.flagged[f];
+    const InvMat m = c.mats[mi];
+    if (k >= m.T || c.st[mi].failed) continue;
+    const int nr = m.T - 1 - k;
+    const long long np = (long long)m.T * 128;
+    T* L = lbuf<T>(c, m);
+    T* W = wbuf<T>(c, m);
+    const T* winv = W + (long long)k * 128 * np + (long long)k * 128;
+    for (int q = blockIdx.x; q < nr + k; q += gridDim.x) {
+      T acc[8][8];
+      zero_acc(acc);
+      if (q < nr) {
+        const int r = k + 1 + q;
+        T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
+        Opnd<T> A{Lrk, np, 1, 128};
+        Opnd<T> B{winv, np, 1, 128};
+        simt_tile<T, T, T>(acc, A, B, 128, smem);
+        tile_store(Lrk, np, acc, 0);
+      } else {
+        const int cc = q - nr;
+        T* Ckc = W + (long long)k * 128 * np + (long long)cc * 128;
+        Opnd<T> A{winv, np, 1, 128};
+        Opnd<T> B{Ckc, 1, np, 128};
+        simt_tile<T, T, T>(acc, A, B, 128, smem);
+        tile_store(Ckc, np, acc, 0);
+      }
+    }
   }
 }
 
 // ------------------------------------------------------------------ fp64 pass: trailing update
 template <typename T>
 __global__ void __launch_bounds__(256) inv_update_kernel(InvCtx c, int k) {
-  const int mi = blockIdx.y;
-  if (!inv_active(c, mi, true)) return;
-  const InvMat m = c.mats[mi];
-  if (k + 1 >= m.T) return;
-  const long long q = blockIdx.x;
-  if (q >= tri(m.T) - tri(k + 1)) return;
-  const long long qq = q + tri(k + 1);
-  const int r = tri_root(qq);
-  const int cc = (int)(qq - tri(r));
   __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
-  const long long np = (long long)m.T * 128;
-  T* L = lbuf<T>(c, m);
-  T* W = wbuf<T>(c, m);
-  const T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
-  T acc[8][8];
-  zero_acc(acc);
-  Opnd<T> A{Lrk, np, 1, 128};
-  if (cc > k) {
-    Opnd<T> B{L + (long long)cc * 128 * np + (long long)k * 128, np, 1, 128};
-    simt_tile<T, T, T>(acc, A, B, 128, smem);
-    tile_store(L + (long long)r * 128 * np + (long long)cc * 128, np, acc, 1);
-  } else {
-    Opnd<T> B{W + (long long)k * 128 * np + (long long)cc * 128, 1, np, 128};
-    simt_tile<T, T, T>(acc, A, B, 128, smem);
-    tile_store(W + (long long)r * 128 * np + (long long)cc * 128, np, acc, cc == k ? 2 : 1);
+  const int nf = *c.nflagged;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = c.flagged[f];
+    const InvMat m = c.mats[mi];
+    if (k + 1 >= m.T || c.st[mi].failed) continue;
+    const long long np = (long long)m.T * 128;
+    T* L = lbuf<T>(c, m);
+    T* W = wbuf<T>(c, m);
+    for (long long q = blockIdx.x; q < tri(m.T) - tri(k + 1); q += gridDim.x) {
+      const long long qq = q + tri(k + 1);
+      const int r = tri_root(qq);
+      const int cc = (int)(qq - tri(r));
+      const T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
+      T acc[8][8];
+      zero_acc(acc);
+      Opnd<T> A{Lrk, np, 1, 128};
+      if (cc > k) {
+        Opnd<T> B{L + (long long)cc * 128 * np + (long long)k * 128, np, 1, 128};
+        simt_tile<T, T, T>(acc, A, B, 128, smem);
+        tile_store(L + (long long)r * 128 * np + (long long)cc * 128, np, acc, 1);
+      } else {
+        Opnd<T> B{W + (long long)k * 128 * np + (long long)cc * 128, 1, np, 128};
+        simt_tile<T, T, T>(acc, A, B, 128, smem);
+        tile_store(W + (long long)r * 128 * np + (long long)cc * 128, np, acc, cc == k ? 2 : 1);
+      }
+    }
   }
 }
 
 // ------------------------------------------------------------------ fp64 pass: X = W^T W
 template <typename T>
 __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
-  const int mi = blockIdx.y;
-  if (!inv_active(c, mi, true)) return;
-  const InvMat m = c.mats[mi];
-  const long long q = blockIdx.x;
-  if (q >= tri(m.T)) return;
-  const int j = tri_root(q);
-  const int i = (int)(q - tri(j));  // i <= j
   __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
-  const long long np = (long long)m.T * 128;
-  const T* W = wbuf<T>(c, m);
-  T acc[8][8];
-  zero_acc(acc);
-  Opnd<T> A{W + (long long)j * 128 * np + (long long)i * 128, 1, np, 128};
-  Opnd<T> B{W + (long long)j * 128 * np + (long long)j * 128, 1, np, 128};
-  simt_tile<T, T, T>(acc, A, B, (int)(np - (long long)j * 128), smem);
+  const int nf = *c.nflagged;
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = c.flagged[f];
+    const InvMat m = c.mats[mi];
+    if (c.st[mi].failed) continue;
+    const long long np = (long long)m.T * 128;
+    const T* W = wbuf<T>(c, m);
+    for (long long q = blockIdx.x; q < tri(m.T); q += gridDim.x) {
+      const int j = tri_root(q);
+      const int i = (int)(q - tri(j));  // i <= j
+      T acc[8][8];
+      zero_acc(acc);
+      Opnd<T> A{W + (long long)j * 128 * np + (long long)i * 128, 1, np, 128};
+      Opnd<T> B{W + (long long)j * 128 * np + (long long)j * 128, 1, np, 128};
+      simt_tile<T, T, T>(acc, A, B, (int)(np - (long long)j * 128), smem);
 #pragma unroll
-  for (int a = 0; a < 8; ++a) {
-    const int mm = ty * 8 + a;
-    const long long row = (long long)i * 128 + mm;
+      for (int a = 0; a < 8; ++a) {
+        const int mm = ty * 8 + a;
+        const long long row = (long long)i * 128 + mm;
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int nn = tx * 8 + b;
-      const long long col = (long long)j * 128 + nn;
-      if (row >= m.d || col >= m.d || (i == j && mm > nn)) continue;
-      const float v = (float)acc[a][b];
-      m.X[row * m.ld_out + col] = v;
-      m.X[col * m.ld_out + row] = v;
+        for (int b = 0; b < 8; ++b) {
+          const int nn = tx * 8 + b;
+          const long long col = (long long)j * 128 + nn;
+          if (row >= m.d || col >= m.d || (i == j && mm > nn)) continue;
+          const float v = (float)acc[a][b];
+          m.X[row * m.ld_out + col] = v;
+          m.X[col * m.ld_out + row] = v;
+        }
+      }
     }
   }
 }
@@ -254,14 +271,15 @@ __global__ void __launch_bounds__(128) inv_flag_kernel(InvCtx c) {
   __shared__ float red[128];
   __shared__ double red2[128];
   const long long np = (long long)m.T * 128;
-  const double* y = c.probe + m.off_probe + (long long)kProbes * np;
+  const float2* y = c.probe + m.off_probe + (long long)kProbes * np;
   float mx = 0.f;
   double e2 = 0.0;  // sum over probes of ||X (D v) - v||^2
   for (int r = threadIdx.x; r < m.d; r += 128) {
     mx = fmaxf(mx, c.rowsum[m.off_rowsum + r]);
 #pragma unroll
     for (int p = 0; p < kProbes; ++p) {
-      const double e = y[p * np + r] - probe_sign(r, p);
+      const float2 yv = y[p * np + r];
+      const double e = df_value(yv.x, yv.y) - probe_sign(r, p);
       e2 += e * e;
     }
   }
@@ -284,6 +302,10 @@ __global__ void __launch_bounds__(128) inv_flag_kernel(InvCtx c) {
     s.kappa = kappa;
     s.est_res = (float)est;
     s.use64 = (s.failed || !(kappa <= kAutoKappa) || !(est <= kAutoResidual)) ? 1 : 0;
+    if (s.use64) {
+      s.failed = 0;  // the fp64 pass starts afresh
+      c.flagged[atomicAdd(c.nflagged, 1)] = mi;
+    }
   }
 }
 
@@ -297,7 +319,7 @@ __global__ void inv_finish_kernel(InvCtx c, int n, int* info, int* route) {
 
 // ------------------------------------------------------------------ host side
 struct InvLayout {
-  size_t mats_off, st_off, rowsum_off, probe_off, region_off, total;
+  size_t mats_off, st_off, flag_off, rowsum_off, probe_off, region_off, total;
   TcLayout tc;
 };
 
@@ -308,7 +330,8 @@ static InvLayout inv_layout(int n, const kfac_inverse_args* args, int refine, lo
   InvLayout L;
   L.mats_off = 0;
   L.st_off = align256(sizeof(InvMat) * (size_t)n);
-  L.rowsum_off = L.st_off + align256(sizeof(InvState) * (size_t)n);
+  L.flag_off = L.st_off + align256(sizeof(InvState) * (size_t)n);
+  L.rowsum_off = L.flag_off + align256(sizeof(int) * (size_t)(n + 1));
   long long rs = 0;
   int Ts[kInvMaxGroup];
   for (int i = 0; i < n; ++i) {
@@ -323,7 +346,7 @@ static InvLayout inv_layout(int n, const kfac_inverse_args* args, int refine, lo
   *rowsum_total = rs;
   *probe_total = 2 * kProbes * rs;
   L.probe_off = L.rowsum_off + align256(sizeof(float) * (size_t)rs);
-  L.region_off = L.probe_off + align256(sizeof(double) * (size_t)(2 * kProbes * rs));
+  L.region_off = L.probe_off + align256(sizeof(float2) * (size_t)(2 * kProbes * rs));
   // the fp32 tensor-core pass and the fp64 pass run one after the other and
   // share the work region
   size_t fp64 = 0;
@@ -351,32 +374,27 @@ size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine) {
   return best;
 }
 
-static int run_fp64_pass(const InvCtx& ctx, int cnt, int Tmax, const int* Ts, cudaStream_t stream) {
+static int run_fp64_pass(const InvCtx& ctx, int Tmax, cudaStream_t stream) {
   const int dsm = diag_smem_bytes<double>();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  const int sms = device_sm_count(dev);
   if (!ensure_smem_attr(dev, (const void*)inv_diag_kernel<double>, dsm)) return KFAC_ERR_CUDA;
-  inv_load_kernel<double><<<dim3((unsigned)tri(Tmax), cnt), 256, 0, stream>>>(ctx);
+  inv_load_kernel<double><<<sms, 256, 0, stream>>>(ctx);
   count_launch();
   for (int k = 0; k < Tmax; ++k) {
-    inv_diag_kernel<double><<<dim3(1, cnt), 128, dsm, stream>>>(ctx, k);
+    inv_diag_kernel<double><<<sms, 128, dsm, stream>>>(ctx, k);
     count_launch();
     if (Tmax > 1) {
-      inv_panel_kernel<double><<<dim3((unsigned)(Tmax - 1), cnt), 256, 0, stream>>>(ctx, k);
+      inv_panel_kernel<double><<<sms, 256, 0, stream>>>(ctx, k);
       count_launch();
-    }
-    long long upd = 0;
-    for (int i = 0; i < cnt; ++i)
-      if (Ts[i] > k + 1) {
-        const long long u = tri(Ts[i]) - tri(k + 1);
-        if (u > upd) upd = u;
+      if (k + 1 < Tmax) {
+        inv_update_kernel<double><<<sms, 256, 0, stream>>>(ctx, k);
+        count_launch();
       }
-    if (upd > 0) {
-      inv_update_kernel<double><<<dim3((unsigned)upd, cnt), 256, 0, stream>>>(ctx, k);
-      count_launch();
     }
   }
-  inv_lauum_kernel<double><<<dim3((unsigned)tri(Tmax), cnt), 256, 0, stream>>>(ctx);
+  inv_lauum_kernel<double><<<sms, 256, 0, stream>>>(ctx);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
@@ -413,8 +431,10 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
     ctx.ws = ws;
     ctx.mats = reinterpret_cast<const InvMat*>(ws + L.mats_off);
     ctx.st = reinterpret_cast<InvState*>(ws + L.st_off);
+    ctx.flagged = reinterpret_cast<int*>(ws + L.flag_off);
+    ctx.nflagged = ctx.flagged + cnt;
     ctx.rowsum = reinterpret_cast<float*>(ws + L.rowsum_off);
-    ctx.probe = reinterpret_cast<double*>(ws + L.probe_off);
+    ctx.probe = reinterpret_cast<float2*>(ws + L.probe_off);
     ctx.region = ws + L.region_off;
     ctx.gamma_extra = gamma_extra;
     ctx.want_rowsum = refine == KFAC_REFINE_AUTO;
@@ -422,8 +442,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
       const long long work = probe_total > cnt ? probe_total : cnt;
       long long blocks = (work + 255) / 256;
       if (blocks > 1024) blocks = 1024;
-      inv_setup_kernel<<<(unsigned)blocks, 256, 0, stream>>>(prm, ws, const_cast<InvMat*>(ctx.mats), ctx.st,
-                                                             ctx.rowsum, ctx.probe);
+      inv_setup_kernel<<<(unsigned)blocks, 256, 0, stream>>>(prm, ctx);
       count_launch();
     }
     int rc;
@@ -439,7 +458,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
     if (refine != KFAC_REFINE_NONE) {
       ctx.pass64 = 1;
       ctx.want_rowsum = 0;
-      rc = run_fp64_pass(ctx, cnt, Tmax, Ts, stream);
+      rc = run_fp64_pass(ctx, Tmax, stream);
       if (rc != KFAC_OK) return rc;
     }
     inv_finish_kernel<<<(cnt + 255) / 256, 256, 0, stream>>>(ctx, cnt, info + base, route ? route + base : nullptr);

@@ -50,12 +50,38 @@ struct InvCtx {
   const InvMat* mats;
   InvState* st;
   float* rowsum;
-  double* probe;  // per matrix: w[kProbes][n_pad] then y[kProbes][n_pad]
+  float2* probe;    // per matrix: w[kProbes][n_pad] then y[kProbes][n_pad], double-float (hi, lo)
+  int* flagged;     // indices of the matrices the fp64 pass inverts
+  int* nflagged;    // their count
   uint8_t* region;  // work buffers of the passes (fp32 tensor-core or fp64)
   float gamma_extra;
   int pass64;       // 0: fp32 pass, 1: fp64 pass
   int want_rowsum;  // fp32 pass of AUTO: record norms and probes
 };
+
+// ------------------------------------------------------------------ double-float sums
+// (hi, lo) += x with the exact rounding error of hi + x carried in lo
+// (Knuth's TwoSum); products of fp32 values by (whi + wlo) keep their exact
+// error through an FMA.  About 48 significant bits with fp32 instructions
+// only (fp64 throughput on this part is a small fraction of fp32).
+__device__ __forceinline__ void df_add(float& hi, float& lo, float x) {
+  const float s = hi + x;
+  const float bb = s - hi;
+  const float e = (hi - (s - bb)) + (x - bb);
+  hi = s;
+  lo += e;
+}
+__device__ __forceinline__ void df_add_prod(float& hi, float& lo, float x, float whi, float wlo) {
+  const float p = x * whi;
+  const float pe = fmaf(x, whi, -p);  // exact error of the product
+  df_add(hi, lo, p);
+  lo += fmaf(x, wlo, pe);
+}
+__device__ __forceinline__ double df_value(float hi, float lo) { return (double)hi + (double)lo; }
+__device__ __forceinline__ float2 df_pack(float hi, float lo) {
+  const float s = hi + lo;  // renormalise so that |lo| <= ulp(hi) / 2
+  return make_float2(s, lo - (s - hi));
+}
 
 // fp64 pass: compact per-matrix buffers in the work region
 template <typename T>

@@ -41,6 +41,7 @@ constexpr int kItOutBlock = 4096;  // one 32 x 32 fp32 block
 constexpr int kItOut = 8 * 2 * kItOutBlock;
 constexpr int kItSmem = kItStages * kItStage + kItOut + 1024 + 256;
 constexpr int kItThreads = 320;
+constexpr int kNormsSmem = (128 * 129 + kProbes * 128) * 4;
 
 enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
 
@@ -409,26 +410,12 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
   const long long q = blockIdx.x;
   if (q >= tri(m.T)) return;
   const int R = tri_root(q), C = (int)(q - tri(R));  // lower tile (R, C), R >= C
-  const long long np = (long long)m.T * 128;
   float* A = b.acc + m.row_off * b.LD;
   __shared__ float sub[32][33];
-  __shared__ float rs_row[128], rs_col[128];
-  __shared__ double pw_row[kProbes][128], pw_col[kProbes][128];  // partial w = D v
-  if (threadIdx.x < 128) {
-    rs_row[threadIdx.x] = 0.f;
-    rs_col[threadIdx.x] = 0.f;
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) pw_row[p][threadIdx.x] = pw_col[p][threadIdx.x] = 0.0;
-  }
-  __syncthreads();
   const int lx = threadIdx.x % 32, ly = threadIdx.x / 32;  // 32 x 8
-  double wcol[4][kProbes];  // partial w for column bn + lx, per column block bn
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) wcol[q4][p] = 0.0;
   for (int sb = 0; sb < 16; ++sb) {
     const int bm = (sb / 4) * 32, bn = (sb % 4) * 32;  // sub-block rows (mm) / cols (nn) of the tile
+    // read D[C*128 + bn + y][R*128 + bm + x] (coalesced along x), store sub[y][x]
     for (int y = ly; y < 32; y += 8) {
       const long long gc = (long long)C * 128 + bn + y;   // D row   = tile column
       const long long gr = (long long)R * 128 + bm + lx;  // D column = tile row
@@ -437,39 +424,17 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
       sub[y][lx] = v;
     }
     __syncthreads();
-    const long long gc = (long long)C * 128 + bn + lx;
-    double vc[kProbes];
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) vc[p] = probe_sign(gc, p);
     for (int y = ly; y < 32; y += 8) {
       const long long gr = (long long)R * 128 + bm + y;
-      const float v = sub[lx][y];
+      const long long gc = (long long)C * 128 + bn + lx;
       float out;
-      bool inside = false;
-      if (gr >= m.d || gc >= m.d) {
+      if (gr >= m.d || gc >= m.d)
         out = (gr == gc) ? 1.f : 0.f;
-      } else if (gr < gc) {
+      else if (gr < gc)
         out = 0.f;
-      } else {
-        out = v + ((gr == gc) ? c.gamma_extra : 0.f);
-        inside = true;
-      }
+      else
+        out = sub[lx][y] + ((gr == gc) ? c.gamma_extra : 0.f);
       A[gr * b.LD + gc] = out;
-      if (c.want_rowsum) {  // uniform over the block
-        const float a = inside ? fabsf(v) : 0.f;
-        float ra = a;
-        for (int o = 16; o > 0; o >>= 1) ra += __shfl_xor_sync(0xffffffffu, ra, o);
-        if (lx == 0) rs_row[bm + y] += ra;  // row bm + y belongs to this warp alone
-        const double x = inside ? (double)out : 0.0;  // the matrix being inverted, as stored
-#pragma unroll
-        for (int p = 0; p < kProbes; ++p) {
-          double s = x * vc[p];
-          for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (lx == 0) pw_row[p][bm + y] += s;
-          if (inside && gr != gc) wcol[bn / 32][p] += x * probe_sign(gr, p);
-        }
-        if (inside && gr != gc) atomicAdd(&rs_col[bn + lx], a);
-      }
     }
     __syncthreads();
   }
@@ -483,55 +448,87 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
       for (int s = 0; s < kSlices; ++s) *reinterpret_cast<uint4*>(dst + s * ss) = make_uint4(0, 0, 0, 0);
     }
   }
-  if (c.want_rowsum) {
+}
+
+// ------------------------------------------------------------------ ||D||_1 and w = D v (AUTO)
+// One CTA per 128-row block R of a matrix: the rows of R gather their sums
+// from the lower tiles (R, C <= R) row-wise and from the tiles (C > R, R)
+// column-wise (D is symmetric), so no atomics are needed.  Double-float sums.
+__global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c, TcBufs b) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, false)) return;
+  const InvMat m = c.mats[mi];
+  const int R = blockIdx.x;
+  if (R >= m.T) return;
+  extern __shared__ __align__(16) uint8_t norms_smem[];
+  float* tile = reinterpret_cast<float*>(norms_smem);  // 128 x 129
+  float* vs = tile + 128 * 129;                        // kProbes x 128 probe signs of the tile's columns
+  const float* A = b.acc + m.row_off * b.LD;
+  const int t = threadIdx.x;
+  float ahi = 0.f, alo = 0.f;  // row abs sum
+  float whi[kProbes], wlo[kProbes];
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-      for (int p = 0; p < kProbes; ++p)
-        if (wcol[q4][p] != 0.0) atomicAdd(&pw_col[p][q4 * 32 + lx], wcol[q4][p]);
+  for (int p = 0; p < kProbes; ++p) whi[p] = wlo[p] = 0.f;
+  const long long r = (long long)R * 128 + t;  // this thread's row (t < 128)
+  for (int C = 0; C < m.T; ++C) {
+    const bool rowwise = C <= R;  // tile (R, C) read along rows; else tile (C, R) along columns
+    const float* src = rowwise ? A + (long long)R * 128 * b.LD + (long long)C * 128
+                               : A + (long long)C * 128 * b.LD + (long long)R * 128;
     __syncthreads();
-    if (threadIdx.x < 128) {
-      const long long gr = (long long)R * 128 + threadIdx.x;
-      const long long gcc = (long long)C * 128 + threadIdx.x;
-      if (gr < m.d && rs_row[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gr], rs_row[threadIdx.x]);
-      if (gcc < m.d && rs_col[threadIdx.x] != 0.f) atomicAdd(&c.rowsum[m.off_rowsum + gcc], rs_col[threadIdx.x]);
-      double* w = c.probe + m.off_probe;
+    for (int e = t; e < 128 * 32; e += 256) {  // 128 rows x 32 float4
+      const int rr = e / 32, c4 = (e % 32) * 4;
+      const float4 v = *reinterpret_cast<const float4*>(src + (long long)rr * b.LD + c4);
+      float* dst = tile + rr * 129 + c4;
+      dst[0] = v.x;
+      dst[1] = v.y;
+      dst[2] = v.z;
+      dst[3] = v.w;
+    }
+    for (int e = t; e < kProbes * 128; e += 256) {
+      const int p = e / 128, i = e % 128;
+      // signs of the entries this row multiplies: the tile's columns (row-wise) or rows (column-wise)
+      vs[p * 128 + i] = (float)probe_sign((long long)C * 128 + i, p);
+    }
+    __syncthreads();
+    if (t < 128 && r < m.d) {
+      for (int i = 0; i < 128; ++i) {
+        const long long cidx = (long long)C * 128 + i;  // the other index of the entry
+        if (cidx >= m.d) break;
+        // row-wise: entry (r, cidx) = tile[t][i] (stored only for cidx <= r within the diagonal tile);
+        // column-wise: entry (cidx, r) = tile[i][t]
+        float x;
+        if (rowwise) {
+          if (C == R && i > t) x = tile[i * 129 + t];  // upper part of the diagonal tile by symmetry
+          else x = tile[t * 129 + i];
+        } else {
+          x = tile[i * 129 + t];
+        }
+        df_add(ahi, alo, fabsf(x));
 #pragma unroll
-      for (int p = 0; p < kProbes; ++p) {
-        if (gr < m.d) atomicAdd(&w[p * np + gr], pw_row[p][threadIdx.x]);
-        if (gcc < m.d) atomicAdd(&w[p * np + gcc], pw_col[p][threadIdx.x]);
+        for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vs[p * 128 + i]);
       }
     }
   }
+  if (t < 128 && r < m.d) {
+    c.rowsum[m.off_rowsum + r] = ahi + alo;
+    const long long np = (long long)m.T * 128;
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) c.probe[m.off_probe + p * np + r] = df_pack(whi[p], wlo[p]);
+  }
 }
 
-// ------------------------------------------------------------------ step k: slices of block column k + diagonal block
-// blockIdx.x == 0: Cholesky and inverse of the diagonal block; blockIdx.x = x >= 1:
-// tile row r (the x-th row other than k) of block column k -> P slices.
-__global__ void __launch_bounds__(128) tc_prep_diag_kernel(InvCtx c, TcBufs b, int k) {
-  const int mi = blockIdx.y;
+// ------------------------------------------------------------------ step k: diagonal block
+// Cholesky and inverse of the diagonal block k: Winv_k rows (the panel's B
+// operand) and U_kk = Winv_k^T, as bf16 slices.
+__global__ void __launch_bounds__(128) tc_diag_kernel(InvCtx c, TcBufs b, int k) {
+  const int mi = blockIdx.x;
   if (!inv_active(c, mi, true)) return;
   const InvMat m = c.mats[mi];
   if (k >= m.T) return;
   const int t = threadIdx.x;
-  const float* A = b.acc + m.row_off * b.LD;
-  if (blockIdx.x > 0) {
-    const int x = blockIdx.x - 1;
-    const int r = x < k ? x : x + 1;
-    if (r >= m.T) return;
-    const float* src = A + ((long long)r * 128 + t) * b.LD + (long long)k * 128;
-    uint16_t* dst = b.p + (m.row_off + (long long)r * 128 + t) * 128;
-    for (int c8 = 0; c8 < 128; c8 += 8) {
-      const float4 u0 = *reinterpret_cast<const float4*>(src + c8);
-      const float4 u1 = *reinterpret_cast<const float4*>(src + c8 + 4);
-      const float x8[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      split8_store(x8, dst + c8, b.R * 128);
-    }
-    return;
-  }
   extern __shared__ __align__(16) uint8_t diag_smem[];
   float* a = reinterpret_cast<float*>(diag_smem);
-  const float* src = A + (long long)k * 128 * b.LD + (long long)k * 128;
+  const float* src = b.acc + (m.row_off + (long long)k * 128) * b.LD + (long long)k * 128;
   for (int r = 0; r < 128; ++r) a[r * kDiagPitch + t] = (t <= r) ? src[(long long)r * b.LD + t] : 0.f;
   __syncthreads();
   float min_piv;
@@ -544,14 +541,13 @@ __global__ void __launch_bounds__(128) tc_prep_diag_kernel(InvCtx c, TcBufs b, i
     return;
   }
   if (t == 0) atomicMin(reinterpret_cast<int*>(&c.st[mi].min_piv), __float_as_int(min_piv));
-  // Winv_k rows (the panel's B operand) and U_kk = Winv_k^T rows, as slices
   uint16_t* wdst = b.winv + ((long long)mi * 128 + t) * 128;
   uint16_t* udst = b.u + (m.row_off + (long long)k * 128 + t) * b.LD + (long long)k * 128;
   for (int c8 = 0; c8 < 128; c8 += 8) {
     float w8[8], u8[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      w8[e] = a[t * kDiagPitch + c8 + e];  // Winv[t][c]  (zero above the diagonal)
+      w8[e] = a[t * kDiagPitch + c8 + e];    // Winv[t][c]  (zero above the diagonal)
       u8[e] = a[(c8 + e) * kDiagPitch + t];  // Winv[c][t]
     }
     split8_store(w8, wdst + c8, (long long)b.n * 128 * 128);
@@ -559,31 +555,76 @@ __global__ void __launch_bounds__(128) tc_prep_diag_kernel(InvCtx c, TcBufs b, i
   }
 }
 
-// ------------------------------------------------------------------ residual probe y = X w, ||X||_F^2
-// one warp per row of X (full symmetric, as written by the lauum step)
-__global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c, int n) {
+// ------------------------------------------------------------------ step k: slices of block column k
+// tile row r (the x-th row other than k) of block column k of Acc -> P slices;
+// a warp per row, coalesced
+__global__ void __launch_bounds__(256) tc_prep_kernel(InvCtx c, TcBufs b, int k) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, true)) return;
+  const InvMat m = c.mats[mi];
+  if (k >= m.T) return;
+  const int x = blockIdx.x;
+  const int r = x < k ? x : x + 1;
+  if (r >= m.T) return;
+  const int lane = threadIdx.x % 32, wq = threadIdx.x / 32;
+  for (int rr = wq; rr < 128; rr += 8) {
+    const float* src = b.acc + (m.row_off + (long long)r * 128 + rr) * b.LD + (long long)k * 128 + lane * 4;
+    const float4 v = *reinterpret_cast<const float4*>(src);
+    uint16_t* dst = b.p + (m.row_off + (long long)r * 128 + rr) * 128 + lane * 4;
+    __nv_bfloat16 s0[kSlices], s1[kSlices], s2[kSlices], s3[kSlices];
+    split_value(v.x, s0);
+    split_value(v.y, s1);
+    split_value(v.z, s2);
+    split_value(v.w, s3);
+#pragma unroll
+    for (int s = 0; s < kSlices; ++s) {
+      __nv_bfloat162 p0, p1;
+      p0.x = s0[s];
+      p0.y = s1[s];
+      p1.x = s2[s];
+      p1.y = s3[s];
+      *reinterpret_cast<uint2*>(dst + s * b.R * 128) =
+          make_uint2(*reinterpret_cast<uint32_t*>(&p0), *reinterpret_cast<uint32_t*>(&p1));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ residual probe y = X w, ||X||_F^2 (AUTO)
+// one warp per row of X (full symmetric, as written by the X = U U^T step),
+// double-float products and sums
+__global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c) {
   const int mi = blockIdx.y;
   if (!inv_active(c, mi, true)) return;
   const InvMat m = c.mats[mi];
   const int lane = threadIdx.x % 32;
   const long long np = (long long)m.T * 128;
-  const double* w = c.probe + m.off_probe;
-  double* y = c.probe + m.off_probe + (long long)kProbes * np;
+  const float2* w = c.probe + m.off_probe;
+  float2* y = c.probe + m.off_probe + (long long)kProbes * np;
   float sq = 0.f;
   for (long long r = (long long)blockIdx.x * 8 + threadIdx.x / 32; r < m.d; r += (long long)gridDim.x * 8) {
-    double acc[kProbes] = {0.0, 0.0, 0.0, 0.0};
+    float hi[kProbes], lo[kProbes];
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) hi[p] = lo[p] = 0.f;
     const float* xr = m.X + r * m.ld_out;
     for (long long col = lane; col < m.d; col += 32) {
       const float v = xr[col];
       sq += v * v;
 #pragma unroll
-      for (int p = 0; p < kProbes; ++p) acc[p] += (double)v * w[p * np + col];
+      for (int p = 0; p < kProbes; ++p) {
+        const float2 wv = w[p * np + col];
+        df_add_prod(hi[p], lo[p], v, wv.x, wv.y);
+      }
     }
 #pragma unroll
     for (int p = 0; p < kProbes; ++p) {
-      double s = acc[p];
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) y[p * np + r] = s;
+      // combine the 32 lanes' double-float partial sums
+      float h = hi[p], l = lo[p];
+      for (int o = 16; o > 0; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, h, o), ol = __shfl_xor_sync(0xffffffffu, l, o);
+        df_add(h, l, oh);
+        l += ol;
+      }
+      if (lane == 0) y[p * np + r] = df_pack(h, l);
     }
   }
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
@@ -684,7 +725,8 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   if (!ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItPanel>, kItSmem) ||
       !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItUpdate>, kItSmem) ||
       !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItLauum>, kItSmem) ||
-      !ensure_smem_attr(dev, (const void*)tc_prep_diag_kernel, diag_smem_bytes<float>()))
+      !ensure_smem_attr(dev, (const void*)tc_diag_kernel, diag_smem_bytes<float>()) ||
+      !ensure_smem_attr(dev, (const void*)tc_norms_kernel, kNormsSmem))
     return KFAC_ERR_CUDA;
   int* status = device_status_ptr();
   if (!status) return KFAC_ERR_CUDA;
@@ -731,15 +773,23 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   int rc = KFAC_OK;
   tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, 0, stream>>>(ctx, b);
   count_launch();
-  for (int k = 0; k < Tmax && rc == KFAC_OK; ++k) {
-    tc_prep_diag_kernel<<<dim3((unsigned)Tmax, n), 128, diag_smem_bytes<float>(), stream>>>(ctx, b, k);
+  if (ctx.want_rowsum) {
+    tc_norms_kernel<<<dim3((unsigned)Tmax, n), 256, kNormsSmem, stream>>>(ctx, b);
     count_launch();
+  }
+  for (int k = 0; k < Tmax && rc == KFAC_OK; ++k) {
+    tc_diag_kernel<<<n, 128, diag_smem_bytes<float>(), stream>>>(ctx, b, k);
+    count_launch();
+    if (Tmax > 1) {
+      tc_prep_kernel<<<dim3((unsigned)(Tmax - 1), n), 256, 0, stream>>>(ctx, b, k);
+      count_launch();
+    }
     rc = launch_it<kItPanel>(prm, Ts, n, k, sms, stream);
     if (rc == KFAC_OK) rc = launch_it<kItUpdate>(prm, Ts, n, k, sms, stream);
   }
   if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, stream);
   if (rc == KFAC_OK && ctx.want_rowsum) {
-    tc_probe_kernel<<<dim3(64, n), 256, 0, stream>>>(ctx, n);
+    tc_probe_kernel<<<dim3(64, n), 256, 0, stream>>>(ctx);
     count_launch();
   }
   delete prm;
