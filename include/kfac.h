@@ -195,6 +195,23 @@ size_t kfac_precondition_workspace(int n, const kfac_precond_args* args);
 int kfac_precondition(int n, const kfac_precond_args* args, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* The same preconditioning with no caller-provided workspace and no device
+ * allocation, for callers that cannot allocate device memory (their device
+ * memory is owned by another allocator, or their hot path must not allocate:
+ * cudaMalloc can synchronise the device and can fail).  The paper has no
+ * counterpart; this is a property of the library.
+ * The scratch is a fixed array inside the library of
+ * kfac_precondition_static_capacity() bytes (64 MiB), held by every GPU that
+ * loads the library until the process exits.  A call whose
+ * kfac_precondition_workspace() exceeds it returns KFAC_ERR_WORKSPACE before
+ * any launch.  The first call on a device looks up the array's address on
+ * that device (cudaGetSymbolAddress), so make it before any stream capture.
+ * All calls share the array and it keeps the last call's contents; calls that
+ * overlap on the GPU (e.g. on two streams at once) race.  Otherwise as
+ * kfac_precondition.                                                         */
+size_t kfac_precondition_static_capacity(void);
+int kfac_precondition_static(int n, const kfac_precond_args* args, void* stream);
+
 /* ------------------------------------------------------------- index tables
  * The work units kfac_factors uses to cover the upper tiles of a d x d factor
  * on the tensor-core path: for every 128-row block i, the columns

@@ -18,7 +18,8 @@ __all__ = [
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status",
     "kfac_factors", "kfac_spatial_sum", "kfac_update_running",
     "kfac_damped_inverse_workspace", "kfac_damped_inverse",
-    "kfac_precondition_workspace", "kfac_precondition", "kfac_factor_tile_map",
+    "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
+    "kfac_precondition_static", "kfac_factor_tile_map",
 ]
 
 KFAC_OK, KFAC_ERR_INVALID_ARG, KFAC_ERR_NOT_SPD, KFAC_ERR_CUDA = 0, 1, 2, 3
@@ -54,7 +55,8 @@ class kfac_precond_args(C.Structure):
 exported_symbols = (
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_factors", "kfac_spatial_sum",
     "kfac_update_running", "kfac_damped_inverse_workspace", "kfac_damped_inverse",
-    "kfac_precondition_workspace", "kfac_precondition", "kfac_factor_tile_map",
+    "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
+    "kfac_precondition_static", "kfac_factor_tile_map",
 )
 
 _lib = None
@@ -86,6 +88,8 @@ def lib() -> C.CDLL:
                                           C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
         "kfac_precondition_workspace": (C.c_size_t, [C.c_int, P(kfac_precond_args)]),
         "kfac_precondition": (C.c_int, [C.c_int, P(kfac_precond_args), C.c_void_p, C.c_size_t, C.c_void_p]),
+        "kfac_precondition_static_capacity": (C.c_size_t, []),
+        "kfac_precondition_static": (C.c_int, [C.c_int, P(kfac_precond_args), C.c_void_p]),
         "kfac_factor_tile_map": (C.c_int, [C.c_int64, C.c_int64, P(C.c_int32), P(C.c_int64), P(C.c_int32),
                                            P(C.c_int64)]),
     }
@@ -173,6 +177,17 @@ def kfac_precondition(args, workspace: int, workspace_bytes: int, stream: int = 
     n, a = _arr(kfac_precond_args, args)
     st = lib().kfac_precondition(n, a, workspace, workspace_bytes, stream)
     return _check("kfac_precondition", st) if check else st
+
+
+def kfac_precondition_static_capacity() -> int:
+    return int(lib().kfac_precondition_static_capacity())
+
+
+def kfac_precondition_static(args, stream: int = 0, check: bool = True) -> int:
+    """kfac_precondition with the library's own fixed scratch (no workspace, no allocation)."""
+    n, a = _arr(kfac_precond_args, args)
+    st = lib().kfac_precondition_static(n, a, stream)
+    return _check("kfac_precondition_static", st) if check else st
 
 
 def kfac_factor_tile_map(d: int):
