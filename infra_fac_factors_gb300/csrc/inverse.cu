@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
 
 // ------------------------------------------------------------------ fp64 pass: diagonal block
 template <typename T>
-__global__ void __launch_bounds__(128) inv_diag_kernel(InvCtx c, int k) {
+__global__ void __launch_bounds__(256, 1) inv_diag_kernel(InvCtx c, int k) {
   extern __shared__ __align__(16) uint8_t diag_smem[];
   T* a = reinterpret_cast<T*>(diag_smem);
   const int nf = *c.nflagged;
@@ -120,7 +120,10 @@ __global__ void __launch_bounds__(128) inv_diag_kernel(InvCtx c, int k) {
     if (k >= m.T || c.st[mi].failed) continue;
     const long long np = (long long)m.T * 128;
     const T* src = lbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
-    for (int r = 0; r < 128; ++r) a[r * kDiagPitch + t] = (t <= r) ? src[(long long)r * np + t] : T(0);
+    for (int e = t; e < 128 * 128; e += blockDim.x) {
+      const int r = e / 128, col = e % 128;
+      a[r * kDiagPitch + col] = (col <= r) ? src[(long long)r * np + col] : T(0);
+    }
     __syncthreads();
     T min_piv;
     const int fail = block_chol_inv<T>(a, m.d - k * 128, min_piv);
@@ -131,7 +134,10 @@ __global__ void __launch_bounds__(128) inv_diag_kernel(InvCtx c, int k) {
       }
     } else {
       T* dst = wbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
-      for (int r = 0; r < 128; ++r) dst[(long long)r * np + t] = (t <= r) ? a[r * kDiagPitch + t] : T(0);
+      for (int e = t; e < 128 * 128; e += blockDim.x) {
+        const int r = e / 128, col = e % 128;
+        dst[(long long)r * np + col] = (col <= r) ? a[r * kDiagPitch + col] : T(0);
+      }
     }
     __syncthreads();
   }
@@ -383,7 +389,7 @@ static int run_fp64_pass(const InvCtx& ctx, int Tmax, cudaStream_t stream) {
   inv_load_kernel<double><<<sms, 256, 0, stream>>>(ctx);
   count_launch();
   for (int k = 0; k < Tmax; ++k) {
-    inv_diag_kernel<double><<<sms, 128, dsm, stream>>>(ctx, k);
+    inv_diag_kernel<double><<<sms, 256, dsm, stream>>>(ctx, k);
     count_launch();
     if (Tmax > 1) {
       inv_panel_kernel<double><<<sms, 256, 0, stream>>>(ctx, k);

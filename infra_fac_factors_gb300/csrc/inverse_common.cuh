@@ -110,12 +110,16 @@ __device__ __forceinline__ int tri_root(long long q) {
   return r;
 }
 
-template <typename T>
-__device__ __forceinline__ T dev_sqrt(T v);
-template <>
-__device__ __forceinline__ float dev_sqrt<float>(float v) { return __fsqrt_rn(v); }
-template <>
-__device__ __forceinline__ double dev_sqrt<double>(double v) { return sqrt(v); }
+// ljj = sqrt(piv) and inv = 1 / ljj of a Cholesky pivot; fp32 through the
+// reciprocal square root (a few ulp, far inside the fp32 pass's error budget)
+__device__ __forceinline__ void pivot_scale(float piv, float& ljj, float& inv) {
+  inv = rsqrtf(piv);
+  ljj = piv * inv;
+}
+__device__ __forceinline__ void pivot_scale(double piv, double& ljj, double& inv) {
+  ljj = sqrt(piv);
+  inv = 1.0 / ljj;
+}
 template <typename T>
 __device__ __forceinline__ T dev_rcp(T v);
 template <>
@@ -129,55 +133,184 @@ constexpr int diag_smem_bytes() {
   return 128 * kDiagPitch * (int)sizeof(T);
 }
 
+// Per-thread share of one warp's product tile, accumulated in registers:
+// rows (lane / 16) * RH + i (i < RH) and columns 2 * (lane % 16) + e (e < 2) of
+// C += A B, with A(r, q) = A[r * lda + q] and B(q, c) = B[q * bq + c * bc],
+// q in [0, K).  Both operands are in shared memory; with the 129-element
+// pitch of the diagonal block the reads are free of bank conflicts.
+template <typename T, int RH>
+__device__ __forceinline__ void warp_tile_mm(T (&acc)[RH][2], const T* A, int lda, const T* B, int bq, int bc,
+                                             int K) {
+  const int lane = threadIdx.x % 32;
+  const T* a0 = A + (lane / 16) * RH * lda;
+  const T* b0 = B + 2 * (lane % 16) * bc;
+#pragma unroll 4
+  for (int q = 0; q < K; ++q) {  // K is a multiple of 32
+    const T b_0 = b0[q * bq], b_1 = b0[q * bq + bc];
+#pragma unroll
+    for (int i = 0; i < RH; ++i) {
+      const T av = a0[i * lda + q];
+      acc[i][0] += av * b_0;
+      acc[i][1] += av * b_1;
+    }
+  }
+}
+
+template <typename T, int RH>
+__device__ __forceinline__ void zero_tile(T (&acc)[RH][2]) {
+#pragma unroll
+  for (int i = 0; i < RH; ++i) acc[i][0] = acc[i][1] = T(0);
+}
+
 // Cholesky factor and inverse of one 128 x 128 diagonal block held in shared
 // memory (`a`, pitch kDiagPitch, lower triangle valid, upper triangle zero),
-// 128 threads.  On return `a` holds Winv = L^-1 (lower, zeros above) and the
-// result is -1, or the block column of the first non-positive pivot.
+// called by all threads of a 256-thread block.  On return `a` holds
+// Winv = L^-1 (lower, zeros above) and the result is -1, or the column of the
+// first non-positive (or NaN) pivot, in which case `a` is partly overwritten.
 // `min_piv` receives the smallest pivot among the first `valid` columns.
+//
+// Blocked by 32 columns.  For each panel one warp factors the 32 x 32
+// diagonal block in registers (lane i holds row i; columns travel by warp
+// shuffles) and inverts it (lane c forms column c of the inverse); then all
+// warps solve the rows below against that inverse and subtract the panel's
+// contribution from the trailing lower triangle.  The inverse of the whole
+// block is then assembled in place from the four diagonal inverses, block
+// column by block column from the right:  W_ij = -(sum_{j<k<=i} W_ik L_kj) W_jj.
 template <typename T>
 __device__ int block_chol_inv(T* a, int valid, T& min_piv) {
-  const int t = threadIdx.x;
-  // Cholesky, right-looking; column j is scaled by 1/sqrt(pivot) one iteration
-  // later, when no thread reads it any more, so each column costs one barrier.
-  int fail = -1;
-  min_piv = T(3.0e38);
-  T prev_rs = T(0);
-  for (int j = 0; j < 128; ++j) {
-    const T piv = a[j * kDiagPitch + j];
-    if (!(piv > T(0))) {  // also catches NaN
-      fail = j;
-      break;
+  constexpr int P = kDiagPitch;
+  __shared__ T wd[4][32][33];  // inverses of the four 32 x 32 diagonal factors
+  __shared__ T tmp[96][33];    // partial products of the assembly step
+  __shared__ int s_fail;
+  __shared__ T s_minpiv;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, nwarps = blockDim.x / 32;
+  if (tid == 0) {
+    s_fail = -1;
+    s_minpiv = T(3.0e38);
+  }
+  __syncthreads();
+  for (int p = 0; p < 4; ++p) {
+    const int p0 = 32 * p;
+    if (warp == 0) {
+      T x[32];  // row p0 + lane of the diagonal block
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[c] = (c <= lane) ? a[(p0 + lane) * P + p0 + c] : T(0);
+      int fail = -1;  // uniform over the warp: every pivot is a broadcast
+      T mp = T(3.0e38);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const T piv = __shfl_sync(0xffffffffu, x[j], j);
+        if (fail < 0 && !(piv > T(0))) fail = j;
+        if (fail < 0) {
+          if (p0 + j < valid && piv < mp) mp = piv;
+          T ljj, inv;
+          pivot_scale(piv, ljj, inv);
+          if (lane > j) x[j] *= inv;
+          if (lane == j) x[j] = ljj;
+#pragma unroll
+          for (int c = j + 1; c < 32; ++c) {
+            const T lcj = __shfl_sync(0xffffffffu, x[j], c);
+            if (lane >= c) x[c] -= x[j] * lcj;
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) a[(p0 + lane) * P + p0 + c] = (c <= lane) ? x[c] : T(0);
+      __syncwarp();
+      if (lane == 0) {
+        if (fail >= 0) s_fail = p0 + fail;
+        if (mp < s_minpiv) s_minpiv = mp;
+      }
+      if (fail < 0) {
+        // column `lane` of the inverse, forward substitution against e_lane
+        T w[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) w[r] = (r == lane) ? T(1) : T(0);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          w[q] *= dev_rcp<T>(a[(p0 + q) * P + p0 + q]);
+#pragma unroll
+          for (int r = q + 1; r < 32; ++r) w[r] -= a[(p0 + r) * P + p0 + q] * w[q];
+        }
+#pragma unroll
+        for (int r = 0; r < 32; ++r) wd[p][r][lane] = w[r];
+      }
     }
-    if (j < valid && piv < min_piv) min_piv = piv;
-    if (j > 0) {
-      const int r = j + t;  // rows j .. 127 of column j-1
-      if (r < 128) a[r * kDiagPitch + (j - 1)] *= prev_rs;
-      if (t == 0) a[(j - 1) * kDiagPitch + (j - 1)] = dev_sqrt<T>(a[(j - 1) * kDiagPitch + (j - 1)]);
+    __syncthreads();
+    if (s_fail >= 0) return s_fail;
+    const int nbt = 3 - p;  // 32-row blocks below the panel
+    if (nbt == 0) break;
+    // rows below the panel: L(r, panel) = A(r, panel) W_pp^T, 16-row items,
+    // each warp reads and then overwrites only its own rows
+    for (int it = warp; it < 2 * nbt; it += nwarps) {
+      const int r0 = p0 + 32 + 16 * it;
+      T acc[8][2];
+      zero_tile(acc);
+      warp_tile_mm<T, 8>(acc, a + r0 * P + p0, P, &wd[p][0][0], 1, 33, 32);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        T* row = a + (r0 + (lane / 16) * 8 + i) * P + p0 + 2 * (lane % 16);
+        row[0] = acc[i][0];
+        row[1] = acc[i][1];
+      }
     }
-    const T ip = dev_rcp<T>(piv);
-    prev_rs = dev_rcp<T>(dev_sqrt<T>(piv));
-    const int col = t;
-    if (col > j) {
-      const T f = a[col * kDiagPitch + j] * ip;
-      for (int r = col; r < 128; ++r) a[r * kDiagPitch + col] -= a[r * kDiagPitch + j] * f;
+    __syncthreads();
+    // trailing lower triangle: A(r, c) -= L(r, panel) L(c, panel)^T, 32 x 32 tiles
+    for (int it = warp; it < nbt * (nbt + 1) / 2; it += nwarps) {
+      int bi = 0;
+      while ((bi + 1) * (bi + 2) / 2 <= it) ++bi;
+      const int bj = it - bi * (bi + 1) / 2;
+      const int r0 = p0 + 32 + 32 * bi, c0 = p0 + 32 + 32 * bj;
+      T acc[16][2];
+      zero_tile(acc);
+      warp_tile_mm<T, 16>(acc, a + r0 * P + p0, P, a + c0 * P + p0, 1, P, 32);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = (lane / 16) * 16 + i, c = 2 * (lane % 16);
+        T* row = a + (r0 + r) * P + c0 + c;
+        if (bi != bj || c <= r) row[0] -= acc[i][0];
+        if (bi != bj || c + 1 <= r) row[1] -= acc[i][1];
+      }
     }
     __syncthreads();
   }
-  if (fail >= 0) return fail;
-  // last column: only its diagonal is left
-  if (t == 0) a[127 * kDiagPitch + 127] = dev_sqrt<T>(a[127 * kDiagPitch + 127]);
+  min_piv = s_minpiv;
+  // the diagonal factors are no longer read: put their inverses in their place
+  for (int e = tid; e < 4 * 32 * 32; e += blockDim.x) {
+    const int p = e / 1024, r = (e / 32) % 32, c = e % 32;
+    a[(32 * p + r) * P + 32 * p + c] = (c <= r) ? wd[p][r][c] : T(0);
+  }
   __syncthreads();
-  // In-place inverse of the lower-triangular block, column by column from the
-  // right: W_jj = 1/L_jj, W_rj = -(sum_{j<s<=r} W_rs L_sj) / L_jj.
-  for (int j = 127; j >= 0; --j) {
-    const T ljj = a[j * kDiagPitch + j];
-    T s = T(0);
-    const int r = t;
-    if (r > j)
-      for (int q = j + 1; q <= r; ++q) s += a[r * kDiagPitch + q] * a[q * kDiagPitch + j];
-    __syncthreads();
-    if (r > j) a[r * kDiagPitch + j] = -s / ljj;
-    if (r == j) a[j * kDiagPitch + j] = dev_rcp<T>(ljj);
+  for (int j = 2; j >= 0; --j) {
+    const int rb = 32 * (j + 1);   // first row below the diagonal block j
+    const int items = 2 * (3 - j);  // 16-row items
+    for (int it = warp; it < items; it += nwarps) {
+      const int r0 = rb + 16 * it, i = r0 / 32;
+      T acc[8][2];
+      zero_tile(acc);
+      // sum over k in (j, i] of W_ik L_kj; W_ik sits in a already (k > j)
+      warp_tile_mm<T, 8>(acc, a + r0 * P + rb, P, a + rb * P + 32 * j, P, 1, 32 * (i - j));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        T* row = &tmp[r0 - rb + (lane / 16) * 8 + q][2 * (lane % 16)];
+        row[0] = acc[q][0];
+        row[1] = acc[q][1];
+      }
+    }
+    __syncthreads();  // every L_kj of this block column has been read
+    for (int it = warp; it < items; it += nwarps) {
+      const int r0 = rb + 16 * it;
+      T acc[8][2];
+      zero_tile(acc);
+      warp_tile_mm<T, 8>(acc, &tmp[r0 - rb][0], 33, &wd[j][0][0], 33, 1, 32);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        T* row = a + (r0 + (lane / 16) * 8 + q) * P + 32 * j + 2 * (lane % 16);
+        row[0] = -acc[q][0];
+        row[1] = -acc[q][1];
+      }
+    }
     __syncthreads();
   }
   return -1;

@@ -17,7 +17,8 @@
 //   Acc   fp32 [R][LD]  lower blocks: A (Schur complements), upper blocks: C'
 //   U     bf16 [3][R][LD]   slices of U
 //   P     bf16 [3][R][128]  slices of block column k of Acc (the panel inputs)
-//   Lp    bf16 [3][R][128]  slices of L_rk, the current panel column
+//   Lp    bf16 [3][R][kOuter * 128]  slices of L_rj for the block columns j
+//                                     of the current outer panel (see kOuter)
 //   Winv  bf16 [3][n*128][128]
 // so that one tensor map per buffer serves every matrix.  Updates land in Acc
 // through TMA add-reductions (no read-modify-write in the kernel).
@@ -41,9 +42,20 @@ constexpr int kItOutBlock = 4096;  // one 32 x 32 fp32 block
 constexpr int kItOut = 8 * 2 * kItOutBlock;
 constexpr int kItSmem = kItStages * kItStage + kItOut + 1024 + 256;
 constexpr int kItThreads = 320;
-constexpr int kNormsSmem = (128 * 129 + kProbes * 128) * 4;
+constexpr int kNormsXch = 1 + 2 * kProbes;
+constexpr int kNormsSmem = (128 * 129 + kProbes * 128 + 128 * kNormsXch) * 4;
 
 enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
+
+// Two-level blocking of the update: block columns are grouped in outer panels
+// of kOuter.  Inside an outer panel each step updates only the panel's own
+// columns (and the substitution accumulators of the panel's block rows); the
+// last step of the panel applies the whole panel (K = kOuter * 128) to
+// everything right of it, so the fp32 trailing matrix is read and written once
+// per outer panel instead of once per block column.  Lp keeps the L_rk of the
+// panel's kOuter block columns side by side.
+constexpr int kOuter = 4;
+constexpr int kLpW = kOuter * 128;
 
 struct TcBufs {
   float* acc;
@@ -81,6 +93,43 @@ struct ItJob {
 // their columns c in (k, r]; columns c <= k pair their rows r > k
 __host__ __device__ inline long long it_pairs(long long R) { return ((R + 1) / 2) * ((R + 2) / 2); }
 
+// column pairs of row r in an inner update at step k: columns c in (k, min(r, cl)]
+__host__ __device__ inline int upd_row_pairs(int r, int k, int cl) {
+  const int last = r < cl ? r : cl;
+  return last > k ? (last - k + 1) / 2 : 0;
+}
+
+// The update jobs of step k for a matrix of T block rows.
+//   outer step (k the last block column of its outer panel [p0, k]):
+//     Schur  A_rc -= sum_{j=p0..k} L_rj L_cj^T     rows r > k, column pairs c in (k, r]
+//     subst  C'_cr -= sum_{j=max(c,p0)..k} U_cj L_rj^T   c <= k, row pairs r > k
+//   inner step (the panel [p0, pe) continues after k; cl = pe - 1):
+//     Schur  A_rc -= L_rk L_ck^T                  rows r > k, column pairs c in (k, min(r, cl)]
+//     subst  C'_cr -= U_ck L_rk^T                 c <= k, row pairs r in (k, cl]
+struct UpdShape {
+  int outer, p0, cl;
+  long long nschur, nsub;
+};
+__host__ __device__ inline UpdShape upd_shape(int T, int k) {
+  UpdShape sh;
+  sh.p0 = k - k % kOuter;
+  sh.outer = (k % kOuter) == kOuter - 1;
+  const int pe = sh.p0 + kOuter < T ? sh.p0 + kOuter : T;
+  sh.cl = pe - 1;
+  sh.nschur = sh.nsub = 0;
+  if (k + 1 >= T) return sh;
+  if (sh.outer) {
+    const int R = T - k - 1;
+    sh.nschur = it_pairs(R);
+    sh.nsub = (long long)(k + 1) * ((R + 1) / 2);
+  } else if (sh.cl > k) {
+    for (int r = k + 1; r < sh.cl; ++r) sh.nschur += upd_row_pairs(r, k, sh.cl);
+    sh.nschur += (long long)(T - sh.cl) * upd_row_pairs(sh.cl, k, sh.cl);
+    sh.nsub = (long long)(k + 1) * ((sh.cl - k + 1) / 2);
+  }
+  return sh;
+}
+
 template <int KIND>
 __device__ ItJob it_decode(const ItParams& prm, long long u) {
   int lo = 0, hi = prm.n;  // find m with job_begin[m] <= u < job_begin[m+1]
@@ -116,40 +165,65 @@ __device__ ItJob it_decode(const ItParams& prm, long long u) {
     J.o_x = k * 128;
     J.mode = r > k ? 0 : 1;
   } else if (KIND == kItUpdate) {
-    const int R = T - k - 1;
-    const long long ni = it_pairs(R);
-    J.K = 128;
+    const UpdShape sh = upd_shape(T, k);
     J.mb = &prm.mLB;
-    J.b_x0 = 0;
     J.b_box = 256;
-    if (q < ni) {
-      int jrow = 1;
-      while (it_pairs(jrow) <= q) ++jrow;  // rows r = k + jrow
-      const int cp = (int)(q - it_pairs(jrow - 1));
-      const int r = k + jrow, c = k + 1 + 2 * cp;
-      const int w = min(2, r - c + 1);
+    if (q < sh.nschur) {
+      int r, cp;
+      if (sh.outer) {
+        int jrow = 1;
+        while (it_pairs(jrow) <= q) ++jrow;  // rows r = k + jrow
+        cp = (int)(q - it_pairs(jrow - 1));
+        r = k + jrow;
+      } else {
+        long long qq = q;
+        r = k + 1;
+        while (r < sh.cl && qq >= upd_row_pairs(r, k, sh.cl)) qq -= upd_row_pairs(r++, k, sh.cl);
+        if (r < sh.cl) {
+          cp = (int)qq;
+        } else {  // rows from cl on all have the same pairs
+          const int cmax = upd_row_pairs(sh.cl, k, sh.cl);
+          r = sh.cl + (int)(qq / cmax);
+          cp = (int)(qq % cmax);
+        }
+      }
+      const int c = k + 1 + 2 * cp;
+      const int last = sh.outer ? r : min(r, sh.cl);
+      const int w = min(2, last - c + 1);
       J.ma = &prm.mLA;
       J.a_y = (int)(ro + r * 128);
-      J.a_x0 = 0;
       J.b_y = (int)(ro + c * 128);
+      J.a_x0 = J.b_x0 = sh.outer ? 0 : (k - sh.p0) * 128;
+      J.K = sh.outer ? (k + 1 - sh.p0) * 128 : 128;
       J.n_mma = 128 * w;
       J.o_y = (int)(ro + r * 128);
       J.o_x = c * 128;
       J.mode = 0;
     } else {
-      const long long q2 = q - ni;
-      const int hp = (R + 1) / 2;
+      const long long q2 = q - sh.nschur;
+      const int rlast = sh.outer ? T - 1 : sh.cl;  // rows r in (k, rlast]
+      const int hp = (rlast - k + 1) / 2;
       const int c = (int)(q2 / hp), rp = (int)(q2 % hp);
       const int r = k + 1 + 2 * rp;
-      const int w = min(2, T - r);
+      const int w = min(2, rlast - r + 1);
       J.ma = &prm.mUA;
       J.a_y = (int)(ro + c * 128);
-      J.a_x0 = k * 128;
       J.b_y = (int)(ro + r * 128);
+      if (sh.outer) {
+        const int j0 = max(c, sh.p0);  // U_cj = 0 for j < c
+        J.a_x0 = j0 * 128;
+        J.b_x0 = (j0 - sh.p0) * 128;
+        J.K = (k + 1 - j0) * 128;
+        J.mode = c >= sh.p0 ? 1 : 0;  // first contribution to C'_cr (r beyond the panel)
+      } else {
+        J.a_x0 = k * 128;
+        J.b_x0 = (k - sh.p0) * 128;
+        J.K = 128;
+        J.mode = c == k ? 1 : 0;
+      }
       J.n_mma = 128 * w;
       J.o_y = (int)(ro + c * 128);
       J.o_x = r * 128;
-      J.mode = c == k ? 1 : 0;
     }
   } else {
     int i = 0;
@@ -337,8 +411,8 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         uint16_t* dst;
         long long sstride;
         if (J.mode == 0) {
-          dst = prm.b.lp + (long long)(J.o_y + mrow) * 128;
-          sstride = prm.b.R * 128;
+          dst = prm.b.lp + (long long)(J.o_y + mrow) * kLpW + (long long)((J.o_x / 128) % kOuter) * 128;
+          sstride = prm.b.R * kLpW;
         } else {
           dst = prm.b.u + (long long)(J.o_y + mrow) * prm.b.LD + J.o_x;
           sstride = prm.b.R * prm.b.LD;
@@ -375,19 +449,34 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
           obuf ^= 1;
         }
       } else {
-        // X tile (i, j + h) of the pair: write it and its mirror
+        // X tile (i, j + h) of the pair and its mirror, in 32 x 32 blocks: the
+        // mirror straight from the registers (lanes hold consecutive rows, so
+        // the stores run along the mirror's rows), the tile itself through a
+        // transpose in the warp's staging buffer, so that both are coalesced
         const InvMat mt = prm.mats[J.m];
         const int jt = J.j + h;
-        const long long row = (long long)J.i * 128 + mrow;
-        if (row < mt.d) {
+        const long long row0 = (long long)J.i * 128 + q * 32;  // this warp's 32 rows
+        float* tb = reinterpret_cast<float*>(out_stage + e * 2 * kItOutBlock);  // 32 x 33 floats
 #pragma unroll
-          for (int t = 0; t < 128; ++t) {
-            const long long col = (long long)jt * 128 + t;
-            if (col < mt.d && (J.i != jt || mrow <= t)) {
-              const float v = run[t];
-              mt.X[row * mt.ld_out + col] = v;
-              mt.X[col * mt.ld_out + row] = v;
-            }
+        for (int g = 0; g < 4; ++g) {
+          const long long col0 = (long long)jt * 128 + g * 32;
+          const long long row = row0 + lane;
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            const long long col = col0 + t;
+            if (row < mt.d && col < mt.d && (J.i != jt || mrow <= g * 32 + t))
+              mt.X[col * mt.ld_out + row] = run[g * 32 + t];
+          }
+          __syncwarp();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) tb[lane * 33 + t] = run[g * 32 + t];
+          __syncwarp();
+          const long long col = col0 + lane;
+#pragma unroll 8
+          for (int rr = 0; rr < 32; ++rr) {
+            const long long r = row0 + rr;
+            if (r < mt.d && col < mt.d && (J.i != jt || q * 32 + rr <= g * 32 + lane))
+              mt.X[r * mt.ld_out + col] = tb[rr * 33 + lane];
           }
         }
       }
@@ -453,7 +542,9 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
 // ------------------------------------------------------------------ ||D||_1 and w = D v (AUTO)
 // One CTA per 128-row block R of a matrix: the rows of R gather their sums
 // from the lower tiles (R, C <= R) row-wise and from the tiles (C > R, R)
-// column-wise (D is symmetric), so no atomics are needed.  Double-float sums.
+// column-wise (D is symmetric), so no atomics are needed.  Each row is split
+// between two threads (64 columns of every tile each); the probe sums w = D v
+// are double-float (the products with v = +-1 are exact).
 __global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c, TcBufs b) {
   const int mi = blockIdx.y;
   if (!inv_active(c, mi, false)) return;
@@ -463,13 +554,16 @@ __global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c, TcBufs b) {
   extern __shared__ __align__(16) uint8_t norms_smem[];
   float* tile = reinterpret_cast<float*>(norms_smem);  // 128 x 129
   float* vs = tile + 128 * 129;                        // kProbes x 128 probe signs of the tile's columns
+  float* xch = vs + kProbes * 128;                     // 128 x kNormsXch sums of the second half of the threads
   const float* A = b.acc + m.row_off * b.LD;
-  const int t = threadIdx.x;
-  float ahi = 0.f, alo = 0.f;  // row abs sum
+  const int t = threadIdx.x, row = t % 128, half = t / 128;
+  // thread (row, half) sums the entries (r, cidx) of its row with cidx in the
+  // tile's columns [64 half, 64 half + 64)
+  float asum = 0.f;  // row abs sum (a norm for a threshold: plain fp32)
   float whi[kProbes], wlo[kProbes];
 #pragma unroll
   for (int p = 0; p < kProbes; ++p) whi[p] = wlo[p] = 0.f;
-  const long long r = (long long)R * 128 + t;  // this thread's row (t < 128)
+  const long long r = (long long)R * 128 + row;
   for (int C = 0; C < m.T; ++C) {
     const bool rowwise = C <= R;  // tile (R, C) read along rows; else tile (C, R) along columns
     const float* src = rowwise ? A + (long long)R * 128 * b.LD + (long long)C * 128
@@ -486,41 +580,51 @@ __global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c, TcBufs b) {
     }
     for (int e = t; e < kProbes * 128; e += 256) {
       const int p = e / 128, i = e % 128;
-      // signs of the entries this row multiplies: the tile's columns (row-wise) or rows (column-wise)
       vs[p * 128 + i] = (float)probe_sign((long long)C * 128 + i, p);
     }
     __syncthreads();
-    if (t < 128 && r < m.d) {
-      for (int i = 0; i < 128; ++i) {
-        const long long cidx = (long long)C * 128 + i;  // the other index of the entry
-        if (cidx >= m.d) break;
-        // row-wise: entry (r, cidx) = tile[t][i] (stored only for cidx <= r within the diagonal tile);
-        // column-wise: entry (cidx, r) = tile[i][t]
-        float x;
-        if (rowwise) {
-          if (C == R && i > t) x = tile[i * 129 + t];  // upper part of the diagonal tile by symmetry
-          else x = tile[t * 129 + i];
-        } else {
-          x = tile[i * 129 + t];
-        }
-        df_add(ahi, alo, fabsf(x));
+    const long long left = m.d - ((long long)C * 128 + 64 * half);  // columns of this half inside d
+    const int iend = left < 0 ? 0 : (left < 64 ? (int)left : 64);
+    if (r < m.d) {
+#pragma unroll 4
+      for (int ii = 0; ii < iend; ++ii) {
+        const int i = 64 * half + ii;
+        // row-wise: entry (r, C*128+i) = tile[row][i], stored only on or below the
+        // diagonal of the diagonal tile (the rest by symmetry); column-wise: tile[i][row]
+        const float x = (!rowwise || (C == R && i > row)) ? tile[i * 129 + row] : tile[row * 129 + i];
+        asum += fabsf(x);
 #pragma unroll
-        for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vs[p * 128 + i]);
+        for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vs[p * 128 + i]);  // exact products
       }
     }
   }
-  if (t < 128 && r < m.d) {
-    c.rowsum[m.off_rowsum + r] = ahi + alo;
+  __syncthreads();
+  if (half == 1) {
+    xch[row * kNormsXch] = asum;
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) {
+      xch[row * kNormsXch + 1 + 2 * p] = whi[p];
+      xch[row * kNormsXch + 2 + 2 * p] = wlo[p];
+    }
+  }
+  __syncthreads();
+  if (half == 0 && r < m.d) {
+    asum += xch[row * kNormsXch];
+    c.rowsum[m.off_rowsum + r] = asum;
     const long long np = (long long)m.T * 128;
 #pragma unroll
-    for (int p = 0; p < kProbes; ++p) c.probe[m.off_probe + p * np + r] = df_pack(whi[p], wlo[p]);
+    for (int p = 0; p < kProbes; ++p) {
+      df_add(whi[p], wlo[p], xch[row * kNormsXch + 1 + 2 * p]);
+      wlo[p] += xch[row * kNormsXch + 2 + 2 * p];
+      c.probe[m.off_probe + p * np + r] = df_pack(whi[p], wlo[p]);
+    }
   }
 }
 
 // ------------------------------------------------------------------ step k: diagonal block
 // Cholesky and inverse of the diagonal block k: Winv_k rows (the panel's B
 // operand) and U_kk = Winv_k^T, as bf16 slices.
-__global__ void __launch_bounds__(128) tc_diag_kernel(InvCtx c, TcBufs b, int k) {
+__global__ void __launch_bounds__(256, 1) tc_diag_kernel(InvCtx c, TcBufs b, int k) {
   const int mi = blockIdx.x;
   if (!inv_active(c, mi, true)) return;
   const InvMat m = c.mats[mi];
@@ -529,7 +633,24 @@ __global__ void __launch_bounds__(128) tc_diag_kernel(InvCtx c, TcBufs b, int k)
   extern __shared__ __align__(16) uint8_t diag_smem[];
   float* a = reinterpret_cast<float*>(diag_smem);
   const float* src = b.acc + (m.row_off + (long long)k * 128) * b.LD + (long long)k * 128;
-  for (int r = 0; r < 128; ++r) a[r * kDiagPitch + t] = (t <= r) ? src[(long long)r * b.LD + t] : 0.f;
+  {
+    // 16 float4 per thread (LD is a multiple of 128), all loads issued before the stores
+    float4 v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = t + 256 * q;  // row e / 32, columns 4 (e % 32) ..
+      v[q] = *reinterpret_cast<const float4*>(src + (long long)(e / 32) * b.LD + (e % 32) * 4);
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = t + 256 * q, r = e / 32, c4 = (e % 32) * 4;
+      float* d = a + r * kDiagPitch + c4;
+      d[0] = c4 <= r ? v[q].x : 0.f;
+      d[1] = c4 + 1 <= r ? v[q].y : 0.f;
+      d[2] = c4 + 2 <= r ? v[q].z : 0.f;
+      d[3] = c4 + 3 <= r ? v[q].w : 0.f;
+    }
+  }
   __syncthreads();
   float min_piv;
   const int fail = block_chol_inv<float>(a, m.d - k * 128, min_piv);
@@ -541,17 +662,18 @@ __global__ void __launch_bounds__(128) tc_diag_kernel(InvCtx c, TcBufs b, int k)
     return;
   }
   if (t == 0) atomicMin(reinterpret_cast<int*>(&c.st[mi].min_piv), __float_as_int(min_piv));
-  uint16_t* wdst = b.winv + ((long long)mi * 128 + t) * 128;
-  uint16_t* udst = b.u + (m.row_off + (long long)k * 128 + t) * b.LD + (long long)k * 128;
+  // threads 0..127 write row t of Winv, threads 128..255 row t - 128 of U_kk
+  const int row = t % 128;
+  const bool upper = t >= 128;
+  uint16_t* dst = upper ? b.u + (m.row_off + (long long)k * 128 + row) * b.LD + (long long)k * 128
+                        : b.winv + ((long long)mi * 128 + row) * 128;
+  const long long slice = upper ? b.R * b.LD : (long long)b.n * 128 * 128;
   for (int c8 = 0; c8 < 128; c8 += 8) {
-    float w8[8], u8[8];
+    float v8[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      w8[e] = a[t * kDiagPitch + c8 + e];    // Winv[t][c]  (zero above the diagonal)
-      u8[e] = a[(c8 + e) * kDiagPitch + t];  // Winv[c][t]
-    }
-    split8_store(w8, wdst + c8, (long long)b.n * 128 * 128);
-    split8_store(u8, udst + c8, b.R * b.LD);
+    for (int e = 0; e < 8; ++e)  // Winv[row][c] (zero above the diagonal), or Winv[c][row]
+      v8[e] = upper ? a[(c8 + e) * kDiagPitch + row] : a[row * kDiagPitch + c8 + e];
+    split8_store(v8, dst + c8, slice);
   }
 }
 
@@ -590,45 +712,68 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(InvCtx c, TcBufs b, int k)
 }
 
 // ------------------------------------------------------------------ residual probe y = X w, ||X||_F^2 (AUTO)
-// one warp per row of X (full symmetric, as written by the X = U U^T step),
-// double-float products and sums
+// A CTA per strip of kPrRows rows of X (full symmetric, as written by the
+// X = U U^T step), columns in chunks of 128: lane l owns columns 4l..4l+3 of
+// the chunk and keeps their w (all probes) in registers for the kPrWarpRows
+// rows of its warp, so w is read once per strip.  Double-float products and sums.
+constexpr int kPrWarpRows = 4;
+constexpr int kPrRows = 8 * kPrWarpRows;
 __global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c) {
   const int mi = blockIdx.y;
   if (!inv_active(c, mi, true)) return;
   const InvMat m = c.mats[mi];
+  const long long rw = (long long)blockIdx.x * kPrRows + (threadIdx.x / 32) * kPrWarpRows;  // the warp's first row
+  if ((long long)blockIdx.x * kPrRows >= m.d) return;
   const int lane = threadIdx.x % 32;
   const long long np = (long long)m.T * 128;
   const float2* w = c.probe + m.off_probe;
   float2* y = c.probe + m.off_probe + (long long)kProbes * np;
+  const int nrow = rw >= m.d ? 0 : (int)(m.d - rw < kPrWarpRows ? m.d - rw : kPrWarpRows);
+  float hi[kPrWarpRows][kProbes], lo[kPrWarpRows][kProbes];
+#pragma unroll
+  for (int q = 0; q < kPrWarpRows; ++q)
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) hi[q][p] = lo[q][p] = 0.f;
   float sq = 0.f;
-  for (long long r = (long long)blockIdx.x * 8 + threadIdx.x / 32; r < m.d; r += (long long)gridDim.x * 8) {
-    float hi[kProbes], lo[kProbes];
+  for (long long c0 = 0; c0 < m.d && nrow > 0; c0 += 128) {
+    const long long col = c0 + 4 * lane;
+    const bool any = col < m.d;  // float4 reads of columns col..col+3 stay inside the row (ld_out % 4 == 0)
+    float2 wv[kProbes][4];
 #pragma unroll
-    for (int p = 0; p < kProbes; ++p) hi[p] = lo[p] = 0.f;
-    const float* xr = m.X + r * m.ld_out;
-    for (long long col = lane; col < m.d; col += 32) {
-      const float v = xr[col];
-      sq += v * v;
+    for (int p = 0; p < kProbes; ++p)
 #pragma unroll
-      for (int p = 0; p < kProbes; ++p) {
-        const float2 wv = w[p * np + col];
-        df_add_prod(hi[p], lo[p], v, wv.x, wv.y);
+      for (int e = 0; e < 4; ++e) wv[p][e] = (col + e < m.d) ? w[p * np + col + e] : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < kPrWarpRows; ++q) {
+      if (q < nrow && any) {
+        const float4 x4 = *reinterpret_cast<const float4*>(m.X + (rw + q) * m.ld_out + col);
+        const float xs[4] = {x4.x, col + 1 < m.d ? x4.y : 0.f, col + 2 < m.d ? x4.z : 0.f,
+                             col + 3 < m.d ? x4.w : 0.f};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          sq += xs[e] * xs[e];
+#pragma unroll
+          for (int p = 0; p < kProbes; ++p) df_add_prod(hi[q][p], lo[q][p], xs[e], wv[p][e].x, wv[p][e].y);
+        }
       }
     }
+  }
+#pragma unroll
+  for (int q = 0; q < kPrWarpRows; ++q) {
 #pragma unroll
     for (int p = 0; p < kProbes; ++p) {
       // combine the 32 lanes' double-float partial sums
-      float h = hi[p], l = lo[p];
+      float h = hi[q][p], l = lo[q][p];
       for (int o = 16; o > 0; o >>= 1) {
         const float oh = __shfl_xor_sync(0xffffffffu, h, o), ol = __shfl_xor_sync(0xffffffffu, l, o);
         df_add(h, l, oh);
         l += ol;
       }
-      if (lane == 0) y[p * np + r] = df_pack(h, l);
+      if (lane == 0 && q < nrow) y[p * np + rw + q] = df_pack(h, l);
     }
   }
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-  if (lane == 0) atomicAdd(&c.st[mi].xnorm2, sq);
+  if (lane == 0 && nrow > 0) atomicAdd(&c.st[mi].xnorm2, sq);
 }
 
 // ------------------------------------------------------------------ host side
@@ -651,7 +796,7 @@ TcLayout tc_layout(int n, const int* T) {
   L.p = off;
   off += al256((size_t)kSlices * R * 128 * 2);
   L.lp = off;
-  off += al256((size_t)kSlices * R * 128 * 2);
+  off += al256((size_t)kSlices * R * kLpW * 2);
   L.winv = off;
   off += al256((size_t)kSlices * n * 128 * 128 * 2);
   L.bytes = off;
@@ -697,8 +842,8 @@ static int launch_it(ItParams* prm, const int* Ts, int n, int k, int sms, cudaSt
     if (KIND == kItPanel) {
       cnt = T > k ? T - 1 : 0;
     } else if (KIND == kItUpdate) {
-      const int R = T - k - 1;
-      cnt = R > 0 ? it_pairs(R) + (long long)(k + 1) * ((R + 1) / 2) : 0;
+      const UpdShape sh = upd_shape(T, k);
+      cnt = sh.nschur + sh.nsub;
     } else {
       cnt = it_pairs(T);
     }
@@ -744,8 +889,8 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   ItParams* prm = new ItParams;
   memset(prm, 0, sizeof(ItParams));
   bool ok = enc_slices(enc, &prm->mUA, b.u, b.R, b.LD, 128) && enc_slices(enc, &prm->mUB, b.u, b.R, b.LD, 256) &&
-            enc_slices(enc, &prm->mP, b.p, b.R, 128, 128) && enc_slices(enc, &prm->mLA, b.lp, b.R, 128, 128) &&
-            enc_slices(enc, &prm->mLB, b.lp, b.R, 128, 256) &&
+            enc_slices(enc, &prm->mP, b.p, b.R, 128, 128) && enc_slices(enc, &prm->mLA, b.lp, b.R, kLpW, 128) &&
+            enc_slices(enc, &prm->mLB, b.lp, b.R, kLpW, 256) &&
             enc_slices(enc, &prm->mW, b.winv, (long long)n * 128, 128, 128);
   {
     cuuint64_t gdim[2] = {(cuuint64_t)b.LD, (cuuint64_t)b.R};
@@ -778,7 +923,7 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
     count_launch();
   }
   for (int k = 0; k < Tmax && rc == KFAC_OK; ++k) {
-    tc_diag_kernel<<<n, 128, diag_smem_bytes<float>(), stream>>>(ctx, b, k);
+    tc_diag_kernel<<<n, 256, diag_smem_bytes<float>(), stream>>>(ctx, b, k);
     count_launch();
     if (Tmax > 1) {
       tc_prep_kernel<<<dim3((unsigned)(Tmax - 1), n), 256, 0, stream>>>(ctx, b, k);
@@ -789,7 +934,7 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   }
   if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, stream);
   if (rc == KFAC_OK && ctx.want_rowsum) {
-    tc_probe_kernel<<<dim3(64, n), 256, 0, stream>>>(ctx);
+    tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, stream>>>(ctx);
     count_launch();
   }
   delete prm;
