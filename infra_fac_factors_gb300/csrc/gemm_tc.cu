@@ -13,9 +13,10 @@
 // preconditioner has gain up to 1/gamma on directions the gradient does not
 // occupy: |grad| |inv_a| can be 6e3 times |grad inv_a|).  The tensor-core
 // accumulator does not round to nearest, and its error grows with the number
-// of accumulations, so each k-step goes to a fresh TMEM accumulator (two,
-// ping-pong) and the epilogue warps add it into fp32 registers with
-// round-to-nearest: the result has the accuracy of an fp32 FMA loop.
+// of accumulations, so every 32-wide k-block (two 16-wide k-steps, twelve
+// MMAs) goes to a fresh TMEM accumulator (two, ping-pong) and the epilogue
+// warps add it into fp32 registers with round-to-nearest: the result keeps
+// close to the accuracy of an fp32 FMA loop.
 //
 // Kernel roles (320 threads, one CTA per SM, persistent over 128 x 256 tiles):
 //   warp 0: TMA producer; warp 1: TMEM allocation + MMA issuer;
@@ -43,6 +44,9 @@ constexpr int kGtB = 256 * kGtBK * 2;  // one slice of the B tile (16 KB)
 constexpr int kGtStage = kGtNS * (kGtA + kGtB);
 constexpr int kGtSmem = kGtStages * kGtStage + 1024 + 256;
 constexpr int kGtThreads = 320;
+// 16-wide k-steps accumulated in one TMEM accumulator between two drains into
+// the epilogue's round-to-nearest fp32 sums
+constexpr int kGtDrain = 2;
 constexpr int kGtEpiWarps = 8;
 
 struct GtParams {
@@ -147,6 +151,8 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
         const GtTile tl = gt_decode(prm, u);
         const uint32_t idesc = idesc_bf16_f32(tl.n_mma, false, false);
         const int nk = (tl.K + kGtBK - 1) / kGtBK;
+        const int n16 = nk * (kGtBK / 16);  // 16-wide k-steps of the tile
+        int st16 = 0;
         for (int kb = 0; kb < nk && ok; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, prm.status)) {
             ok = false;
@@ -155,12 +161,16 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
           const uint32_t a0 = smem_u32(smem + stage * kGtStage);
           const uint32_t b0 = a0 + kGtNS * kGtA;
 #pragma unroll
-          for (int kk = 0; kk < kGtBK / 16; ++kk) {
-            if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) {
-              ok = false;
-              break;
+          for (int kk = 0; kk < kGtBK / 16; ++kk, ++st16) {
+            const bool gfirst = st16 % kGtDrain == 0;
+            const bool glast = st16 % kGtDrain == kGtDrain - 1 || st16 == n16 - 1;
+            if (gfirst) {
+              if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
             }
-            tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * 256;
             const uint32_t off = kk * 32;  // 16 values of k = 32 bytes along the swizzled row
             uint64_t da[kGtNS], db[kGtNS];
@@ -169,15 +179,17 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
               da[s] = gt_desc(a0 + s * kGtA + off);
               db[s] = gt_desc(b0 + s * kGtB + off);
             }
-            tc_mma_bf16(d_tmem, da[0], db[0], idesc, 0u);
+            tc_mma_bf16(d_tmem, da[0], db[0], idesc, gfirst ? 0u : 1u);
             tc_mma_bf16(d_tmem, da[0], db[1], idesc, 1u);
             tc_mma_bf16(d_tmem, da[1], db[0], idesc, 1u);
             tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
             tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
             tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
-            tc_commit(&acc_full[acc]);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
+            if (glast) {
+              tc_commit(&acc_full[acc]);
+              acc ^= 1;
+              if (acc == 0) acc_phase ^= 1;
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == kGtStages) {
@@ -198,7 +210,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
     for (long long u = blockIdx.x; u < prm.total_tiles && ok; u += gridDim.x) {
       const GtTile tl = gt_decode(prm, u);
       const GtProb& pr = prm.probs[tl.prob];
-      const int nsteps = (tl.K + kGtBK - 1) / kGtBK * (kGtBK / 16);
+      const int nsteps = ((tl.K + kGtBK - 1) / kGtBK * (kGtBK / 16) + kGtDrain - 1) / kGtDrain;
       float run[128];
 #pragma unroll
       for (int t = 0; t < 128; ++t) run[t] = 0.f;

@@ -1,8 +1,8 @@
 // fp32 pass of the batched damped inverse on tcgen05 tensor cores (the
 // algorithm is described in inverse.cu).  Every tile product is a split-bf16
 // NT GEMM (three slices per fp32 value, six MMAs per 16-wide k-step, each
-// k-step drained into round-to-nearest fp32 sums, as in gemm_tc.cu), so the
-// arithmetic has fp32 accuracy.
+// 32-wide k-block drained into round-to-nearest fp32 sums, as in gemm_tc.cu),
+// so the arithmetic has close to fp32 accuracy.
 //
 // To make every product NT with K-major operands, the blocked inverse
 // W = L^-1 is kept transposed, U = W^T (block upper triangular), and so are
@@ -42,6 +42,9 @@ constexpr int kItOutBlock = 4096;  // one 32 x 32 fp32 block
 constexpr int kItOut = 8 * 2 * kItOutBlock;
 constexpr int kItSmem = kItStages * kItStage + kItOut + 1024 + 256;
 constexpr int kItThreads = 320;
+// 16-wide k-steps accumulated in one TMEM accumulator between two drains into
+// the epilogue's round-to-nearest fp32 sums
+constexpr int kItDrain = 2;
 constexpr int kNormsXch = 1 + 2 * kProbes;
 constexpr int kNormsSmem = (128 * 129 + kProbes * 128 + 128 * kNormsXch) * 4;
 
@@ -324,6 +327,8 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         const ItJob J = it_decode<KIND>(prm, u);
         if (!J.valid) continue;
         const uint32_t idesc = idesc_bf16_f32(J.n_mma, false, false);
+        const int n16 = J.K / 16;  // 16-wide k-steps of the job
+        int st16 = 0;
         for (int kb = 0; kb < J.K / kItBK && ok; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, prm.status)) {
             ok = false;
@@ -332,12 +337,16 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
           const uint32_t a0 = smem_u32(smem + stage * kItStage);
           const uint32_t b0 = a0 + kSlices * kItA;
 #pragma unroll
-          for (int kk = 0; kk < kItBK / 16; ++kk) {
-            if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) {
-              ok = false;
-              break;
+          for (int kk = 0; kk < kItBK / 16; ++kk, ++st16) {
+            const bool gfirst = st16 % kItDrain == 0;
+            const bool glast = st16 % kItDrain == kItDrain - 1 || st16 == n16 - 1;
+            if (gfirst) {
+              if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
             }
-            tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * 256;
             const uint32_t off = kk * 32;
             uint64_t da[kSlices], db[kSlices];
@@ -346,15 +355,17 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
               da[s] = it_desc(a0 + s * kItA + off);
               db[s] = it_desc(b0 + s * kItB + off);
             }
-            tc_mma_bf16(d_tmem, da[0], db[0], idesc, 0u);
+            tc_mma_bf16(d_tmem, da[0], db[0], idesc, gfirst ? 0u : 1u);
             tc_mma_bf16(d_tmem, da[0], db[1], idesc, 1u);
             tc_mma_bf16(d_tmem, da[1], db[0], idesc, 1u);
             tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
             tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
             tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
-            tc_commit(&acc_full[acc]);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
+            if (glast) {
+              tc_commit(&acc_full[acc]);
+              acc ^= 1;
+              if (acc == 0) acc_phase ^= 1;
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == kItStages) {
@@ -380,7 +391,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
       float run[128];
 #pragma unroll
       for (int t = 0; t < 128; ++t) run[t] = 0.f;
-      const int nsteps = J.K / 16;
+      const int nsteps = (J.K / 16 + kItDrain - 1) / kItDrain;
       for (int st = 0; st < nsteps; ++st) {
         if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) {
           ok = false;
