@@ -10,6 +10,11 @@ the step in order (SPD-KFAC §II-B/§II-C):
   4. kfac_damped_inverse    (A + gamma I)^-1, (G + gamma I)^-1 of all factors
   5. kfac_precondition      (G + gamma I)^-1 grad (A + gamma I)^-1 of all layers
 
+``step`` overlaps 2 and 3: the layers are cut into groups of about equal
+factor work, and the running-average pass of group i (memory-bound, on a
+second stream) runs while the tensor-core factor pass of group i + 1 runs on
+the caller's stream; the two kernels fit on the same SMs.
+
 Buffers are row-major with leading dimensions padded to 16-byte multiples
 (bf16 inputs) or 128-byte multiples (fp32 factor matrices).
 """
@@ -36,6 +41,23 @@ class LayerSpec:
     hw: int = 1          # spatial positions (1 for linear layers)
 
 
+def layer_groups(layers: Sequence[LayerSpec], n_groups: int):
+    """Cut the layers into at most `n_groups` contiguous, non-empty groups of
+    about equal factor work (rows * d^2 summed over both factors); returns
+    [(first, end)] covering every layer once, in order."""
+    work = [L.rows * L.d_in ** 2 + (L.batch if L.hw > 1 else L.rows) * L.d_out ** 2 for L in layers]
+    total = float(sum(work)) or 1.0
+    n = max(1, min(n_groups, len(layers)))
+    bounds, acc, cut = [0], 0.0, 1
+    for li, w in enumerate(work):
+        acc += w
+        if cut < n and acc >= total * cut / n and li + 1 < len(layers):
+            bounds.append(li + 1)
+            cut += 1
+    bounds.append(len(layers))
+    return list(zip(bounds[:-1], bounds[1:]))
+
+
 class FactorBufs:
     def __init__(self, d: int, P: int, device):
         self.d = d
@@ -50,7 +72,7 @@ class FactorBufs:
 
 class KFACStep:
     def __init__(self, layers: Sequence[LayerSpec], P: int, gamma: float, decay: float, in_dtype: str,
-                 refine: int = capi.KFAC_REFINE_AUTO, device="cuda"):
+                 refine: int = capi.KFAC_REFINE_AUTO, device="cuda", n_groups: int = 4):
         self.layers = list(layers)
         self.P = P
         self.gamma = float(gamma)
@@ -84,6 +106,10 @@ class KFACStep:
         self.info = torch.zeros(nf, dtype=torch.int32, device=dev)
         self.route = torch.zeros(nf, dtype=torch.int32, device=dev)
         self._build_args()
+        self._build_groups(n_groups)
+        self._side = torch.cuda.Stream(device=dev)
+        self._ev_fac = [torch.cuda.Event() for _ in self._groups]
+        self._ev_side = torch.cuda.Event()
         self.inv_ws_bytes = capi.kfac_damped_inverse_workspace(self._inv_args, refine)
         self.pc_ws_bytes = capi.kfac_precondition_workspace(self._pc_args)
         if self.inv_ws_bytes == 0 or self.pc_ws_bytes == 0:
@@ -125,6 +151,21 @@ class KFACStep:
                 G.inv.data_ptr(), G.ld, self.grad[li].data_ptr(), self.grad[li].shape[1],
                 A.inv.data_ptr(), A.ld, self.out[li].data_ptr(), self.out[li].shape[1], L.d_out, L.d_in))
 
+    def _build_groups(self, n_groups: int):
+        """The argument arrays of each layer group (see layer_groups)."""
+        nl = len(self.layers)
+        self._groups = []
+        for b, e in layer_groups(self.layers, n_groups):
+            lis = range(b, e)
+            main = [self._fac_main[li] for li in lis]  # A factors
+            main += [self._fac_main[nl + li - self._n_conv_before(li)] for li in lis if self.layers[li].hw == 1]
+            fp32 = [self._fac_fp32[self._n_conv_before(li)] for li in lis if self.layers[li].hw > 1]
+            run = [self._run_args[li] for li in lis] + [self._run_args[nl + li] for li in lis]
+            self._groups.append((list(lis), main, fp32, run))
+
+    def _n_conv_before(self, li: int) -> int:
+        return sum(1 for L in self.layers[:li] if L.hw > 1)
+
     # ------------------------------------------------------------------ inputs
     def set_layer_inputs(self, li: int, a: torch.Tensor, g: torch.Tensor, grad: torch.Tensor,
                          non_blocking: bool = False):
@@ -162,12 +203,47 @@ class KFACStep:
     def precondition(self, stream: int):
         capi.kfac_precondition(self._pc_args, self.pc_ws.data_ptr(), self.pc_ws_bytes, stream)
 
-    def step(self, first_step: bool, stream: Optional[torch.cuda.Stream] = None):
-        s = self.stream_handle(stream)
-        self.factors(s)
-        self.update_running(first_step, s)
+    def factors_and_running(self, first_step: bool, stream: Optional[torch.cuda.Stream] = None):
+        """Stages 2 and 3, the running-average pass of each layer group on a
+        second stream behind the factor pass of the next group; returns when
+        both are ordered before later work on `stream`."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        ms, ss = main.cuda_stream, self._side.cuda_stream
+        decay = 0.0 if first_step else self.decay
+        self._side.wait_stream(main)  # the side stream's earlier work must not overtake the inputs
+        for (lis, fmain, ffp32, run), ev in zip(self._groups, self._ev_fac):
+            for li in lis:
+                L = self.layers[li]
+                if L.hw > 1:
+                    gs = self.gs[li]
+                    capi.kfac_spatial_sum(self.g[li].data_ptr(), self.kdt, L.batch, L.hw, L.d_out,
+                                          self.g[li].shape[1], gs.data_ptr(), gs.shape[1], ms)
+            if fmain:
+                capi.kfac_factors(fmain, self.kdt, self.P, 0, ms)
+            if ffp32:
+                capi.kfac_factors(ffp32, capi.KFAC_FP32, self.P, 0, ms)
+            ev.record(main)
+            self._side.wait_event(ev)
+            capi.kfac_update_running(run, self.P, decay, self.gamma, first_step, ss)
+        self._ev_side.record(self._side)
+        main.wait_event(self._ev_side)
+
+    def step(self, first_step: bool, stream: Optional[torch.cuda.Stream] = None, marks=None):
+        """One whole step on `stream`; `marks` (optional, four CUDA events) are
+        recorded at its start and after stages 2+3, 4 and 5."""
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        s = main.cuda_stream
+        if marks is not None:
+            marks[0].record(main)
+        self.factors_and_running(first_step, main)
+        if marks is not None:
+            marks[1].record(main)
         self.inverse(s)
+        if marks is not None:
+            marks[2].record(main)
         self.precondition(s)
+        if marks is not None:
+            marks[3].record(main)
 
     # ------------------------------------------------------------------ counts
     def algorithmic_work(self):

@@ -1,0 +1,56 @@
+"""KFACStep.step overlaps the factor pass of one layer group with the
+running-average pass of the previous group on a second stream.  Each kernel's
+result for a factor does not depend on how the layers are grouped, so the
+overlapped step must reproduce the stage-by-stage sequence bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from infra_fac_factors_gb300 import capi
+from infra_fac_factors_gb300.step import KFACStep, LayerSpec
+
+from gpu_util import ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    ensure_built()
+
+
+def run(key, steps, overlapped, n_groups):
+    cfg = synth.config(key)
+    specs = [LayerSpec(l.d_in, l.d_out, cfg.rows(l), cfg.batch, l.hw) for l in cfg.layers]
+    st = KFACStep(specs, cfg.P, cfg.gamma, cfg.decay or 0.0, cfg.in_dtype, refine=capi.KFAC_REFINE_AUTO,
+                  n_groups=n_groups)
+    stream = torch.cuda.current_stream()
+    for t in range(steps):
+        for li in range(len(specs)):
+            dd = synth.layer_inputs(cfg, t, li)
+            st.set_layer_inputs(li, torch.from_numpy(dd["a"]), torch.from_numpy(dd["g"]),
+                                torch.from_numpy(dd["grad"]))
+        if overlapped:
+            st.step(t == 0, stream)
+        else:
+            s = stream.cuda_stream
+            st.factors(s)
+            st.update_running(t == 0, s)
+            st.inverse(s)
+            st.precondition(s)
+    torch.cuda.synchronize()
+    assert capi.kfac_device_status(clear=True) == capi.KFAC_OK
+    return ([o.cpu().numpy() for o in st.out], [F.inv.cpu().numpy() for F in st.factor_list()],
+            [F.running.cpu().numpy() for F in st.factor_list()])
+
+
+@pytest.mark.parametrize("key,steps,n_groups", [("mlp", 3, 2), ("mlp", 2, 4), ("resnet_conv", 1, 3)])
+def test_overlapped_step_equals_stage_sequence(key, steps, n_groups):
+    seq = run(key, steps, False, n_groups)
+    ovl = run(key, steps, True, n_groups)
+    for a_list, b_list in zip(seq, ovl):
+        for a, b in zip(a_list, b_list):
+            assert np.array_equal(a, b)
