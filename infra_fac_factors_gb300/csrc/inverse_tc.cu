@@ -17,11 +17,14 @@
 //   Acc   fp32 [R][LD]  lower blocks: A (Schur complements), upper blocks: C'
 //   U     bf16 [3][R][LD]   slices of U
 //   P     bf16 [3][R][128]  slices of block column k of Acc (the panel inputs)
-//   Lp    bf16 [3][R][kOuter * 128]  slices of L_rj for the block columns j
-//                                     of the current outer panel (see kOuter)
+//   Lp    bf16 [3][2R][kOuter * 128]  slices of L_rj for the block columns j
+//                                      of an outer panel (see kOuter); two
+//                                      buffers, alternating between panels
 //   Winv  bf16 [3][n*128][128]
 // so that one tensor map per buffer serves every matrix.  Updates land in Acc
 // through TMA add-reductions (no read-modify-write in the kernel).
+#include <mutex>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -81,6 +84,8 @@ struct ItParams {
   int* status;
   long long total_jobs;
   int n, k;
+  int upd_mode;  // update launches: kUpdInner / kUpdFull / kUpdNear / kUpdFar
+  int lp_off;    // first row of the current outer panel's Lp buffer (0 or R)
 };
 
 struct ItJob {
@@ -96,40 +101,45 @@ struct ItJob {
 // their columns c in (k, r]; columns c <= k pair their rows r > k
 __host__ __device__ inline long long it_pairs(long long R) { return ((R + 1) / 2) * ((R + 2) / 2); }
 
-// column pairs of row r in an inner update at step k: columns c in (k, min(r, cl)]
-__host__ __device__ inline int upd_row_pairs(int r, int k, int cl) {
-  const int last = r < cl ? r : cl;
-  return last > k ? (last - k + 1) / 2 : 0;
-}
-
 // The update jobs of step k for a matrix of T block rows.
 //   outer step (k the last block column of its outer panel [p0, k]):
-//     Schur  A_rc -= sum_{j=p0..k} L_rj L_cj^T     rows r > k, column pairs c in (k, r]
-//     subst  C'_cr -= sum_{j=max(c,p0)..k} U_cj L_rj^T   c <= k, row pairs r > k
-//   inner step (the panel [p0, pe) continues after k; cl = pe - 1):
-//     Schur  A_rc -= L_rk L_ck^T                  rows r > k, column pairs c in (k, min(r, cl)]
-//     subst  C'_cr -= U_ck L_rk^T                 c <= k, row pairs r in (k, cl]
+//     Schur  A_rc -= sum_{j=p0..k} L_rj L_cj^T          rows r >= c_lo, column pairs c in [c_lo, min(r, c_hi)]
+//     subst  C'_cr -= sum_{j=max(c,p0)..k} U_cj L_rj^T   c <= k, row pairs r in [c_lo, c_hi]
+//     with the column range [k+1, T) whole (kUpdFull), or cut into the next
+//     outer panel's columns (kUpdNear: [k+1, k+kOuter]) and the rest (kUpdFar)
+//   inner step (the panel continues after k; cl its last block column):
+//     Schur  A_rc -= L_rk L_ck^T                       rows r > k, column pairs c in (k, min(r, cl)]
+//     subst  C'_cr -= U_ck L_rk^T                      c <= k, row pairs r in (k, cl]
+enum { kUpdInner = 0, kUpdFull = 1, kUpdNear = 2, kUpdFar = 3 };
 struct UpdShape {
-  int outer, p0, cl;
+  int outer, p0, c_lo, c_hi;
   long long nschur, nsub;
 };
-__host__ __device__ inline UpdShape upd_shape(int T, int k) {
+__host__ __device__ inline UpdShape upd_shape(int T, int k, int mode) {
   UpdShape sh;
   sh.p0 = k - k % kOuter;
-  sh.outer = (k % kOuter) == kOuter - 1;
-  const int pe = sh.p0 + kOuter < T ? sh.p0 + kOuter : T;
-  sh.cl = pe - 1;
-  sh.nschur = sh.nsub = 0;
-  if (k + 1 >= T) return sh;
-  if (sh.outer) {
-    const int R = T - k - 1;
-    sh.nschur = it_pairs(R);
-    sh.nsub = (long long)(k + 1) * ((R + 1) / 2);
-  } else if (sh.cl > k) {
-    for (int r = k + 1; r < sh.cl; ++r) sh.nschur += upd_row_pairs(r, k, sh.cl);
-    sh.nschur += (long long)(T - sh.cl) * upd_row_pairs(sh.cl, k, sh.cl);
-    sh.nsub = (long long)(k + 1) * ((sh.cl - k + 1) / 2);
+  sh.outer = mode != kUpdInner;
+  if (mode == kUpdInner) {
+    sh.c_lo = k + 1;
+    sh.c_hi = (sh.p0 + kOuter < T ? sh.p0 + kOuter : T) - 1;
+  } else if (mode == kUpdFull) {
+    sh.c_lo = k + 1;
+    sh.c_hi = T - 1;
+  } else if (mode == kUpdNear) {
+    sh.c_lo = k + 1;
+    sh.c_hi = k + kOuter < T - 1 ? k + kOuter : T - 1;
+  } else {
+    sh.c_lo = k + kOuter + 1;
+    sh.c_hi = T - 1;
   }
+  sh.nschur = sh.nsub = 0;
+  if (sh.c_lo > T - 1 || sh.c_hi < sh.c_lo) return sh;
+  // rows [c_lo, c_hi) pair the columns [c_lo, r]; rows from c_hi on all pair [c_lo, c_hi]
+  const int r1 = (sh.c_hi < T ? sh.c_hi : T) - sh.c_lo;
+  const int cmax = (sh.c_hi - sh.c_lo + 2) / 2;
+  sh.nschur = it_pairs(r1) + (long long)(T > sh.c_hi ? T - sh.c_hi : 0) * cmax;
+  const int rl = sh.c_hi < T - 1 ? sh.c_hi : T - 1;
+  sh.nsub = (long long)(k + 1) * ((rl - sh.c_lo + 2) / 2);
   return sh;
 }
 
@@ -168,34 +178,29 @@ __device__ ItJob it_decode(const ItParams& prm, long long u) {
     J.o_x = k * 128;
     J.mode = r > k ? 0 : 1;
   } else if (KIND == kItUpdate) {
-    const UpdShape sh = upd_shape(T, k);
+    const UpdShape sh = upd_shape(T, k, prm.upd_mode);
+    const int lp_off = prm.lp_off;  // this outer panel's half of the double-buffered Lp
     J.mb = &prm.mLB;
     J.b_box = 256;
     if (q < sh.nschur) {
+      const int r1 = (sh.c_hi < T ? sh.c_hi : T) - sh.c_lo;
       int r, cp;
-      if (sh.outer) {
+      if (q < it_pairs(r1)) {
         int jrow = 1;
-        while (it_pairs(jrow) <= q) ++jrow;  // rows r = k + jrow
+        while (it_pairs(jrow) <= q) ++jrow;
+        r = sh.c_lo + jrow - 1;
         cp = (int)(q - it_pairs(jrow - 1));
-        r = k + jrow;
       } else {
-        long long qq = q;
-        r = k + 1;
-        while (r < sh.cl && qq >= upd_row_pairs(r, k, sh.cl)) qq -= upd_row_pairs(r++, k, sh.cl);
-        if (r < sh.cl) {
-          cp = (int)qq;
-        } else {  // rows from cl on all have the same pairs
-          const int cmax = upd_row_pairs(sh.cl, k, sh.cl);
-          r = sh.cl + (int)(qq / cmax);
-          cp = (int)(qq % cmax);
-        }
+        const int cmax = (sh.c_hi - sh.c_lo + 2) / 2;
+        const long long qq = q - it_pairs(r1);
+        r = sh.c_hi + (int)(qq / cmax);
+        cp = (int)(qq % cmax);
       }
-      const int c = k + 1 + 2 * cp;
-      const int last = sh.outer ? r : min(r, sh.cl);
-      const int w = min(2, last - c + 1);
+      const int c = sh.c_lo + 2 * cp;
+      const int w = min(2, min(r, sh.c_hi) - c + 1);
       J.ma = &prm.mLA;
-      J.a_y = (int)(ro + r * 128);
-      J.b_y = (int)(ro + c * 128);
+      J.a_y = (int)(lp_off + ro + r * 128);
+      J.b_y = (int)(lp_off + ro + c * 128);
       J.a_x0 = J.b_x0 = sh.outer ? 0 : (k - sh.p0) * 128;
       J.K = sh.outer ? (k + 1 - sh.p0) * 128 : 128;
       J.n_mma = 128 * w;
@@ -204,14 +209,14 @@ __device__ ItJob it_decode(const ItParams& prm, long long u) {
       J.mode = 0;
     } else {
       const long long q2 = q - sh.nschur;
-      const int rlast = sh.outer ? T - 1 : sh.cl;  // rows r in (k, rlast]
-      const int hp = (rlast - k + 1) / 2;
+      const int rl = sh.c_hi < T - 1 ? sh.c_hi : T - 1;  // rows r in [c_lo, rl]
+      const int hp = (rl - sh.c_lo + 2) / 2;
       const int c = (int)(q2 / hp), rp = (int)(q2 % hp);
-      const int r = k + 1 + 2 * rp;
-      const int w = min(2, rlast - r + 1);
+      const int r = sh.c_lo + 2 * rp;
+      const int w = min(2, rl - r + 1);
       J.ma = &prm.mUA;
       J.a_y = (int)(ro + c * 128);
-      J.b_y = (int)(ro + r * 128);
+      J.b_y = (int)(lp_off + ro + r * 128);
       if (sh.outer) {
         const int j0 = max(c, sh.p0);  // U_cj = 0 for j < c
         J.a_x0 = j0 * 128;
@@ -422,8 +427,8 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         uint16_t* dst;
         long long sstride;
         if (J.mode == 0) {
-          dst = prm.b.lp + (long long)(J.o_y + mrow) * kLpW + (long long)((J.o_x / 128) % kOuter) * 128;
-          sstride = prm.b.R * kLpW;
+          dst = prm.b.lp + (long long)(prm.lp_off + J.o_y + mrow) * kLpW + (long long)((J.o_x / 128) % kOuter) * 128;
+          sstride = 2 * prm.b.R * kLpW;
         } else {
           dst = prm.b.u + (long long)(J.o_y + mrow) * prm.b.LD + J.o_x;
           sstride = prm.b.R * prm.b.LD;
@@ -807,7 +812,7 @@ TcLayout tc_layout(int n, const int* T) {
   L.p = off;
   off += al256((size_t)kSlices * R * 128 * 2);
   L.lp = off;
-  off += al256((size_t)kSlices * R * kLpW * 2);
+  off += al256((size_t)kSlices * 2 * R * kLpW * 2);  // two outer panels' worth (see run_tc_pass)
   L.winv = off;
   off += al256((size_t)kSlices * n * 128 * 128 * 2);
   L.bytes = off;
@@ -843,32 +848,81 @@ static bool enc_slices(EncodeTiledFn enc, CUtensorMap* map, uint16_t* base, long
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Job counts of one launch (filling prm->job_begin); *work gets the launch's
+// multiply-add volume in 128 x 128 x 128 tile units.
 template <int KIND>
-static int launch_it(ItParams* prm, const int* Ts, int n, int k, int sms, cudaStream_t stream) {
+static long long count_jobs(ItParams* prm, const int* Ts, int n, int k, int upd_mode, double* work) {
   long long jobs = 0;
+  double w = 0.0;
   for (int i = 0; i < n; ++i) {
     prm->job_begin[i] = (int)jobs;
     long long cnt = 0;
     const int T = Ts[i];
     if (KIND == kItPanel) {
       cnt = T > k ? T - 1 : 0;
+      w += (double)cnt;
     } else if (KIND == kItUpdate) {
-      const UpdShape sh = upd_shape(T, k);
+      const UpdShape sh = upd_shape(T, k, upd_mode);
       cnt = sh.nschur + sh.nsub;
+      w += 2.0 * (double)cnt * (sh.outer ? (k + 1 - sh.p0) : 1);
     } else {
       cnt = it_pairs(T);
     }
     jobs += cnt;
   }
   prm->job_begin[n] = (int)jobs;
+  if (work) *work = w;
+  return jobs;
+}
+
+template <int KIND>
+static int launch_it(ItParams* prm, const int* Ts, int n, int k, int grid_cap, cudaStream_t stream,
+                     int upd_mode = kUpdInner) {
+  const long long jobs = count_jobs<KIND>(prm, Ts, n, k, upd_mode, nullptr);
   prm->total_jobs = jobs;
   prm->k = k;
+  prm->upd_mode = upd_mode;
   if (jobs == 0) return KFAC_OK;
-  const int grid = (int)(jobs < sms ? jobs : sms);
+  const int grid = (int)(jobs < grid_cap ? jobs : grid_cap);
   inv_tc_kernel<KIND><<<grid, kItThreads, kItSmem, stream>>>(*prm);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
+
+// A highest-priority stream of this library per device and the events that
+// fork work from the caller's stream onto it and join it back (created once,
+// kept until exit).
+struct AuxStream {
+  cudaStream_t hi = nullptr;
+  cudaEvent_t start = nullptr, fork = nullptr, join = nullptr, end = nullptr;
+};
+static bool aux_stream(int dev, AuxStream* out) {
+  static std::mutex mu;
+  static AuxStream table[64];
+  if (dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  AuxStream& t = table[dev];
+  if (!t.hi) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
+    cudaEvent_t ev[4];
+    for (int i = 0; i < 4; ++i)
+      if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return false;
+    cudaStream_t st;
+    if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
+    t.start = ev[0];
+    t.fork = ev[1];
+    t.join = ev[2];
+    t.end = ev[3];
+    t.hi = st;
+  }
+  *out = t;
+  return true;
+}
+
+// Jobs per CTA of a far update: its CTAs retire every few jobs, so that the
+// higher-priority chain on the other stream finds SMs within tens of us.
+constexpr int kFarJobsPerCta = 4;
 
 int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, const int* Ts, const TcLayout& L,
                 cudaStream_t stream) {
@@ -900,8 +954,8 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   ItParams* prm = new ItParams;
   memset(prm, 0, sizeof(ItParams));
   bool ok = enc_slices(enc, &prm->mUA, b.u, b.R, b.LD, 128) && enc_slices(enc, &prm->mUB, b.u, b.R, b.LD, 256) &&
-            enc_slices(enc, &prm->mP, b.p, b.R, 128, 128) && enc_slices(enc, &prm->mLA, b.lp, b.R, kLpW, 128) &&
-            enc_slices(enc, &prm->mLB, b.lp, b.R, kLpW, 256) &&
+            enc_slices(enc, &prm->mP, b.p, b.R, 128, 128) && enc_slices(enc, &prm->mLA, b.lp, 2 * b.R, kLpW, 128) &&
+            enc_slices(enc, &prm->mLB, b.lp, 2 * b.R, kLpW, 256) &&
             enc_slices(enc, &prm->mW, b.winv, (long long)n * 128, 128, 128);
   {
     cuuint64_t gdim[2] = {(cuuint64_t)b.LD, (cuuint64_t)b.R};
@@ -927,27 +981,82 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   prm->n = n;
 
   int rc = KFAC_OK;
-  tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, 0, stream>>>(ctx, b);
-  count_launch();
-  if (ctx.want_rowsum) {
-    tc_norms_kernel<<<dim3((unsigned)Tmax, n), 256, kNormsSmem, stream>>>(ctx, b);
-    count_launch();
+  // Look-ahead: at the last step of each outer panel the trailing update is
+  // cut into the next outer panel's block columns (near) and the rest (far).
+  // The sweep itself (diagonal blocks, slicing, panels, inner and near
+  // updates) runs on the library's highest-priority stream; each far update
+  // runs on the caller's stream, in CTAs of a few jobs, and is joined before
+  // the next outer step.  Whenever SMs come free the hardware gives them to
+  // the sweep first, and the far update fills the rest.  The next panel's
+  // steps only touch their own block columns, and the far update's inputs stay
+  // intact meanwhile: Lp is double-buffered between outer panels, and the next
+  // panel writes U only in its own block columns.
+  AuxStream aux;
+  const bool fork_ok = aux_stream(dev, &aux);
+  cudaStream_t main = stream;  // the sweep's stream
+  if (fork_ok) {
+    if (cudaEventRecord(aux.start, stream) != cudaSuccess || cudaStreamWaitEvent(aux.hi, aux.start, 0) != cudaSuccess)
+      rc = KFAC_ERR_CUDA;
+    main = aux.hi;
   }
-  for (int k = 0; k < Tmax && rc == KFAC_OK; ++k) {
-    tc_diag_kernel<<<n, 256, diag_smem_bytes<float>(), stream>>>(ctx, b, k);
+  if (rc == KFAC_OK) {
+    tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, 0, main>>>(ctx, b);
     count_launch();
-    if (Tmax > 1) {
-      tc_prep_kernel<<<dim3((unsigned)(Tmax - 1), n), 256, 0, stream>>>(ctx, b, k);
+    if (ctx.want_rowsum) {
+      tc_norms_kernel<<<dim3((unsigned)Tmax, n), 256, kNormsSmem, main>>>(ctx, b);
       count_launch();
     }
-    rc = launch_it<kItPanel>(prm, Ts, n, k, sms, stream);
-    if (rc == KFAC_OK) rc = launch_it<kItUpdate>(prm, Ts, n, k, sms, stream);
   }
-  if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, stream);
+  bool pending = false;  // a far update in flight on `stream`
+  for (int k = 0; k < Tmax && rc == KFAC_OK; ++k) {
+    prm->lp_off = (int)(((k / kOuter) & 1) * b.R);
+    tc_diag_kernel<<<n, 256, diag_smem_bytes<float>(), main>>>(ctx, b, k);
+    count_launch();
+    if (Tmax > 1) {
+      tc_prep_kernel<<<dim3((unsigned)(Tmax - 1), n), 256, 0, main>>>(ctx, b, k);
+      count_launch();
+    }
+    rc = launch_it<kItPanel>(prm, Ts, n, k, sms, main);
+    if (rc != KFAC_OK) break;
+    if (k % kOuter != kOuter - 1) {
+      rc = launch_it<kItUpdate>(prm, Ts, n, k, sms, main, kUpdInner);
+      continue;
+    }
+    if (pending) {
+      if (cudaStreamWaitEvent(main, aux.join, 0) != cudaSuccess) {
+        rc = KFAC_ERR_CUDA;
+        break;
+      }
+      pending = false;
+    }
+    const long long far_jobs = fork_ok ? count_jobs<kItUpdate>(prm, Ts, n, k, kUpdFar, nullptr) : 0;
+    if (far_jobs < 2 * sms) {
+      rc = launch_it<kItUpdate>(prm, Ts, n, k, sms, main, kUpdFull);
+      continue;
+    }
+    if (cudaEventRecord(aux.fork, main) != cudaSuccess || cudaStreamWaitEvent(stream, aux.fork, 0) != cudaSuccess) {
+      rc = KFAC_ERR_CUDA;
+      break;
+    }
+    const int far_grid = (int)((far_jobs + kFarJobsPerCta - 1) / kFarJobsPerCta);
+    rc = launch_it<kItUpdate>(prm, Ts, n, k, far_grid, stream, kUpdFar);
+    if (rc != KFAC_OK) break;
+    if (cudaEventRecord(aux.join, stream) != cudaSuccess) {
+      rc = KFAC_ERR_CUDA;
+      break;
+    }
+    pending = true;
+    rc = launch_it<kItUpdate>(prm, Ts, n, k, sms, main, kUpdNear);
+  }
+  if (pending && cudaStreamWaitEvent(main, aux.join, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
+  if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, main);
   if (rc == KFAC_OK && ctx.want_rowsum) {
-    tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, stream>>>(ctx);
+    tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, main>>>(ctx);
     count_launch();
   }
+  // everything is ordered on the caller's stream again
+  if (fork_ok && (cudaEventRecord(aux.end, main) != cudaSuccess || cudaStreamWaitEvent(stream, aux.end, 0) != cudaSuccess))
+    rc = KFAC_ERR_CUDA;
   delete prm;
   if (rc == KFAC_OK && cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
   return rc;
