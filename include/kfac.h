@@ -148,9 +148,11 @@ int kfac_update_running(int n, const kfac_running_args* args, int P,
  * symmetric).  Matrices may have different sizes.
  *
  * refine: KFAC_REFINE_NONE   fp32 arithmetic for every matrix;
- *         KFAC_REFINE_AUTO   fp32, then matrices whose condition estimate
- *                            ||D||_1 / min_j L_jj^2 exceeds 1e5 (or whose fp32
- *                            factorisation failed) are recomputed in fp64;
+ *         KFAC_REFINE_AUTO   fp32, then a matrix is recomputed in fp64 when
+ *                            its residual ||inv D - I||_F / sqrt(d), estimated
+ *                            with four random +-1 probes, exceeds 2.5e-4, when
+ *                            ||D||_1 / min_j L_jj^2 exceeds 3e5, or when its
+ *                            fp32 factorisation failed;
  *         KFAC_REFINE_ALWAYS fp64 arithmetic for every matrix.
  * info: device int[n]; info[i] = 0 on success, k > 0 when the k-th pivot
  *       (1-based) is not positive (LAPACK potrf convention); inv_i is then
@@ -158,7 +160,12 @@ int kfac_update_running(int n, const kfac_running_args* args, int P,
  *       from the fp32 pass, 1 from the fp64 pass.
  * ld_in, ld_out % 4 == 0.  n <= 4096, 1 <= d <= 65536.
  * Workspace: kfac_damped_inverse_workspace(n, args, refine) bytes, 256-byte
- * aligned, fully overwritten (no initialisation needed).                     */
+ * aligned, fully overwritten (no initialisation needed).
+ * Streams: part of the work runs on a highest-priority stream that the
+ * library creates once per device (with its events), forked from `stream`
+ * after the work already queued there and joined back into `stream` before
+ * the call returns, so ordering on `stream` is as for a single-stream call.
+ * Calls on one device from several host threads share that stream.          */
 enum kfac_refine { KFAC_REFINE_NONE = 0, KFAC_REFINE_AUTO = 1, KFAC_REFINE_ALWAYS = 2 };
 
 typedef struct {

@@ -556,12 +556,14 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
 }
 
 // ------------------------------------------------------------------ ||D||_1 and w = D v (AUTO)
-// One CTA per 128-row block R of a matrix: the rows of R gather their sums
-// from the lower tiles (R, C <= R) row-wise and from the tiles (C > R, R)
-// column-wise (D is symmetric), so no atomics are needed.  Each row is split
-// between two threads (64 columns of every tile each); the probe sums w = D v
-// are double-float (the products with v = +-1 are exact).
-__global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c, TcBufs b) {
+// One CTA per 128-row block R of a matrix, straight from the upper triangle of
+// the caller's damped matrix plus gamma_extra on the diagonal, so that it can
+// run beside the sweep: the rows of R gather their
+// sums from the tiles (R, C >= R) row-wise and from the tiles (C < R, R)
+// column-wise, and no atomics are needed.  Each row is split between two
+// threads (64 columns of every tile each); the probe sums w = D v are
+// double-float (the products with v = +-1 are exact).
+__global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c) {
   const int mi = blockIdx.y;
   if (!inv_active(c, mi, false)) return;
   const InvMat m = c.mats[mi];
@@ -571,23 +573,26 @@ __global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c, TcBufs b) {
   float* tile = reinterpret_cast<float*>(norms_smem);  // 128 x 129
   float* vs = tile + 128 * 129;                        // kProbes x 128 probe signs of the tile's columns
   float* xch = vs + kProbes * 128;                     // 128 x kNormsXch sums of the second half of the threads
-  const float* A = b.acc + m.row_off * b.LD;
   const int t = threadIdx.x, row = t % 128, half = t / 128;
-  // thread (row, half) sums the entries (r, cidx) of its row with cidx in the
-  // tile's columns [64 half, 64 half + 64)
   float asum = 0.f;  // row abs sum (a norm for a threshold: plain fp32)
   float whi[kProbes], wlo[kProbes];
 #pragma unroll
   for (int p = 0; p < kProbes; ++p) whi[p] = wlo[p] = 0.f;
   const long long r = (long long)R * 128 + row;
   for (int C = 0; C < m.T; ++C) {
-    const bool rowwise = C <= R;  // tile (R, C) read along rows; else tile (C, R) along columns
-    const float* src = rowwise ? A + (long long)R * 128 * b.LD + (long long)C * 128
-                               : A + (long long)C * 128 * b.LD + (long long)R * 128;
+    const bool rowwise = C >= R;  // tile (R, C) read along rows; else tile (C, R) along columns
+    const long long sr = (long long)(rowwise ? R : C) * 128, sc = (long long)(rowwise ? C : R) * 128;
     __syncthreads();
-    for (int e = t; e < 128 * 32; e += 256) {  // 128 rows x 32 float4
+    for (int e = t; e < 128 * 32; e += 256) {  // 128 rows x 32 float4; ld_in % 4 == 0 keeps them in the row
       const int rr = e / 32, c4 = (e % 32) * 4;
-      const float4 v = *reinterpret_cast<const float4*>(src + (long long)rr * b.LD + c4);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      const long long gr = sr + rr, gc = sc + c4;
+      if (gr < m.d && gc < m.d) {
+        v = *reinterpret_cast<const float4*>(m.D + gr * m.ld_in + gc);
+        if (gc + 1 >= m.d) v.y = 0.f;
+        if (gc + 2 >= m.d) v.z = 0.f;
+        if (gc + 3 >= m.d) v.w = 0.f;
+      }
       float* dst = tile + rr * 129 + c4;
       dst[0] = v.x;
       dst[1] = v.y;
@@ -605,9 +610,10 @@ __global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c, TcBufs b) {
 #pragma unroll 4
       for (int ii = 0; ii < iend; ++ii) {
         const int i = 64 * half + ii;
-        // row-wise: entry (r, C*128+i) = tile[row][i], stored only on or below the
-        // diagonal of the diagonal tile (the rest by symmetry); column-wise: tile[i][row]
-        const float x = (!rowwise || (C == R && i > row)) ? tile[i * 129 + row] : tile[row * 129 + i];
+        // the caller's matrix is read on and above the diagonal only: the
+        // diagonal tile's lower part comes from its mirror
+        float x = (rowwise && !(C == R && i < row)) ? tile[row * 129 + i] : tile[i * 129 + row];
+        if (C == R && i == row) x += c.gamma_extra;
         asum += fabsf(x);
 #pragma unroll
         for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vs[p * 128 + i]);  // exact products
@@ -889,12 +895,12 @@ static int launch_it(ItParams* prm, const int* Ts, int n, int k, int grid_cap, c
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
 
-// A highest-priority stream of this library per device and the events that
-// fork work from the caller's stream onto it and join it back (created once,
-// kept until exit).
+// Two streams of this library per device, one of highest and one of lowest
+// priority, and the events that fork work from the caller's stream onto them
+// and join it back (created once, kept until exit).
 struct AuxStream {
-  cudaStream_t hi = nullptr;
-  cudaEvent_t start = nullptr, fork = nullptr, join = nullptr, end = nullptr;
+  cudaStream_t hi = nullptr, lo = nullptr;
+  cudaEvent_t start = nullptr, fork = nullptr, join = nullptr, end = nullptr, norms = nullptr;
 };
 static bool aux_stream(int dev, AuxStream* out) {
   static std::mutex mu;
@@ -905,15 +911,18 @@ static bool aux_stream(int dev, AuxStream* out) {
   if (!t.hi) {
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
-    cudaEvent_t ev[4];
-    for (int i = 0; i < 4; ++i)
+    cudaEvent_t ev[5];
+    for (int i = 0; i < 5; ++i)
       if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return false;
-    cudaStream_t st;
+    cudaStream_t st, sl;
+    if (cudaStreamCreateWithPriority(&sl, cudaStreamNonBlocking, least) != cudaSuccess) return false;
     if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
+    t.lo = sl;
     t.start = ev[0];
     t.fork = ev[1];
     t.join = ev[2];
     t.end = ev[3];
+    t.norms = ev[4];
     t.hi = st;
   }
   *out = t;
@@ -994,6 +1003,7 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   AuxStream aux;
   const bool fork_ok = aux_stream(dev, &aux);
   cudaStream_t main = stream;  // the sweep's stream
+  bool norms_forked = false;
   if (fork_ok) {
     if (cudaEventRecord(aux.start, stream) != cudaSuccess || cudaStreamWaitEvent(aux.hi, aux.start, 0) != cudaSuccess)
       rc = KFAC_ERR_CUDA;
@@ -1002,9 +1012,13 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   if (rc == KFAC_OK) {
     tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, 0, main>>>(ctx, b);
     count_launch();
-    if (ctx.want_rowsum) {
-      tc_norms_kernel<<<dim3((unsigned)Tmax, n), 256, kNormsSmem, main>>>(ctx, b);
+    if (ctx.want_rowsum) {  // reads the caller's matrices only: beside the sweep, at lowest priority
+      norms_forked = fork_ok;
+      cudaStream_t ns = fork_ok ? aux.lo : stream;
+      if (fork_ok && cudaStreamWaitEvent(aux.lo, aux.start, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
+      tc_norms_kernel<<<dim3((unsigned)Tmax, n), 256, kNormsSmem, ns>>>(ctx);
       count_launch();
+      if (fork_ok && cudaEventRecord(aux.norms, aux.lo) != cudaSuccess) rc = KFAC_ERR_CUDA;
     }
   }
   bool pending = false;  // a far update in flight on `stream`
@@ -1051,12 +1065,15 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   if (pending && cudaStreamWaitEvent(main, aux.join, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
   if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, main);
   if (rc == KFAC_OK && ctx.want_rowsum) {
+    // y = X w needs the norms' w
+    if (fork_ok && cudaStreamWaitEvent(main, aux.norms, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
     tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, main>>>(ctx);
     count_launch();
   }
-  // everything is ordered on the caller's stream again
+  // everything is ordered on the caller's stream again, also after an error
   if (fork_ok && (cudaEventRecord(aux.end, main) != cudaSuccess || cudaStreamWaitEvent(stream, aux.end, 0) != cudaSuccess))
     rc = KFAC_ERR_CUDA;
+  if (norms_forked && cudaStreamWaitEvent(stream, aux.norms, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
   delete prm;
   if (rc == KFAC_OK && cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
   return rc;
