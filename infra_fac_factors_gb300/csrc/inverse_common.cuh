@@ -120,12 +120,6 @@ __device__ __forceinline__ void pivot_scale(double piv, double& ljj, double& inv
   ljj = sqrt(piv);
   inv = 1.0 / ljj;
 }
-template <typename T>
-__device__ __forceinline__ T dev_rcp(T v);
-template <>
-__device__ __forceinline__ float dev_rcp<float>(float v) { return __frcp_rn(v); }
-template <>
-__device__ __forceinline__ double dev_rcp<double>(double v) { return 1.0 / v; }
 
 constexpr int kDiagPitch = 129;
 template <typename T>
@@ -180,6 +174,7 @@ template <typename T>
 __device__ int block_chol_inv(T* a, int valid, T& min_piv) {
   constexpr int P = kDiagPitch;
   __shared__ T wd[4][32][33];  // inverses of the four 32 x 32 diagonal factors
+  __shared__ T dinv[128];      // 1 / L_jj
   __shared__ T tmp[96][33];    // partial products of the assembly step
   __shared__ int s_fail;
   __shared__ T s_minpiv;
@@ -206,7 +201,10 @@ __device__ int block_chol_inv(T* a, int valid, T& min_piv) {
           T ljj, inv;
           pivot_scale(piv, ljj, inv);
           if (lane > j) x[j] *= inv;
-          if (lane == j) x[j] = ljj;
+          if (lane == j) {
+            x[j] = ljj;
+            dinv[p0 + j] = inv;
+          }
 #pragma unroll
           for (int c = j + 1; c < 32; ++c) {
             const T lcj = __shfl_sync(0xffffffffu, x[j], c);
@@ -228,7 +226,7 @@ __device__ int block_chol_inv(T* a, int valid, T& min_piv) {
         for (int r = 0; r < 32; ++r) w[r] = (r == lane) ? T(1) : T(0);
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
-          w[q] *= dev_rcp<T>(a[(p0 + q) * P + p0 + q]);
+          w[q] *= dinv[p0 + q];
 #pragma unroll
           for (int r = q + 1; r < 32; ++r) w[r] -= a[(p0 + r) * P + p0 + q] * w[q];
         }

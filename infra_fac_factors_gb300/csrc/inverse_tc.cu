@@ -37,13 +37,8 @@
 namespace kfac {
 
 constexpr int kItBK = 32;
-constexpr int kItStages = 2;
 constexpr int kItA = 128 * kItBK * 2;  // one slice of the A tile (8 KB)
-constexpr int kItB = 256 * kItBK * 2;  // one slice of the B tile (16 KB, 128-row boxes use half)
-constexpr int kItStage = kSlices * (kItA + kItB);
-constexpr int kItOutBlock = 4096;  // one 32 x 32 fp32 block
-constexpr int kItOut = 8 * 2 * kItOutBlock;
-constexpr int kItSmem = kItStages * kItStage + kItOut + 1024 + 256;
+constexpr int kItOutBlock = 4096;     // one 32 x 32 fp32 block
 constexpr int kItThreads = 320;
 // 16-wide k-steps accumulated in one TMEM accumulator between two drains into
 // the epilogue's round-to-nearest fp32 sums
@@ -52,6 +47,21 @@ constexpr int kNormsXch = 1 + 2 * kProbes;
 constexpr int kNormsSmem = (128 * 129 + kProbes * 128 + 128 * kNormsXch) * 4;
 
 enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
+
+// Shared-memory ring of each kind: a stage holds one 32-wide k-block of all
+// three slices of A (128 rows) and B.  The panel's B is the 128-row diagonal
+// inverse and its epilogue stores straight to global memory, so it runs four
+// 48 KB stages; the updates and X = U U^T (B of 256 rows) run two 72 KB
+// stages beside 64 KB of epilogue staging (TMA reductions, transposes).
+template <int KIND>
+struct ItCfg {
+  static constexpr int b_rows = KIND == kItPanel ? 128 : 256;
+  static constexpr int stages = KIND == kItPanel ? 4 : 2;
+  static constexpr int b_slice = b_rows * kItBK * 2;
+  static constexpr int stage = kSlices * (kItA + b_slice);
+  static constexpr int out = KIND == kItPanel ? 0 : 8 * 2 * kItOutBlock;
+  static constexpr int smem = stages * stage + out + 1024 + 256;
+};
 
 // Two-level blocking of the update: block columns are grouped in outer panels
 // of kOuter.  Inside an outer panel each step updates only the panel's own
@@ -272,10 +282,11 @@ template <int KIND>
 __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_constant__ ItParams prm) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* out_stage = smem + kItStages * kItStage;
-  uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + kItOut);
-  uint64_t* empty = full + kItStages;
-  uint64_t* acc_full = empty + kItStages;
+  using Cfg = ItCfg<KIND>;
+  uint8_t* out_stage = smem + Cfg::stages * Cfg::stage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + Cfg::out);
+  uint64_t* empty = full + Cfg::stages;
+  uint64_t* acc_full = empty + Cfg::stages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* done_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -283,7 +294,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kItStages; ++s) {
+    for (int s = 0; s < Cfg::stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -310,14 +321,14 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         const uint32_t bytes = kSlices * (kItA + J.b_box * kItBK * 2);
         for (int kb = 0; kb < J.K / kItBK; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
-          uint8_t* s0 = smem + stage * kItStage;
+          uint8_t* s0 = smem + stage * Cfg::stage;
           mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
           for (int s = 0; s < kSlices; ++s) {
             tma_load_3d(s0 + s * kItA, J.ma, J.a_x0 + kb * kItBK, J.a_y, s, &full[stage]);
-            tma_load_3d(s0 + kSlices * kItA + s * kItB, J.mb, J.b_x0 + kb * kItBK, J.b_y, s, &full[stage]);
+            tma_load_3d(s0 + kSlices * kItA + s * Cfg::b_slice, J.mb, J.b_x0 + kb * kItBK, J.b_y, s, &full[stage]);
           }
-          if (++stage == kItStages) {
+          if (++stage == Cfg::stages) {
             stage = 0;
             phase ^= 1;
           }
@@ -339,7 +350,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
             ok = false;
             break;
           }
-          const uint32_t a0 = smem_u32(smem + stage * kItStage);
+          const uint32_t a0 = smem_u32(smem + stage * Cfg::stage);
           const uint32_t b0 = a0 + kSlices * kItA;
 #pragma unroll
           for (int kk = 0; kk < kItBK / 16; ++kk, ++st16) {
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
 #pragma unroll
             for (int s = 0; s < kSlices; ++s) {
               da[s] = it_desc(a0 + s * kItA + off);
-              db[s] = it_desc(b0 + s * kItB + off);
+              db[s] = it_desc(b0 + s * Cfg::b_slice + off);
             }
             tc_mma_bf16(d_tmem, da[0], db[0], idesc, gfirst ? 0u : 1u);
             tc_mma_bf16(d_tmem, da[0], db[1], idesc, 1u);
@@ -373,7 +384,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
             }
           }
           tc_commit(&empty[stage]);
-          if (++stage == kItStages) {
+          if (++stage == Cfg::stages) {
             stage = 0;
             phase ^= 1;
           }
@@ -684,13 +695,15 @@ __global__ void __launch_bounds__(256, 1) tc_diag_kernel(InvCtx c, TcBufs b, int
     return;
   }
   if (t == 0) atomicMin(reinterpret_cast<int*>(&c.st[mi].min_piv), __float_as_int(min_piv));
-  // threads 0..127 write row t of Winv, threads 128..255 row t - 128 of U_kk
-  const int row = t % 128;
-  const bool upper = t >= 128;
-  uint16_t* dst = upper ? b.u + (m.row_off + (long long)k * 128 + row) * b.LD + (long long)k * 128
-                        : b.winv + ((long long)mi * 128 + row) * 128;
-  const long long slice = upper ? b.R * b.LD : (long long)b.n * 128 * 128;
-  for (int c8 = 0; c8 < 128; c8 += 8) {
+  // the 128 rows of Winv, then the 128 rows of U_kk = Winv^T: a half-warp per
+  // row, each lane 8 consecutive columns, so that every store is coalesced
+  const int half = t / 16, c8 = (t % 16) * 8;
+  for (int rr = half; rr < 256; rr += 16) {
+    const bool upper = rr >= 128;
+    const int row = rr % 128;
+    uint16_t* dst = upper ? b.u + (m.row_off + (long long)k * 128 + row) * b.LD + (long long)k * 128
+                          : b.winv + ((long long)mi * 128 + row) * 128;
+    const long long slice = upper ? b.R * b.LD : (long long)b.n * 128 * 128;
     float v8[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e)  // Winv[row][c] (zero above the diagonal), or Winv[c][row]
@@ -740,10 +753,11 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(InvCtx c, TcBufs b, int k)
 // rows of its warp, so w is read once per strip.  Double-float products and sums.
 constexpr int kPrWarpRows = 4;
 constexpr int kPrRows = 8 * kPrWarpRows;
-__global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c) {
+__global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c, int t_only) {
   const int mi = blockIdx.y;
   if (!inv_active(c, mi, true)) return;
   const InvMat m = c.mats[mi];
+  if (t_only && m.T != t_only) return;  // only the matrices of T block rows
   const long long rw = (long long)blockIdx.x * kPrRows + (threadIdx.x / 32) * kPrWarpRows;  // the warp's first row
   if ((long long)blockIdx.x * kPrRows >= m.d) return;
   const int lane = threadIdx.x % 32;
@@ -857,7 +871,8 @@ static bool enc_slices(EncodeTiledFn enc, CUtensorMap* map, uint16_t* base, long
 // Job counts of one launch (filling prm->job_begin); *work gets the launch's
 // multiply-add volume in 128 x 128 x 128 tile units.
 template <int KIND>
-static long long count_jobs(ItParams* prm, const int* Ts, int n, int k, int upd_mode, double* work) {
+static long long count_jobs(ItParams* prm, const int* Ts, int n, int k, int upd_mode, double* work,
+                            int t_only = 0) {
   long long jobs = 0;
   double w = 0.0;
   for (int i = 0; i < n; ++i) {
@@ -872,7 +887,7 @@ static long long count_jobs(ItParams* prm, const int* Ts, int n, int k, int upd_
       cnt = sh.nschur + sh.nsub;
       w += 2.0 * (double)cnt * (sh.outer ? (k + 1 - sh.p0) : 1);
     } else {
-      cnt = it_pairs(T);
+      cnt = (t_only == 0 || T == t_only) ? it_pairs(T) : 0;
     }
     jobs += cnt;
   }
@@ -883,14 +898,14 @@ static long long count_jobs(ItParams* prm, const int* Ts, int n, int k, int upd_
 
 template <int KIND>
 static int launch_it(ItParams* prm, const int* Ts, int n, int k, int grid_cap, cudaStream_t stream,
-                     int upd_mode = kUpdInner) {
-  const long long jobs = count_jobs<KIND>(prm, Ts, n, k, upd_mode, nullptr);
+                     int upd_mode = kUpdInner, int t_only = 0) {
+  const long long jobs = count_jobs<KIND>(prm, Ts, n, k, upd_mode, nullptr, t_only);
   prm->total_jobs = jobs;
   prm->k = k;
   prm->upd_mode = upd_mode;
   if (jobs == 0) return KFAC_OK;
   const int grid = (int)(jobs < grid_cap ? jobs : grid_cap);
-  inv_tc_kernel<KIND><<<grid, kItThreads, kItSmem, stream>>>(*prm);
+  inv_tc_kernel<KIND><<<grid, kItThreads, ItCfg<KIND>::smem, stream>>>(*prm);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
@@ -900,7 +915,8 @@ static int launch_it(ItParams* prm, const int* Ts, int n, int k, int grid_cap, c
 // and join it back (created once, kept until exit).
 struct AuxStream {
   cudaStream_t hi = nullptr, lo = nullptr;
-  cudaEvent_t start = nullptr, fork = nullptr, join = nullptr, end = nullptr, norms = nullptr;
+  cudaEvent_t start = nullptr, fork = nullptr, join = nullptr, end = nullptr, norms = nullptr, early = nullptr,
+              lodone = nullptr;
 };
 static bool aux_stream(int dev, AuxStream* out) {
   static std::mutex mu;
@@ -911,8 +927,8 @@ static bool aux_stream(int dev, AuxStream* out) {
   if (!t.hi) {
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
-    cudaEvent_t ev[5];
-    for (int i = 0; i < 5; ++i)
+    cudaEvent_t ev[7];
+    for (int i = 0; i < 7; ++i)
       if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return false;
     cudaStream_t st, sl;
     if (cudaStreamCreateWithPriority(&sl, cudaStreamNonBlocking, least) != cudaSuccess) return false;
@@ -923,6 +939,8 @@ static bool aux_stream(int dev, AuxStream* out) {
     t.join = ev[2];
     t.end = ev[3];
     t.norms = ev[4];
+    t.early = ev[5];
+    t.lodone = ev[6];
     t.hi = st;
   }
   *out = t;
@@ -941,9 +959,9 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return KFAC_ERR_CUDA;
-  if (!ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItPanel>, kItSmem) ||
-      !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItUpdate>, kItSmem) ||
-      !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItLauum>, kItSmem) ||
+  if (!ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItPanel>, ItCfg<kItPanel>::smem) ||
+      !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItUpdate>, ItCfg<kItUpdate>::smem) ||
+      !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItLauum>, ItCfg<kItLauum>::smem) ||
       !ensure_smem_attr(dev, (const void*)tc_diag_kernel, diag_smem_bytes<float>()) ||
       !ensure_smem_attr(dev, (const void*)tc_norms_kernel, kNormsSmem))
     return KFAC_ERR_CUDA;
@@ -1022,7 +1040,27 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
     }
   }
   bool pending = false;  // a far update in flight on `stream`
+  bool early_any = false;
   for (int k = 0; k < Tmax && rc == KFAC_OK; ++k) {
+    // matrices of k block rows finished their sweep at step k - 1: their
+    // X = U U^T and residual probe run now, at lowest priority, in CTAs of
+    // two jobs, beside the larger matrices' sweep
+    bool ends_here = false;
+    for (int i = 0; i < n; ++i) ends_here = ends_here || Ts[i] == k;
+    if (fork_ok && k > 0 && ends_here) {
+      if (cudaEventRecord(aux.early, main) != cudaSuccess || cudaStreamWaitEvent(aux.lo, aux.early, 0) != cudaSuccess) {
+        rc = KFAC_ERR_CUDA;
+        break;
+      }
+      const long long lj = count_jobs<kItLauum>(prm, Ts, n, 0, kUpdInner, nullptr, k);
+      rc = launch_it<kItLauum>(prm, Ts, n, 0, (int)((lj + 1) / 2), aux.lo, kUpdInner, k);
+      if (rc != KFAC_OK) break;
+      if (ctx.want_rowsum) {
+        tc_probe_kernel<<<dim3((unsigned)(k * 128 / kPrRows), n), 256, 0, aux.lo>>>(ctx, k);
+        count_launch();
+      }
+      early_any = true;
+    }
     prm->lp_off = (int)(((k / kOuter) & 1) * b.R);
     tc_diag_kernel<<<n, 256, diag_smem_bytes<float>(), main>>>(ctx, b, k);
     count_launch();
@@ -1063,13 +1101,19 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
     rc = launch_it<kItUpdate>(prm, Ts, n, k, sms, main, kUpdNear);
   }
   if (pending && cudaStreamWaitEvent(main, aux.join, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
-  if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, main);
+  // the matrices that finished last (all of them when nothing was started early)
+  const int t_last = early_any ? Tmax : 0;
+  if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, main, kUpdInner, t_last);
   if (rc == KFAC_OK && ctx.want_rowsum) {
     // y = X w needs the norms' w
     if (fork_ok && cudaStreamWaitEvent(main, aux.norms, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
-    tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, main>>>(ctx);
+    tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, main>>>(ctx, t_last);
     count_launch();
   }
+  // the early X = U U^T and probes on the lowest-priority stream
+  if (early_any && (cudaEventRecord(aux.lodone, aux.lo) != cudaSuccess ||
+                    cudaStreamWaitEvent(main, aux.lodone, 0) != cudaSuccess))
+    rc = KFAC_ERR_CUDA;
   // everything is ordered on the caller's stream again, also after an error
   if (fork_ok && (cudaEventRecord(aux.end, main) != cudaSuccess || cudaStreamWaitEvent(stream, aux.end, 0) != cudaSuccess))
     rc = KFAC_ERR_CUDA;
