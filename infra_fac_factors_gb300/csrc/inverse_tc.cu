@@ -43,6 +43,7 @@ constexpr int kItThreads = 320;
 // 16-wide k-steps accumulated in one TMEM accumulator between two drains into
 // the epilogue's round-to-nearest fp32 sums
 constexpr int kItDrain = 2;
+constexpr int kLoadSmem = 128 * 129 * 4;
 constexpr int kNormsXch = 1 + 2 * kProbes;
 constexpr int kNormsSmem = (128 * 129 + kProbes * 128 + 128 * kNormsXch) * 4;
 
@@ -527,32 +528,44 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
   if (q >= tri(m.T)) return;
   const int R = tri_root(q), C = (int)(q - tri(R));  // lower tile (R, C), R >= C
   float* A = b.acc + m.row_off * b.LD;
-  __shared__ float sub[32][33];
-  const int lx = threadIdx.x % 32, ly = threadIdx.x / 32;  // 32 x 8
-  for (int sb = 0; sb < 16; ++sb) {
-    const int bm = (sb / 4) * 32, bn = (sb % 4) * 32;  // sub-block rows (mm) / cols (nn) of the tile
-    // read D[C*128 + bn + y][R*128 + bm + x] (coalesced along x), store sub[y][x]
-    for (int y = ly; y < 32; y += 8) {
-      const long long gc = (long long)C * 128 + bn + y;   // D row   = tile column
-      const long long gr = (long long)R * 128 + bm + lx;  // D column = tile row
-      float v = 0.f;
-      if (gc < m.d && gr < m.d && gr >= gc) v = m.D[gc * m.ld_in + gr];
-      sub[y][lx] = v;
-    }
-    __syncthreads();
-    for (int y = ly; y < 32; y += 8) {
-      const long long gr = (long long)R * 128 + bm + y;
-      const long long gc = (long long)C * 128 + bn + lx;
-      float out;
+  extern __shared__ __align__(16) uint8_t load_smem[];
+  float* sub = reinterpret_cast<float*>(load_smem);  // 128 x 129: sub[i][j] = D[C*128 + i][R*128 + j]
+  const int t = threadIdx.x;
+  // read the upper tile (C, R) of D along its rows, 16 float4 per thread (ld_in % 4 == 0
+  // keeps a float4 that starts inside the row inside it)
+#pragma unroll 4
+  for (int e = t; e < 128 * 32; e += 256) {
+    const int i = e / 32, j4 = (e % 32) * 4;
+    const long long gc = (long long)C * 128 + i, gr = (long long)R * 128 + j4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (gc < m.d && gr < m.d) v = *reinterpret_cast<const float4*>(m.D + gc * m.ld_in + gr);
+    float* d = sub + i * 129 + j4;
+    d[0] = v.x;
+    d[1] = v.y;
+    d[2] = v.z;
+    d[3] = v.w;
+  }
+  __syncthreads();
+  // write the lower tile (R, C) of the work buffer along its rows: element
+  // (R*128 + j, C*128 + i) = D(C*128 + i, R*128 + j); identity past d, zero
+  // above the diagonal, gamma_extra on it
+#pragma unroll 4
+  for (int e = t; e < 128 * 32; e += 256) {
+    const int j = e / 32, i4 = (e % 32) * 4;
+    const long long gr = (long long)R * 128 + j;
+    float o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i4 + u;
+      const long long gc = (long long)C * 128 + i;
       if (gr >= m.d || gc >= m.d)
-        out = (gr == gc) ? 1.f : 0.f;
+        o[u] = (gr == gc) ? 1.f : 0.f;
       else if (gr < gc)
-        out = 0.f;
+        o[u] = 0.f;
       else
-        out = sub[lx][y] + ((gr == gc) ? c.gamma_extra : 0.f);
-      A[gr * b.LD + gc] = out;
+        o[u] = sub[i * 129 + j] + ((gr == gc) ? c.gamma_extra : 0.f);
     }
-    __syncthreads();
+    *reinterpret_cast<float4*>(A + gr * b.LD + (long long)C * 128 + i4) = make_float4(o[0], o[1], o[2], o[3]);
   }
   // zero the sub-diagonal U block (R, R-1): the X = U U^T products read it when they pair block rows
   if (R == C + 1) {
@@ -910,13 +923,13 @@ static int launch_it(ItParams* prm, const int* Ts, int n, int k, int grid_cap, c
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
 
-// Two streams of this library per device, one of highest and one of lowest
+// Three streams of this library per device, two of highest and one of lowest
 // priority, and the events that fork work from the caller's stream onto them
 // and join it back (created once, kept until exit).
 struct AuxStream {
-  cudaStream_t hi = nullptr, lo = nullptr;
+  cudaStream_t hi = nullptr, hi2 = nullptr, lo = nullptr;
   cudaEvent_t start = nullptr, fork = nullptr, join = nullptr, end = nullptr, norms = nullptr, early = nullptr,
-              lodone = nullptr;
+              lodone = nullptr, prep0 = nullptr, prep1 = nullptr;
 };
 static bool aux_stream(int dev, AuxStream* out) {
   static std::mutex mu;
@@ -927,13 +940,15 @@ static bool aux_stream(int dev, AuxStream* out) {
   if (!t.hi) {
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
-    cudaEvent_t ev[7];
-    for (int i = 0; i < 7; ++i)
+    cudaEvent_t ev[9];
+    for (int i = 0; i < 9; ++i)
       if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return false;
-    cudaStream_t st, sl;
+    cudaStream_t st, st2, sl;
     if (cudaStreamCreateWithPriority(&sl, cudaStreamNonBlocking, least) != cudaSuccess) return false;
+    if (cudaStreamCreateWithPriority(&st2, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
     if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
     t.lo = sl;
+    t.hi2 = st2;
     t.start = ev[0];
     t.fork = ev[1];
     t.join = ev[2];
@@ -941,6 +956,8 @@ static bool aux_stream(int dev, AuxStream* out) {
     t.norms = ev[4];
     t.early = ev[5];
     t.lodone = ev[6];
+    t.prep0 = ev[7];
+    t.prep1 = ev[8];
     t.hi = st;
   }
   *out = t;
@@ -963,7 +980,8 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItUpdate>, ItCfg<kItUpdate>::smem) ||
       !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItLauum>, ItCfg<kItLauum>::smem) ||
       !ensure_smem_attr(dev, (const void*)tc_diag_kernel, diag_smem_bytes<float>()) ||
-      !ensure_smem_attr(dev, (const void*)tc_norms_kernel, kNormsSmem))
+      !ensure_smem_attr(dev, (const void*)tc_norms_kernel, kNormsSmem) ||
+      !ensure_smem_attr(dev, (const void*)tc_load_kernel, kLoadSmem))
     return KFAC_ERR_CUDA;
   int* status = device_status_ptr();
   if (!status) return KFAC_ERR_CUDA;
@@ -1028,7 +1046,7 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
     main = aux.hi;
   }
   if (rc == KFAC_OK) {
-    tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, 0, main>>>(ctx, b);
+    tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, kLoadSmem, main>>>(ctx, b);
     count_launch();
     if (ctx.want_rowsum) {  // reads the caller's matrices only: beside the sweep, at lowest priority
       norms_forked = fork_ok;
@@ -1062,11 +1080,24 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       early_any = true;
     }
     prm->lp_off = (int)(((k / kOuter) & 1) * b.R);
+    // the diagonal block and the slicing of the rest of block column k are
+    // independent: the slicing runs on the second sweep stream
+    const bool fork_prep = fork_ok && Tmax > 1;
+    if (fork_prep && (cudaEventRecord(aux.prep0, main) != cudaSuccess ||
+                      cudaStreamWaitEvent(aux.hi2, aux.prep0, 0) != cudaSuccess)) {
+      rc = KFAC_ERR_CUDA;
+      break;
+    }
     tc_diag_kernel<<<n, 256, diag_smem_bytes<float>(), main>>>(ctx, b, k);
     count_launch();
     if (Tmax > 1) {
-      tc_prep_kernel<<<dim3((unsigned)(Tmax - 1), n), 256, 0, main>>>(ctx, b, k);
+      tc_prep_kernel<<<dim3((unsigned)(Tmax - 1), n), 256, 0, fork_prep ? aux.hi2 : main>>>(ctx, b, k);
       count_launch();
+    }
+    if (fork_prep && (cudaEventRecord(aux.prep1, aux.hi2) != cudaSuccess ||
+                      cudaStreamWaitEvent(main, aux.prep1, 0) != cudaSuccess)) {
+      rc = KFAC_ERR_CUDA;
+      break;
     }
     rc = launch_it<kItPanel>(prm, Ts, n, k, sms, main);
     if (rc != KFAC_OK) break;
