@@ -76,16 +76,25 @@ struct SyUnit {
   int64_t j0;
 };
 
+// Work unit u -> (problem, shard, row block, columns): binary search over the
+// problems, then the constant-time tile map (all three roles decode every unit).
 __device__ __forceinline__ SyUnit sy_decode(const SyParams& prm, long long u) {
+  int lo = 0, hi = prm.n_probs;  // largest pi with unit_begin <= u
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (prm.probs[mid].unit_begin <= u)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const SyProb& pr = prm.probs[lo];
+  const int local = (int)(u - pr.unit_begin);
   SyUnit r;
-  int pi = 0;
-  while (pi + 1 < prm.n_probs && prm.probs[pi + 1].unit_begin <= u) ++pi;
-  const SyProb& pr = prm.probs[pi];
-  const long long local = u - pr.unit_begin;
-  r.prob = pi;
-  r.p = (int)(local / pr.units_per_shard);
-  const long long t = local % pr.units_per_shard;
-  factor_unit(pr.d, t, r.i, r.j0, r.w);
+  r.prob = lo;
+  r.p = local / pr.units_per_shard;
+  int j0;
+  factor_unit_fast(pr.d, local - r.p * pr.units_per_shard, r.i, j0, r.w);
+  r.j0 = j0;
   return r;
 }
 

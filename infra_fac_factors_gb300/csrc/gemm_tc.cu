@@ -62,15 +62,24 @@ struct GtTile {
   int prob, m0, n0, n_mma, K;
 };
 
+// tile u -> (problem, m0, n0): binary search over the problems, 32-bit
+// arithmetic inside one (every role decodes every tile)
 __device__ __forceinline__ GtTile gt_decode(const GtParams& prm, long long u) {
-  int pi = 0;
-  while (pi + 1 < prm.n_probs && prm.probs[pi + 1].tile_begin <= u) ++pi;
+  int lo = 0, hi = prm.n_probs;  // largest pi with tile_begin <= u
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (prm.probs[mid].tile_begin <= u)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int pi = lo;
   const GtProb& p = prm.probs[pi];
-  const long long t = u - p.tile_begin;
+  const int t = (int)(u - p.tile_begin);
   GtTile r;
   r.prob = pi;
-  r.m0 = (int)(t / p.tiles_n) * 128;
-  r.n0 = (int)(t % p.tiles_n) * 256;
+  r.m0 = (t / p.tiles_n) * 128;
+  r.n0 = (t - (t / p.tiles_n) * p.tiles_n) * 256;
   r.n_mma = (min(256, p.N - r.n0) + 15) / 16 * 16;
   r.K = p.K;
   return r;

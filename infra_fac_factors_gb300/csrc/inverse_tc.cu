@@ -197,10 +197,16 @@ __device__ ItJob it_decode(const ItParams& prm, long long u) {
       const int r1 = (sh.c_hi < T ? sh.c_hi : T) - sh.c_lo;
       int r, cp;
       if (q < it_pairs(r1)) {
-        int jrow = 1;
-        while (it_pairs(jrow) <= q) ++jrow;
-        r = sh.c_lo + jrow - 1;
-        cp = (int)(q - it_pairs(jrow - 1));
+        int lo = 0, hi = r1;  // it_pairs(lo) <= q < it_pairs(hi)
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) / 2;
+          if (it_pairs(mid) <= q)
+            lo = mid;
+          else
+            hi = mid;
+        }
+        r = sh.c_lo + lo;
+        cp = (int)(q - it_pairs(lo));
       } else {
         const int cmax = (sh.c_hi - sh.c_lo + 2) / 2;
         const long long qq = q - it_pairs(r1);
@@ -245,12 +251,18 @@ __device__ ItJob it_decode(const ItParams& prm, long long u) {
       J.o_x = r * 128;
     }
   } else {
-    int i = 0;
-    long long qq = q;
-    while (qq >= (T - i + 1) / 2) {
-      qq -= (T - i + 1) / 2;
-      ++i;
+    // row i holds ceil((T - i) / 2) column pairs, so rows 0 .. i-1 hold
+    // it_pairs(T) - it_pairs(T - i)
+    int lo = 0, hi = T;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) / 2;
+      if (it_pairs(T) - it_pairs(T - mid) <= q)
+        lo = mid;
+      else
+        hi = mid;
     }
+    const int i = lo;
+    const long long qq = q - (it_pairs(T) - it_pairs(T - i));
     const int j = i + 2 * (int)qq;
     const int w = min(2, T - j);
     J.i = i;

@@ -7,6 +7,7 @@
 // work unit each: unit = (row block i, first column j0, width w).  Units are
 // numbered row block by row block, left to right.
 #pragma once
+#include <math.h>
 #include <stdint.h>
 
 namespace kfac {
@@ -42,6 +43,35 @@ __host__ __device__ inline void factor_unit(int64_t d, int64_t t, int& i, int64_
   i = -1;
   j0 = 0;
   w = 0;
+}
+
+// The same map in constant time (32-bit; t < 2^31).  Row blocks 2k and 2k + 1
+// hold n0 - k and n1 - k units (n0 = ceil(d / 256), n1 = floor((d + 127) / 256);
+// a row block past the factor's last one holds none), so the units of the
+// first k pairs of row blocks number C(k) = k (n0 + n1) - k (k - 1), and the
+// pair of unit t is the largest k with C(k) <= t (a quadratic, inverted with
+// one fp32 square root and corrected by +-1).
+__host__ __device__ inline void factor_unit_fast(int d, int t, int& i, int& j0, int& w) {
+  const int n0 = (d + 255) / 256, n1 = (d + 127) / 256, s = n0 + n1;
+  auto C = [&](int k) { return k * s - k * (k - 1); };
+  const float disc = (float)(s + 1) * (float)(s + 1) - 4.0f * (float)t;  // rounding is corrected below
+  int k = (int)(((float)(s + 1) - sqrtf(disc > 0.f ? disc : 0.f)) * 0.5f);
+  if (k < 0) k = 0;
+  while (k > 0 && C(k) > t) --k;
+  while (C(k + 1) <= t && k + 1 <= n0) ++k;
+  const int rem = t - C(k);
+  int r, u;
+  if (rem < n0 - k) {
+    r = 2 * k;
+    u = rem;
+  } else {
+    r = 2 * k + 1;
+    u = rem - (n0 - k);
+  }
+  i = r;
+  j0 = kTileM * r + kTileN * u;
+  const int left = d - j0;
+  w = left < kTileN ? left : kTileN;
 }
 
 }  // namespace kfac

@@ -178,3 +178,38 @@ def test_empty_calls_are_no_ops():
     assert capi.kfac_factors([], capi.KFAC_BF16, 1, check=False) == capi.KFAC_OK
     assert capi.kfac_update_running([], 1, 0.5, 0.0, True, check=False) == capi.KFAC_OK
     assert capi.kfac_precondition([], 0, 0, check=False) == capi.KFAC_OK
+
+
+def test_constant_time_tile_map_equals_enumeration():
+    # the kernels decode work units with factor_unit_fast; it must agree with the
+    # enumerated map (factor_unit, pinned to the oracle above) unit for unit
+    src = r"""
+#include <cstdio>
+#include "tilemap.cuh"
+using namespace kfac;
+int main() {
+  long long bad = 0, n = 0;
+  const int big[] = {16384, 32768, 65536};
+  for (int q = 0; q < 3000 + 3; ++q) {
+    const int d = q < 3000 ? q + 1 + (q / 1000) * 2000 : big[q - 3000];
+    const long long nu = factor_units(d);
+    for (long long t = 0; t < nu; ++t, ++n) {
+      int i1, w1, i2, j2, w2; int64_t j1;
+      factor_unit(d, t, i1, j1, w1);
+      factor_unit_fast(d, (int)t, i2, j2, w2);
+      bad += (i1 != i2 || j1 != j2 || w1 != w2);
+    }
+  }
+  printf("%lld %lld\n", n, bad);
+  return 0;
+}
+"""
+    csrc = os.path.join(ROOT, "infra_fac_factors_gb300", "csrc")
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "t.cpp")
+        exe = os.path.join(td, "t")
+        open(c, "w").write(src)
+        subprocess.run(["g++", "-O2", "-std=c++17", "-D__host__=", "-D__device__=", "-I", csrc, c, "-o", exe],
+                       check=True)
+        n, bad = map(int, subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split())
+    assert n == 988736 and bad == 0
