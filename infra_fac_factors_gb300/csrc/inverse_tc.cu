@@ -251,19 +251,17 @@ __device__ ItJob it_decode(const ItParams& prm, long long u) {
       J.o_x = r * 128;
     }
   } else {
-    // row i holds ceil((T - i) / 2) column pairs, so rows 0 .. i-1 hold
-    // it_pairs(T) - it_pairs(T - i)
-    int lo = 0, hi = T;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) / 2;
-      if (it_pairs(T) - it_pairs(T - mid) <= q)
-        lo = mid;
-      else
-        hi = mid;
-    }
-    const int i = lo;
-    const long long qq = q - (it_pairs(T) - it_pairs(T - i));
-    const int j = i + 2 * (int)qq;
+    // Row i pairs the columns (j, j + 1) for j = i, i + 2, ...; the jobs are
+    // numbered so that consecutive ones share B = U rows (j, j + 1): even rows
+    // first, then odd ones; within a parity class by the pair j = par + 2a,
+    // then by the rows i = par + 2b, b <= a (a + 1 jobs per pair, all with
+    // K = (T - j) * 128).
+    const long long n_even = tri((T + 1) / 2);
+    const int par = q < n_even ? 0 : 1;
+    const long long qp = par ? q - n_even : q;
+    const int a = tri_root(qp);
+    const int i = par + 2 * (int)(qp - tri(a));
+    const int j = par + 2 * a;
     const int w = min(2, T - j);
     J.i = i;
     J.j = j;

@@ -72,7 +72,7 @@ class FactorBufs:
 
 class KFACStep:
     def __init__(self, layers: Sequence[LayerSpec], P: int, gamma: float, decay: float, in_dtype: str,
-                 refine: int = capi.KFAC_REFINE_AUTO, device="cuda", n_groups: int = 4):
+                 refine: int = capi.KFAC_REFINE_AUTO, device="cuda", n_groups: int = 8):
         self.layers = list(layers)
         self.P = P
         self.gamma = float(gamma)
