@@ -161,11 +161,14 @@ int kfac_update_running(int n, const kfac_running_args* args, int P,
  * ld_in, ld_out % 4 == 0.  n <= 4096, 1 <= d <= 65536.
  * Workspace: kfac_damped_inverse_workspace(n, args, refine) bytes, 256-byte
  * aligned, fully overwritten (no initialisation needed).
- * Streams: part of the work runs on a highest-priority stream that the
- * library creates once per device (with its events), forked from `stream`
- * after the work already queued there and joined back into `stream` before
- * the call returns, so ordering on `stream` is as for a single-stream call.
- * Calls on one device from several host threads share that stream.          */
+ * Streams: part of the work runs on streams that the library creates once
+ * (two of highest and one of lowest priority, with their events), forked
+ * from `stream` after the work already queued there and joined back into
+ * `stream` before the call returns, so ordering on `stream` is as for a
+ * single-stream call.  Each caller stream gets its own set (up to four per
+ * device; further caller streams share the first set), so inverses issued on
+ * different streams overlap.  A set is not meant for concurrent calls from
+ * several host threads on the same caller stream.                           */
 enum kfac_refine { KFAC_REFINE_NONE = 0, KFAC_REFINE_AUTO = 1, KFAC_REFINE_ALWAYS = 2 };
 
 typedef struct {

@@ -941,12 +941,26 @@ struct AuxStream {
   cudaEvent_t start = nullptr, fork = nullptr, join = nullptr, end = nullptr, norms = nullptr, early = nullptr,
               lodone = nullptr, prep0 = nullptr, prep1 = nullptr;
 };
-static bool aux_stream(int dev, AuxStream* out) {
+// One set per (device, caller's stream), up to kAuxSets per device, so that
+// inverses issued on different streams run concurrently; further callers share
+// the first set (their work is then ordered one after the other).
+constexpr int kAuxSets = 4;
+static bool aux_stream(int dev, cudaStream_t caller, AuxStream* out) {
   static std::mutex mu;
-  static AuxStream table[64];
+  static AuxStream table[64][kAuxSets];
+  static cudaStream_t owner[64][kAuxSets];
   if (dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lk(mu);
-  AuxStream& t = table[dev];
+  int slot = -1;
+  for (int i = 0; i < kAuxSets && slot < 0; ++i)
+    if (table[dev][i].hi && owner[dev][i] == caller) slot = i;
+  for (int i = 0; i < kAuxSets && slot < 0; ++i)
+    if (!table[dev][i].hi) {
+      slot = i;
+      owner[dev][i] = caller;
+    }
+  if (slot < 0) slot = 0;
+  AuxStream& t = table[dev][slot];
   if (!t.hi) {
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
@@ -1047,7 +1061,7 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   // intact meanwhile: Lp is double-buffered between outer panels, and the next
   // panel writes U only in its own block columns.
   AuxStream aux;
-  const bool fork_ok = aux_stream(dev, &aux);
+  const bool fork_ok = aux_stream(dev, stream, &aux);
   cudaStream_t main = stream;  // the sweep's stream
   bool norms_forked = false;
   if (fork_ok) {

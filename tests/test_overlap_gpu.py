@@ -1,7 +1,8 @@
 """KFACStep.step overlaps the factor pass of one layer group with the
-running-average pass of the previous group on a second stream.  Each kernel's
-result for a factor does not depend on how the layers are grouped, so the
-overlapped step must reproduce the stage-by-stage sequence bit for bit."""
+running-average pass of the previous group on a second stream.  Each
+kernel's result for a factor does not depend on how the layers are grouped,
+so the overlapped step must reproduce the stage-by-stage sequence bit for
+bit."""
 import numpy as np
 import pytest
 import torch
@@ -47,7 +48,7 @@ def run(key, steps, overlapped, n_groups):
             [F.running.cpu().numpy() for F in st.factor_list()])
 
 
-@pytest.mark.parametrize("key,steps,n_groups", [("mlp", 3, 2), ("mlp", 2, 4), ("resnet_conv", 1, 3)])
+@pytest.mark.parametrize("key,steps,n_groups", [("mlp", 3, 2), ("mlp", 2, 4), ("resnet_conv", 1, 3), ("bert_layer", 2, 4)])
 def test_overlapped_step_equals_stage_sequence(key, steps, n_groups):
     seq = run(key, steps, False, n_groups)
     ovl = run(key, steps, True, n_groups)
