@@ -190,7 +190,22 @@ int kfac_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra,
  *     out = inv_g * grad * inv_a        (d_out x d_out)(d_out x d_in)(d_in x d_in)
  * inv_g and inv_a must be full symmetric matrices (as kfac_damped_inverse
  * writes them).  All fp32; every ld % 4 == 0.  out must not alias an input.
- * Workspace: kfac_precondition_workspace(n, args) bytes (holds grad * inv_a). */
+ * Workspace: kfac_precondition_workspace(n, args) bytes (bf16 slices of the
+ * operands and of grad * inv_a, probe vectors, flags), 16-byte aligned.
+ *
+ * precision: the products run on bf16 tensor cores with each fp32 operand
+ * cut into bf16 slices, summed in fp32 with round-to-nearest every twelve MMAs.
+ *   KFAC_PRECOND_FP32  all 24 bits of every operand (six MMAs per multiply-add)
+ *                      for every layer: close to an fp32 FMA loop.
+ *   KFAC_PRECOND_AUTO  16-bit operands (three MMAs), then every layer's result
+ *                      is checked with eight random +-1 probes on each side
+ *                      (the 8 x 8 bilinear forms Z'^T out Z against
+ *                      (inv_g Z')^T grad (inv_a Z), which estimate the relative
+ *                      Frobenius error of out); a layer whose estimate exceeds
+ *                      4e-4, or is not finite, is recomputed as with FP32.
+ * route: NULL, or a device int[n] receiving, per layer, the MMAs per
+ * multiply-add its result came from (3 or 6).  Invalid precision, or a route
+ * pointer not 4-byte aligned, returns KFAC_ERR_INVALID_ARG.                   */
 typedef struct {
   const float* inv_g;  int64_t ld_g;
   const float* grad;   int64_t ld_grad;
@@ -202,8 +217,10 @@ typedef struct {
 
 size_t kfac_precondition_workspace(int n, const kfac_precond_args* args);
 
-int kfac_precondition(int n, const kfac_precond_args* args, void* workspace,
-                      size_t workspace_bytes, void* stream);
+typedef enum { KFAC_PRECOND_FP32 = 0, KFAC_PRECOND_AUTO = 1 } kfac_precond_precision;
+
+int kfac_precondition(int n, const kfac_precond_args* args, int precision, int* route,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* The same preconditioning with no caller-provided workspace and no device
  * allocation, for callers that cannot allocate device memory (their device
@@ -220,7 +237,8 @@ int kfac_precondition(int n, const kfac_precond_args* args, void* workspace,
  * overlap on the GPU (e.g. on two streams at once) race.  Otherwise as
  * kfac_precondition.                                                         */
 size_t kfac_precondition_static_capacity(void);
-int kfac_precondition_static(int n, const kfac_precond_args* args, void* stream);
+int kfac_precondition_static(int n, const kfac_precond_args* args, int precision,
+                             int* route, void* stream);
 
 /* ------------------------------------------------------------- index tables
  * The work units kfac_factors uses to cover the upper tiles of a d x d factor

@@ -13,6 +13,7 @@ __all__ = [
     "KFAC_OK", "KFAC_ERR_INVALID_ARG", "KFAC_ERR_NOT_SPD", "KFAC_ERR_CUDA",
     "KFAC_ERR_UNSUPPORTED", "KFAC_ERR_TIMEOUT", "KFAC_ERR_WORKSPACE",
     "KFAC_BF16", "KFAC_FP32", "KFAC_REFINE_NONE", "KFAC_REFINE_AUTO", "KFAC_REFINE_ALWAYS",
+    "KFAC_PRECOND_FP32", "KFAC_PRECOND_AUTO",
     "kfac_factor_args", "kfac_running_args", "kfac_inverse_args", "kfac_precond_args",
     "KFACError", "lib", "library_path", "exported_symbols",
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status",
@@ -26,6 +27,7 @@ KFAC_OK, KFAC_ERR_INVALID_ARG, KFAC_ERR_NOT_SPD, KFAC_ERR_CUDA = 0, 1, 2, 3
 KFAC_ERR_UNSUPPORTED, KFAC_ERR_TIMEOUT, KFAC_ERR_WORKSPACE = 4, 5, 6
 KFAC_BF16, KFAC_FP32 = 0, 1
 KFAC_REFINE_NONE, KFAC_REFINE_AUTO, KFAC_REFINE_ALWAYS = 0, 1, 2
+KFAC_PRECOND_FP32, KFAC_PRECOND_AUTO = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libkfac_gb300.so")
@@ -87,9 +89,10 @@ def lib() -> C.CDLL:
         "kfac_damped_inverse": (C.c_int, [C.c_int, P(kfac_inverse_args), C.c_float, C.c_int, C.c_void_p,
                                           C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]),
         "kfac_precondition_workspace": (C.c_size_t, [C.c_int, P(kfac_precond_args)]),
-        "kfac_precondition": (C.c_int, [C.c_int, P(kfac_precond_args), C.c_void_p, C.c_size_t, C.c_void_p]),
+        "kfac_precondition": (C.c_int, [C.c_int, P(kfac_precond_args), C.c_int, C.c_void_p, C.c_void_p, C.c_size_t,
+                                        C.c_void_p]),
         "kfac_precondition_static_capacity": (C.c_size_t, []),
-        "kfac_precondition_static": (C.c_int, [C.c_int, P(kfac_precond_args), C.c_void_p]),
+        "kfac_precondition_static": (C.c_int, [C.c_int, P(kfac_precond_args), C.c_int, C.c_void_p, C.c_void_p]),
         "kfac_factor_tile_map": (C.c_int, [C.c_int64, C.c_int64, P(C.c_int32), P(C.c_int64), P(C.c_int32),
                                            P(C.c_int64)]),
     }
@@ -173,9 +176,10 @@ def kfac_precondition_workspace(args) -> int:
     return lib().kfac_precondition_workspace(n, a)
 
 
-def kfac_precondition(args, workspace: int, workspace_bytes: int, stream: int = 0, check: bool = True) -> int:
+def kfac_precondition(args, precision: int, route: int, workspace: int, workspace_bytes: int, stream: int = 0,
+                      check: bool = True) -> int:
     n, a = _arr(kfac_precond_args, args)
-    st = lib().kfac_precondition(n, a, workspace, workspace_bytes, stream)
+    st = lib().kfac_precondition(n, a, precision, route, workspace, workspace_bytes, stream)
     return _check("kfac_precondition", st) if check else st
 
 
@@ -183,10 +187,10 @@ def kfac_precondition_static_capacity() -> int:
     return int(lib().kfac_precondition_static_capacity())
 
 
-def kfac_precondition_static(args, stream: int = 0, check: bool = True) -> int:
+def kfac_precondition_static(args, precision: int, route: int, stream: int = 0, check: bool = True) -> int:
     """kfac_precondition with the library's own fixed scratch (no workspace, no allocation)."""
     n, a = _arr(kfac_precond_args, args)
-    st = lib().kfac_precondition_static(n, a, stream)
+    st = lib().kfac_precondition_static(n, a, precision, route, stream)
     return _check("kfac_precondition_static", st) if check else st
 
 

@@ -216,14 +216,18 @@ size_t kfac_precondition_workspace(int n, const kfac_precond_args* args) {
   return precondition_workspace(n, args);
 }
 
-int kfac_precondition(int n, const kfac_precond_args* args, void* workspace, size_t workspace_bytes, void* stream) {
+int kfac_precondition(int n, const kfac_precond_args* args, int precision, int* route, void* workspace,
+                      size_t workspace_bytes, void* stream) {
   if (!precond_args_ok(n, args)) return KFAC_ERR_INVALID_ARG;
+  if (precision != KFAC_PRECOND_FP32 && precision != KFAC_PRECOND_AUTO) return KFAC_ERR_INVALID_ARG;
+  if (route && (reinterpret_cast<uintptr_t>(route) & 3)) return KFAC_ERR_INVALID_ARG;
   if (n == 0) return KFAC_OK;
   if (!workspace || !aligned16(workspace)) return KFAC_ERR_WORKSPACE;
   if (workspace_bytes < precondition_workspace(n, args)) return KFAC_ERR_WORKSPACE;
   const int dc = check_device();
   if (dc != KFAC_OK) return dc;
-  return launch_precondition(n, args, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  return launch_precondition(n, args, precision, route, workspace, workspace_bytes,
+                             static_cast<cudaStream_t>(stream));
 }
 
 int kfac_factor_tile_map(int64_t d, int64_t capacity, int32_t* row_block, int64_t* col_start, int32_t* width,

@@ -3,20 +3,22 @@
 //     C[m, n] = alpha * sum_k A[m, k] B[n, k]        (A: M x K, B: N x K)
 //
 // Every fp32 operand x is carried as three bf16 slices x = hi + mid + lo (all
-// 24 bits of fp32), and each 16-wide k-step issues six MMAs: hi*hi + hi*mid +
-// mid*hi + hi*lo + lo*hi + mid*mid (the dropped terms are below 2^-24 of the
-// product).  The slices of an operand are the z-planes of one row-major
-// buffer [3][rows][ld], read by TMA K-major (32 values of k per stage row,
-// 64-byte swizzle, three stages of all six tiles in shared memory).
+// 24 bits of fp32).  With all three read (NS = 3), each 16-wide k-step issues
+// six MMAs: hi*hi + hi*mid + mid*hi + hi*lo + lo*hi + mid*mid (the dropped
+// terms are below 2^-24 of the product).  With two (NS = 2: x ~ hi + mid, 16
+// bits), three MMAs: hi*hi + hi*mid + mid*hi (dropped terms below 2^-16).  The
+// slices of an operand are the z-planes of one row-major buffer [3][rows][ld],
+// read by TMA K-major (32 values of k per stage row, 64-byte swizzle; three
+// stages of all six tiles in shared memory for NS = 3, four of four for NS = 2).
 //
 // Accumulation.  The products the K-FAC step multiplies cancel heavily (the
 // preconditioner has gain up to 1/gamma on directions the gradient does not
 // occupy: |grad| |inv_a| can be 6e3 times |grad inv_a|).  The tensor-core
 // accumulator does not round to nearest, and its error grows with the number
-// of accumulations, so every 32-wide k-block (two 16-wide k-steps, twelve
-// MMAs) goes to a fresh TMEM accumulator (two, ping-pong) and the epilogue
-// warps add it into fp32 registers with round-to-nearest: the result keeps
-// close to the accuracy of an fp32 FMA loop.
+// of accumulations, so every twelve MMAs (two 16-wide k-steps for NS = 3,
+// four for NS = 2) go to a fresh TMEM accumulator (two, ping-pong) and the
+// epilogue warps add them into fp32 registers with round-to-nearest: the
+// result keeps close to the accuracy of an fp32 FMA loop.
 //
 // Kernel roles (320 threads, one CTA per SM, persistent over 128 x 256 tiles):
 //   warp 0: TMA producer; warp 1: TMEM allocation + MMA issuer;
@@ -37,26 +39,36 @@
 namespace kfac {
 
 constexpr int kGtBK = 32;
-constexpr int kGtStages = 3;
-constexpr int kGtNS = 3;
 constexpr int kGtA = 128 * kGtBK * 2;  // one slice of the A tile (8 KB)
 constexpr int kGtB = 256 * kGtBK * 2;  // one slice of the B tile (16 KB)
-constexpr int kGtStage = kGtNS * (kGtA + kGtB);
-constexpr int kGtSmem = kGtStages * kGtStage + 1024 + 256;
 constexpr int kGtThreads = 320;
-// 16-wide k-steps accumulated in one TMEM accumulator between two drains into
-// the epilogue's round-to-nearest fp32 sums
-constexpr int kGtDrain = 2;
 constexpr int kGtEpiWarps = 8;
+
+template <int NS>
+struct GtCfg {
+  static constexpr int stage = NS * (kGtA + kGtB);
+  static constexpr int stages = NS == 3 ? 3 : 4;
+  static constexpr int smem = stages * stage + 1024 + 256;
+  // 16-wide k-steps accumulated in one TMEM accumulator between two drains
+  // into the epilogue's round-to-nearest fp32 sums (twelve MMAs either way)
+  static constexpr int drain = NS == 3 ? 2 : 4;
+};
 
 struct GtParams {
   CUtensorMap mapA[kGtMaxProbs];
   CUtensorMap mapB[kGtMaxProbs];
   GtProb probs[kGtMaxProbs];
+  const int* flags;
   long long total_tiles;
   int* status;
   int n_probs;
 };
+
+// a tile of a problem switched off by its flag is skipped by every role alike
+__device__ __forceinline__ bool gt_skip(const GtParams& prm, int prob) {
+  const int f = prm.probs[prob].flag_idx;
+  return prm.flags != nullptr && f >= 0 && prm.flags[f] == 0;
+}
 
 struct GtTile {
   int prob, m0, n0, n_mma, K;
@@ -97,7 +109,12 @@ __device__ __forceinline__ uint64_t gt_desc(uint32_t saddr) {
   return d;
 }
 
+template <int NS>
 __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_constant__ GtParams prm) {
+  using Cfg = GtCfg<NS>;
+  constexpr int kGtStages = Cfg::stages;
+  constexpr int kGtStage = Cfg::stage;
+  constexpr int kGtDrain = Cfg::drain;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGtStages * kGtStage);
@@ -133,6 +150,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
       uint32_t stage = 0, phase = 0;
       for (long long u = blockIdx.x; u < prm.total_tiles && !*abort_flag; u += gridDim.x) {
         const GtTile tl = gt_decode(prm, u);
+        if (gt_skip(prm, tl.prob)) continue;
         const CUtensorMap* ma = &prm.mapA[tl.prob];
         const CUtensorMap* mb = &prm.mapB[tl.prob];
         const int nk = (tl.K + kGtBK - 1) / kGtBK;
@@ -141,9 +159,9 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
           uint8_t* s0 = smem + stage * kGtStage;
           mbar_arrive_expect_tx(&full[stage], (uint32_t)kGtStage);
 #pragma unroll
-          for (int s = 0; s < kGtNS; ++s) {
+          for (int s = 0; s < NS; ++s) {
             tma_load_3d(s0 + s * kGtA, ma, kb * kGtBK, tl.m0, s, &full[stage]);
-            tma_load_3d(s0 + kGtNS * kGtA + s * kGtB, mb, kb * kGtBK, tl.n0, s, &full[stage]);
+            tma_load_3d(s0 + NS * kGtA + s * kGtB, mb, kb * kGtBK, tl.n0, s, &full[stage]);
           }
           if (++stage == kGtStages) {
             stage = 0;
@@ -158,6 +176,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
       bool ok = true;
       for (long long u = blockIdx.x; u < prm.total_tiles && ok; u += gridDim.x) {
         const GtTile tl = gt_decode(prm, u);
+        if (gt_skip(prm, tl.prob)) continue;
         const uint32_t idesc = idesc_bf16_f32(tl.n_mma, false, false);
         const int nk = (tl.K + kGtBK - 1) / kGtBK;
         const int n16 = nk * (kGtBK / 16);  // 16-wide k-steps of the tile
@@ -168,7 +187,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
             break;
           }
           const uint32_t a0 = smem_u32(smem + stage * kGtStage);
-          const uint32_t b0 = a0 + kGtNS * kGtA;
+          const uint32_t b0 = a0 + NS * kGtA;
 #pragma unroll
           for (int kk = 0; kk < kGtBK / 16; ++kk, ++st16) {
             const bool gfirst = st16 % kGtDrain == 0;
@@ -182,18 +201,20 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
             }
             const uint32_t d_tmem = tmem_base + acc * 256;
             const uint32_t off = kk * 32;  // 16 values of k = 32 bytes along the swizzled row
-            uint64_t da[kGtNS], db[kGtNS];
+            uint64_t da[NS], db[NS];
 #pragma unroll
-            for (int s = 0; s < kGtNS; ++s) {
+            for (int s = 0; s < NS; ++s) {
               da[s] = gt_desc(a0 + s * kGtA + off);
               db[s] = gt_desc(b0 + s * kGtB + off);
             }
             tc_mma_bf16(d_tmem, da[0], db[0], idesc, gfirst ? 0u : 1u);
             tc_mma_bf16(d_tmem, da[0], db[1], idesc, 1u);
             tc_mma_bf16(d_tmem, da[1], db[0], idesc, 1u);
-            tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
-            tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
-            tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
+            if (NS == 3) {
+              tc_mma_bf16(d_tmem, da[0], db[NS - 1], idesc, 1u);
+              tc_mma_bf16(d_tmem, da[NS - 1], db[0], idesc, 1u);
+              tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
+            }
             if (glast) {
               tc_commit(&acc_full[acc]);
               acc ^= 1;
@@ -218,6 +239,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
     bool ok = true;
     for (long long u = blockIdx.x; u < prm.total_tiles && ok; u += gridDim.x) {
       const GtTile tl = gt_decode(prm, u);
+      if (gt_skip(prm, tl.prob)) continue;
       const GtProb& pr = prm.probs[tl.prob];
       const int nsteps = ((tl.K + kGtBK - 1) / kGtBK * (kGtBK / 16) + kGtDrain - 1) / kGtDrain;
       float run[128];
@@ -273,7 +295,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
                 float x8[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) x8[k] = run[g * 32 + t + k] * pr.alpha;
-                split8_store(x8, dst + t, pr.out_slice_stride);
+                split8_store<NS>(x8, dst + t, pr.out_slice_stride);
               }
             } else {
 #pragma unroll
@@ -282,7 +304,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
                   __nv_bfloat16 s[kSlices];
                   split_value(run[g * 32 + t] * pr.alpha, s);
 #pragma unroll
-                  for (int k = 0; k < kGtNS; ++k)
+                  for (int k = 0; k < NS; ++k)
                     dst[t + k * pr.out_slice_stride] = *reinterpret_cast<uint16_t*>(&s[k]);
                 }
             }
@@ -299,11 +321,32 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
 }
 
 // ------------------------------------------------------------------ fp32 -> bf16 slices
-constexpr int kSplitChunk = 2048;  // work items (8 values each) per block iteration
+constexpr int kSplitSeg = 256;   // columns of one warp unit (32 lanes x 8)
+constexpr int kSplitChunk = 64;  // warp units per block iteration (8 warps x 8)
 
+// p[k] = sum_e z_k[c0 + e] x[e] for the eight probes of probe_sign8
+__device__ __forceinline__ void probe8(const float (&x)[8], long long c0, int shift, float (&p)[8]) {
+  const uint32_t h = probe_hash((uint32_t)(c0 >> 3)) >> shift;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) p[e] = ((h >> e) & 1u) ? -x[e] : x[e];
+  // 8-point Walsh-Hadamard transform: p[k] = sum_e (-1)^popcount(k & e) p[e]
+#pragma unroll
+  for (int len = 1; len < 8; len <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if ((e & len) == 0) {
+        const float a = p[e], b = p[e + len];
+        p[e] = a + b;
+        p[e + len] = a - b;
+      }
+}
+
+template <int NP>
 __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitParams prm) {
-  // work item = 8 consecutive columns of one row; chunks of kSplitChunk work
-  // items never straddle two matrices, so the matrix lookup is block-uniform
+  // warp unit = 256 consecutive columns of one row (8 per lane); chunks of
+  // kSplitChunk units never straddle two matrices, so the matrix lookup is
+  // block-uniform
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (long long ch = blockIdx.x; ch < prm.total_items; ch += gridDim.x) {
     int lo = 0, hi = prm.n;  // matrix with item_begin (in chunks) <= ch
     while (hi - lo > 1) {
@@ -314,24 +357,44 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
         hi = mid;
     }
     const SplitItem& it = prm.items[lo];
-    const long long per_row = (it.cols + 7) / 8;
-    const long long work = it.rows * per_row;
+    if (prm.flags != nullptr && it.flag_idx >= 0 && prm.flags[it.flag_idx] == 0) continue;
+    const long long segs = (it.cols + kSplitSeg - 1) / kSplitSeg;
+    const long long work = it.rows * segs;
     const long long w0 = (ch - it.item_begin) * kSplitChunk;
-    for (long long local = w0 + threadIdx.x; local < w0 + kSplitChunk && local < work; local += blockDim.x) {
-    const long long r = local / per_row;
-    const long long c0 = (local % per_row) * 8;
-    const float* src = it.src + r * it.ld_src + c0;
-    float x[8];
-    if (c0 + 8 <= it.cols) {
-      const float4 a = *reinterpret_cast<const float4*>(src);
-      const float4 b = *reinterpret_cast<const float4*>(src + 4);
-      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    } else {
+    for (long long unit = w0 + warp; unit < w0 + kSplitChunk && unit < work; unit += 8) {
+      const long long r = unit / segs;
+      const long long c0 = (unit - r * segs) * kSplitSeg + lane * 8;
+      float x[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = (c0 + e < it.cols) ? src[e] : 0.f;
-    }
-    split8_store(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
+      for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      if (c0 < it.cols) {
+        const float* src = it.src + r * it.ld_src + c0;
+        if (c0 + 8 <= it.cols) {
+          const float4 a = *reinterpret_cast<const float4*>(src);
+          const float4 b = *reinterpret_cast<const float4*>(src + 4);
+          x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+          x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = (c0 + e < it.cols) ? src[e] : 0.f;
+        }
+        split8_store<NP>(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
+      }
+      if (it.probe != nullptr) {  // warp-uniform
+        float p[8];
+        probe8(x, c0, it.probe_shift, p);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) p[k] += __shfl_xor_sync(0xffffffffu, p[k], o);
+        if (lane < kProbeN) {
+          float v = p[0];
+#pragma unroll
+          for (int k = 1; k < 8; ++k)
+            if (lane == k) v = p[k];
+          atomicAdd(it.probe + r * kProbeN + lane, v);
+        }
+      }
     }
   }
 }
@@ -357,7 +420,7 @@ static EncodeTiledFn gt_encode_fn() {
 // Slices of one operand: [3][rows][ld] bf16, K = inner extent.
 static bool encode_slices(EncodeTiledFn enc, CUtensorMap* map, const uint16_t* base, long long rows, long long K,
                           long long ld, int box_rows) {
-  cuuint64_t gdim[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)kGtNS};
+  cuuint64_t gdim[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)kSlices};
   cuuint64_t gstride[2] = {(cuuint64_t)ld * 2, (cuuint64_t)(rows * ld * 2)};
   cuuint32_t box[3] = {(cuuint32_t)kGtBK, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
@@ -366,7 +429,8 @@ static bool encode_slices(EncodeTiledFn enc, CUtensorMap* map, const uint16_t* b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int launch_split(const SplitItem* items, int n, cudaStream_t stream) {
+int launch_split(const SplitItem* items, int n, int planes, const int* flags, cudaStream_t stream) {
+  if (planes != 2 && planes != 3) return KFAC_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
@@ -377,39 +441,48 @@ int launch_split(const SplitItem* items, int n, cudaStream_t stream) {
     long long total = 0;
     for (int i = 0; i < cnt; ++i) {
       prm.items[i] = items[base + i];
-      prm.items[i].item_begin = total;  // in chunks of kSplitChunk work items
-      const long long work = prm.items[i].rows * ((prm.items[i].cols + 7) / 8);
+      prm.items[i].item_begin = total;  // in chunks of kSplitChunk warp units
+      const long long work = prm.items[i].rows * ((prm.items[i].cols + kSplitSeg - 1) / kSplitSeg);
       total += (work + kSplitChunk - 1) / kSplitChunk;
     }
     prm.n = cnt;
+    prm.flags = flags;
+    prm.planes = planes;
     prm.total_items = total;
     if (total == 0) continue;
     const long long cap = (long long)sms * 8;
-    split_kernel<<<(unsigned)(total < cap ? total : cap), 256, 0, stream>>>(prm);
+    const unsigned grid = (unsigned)(total < cap ? total : cap);
+    if (planes == 3)
+      split_kernel<3><<<grid, 256, 0, stream>>>(prm);
+    else
+      split_kernel<2><<<grid, 256, 0, stream>>>(prm);
     count_launch();
     if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
   }
   return KFAC_OK;
 }
 
-int launch_gemm_tc(const GtOperand* ops_in, int n, cudaStream_t stream) {
+int launch_gemm_tc(const GtOperand* ops_in, int n, int ns, const int* flags, cudaStream_t stream) {
   // longest K first: tiles are dealt round-robin to a persistent grid
   GtOperand* ops = new GtOperand[n > 0 ? n : 1];
   std::copy(ops_in, ops_in + n, ops);
   std::stable_sort(ops, ops + n, [](const GtOperand& x, const GtOperand& y) { return x.K > y.K; });
-  const int rc = launch_gemm_tc_sorted(ops, n, stream);
+  const int rc = launch_gemm_tc_sorted(ops, n, ns, flags, stream);
   delete[] ops;
   return rc;
 }
 
-int launch_gemm_tc_sorted(const GtOperand* ops, int n, cudaStream_t stream) {
+int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream) {
+  if (ns != 2 && ns != 3) return KFAC_ERR_INVALID_ARG;
   EncodeTiledFn enc = gt_encode_fn();
   if (!enc) return KFAC_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return KFAC_ERR_CUDA;
-  if (!ensure_smem_attr(dev, (const void*)gemm_tc_kernel, kGtSmem)) return KFAC_ERR_CUDA;
+  const void* kern = ns == 3 ? (const void*)gemm_tc_kernel<3> : (const void*)gemm_tc_kernel<2>;
+  const int smem = ns == 3 ? GtCfg<3>::smem : GtCfg<2>::smem;
+  if (!ensure_smem_attr(dev, kern, smem)) return KFAC_ERR_CUDA;
   int* status = device_status_ptr();
   if (!status) return KFAC_ERR_CUDA;
   GtParams* prm = new GtParams;
@@ -434,17 +507,22 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, cudaStream_t stream) {
       p.K = (int)o.K;
       p.tiles_n = (int)((o.N + 255) / 256);
       p.out_split = o.out_split;
+      p.flag_idx = flags != nullptr ? o.flag_idx : -1;
       p.alpha = o.alpha;
       p.tile_begin = tiles;
       tiles += (long long)((o.M + 127) / 128) * p.tiles_n;
     }
     if (rc != KFAC_OK) break;
     prm->n_probs = cnt;
+    prm->flags = flags;
     prm->total_tiles = tiles;
     prm->status = status;
     if (tiles > 0) {
       const int grid = (int)(tiles < sms ? tiles : sms);
-      gemm_tc_kernel<<<grid, kGtThreads, kGtSmem, stream>>>(*prm);
+      if (ns == 3)
+        gemm_tc_kernel<3><<<grid, kGtThreads, smem, stream>>>(*prm);
+      else
+        gemm_tc_kernel<2><<<grid, kGtThreads, smem, stream>>>(*prm);
       count_launch();
       if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
     }

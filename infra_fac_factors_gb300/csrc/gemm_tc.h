@@ -8,39 +8,66 @@ namespace kfac {
 constexpr int kGtMaxProbs = 96;  // problems per launch (kernel parameter space)
 constexpr int kSplitMax = 384;   // matrices per split launch (64 B each in parameter space)
 
-// One problem C = alpha * A B^T.  a / b: bf16 slices [NS][rows][ld].
+// One problem C = alpha * A B^T.  a / b: bf16 slices [3][rows][ld].
 struct GtOperand {
   const uint16_t* a;
   const uint16_t* b;
   long long M, N, K, lda, ldb;
-  void* out;                   // fp32 [M][ldc], or bf16 slices [NS][M][ldc] when out_split
+  void* out;                   // fp32 [M][ldc], or bf16 slices [3][M][ldc] when out_split
   long long ldc, out_slice_stride;
   int out_split;
   float alpha;
+  int flag_idx;                // index into the launch's flags (see launch_gemm_tc), or -1
 };
 
 struct GtProb {
   void* out;
   long long ldc, out_slice_stride, tile_begin;
-  int M, N, K, tiles_n, out_split;
+  int M, N, K, tiles_n, out_split, flag_idx;
   float alpha;
 };
 
 // fp32 src [rows][ld_src] -> bf16 dst slices: slice k at dst + k * slice_stride.
+// When `probe` is set, the same pass adds src * z into probe[rows][kProbeN]
+// (z: the Rademacher probes of kfac::probe_sign, bit offset probe_shift).
 struct SplitItem {
   const float* src;
   uint16_t* dst;
   long long rows, cols, ld_src, ld_dst, slice_stride, item_begin;
+  float* probe;
+  int probe_shift;
+  int flag_idx;
 };
 struct SplitParams {
   SplitItem items[kSplitMax];
+  const int* flags;
   long long total_items;
   int n;
+  int planes;
 };
 
-// Three bf16 slices per fp32 value (see gemm_tc.cu).
-int launch_split(const SplitItem* items, int n, cudaStream_t stream);
-int launch_gemm_tc(const GtOperand* ops, int n, cudaStream_t stream);         // sorts by K
-int launch_gemm_tc_sorted(const GtOperand* ops, int n, cudaStream_t stream);  // as given
+// Probes of the preconditioning check: eight Rademacher vectors on each side.
+constexpr int kProbeN = 8;
+
+// sign (+1 / -1) of probe k at index i: bit k + shift of a 32-bit integer
+// hash of i (the "lowbias32" mixing function: xor-shift / multiply rounds)
+__host__ __device__ __forceinline__ uint32_t probe_hash(uint32_t x) {
+  x ^= x >> 16;
+  x *= 0x7feb352dU;
+  x ^= x >> 15;
+  x *= 0x846ca68bU;
+  x ^= x >> 16;
+  return x;
+}
+
+// `planes` bf16 slices per fp32 value (2 or 3).  Items whose flag_idx >= 0 run
+// only when flags[flag_idx] != 0 (flags may be null: every item runs).
+int launch_split(const SplitItem* items, int n, int planes, const int* flags, cudaStream_t stream);
+// ns = operand slices read per product: 3 (six MMAs per multiply-add, all 24
+// bits) or 2 (three MMAs: hi*hi + hi*mid + mid*hi, 16 bits).  Split outputs
+// are written with ns slices.  Problems whose flag_idx >= 0 run only when
+// flags[flag_idx] != 0.
+int launch_gemm_tc(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream);  // sorts by K
+int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream);
 
 }  // namespace kfac

@@ -24,7 +24,7 @@ size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine);
 int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra, int refine, int* info, int* route,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t precondition_workspace(int n, const kfac_precond_args* args);
-int launch_precondition(int n, const kfac_precond_args* args, void* workspace, size_t workspace_bytes,
-                        cudaStream_t stream);
+int launch_precondition(int n, const kfac_precond_args* args, int precision, int* route, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
 
 }  // namespace kfac

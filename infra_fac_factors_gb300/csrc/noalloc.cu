@@ -51,15 +51,15 @@ extern "C" {
 
 size_t kfac_precondition_static_capacity(void) { return kfac::kStaticScratchBytes; }
 
-int kfac_precondition_static(int n, const kfac_precond_args* args, void* stream) {
+int kfac_precondition_static(int n, const kfac_precond_args* args, int precision, int* route, void* stream) {
   if (n < 0 || (n > 0 && !args)) return KFAC_ERR_INVALID_ARG;
-  if (n == 0) return kfac_precondition(0, args, nullptr, 0, stream);
+  if (n == 0) return kfac_precondition(0, args, precision, route, nullptr, 0, stream);
   const size_t need = kfac_precondition_workspace(n, args);
   if (need == 0) return KFAC_ERR_INVALID_ARG;  // the query rejects invalid arguments
   if (need > kfac::kStaticScratchBytes) return KFAC_ERR_WORKSPACE;
   void* scratch = kfac::scratch_address();
   if (!scratch) return KFAC_ERR_CUDA;
-  return kfac_precondition(n, args, scratch, kfac::kStaticScratchBytes, stream);
+  return kfac_precondition(n, args, precision, route, scratch, kfac::kStaticScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -1,25 +1,49 @@
 // Preconditioned gradient of each layer (SPD-KFAC §II-B, the damped update
 // rule):  out = inv_g * grad * inv_a, on tcgen05 tensor cores.
 //
-// The fp32 operands are carried as three bf16 slices (x = hi + mid + lo, all 24
-// bits of fp32; six products per multiply-add, gemm_tc.cu), and every 16-wide
-// k-step is summed into fp32 registers with round-to-nearest.  Less does not
-// do: grad lies in the row space of the layer input while inv_a has gain up to
-// 1/gamma on the other directions, so operand rounding and accumulation error
-// are amplified ~1/gamma-fold (two slices, 16 bits, gave 1e-2 relative error on
-// the first steps of the MLP workload, where 529 of 785 directions have gain
-// 1000; one tensor-core accumulator over the whole K gave 5e-3).
-//   1. split      grad, inv_a, inv_g -> bf16 slices               (one launch)
+// The fp32 operands are carried as bf16 slices (x = hi + mid + lo, all 24 bits
+// of fp32, gemm_tc.cu), and every twelve MMAs are summed into fp32 registers
+// with round-to-nearest.  grad lies in the row space of the layer input while
+// inv_a has gain up to 1/gamma on the other directions, so operand rounding is
+// amplified up to ~1/gamma-fold: with 16-bit operands (two slices, three MMAs
+// per multiply-add) the relative error of out is 6e-6 on the BERT QKV layer
+// and 1.4e-4 on its FFN-out layer, but 9e-3 on the first steps of the MLP
+// workload (529 of 785 directions have gain 1000) and 3.5e-3 on the C = 512
+// ResNet conv.  With all 24 bits (three slices, six MMAs) it stays near 1e-5.
+//
+// KFAC_PRECOND_FP32: six MMAs per multiply-add for every layer.
+//   1. split      grad, inv_a, inv_g -> three bf16 slices            (one launch)
 //   2. GEMM 1     tmp^T = inv_a * grad^T   (d_in x d_out), written as slices
 //   3. GEMM 2     out   = inv_g * tmp      (= inv_g * (tmp^T)^T), fp32
-// inv_a and inv_g are symmetric, so their rows serve as the K-major operands.
+// KFAC_PRECOND_AUTO: the same with three MMAs per multiply-add, then an
+// a-posteriori check of every layer, and the six-MMA pass (steps 1-3, three
+// slices) for the layers the check flags only:
+//   1'. split (two slices), fused with y = inv_a Z and s = inv_g Z' for eight
+//       Rademacher probes on each side (Z: d_in x 8, Z': d_out x 8)
+//   2', 3'. GEMMs with two slices
+//   4. check: per layer, the 8 x 8 bilinear forms Z'^T out Z and
+//      s^T grad y = Z'^T inv_g grad inv_a Z in one pass over grad and out;
+//      the estimate ||Z'^T (out - inv_g grad inv_a) Z||_F / ||Z'^T inv_g grad
+//      inv_a Z||_F tracks the relative Frobenius error of out (each bilinear
+//      form of independent Rademacher vectors has mean square ||.||_F^2)
+//   5. flag the layers whose estimate exceeds kPcAutoTol (or is not finite)
+//   6. steps 1-3 with three slices for the flagged layers (device-side flags:
+//      the launches skip the other layers' work)
+// inv_a and inv_g are symmetric, so their rows serve as the K-major operands,
+// and s = inv_g Z' = (Z'^T inv_g)^T.
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "launch.h"
+#include "split.cuh"
 
 namespace kfac {
 
-constexpr int kPcSlices = 3;
+// Largest accepted estimate of the 16-bit result's relative error: 5x under
+// the 2e-3 bar.  On the workloads the estimate falls within 0.79x..1.28x of
+// the true error.
+constexpr float kPcAutoTol = 4e-4f;
+constexpr int kChkRows = 32;    // rows of out / grad per warp unit of the check
+constexpr int kChkMax = 256;    // layers per check launch (parameter space)
 
 static long long pad8(long long v) { return (v + 7) / 8 * 8; }
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -30,7 +54,7 @@ struct PcLayout {
 
 // Workspace of layer i starting at byte `off`: four sliced operands.
 static PcLayout pc_layout(const kfac_precond_args& a, size_t off) {
-  const size_t s = kPcSlices * sizeof(uint16_t);
+  const size_t s = kSlices * sizeof(uint16_t);
   PcLayout L;
   L.grad = off;
   off += align256(s * a.d_out * pad8(a.d_in));
@@ -44,20 +68,243 @@ static PcLayout pc_layout(const kfac_precond_args& a, size_t off) {
   return L;
 }
 
+// After all layers' slices: the probe region (zeroed by every AUTO call), then
+// the flags.  Per layer: y [d_in][8] and s [d_out][8] fp32; then per layer 128
+// doubles (Z'^T out Z and s^T grad y, 8 x 8 each).
+struct PcProbeLayout {
+  size_t begin, acc, flags, end;
+};
+
+static PcProbeLayout pc_probe_layout(int n, const kfac_precond_args* args, size_t off) {
+  PcProbeLayout P;
+  P.begin = off;
+  for (int i = 0; i < n; ++i) off += align256(sizeof(float) * kProbeN * (args[i].d_in + args[i].d_out));
+  P.acc = off;
+  off += align256(sizeof(double) * 2 * kProbeN * kProbeN * (size_t)n);
+  P.flags = off;
+  off += align256(sizeof(int) * (size_t)n);
+  P.end = off;
+  return P;
+}
+
 size_t precondition_workspace(int n, const kfac_precond_args* args) {
   size_t off = 0;
   for (int i = 0; i < n; ++i) off = pc_layout(args[i], off).end;
-  return off;
+  return pc_probe_layout(n, args, off).end;
 }
 
-int launch_precondition(int n, const kfac_precond_args* args, void* workspace, size_t workspace_bytes,
-                        cudaStream_t stream) {
+// ------------------------------------------------------------------ check
+struct PcChkItem {
+  const float* grad;
+  const float* out;
+  const float* y;  // [d_in][8]
+  const float* s;  // [d_out][8]
+  double* acc;     // [2][8][8]: Z'^T out Z, s^T grad y
+  long long ld_grad, ld_out, d_out, d_in, unit_begin;
+};
+
+struct PcChkParams {
+  PcChkItem items[kChkMax];
+  long long total_units;
+  int n;
+};
+
+// sign of left probe l at row r (the probes of probe8 with bit offset 8)
+__device__ __forceinline__ float left_sign(long long r, int l) {
+  const uint32_t h = probe_hash((uint32_t)(r >> 3)) >> 8;
+  const int e = (int)(r & 7);
+  return ((__popc(l & e) + (int)((h >> e) & 1u)) & 1) ? -1.f : 1.f;
+}
+
+// p[k] = sum_e z_k[c0 + e] x[e]: the right probes (bit offset 0)
+__device__ __forceinline__ void right_probe8(const float (&x)[8], long long c0, float (&p)[8]) {
+  const uint32_t h = probe_hash((uint32_t)(c0 >> 3));
+#pragma unroll
+  for (int e = 0; e < 8; ++e) p[e] = ((h >> e) & 1u) ? -x[e] : x[e];
+#pragma unroll
+  for (int len = 1; len < 8; len <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if ((e & len) == 0) {
+        const float a = p[e], b = p[e + len];
+        p[e] = a + b;
+        p[e + len] = a - b;
+      }
+}
+
+// Warp unit: one 256-column segment (8 columns per lane) of kChkRows rows.
+// Per row the lanes' partial sums w_k = (grad y_k)_r and q_k = (out z_k)_r
+// (16 values) are reduce-scattered in 16 shuffles; lane pairs (2j, 2j + 1)
+// then hold value j (q_0..7 for j < 8, w_0..7 after) and multiply it by
+// z'_l[r] (for q) or s_l[r] (for w), each lane of the pair for four l.
+__global__ void __launch_bounds__(256) pc_check_kernel(const __grid_constant__ PcChkParams prm) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // value this lane holds after the reduce-scatter: bits 4..1 of the lane
+  const int j = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+  const int is_w = j >> 3, kj = j & 7, l0 = (lane & 1) * 4;
+  for (long long u = (long long)blockIdx.x * 8 + warp; u < prm.total_units; u += (long long)gridDim.x * 8) {
+    int lo = 0, hi = prm.n;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prm.items[mid].unit_begin <= u)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const PcChkItem& it = prm.items[lo];
+    const long long segs = (it.d_in + 255) / 256;
+    const long long local = u - it.unit_begin;
+    const long long rg = local / segs;
+    const long long c0 = (local - rg * segs) * 256 + lane * 8;
+    float yv[8][8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (c0 + e < it.d_in) {
+        const float4 a = *reinterpret_cast<const float4*>(it.y + (c0 + e) * kProbeN);
+        const float4 b = *reinterpret_cast<const float4*>(it.y + (c0 + e) * kProbeN + 4);
+        yv[e][0] = a.x; yv[e][1] = a.y; yv[e][2] = a.z; yv[e][3] = a.w;
+        yv[e][4] = b.x; yv[e][5] = b.y; yv[e][6] = b.z; yv[e][7] = b.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) yv[e][k] = 0.f;
+      }
+    }
+    float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+    const long long r_end = (rg + 1) * kChkRows < it.d_out ? (rg + 1) * kChkRows : it.d_out;
+    for (long long r = rg * kChkRows; r < r_end; ++r) {
+      float g8[8], o8[8];
+      if (c0 + 8 <= it.d_in) {
+        const float4 a = *reinterpret_cast<const float4*>(it.grad + r * it.ld_grad + c0);
+        const float4 b = *reinterpret_cast<const float4*>(it.grad + r * it.ld_grad + c0 + 4);
+        const float4 c = *reinterpret_cast<const float4*>(it.out + r * it.ld_out + c0);
+        const float4 d = *reinterpret_cast<const float4*>(it.out + r * it.ld_out + c0 + 4);
+        g8[0] = a.x; g8[1] = a.y; g8[2] = a.z; g8[3] = a.w; g8[4] = b.x; g8[5] = b.y; g8[6] = b.z; g8[7] = b.w;
+        o8[0] = c.x; o8[1] = c.y; o8[2] = c.z; o8[3] = c.w; o8[4] = d.x; o8[5] = d.y; o8[6] = d.z; o8[7] = d.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const bool in = c0 + e < it.d_in;
+          g8[e] = in ? it.grad[r * it.ld_grad + c0 + e] : 0.f;
+          o8[e] = in ? it.out[r * it.ld_out + c0 + e] : 0.f;
+        }
+      }
+      float v[16], q[8];
+      right_probe8(o8, c0, q);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[k] = q[k];
+        float w = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w = fmaf(g8[e], yv[e][k], w);
+        v[8 + k] = w;
+      }
+      // reduce-scatter over the warp: offsets 16, 8, 4, 2 halve the values
+      // held, offset 1 completes the sum (lanes 2j and 2j + 1 agree)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const bool up = lane & 16;
+        const float send = up ? v[i] : v[i + 8], keep = up ? v[i + 8] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool up = lane & 8;
+        const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const bool up = lane & 4;
+        const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+      {
+        const bool up = lane & 2;
+        const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+      if (is_w) {
+        const float4 sl = *reinterpret_cast<const float4*>(it.s + r * kProbeN + l0);
+        acc4[0] = fmaf(sl.x, v[0], acc4[0]);
+        acc4[1] = fmaf(sl.y, v[0], acc4[1]);
+        acc4[2] = fmaf(sl.z, v[0], acc4[2]);
+        acc4[3] = fmaf(sl.w, v[0], acc4[3]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) acc4[t] = fmaf(left_sign(r, l0 + t), v[0], acc4[t]);
+      }
+    }
+    // acc[is_w][k][l]: Z'^T out Z (is_w = 0) and s^T grad y (is_w = 1)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) atomicAdd(it.acc + is_w * 64 + kj * 8 + l0 + t, (double)acc4[t]);
+  }
+}
+
+// Per layer: flag when ||Z'^T out Z - s^T grad y||_F > tol ||s^T grad y||_F
+// (or when either is not finite); route = products per multiply-add used.
+__global__ void pc_flag_kernel(const double* acc, int n, float tol, int* flags, int* route) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const double* a = acc + (size_t)i * 2 * kProbeN * kProbeN;
+    double num = 0.0, den = 0.0;
+    for (int t = 0; t < kProbeN * kProbeN; ++t) {
+      const double d = a[t] - a[64 + t];
+      num += d * d;
+      den += a[64 + t] * a[64 + t];
+    }
+    const bool ok = num <= (double)tol * (double)tol * den;  // false for NaN
+    flags[i] = ok ? 0 : 1;
+    if (route) route[i] = ok ? 3 : 6;
+  }
+}
+
+__global__ void pc_route_fill_kernel(int* route, int n, int v) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) route[i] = v;
+}
+
+static int launch_check(int n, const PcChkItem* items, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  PcChkParams* prm = new PcChkParams;
+  int rc = KFAC_OK;
+  for (int base = 0; base < n && rc == KFAC_OK; base += kChkMax) {
+    const int cnt = n - base < kChkMax ? n - base : kChkMax;
+    long long total = 0;
+    for (int i = 0; i < cnt; ++i) {
+      prm->items[i] = items[base + i];
+      prm->items[i].unit_begin = total;
+      const PcChkItem& it = prm->items[i];
+      total += ((it.d_in + 255) / 256) * ((it.d_out + kChkRows - 1) / kChkRows);
+    }
+    prm->n = cnt;
+    prm->total_units = total;
+    const long long blocks = (total + 7) / 8, cap = (long long)sms * 8;
+    pc_check_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, stream>>>(*prm);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
+  }
+  delete prm;
+  return rc;
+}
+
+// ------------------------------------------------------------------ driver
+int launch_precondition(int n, const kfac_precond_args* args, int precision, int* route, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
   if (workspace_bytes < precondition_workspace(n, args) || (workspace == nullptr && n > 0)) return KFAC_ERR_WORKSPACE;
+  const bool autop = precision == KFAC_PRECOND_AUTO;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   SplitItem* items = new SplitItem[3 * (size_t)n];
   GtOperand* g1 = new GtOperand[n];
   GtOperand* g2 = new GtOperand[n];
+  PcChkItem* chk = new PcChkItem[n];
   size_t off = 0;
+  for (int i = 0; i < n; ++i) off = pc_layout(args[i], off).end;
+  const PcProbeLayout PL = pc_probe_layout(n, args, off);
+  double* acc = reinterpret_cast<double*>(ws + PL.acc);
+  int* flags = reinterpret_cast<int*>(ws + PL.flags);
+  off = 0;
+  size_t poff = PL.begin;
   for (int i = 0; i < n; ++i) {
     const kfac_precond_args& a = args[i];
     const PcLayout L = pc_layout(a, off);
@@ -66,21 +313,51 @@ int launch_precondition(int n, const kfac_precond_args* args, void* workspace, s
     uint16_t* s_ia = reinterpret_cast<uint16_t*>(ws + L.inv_a);
     uint16_t* s_ig = reinterpret_cast<uint16_t*>(ws + L.inv_g);
     uint16_t* s_tmp = reinterpret_cast<uint16_t*>(ws + L.tmp);
+    float* y = reinterpret_cast<float*>(ws + poff);
+    float* sv = y + kProbeN * a.d_in;
+    poff += align256(sizeof(float) * kProbeN * (a.d_in + a.d_out));
     const long long ldi = pad8(a.d_in), ldo = pad8(a.d_out);
-    items[3 * i + 0] = SplitItem{a.grad, s_grad, a.d_out, a.d_in, a.ld_grad, ldi, a.d_out * ldi, 0};
-    items[3 * i + 1] = SplitItem{a.inv_a, s_ia, a.d_in, a.d_in, a.ld_a, ldi, a.d_in * ldi, 0};
-    items[3 * i + 2] = SplitItem{a.inv_g, s_ig, a.d_out, a.d_out, a.ld_g, ldo, a.d_out * ldo, 0};
+    items[3 * i + 0] = SplitItem{a.grad, s_grad, a.d_out, a.d_in, a.ld_grad, ldi, a.d_out * ldi, 0, nullptr, 0, i};
+    items[3 * i + 1] = SplitItem{a.inv_a, s_ia, a.d_in, a.d_in, a.ld_a, ldi, a.d_in * ldi, 0, autop ? y : nullptr, 0, i};
+    items[3 * i + 2] =
+        SplitItem{a.inv_g, s_ig, a.d_out, a.d_out, a.ld_g, ldo, a.d_out * ldo, 0, autop ? sv : nullptr, 8, i};
     // tmp^T[n][m] = sum_k inv_a[n][k] grad[m][k]: M = d_in, N = d_out, K = d_in
-    g1[i] = GtOperand{s_ia, s_grad, a.d_in, a.d_out, a.d_in, ldi, ldi, s_tmp, ldo, a.d_in * ldo, 1, 1.0f};
+    g1[i] = GtOperand{s_ia, s_grad, a.d_in, a.d_out, a.d_in, ldi, ldi, s_tmp, ldo, a.d_in * ldo, 1, 1.0f, i};
     // out[m][n] = sum_k inv_g[m][k] tmp^T[n][k]: M = d_out, N = d_in, K = d_out
-    g2[i] = GtOperand{s_ig, s_tmp, a.d_out, a.d_in, a.d_out, ldo, ldo, a.out, a.ld_out, 0, 0, 1.0f};
+    g2[i] = GtOperand{s_ig, s_tmp, a.d_out, a.d_in, a.d_out, ldo, ldo, a.out, a.ld_out, 0, 0, 1.0f, i};
+    chk[i] = PcChkItem{a.grad, a.out, y, sv, acc + (size_t)i * 2 * kProbeN * kProbeN,
+                       a.ld_grad, a.ld_out, a.d_out, a.d_in, 0};
   }
-  int rc = launch_split(items, 3 * n, stream);
-  if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, stream);
-  if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, stream);
+  int rc = KFAC_OK;
+  if (!autop) {
+    rc = launch_split(items, 3 * n, 3, nullptr, stream);
+    if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, 3, nullptr, stream);
+    if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, 3, nullptr, stream);
+    if (rc == KFAC_OK && route && n > 0) {
+      pc_route_fill_kernel<<<(n + 255) / 256, 256, 0, stream>>>(route, n, 6);
+      count_launch();
+      if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
+    }
+  } else {
+    if (cudaMemsetAsync(ws + PL.begin, 0, PL.flags - PL.begin, stream) != cudaSuccess) rc = KFAC_ERR_CUDA;
+    if (rc == KFAC_OK) rc = launch_split(items, 3 * n, 2, nullptr, stream);
+    if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, 2, nullptr, stream);
+    if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, 2, nullptr, stream);
+    if (rc == KFAC_OK) rc = launch_check(n, chk, stream);
+    if (rc == KFAC_OK) {
+      pc_flag_kernel<<<(n + 127) / 128, 128, 0, stream>>>(acc, n, kPcAutoTol, flags, route);
+      count_launch();
+      if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
+    }
+    for (int i = 0; i < 3 * n; ++i) items[i].probe = nullptr;  // the probes are taken
+    if (rc == KFAC_OK) rc = launch_split(items, 3 * n, 3, flags, stream);
+    if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, 3, flags, stream);
+    if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, 3, flags, stream);
+  }
   delete[] items;
   delete[] g1;
   delete[] g2;
+  delete[] chk;
   return rc;
 }
 

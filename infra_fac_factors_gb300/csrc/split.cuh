@@ -18,7 +18,9 @@ __device__ __forceinline__ void split_value(float x, __nv_bfloat16 (&s)[kSlices]
   }
 }
 
-// eight consecutive values -> one 16-byte store per slice (dst 16-byte aligned)
+// eight consecutive values -> one 16-byte store per slice (dst 16-byte
+// aligned); the first NP slices are written
+template <int NP = kSlices>
 __device__ __forceinline__ void split8_store(const float (&x)[8], uint16_t* dst, long long slice_stride) {
   uint32_t w[kSlices][4];
 #pragma unroll
@@ -35,7 +37,7 @@ __device__ __forceinline__ void split8_store(const float (&x)[8], uint16_t* dst,
     }
   }
 #pragma unroll
-  for (int k = 0; k < kSlices; ++k)
+  for (int k = 0; k < NP; ++k)
     *reinterpret_cast<uint4*>(dst + k * slice_stride) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
 }
 

@@ -72,13 +72,15 @@ class FactorBufs:
 
 class KFACStep:
     def __init__(self, layers: Sequence[LayerSpec], P: int, gamma: float, decay: float, in_dtype: str,
-                 refine: int = capi.KFAC_REFINE_AUTO, device="cuda", n_groups: int = 8):
+                 refine: int = capi.KFAC_REFINE_AUTO, device="cuda", n_groups: int = 8,
+                 precond_precision: int = capi.KFAC_PRECOND_AUTO):
         self.layers = list(layers)
         self.P = P
         self.gamma = float(gamma)
         self.decay = float(decay)
         self.in_dtype = in_dtype
         self.refine = refine
+        self.precond_precision = precond_precision
         self.device = torch.device(device)
         tdt = torch.bfloat16 if in_dtype == "bf16" else torch.float32
         self.kdt = capi.KFAC_BF16 if in_dtype == "bf16" else capi.KFAC_FP32
@@ -105,6 +107,8 @@ class KFACStep:
         nf = 2 * len(self.layers)
         self.info = torch.zeros(nf, dtype=torch.int32, device=dev)
         self.route = torch.zeros(nf, dtype=torch.int32, device=dev)
+        # MMAs per multiply-add each layer's preconditioned gradient came from (3 or 6)
+        self.pc_route = torch.zeros(len(self.layers), dtype=torch.int32, device=dev)
         self._build_args()
         self._build_groups(n_groups)
         self._side = torch.cuda.Stream(device=dev)
@@ -201,7 +205,8 @@ class KFACStep:
                                  self.inv_ws.data_ptr(), self.inv_ws_bytes, stream)
 
     def precondition(self, stream: int):
-        capi.kfac_precondition(self._pc_args, self.pc_ws.data_ptr(), self.pc_ws_bytes, stream)
+        capi.kfac_precondition(self._pc_args, self.precond_precision, self.pc_route.data_ptr(),
+                               self.pc_ws.data_ptr(), self.pc_ws_bytes, stream)
 
     def factors_and_running(self, first_step: bool, stream: Optional[torch.cuda.Stream] = None):
         """Stages 2 and 3, the running-average pass of each layer group on a

@@ -158,12 +158,17 @@ def pa(**kw):
 
 def test_precondition_rejects_invalid():
     ws = capi.kfac_precondition_workspace([pa()])
-    # four operands as three bf16 slices: grad 8x16, inv_a 12x16, inv_g 8x8, tmp^T 12x8, each 256-B aligned
-    assert ws == 768 + 1280 + 512 + 768
+    # four operands as three bf16 slices: grad 8x16, inv_a 12x16, inv_g 8x8, tmp^T 12x8, each 256-B aligned;
+    # then the probe vectors (12 + 8 rows of 8 fp32), the 2 x 8 x 8 fp64 bilinear sums and the flag
+    assert ws == (768 + 1280 + 512 + 768) + 768 + 1024 + 256
     for bad in (pa(d_in=0), pa(ld_g=4), pa(ld_grad=10), pa(out=A16 * 2), pa(inv_a=A16 + 4)):
         assert capi.kfac_precondition_workspace([bad]) == 0
-        assert capi.kfac_precondition([bad], A16 * 5, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
-    assert capi.kfac_precondition([pa()], A16 * 5, ws - 4, check=False) == capi.KFAC_ERR_WORKSPACE
+        assert capi.kfac_precondition([bad], 0, 0, A16 * 5, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_precondition([pa()], 0, 0, A16 * 5, ws - 4, check=False) == capi.KFAC_ERR_WORKSPACE
+    # precision outside the enum, and a route array that is not 4-byte aligned
+    assert capi.kfac_precondition([pa()], 2, 0, A16 * 5, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_precondition([pa()], capi.KFAC_PRECOND_AUTO, A16 + 2, A16 * 5, ws,
+                                  check=False) == capi.KFAC_ERR_INVALID_ARG
 
 
 def test_spatial_sum_rejects_invalid():
@@ -177,7 +182,7 @@ def test_spatial_sum_rejects_invalid():
 def test_empty_calls_are_no_ops():
     assert capi.kfac_factors([], capi.KFAC_BF16, 1, check=False) == capi.KFAC_OK
     assert capi.kfac_update_running([], 1, 0.5, 0.0, True, check=False) == capi.KFAC_OK
-    assert capi.kfac_precondition([], 0, 0, check=False) == capi.KFAC_OK
+    assert capi.kfac_precondition([], 0, 0, 0, 0, check=False) == capi.KFAC_OK
 
 
 def test_constant_time_tile_map_equals_enumeration():

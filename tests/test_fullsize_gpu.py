@@ -122,3 +122,18 @@ def test_sampled_preconditioned_rows(run):
         rows = rng.choice(L.d_out, size=8, replace=False)
         ref = (XG[rows] @ grad) @ XA
         assert rel_fro(V[rows], ref) <= 2e-3, (li, rel_fro(V[rows], ref))
+
+
+def test_preconditioned_ffn_out_layer_whole(run):
+    # the layer with the largest cancellation (rank-deficient 4097-wide input):
+    # the whole 1024 x 4097 result against the oracle, and the products used
+    st = run["step"]
+    li = 95
+    L = run["specs"][li]
+    XG = st.fg[li].inv.cpu().numpy()[:, :L.d_out]
+    XA = st.fa[li].inv.cpu().numpy()[:, :L.d_in]
+    grad = st.grad[li].cpu().numpy()[:, :L.d_in]
+    V = st.out[li].cpu().numpy()[:, :L.d_in]
+    assert rel_fro(V, oracle.precondition(XG, grad, XA)) <= 2e-3
+    route = st.pc_route.cpu().numpy()
+    assert set(route.tolist()) <= {3, 6}

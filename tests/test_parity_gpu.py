@@ -252,7 +252,7 @@ def test_damped_inverse_reports_first_bad_pivot():
 
 
 # ------------------------------------------------------------------ a5: precondition
-def run_precondition(XG, grad, XA):
+def run_precondition(XG, grad, XA, precision=capi.KFAC_PRECOND_FP32, with_route=False):
     d_out, d_in = grad.shape
     ldg, lda, ldw, ldo = pad(d_out, 4), pad(d_in, 4) + 4, pad(d_in, 4), pad(d_in, 4) + 8
     tg = to_dev(XG, capi.KFAC_FP32, ldg)
@@ -263,9 +263,14 @@ def run_precondition(XG, grad, XA):
                                    d_out, d_in)]
     wsb = capi.kfac_precondition_workspace(args)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
-    capi.kfac_precondition(args, ws.data_ptr(), wsb, stream())
+    route = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    capi.kfac_precondition(args, precision, route.data_ptr(), ws.data_ptr(), wsb, stream())
     sync()
-    return out.cpu().numpy()
+    got = out.cpu().numpy()
+    assert np.isnan(got[:, d_in:]).all()  # padding of out untouched
+    if with_route:
+        return got, int(route.item())
+    return got
 
 
 def test_precondition_identity_is_exact():
@@ -288,28 +293,59 @@ def test_precondition_diagonal_uses_all_24_bits():
     assert np.abs(got[:, :d_in] - ref).max() <= 3e-7 * np.abs(ref).max()
 
 
+@pytest.mark.parametrize("precision", [capi.KFAC_PRECOND_FP32, capi.KFAC_PRECOND_AUTO])
 @pytest.mark.parametrize("d_out,d_in", [(3, 4), (32, 65), (129, 300), (10, 1025), (300, 129)])
-def test_precondition(d_out, d_in):
+def test_precondition(d_out, d_in, precision):
     rng = np.random.default_rng(d_out * 7 + d_in)
     XG, _ = oracle.spd_inverse(spd_case(d_out, rng).astype(np.float64))
     XA, _ = oracle.spd_inverse(spd_case(d_in, rng).astype(np.float64))
     XG, XA = XG.astype(np.float32), XA.astype(np.float32)
     grad = (rng.standard_normal((d_out, d_in)) * 1e-2).astype(np.float32)
-    ldg, lda, ldw, ldo = pad(d_out, 4), pad(d_in, 4) + 4, pad(d_in, 4), pad(d_in, 4) + 8
-    tg = to_dev(XG, capi.KFAC_FP32, ldg)
-    ta = to_dev(XA, capi.KFAC_FP32, lda)
-    tw = to_dev(grad, capi.KFAC_FP32, ldw)
-    out = torch.full((d_out, ldo), float("nan"), device="cuda")
-    args = [capi.kfac_precond_args(tg.data_ptr(), ldg, tw.data_ptr(), ldw, ta.data_ptr(), lda, out.data_ptr(), ldo,
-                                   d_out, d_in)]
-    wsb = capi.kfac_precondition_workspace(args)
-    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
-    capi.kfac_precondition(args, ws.data_ptr(), wsb, stream())
-    sync()
-    got = out.cpu().numpy()
+    got, route = run_precondition(XG, grad, XA, precision, with_route=True)
     ref = oracle.precondition(XG, grad, XA)
-    assert rel_fro(got[:, :d_in], ref) <= 2e-3
-    assert np.isnan(got[:, d_in:]).all()
+    err = rel_fro(got[:, :d_in], ref)
+    assert err <= 2e-3
+    if precision == capi.KFAC_PRECOND_FP32:
+        assert route == 6
+    else:
+        assert route in (3, 6)
+        if route == 3:  # kept only when the 16-bit result passed the check
+            assert err <= 1e-3
+
+
+def amplifying_layer(rows, d_in, d_out, gamma, rng):
+    """A layer whose gradient lies in the row space of a rank-deficient input
+    (rows < d_in): the damped inverse has gain 1/gamma off that space, the
+    cancellation that 16-bit operands cannot carry."""
+    a = rng.standard_normal((rows, d_in))
+    g = rng.standard_normal((rows, d_out)) * 1e-3
+    XA, _ = oracle.spd_inverse(a.T @ a / rows + gamma * np.eye(d_in))
+    XG, _ = oracle.spd_inverse(g.T @ g / rows + gamma * np.eye(d_out))
+    grad = g.T @ a / rows
+    return XG.astype(np.float32), grad.astype(np.float32), XA.astype(np.float32)
+
+
+def test_precondition_auto_recomputes_amplifying_layer():
+    # 16-bit operands give ~1e-2 here (the MLP's first steps); the check must
+    # catch it and the six-MMA pass must meet the bar
+    rng = np.random.default_rng(23)
+    XG, grad, XA = amplifying_layer(64, 300, 200, 1e-3, rng)
+    ref = oracle.precondition(XG, grad, XA)
+    got, route = run_precondition(XG, grad, XA, capi.KFAC_PRECOND_AUTO, with_route=True)
+    assert route == 6
+    assert rel_fro(got[:, :300], ref) <= 2e-3
+    exact, _ = run_precondition(XG, grad, XA, capi.KFAC_PRECOND_FP32, with_route=True)
+    assert np.array_equal(got[:, :300], exact[:, :300])  # the recomputation is the FP32 path's result
+
+
+def test_precondition_auto_keeps_benign_layer():
+    # full-rank input (rows >> d_in): no amplification, 16-bit operands suffice
+    rng = np.random.default_rng(24)
+    XG, grad, XA = amplifying_layer(4096, 300, 200, 1e-3, rng)
+    ref = oracle.precondition(XG, grad, XA)
+    got, route = run_precondition(XG, grad, XA, capi.KFAC_PRECOND_AUTO, with_route=True)
+    assert route == 3
+    assert rel_fro(got[:, :300], ref) <= 4e-4
 
 
 # ------------------------------------------------------------------ whole configurations, stage-wise

@@ -58,8 +58,9 @@ def test_static_scratch_matches_workspace_version_twice():
         wsb = capi.kfac_precondition_workspace(ws_args)
         assert 0 < wsb <= capi.kfac_precondition_static_capacity()
         ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
-        capi.kfac_precondition(ws_args, ws.data_ptr(), wsb, stream())
-        capi.kfac_precondition_static(st_args, stream())
+        precision = capi.KFAC_PRECOND_AUTO if call == 0 else capi.KFAC_PRECOND_FP32
+        capi.kfac_precondition(ws_args, precision, 0, ws.data_ptr(), wsb, stream())
+        capi.kfac_precondition_static(st_args, precision, 0, stream())
         torch.cuda.synchronize()
         assert capi.kfac_device_status(clear=True) == capi.KFAC_OK
         for _, _, o1, o2, d_in in layers:
@@ -73,6 +74,6 @@ def test_static_scratch_rejects_oversized_layers():
     # a 4096 x 4097 layer needs about 300 MB of scratch: refused before any launch
     big = capi.kfac_precond_args(1 << 20, 4096, 2 << 20, 4100, 3 << 20, 4100, 4 << 20, 4100, 4096, 4097)
     assert capi.kfac_precondition_workspace([big]) > capi.kfac_precondition_static_capacity()
-    assert capi.kfac_precondition_static([big], check=False) == capi.KFAC_ERR_WORKSPACE
+    assert capi.kfac_precondition_static([big], capi.KFAC_PRECOND_AUTO, 0, check=False) == capi.KFAC_ERR_WORKSPACE
     bad = capi.kfac_precond_args(1 << 20, 4, 2 << 20, 8, 3 << 20, 8, 2 << 20, 8, 4, 8)  # out aliases grad
-    assert capi.kfac_precondition_static([bad], check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_precondition_static([bad], capi.KFAC_PRECOND_AUTO, 0, check=False) == capi.KFAC_ERR_INVALID_ARG
