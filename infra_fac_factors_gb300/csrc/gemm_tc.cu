@@ -51,7 +51,7 @@ struct GtCfg {
   static constexpr int smem = stages * stage + 1024 + 256;
   // 16-wide k-steps accumulated in one TMEM accumulator between two drains
   // into the epilogue's round-to-nearest fp32 sums (twelve MMAs either way)
-  static constexpr int drain = NS == 3 ? 2 : 4;
+  static constexpr int drain = NS == 3 ? 2 : 8;
 };
 
 struct GtParams {
@@ -75,8 +75,11 @@ struct GtTile {
 };
 
 // tile u -> (problem, m0, n0): binary search over the problems, 32-bit
-// arithmetic inside one (every role decodes every tile)
-__device__ __forceinline__ GtTile gt_decode(const GtParams& prm, long long u) {
+// arithmetic inside one (every role decodes every tile).  With CTA pairs (MC)
+// a work item is two vertically adjacent tiles; CTA `rank` of the pair takes
+// rows m0 + 128 * rank.
+template <bool MC>
+__device__ __forceinline__ GtTile gt_decode(const GtParams& prm, long long u, uint32_t rank) {
   int lo = 0, hi = prm.n_probs;  // largest pi with tile_begin <= u
   while (hi - lo > 1) {
     const int mid = (lo + hi) / 2;
@@ -90,7 +93,7 @@ __device__ __forceinline__ GtTile gt_decode(const GtParams& prm, long long u) {
   const int t = (int)(u - p.tile_begin);
   GtTile r;
   r.prob = pi;
-  r.m0 = (t / p.tiles_n) * 128;
+  r.m0 = (t / p.tiles_n) * (MC ? 256 : 128) + (int)rank * 128;
   r.n0 = (t - (t / p.tiles_n) * p.tiles_n) * 256;
   r.n_mma = (min(256, p.N - r.n0) + 15) / 16 * 16;
   r.K = p.K;
@@ -109,7 +112,12 @@ __device__ __forceinline__ uint64_t gt_desc(uint32_t saddr) {
   return d;
 }
 
-template <int NS>
+// MC: CTA pairs (clusters of two) on vertically adjacent tiles share the B
+// tile: each CTA loads one 128-row half of it with a TMA multicast into both
+// CTAs' shared memory, so an SM reads 128 + 128 operand rows per k instead of
+// 128 + 256.  A stage is refilled only when both CTAs' MMAs have released it
+// (each commit arrives on the empty barriers of both CTAs).
+template <int NS, bool MC>
 __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_constant__ GtParams prm) {
   using Cfg = GtCfg<NS>;
   constexpr int kGtStages = Cfg::stages;
@@ -129,7 +137,7 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGtStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], MC ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -141,15 +149,21 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
   }
   if (warp == 1) tc_alloc(tmem_slot, 512);
   tc_fence_before();
-  __syncthreads();
+  if (MC)
+    cluster_sync();  // the partner's barriers exist before any multicast reaches them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const uint32_t rank = MC ? cluster_ctarank() : 0u;
+  const long long item0 = MC ? blockIdx.x / 2 : blockIdx.x;
+  const long long items_step = MC ? gridDim.x / 2 : gridDim.x;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      for (long long u = blockIdx.x; u < prm.total_tiles && !*abort_flag; u += gridDim.x) {
-        const GtTile tl = gt_decode(prm, u);
+      for (long long u = item0; u < prm.total_tiles && !*abort_flag; u += items_step) {
+        const GtTile tl = gt_decode<MC>(prm, u, rank);
         if (gt_skip(prm, tl.prob)) continue;
         const CUtensorMap* ma = &prm.mapA[tl.prob];
         const CUtensorMap* mb = &prm.mapB[tl.prob];
@@ -161,7 +175,11 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
           for (int s = 0; s < NS; ++s) {
             tma_load_3d(s0 + s * kGtA, ma, kb * kGtBK, tl.m0, s, &full[stage]);
-            tma_load_3d(s0 + NS * kGtA + s * kGtB, mb, kb * kGtBK, tl.n0, s, &full[stage]);
+            if (MC)  // this CTA's half of B (rows n0 + 128 rank ..), into both CTAs
+              tma_load_3d_mc(s0 + NS * kGtA + s * kGtB + rank * (kGtB / 2), mb, kb * kGtBK,
+                             tl.n0 + 128 * (int)rank, s, &full[stage], (uint16_t)0x3);
+            else
+              tma_load_3d(s0 + NS * kGtA + s * kGtB, mb, kb * kGtBK, tl.n0, s, &full[stage]);
           }
           if (++stage == kGtStages) {
             stage = 0;
@@ -174,8 +192,8 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (long long u = blockIdx.x; u < prm.total_tiles && ok; u += gridDim.x) {
-        const GtTile tl = gt_decode(prm, u);
+      for (long long u = item0; u < prm.total_tiles && ok; u += items_step) {
+        const GtTile tl = gt_decode<MC>(prm, u, rank);
         if (gt_skip(prm, tl.prob)) continue;
         const uint32_t idesc = idesc_bf16_f32(tl.n_mma, false, false);
         const int nk = (tl.K + kGtBK - 1) / kGtBK;
@@ -221,7 +239,10 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
               if (acc == 0) acc_phase ^= 1;
             }
           }
-          tc_commit(&empty[stage]);
+          if (MC)
+            tc_commit_mc(&empty[stage], (uint16_t)0x3);
+          else
+            tc_commit(&empty[stage]);
           if (++stage == kGtStages) {
             stage = 0;
             phase ^= 1;
@@ -237,8 +258,8 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
     const int h = e / 4;              // column half of the 256-wide tile
     uint32_t acc = 0, acc_phase = 0;
     bool ok = true;
-    for (long long u = blockIdx.x; u < prm.total_tiles && ok; u += gridDim.x) {
-      const GtTile tl = gt_decode(prm, u);
+    for (long long u = item0; u < prm.total_tiles && ok; u += items_step) {
+      const GtTile tl = gt_decode<MC>(prm, u, rank);
       if (gt_skip(prm, tl.prob)) continue;
       const GtProb& pr = prm.probs[tl.prob];
       const int nsteps = ((tl.K + kGtBK - 1) / kGtBK * (kGtBK / 16) + kGtDrain - 1) / kGtDrain;
@@ -313,7 +334,10 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
       }
     }
   }
-  __syncthreads();
+  if (MC)
+    cluster_sync();  // no multicast or remote arrival is still headed for this CTA
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tc_dealloc(tmem_base, 512);
@@ -462,25 +486,45 @@ int launch_split(const SplitItem* items, int n, int planes, const int* flags, cu
   return KFAC_OK;
 }
 
-int launch_gemm_tc(const GtOperand* ops_in, int n, int ns, const int* flags, cudaStream_t stream) {
+int launch_gemm_tc(const GtOperand* ops_in, int n, int ns, const int* flags, cudaStream_t stream, bool pairs) {
   // longest K first: tiles are dealt round-robin to a persistent grid
   GtOperand* ops = new GtOperand[n > 0 ? n : 1];
   std::copy(ops_in, ops_in + n, ops);
   std::stable_sort(ops, ops + n, [](const GtOperand& x, const GtOperand& y) { return x.K > y.K; });
-  const int rc = launch_gemm_tc_sorted(ops, n, ns, flags, stream);
+  const int rc = launch_gemm_tc_sorted(ops, n, ns, flags, stream, pairs);
   delete[] ops;
   return rc;
 }
 
-int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream) {
+template <int NS, bool MC>
+static int launch_gemm_kernel(const GtParams& prm, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kGtThreads);
+  cfg.dynamicSmemBytes = GtCfg<NS>::smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = MC ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NS, MC>, prm) != cudaSuccess) return KFAC_ERR_CUDA;
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
+int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream, bool pairs) {
   if (ns != 2 && ns != 3) return KFAC_ERR_INVALID_ARG;
   EncodeTiledFn enc = gt_encode_fn();
   if (!enc) return KFAC_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
-  if (sms <= 0) return KFAC_ERR_CUDA;
-  const void* kern = ns == 3 ? (const void*)gemm_tc_kernel<3> : (const void*)gemm_tc_kernel<2>;
+  if (sms < 2) return KFAC_ERR_CUDA;
+  const void* kern = ns == 3 ? (pairs ? (const void*)gemm_tc_kernel<3, true> : (const void*)gemm_tc_kernel<3, false>)
+                             : (pairs ? (const void*)gemm_tc_kernel<2, true> : (const void*)gemm_tc_kernel<2, false>);
   const int smem = ns == 3 ? GtCfg<3>::smem : GtCfg<2>::smem;
   if (!ensure_smem_attr(dev, kern, smem)) return KFAC_ERR_CUDA;
   int* status = device_status_ptr();
@@ -494,7 +538,7 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags,
     for (int i = 0; i < cnt && rc == KFAC_OK; ++i) {
       const GtOperand& o = ops[base + i];
       if (!encode_slices(enc, &prm->mapA[i], o.a, o.M, o.K, o.lda, 128) ||
-          !encode_slices(enc, &prm->mapB[i], o.b, o.N, o.K, o.ldb, 256)) {
+          !encode_slices(enc, &prm->mapB[i], o.b, o.N, o.K, o.ldb, pairs ? 128 : 256)) {
         rc = KFAC_ERR_INVALID_ARG;
         break;
       }
@@ -510,7 +554,8 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags,
       p.flag_idx = flags != nullptr ? o.flag_idx : -1;
       p.alpha = o.alpha;
       p.tile_begin = tiles;
-      tiles += (long long)((o.M + 127) / 128) * p.tiles_n;
+      const long long tiles_m = (o.M + 127) / 128;
+      tiles += (pairs ? (tiles_m + 1) / 2 : tiles_m) * p.tiles_n;  // work items (tile pairs with `pairs`)
     }
     if (rc != KFAC_OK) break;
     prm->n_probs = cnt;
@@ -518,13 +563,15 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags,
     prm->total_tiles = tiles;
     prm->status = status;
     if (tiles > 0) {
-      const int grid = (int)(tiles < sms ? tiles : sms);
-      if (ns == 3)
-        gemm_tc_kernel<3><<<grid, kGtThreads, smem, stream>>>(*prm);
-      else
-        gemm_tc_kernel<2><<<grid, kGtThreads, smem, stream>>>(*prm);
-      count_launch();
-      if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
+      if (pairs) {
+        const long long clusters = tiles < sms / 2 ? tiles : sms / 2;
+        const int grid = (int)(2 * clusters);
+        rc = ns == 3 ? launch_gemm_kernel<3, true>(*prm, grid, stream) : launch_gemm_kernel<2, true>(*prm, grid, stream);
+      } else {
+        const int grid = (int)(tiles < sms ? tiles : sms);
+        rc = ns == 3 ? launch_gemm_kernel<3, false>(*prm, grid, stream)
+                     : launch_gemm_kernel<2, false>(*prm, grid, stream);
+      }
     }
   }
   delete prm;

@@ -66,8 +66,10 @@ int launch_split(const SplitItem* items, int n, int planes, const int* flags, cu
 // ns = operand slices read per product: 3 (six MMAs per multiply-add, all 24
 // bits) or 2 (three MMAs: hi*hi + hi*mid + mid*hi, 16 bits).  Split outputs
 // are written with ns slices.  Problems whose flag_idx >= 0 run only when
-// flags[flag_idx] != 0.
-int launch_gemm_tc(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream);  // sorts by K
-int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream);
+// flags[flag_idx] != 0.  pairs: CTA pairs sharing B through TMA multicast.
+int launch_gemm_tc(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream,
+                   bool pairs = true);  // sorts by K
+int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream,
+                          bool pairs = true);
 
 }  // namespace kfac
