@@ -297,13 +297,9 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
   uint8_t* out_stage = smem + Cfg::stages * Cfg::stage;
   uint64_t* full = reinterpret_cast<uint64_t*>(out_stage + Cfg::out);
   uint64_t* empty = full + Cfg::stages;
-  // TMEM accumulators in a ring: two of 256 columns, or four of 128 for the
-  // panel's 128-wide tiles (its short jobs drain often)
-  constexpr int kAccN = KIND == kItPanel ? 4 : 2;
-  constexpr uint32_t kAccCols = 512 / kAccN;
   uint64_t* acc_full = empty + Cfg::stages;
-  uint64_t* acc_empty = acc_full + kAccN;
-  uint64_t* done_bar = acc_empty + kAccN;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done_bar = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -313,7 +309,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < kAccN; ++a) {
+    for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
       mbar_init(&acc_empty[a], 8);
     }
@@ -378,7 +374,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
               }
               tc_fence_after();
             }
-            const uint32_t d_tmem = tmem_base + acc * kAccCols;
+            const uint32_t d_tmem = tmem_base + acc * 256;
             const uint32_t off = kk * 32;
             uint64_t da[kSlices], db[kSlices];
 #pragma unroll
@@ -394,10 +390,8 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
             tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
             if (glast) {
               tc_commit(&acc_full[acc]);
-              if (++acc == kAccN) {
-                acc = 0;
-                acc_phase ^= 1;
-              }
+              acc ^= 1;
+              if (acc == 0) acc_phase ^= 1;
             }
           }
           tc_commit(&empty[stage]);
@@ -420,13 +414,10 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
     for (long long u = blockIdx.x; u < prm.total_jobs && ok; u += gridDim.x) {
       const ItJob J = it_decode<KIND>(prm, u);
       if (!J.valid) continue;
-      // columns per epilogue warp: the panel's 128-wide tiles are shared by all
-      // eight warps (64 each), the 256-wide ones of the other kinds by halves
-      constexpr int kCw = KIND == kItPanel ? 64 : 128;
-      const bool mine = h * kCw < J.n_mma;  // this warp's columns exist
-      float run[kCw];
+      const bool mine = h * 128 < J.n_mma;  // this warp's 128 columns exist
+      float run[128];
 #pragma unroll
-      for (int t = 0; t < kCw; ++t) run[t] = 0.f;
+      for (int t = 0; t < 128; ++t) run[t] = 0.f;
       const int nsteps = (J.K / 16 + kItDrain - 1) / kItDrain;
       for (int st = 0; st < nsteps; ++st) {
         if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) {
@@ -435,9 +426,9 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         }
         tc_fence_after();
         if (mine) {
-          const uint32_t base = tmem_base + ((uint32_t)(q * 32) << 16) + acc * kAccCols + h * kCw;
+          const uint32_t base = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + h * 128;
 #pragma unroll
-          for (int g = 0; g < kCw / 32; ++g) {
+          for (int g = 0; g < 4; ++g) {
             uint32_t v[32];
             tc_ld_32x32b_x32(base + g * 32, v);
             tc_wait_ld();
@@ -448,14 +439,12 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
-        if (++acc == kAccN) {
-          acc = 0;
-          acc_phase ^= 1;
-        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
       }
       if (!ok || !mine) continue;
       const int mrow = q * 32 + lane;  // row of the 128-row output tile
-      if constexpr (KIND == kItPanel) {
+      if (KIND == kItPanel) {
         // L_rk (r > k) into Lp, or U_rk (r < k) into U, as three bf16 slices
         uint16_t* dst;
         long long sstride;
@@ -466,15 +455,14 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
           dst = prm.b.u + (long long)(J.o_y + mrow) * prm.b.LD + J.o_x;
           sstride = prm.b.R * prm.b.LD;
         }
-        dst += h * kCw;
 #pragma unroll
-        for (int t = 0; t < kCw; t += 8) {
+        for (int t = 0; t < 128; t += 8) {
           float x8[8];
 #pragma unroll
           for (int e8 = 0; e8 < 8; ++e8) x8[e8] = run[t + e8];
           split8_store(x8, dst + t, sstride);
         }
-      } else if constexpr (KIND == kItUpdate) {
+      } else if (KIND == kItUpdate) {
         // -acc into Acc through 32 x 32 TMA add-reductions (or stores, first time)
         for (int g = 0; g < 4; ++g) {
           uint8_t* buf = out_stage + (e * 2 + obuf) * kItOutBlock;
