@@ -73,7 +73,7 @@ class FactorBufs:
 class KFACStep:
     def __init__(self, layers: Sequence[LayerSpec], P: int, gamma: float, decay: float, in_dtype: str,
                  refine: int = capi.KFAC_REFINE_AUTO, device="cuda", n_groups: int = 8,
-                 precond_precision: int = capi.KFAC_PRECOND_AUTO):
+                 precond_precision: int = capi.KFAC_PRECOND_AUTO, inverse_order: str = "size"):
         self.layers = list(layers)
         self.P = P
         self.gamma = float(gamma)
@@ -81,6 +81,9 @@ class KFACStep:
         self.in_dtype = in_dtype
         self.refine = refine
         self.precond_precision = precond_precision
+        if inverse_order not in ("size", "call"):
+            raise ValueError("inverse_order is 'size' or 'call'")
+        self.inverse_order = inverse_order
         self.device = torch.device(device)
         tdt = torch.bfloat16 if in_dtype == "bf16" else torch.float32
         self.kdt = capi.KFAC_BF16 if in_dtype == "bf16" else capi.KFAC_FP32
@@ -146,8 +149,18 @@ class KFACStep:
         self._fac_fp32 = fa_fp32
         self._run_args = [capi.kfac_running_args(F.shards.data_ptr(), F.stride, F.running.data_ptr(),
                                                  F.damped.data_ptr(), F.d, F.ld) for F in self.factor_list()]
-        self._inv_args = [capi.kfac_inverse_args(F.damped.data_ptr(), F.inv.data_ptr(), F.d, F.ld, F.ld)
-                          for F in self.factor_list()]
+        # Inverse batch order: largest factors first ("size", the longest-job-first
+        # rule the pages' inverse placement uses), so that the persistent grids of
+        # every sweep launch start on the longest jobs; or the factor_list order.
+        # info[] and route[] follow the batch order; inv_order[i] is the
+        # factor_list index of batch entry i.
+        facs = self.factor_list()
+        order = list(range(len(facs)))
+        if self.inverse_order == "size":
+            order.sort(key=lambda i: -facs[i].d)
+        self.inv_order = order
+        self._inv_args = [capi.kfac_inverse_args(facs[i].damped.data_ptr(), facs[i].inv.data_ptr(), facs[i].d,
+                                                 facs[i].ld, facs[i].ld) for i in order]
         self._pc_args = []
         for li, L in enumerate(self.layers):
             A, G = self.fa[li], self.fg[li]
