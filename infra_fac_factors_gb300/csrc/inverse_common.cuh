@@ -176,6 +176,7 @@ __device__ int block_chol_inv(T* a, int valid, T& min_piv) {
   __shared__ T wd[4][32][33];  // inverses of the four 32 x 32 diagonal factors
   __shared__ T dinv[128];      // 1 / L_jj
   __shared__ T tmp[96][33];    // partial products of the assembly step
+  __shared__ T colbuf[32];     // pivot, then column j of L, during the 32 x 32 factorisation
   __shared__ int s_fail;
   __shared__ T s_minpiv;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32, nwarps = blockDim.x / 32;
@@ -192,9 +193,15 @@ __device__ int block_chol_inv(T* a, int valid, T& min_piv) {
       for (int c = 0; c < 32; ++c) x[c] = (c <= lane) ? a[(p0 + lane) * P + p0 + c] : T(0);
       int fail = -1;  // uniform over the warp: every pivot is a broadcast
       T mp = T(3.0e38);
+      // Step j: the pivot and then the scaled column j travel through shared
+      // memory (one store per lane, broadcast loads that issue back to back),
+      // not through a chain of 32 shuffles.
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const T piv = __shfl_sync(0xffffffffu, x[j], j);
+        if (lane == j) colbuf[j] = x[j];
+        __syncwarp();
+        const T piv = colbuf[j];
+        __syncwarp();
         if (fail < 0 && !(piv > T(0))) fail = j;
         if (fail < 0) {
           if (p0 + j < valid && piv < mp) mp = piv;
@@ -205,11 +212,14 @@ __device__ int block_chol_inv(T* a, int valid, T& min_piv) {
             x[j] = ljj;
             dinv[p0 + j] = inv;
           }
+          colbuf[lane] = x[j];  // column j of L (zero above the diagonal)
+          __syncwarp();
 #pragma unroll
           for (int c = j + 1; c < 32; ++c) {
-            const T lcj = __shfl_sync(0xffffffffu, x[j], c);
+            const T lcj = colbuf[c];
             if (lane >= c) x[c] -= x[j] * lcj;
           }
+          __syncwarp();
         }
       }
 #pragma unroll
