@@ -213,6 +213,17 @@ typedef struct {
   float* out;          int64_t ld_out;
   int64_t d_out;
   int64_t d_in;
+  /* Optional fused weight step (§II-B, the damped update rule: the weights move
+   * by -lr times the preconditioned gradient).  When `weight` is not NULL the
+   * call also performs weight[r][c] -= lr * out[r][c] (one fp32 fused
+   * multiply-add per element) for r < d_out, c < d_in, once per call with the
+   * final out: in the epilogue of the GEMM that produces it (FP32, and the
+   * layers AUTO recomputes), or in an elementwise pass over the stored out
+   * after the check (the layers AUTO keeps at 16 bits).  weight is fp32
+   * d_out x d_in row-major, ld_weight >= d_in, ld_weight % 4 == 0, 16-byte
+   * aligned, and must not alias out or an input.  NULL: no weight step.     */
+  float* weight;       int64_t ld_weight;
+  float lr;
 } kfac_precond_args;
 
 size_t kfac_precondition_workspace(int n, const kfac_precond_args* args);

@@ -51,7 +51,8 @@ class kfac_inverse_args(C.Structure):
 class kfac_precond_args(C.Structure):
     _fields_ = [("inv_g", C.c_void_p), ("ld_g", C.c_int64), ("grad", C.c_void_p), ("ld_grad", C.c_int64),
                 ("inv_a", C.c_void_p), ("ld_a", C.c_int64), ("out", C.c_void_p), ("ld_out", C.c_int64),
-                ("d_out", C.c_int64), ("d_in", C.c_int64)]
+                ("d_out", C.c_int64), ("d_in", C.c_int64),
+                ("weight", C.c_void_p), ("ld_weight", C.c_int64), ("lr", C.c_float)]
 
 
 exported_symbols = (

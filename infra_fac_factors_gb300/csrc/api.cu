@@ -207,6 +207,13 @@ static bool precond_args_ok(int n, const kfac_precond_args* args) {
     if ((const void*)a.out == (const void*)a.grad || (const void*)a.out == (const void*)a.inv_a ||
         (const void*)a.out == (const void*)a.inv_g)
       return false;
+    if (a.weight) {
+      if (!aligned16(a.weight) || a.ld_weight < a.d_in || a.ld_weight % 4) return false;
+      const void* w = a.weight;
+      if (w == (const void*)a.out || w == (const void*)a.grad || w == (const void*)a.inv_a ||
+          w == (const void*)a.inv_g)
+        return false;
+    }
   }
   return true;
 }

@@ -74,6 +74,26 @@ struct GtTile {
   int prob, m0, n0, n_mma, K;
 };
 
+// w[r][c] = w[r][c] - lr * v, one rounding (the weight step of a row segment
+// of n <= 32 values; every index below is static, so v stays in registers)
+__device__ __forceinline__ void gt_weight_step(float* w, float lr, const float (&v)[32], int n) {
+  if (n == 32) {
+#pragma unroll
+    for (int t = 0; t < 32; t += 4) {
+      float4 x = *reinterpret_cast<const float4*>(w + t);
+      x.x = __fmaf_rn(-lr, v[t], x.x);
+      x.y = __fmaf_rn(-lr, v[t + 1], x.y);
+      x.z = __fmaf_rn(-lr, v[t + 2], x.z);
+      x.w = __fmaf_rn(-lr, v[t + 3], x.w);
+      *reinterpret_cast<float4*>(w + t) = x;
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (t < n) w[t] = __fmaf_rn(-lr, v[t], w[t]);
+  }
+}
+
 // tile u -> (problem, m0, n0): binary search over the problems, 32-bit
 // arithmetic inside one (every role decodes every tile).  With CTA pairs (MC)
 // a work item is two vertically adjacent tiles; CTA `rank` of the pair takes
@@ -307,6 +327,12 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
               for (int t = 0; t < 32; ++t)
                 if (col0 + t < pr.N) dst[t] = run[g * 32 + t] * pr.alpha;
+            }
+            if (pr.w != nullptr) {
+              float v[32];
+#pragma unroll
+              for (int t = 0; t < 32; ++t) v[t] = run[g * 32 + t] * pr.alpha;
+              gt_weight_step(pr.w + (long long)r * pr.ldw + col0, pr.lr, v, fullc ? 32 : pr.N - col0);
             }
           } else {
             uint16_t* dst = static_cast<uint16_t*>(pr.out) + (long long)r * pr.ldc + col0;
@@ -553,6 +579,9 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags,
       p.out_split = o.out_split;
       p.flag_idx = flags != nullptr ? o.flag_idx : -1;
       p.alpha = o.alpha;
+      p.w = o.w;
+      p.ldw = o.ldw;
+      p.lr = o.lr;
       p.tile_begin = tiles;
       const long long tiles_m = (o.M + 127) / 128;
       tiles += (pairs ? (tiles_m + 1) / 2 : tiles_m) * p.tiles_n;  // work items (tile pairs with `pairs`)

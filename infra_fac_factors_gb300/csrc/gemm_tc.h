@@ -18,13 +18,17 @@ struct GtOperand {
   int out_split;
   float alpha;
   int flag_idx;                // index into the launch's flags (see launch_gemm_tc), or -1
+  float* w;                    // fp32 [M][ldw] weights: w -= lr * C (fp32 output only), or null
+  long long ldw;
+  float lr;
 };
 
 struct GtProb {
   void* out;
-  long long ldc, out_slice_stride, tile_begin;
+  float* w;
+  long long ldc, out_slice_stride, tile_begin, ldw;
   int M, N, K, tiles_n, out_split, flag_idx;
-  float alpha;
+  float alpha, lr;
 };
 
 // fp32 src [rows][ld_src] -> bf16 dst slices: slice k at dst + k * slice_stride.
@@ -67,6 +71,7 @@ int launch_split(const SplitItem* items, int n, int planes, const int* flags, cu
 // bits) or 2 (three MMAs: hi*hi + hi*mid + mid*hi, 16 bits).  Split outputs
 // are written with ns slices.  Problems whose flag_idx >= 0 run only when
 // flags[flag_idx] != 0.  pairs: CTA pairs sharing B through TMA multicast.
+// A problem with w applies w -= lr * C in the epilogue (fp32 output only).
 int launch_gemm_tc(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream,
                    bool pairs = true);  // sorts by K
 int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream,

@@ -29,6 +29,10 @@
 //   5. flag the layers whose estimate exceeds kPcAutoTol (or is not finite)
 //   6. steps 1-3 with three slices for the flagged layers (device-side flags:
 //      the launches skip the other layers' work)
+// The optional weight step (weight -= lr * out) runs in the epilogue of the
+// GEMM 2 launch that produces the final out (FP32: the only one; AUTO: the
+// recomputation, for the flagged layers), and for the layers AUTO keeps at 16
+// bits in pc_weight_kernel, from the stored out, after the check.
 // inv_a and inv_g are symmetric, so their rows serve as the K-major operands,
 // and s = inv_g Z' = (Z'^T inv_g)^T.
 #include "common.cuh"
@@ -258,6 +262,88 @@ __global__ void pc_flag_kernel(const double* acc, int n, float tol, int* flags, 
   }
 }
 
+// weight -= lr * out for the layers whose flag is 0 (kept at 16 bits): one
+// warp per 128-column row segment, four consecutive columns per lane
+struct PcWItem {
+  const float* out;
+  float* w;
+  long long ld_out, ld_w, d_out, d_in, unit_begin;
+  float lr;
+  int flag_idx;
+};
+constexpr int kPcWMax = 256;
+struct PcWParams {
+  PcWItem items[kPcWMax];
+  const int* flags;
+  long long total_units;
+  int n;
+};
+
+__global__ void __launch_bounds__(256) pc_weight_kernel(const __grid_constant__ PcWParams prm) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (long long u = (long long)blockIdx.x * 8 + warp; u < prm.total_units; u += (long long)gridDim.x * 8) {
+    int lo = 0, hi = prm.n;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prm.items[mid].unit_begin <= u)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const PcWItem& it = prm.items[lo];
+    if (prm.flags[it.flag_idx] != 0) continue;  // recomputed: stepped in the GEMM epilogue
+    const long long segs = (it.d_in + 127) / 128;
+    const long long local = u - it.unit_begin;
+    const long long r = local / segs;
+    const long long c = (local - r * segs) * 128 + lane * 4;
+    const float* src = it.out + r * it.ld_out + c;
+    float* w = it.w + r * it.ld_w + c;
+    if (c + 4 <= it.d_in) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      float4 x = *reinterpret_cast<const float4*>(w);
+      x.x = __fmaf_rn(-it.lr, v.x, x.x);
+      x.y = __fmaf_rn(-it.lr, v.y, x.y);
+      x.z = __fmaf_rn(-it.lr, v.z, x.z);
+      x.w = __fmaf_rn(-it.lr, v.w, x.w);
+      *reinterpret_cast<float4*>(w) = x;
+    } else {
+      for (int t = 0; t < 4 && c + t < it.d_in; ++t) w[t] = __fmaf_rn(-it.lr, src[t], w[t]);
+    }
+  }
+}
+
+static int launch_weight_step(int n, const kfac_precond_args* args, const int* flags, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  PcWParams* prm = new PcWParams;
+  int rc = KFAC_OK;
+  int cnt = 0;
+  long long total = 0;
+  auto flush = [&]() {
+    if (cnt == 0 || rc != KFAC_OK) return;
+    prm->n = cnt;
+    prm->flags = flags;
+    prm->total_units = total;
+    const long long blocks = (total + 7) / 8, cap = (long long)sms * 8;
+    pc_weight_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, stream>>>(*prm);
+    count_launch();
+    if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
+    cnt = 0;
+    total = 0;
+  };
+  for (int i = 0; i < n && rc == KFAC_OK; ++i) {
+    const kfac_precond_args& a = args[i];
+    if (!a.weight) continue;
+    prm->items[cnt] = PcWItem{a.out, a.weight, a.ld_out, a.ld_weight, a.d_out, a.d_in, total, a.lr, i};
+    total += a.d_out * ((a.d_in + 127) / 128);
+    if (++cnt == kPcWMax) flush();
+  }
+  flush();
+  delete prm;
+  return rc;
+}
+
 __global__ void pc_route_fill_kernel(int* route, int n, int v) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) route[i] = v;
 }
@@ -328,11 +414,18 @@ int launch_precondition(int n, const kfac_precond_args* args, int precision, int
     chk[i] = PcChkItem{a.grad, a.out, y, sv, acc + (size_t)i * 2 * kProbeN * kProbeN,
                        a.ld_grad, a.ld_out, a.d_out, a.d_in, 0};
   }
+  GtOperand* g2w = new GtOperand[n];  // GEMM 2 with the weight step
+  for (int i = 0; i < n; ++i) {
+    g2w[i] = g2[i];
+    g2w[i].w = args[i].weight;
+    g2w[i].ldw = args[i].ld_weight;
+    g2w[i].lr = args[i].lr;
+  }
   int rc = KFAC_OK;
   if (!autop) {
     rc = launch_split(items, 3 * n, 3, nullptr, stream);
     if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, 3, nullptr, stream);
-    if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, 3, nullptr, stream);
+    if (rc == KFAC_OK) rc = launch_gemm_tc(g2w, n, 3, nullptr, stream);
     if (rc == KFAC_OK && route && n > 0) {
       pc_route_fill_kernel<<<(n + 255) / 256, 256, 0, stream>>>(route, n, 6);
       count_launch();
@@ -352,11 +445,13 @@ int launch_precondition(int n, const kfac_precond_args* args, int precision, int
     for (int i = 0; i < 3 * n; ++i) items[i].probe = nullptr;  // the probes are taken
     if (rc == KFAC_OK) rc = launch_split(items, 3 * n, 3, flags, stream);
     if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, 3, flags, stream);
-    if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, 3, flags, stream);
+    if (rc == KFAC_OK) rc = launch_gemm_tc(g2w, n, 3, flags, stream);
+    if (rc == KFAC_OK) rc = launch_weight_step(n, args, flags, stream);
   }
   delete[] items;
   delete[] g1;
   delete[] g2;
+  delete[] g2w;
   delete[] chk;
   return rc;
 }

@@ -73,7 +73,8 @@ class FactorBufs:
 class KFACStep:
     def __init__(self, layers: Sequence[LayerSpec], P: int, gamma: float, decay: float, in_dtype: str,
                  refine: int = capi.KFAC_REFINE_AUTO, device="cuda", n_groups: int = 8,
-                 precond_precision: int = capi.KFAC_PRECOND_AUTO, inverse_order: str = "size"):
+                 precond_precision: int = capi.KFAC_PRECOND_AUTO, inverse_order: str = "size",
+                 weight_lr: Optional[float] = None):
         self.layers = list(layers)
         self.P = P
         self.gamma = float(gamma)
@@ -84,12 +85,14 @@ class KFACStep:
         if inverse_order not in ("size", "call"):
             raise ValueError("inverse_order is 'size' or 'call'")
         self.inverse_order = inverse_order
+        # with weight_lr, the preconditioning call also steps weight[l] -= lr * out[l]
+        self.weight_lr = weight_lr
         self.device = torch.device(device)
         tdt = torch.bfloat16 if in_dtype == "bf16" else torch.float32
         self.kdt = capi.KFAC_BF16 if in_dtype == "bf16" else capi.KFAC_FP32
         vec = 8 if in_dtype == "bf16" else 4
         dev = self.device
-        self.a, self.g, self.gs, self.grad, self.out = [], [], [], [], []
+        self.a, self.g, self.gs, self.grad, self.out, self.weight = [], [], [], [], [], []
         self.fa: List[FactorBufs] = []
         self.fg: List[FactorBufs] = []
         for L in self.layers:
@@ -105,6 +108,8 @@ class KFACStep:
                 self.gs.append(None)
             self.grad.append(torch.zeros((L.d_out, _pad(L.d_in, 32)), dtype=torch.float32, device=dev))
             self.out.append(torch.zeros((L.d_out, _pad(L.d_in, 32)), dtype=torch.float32, device=dev))
+            if weight_lr is not None:
+                self.weight.append(torch.zeros((L.d_out, _pad(L.d_in, 32)), dtype=torch.float32, device=dev))
             self.fa.append(FactorBufs(L.d_in, P, dev))
             self.fg.append(FactorBufs(L.d_out, P, dev))
         nf = 2 * len(self.layers)
@@ -164,9 +169,12 @@ class KFACStep:
         self._pc_args = []
         for li, L in enumerate(self.layers):
             A, G = self.fa[li], self.fg[li]
+            W = self.weight[li] if self.weight_lr is not None else None
             self._pc_args.append(capi.kfac_precond_args(
                 G.inv.data_ptr(), G.ld, self.grad[li].data_ptr(), self.grad[li].shape[1],
-                A.inv.data_ptr(), A.ld, self.out[li].data_ptr(), self.out[li].shape[1], L.d_out, L.d_in))
+                A.inv.data_ptr(), A.ld, self.out[li].data_ptr(), self.out[li].shape[1], L.d_out, L.d_in,
+                W.data_ptr() if W is not None else None, W.shape[1] if W is not None else 0,
+                float(self.weight_lr or 0.0)))
 
     def _build_groups(self, n_groups: int):
         """The argument arrays of each layer group (see layer_groups)."""

@@ -174,6 +174,12 @@ def kron_precondition_bruteforce(A, G, grad, gamma: float) -> np.ndarray:
     return v.reshape(grad.shape, order="F")
 
 
+def weight_step(W: np.ndarray, V: np.ndarray, lr: float) -> np.ndarray:
+    """§II-B damped update rule, the step itself: the weights move against the
+    preconditioned gradient, W - lr * V."""
+    return np.asarray(W, np.float64) - float(lr) * np.asarray(V, np.float64)
+
+
 # ---------------------------------------------------------------- conv helper
 def spatial_sum(g: np.ndarray, batch: int, hw: int) -> np.ndarray:
     """Per-sample sum of a conv layer's output gradients over its H*W

@@ -161,7 +161,11 @@ def test_precondition_rejects_invalid():
     # four operands as three bf16 slices: grad 8x16, inv_a 12x16, inv_g 8x8, tmp^T 12x8, each 256-B aligned;
     # then the probe vectors (12 + 8 rows of 8 fp32), the 2 x 8 x 8 fp64 bilinear sums and the flag
     assert ws == (768 + 1280 + 512 + 768) + 768 + 1024 + 256
-    for bad in (pa(d_in=0), pa(ld_g=4), pa(ld_grad=10), pa(out=A16 * 2), pa(inv_a=A16 + 4)):
+    assert capi.kfac_precondition_workspace([pa(weight=A16 * 6, ld_weight=12, lr=0.1)]) == ws
+    for bad in (pa(d_in=0), pa(ld_g=4), pa(ld_grad=10), pa(out=A16 * 2), pa(inv_a=A16 + 4),
+                # the weight step: aliasing out, misaligned, too short a row, ld not a multiple of 4
+                pa(weight=A16 * 4, ld_weight=12), pa(weight=A16 * 6 + 4, ld_weight=12),
+                pa(weight=A16 * 6, ld_weight=8), pa(weight=A16 * 6, ld_weight=14)):
         assert capi.kfac_precondition_workspace([bad]) == 0
         assert capi.kfac_precondition([bad], 0, 0, A16 * 5, ws, check=False) == capi.KFAC_ERR_INVALID_ARG
     assert capi.kfac_precondition([pa()], 0, 0, A16 * 5, ws - 4, check=False) == capi.KFAC_ERR_WORKSPACE

@@ -215,6 +215,30 @@ def test_precondition_equals_bruteforce_kronecker(d_in, d_out):
     assert np.abs(XA @ grad.T @ XG - V.T).max() < 1e-9 * np.abs(V).max()
 
 
+def test_weight_step_values_and_quadratic_minimiser():
+    # the step itself, by hand
+    W = np.array([[1.0, -2.0], [0.5, 4.0]])
+    V = np.array([[0.25, 1.0], [-2.0, 0.0]])
+    assert np.array_equal(oracle.weight_step(W, V, 0.5), np.array([[0.875, -2.5], [1.5, 4.0]]))
+    # f(W) = 1/2 <W, G W A> - <B, W> has curvature exactly A (x) G and gradient
+    # G W A - B: one damped K-FAC step with lr = 1 from any W lands on the
+    # minimiser G^-1 B A^-1 as gamma -> 0
+    A, G = spd(5, seed=11), spd(4, seed=12)
+    B = rnd(4, 5, seed=13)
+    W0 = rnd(4, 5, seed=14)
+    grad = G @ W0 @ A - B
+    XA, _ = oracle.spd_inverse(oracle.damp(A, 1e-12))
+    XG, _ = oracle.spd_inverse(oracle.damp(G, 1e-12))
+    W1 = oracle.weight_step(W0, oracle.precondition(XG, grad, XA), 1.0)
+    assert np.abs(G @ W1 @ A - B).max() <= 1e-8 * np.abs(B).max()
+    # with damping the step is shorter along every direction: f decreases, not to the minimum
+    XA, _ = oracle.spd_inverse(oracle.damp(A, 0.5))
+    XG, _ = oracle.spd_inverse(oracle.damp(G, 0.5))
+    W2 = oracle.weight_step(W0, oracle.precondition(XG, grad, XA), 1.0)
+    f = lambda W: 0.5 * np.sum(W * (G @ W @ A)) - np.sum(B * W)
+    assert f(W1) < f(W2) < f(W0)
+
+
 def test_precondition_self_adjoint_and_linear():
     # adjoint test <P(U), V> = <U, P(V)> for the symmetric map P(V) = XG V XA
     XG, _ = oracle.spd_inverse(spd(7, seed=1))

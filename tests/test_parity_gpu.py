@@ -252,15 +252,18 @@ def test_damped_inverse_reports_first_bad_pivot():
 
 
 # ------------------------------------------------------------------ a5: precondition
-def run_precondition(XG, grad, XA, precision=capi.KFAC_PRECOND_FP32, with_route=False):
+def run_precondition(XG, grad, XA, precision=capi.KFAC_PRECOND_FP32, with_route=False, weight=None, lr=0.0):
+    """out (and with `weight`: the stepped weights) of one layer's call."""
     d_out, d_in = grad.shape
     ldg, lda, ldw, ldo = pad(d_out, 4), pad(d_in, 4) + 4, pad(d_in, 4), pad(d_in, 4) + 8
     tg = to_dev(XG, capi.KFAC_FP32, ldg)
     ta = to_dev(XA, capi.KFAC_FP32, lda)
     tw = to_dev(grad, capi.KFAC_FP32, ldw)
     out = torch.full((d_out, ldo), float("nan"), device="cuda")
+    ldW = pad(d_in, 4) + 12
+    tW = to_dev(weight, capi.KFAC_FP32, ldW) if weight is not None else None
     args = [capi.kfac_precond_args(tg.data_ptr(), ldg, tw.data_ptr(), ldw, ta.data_ptr(), lda, out.data_ptr(), ldo,
-                                   d_out, d_in)]
+                                   d_out, d_in, tW.data_ptr() if tW is not None else None, ldW, lr)]
     wsb = capi.kfac_precondition_workspace(args)
     ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
     route = torch.full((1,), -1, dtype=torch.int32, device="cuda")
@@ -268,6 +271,10 @@ def run_precondition(XG, grad, XA, precision=capi.KFAC_PRECOND_FP32, with_route=
     sync()
     got = out.cpu().numpy()
     assert np.isnan(got[:, d_in:]).all()  # padding of out untouched
+    if weight is not None:
+        Wn = tW.cpu().numpy()
+        assert (Wn[:, d_in:] == 0).all()  # padding untouched
+        return got, int(route.item()), Wn[:, :d_in]
     if with_route:
         return got, int(route.item())
     return got
@@ -336,6 +343,30 @@ def test_precondition_auto_recomputes_amplifying_layer():
     assert rel_fro(got[:, :300], ref) <= 2e-3
     exact, _ = run_precondition(XG, grad, XA, capi.KFAC_PRECOND_FP32, with_route=True)
     assert np.array_equal(got[:, :300], exact[:, :300])  # the recomputation is the FP32 path's result
+
+
+@pytest.mark.parametrize("precision", [capi.KFAC_PRECOND_FP32, capi.KFAC_PRECOND_AUTO])
+@pytest.mark.parametrize("rows", [64, 4096])
+def test_precondition_fused_weight_step(precision, rows):
+    # rows = 64: the amplifying layer (AUTO recomputes it: the step comes from the
+    # recomputed tiles); rows = 4096: kept at 16 bits (the step comes from the
+    # stored out in the last launch)
+    rng = np.random.default_rng(25 + rows)
+    XG, grad, XA = amplifying_layer(rows, 300, 200, 1e-3, rng)
+    W = rng.standard_normal(grad.shape).astype(np.float32)
+    lr = np.float32(0.05)
+    got, route, Wn = run_precondition(XG, grad, XA, precision, weight=W, lr=float(lr))
+    V = got[:, :300]
+    if precision == capi.KFAC_PRECOND_AUTO:
+        assert route == (6 if rows == 64 else 3)
+    # one fused multiply-add per element from the call's own out
+    exact = (W.astype(np.float64) - np.float64(lr) * V.astype(np.float64)).astype(np.float32)
+    assert (np.abs(Wn - exact) <= np.spacing(np.abs(exact))).all()
+    # against the oracle: the step's error is lr times out's error, plus W's rounding
+    Vref = oracle.precondition(XG, grad, XA)
+    ref = oracle.weight_step(W, Vref, float(lr))
+    bound = 2e-3 * float(lr) * np.linalg.norm(Vref) + 2.0 ** -23 * np.linalg.norm(W)
+    assert np.linalg.norm(Wn - ref) <= bound
 
 
 def test_precondition_auto_keeps_benign_layer():
@@ -444,3 +475,26 @@ def test_config_resnet_conv_one_step():
 
 def test_config_bert_layer_three_steps():
     check_config("bert_layer", 3, inv_steps=(0, 2))
+
+
+def test_step_applies_the_weight_step_after_routing():
+    # two layers of 256 rows: a 785-wide input (rank-deficient: AUTO recomputes
+    # it with 24-bit operands) and a 65-wide one (kept at 16 bits); from zero
+    # weights one step must leave weight = -lr * out exactly in both
+    rng = np.random.default_rng(26)
+    specs = [LayerSpec(785, 64, 256, 256, 1), LayerSpec(65, 64, 256, 256, 1)]
+    step = KFACStep(specs, 4, 1e-3, 0.95, "bf16", refine=capi.KFAC_REFINE_AUTO, weight_lr=0.25)
+    for li, L in enumerate(specs):
+        a = synth.round_bf16(np.maximum(rng.standard_normal((256, L.d_in)), 0.0)).astype(np.float32)
+        a[:, -1] = 1.0
+        g = synth.round_bf16(rng.standard_normal((256, L.d_out)) * 1e-3).astype(np.float32)
+        grad = (g.astype(np.float64).T @ a.astype(np.float64) / 256).astype(np.float32)
+        step.set_layer_inputs(li, torch.from_numpy(a), torch.from_numpy(g), torch.from_numpy(grad))
+    step.step(first_step=True)
+    sync()
+    assert step.pc_route.cpu().numpy().tolist() == [6, 3]  # both paths of the last launch
+    for li, L in enumerate(specs):
+        V = step.out[li].cpu().numpy()[:, :L.d_in]
+        W = step.weight[li].cpu().numpy()
+        assert np.array_equal(W[:, :L.d_in], (np.float32(-0.25) * V).astype(np.float32))
+        assert (W[:, L.d_in:] == 0).all()
