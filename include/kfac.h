@@ -253,10 +253,14 @@ int kfac_precondition_static(int n, const kfac_precond_args* args, int precision
 
 /* ------------------------------------------------------------- index tables
  * The work units kfac_factors uses to cover the upper tiles of a d x d factor
- * on the tensor-core path: for every 128-row block i, the columns
- * [128 i, d) cut into chunks of at most 256.  Unit u is
- * (row_block[u], col_start[u], width[u]).  Writes min(count, capacity)
- * entries and returns the total count in *count.  Host only.                 */
+ * on the tensor-core path (one per CTA of a CTA pair): row blocks 2s and
+ * 2s + 1 both take the columns [256 s, d) cut into chunks of at most 256;
+ * units 2v and 2v + 1 are the two row blocks of chunk v.  A unit stores only
+ * its columns >= 128 i of an existing row block i (row block 2s + 1's first
+ * chunk begins with its lower tile; with an odd number of row blocks the last
+ * pair's second unit stores nothing).  Unit u is (row_block[u], col_start[u],
+ * width[u]).  Writes min(count, capacity) entries and returns the total count
+ * in *count.  Host only.                                                      */
 int kfac_factor_tile_map(int64_t d, int64_t capacity, int32_t* row_block,
                          int64_t* col_start, int32_t* width, int64_t* count);
 

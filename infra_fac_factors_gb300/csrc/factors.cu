@@ -15,6 +15,11 @@
 //   warps 2-5 epilogue: TMEM -> registers -> scale -> global fp32 stores.
 // Two 128 x 256 fp32 accumulators in TMEM (all 512 columns) let the epilogue
 // of one unit overlap the main loop of the next.
+// CTA pairs (clusters of two) take the two row blocks of one pair-chunk of the
+// tile map (tilemap.cuh): they share the column operand x[k, j0:j0+w], each
+// CTA loading half of its 64-column boxes with a TMA multicast into both, so
+// an SM reads 128 + 128 operand columns per k instead of 128 + 256.  A stage
+// is refilled once both CTAs' MMAs have released it.
 //
 // fp32 inputs: exact fp32 products on CUDA cores (simt.cuh).
 #include <cuda.h>
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSyStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 2);  // both CTAs' MMAs release a stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -126,19 +131,24 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
   }
   if (warp == 1) tc_alloc(tmem_slot, 512);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // the partner's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const uint32_t rank = cluster_ctarank();
+  // this CTA's units: 2 v + rank for the pair-chunks v of its cluster
+  const long long pair0 = blockIdx.x / 2, pair_step = gridDim.x / 2, npairs = prm.total_units / 2;
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      for (long long u = blockIdx.x; u < prm.total_units && !*abort_flag; u += gridDim.x) {
-        const SyUnit un = sy_decode(prm, u);
+      for (long long v = pair0; v < npairs && !*abort_flag; v += pair_step) {
+        const SyUnit un = sy_decode(prm, 2 * v + rank);
         const SyProb& pr = prm.probs[un.prob];
         const CUtensorMap* map = &prm.maps[un.prob];
         const int nb = (un.w + 63) / 64;
         const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
+        // this CTA's share of the column boxes (multicast to both CTAs)
+        const int half = (nb + 1) / 2, q0 = rank == 0 ? 0 : half, q1 = rank == 0 ? half : nb;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
           uint8_t* sa = smem + stage * kSyStageBytes;
@@ -146,8 +156,9 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
           mbar_arrive_expect_tx(&full[stage], (uint32_t)((2 + nb) * kSyBox));
           tma_load_3d(sa, map, un.i * 128, kb * kSyBK, un.p, &full[stage]);
           tma_load_3d(sa + kSyBox, map, un.i * 128 + 64, kb * kSyBK, un.p, &full[stage]);
-          for (int q = 0; q < nb; ++q)
-            tma_load_3d(sb + q * kSyBox, map, (int)un.j0 + 64 * q, kb * kSyBK, un.p, &full[stage]);
+          for (int q = q0; q < q1; ++q)
+            tma_load_3d_mc(sb + q * kSyBox, map, (int)un.j0 + 64 * q, kb * kSyBK, un.p, &full[stage],
+                           (uint16_t)0x3);
           if (++stage == kSyStages) {
             stage = 0;
             phase ^= 1;
@@ -159,8 +170,8 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (long long u = blockIdx.x; u < prm.total_units && ok; u += gridDim.x) {
-        const SyUnit un = sy_decode(prm, u);
+      for (long long v = pair0; v < npairs && ok; v += pair_step) {
+        const SyUnit un = sy_decode(prm, 2 * v + rank);
         const SyProb& pr = prm.probs[un.prob];
         const int nb = (un.w + 63) / 64;
         const uint32_t idesc = idesc_bf16_f32(nb * 64, true, true);
@@ -188,7 +199,7 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
               const uint64_t bd = smem_desc_sw128(b0 + kk * 2048, kSyBox, 1024);
               tc_mma_bf16(d_tmem, ad, bd, idesc, (kb != kc || kk != 0) ? 1u : 0u);
             }
-            tc_commit(&empty[stage]);
+            tc_commit_mc(&empty[stage], (uint16_t)0x3);
             if (++stage == kSyStages) {
               stage = 0;
               phase ^= 1;
@@ -209,8 +220,8 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
     uint32_t acc = 0, acc_phase = 0;
     int obuf = 0;  // staging buffer of this warp in use
     bool ok = true;
-    for (long long u = blockIdx.x; u < prm.total_units && ok; u += gridDim.x) {
-      const SyUnit un = sy_decode(prm, u);
+    for (long long v = pair0; v < npairs && ok; v += pair_step) {
+      const SyUnit un = sy_decode(prm, 2 * v + rank);
       const SyProb& pr = prm.probs[un.prob];
       const int nb = (un.w + 63) / 64;
       const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
@@ -220,6 +231,7 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
       float* orow = outp + (long long)r * pr.ld_out;
       const long long jend = un.j0 + un.w;
       const long long lower_from = (long long)(un.i + 1) * 128;  // columns in lower-tile territory
+      const long long store_from = (long long)un.i * 128;          // columns before it: not this unit's
       for (int ch = 0; ch < nchunks; ++ch) {
         if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) {
           ok = false;
@@ -242,7 +254,7 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
             tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
             tc_wait_ld();
             const long long col0 = un.j0 + c * 32;
-            if (col0 >= jend || r0 >= pr.d) continue;  // uniform over the warp
+            if (col0 >= jend || col0 < store_from || r0 >= pr.d) continue;  // uniform over the warp
             if (col0 + 32 > d4 && d4 != pr.d) {
               if (r < pr.d)
                 for (int t = 0; t < 32; ++t) {
@@ -281,7 +293,7 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
           tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
           tc_wait_ld();
           const long long col0 = un.j0 + c * 32;
-          if (r < pr.d && col0 < jend) {
+          if (r < pr.d && col0 < jend && col0 >= store_from) {
             float o[32];
 #pragma unroll
             for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(v[t]) * pr.scale;
@@ -323,7 +335,7 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
     if (lane == 0) bulk_wait<0>();  // all TMA stores of this warp complete before exit
     __syncwarp();
   }
-  __syncthreads();
+  cluster_sync();  // no multicast or remote arrival is still headed for this CTA
   if (warp == 1) {
     tc_fence_after();
     tc_dealloc(tmem_base, 512);
@@ -476,8 +488,21 @@ int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mi
       prm.status = device_status_ptr();
       if (!prm.status) return KFAC_ERR_CUDA;
       if (units == 0) continue;
-      const int grid = (int)(units < sms ? units : sms);
-      syrk_tc_kernel<<<grid, 192, kSySmem, stream>>>(prm);
+      // clusters of two CTAs, one per pair-chunk of the tile map
+      const long long pairs = units / 2, clusters = pairs < sms / 2 ? pairs : sms / 2;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(2 * clusters));
+      cfg.blockDim = dim3(192);
+      cfg.dynamicSmemBytes = kSySmem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, syrk_tc_kernel, prm) != cudaSuccess) return KFAC_ERR_CUDA;
       count_launch();
       if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
     }

@@ -16,5 +16,5 @@ from .kfac import (  # noqa: F401
     factor, shard_factors, aggregate, update_running, damp,
     cholesky_lower, lower_tri_inverse, spd_inverse, damped_inverse,
     precondition, spatial_sum, factor_tile_units, upper_tiles,
-    packed_index, kron_precondition_bruteforce, kfac_step, weight_step,
+    packed_index, kron_precondition_bruteforce, kfac_step, weight_step, stored_part,
 )

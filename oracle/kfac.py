@@ -198,18 +198,30 @@ def upper_tiles(d: int, tile: int = 128):
 
 
 def factor_tile_units(d: int, bm: int = 128, bn: int = 256):
-    """Work units that cover the upper-triangle tiles of a d x d factor:
-    for each row block i (rows [i*bm, i*bm+bm)), the columns [i*bm, d) are cut
-    into chunks of at most bn.  Each unit is (i, j0, width)."""
-    T = -(-d // bm)
+    """Work units that cover the upper-triangle tiles of a d x d factor, in
+    pairs of row blocks (the tensor-core SYRK runs a CTA pair per pair):
+    pair s = row blocks (2s, 2s+1) takes the columns [s*bn, d) in chunks of at
+    most bn (bn = 2*bm); each chunk gives the units (2s, j0, w) and
+    (2s+1, j0, w).  A unit stores only its columns >= i*bm of an existing row
+    block i (see ``stored_part``)."""
+    assert bn == 2 * bm
+    n0 = -(-d // bn)
     units = []
-    for i in range(T):
-        j0 = i * bm
-        while j0 < d:
+    for s in range(n0):
+        for v in range(n0 - s):
+            j0 = bn * (s + v)
             w = min(bn, d - j0)
-            units.append((i, j0, w))
-            j0 += bn
+            units.append((2 * s, j0, w))
+            units.append((2 * s + 1, j0, w))
     return units
+
+
+def stored_part(unit, d: int, bm: int = 128):
+    """(rows, cols) ranges of a unit that land in the factor (possibly empty)."""
+    i, j0, w = unit
+    r0, r1 = i * bm, min(i * bm + bm, d)
+    c0, c1 = max(j0, i * bm), j0 + w
+    return (r0, max(r0, r1)), (c0, max(c0, c1))
 
 
 def packed_index(i: int, j: int, d: int) -> int:

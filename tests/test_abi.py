@@ -221,4 +221,6 @@ int main() {
         subprocess.run(["g++", "-O2", "-std=c++17", "-D__host__=", "-D__device__=", "-I", csrc, c, "-o", exe],
                        check=True)
         n, bad = map(int, subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split())
-    assert n == 988736 and bad == 0
+    # every unit of every size decoded: sum over the sizes of 2 * n0 (n0 + 1) / 2, n0 = ceil(d / 256)
+    sizes = [q + 1 + (q // 1000) * 2000 for q in range(3000)] + [16384, 32768, 65536]
+    assert n == sum((-(-d // 256)) * (-(-d // 256) + 1) for d in sizes) and bad == 0

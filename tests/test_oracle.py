@@ -268,15 +268,23 @@ def test_factor_tile_units_cover_upper_tiles_once(d):
     bm, bn = 128, 256
     units = oracle.factor_tile_units(d, bm, bn)
     seen = np.zeros((d, d), dtype=np.int32)
-    for i, j0, w in units:
-        assert 1 <= w <= bn and j0 >= i * bm and j0 + w <= d
-        seen[i * bm:min(i * bm + bm, d), j0:j0 + w] += 1
+    for u in units:
+        i, j0, w = u
+        assert 1 <= w <= bn and j0 % bn == 0 and j0 + w <= d
+        # what a unit computes but drops: at most its first bm columns (the
+        # lower tile of the pair's second row block), or all of a stand-in
+        (r0, r1), (c0, c1) = oracle.stored_part(u, d, bm)
+        assert c0 - j0 in (0, bm) or r0 >= d
+        seen[r0:r1, c0:c1] += 1
     r = np.arange(d)[:, None]
     c = np.arange(d)[None, :]
     want = (c >= (r // bm) * bm).astype(np.int32)
     assert np.array_equal(seen, want)
-    # units are ordered by row block, then column
-    assert units == sorted(units)
+    # units come in pairs of row blocks (2s, 2s+1) sharing their columns,
+    # ordered by pair, then column
+    assert all(units[2 * k][0] + 1 == units[2 * k + 1][0] and units[2 * k][0] % 2 == 0
+               and units[2 * k][1:] == units[2 * k + 1][1:] for k in range(len(units) // 2))
+    assert units[0::2] == sorted(units[0::2])
 
 
 @pytest.mark.parametrize("d", [1, 5, 128, 300])
