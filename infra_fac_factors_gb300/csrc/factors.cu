@@ -81,17 +81,14 @@ struct SyUnit {
   int64_t j0;
 };
 
-// Work unit u -> (problem, shard, row block, columns): binary search over the
-// problems, then the constant-time tile map (all three roles decode every unit).
-__device__ __forceinline__ SyUnit sy_decode(const SyParams& prm, long long u) {
-  int lo = 0, hi = prm.n_probs;  // largest pi with unit_begin <= u
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) / 2;
-    if (prm.probs[mid].unit_begin <= u)
-      lo = mid;
-    else
-      hi = mid;
-  }
+// Work unit u -> (problem, shard, row block, columns), then the constant-time
+// tile map (all three roles decode every unit).  Each role walks its units in
+// increasing order, so the problem is found by advancing a cursor (`lo`, 0 at
+// the start) over the problem table, which lives in the kernel's parameter
+// space: a search with data-dependent indices there costs a constant-cache
+// miss per probe.
+__device__ __forceinline__ SyUnit sy_decode(const SyParams& prm, long long u, int& lo) {
+  while (lo + 1 < prm.n_probs && prm.probs[lo + 1].unit_begin <= u) ++lo;
   const SyProb& pr = prm.probs[lo];
   const int local = (int)(u - pr.unit_begin);
   SyUnit r;
@@ -141,8 +138,9 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
+      int cur = 0;
       for (long long v = pair0; v < npairs && !*abort_flag; v += pair_step) {
-        const SyUnit un = sy_decode(prm, 2 * v + rank);
+        const SyUnit un = sy_decode(prm, 2 * v + rank, cur);
         const SyProb& pr = prm.probs[un.prob];
         const CUtensorMap* map = &prm.maps[un.prob];
         const int nb = (un.w + 63) / 64;
@@ -170,8 +168,9 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
+      int cur = 0;
       for (long long v = pair0; v < npairs && ok; v += pair_step) {
-        const SyUnit un = sy_decode(prm, 2 * v + rank);
+        const SyUnit un = sy_decode(prm, 2 * v + rank, cur);
         const SyProb& pr = prm.probs[un.prob];
         const int nb = (un.w + 63) / 64;
         const uint32_t idesc = idesc_bf16_f32(nb * 64, true, true);
@@ -220,8 +219,9 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
     uint32_t acc = 0, acc_phase = 0;
     int obuf = 0;  // staging buffer of this warp in use
     bool ok = true;
+    int cur = 0;
     for (long long v = pair0; v < npairs && ok; v += pair_step) {
-      const SyUnit un = sy_decode(prm, 2 * v + rank);
+      const SyUnit un = sy_decode(prm, 2 * v + rank, cur);
       const SyProb& pr = prm.probs[un.prob];
       const int nb = (un.w + 63) / 64;
       const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
