@@ -76,6 +76,15 @@ unsigned long long kfac_launch_count(void);
  * Synchronises `stream`. */
 int kfac_device_status(int* status_out, int clear, void* stream);
 
+/* Failure-detection self-test (no counterpart on the pages; a property of the
+ * library): launches one CTA that waits, with the same bounded wait every
+ * tcgen05 kernel of the library uses, on an mbarrier that nothing arrives on.
+ * After limit_cycles SM clock cycles the wait gives up, the kernel records
+ * KFAC_ERR_TIMEOUT in the device status word (see kfac_device_status) and
+ * returns; the context stays usable.  limit_cycles in [1000, 4e9] (the
+ * kernels' own limit), else KFAC_ERR_INVALID_ARG.  Asynchronous on stream.  */
+int kfac_wait_selftest(int64_t limit_cycles, void* stream);
+
 /* -------------------------------------------------------- 1. factors (a1, a2)
  * Per-worker Kronecker factors (§II-B, Eq. (7)/(8); §II-C local factors).
  * For each problem, x holds `rows` rows split into P equal contiguous shards

@@ -16,7 +16,7 @@ __all__ = [
     "KFAC_PRECOND_FP32", "KFAC_PRECOND_AUTO",
     "kfac_factor_args", "kfac_running_args", "kfac_inverse_args", "kfac_precond_args",
     "KFACError", "lib", "library_path", "exported_symbols",
-    "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status",
+    "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
     "kfac_factors", "kfac_spatial_sum", "kfac_update_running",
     "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
@@ -56,7 +56,8 @@ class kfac_precond_args(C.Structure):
 
 
 exported_symbols = (
-    "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_factors", "kfac_spatial_sum",
+    "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
+    "kfac_factors", "kfac_spatial_sum",
     "kfac_update_running", "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
     "kfac_precondition_static", "kfac_factor_tile_map",
@@ -81,6 +82,7 @@ def lib() -> C.CDLL:
         "kfac_version": (C.c_int, []),
         "kfac_launch_count": (C.c_ulonglong, []),
         "kfac_device_status": (C.c_int, [P(C.c_int), C.c_int, C.c_void_p]),
+        "kfac_wait_selftest": (C.c_int, [C.c_int64, C.c_void_p]),
         "kfac_factors": (C.c_int, [C.c_int, P(kfac_factor_args), C.c_int, C.c_int, C.c_int, C.c_void_p]),
         "kfac_spatial_sum": (C.c_int, [C.c_void_p, C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
                                        C.c_void_p, C.c_int64, C.c_void_p]),
@@ -139,6 +141,12 @@ def kfac_device_status(clear: bool = False, stream: int = 0) -> int:
     v = C.c_int(0)
     _check("kfac_device_status", lib().kfac_device_status(C.byref(v), int(clear), stream))
     return v.value
+
+
+def kfac_wait_selftest(limit_cycles: int, stream: int = 0, check: bool = True) -> int:
+    """One CTA's bounded wait on an mbarrier nothing arrives on (records KFAC_ERR_TIMEOUT)."""
+    st = lib().kfac_wait_selftest(int(limit_cycles), stream)
+    return _check("kfac_wait_selftest", st) if check else st
 
 
 def kfac_factors(args, dtype: int, P: int, mirror: int = 0, stream: int = 0, check: bool = True) -> int:

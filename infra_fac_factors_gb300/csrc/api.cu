@@ -6,6 +6,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "common.cuh"
 #include "launch.h"
 #include "tilemap.cuh"
 
@@ -92,6 +93,39 @@ const char* kfac_status_string(int status) {
 int kfac_version(void) { return 100; }
 
 unsigned long long kfac_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"
+
+namespace kfac {
+// One CTA waits, with the kernels' bounded wait, on an mbarrier that nothing
+// arrives on: the wait must give up after `limit` cycles, record
+// KFAC_ERR_TIMEOUT in the status word and let the kernel return.
+__global__ void wait_selftest_kernel(int* status, long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, limit);
+  __syncthreads();
+}
+}  // namespace kfac
+
+extern "C" {
+
+int kfac_wait_selftest(int64_t limit_cycles, void* stream) {
+  if (limit_cycles < 1000 || limit_cycles > kfac::kWaitLimitCycles) return KFAC_ERR_INVALID_ARG;
+  const int dc = kfac::check_device();
+  if (dc != KFAC_OK) return dc;
+  int* p = kfac::device_status_ptr();
+  if (!p) return KFAC_ERR_CUDA;
+  kfac::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(p, (long long)limit_cycles);
+  kfac::count_launch();
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
 
 int kfac_device_status(int* status_out, int clear, void* stream) {
   if (!status_out) return KFAC_ERR_INVALID_ARG;

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_exports_every_declared_function():
     names = declared_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     out = subprocess.run(["nm", "-D", "--defined-only", capi.library_path], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (kfac_[a-z_0-9]+)$", out, flags=re.M))
     for n in names:
@@ -181,6 +181,11 @@ def test_spatial_sum_rejects_invalid():
     assert f(A16, 0, 2, 4, 8, 4, A16, 8, check=False) == capi.KFAC_ERR_INVALID_ARG
     assert f(A16, 0, 0, 4, 8, 8, A16, 8, check=False) == capi.KFAC_ERR_INVALID_ARG
     assert f(A16, 1, 2, 4, 8, 8, A16, 6, check=False) == capi.KFAC_ERR_INVALID_ARG
+
+
+def test_wait_selftest_rejects_limits_outside_the_kernels_range():
+    assert capi.kfac_wait_selftest(10, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_wait_selftest(5_000_000_000, check=False) == capi.KFAC_ERR_INVALID_ARG
 
 
 def test_empty_calls_are_no_ops():

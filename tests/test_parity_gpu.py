@@ -498,3 +498,21 @@ def test_step_applies_the_weight_step_after_routing():
         W = step.weight[li].cpu().numpy()
         assert np.array_equal(W[:, :L.d_in], (np.float32(-0.25) * V).astype(np.float32))
         assert (W[:, L.d_in:] == 0).all()
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    # a wait that nothing ends (an mbarrier no one arrives on) must give up after
+    # its limit (here 2e8 cycles, ~0.1 s), record KFAC_ERR_TIMEOUT and return
+    assert capi.kfac_device_status(clear=True) in (capi.KFAC_OK, capi.KFAC_ERR_TIMEOUT)
+    capi.kfac_wait_selftest(200_000_000, stream())
+    torch.cuda.synchronize()  # the kernel returned on its own
+    assert capi.kfac_device_status(clear=True) == capi.KFAC_ERR_TIMEOUT
+    assert capi.kfac_device_status() == capi.KFAC_OK
+    # the library still computes on the same context
+    rng = np.random.default_rng(27)
+    XG, _ = oracle.spd_inverse(spd_case(40, rng).astype(np.float64))
+    XA, _ = oracle.spd_inverse(spd_case(70, rng).astype(np.float64))
+    grad = rng.standard_normal((40, 70)).astype(np.float32)
+    got = run_precondition(XG.astype(np.float32), grad, XA.astype(np.float32))
+    assert rel_fro(got[:, :70], oracle.precondition(XG, grad, XA)) <= 2e-3
+    assert capi.kfac_device_status() == capi.KFAC_OK
