@@ -38,7 +38,6 @@ namespace kfac {
 
 constexpr int kItBK = 32;
 constexpr int kItA = 128 * kItBK * 2;  // one slice of the A tile (8 KB)
-constexpr int kItOutBlock = 4096;     // one 32 x 32 fp32 block
 constexpr int kItThreads = 320;
 // 16-wide k-steps accumulated in one TMEM accumulator between two drains into
 // the epilogue's round-to-nearest fp32 sums
@@ -51,16 +50,22 @@ enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
 
 // Shared-memory ring of each kind: a stage holds one 32-wide k-block of all
 // three slices of A (128 rows) and B.  The panel's B is the 128-row diagonal
-// inverse and its epilogue stores straight to global memory, so it runs four
-// 48 KB stages; the updates and X = U U^T (B of 256 rows) run two 72 KB
-// stages beside 64 KB of epilogue staging (TMA reductions, transposes).
+// inverse and its epilogue stores straight to global memory: four 48 KB
+// stages.  X = U U^T (B of 256 rows) also stores straight from registers
+// (row stores of X and of its mirror): three 72 KB stages.  The updates add
+// into the work buffer through 32 x 32 TMA reductions staged in shared memory
+// (64 KB): two 72 KB stages.  (Vector reductions straight from registers,
+// which would free room for a third stage, left the MMA issuer waiting for a
+// drained accumulator 35 % of the time instead of 4 %: the lanes' rows are
+// 128 B apart, so each reduction instruction touches 32 lines.)
+constexpr int kItOutBlock = 4096;  // one 32 x 32 fp32 block
 template <int KIND>
 struct ItCfg {
   static constexpr int b_rows = KIND == kItPanel ? 128 : 256;
-  static constexpr int stages = KIND == kItPanel ? 4 : 2;
+  static constexpr int stages = KIND == kItUpdate ? 2 : KIND == kItPanel ? 4 : 3;
   static constexpr int b_slice = b_rows * kItBK * 2;
   static constexpr int stage = kSlices * (kItA + b_slice);
-  static constexpr int out = KIND == kItPanel ? 0 : 8 * 2 * kItOutBlock;
+  static constexpr int out = KIND == kItUpdate ? 8 * 2 * kItOutBlock : 0;
   static constexpr int smem = stages * stage + out + 1024 + 256;
 };
 
@@ -489,32 +494,32 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
       } else {
         // X tile (i, j + h) of the pair and its mirror, in 32 x 32 blocks: the
         // mirror straight from the registers (lanes hold consecutive rows, so
-        // the stores run along the mirror's rows), the tile itself through a
-        // transpose in the warp's staging buffer, so that both are coalesced
+        // the stores run along the mirror's rows), the tile as row stores of
+        // this thread's 32 columns
         const InvMat mt = prm.mats[J.m];
         const int jt = J.j + h;
-        const long long row0 = (long long)J.i * 128 + q * 32;  // this warp's 32 rows
-        float* tb = reinterpret_cast<float*>(out_stage + e * 2 * kItOutBlock);  // 32 x 33 floats
+        const long long row = (long long)J.i * 128 + q * 32 + lane;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const long long col0 = (long long)jt * 128 + g * 32;
-          const long long row = row0 + lane;
 #pragma unroll
           for (int t = 0; t < 32; ++t) {
             const long long col = col0 + t;
             if (row < mt.d && col < mt.d && (J.i != jt || mrow <= g * 32 + t))
               mt.X[col * mt.ld_out + row] = run[g * 32 + t];
           }
-          __syncwarp();
+          if (row < mt.d) {
+            float* xr = mt.X + row * mt.ld_out + col0;
+            if (col0 + 32 <= mt.d && (J.i != jt || mrow <= g * 32)) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) tb[lane * 33 + t] = run[g * 32 + t];
-          __syncwarp();
-          const long long col = col0 + lane;
-#pragma unroll 8
-          for (int rr = 0; rr < 32; ++rr) {
-            const long long r = row0 + rr;
-            if (r < mt.d && col < mt.d && (J.i != jt || q * 32 + rr <= g * 32 + lane))
-              mt.X[r * mt.ld_out + col] = tb[rr * 33 + lane];
+              for (int t = 0; t < 32; t += 4)
+                *reinterpret_cast<float4*>(xr + t) =
+                    make_float4(run[g * 32 + t], run[g * 32 + t + 1], run[g * 32 + t + 2], run[g * 32 + t + 3]);
+            } else {
+#pragma unroll
+              for (int t = 0; t < 32; ++t)
+                if (col0 + t < mt.d && (J.i != jt || mrow <= g * 32 + t)) xr[t] = run[g * 32 + t];
+            }
           }
         }
       }
