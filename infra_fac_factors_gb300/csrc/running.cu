@@ -7,8 +7,9 @@
 //   damped  = running + gamma * I
 //
 // HBM-bound: per element P (+1) fp32 reads and 2 fp32 writes.  One warp streams
-// one row segment [128*floor(r/128), d) with 16-byte loads; all P shard loads
-// of an iteration are issued before they are summed.
+// one row segment [128*floor(r/128), d) with 16-byte loads, two per lane per
+// iteration (columns c and c + 128); the loads of up to eight shards of both
+// are issued before they are summed.
 #include "common.cuh"
 #include "launch.h"
 
@@ -30,68 +31,78 @@ struct RunParams {
   float decay, gamma, inv_p;
 };
 
-template <int PC>
-__device__ __forceinline__ float4 sum_shards(const float* base, long long stride, int P) {
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  // PC shards per batch of independent loads
-  for (int p0 = 0; p0 < P; p0 += PC) {
-    float4 v[PC];
-#pragma unroll
-    for (int q = 0; q < PC; ++q)
-      if (p0 + q < P) v[q] = __ldcs(reinterpret_cast<const float4*>(base + (long long)(p0 + q) * stride));
-#pragma unroll
-    for (int q = 0; q < PC; ++q)
-      if (p0 + q < P) {
-        acc.x += v[q].x;
-        acc.y += v[q].y;
-        acc.z += v[q].z;
-        acc.w += v[q].w;
-      }
-  }
-  return acc;
-}
-
 __global__ void __launch_bounds__(256) update_running_kernel(const __grid_constant__ RunParams prm) {
   const int lane = threadIdx.x % 32;
   const long long warp_global = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) / 32;
   const float decay = prm.decay, keep = 1.f - prm.decay;
+  int pi = 0;  // rows are visited in increasing order: the problem only advances
   for (long long g = warp_global; g < prm.total_rows; g += nwarps) {
-    int pi = 0;
     while (pi + 1 < prm.n_probs && prm.probs[pi + 1].row_begin <= g) ++pi;
     const RunProb& pr = prm.probs[pi];
     const long long r = g - pr.row_begin;
     const long long c_begin = (r / 128) * 128;
     const long long off_row = r * pr.ld;
-    // vector part
+    // vector part: two 16-byte groups per lane per iteration (c and c + 128)
     const long long c_vec_end = c_begin + ((pr.d - c_begin) / 4) * 4;
-    for (long long c = c_begin + lane * 4; c < c_vec_end; c += 128) {
-      const long long off = off_row + c;
-      float4 f = sum_shards<8>(pr.shards + off, pr.stride, prm.P);
-      f.x *= prm.inv_p;
-      f.y *= prm.inv_p;
-      f.z *= prm.inv_p;
-      f.w *= prm.inv_p;
-      float4 rn;
-      if (prm.first_step) {
-        rn = f;
-      } else {
-        const float4 old = *reinterpret_cast<const float4*>(pr.running + off);
-        rn.x = fmaf(decay, old.x, keep * f.x);
-        rn.y = fmaf(decay, old.y, keep * f.y);
-        rn.z = fmaf(decay, old.z, keep * f.z);
-        rn.w = fmaf(decay, old.w, keep * f.w);
+    for (long long cb = c_begin + lane * 4; cb < c_vec_end; cb += 256) {
+      float4 f2[2];
+      const bool two = cb + 128 < c_vec_end;
+      {
+        float4 v[16];
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+          if (p < prm.P) {
+            v[p] = __ldcs(reinterpret_cast<const float4*>(pr.shards + off_row + cb + (long long)p * pr.stride));
+            if (two) v[8 + p] = __ldcs(reinterpret_cast<const float4*>(pr.shards + off_row + cb + 128 + (long long)p * pr.stride));
+          }
+        for (int h = 0; h < 2; ++h) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int p = 0; p < 8; ++p)
+            if (p < prm.P) {
+              acc.x += v[8 * h + p].x; acc.y += v[8 * h + p].y; acc.z += v[8 * h + p].z; acc.w += v[8 * h + p].w;
+            }
+          f2[h] = acc;
+        }
+        for (int p0 = 8; p0 < prm.P; ++p0) {  // P > 8: the rest one by one
+          const float4 a = __ldcs(reinterpret_cast<const float4*>(pr.shards + off_row + cb + (long long)p0 * pr.stride));
+          f2[0].x += a.x; f2[0].y += a.y; f2[0].z += a.z; f2[0].w += a.w;
+          if (two) {
+            const float4 b = __ldcs(reinterpret_cast<const float4*>(pr.shards + off_row + cb + 128 + (long long)p0 * pr.stride));
+            f2[1].x += b.x; f2[1].y += b.y; f2[1].z += b.z; f2[1].w += b.w;
+          }
+        }
       }
-      float4 dm = rn;
-      if (r >= c && r < c + 4) {
-        const int k = (int)(r - c);
-        if (k == 0) dm.x += prm.gamma;
-        if (k == 1) dm.y += prm.gamma;
-        if (k == 2) dm.z += prm.gamma;
-        if (k == 3) dm.w += prm.gamma;
+      for (int h = 0; h < (two ? 2 : 1); ++h) {
+        const long long c = cb + 128 * h;
+        const long long off = off_row + c;
+        float4 f = f2[h];
+        f.x *= prm.inv_p;
+        f.y *= prm.inv_p;
+        f.z *= prm.inv_p;
+        f.w *= prm.inv_p;
+        float4 rn;
+        if (prm.first_step) {
+          rn = f;
+        } else {
+          const float4 old = *reinterpret_cast<const float4*>(pr.running + off);
+          rn.x = fmaf(decay, old.x, keep * f.x);
+          rn.y = fmaf(decay, old.y, keep * f.y);
+          rn.z = fmaf(decay, old.z, keep * f.z);
+          rn.w = fmaf(decay, old.w, keep * f.w);
+        }
+        float4 dm = rn;
+        if (r >= c && r < c + 4) {
+          const int k = (int)(r - c);
+          if (k == 0) dm.x += prm.gamma;
+          if (k == 1) dm.y += prm.gamma;
+          if (k == 2) dm.z += prm.gamma;
+          if (k == 3) dm.w += prm.gamma;
+        }
+        *reinterpret_cast<float4*>(pr.running + off) = rn;
+        __stcs(reinterpret_cast<float4*>(pr.damped + off), dm);
       }
-      *reinterpret_cast<float4*>(pr.running + off) = rn;
-      __stcs(reinterpret_cast<float4*>(pr.damped + off), dm);
     }
     // scalar tail (d not a multiple of 4)
     const long long c = c_vec_end + lane;
