@@ -361,8 +361,8 @@ struct SmParams {
 template <typename Tin>
 __global__ void __launch_bounds__(256) syrk_simt_kernel(const __grid_constant__ SmParams prm) {
   __shared__ __align__(16) float smem[simt_smem_bytes<float>() / sizeof(float)];
+  int pi = 0;  // tiles are visited in increasing order: the problem only advances
   for (long long u = blockIdx.x; u < prm.total_tiles; u += gridDim.x) {
-    int pi = 0;
     while (pi + 1 < prm.n_probs && prm.probs[pi + 1].tile_begin <= u) ++pi;
     const SmProb& pr = prm.probs[pi];
     const long long local = u - pr.tile_begin;
