@@ -18,7 +18,7 @@ we have; the surviving prose fixes the following, and each function cites it:
       decomposition; the inverse of a symmetric factor is symmetric, so only
       its upper triangle (d(d+1)/2 elements) needs to travel.
 
-Readings where the pages are silent (also listed in the design doc):
+Readings where the pages are silent:
   * factor normalisation is the mean over the rows a worker holds
     (A^p = a_p^T a_p / rows_p); conv layers use per-sample spatially summed
     output gradients for G (G^p = gs_p^T gs_p / samples_p);
