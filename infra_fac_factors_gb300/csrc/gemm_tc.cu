@@ -374,7 +374,9 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
 constexpr int kSplitSeg = 256;   // columns of one warp unit (32 lanes x 8)
 constexpr int kSplitChunk = 64;  // warp units per block iteration (8 warps x 8)
 
-// p[k] = sum_e z_k[c0 + e] x[e] for the eight probes of probe_sign8
+// p[k] = sum_e z_k[c0 + e] x[e] for eight Rademacher probes z_k: z_k[c] is
+// H8[k][c % 8] times the sign in bit (c % 8) + shift of probe_hash(c / 8),
+// H8 the 8 x 8 Sylvester-Hadamard matrix
 __device__ __forceinline__ void probe8(const float (&x)[8], long long c0, int shift, float (&p)[8]) {
   const uint32_t h = probe_hash((uint32_t)(c0 >> 3)) >> shift;
 #pragma unroll

@@ -33,7 +33,8 @@ struct GtProb {
 
 // fp32 src [rows][ld_src] -> bf16 dst slices: slice k at dst + k * slice_stride.
 // When `probe` is set, the same pass adds src * z into probe[rows][kProbeN]
-// (z: the Rademacher probes of kfac::probe_sign, bit offset probe_shift).
+// (z: the Rademacher probes of probe8 in gemm_tc.cu, bit offset probe_shift:
+// 0 for the right probes, 8 for the left ones).
 struct SplitItem {
   const float* src;
   uint16_t* dst;
