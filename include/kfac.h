@@ -76,6 +76,30 @@ unsigned long long kfac_launch_count(void);
  * Synchronises `stream`. */
 int kfac_device_status(int* status_out, int clear, void* stream);
 
+/* Per-launch timing of the library's main kernels (no counterpart on the
+ * pages; a measurement aid).  kfac_profile(1) clears the record and starts
+ * recording: every later launch of the kernels below gets a CUDA event on
+ * its stream just before and just after it, and its work is noted;
+ * kfac_profile(0) stops recording.  kfac_profile_read synchronises on the
+ * recorded events and returns, for one kind, the number of launches, the sum
+ * of their durations (ms; launches on concurrent streams overlap other work)
+ * and the sum of their work:
+ *   KFAC_K_SYRK        factor SYRK (tensor cores)      work: algorithmic flops, 2 rows d(d+1)/2 per shard
+ *   KFAC_K_RUNNING     running average + damping       work: algorithmic bytes, (P+3) 4 d(d+1)/2 per factor
+ *   KFAC_K_INV_PANEL   inverse panel products          work: flops of the tile products (2 per multiply-add)
+ *   KFAC_K_INV_UPDATE  inverse trailing updates        work: as above
+ *   KFAC_K_INV_LAUUM   inverse X = U U^T               work: as above
+ *   KFAC_K_GEMM16      preconditioning GEMMs, 16-bit   work: 2 M N K per problem
+ *   KFAC_K_GEMM24      preconditioning GEMMs, 24-bit   work: 2 M N K per problem run
+ * Recording holds at most 65536 launches (later ones are not recorded).
+ * Invalid kind: KFAC_ERR_INVALID_ARG.                                        */
+typedef enum {
+  KFAC_K_SYRK = 0, KFAC_K_RUNNING = 1, KFAC_K_INV_PANEL = 2, KFAC_K_INV_UPDATE = 3,
+  KFAC_K_INV_LAUUM = 4, KFAC_K_GEMM16 = 5, KFAC_K_GEMM24 = 6, KFAC_K_COUNT = 7
+} kfac_kernel_kind;
+int kfac_profile(int enable);
+int kfac_profile_read(int kind, int64_t* launches, double* ms, double* work);
+
 /* Failure-detection self-test (no counterpart on the pages; a property of the
  * library): launches one CTA that waits, with the same bounded wait every
  * tcgen05 kernel of the library uses, on an mbarrier that nothing arrives on.

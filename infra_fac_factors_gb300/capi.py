@@ -15,8 +15,9 @@ __all__ = [
     "KFAC_BF16", "KFAC_FP32", "KFAC_REFINE_NONE", "KFAC_REFINE_AUTO", "KFAC_REFINE_ALWAYS",
     "KFAC_PRECOND_FP32", "KFAC_PRECOND_AUTO",
     "kfac_factor_args", "kfac_running_args", "kfac_inverse_args", "kfac_precond_args",
-    "KFACError", "lib", "library_path", "exported_symbols",
+    "KFACError", "lib", "library_path", "exported_symbols", "KERNEL_KINDS",
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
+    "kfac_profile", "kfac_profile_read",
     "kfac_factors", "kfac_spatial_sum", "kfac_update_running",
     "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
@@ -28,6 +29,7 @@ KFAC_ERR_UNSUPPORTED, KFAC_ERR_TIMEOUT, KFAC_ERR_WORKSPACE = 4, 5, 6
 KFAC_BF16, KFAC_FP32 = 0, 1
 KFAC_REFINE_NONE, KFAC_REFINE_AUTO, KFAC_REFINE_ALWAYS = 0, 1, 2
 KFAC_PRECOND_FP32, KFAC_PRECOND_AUTO = 0, 1
+KERNEL_KINDS = ("syrk", "running", "inv_panel", "inv_update", "inv_lauum", "gemm16", "gemm24")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libkfac_gb300.so")
@@ -57,7 +59,7 @@ class kfac_precond_args(C.Structure):
 
 exported_symbols = (
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
-    "kfac_factors", "kfac_spatial_sum",
+    "kfac_profile", "kfac_profile_read", "kfac_factors", "kfac_spatial_sum",
     "kfac_update_running", "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
     "kfac_precondition_static", "kfac_factor_tile_map",
@@ -83,6 +85,8 @@ def lib() -> C.CDLL:
         "kfac_launch_count": (C.c_ulonglong, []),
         "kfac_device_status": (C.c_int, [P(C.c_int), C.c_int, C.c_void_p]),
         "kfac_wait_selftest": (C.c_int, [C.c_int64, C.c_void_p]),
+        "kfac_profile": (C.c_int, [C.c_int]),
+        "kfac_profile_read": (C.c_int, [C.c_int, P(C.c_int64), P(C.c_double), P(C.c_double)]),
         "kfac_factors": (C.c_int, [C.c_int, P(kfac_factor_args), C.c_int, C.c_int, C.c_int, C.c_void_p]),
         "kfac_spatial_sum": (C.c_int, [C.c_void_p, C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
                                        C.c_void_p, C.c_int64, C.c_void_p]),
@@ -147,6 +151,20 @@ def kfac_wait_selftest(limit_cycles: int, stream: int = 0, check: bool = True) -
     """One CTA's bounded wait on an mbarrier nothing arrives on (records KFAC_ERR_TIMEOUT)."""
     st = lib().kfac_wait_selftest(int(limit_cycles), stream)
     return _check("kfac_wait_selftest", st) if check else st
+
+
+def kfac_profile(enable: bool) -> None:
+    """Start (clearing the record) or stop the per-launch timing of the main kernels."""
+    _check("kfac_profile", lib().kfac_profile(int(bool(enable))))
+
+
+def kfac_profile_read(kind) -> dict:
+    """Launches, summed duration (ms) and summed work of one kernel kind (a name of
+    KERNEL_KINDS or its index); synchronises on the recorded events."""
+    k = KERNEL_KINDS.index(kind) if isinstance(kind, str) else int(kind)
+    n, ms, w = C.c_int64(0), C.c_double(0.0), C.c_double(0.0)
+    _check("kfac_profile_read", lib().kfac_profile_read(k, C.byref(n), C.byref(ms), C.byref(w)))
+    return {"launches": int(n.value), "ms": float(ms.value), "work": float(w.value)}
 
 
 def kfac_factors(args, dtype: int, P: int, mirror: int = 0, stream: int = 0, check: bool = True) -> int:

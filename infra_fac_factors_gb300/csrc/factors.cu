@@ -485,6 +485,11 @@ int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mi
       prm.P = P;
       prm.mirror = mirror;
       prm.total_units = units;
+      double work = 0.0;  // algorithmic flops of the launch
+      for (int k = 0; k < cnt; ++k) {
+        const double d = (double)args[base + k].d;
+        work += 2.0 * (double)args[base + k].rows * d * (d + 1.0) / 2.0;
+      }
       prm.status = device_status_ptr();
       if (!prm.status) return KFAC_ERR_CUDA;
       if (units == 0) continue;
@@ -502,7 +507,10 @@ int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mi
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
+      ProfMark pm;
+      prof_begin(stream, pm);
       if (cudaLaunchKernelEx(&cfg, syrk_tc_kernel, prm) != cudaSuccess) return KFAC_ERR_CUDA;
+      prof_end(KFAC_K_SYRK, stream, pm, work);
       count_launch();
       if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
     }

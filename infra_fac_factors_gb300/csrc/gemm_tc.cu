@@ -525,7 +525,7 @@ int launch_gemm_tc(const GtOperand* ops_in, int n, int ns, const int* flags, cud
 }
 
 template <int NS, bool MC>
-static int launch_gemm_kernel(const GtParams& prm, int grid, cudaStream_t stream) {
+static int launch_gemm_kernel(const GtParams& prm, int grid, cudaStream_t stream, double work) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kGtThreads);
@@ -538,7 +538,10 @@ static int launch_gemm_kernel(const GtParams& prm, int grid, cudaStream_t stream
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  ProfMark pm;
+  prof_begin(stream, pm);
   if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel<NS, MC>, prm) != cudaSuccess) return KFAC_ERR_CUDA;
+  prof_end(NS == 2 ? KFAC_K_GEMM16 : KFAC_K_GEMM24, stream, pm, work);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
@@ -589,6 +592,10 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags,
       tiles += (pairs ? (tiles_m + 1) / 2 : tiles_m) * p.tiles_n;  // work items (tile pairs with `pairs`)
     }
     if (rc != KFAC_OK) break;
+    // work of the launch (2 M N K per problem); unknown when flags pick the problems
+    double work = 0.0;
+    if (flags == nullptr)
+      for (int i = 0; i < cnt; ++i) work += 2.0 * (double)ops[base + i].M * ops[base + i].N * ops[base + i].K;
     prm->n_probs = cnt;
     prm->flags = flags;
     prm->total_tiles = tiles;
@@ -597,11 +604,12 @@ int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags,
       if (pairs) {
         const long long clusters = tiles < sms / 2 ? tiles : sms / 2;
         const int grid = (int)(2 * clusters);
-        rc = ns == 3 ? launch_gemm_kernel<3, true>(*prm, grid, stream) : launch_gemm_kernel<2, true>(*prm, grid, stream);
+        rc = ns == 3 ? launch_gemm_kernel<3, true>(*prm, grid, stream, work)
+                     : launch_gemm_kernel<2, true>(*prm, grid, stream, work);
       } else {
         const int grid = (int)(tiles < sms ? tiles : sms);
-        rc = ns == 3 ? launch_gemm_kernel<3, false>(*prm, grid, stream)
-                     : launch_gemm_kernel<2, false>(*prm, grid, stream);
+        rc = ns == 3 ? launch_gemm_kernel<3, false>(*prm, grid, stream, work)
+                     : launch_gemm_kernel<2, false>(*prm, grid, stream, work);
       }
     }
   }

@@ -896,8 +896,32 @@ static bool enc_slices(EncodeTiledFn enc, CUtensorMap* map, uint16_t* base, long
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 128 x 128 x 128 tile products (units of 128^3 multiply-adds) of one
+// launch's jobs for a matrix of T block rows
+template <int KIND>
+static double tile_macs(int T, int k, int upd_mode, int t_only) {
+  double u = 0.0;
+  if (KIND == kItPanel) {
+    u = T > k ? T - 1 : 0;  // one 128 x 128 tile, K = 128, per job
+  } else if (KIND == kItUpdate) {
+    const UpdShape sh = upd_shape(T, k, upd_mode);
+    if (sh.nschur + sh.nsub == 0) return 0.0;
+    const int kunits = sh.outer ? k + 1 - sh.p0 : 1;
+    for (int r = sh.c_lo; r < T; ++r) u += (double)((r < sh.c_hi ? r : sh.c_hi) - sh.c_lo + 1) * kunits;
+    const int rl = sh.c_hi < T - 1 ? sh.c_hi : T - 1;
+    for (int c = 0; c <= k; ++c)
+      u += (double)(rl - sh.c_lo + 1) * (sh.outer ? k + 1 - (c > sh.p0 ? c : sh.p0) : 1);
+  } else if (t_only == 0 || T == t_only) {
+    for (int j = 0; j < T; ++j) {  // pair (j, j + 1): rows i = j % 2, j % 2 + 2, .., j
+      const int w = T - j < 2 ? T - j : 2;
+      u += (double)(j / 2 + 1) * w * (T - j);
+    }
+  }
+  return u;
+}
+
 // Job counts of one launch (filling prm->job_begin); *work gets the launch's
-// multiply-add volume in 128 x 128 x 128 tile units.
+// flops (2 per multiply-add of its tile products).
 template <int KIND>
 static long long count_jobs(ItParams* prm, const int* Ts, int n, int k, int upd_mode, double* work,
                             int t_only = 0) {
@@ -909,31 +933,35 @@ static long long count_jobs(ItParams* prm, const int* Ts, int n, int k, int upd_
     const int T = Ts[i];
     if (KIND == kItPanel) {
       cnt = T > k ? T - 1 : 0;
-      w += (double)cnt;
     } else if (KIND == kItUpdate) {
       const UpdShape sh = upd_shape(T, k, upd_mode);
       cnt = sh.nschur + sh.nsub;
-      w += 2.0 * (double)cnt * (sh.outer ? (k + 1 - sh.p0) : 1);
     } else {
       cnt = (t_only == 0 || T == t_only) ? it_pairs(T) : 0;
     }
+    if (work && cnt > 0) w += tile_macs<KIND>(T, k, upd_mode, t_only);
     jobs += cnt;
   }
   prm->job_begin[n] = (int)jobs;
-  if (work) *work = w;
+  if (work) *work = w * 2.0 * 128.0 * 128.0 * 128.0;
   return jobs;
 }
 
 template <int KIND>
 static int launch_it(ItParams* prm, const int* Ts, int n, int k, int grid_cap, cudaStream_t stream,
                      int upd_mode = kUpdInner, int t_only = 0) {
-  const long long jobs = count_jobs<KIND>(prm, Ts, n, k, upd_mode, nullptr, t_only);
+  double work = 0.0;
+  const long long jobs = count_jobs<KIND>(prm, Ts, n, k, upd_mode, &work, t_only);
   prm->total_jobs = jobs;
   prm->k = k;
   prm->upd_mode = upd_mode;
   if (jobs == 0) return KFAC_OK;
   const int grid = (int)(jobs < grid_cap ? jobs : grid_cap);
+  ProfMark pm;
+  prof_begin(stream, pm);
   inv_tc_kernel<KIND><<<grid, kItThreads, ItCfg<KIND>::smem, stream>>>(*prm);
+  prof_end(KIND == kItPanel ? KFAC_K_INV_PANEL : KIND == kItUpdate ? KFAC_K_INV_UPDATE : KFAC_K_INV_LAUUM, stream,
+           pm, work);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }

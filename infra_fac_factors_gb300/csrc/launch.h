@@ -15,6 +15,15 @@ int* device_status_ptr();
 void count_launch();
 bool ensure_smem_attr(int dev, const void* fn, int bytes);
 
+// Per-launch timing of the main kernels, for kfac_profile / kfac_profile_read:
+// when recording is on, prof_begin records an event on the launch's stream
+// and prof_end a second one after the launch, with the launch's work.
+struct ProfMark {
+  cudaEvent_t start = nullptr;
+};
+void prof_begin(cudaStream_t stream, ProfMark& m);
+void prof_end(int kind, cudaStream_t stream, const ProfMark& m, double work);
+
 int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirror, cudaStream_t stream);
 int launch_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw, int64_t C, int64_t ld_g, float* gs,
                        int64_t ld_gs, cudaStream_t stream);

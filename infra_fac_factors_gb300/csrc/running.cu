@@ -152,7 +152,15 @@ int launch_update_running(int n, const kfac_running_args* args, int P, float dec
     const long long want = (rows + 7) / 8;  // 8 warps per block, one row per warp
     const long long cap = (long long)sms * 8;
     const int grid = (int)(want < cap ? want : cap);
+    double work = 0.0;  // algorithmic bytes: P shard reads, running read (not on a first step) and write, damped write
+    for (int k = 0; k < cnt; ++k) {
+      const double d = (double)args[base + k].d;
+      work += (double)(P + (first_step ? 2 : 3)) * 4.0 * d * (d + 1.0) / 2.0;
+    }
+    ProfMark pm;
+    prof_begin(stream, pm);
     update_running_kernel<<<grid, 256, 0, stream>>>(prm);
+    prof_end(KFAC_K_RUNNING, stream, pm, work);
     count_launch();
     if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
   }

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_exports_every_declared_function():
     names = declared_functions()
-    assert len(names) == 15
+    assert len(names) == 17
     out = subprocess.run(["nm", "-D", "--defined-only", capi.library_path], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (kfac_[a-z_0-9]+)$", out, flags=re.M))
     for n in names:
@@ -229,3 +229,12 @@ int main() {
     # every unit of every size decoded: sum over the sizes of 2 * n0 (n0 + 1) / 2, n0 = ceil(d / 256)
     sizes = [q + 1 + (q // 1000) * 2000 for q in range(3000)] + [16384, 32768, 65536]
     assert n == sum((-(-d // 256)) * (-(-d // 256) + 1) for d in sizes) and bad == 0
+
+
+def test_profile_api_without_launches():
+    capi.kfac_profile(True)
+    for kind in capi.KERNEL_KINDS:
+        assert capi.kfac_profile_read(kind) == {"launches": 0, "ms": 0.0, "work": 0.0}
+    capi.kfac_profile(False)
+    with pytest.raises(capi.KFACError):
+        capi.kfac_profile_read(len(capi.KERNEL_KINDS))

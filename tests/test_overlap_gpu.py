@@ -55,3 +55,30 @@ def test_overlapped_step_equals_stage_sequence(key, steps, n_groups):
     for a_list, b_list in zip(seq, ovl):
         for a, b in zip(a_list, b_list):
             assert np.array_equal(a, b)
+
+
+def test_kernel_profile_counts_the_step_work():
+    # one steady-state step of one encoder layer with per-launch events on:
+    # the recorded work of the factor and running-average launches is the
+    # step's algorithmic work, and every kind of the default path appears
+    cfg = synth.config("bert_layer")
+    specs = [LayerSpec(l.d_in, l.d_out, cfg.rows(l), cfg.batch, l.hw) for l in cfg.layers]
+    st = KFACStep(specs, cfg.P, cfg.gamma, cfg.decay, cfg.in_dtype, refine=capi.KFAC_REFINE_AUTO, n_groups=2)
+    for li in range(len(specs)):
+        dd = synth.device_layer_inputs(cfg, 0, li)
+        st.set_layer_inputs(li, dd["a"], dd["g"], dd["grad"])
+    st.step(first_step=True)
+    torch.cuda.synchronize()
+    capi.kfac_profile(True)
+    st.step(first_step=False)
+    capi.kfac_profile(False)
+    torch.cuda.synchronize()
+    prof = {k: capi.kfac_profile_read(k) for k in capi.KERNEL_KINDS}
+    work = st.algorithmic_work()
+    assert abs(prof["syrk"]["work"] - work["factor_flops"]) <= 1e-9 * work["factor_flops"]
+    assert abs(prof["running"]["work"] - work["update_bytes"]) <= 1e-9 * work["update_bytes"]
+    for k in ("syrk", "running", "inv_panel", "inv_update", "inv_lauum", "gemm16", "gemm24"):
+        assert prof[k]["launches"] > 0 and prof[k]["ms"] > 0, (k, prof[k])
+    # the 16-bit GEMMs carry the layer's 2 M N K products; the 24-bit re-run picks its layers on the device
+    assert abs(prof["gemm16"]["work"] - work["precond_flops"]) <= 1e-9 * work["precond_flops"]
+    assert prof["gemm24"]["work"] == 0.0
