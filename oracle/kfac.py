@@ -189,6 +189,22 @@ def spatial_sum(g: np.ndarray, batch: int, hw: int) -> np.ndarray:
     return g.reshape(batch, hw, g.shape[1]).sum(axis=1)
 
 
+def im2col3x3(x: np.ndarray, bias: bool = True) -> np.ndarray:
+    """Patch rows of a 3 x 3, stride 1, zero-padding 1 convolution over an NHWC
+    activation x[b, h, w, c] (the conv layer's input a of the Kronecker factor
+    A; reading: the pages do not describe conv factors).  Row (b, h, w), in
+    that order; column (dh * 3 + dw) * C + c holds x[b, h + dh - 1, w + dw - 1, c]
+    (0 outside the image); with `bias` a last column of ones."""
+    x = np.asarray(x, np.float64)
+    B, H, W, C = x.shape
+    xp = np.zeros((B, H + 2, W + 2, C))
+    xp[:, 1:H + 1, 1:W + 1, :] = x
+    cols = [xp[:, dh:dh + H, dw:dw + W, :].reshape(B * H * W, C) for dh in range(3) for dw in range(3)]
+    if bias:
+        cols.append(np.ones((B * H * W, 1)))
+    return np.concatenate(cols, axis=1)
+
+
 # ---------------------------------------------------------------- index maps
 def upper_tiles(d: int, tile: int = 128):
     """Upper-triangle tiles (i, j), i <= j, of a d x d symmetric matrix cut into

@@ -287,6 +287,44 @@ def test_factor_tile_units_cover_upper_tiles_once(d):
     assert units[0::2] == sorted(units[0::2])
 
 
+def test_im2col3x3_by_loops_and_as_convolution():
+    rng = np.random.default_rng(31)
+    B, H, W, C, Co = 2, 4, 5, 3, 2
+    x = rng.standard_normal((B, H, W, C))
+    P = oracle.im2col3x3(x)
+    assert P.shape == (B * H * W, 9 * C + 1)
+    # entry by entry against nested loops over the padded image
+    for b in range(B):
+        for h in range(H):
+            for w in range(W):
+                r = (b * H + h) * W + w
+                for dh in range(3):
+                    for dw in range(3):
+                        for c in range(C):
+                            hh, ww = h + dh - 1, w + dw - 1
+                            v = x[b, hh, ww, c] if 0 <= hh < H and 0 <= ww < W else 0.0
+                            assert P[r, (dh * 3 + dw) * C + c] == v
+                assert P[r, -1] == 1.0
+    # patches times the flattened kernel is the convolution (cross-correlation)
+    K = rng.standard_normal((Co, 3, 3, C))
+    bias = rng.standard_normal(Co)
+    out = P @ np.concatenate([K.reshape(Co, 9 * C), bias[:, None]], axis=1).T
+    for b in range(B):
+        for h in range(H):
+            for w in range(W):
+                for o in range(Co):
+                    acc = bias[o]
+                    for dh in range(3):
+                        for dw in range(3):
+                            hh, ww = h + dh - 1, w + dw - 1
+                            if 0 <= hh < H and 0 <= ww < W:
+                                acc += K[o, dh, dw] @ x[b, hh, ww]
+                    assert abs(out[(b * H + h) * W + w, o] - acc) <= 1e-12
+    # an interior position sees all nine taps, a corner four
+    assert np.count_nonzero(P[(0 * H + 1) * W + 1, :-1]) == 9 * C
+    assert np.count_nonzero(P[0, :-1]) == 4 * C
+
+
 @pytest.mark.parametrize("d", [1, 5, 128, 300])
 def test_upper_tiles_count(d):
     T = -(-d // 128)
