@@ -91,11 +91,13 @@ int kfac_device_status(int* status_out, int clear, void* stream);
  *   KFAC_K_INV_LAUUM   inverse X = U U^T               work: as above
  *   KFAC_K_GEMM16      preconditioning GEMMs, 16-bit   work: 2 M N K per problem
  *   KFAC_K_GEMM24      preconditioning GEMMs, 24-bit   work: 2 M N K per problem run
+ *   KFAC_K_CONV_SYRK   conv factor SYRK (implicit im2col) work: as KFAC_K_SYRK, rows = patch rows
  * Recording holds at most 65536 launches (later ones are not recorded).
  * Invalid kind: KFAC_ERR_INVALID_ARG.                                        */
 typedef enum {
   KFAC_K_SYRK = 0, KFAC_K_RUNNING = 1, KFAC_K_INV_PANEL = 2, KFAC_K_INV_UPDATE = 3,
-  KFAC_K_INV_LAUUM = 4, KFAC_K_GEMM16 = 5, KFAC_K_GEMM24 = 6, KFAC_K_COUNT = 7
+  KFAC_K_INV_LAUUM = 4, KFAC_K_GEMM16 = 5, KFAC_K_GEMM24 = 6, KFAC_K_CONV_SYRK = 7,
+  KFAC_K_COUNT = 8
 } kfac_kernel_kind;
 int kfac_profile(int enable);
 int kfac_profile_read(int kind, int64_t* launches, double* ms, double* work);
@@ -148,6 +150,36 @@ int kfac_factors(int n, const kfac_factor_args* args, int dtype, int P,
 int kfac_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw,
                      int64_t C, int64_t ld_g, float* gs, int64_t ld_gs,
                      void* stream);
+
+/* Conv factor A straight from the activations (implicit im2col; the pages do
+ * not describe conv factors: the reading taken is the Kronecker factor of a
+ * 3 x 3 convolution, stride 1, zero padding 1, with bias, whose per-position
+ * input is its 3 x 3 x C patch, §II-B Eq. (7)).  For each problem the patch
+ * matrix X has one row per output position (b, h, w), in that order, and
+ * d = 9 C + 1 columns:
+ *     X[(b,h,w), (dh*3 + dw)*C + c] = x[b, h+dh-1, w+dw-1, c]  (0 outside),
+ *     X[(b,h,w), 9C] = 1.
+ * Worker p owns images [p*B/P, (p+1)*B/P), i.e. patch rows
+ * [p*rows_p, (p+1)*rows_p) with rows_p = (B/P) H W, and
+ *     out[p] = scale * X_p^T X_p          (d x d, fp32)
+ * exactly as kfac_factors would give on the materialised X (bf16 products,
+ * fp32 accumulation, the same upper tiles written, `mirror` as there); X is
+ * never formed in memory.
+ * x: device, bf16, NHWC [B][H][W][C] contiguous, 16-byte aligned, C % 64 == 0,
+ *    64 <= C <= 7232 (d <= 65089); B % P == 0; B H W <= 2^31 - 1.
+ * out: as kfac_factors (ld_out % 4 == 0, ld_out >= d, stride_out >= d ld_out
+ *    and % 4 == 0 when P > 1).  n <= 4096.  Errors: KFAC_ERR_INVALID_ARG.   */
+typedef struct {
+  const void* x;       /* device, bf16 NHWC activations of all P workers  */
+  int64_t B, H, W, C;  /* images, height, width, channels                 */
+  float* out;          /* device, P fp32 matrices d x d, d = 9 C + 1      */
+  int64_t ld_out;      /* leading dimension of out (elements)             */
+  int64_t stride_out;  /* elements between out[p] and out[p+1]            */
+  float scale;         /* multiplies X_p^T X_p                            */
+} kfac_conv_factor_args;
+
+int kfac_conv_factors(int n, const kfac_conv_factor_args* args, int P,
+                      int mirror, void* stream);
 
 /* --------------------------------------- 2. reduce + running average + damp (a3)
  * One fused pass over the upper tiles of each factor (§II-C aggregation,

@@ -18,7 +18,7 @@ __all__ = [
     "KFACError", "lib", "library_path", "exported_symbols", "KERNEL_KINDS",
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
     "kfac_profile", "kfac_profile_read",
-    "kfac_factors", "kfac_spatial_sum", "kfac_update_running",
+    "kfac_factors", "kfac_conv_factor_args", "kfac_conv_factors", "kfac_spatial_sum", "kfac_update_running",
     "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
     "kfac_precondition_static", "kfac_factor_tile_map",
@@ -29,7 +29,7 @@ KFAC_ERR_UNSUPPORTED, KFAC_ERR_TIMEOUT, KFAC_ERR_WORKSPACE = 4, 5, 6
 KFAC_BF16, KFAC_FP32 = 0, 1
 KFAC_REFINE_NONE, KFAC_REFINE_AUTO, KFAC_REFINE_ALWAYS = 0, 1, 2
 KFAC_PRECOND_FP32, KFAC_PRECOND_AUTO = 0, 1
-KERNEL_KINDS = ("syrk", "running", "inv_panel", "inv_update", "inv_lauum", "gemm16", "gemm24")
+KERNEL_KINDS = ("syrk", "running", "inv_panel", "inv_update", "inv_lauum", "gemm16", "gemm24", "conv_syrk")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libkfac_gb300.so")
@@ -37,6 +37,11 @@ library_path = os.path.join(_HERE, "libkfac_gb300.so")
 
 class kfac_factor_args(C.Structure):
     _fields_ = [("x", C.c_void_p), ("rows", C.c_int64), ("d", C.c_int64), ("ld_x", C.c_int64),
+                ("out", C.c_void_p), ("ld_out", C.c_int64), ("stride_out", C.c_int64), ("scale", C.c_float)]
+
+
+class kfac_conv_factor_args(C.Structure):
+    _fields_ = [("x", C.c_void_p), ("B", C.c_int64), ("H", C.c_int64), ("W", C.c_int64), ("C", C.c_int64),
                 ("out", C.c_void_p), ("ld_out", C.c_int64), ("stride_out", C.c_int64), ("scale", C.c_float)]
 
 
@@ -59,7 +64,7 @@ class kfac_precond_args(C.Structure):
 
 exported_symbols = (
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
-    "kfac_profile", "kfac_profile_read", "kfac_factors", "kfac_spatial_sum",
+    "kfac_profile", "kfac_profile_read", "kfac_factors", "kfac_conv_factors", "kfac_spatial_sum",
     "kfac_update_running", "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
     "kfac_precondition_static", "kfac_factor_tile_map",
@@ -88,6 +93,7 @@ def lib() -> C.CDLL:
         "kfac_profile": (C.c_int, [C.c_int]),
         "kfac_profile_read": (C.c_int, [C.c_int, P(C.c_int64), P(C.c_double), P(C.c_double)]),
         "kfac_factors": (C.c_int, [C.c_int, P(kfac_factor_args), C.c_int, C.c_int, C.c_int, C.c_void_p]),
+        "kfac_conv_factors": (C.c_int, [C.c_int, P(kfac_conv_factor_args), C.c_int, C.c_int, C.c_void_p]),
         "kfac_spatial_sum": (C.c_int, [C.c_void_p, C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
                                        C.c_void_p, C.c_int64, C.c_void_p]),
         "kfac_update_running": (C.c_int, [C.c_int, P(kfac_running_args), C.c_int, C.c_float, C.c_float,
@@ -171,6 +177,13 @@ def kfac_factors(args, dtype: int, P: int, mirror: int = 0, stream: int = 0, che
     n, a = _arr(kfac_factor_args, args)
     st = lib().kfac_factors(n, a, dtype, P, mirror, stream)
     return _check("kfac_factors", st) if check else st
+
+
+def kfac_conv_factors(args, P: int, mirror: int = 0, stream: int = 0, check: bool = True) -> int:
+    """Conv factors straight from NHWC bf16 activations (implicit im2col)."""
+    n, a = _arr(kfac_conv_factor_args, args)
+    st = lib().kfac_conv_factors(n, a, P, mirror, stream)
+    return _check("kfac_conv_factors", st) if check else st
 
 
 def kfac_spatial_sum(g: int, dtype: int, batch: int, hw: int, C_: int, ld_g: int, gs: int, ld_gs: int,

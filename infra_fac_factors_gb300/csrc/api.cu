@@ -50,6 +50,20 @@ bool ensure_smem_attr(int dev, const void* fn, int bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
 }
 
+EncodeTiledFn tensor_map_encoder() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
 // The kernels are built for sm_103a only.
 static int check_device() {
   int dev = 0;
@@ -162,6 +176,26 @@ int kfac_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirr
   const int dc = check_device();
   if (dc != KFAC_OK) return dc;
   return launch_factors(n, args, dtype, P, mirror, static_cast<cudaStream_t>(stream));
+}
+
+int kfac_conv_factors(int n, const kfac_conv_factor_args* args, int P, int mirror, void* stream) {
+  if (n < 0 || n > 4096 || (n > 0 && !args)) return KFAC_ERR_INVALID_ARG;
+  if (P < 1 || P > 65535) return KFAC_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const kfac_conv_factor_args& a = args[i];
+    if (!a.x || !a.out || !aligned16(a.x) || !aligned16(a.out)) return KFAC_ERR_INVALID_ARG;
+    if (a.C < 64 || a.C > 7232 || a.C % 64 != 0) return KFAC_ERR_INVALID_ARG;
+    if (a.B < P || a.B % P != 0 || a.H < 1 || a.W < 1) return KFAC_ERR_INVALID_ARG;
+    if (a.H > 0x7fffffff / a.W || a.B > 0x7fffffff / (a.H * a.W)) return KFAC_ERR_INVALID_ARG;
+    const int64_t d = 9 * a.C + 1;
+    if (a.ld_out < d || a.ld_out % 4 != 0) return KFAC_ERR_INVALID_ARG;
+    if (P > 1 && (a.stride_out < d * a.ld_out || a.stride_out % 4 != 0)) return KFAC_ERR_INVALID_ARG;
+    if (!finite(a.scale)) return KFAC_ERR_INVALID_ARG;
+  }
+  if (n == 0) return KFAC_OK;
+  const int dc = check_device();
+  if (dc != KFAC_OK) return dc;
+  return launch_conv_factors(n, args, P, mirror, static_cast<cudaStream_t>(stream));
 }
 
 int kfac_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw, int64_t C, int64_t ld_g, float* gs,

@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "factor_epilogue.cuh"
 #include "launch.h"
 #include "simt.cuh"
 #include "tilemap.cuh"
@@ -51,8 +52,7 @@ constexpr int kSyStageBytes = kSyABytes + kSyBBytes;
 constexpr int kSyMaxProbs = 96;
 // Epilogue staging: per epilogue warp two 32 x 32 fp32 blocks (4 KB each,
 // 128-byte swizzled), written to global memory by TMA stores.
-constexpr int kSyStageOut = 4096;
-constexpr int kSyOutBytes = 4 * 2 * kSyStageOut;
+constexpr int kSyOutBytes = 4 * 2 * kFeStageOut;
 constexpr int kSySmem = kSyStages * kSyStageBytes + kSyOutBytes + 1024 + 256;
 // The TMEM accumulator is restarted every kSyChunkKB stages (1024 rows) and the
 // partial products are summed in fp32 by the epilogue: long worker shards
@@ -223,108 +223,18 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
     for (long long v = pair0; v < npairs && ok; v += pair_step) {
       const SyUnit un = sy_decode(prm, 2 * v + rank, cur);
       const SyProb& pr = prm.probs[un.prob];
-      const int nb = (un.w + 63) / 64;
       const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
       const int nchunks = (nk + kSyChunkKB - 1) / kSyChunkKB;
-      const int r = un.i * 128 + q * 32 + lane;
-      float* outp = pr.out + (long long)un.p * pr.stride_out;
-      float* orow = outp + (long long)r * pr.ld_out;
-      const long long jend = un.j0 + un.w;
-      const long long lower_from = (long long)(un.i + 1) * 128;  // columns in lower-tile territory
-      const long long store_from = (long long)un.i * 128;          // columns before it: not this unit's
+      const FeUnit fu{pr.out + (long long)un.p * pr.stride_out, &prm.omaps[un.prob], pr.ld_out, un.j0, pr.d,
+                      un.i, un.w, un.p, pr.scale};
       for (int ch = 0; ch < nchunks; ++ch) {
         if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const bool first = ch == 0, last = ch == nchunks - 1;
-        if (!prm.mirror) {
-          // Stage each 32 x 32 block in shared memory (128-byte swizzle: chunk j
-          // of row t lands at chunk j ^ (t & 7), conflict-free) and write it with
-          // a TMA store; later K-chunks of the same unit add with a TMA reduce.
-          if (!first && lane == 0) bulk_wait<0>();  // earlier writes of this unit are done
-          __syncwarp();
-          const int r0 = un.i * 128 + q * 32;
-          // TMA writes whole 16-byte groups at the inner edge: a chunk reaching
-          // past the last full group (d rounded down to 4) is stored directly.
-          const long long d4 = (long long)(pr.d / 4) * 4;
-          for (int c = 0; c < nb * 2; ++c) {
-            uint32_t v[32];
-            tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
-            tc_wait_ld();
-            const long long col0 = un.j0 + c * 32;
-            if (col0 >= jend || col0 < store_from || r0 >= pr.d) continue;  // uniform over the warp
-            if (col0 + 32 > d4 && d4 != pr.d) {
-              if (r < pr.d)
-                for (int t = 0; t < 32; ++t) {
-                  const long long col = col0 + t;
-                  if (col >= jend) break;
-                  float o = __uint_as_float(v[t]) * pr.scale;
-                  if (!first) o += orow[col];
-                  orow[col] = o;
-                }
-              continue;
-            }
-            uint8_t* buf = out_stage + (q * 2 + obuf) * kSyStageOut;
-            if (lane == 0) bulk_wait_read<1>();  // the store that last used `buf` has read it
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float4 o = make_float4(__uint_as_float(v[4 * j]) * pr.scale, __uint_as_float(v[4 * j + 1]) * pr.scale,
-                                     __uint_as_float(v[4 * j + 2]) * pr.scale,
-                                     __uint_as_float(v[4 * j + 3]) * pr.scale);
-              *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              if (first)
-                tma_store_3d(&prm.omaps[un.prob], buf, (int)col0, r0, un.p);
-              else
-                tma_reduce_add_3d(&prm.omaps[un.prob], buf, (int)col0, r0, un.p);
-              bulk_commit();
-            }
-            obuf ^= 1;
-          }
-        } else
-        for (int c = 0; c < nb * 2; ++c) {
-          uint32_t v[32];
-          tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + c * 32, v);
-          tc_wait_ld();
-          const long long col0 = un.j0 + c * 32;
-          if (r < pr.d && col0 < jend && col0 >= store_from) {
-            float o[32];
-#pragma unroll
-            for (int t = 0; t < 32; ++t) o[t] = __uint_as_float(v[t]) * pr.scale;
-            if (col0 + 32 <= jend) {
-#pragma unroll
-              for (int t = 0; t < 32; t += 4) {
-                float4* dst = reinterpret_cast<float4*>(orow + col0 + t);
-                if (!first) {
-                  const float4 prev = *dst;
-                  o[t] += prev.x;
-                  o[t + 1] += prev.y;
-                  o[t + 2] += prev.z;
-                  o[t + 3] += prev.w;
-                }
-                *dst = make_float4(o[t], o[t + 1], o[t + 2], o[t + 3]);
-              }
-            } else {
-              for (int t = 0; t < 32; ++t)
-                if (col0 + t < jend) {
-                  if (!first) o[t] += orow[col0 + t];
-                  orow[col0 + t] = o[t];
-                }
-            }
-            if (prm.mirror && last) {
-              for (int t = 0; t < 32; ++t) {
-                const long long col = col0 + t;
-                if (col < jend && col >= lower_from) outp[col * pr.ld_out + r] = o[t];
-              }
-            }
-          }
-        }
+        factor_epilogue_chunk(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256, q, lane, fu, ch == 0,
+                              ch == nchunks - 1, prm.mirror != 0, out_stage + q * 2 * kFeStageOut, obuf);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -420,26 +330,9 @@ __global__ void __launch_bounds__(256) spatial_sum_kernel(const Tin* __restrict_
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirror, cudaStream_t stream) {
   if (dtype == KFAC_BF16) {
-    EncodeTiledFn enc = encode_fn();
+    EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return KFAC_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;

@@ -452,23 +452,6 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn gt_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 // Slices of one operand: [3][rows][ld] bf16, K = inner extent.
 static bool encode_slices(EncodeTiledFn enc, CUtensorMap* map, const uint16_t* base, long long rows, long long K,
                           long long ld, int box_rows) {
@@ -548,7 +531,7 @@ static int launch_gemm_kernel(const GtParams& prm, int grid, cudaStream_t stream
 
 int launch_gemm_tc_sorted(const GtOperand* ops, int n, int ns, const int* flags, cudaStream_t stream, bool pairs) {
   if (ns != 2 && ns != 3) return KFAC_ERR_INVALID_ARG;
-  EncodeTiledFn enc = gt_encode_fn();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return KFAC_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;

@@ -867,23 +867,6 @@ TcLayout tc_layout(int n, const int* T) {
   return L;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn it_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
 // slices [3][rows][cols] bf16, K-major boxes {32, box_rows}
 static bool enc_slices(EncodeTiledFn enc, CUtensorMap* map, uint16_t* base, long long rows, long long cols,
                        int box_rows) {
@@ -1027,7 +1010,7 @@ constexpr int kFarJobsPerCta = 4;
 
 int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, const int* Ts, const TcLayout& L,
                 cudaStream_t stream) {
-  EncodeTiledFn enc = it_encode_fn();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (!enc) return KFAC_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;

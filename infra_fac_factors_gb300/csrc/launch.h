@@ -1,5 +1,6 @@
 // Internal launchers (host side) behind the C ABI of kfac.h.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -14,6 +15,12 @@ int* device_status_ptr();
 // Counts every kernel launch of the library (reported by kfac_launch_count).
 void count_launch();
 bool ensure_smem_attr(int dev, const void* fn, int bytes);
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime
+// (nullptr when the driver does not provide it).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 // Per-launch timing of the main kernels, for kfac_profile / kfac_profile_read:
 // when recording is on, prof_begin records an event on the launch's stream
@@ -25,6 +32,7 @@ void prof_begin(cudaStream_t stream, ProfMark& m);
 void prof_end(int kind, cudaStream_t stream, const ProfMark& m, double work);
 
 int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirror, cudaStream_t stream);
+int launch_conv_factors(int n, const kfac_conv_factor_args* args, int P, int mirror, cudaStream_t stream);
 int launch_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw, int64_t C, int64_t ld_g, float* gs,
                        int64_t ld_gs, cudaStream_t stream);
 int launch_update_running(int n, const kfac_running_args* args, int P, float decay, float gamma, int first_step,

@@ -26,7 +26,7 @@ import numpy as np
 __all__ = [
     "Layer", "Config", "CONFIGS", "config", "rng_for",
     "to_bf16_bits", "bf16_bits_to_f32", "round_bf16",
-    "layer_inputs", "padded_ld",
+    "layer_inputs", "padded_ld", "conv_shape", "conv_activations", "device_conv_activations",
 ]
 
 
@@ -156,6 +156,34 @@ def _mlp_weights(cfg: Config):
 def _round(cfg: Config, x: np.ndarray) -> np.ndarray:
     x32 = x.astype(np.float32)
     return round_bf16(x32) if cfg.in_dtype == "bf16" else x32
+
+
+def conv_shape(cfg: Config, layer: Layer):
+    """(B, H, W, C) of the NHWC input of a 3 x 3 conv layer: C = (d_in - 1) / 9
+    channels, square H = W images of `hw` positions, B = cfg.batch images."""
+    assert layer.kind == "conv3x3" and (layer.d_in - 1) % 9 == 0
+    side = int(round(layer.hw ** 0.5))
+    assert side * side == layer.hw
+    return cfg.batch, side, side, (layer.d_in - 1) // 9
+
+
+def conv_activations(shape, seed_keys, dist: str = "relu_normal", sigma: float = 1.0) -> np.ndarray:
+    """NHWC activations x[b, h, w, c] of `shape`, drawn from `dist` (ReLU of
+    N(0, sigma) for the conv workloads) and rounded to bf16; float32."""
+    return round_bf16(_draw(rng_for("conv", *seed_keys), tuple(shape), dist, sigma).astype(np.float32))
+
+
+def device_conv_activations(shape, seed_keys, dist: str = "relu_normal", sigma: float = 1.0, device="cuda"):
+    """The same distribution as ``conv_activations``, drawn on the device from a
+    seeded torch generator (bf16 tensor, NHWC contiguous)."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(torch_seed("conv", *seed_keys))
+    z = torch.randn(tuple(shape), generator=gen, device=device, dtype=torch.float32) * sigma
+    if dist == "relu_normal":
+        z.clamp_(min=0.0)
+    return z.to(torch.bfloat16)
 
 
 def torch_seed(*keys) -> int:

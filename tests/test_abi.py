@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_exports_every_declared_function():
     names = declared_functions()
-    assert len(names) == 17
+    assert len(names) == 18
     out = subprocess.run(["nm", "-D", "--defined-only", capi.library_path], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (kfac_[a-z_0-9]+)$", out, flags=re.M))
     for n in names:
@@ -52,6 +52,8 @@ int main(void) {
   S(kfac_running_args) O(kfac_running_args, damped) O(kfac_running_args, ld)
   S(kfac_inverse_args) O(kfac_inverse_args, ld_out)
   S(kfac_precond_args) O(kfac_precond_args, out) O(kfac_precond_args, d_in)
+  S(kfac_conv_factor_args) O(kfac_conv_factor_args, C) O(kfac_conv_factor_args, out)
+  O(kfac_conv_factor_args, scale)
   return 0;
 }
 """
@@ -63,7 +65,8 @@ int main(void) {
         lines = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
     got = dict(l.split() for l in lines if l)
     for name, st in (("kfac_factor_args", capi.kfac_factor_args), ("kfac_running_args", capi.kfac_running_args),
-                     ("kfac_inverse_args", capi.kfac_inverse_args), ("kfac_precond_args", capi.kfac_precond_args)):
+                     ("kfac_inverse_args", capi.kfac_inverse_args), ("kfac_precond_args", capi.kfac_precond_args),
+                     ("kfac_conv_factor_args", capi.kfac_conv_factor_args)):
         assert int(got[name]) == C.sizeof(st), name
         for key, val in got.items():
             if key.startswith(name + "."):
@@ -175,6 +178,33 @@ def test_precondition_rejects_invalid():
                                   check=False) == capi.KFAC_ERR_INVALID_ARG
 
 
+def ca(**kw):
+    base = dict(x=A16, B=4, H=5, W=7, C=64, out=A16 * 2, ld_out=580, stride_out=577 * 580, scale=1.0)
+    base.update(kw)
+    return capi.kfac_conv_factor_args(**base)
+
+
+@pytest.mark.parametrize("kw,P", [
+    (dict(x=None), 2),
+    (dict(x=A16 + 2), 2),                # misaligned activations
+    (dict(out=A16 + 4), 2),              # misaligned output
+    (dict(C=96), 2),                     # C % 64
+    (dict(C=0), 2),
+    (dict(C=7296), 2),                   # d = 9 C + 1 above the limit
+    (dict(B=3), 2),                      # B % P
+    (dict(H=0), 2),
+    (dict(W=-1), 2),
+    (dict(B=2, H=1 << 16, W=1 << 15), 2),  # B H W above 2^31 - 1
+    (dict(ld_out=576), 2),               # ld_out < d
+    (dict(ld_out=578), 2),               # fp32 ld not a multiple of 4
+    (dict(stride_out=100), 2),           # shards overlap
+    (dict(scale=float("inf")), 2),
+    (dict(), 0),                         # P
+])
+def test_conv_factors_rejects_invalid(kw, P):
+    assert capi.kfac_conv_factors([ca(**kw)], P, check=False) == capi.KFAC_ERR_INVALID_ARG
+
+
 def test_spatial_sum_rejects_invalid():
     f = capi.kfac_spatial_sum
     assert f(0, 0, 2, 4, 8, 8, A16, 8, check=False) == capi.KFAC_ERR_INVALID_ARG
@@ -190,6 +220,7 @@ def test_wait_selftest_rejects_limits_outside_the_kernels_range():
 
 def test_empty_calls_are_no_ops():
     assert capi.kfac_factors([], capi.KFAC_BF16, 1, check=False) == capi.KFAC_OK
+    assert capi.kfac_conv_factors([], 1, check=False) == capi.KFAC_OK
     assert capi.kfac_update_running([], 1, 0.5, 0.0, True, check=False) == capi.KFAC_OK
     assert capi.kfac_precondition([], 0, 0, 0, 0, check=False) == capi.KFAC_OK
 

@@ -1,0 +1,136 @@
+"""GPU parity of the implicit-im2col conv factors (kfac_conv_factors) against
+the fp64 oracle: oracle.factor of oracle.im2col3x3 of each worker's images.
+
+Tolerance: factors <= 1e-5 relative Frobenius (bf16 products are exact in
+fp32; the error is fp32 accumulation).  NaN sentinels in the lower tiles and
+the padding catch stray writes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from infra_fac_factors_gb300 import capi
+
+from gpu_util import ensure_built, pad, rel_fro, stream, upper_tile_mask
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    ensure_built()
+    torch.cuda.init()
+
+
+def sync():
+    torch.cuda.synchronize()
+    assert capi.kfac_device_status(clear=True) == capi.KFAC_OK
+
+
+def conv_args(x_dev, shape, out, ldo, P):
+    B, H, W, C = shape
+    d = 9 * C + 1
+    rows_p = B // P * H * W
+    return capi.kfac_conv_factor_args(x_dev.data_ptr(), B, H, W, C, out.data_ptr(), ldo, d * ldo, 1.0 / rows_p)
+
+
+def run_conv(x, P, mirror=0, ld_extra=4):
+    B, H, W, C = x.shape
+    d = 9 * C + 1
+    ldo = pad(d, 4) + ld_extra
+    xt = torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+    out = torch.full((P, d, ldo), float("nan"), dtype=torch.float32, device="cuda")
+    capi.kfac_conv_factors([conv_args(xt, x.shape, out, ldo, P)], P, mirror, stream())
+    sync()
+    return out.cpu().numpy()
+
+
+def oracle_shard(x, P, p):
+    B = x.shape[0]
+    X = oracle.im2col3x3(x[p * B // P:(p + 1) * B // P])
+    return oracle.factor(X, 1.0 / X.shape[0])
+
+
+def check_upper(res, x, P, shards=None):
+    B, H, W, C = x.shape
+    d = 9 * C + 1
+    m = upper_tile_mask(d)
+    for p in (range(P) if shards is None else shards):
+        ref = oracle_shard(x, P, p)
+        got = res[p][:, :d]
+        err = rel_fro(got, ref, m)
+        assert err <= 1e-5, (p, err)
+        assert np.isnan(got[~m]).all(), "lower tiles must stay untouched"
+        assert np.isnan(res[p][:, d:]).all(), "padding must stay untouched"
+
+
+@pytest.mark.parametrize("shape,P", [
+    ((4, 5, 7, 64), 2),      # 70 patch rows per worker: one full 64-row stage and a ragged one
+    ((2, 3, 3, 128), 1),     # every position touches the zero padding
+    ((3, 1, 1, 64), 3),      # 1 x 1 images: only the centre tap and the bias are non-zero
+    ((2, 2, 65, 64), 2),     # one-row-high images, a width past two 64-row stages
+    ((8, 24, 24, 64), 2),    # 2304 rows per worker: three 1024-row accumulation chunks
+    ((2, 6, 5, 192), 2),     # d = 1729: fourteen 128-row blocks, three 64-channel boxes per tap
+])
+def test_conv_factors_match_oracle(shape, P):
+    x = synth.conv_activations(shape, ("test", *shape, P))
+    check_upper(run_conv(x, P), x, P)
+
+
+def test_conv_factors_mirror_gives_full_symmetric():
+    shape, P = (2, 6, 5, 64), 2
+    x = synth.conv_activations(shape, ("mirror",))
+    res = run_conv(x, P, mirror=1, ld_extra=0)
+    d = 9 * shape[3] + 1
+    for p in range(P):
+        got = res[p][:, :d]
+        assert not np.isnan(got).any()
+        assert rel_fro(got, oracle_shard(x, P, p)) <= 1e-5
+        assert np.abs(got - got.T).max() <= 1e-6 * np.abs(got).max()
+
+
+def test_conv_factors_signed_inputs_and_bias_column():
+    # signed activations (no ReLU): cancellation in the sums; the bias row of
+    # each factor is the patch mean and its corner is exactly 1
+    shape, P = (4, 4, 4, 64), 4
+    x = synth.conv_activations(shape, ("signed",), dist="normal")
+    res = run_conv(x, P)
+    check_upper(res, x, P)
+    d = 9 * shape[3] + 1
+    for p in range(P):
+        assert res[p][d - 1, d - 1] == 1.0
+
+
+def test_conv_factors_several_layers_in_one_call():
+    P = 4
+    shapes = [(4, 7, 7, 64), (8, 3, 5, 128), (4, 2, 2, 256)]
+    xs, outs, args, lds = [], [], [], []
+    for k, sh in enumerate(shapes):
+        x = synth.conv_activations(sh, ("multi", k))
+        d = 9 * sh[3] + 1
+        ldo = pad(d, 4)
+        xt = torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+        out = torch.full((P, d, ldo), float("nan"), dtype=torch.float32, device="cuda")
+        xs.append((x, xt))
+        outs.append(out)
+        args.append(conv_args(xt, sh, out, ldo, P))
+    capi.kfac_conv_factors(args, P, 0, stream())
+    sync()
+    for (x, _), out in zip(xs, outs):
+        check_upper(out.cpu().numpy(), x, P)
+
+
+@pytest.mark.parametrize("layer_index", [0, 1, 2, 3])
+def test_conv_factors_resnet_full_size_sampled_workers(layer_index):
+    # the ResNet-50 3 x 3 conv shapes at batch 32 in 8 workers; the first and
+    # last workers' factors are compared whole with the oracle
+    cfg = synth.config("resnet_conv")
+    layer = cfg.layers[layer_index]
+    shape = synth.conv_shape(cfg, layer)
+    P = cfg.P
+    x = synth.conv_activations(shape, (cfg.key, 0, layer_index))
+    res = run_conv(x, P, ld_extra=0)
+    check_upper(res, x, P, shards=(0, P - 1))
