@@ -25,6 +25,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "factor_epilogue.cuh"
 #include "launch.h"
@@ -67,14 +69,33 @@ struct SyProb {
   float scale;
 };
 
+// Input side of a launch: the rows of bf16 matrices (linear layers) ...
+struct SyLinear {};
+// ... or the 3 x 3 patches of NHWC activations (conv layers, implicit im2col):
+// one problem per worker, its tensor map an im2col map over the worker's
+// images; the bias column and the columns past d come from `ones`.
+struct SyConvGeom {
+  int c64, H, W;     // channels / 64, image height and width
+  int sw, sh, sn;    // 64 positions = sn images + sh rows + sw columns
+};
+struct SyConv {
+  CUtensorMap ones;  // {64, 128} bf16: rows 0-63 = (1, 0, ..., 0), rows 64-127 = 0; box 64 x 64
+  SyConvGeom g[kSyMaxProbs];
+};
+
+template <class In>
 struct SyParams {  // 128-byte aligned through CUtensorMap
-  CUtensorMap maps[kSyMaxProbs];   // inputs  {d, rows_p, P} bf16, box 64 x 64
+  // inputs: linear {d, rows_p, P} bf16, box 64 x 64; conv: im2col {C, W, H, B/P}
+  // of one worker, bounding box corners -1 (3 x 3, padding 1), 64 pixels x 64 channels
+  CUtensorMap maps[kSyMaxProbs];
   CUtensorMap omaps[kSyMaxProbs];  // outputs {d, d, P} fp32, box 32 x 32, swizzled
   SyProb probs[kSyMaxProbs];
+  In in;
   long long total_units;
   int* status;
   int n_probs, P, mirror;
 };
+static_assert(sizeof(SyParams<SyConv>) <= 32764, "kernel parameters exceed 32764 bytes");
 
 struct SyUnit {
   int prob, p, i, w;
@@ -87,7 +108,8 @@ struct SyUnit {
 // the start) over the problem table, which lives in the kernel's parameter
 // space: a search with data-dependent indices there costs a constant-cache
 // miss per probe.
-__device__ __forceinline__ SyUnit sy_decode(const SyParams& prm, long long u, int& lo) {
+template <class In>
+__device__ __forceinline__ SyUnit sy_decode(const SyParams<In>& prm, long long u, int& lo) {
   while (lo + 1 < prm.n_probs && prm.probs[lo + 1].unit_begin <= u) ++lo;
   const SyProb& pr = prm.probs[lo];
   const int local = (int)(u - pr.unit_begin);
@@ -100,7 +122,52 @@ __device__ __forceinline__ SyUnit sy_decode(const SyParams& prm, long long u, in
   return r;
 }
 
-__global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__ SyParams prm) {
+// Source of column box q (patch columns 64q .. 64q + 63) of a conv problem.
+// With C % 64 == 0 a box is 64 channels (from c0) of one tap (dh, dw); box
+// 9C/64 holds the bias column and later boxes are past d.
+struct SyConvBox {
+  int c0, dw, dh;
+  int kind;  // 0 tap, 1 bias column, 2 zeros
+};
+__device__ __forceinline__ SyConvBox sy_conv_box_source(const SyConvGeom& g, int q) {
+  SyConvBox b{0, 0, 0, q == 9 * g.c64 ? 1 : 2};
+  if (q < 9 * g.c64) {
+    const int tap = q / g.c64;
+    b.dh = tap / 3;
+    b.dw = tap - 3 * b.dh;
+    b.c0 = (q - tap * g.c64) * 64;
+    b.kind = 0;
+  }
+  return b;
+}
+
+// One box of the 64 patch rows that start at output position (n, h, w) of the
+// worker's images, `rem` of them inside the worker's rows.  A tap box is an
+// im2col load from (w - 1, h - 1) (the map's bounding box starts one pixel
+// before the image) with offsets (dw, dh); rows past the worker's last image
+// fall outside the map and read zero.  The bias box reads rows 0-63 of
+// `ones` (from row 64 - rem for a tail), a box past d rows 64-127.
+template <bool MC>
+__device__ __forceinline__ void sy_conv_load(const SyParams<SyConv>& prm, int e, const SyConvBox& b, int n, int h,
+                                             int w, int rem, void* dst, uint64_t* bar) {
+  if (b.kind == 0) {
+    if (MC)
+      tma_load_im2col_4d_mc(dst, &prm.maps[e], b.c0, w - 1, h - 1, n, (uint16_t)b.dw, (uint16_t)b.dh, bar,
+                            (uint16_t)0x3);
+    else
+      tma_load_im2col_4d(dst, &prm.maps[e], b.c0, w - 1, h - 1, n, (uint16_t)b.dw, (uint16_t)b.dh, bar);
+  } else {
+    const int y = b.kind == 1 ? (rem >= 64 ? 0 : 64 - rem) : 64;
+    if (MC)
+      tma_load_2d_mc(dst, &prm.in.ones, 0, y, bar, (uint16_t)0x3);
+    else
+      tma_load_2d(dst, &prm.in.ones, 0, y, bar);
+  }
+}
+
+template <class In>
+__global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__ SyParams<In> prm) {
+  constexpr bool kConv = std::is_same<In, SyConv>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* out_stage = smem + kSyStages * kSyStageBytes;  // 1024-aligned
@@ -147,16 +214,48 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
         const int nk = (pr.rows_p + kSyBK - 1) / kSyBK;
         // this CTA's share of the column boxes (multicast to both CTAs)
         const int half = (nb + 1) / 2, q0 = rank == 0 ? 0 : half, q1 = rank == 0 ? half : nb;
+        // conv: the unit's box sources (at most two column boxes per CTA) and the
+        // output position (n, h, w) of the k-block's first patch row, stepped by 64
+        SyConvBox bx[4];
+        SyConvGeom g{};
+        int n = 0, h = 0, w = 0;
+        if constexpr (kConv) {
+          g = prm.in.g[un.prob];
+          bx[0] = sy_conv_box_source(g, un.i * 2);
+          bx[1] = sy_conv_box_source(g, un.i * 2 + 1);
+          bx[2] = sy_conv_box_source(g, (int)(un.j0 / 64) + q0);
+          bx[3] = sy_conv_box_source(g, (int)(un.j0 / 64) + q0 + 1);
+        }
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
           uint8_t* sa = smem + stage * kSyStageBytes;
           uint8_t* sb = sa + kSyABytes;
           mbar_arrive_expect_tx(&full[stage], (uint32_t)((2 + nb) * kSyBox));
-          tma_load_3d(sa, map, un.i * 128, kb * kSyBK, un.p, &full[stage]);
-          tma_load_3d(sa + kSyBox, map, un.i * 128 + 64, kb * kSyBK, un.p, &full[stage]);
-          for (int q = q0; q < q1; ++q)
-            tma_load_3d_mc(sb + q * kSyBox, map, (int)un.j0 + 64 * q, kb * kSyBK, un.p, &full[stage],
-                           (uint16_t)0x3);
+          if constexpr (kConv) {
+            const int rem = pr.rows_p - kb * kSyBK;
+            sy_conv_load<false>(prm, un.prob, bx[0], n, h, w, rem, sa, &full[stage]);
+            sy_conv_load<false>(prm, un.prob, bx[1], n, h, w, rem, sa + kSyBox, &full[stage]);
+            if (q1 > q0) sy_conv_load<true>(prm, un.prob, bx[2], n, h, w, rem, sb + q0 * kSyBox, &full[stage]);
+            if (q1 > q0 + 1)
+              sy_conv_load<true>(prm, un.prob, bx[3], n, h, w, rem, sb + (q0 + 1) * kSyBox, &full[stage]);
+            w += g.sw;
+            if (w >= g.W) {
+              w -= g.W;
+              ++h;
+            }
+            h += g.sh;
+            if (h >= g.H) {
+              h -= g.H;
+              ++n;
+            }
+            n += g.sn;
+          } else {
+            tma_load_3d(sa, map, un.i * 128, kb * kSyBK, un.p, &full[stage]);
+            tma_load_3d(sa + kSyBox, map, un.i * 128 + 64, kb * kSyBK, un.p, &full[stage]);
+            for (int q = q0; q < q1; ++q)
+              tma_load_3d_mc(sb + q * kSyBox, map, (int)un.j0 + 64 * q, kb * kSyBK, un.p, &full[stage],
+                             (uint16_t)0x3);
+          }
           if (++stage == kSyStages) {
             stage = 0;
             phase ^= 1;
@@ -330,6 +429,55 @@ __global__ void __launch_bounds__(256) spatial_sum_kernel(const Tin* __restrict_
 }
 
 // ------------------------------------------------------------------ host side
+// Output side of one problem: the fp32 factors {d, d, P} (TMA map and unit table).
+static int sy_set_output(EncodeTiledFn enc, CUtensorMap* omap, SyProb& pr, float* out, long long d, long long ld_out,
+                         long long stride_out, int P, long long rows_p, float scale, long long& units) {
+  const long long so = P > 1 ? stride_out : d * ld_out;
+  cuuint64_t odim[3] = {(cuuint64_t)d, (cuuint64_t)d, (cuuint64_t)P};
+  cuuint64_t ostride[2] = {(cuuint64_t)ld_out * 4, (cuuint64_t)so * 4};
+  cuuint32_t obox[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, odim, ostride, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return KFAC_ERR_INVALID_ARG;
+  pr.out = out;
+  pr.ld_out = ld_out;
+  pr.stride_out = stride_out;
+  pr.d = (int)d;
+  pr.rows_p = (int)rows_p;
+  pr.units_per_shard = (int)factor_units(d);
+  pr.unit_begin = units;
+  pr.scale = scale;
+  units += (long long)pr.units_per_shard * P;
+  return KFAC_OK;
+}
+
+// One launch: clusters of two CTAs, one per pair-chunk of the tile map.
+template <class In>
+static int sy_launch(const SyParams<In>& prm, int sms, double work, int kind, cudaStream_t stream) {
+  if (prm.total_units == 0) return KFAC_OK;
+  const long long pairs = prm.total_units / 2, clusters = pairs < sms / 2 ? pairs : sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = kSySmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ProfMark pm;
+  prof_begin(stream, pm);
+  if (cudaLaunchKernelEx(&cfg, syrk_tc_kernel<In>, prm) != cudaSuccess) return KFAC_ERR_CUDA;
+  prof_end(kind, stream, pm, work);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
 int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirror, cudaStream_t stream) {
   if (dtype == KFAC_BF16) {
     EncodeTiledFn enc = tensor_map_encoder();
@@ -338,12 +486,13 @@ int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mi
     if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
     const int sms = device_sm_count(dev);
     if (sms <= 0) return KFAC_ERR_CUDA;
-    if (!ensure_smem_attr(dev, (const void*)syrk_tc_kernel, kSySmem)) return KFAC_ERR_CUDA;
+    if (!ensure_smem_attr(dev, (const void*)syrk_tc_kernel<SyLinear>, kSySmem)) return KFAC_ERR_CUDA;
     for (int base = 0; base < n; base += kSyMaxProbs) {
       const int cnt = n - base < kSyMaxProbs ? n - base : kSyMaxProbs;
-      SyParams prm;
+      SyParams<SyLinear> prm;
       memset(&prm, 0, sizeof(prm));
       long long units = 0;
+      double work = 0.0;  // algorithmic flops of the launch
       for (int k = 0; k < cnt; ++k) {
         const kfac_factor_args& a = args[base + k];
         const long long rows_p = a.rows / P;
@@ -355,57 +504,20 @@ int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mi
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (cr != CUDA_SUCCESS) return KFAC_ERR_INVALID_ARG;
-        const long long so = P > 1 ? a.stride_out : a.d * a.ld_out;
-        cuuint64_t odim[3] = {(cuuint64_t)a.d, (cuuint64_t)a.d, (cuuint64_t)P};
-        cuuint64_t ostride[2] = {(cuuint64_t)a.ld_out * 4, (cuuint64_t)so * 4};
-        cuuint32_t obox[3] = {32, 32, 1};
-        cr = enc(&prm.omaps[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.out, odim, ostride, obox, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (cr != CUDA_SUCCESS) return KFAC_ERR_INVALID_ARG;
-        SyProb& pr = prm.probs[k];
-        pr.out = a.out;
-        pr.ld_out = a.ld_out;
-        pr.stride_out = a.stride_out;
-        pr.d = (int)a.d;
-        pr.rows_p = (int)rows_p;
-        pr.units_per_shard = (int)factor_units(a.d);
-        pr.unit_begin = units;
-        pr.scale = a.scale;
-        units += (long long)pr.units_per_shard * P;
+        const int st = sy_set_output(enc, &prm.omaps[k], prm.probs[k], a.out, a.d, a.ld_out, a.stride_out, P, rows_p,
+                                     a.scale, units);
+        if (st != KFAC_OK) return st;
+        const double d = (double)a.d;
+        work += 2.0 * (double)a.rows * d * (d + 1.0) / 2.0;
       }
       prm.n_probs = cnt;
       prm.P = P;
       prm.mirror = mirror;
       prm.total_units = units;
-      double work = 0.0;  // algorithmic flops of the launch
-      for (int k = 0; k < cnt; ++k) {
-        const double d = (double)args[base + k].d;
-        work += 2.0 * (double)args[base + k].rows * d * (d + 1.0) / 2.0;
-      }
       prm.status = device_status_ptr();
       if (!prm.status) return KFAC_ERR_CUDA;
-      if (units == 0) continue;
-      // clusters of two CTAs, one per pair-chunk of the tile map
-      const long long pairs = units / 2, clusters = pairs < sms / 2 ? pairs : sms / 2;
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3((unsigned)(2 * clusters));
-      cfg.blockDim = dim3(192);
-      cfg.dynamicSmemBytes = kSySmem;
-      cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      ProfMark pm;
-      prof_begin(stream, pm);
-      if (cudaLaunchKernelEx(&cfg, syrk_tc_kernel, prm) != cudaSuccess) return KFAC_ERR_CUDA;
-      prof_end(KFAC_K_SYRK, stream, pm, work);
-      count_launch();
-      if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
+      const int st = sy_launch(prm, sms, work, KFAC_K_SYRK, stream);
+      if (st != KFAC_OK) return st;
     }
     return KFAC_OK;
   }
@@ -444,6 +556,83 @@ int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mi
     syrk_simt_kernel<float><<<grid, 256, 0, stream>>>(prm);
     count_launch();
     if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
+  }
+  return KFAC_OK;
+}
+
+// Rows 0-63: (1, 0, ..., 0), rows 64-127: zeros (64 bf16 per row): the bias
+// column of the conv patch matrix and the boxes past d.
+struct SyOnesTile {
+  uint16_t v[128 * 64];
+};
+static constexpr SyOnesTile make_ones_tile() {
+  SyOnesTile t{};
+  for (int r = 0; r < 64; ++r) t.v[r * 64] = 0x3F80;  // bf16 1.0
+  return t;
+}
+__device__ __align__(128) SyOnesTile g_conv_ones = make_ones_tile();
+
+int launch_conv_factors(int n, const kfac_conv_factor_args* args, int P, int mirror, cudaStream_t stream) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  EncodeIm2colFn enc_i2c = tensor_map_im2col_encoder();
+  if (!enc || !enc_i2c) return KFAC_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return KFAC_ERR_CUDA;
+  if (!ensure_smem_attr(dev, (const void*)syrk_tc_kernel<SyConv>, kSySmem)) return KFAC_ERR_CUDA;
+  void* ones = nullptr;
+  if (cudaGetSymbolAddress(&ones, g_conv_ones) != cudaSuccess) return KFAC_ERR_CUDA;
+  // one problem per (layer, worker)
+  const long long total = (long long)n * P;
+  for (long long base = 0; base < total; base += kSyMaxProbs) {
+    const int cnt = (int)(total - base < kSyMaxProbs ? total - base : kSyMaxProbs);
+    SyParams<SyConv> prm;
+    memset(&prm, 0, sizeof(prm));
+    {
+      cuuint64_t gdim[2] = {64, 128};
+      cuuint64_t gstride[1] = {128};
+      cuuint32_t box[2] = {64, 64};
+      cuuint32_t estr[2] = {1, 1};
+      if (enc(&prm.in.ones, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ones, gdim, gstride, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return KFAC_ERR_CUDA;
+    }
+    long long units = 0;
+    double work = 0.0;  // algorithmic flops of the launch
+    for (int k = 0; k < cnt; ++k) {
+      const long long e = base + k;
+      const kfac_conv_factor_args& a = args[e / P];
+      const int p = (int)(e % P);
+      const long long Bp = a.B / P, d = 9 * a.C + 1, rows_p = Bp * a.H * a.W;
+      // this worker's images, NHWC: {C, W, H, B/P}; the bounding box of a 3 x 3,
+      // padding 1 window starts one pixel before the image and ends two before its end
+      const uint16_t* x = static_cast<const uint16_t*>(a.x) + (long long)p * rows_p * a.C;
+      cuuint64_t gdim[4] = {(cuuint64_t)a.C, (cuuint64_t)a.W, (cuuint64_t)a.H, (cuuint64_t)Bp};
+      cuuint64_t gstride[3] = {(cuuint64_t)(a.C * 2), (cuuint64_t)(a.W * a.C * 2), (cuuint64_t)(a.H * a.W * a.C * 2)};
+      int lower[2] = {-1, -1}, upper[2] = {-1, -1};
+      cuuint32_t estr[4] = {1, 1, 1, 1};
+      if (enc_i2c(&prm.maps[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(x), gdim, gstride, lower,
+                  upper, 64, kSyBK, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return KFAC_ERR_INVALID_ARG;
+      const int st = sy_set_output(enc, &prm.omaps[k], prm.probs[k], a.out + (long long)p * a.stride_out, d,
+                                   a.ld_out, 0, 1, rows_p, a.scale, units);
+      if (st != KFAC_OK) return st;
+      const int steps_w = (int)(kSyBK / a.W);  // 64 = sn H W + sh W + sw
+      prm.in.g[k] = SyConvGeom{(int)(a.C / 64), (int)a.H,       (int)a.W, (int)(kSyBK % a.W),
+                               (int)(steps_w % a.H), (int)(steps_w / a.H)};
+      work += 2.0 * (double)rows_p * (double)d * ((double)d + 1.0) / 2.0;
+    }
+    prm.n_probs = cnt;
+    prm.P = 1;
+    prm.mirror = mirror;
+    prm.total_units = units;
+    prm.status = device_status_ptr();
+    if (!prm.status) return KFAC_ERR_CUDA;
+    const int st = sy_launch(prm, sms, work, KFAC_K_CONV_SYRK, stream);
+    if (st != KFAC_OK) return st;
   }
   return KFAC_OK;
 }

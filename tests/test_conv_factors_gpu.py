@@ -74,6 +74,7 @@ def check_upper(res, x, P, shards=None):
     ((2, 2, 65, 64), 2),     # one-row-high images, a width past two 64-row stages
     ((8, 24, 24, 64), 2),    # 2304 rows per worker: three 1024-row accumulation chunks
     ((2, 6, 5, 192), 2),     # d = 1729: fourteen 128-row blocks, three 64-channel boxes per tap
+    ((4, 33, 1, 64), 2),     # one-pixel-wide images: a 64-row block spans two images
 ])
 def test_conv_factors_match_oracle(shape, P):
     x = synth.conv_activations(shape, ("test", *shape, P))
