@@ -6,6 +6,8 @@ the step in order (SPD-KFAC §II-B/§II-C):
 
   1. kfac_spatial_sum       (conv layers: per-sample sum of g over H*W)
   2. kfac_factors           per-worker factors A^p, G^p of all layers
+     kfac_conv_factors      (conv layers given by their NHWC activations: A
+                            from the implicit im2col of a 3 x 3 convolution)
   3. kfac_update_running    mean over workers, running average, damping
   4. kfac_damped_inverse    (A + gamma I)^-1, (G + gamma I)^-1 of all factors
   5. kfac_precondition      (G + gamma I)^-1 grad (A + gamma I)^-1 of all layers
@@ -21,7 +23,7 @@ Buffers are row-major with leading dimensions padded to 16-byte multiples
 from __future__ import annotations
 
 import dataclasses
-from typing import List, Optional, Sequence
+from typing import List, Optional, Sequence, Tuple
 
 import torch
 
@@ -39,6 +41,10 @@ class LayerSpec:
     rows: int            # rows of a and g per step
     batch: int           # samples per step (conv: rows = batch * hw)
     hw: int = 1          # spatial positions (1 for linear layers)
+    # (H, W) for a 3 x 3 conv layer (stride 1, padding 1) whose input is given
+    # as NHWC activations (batch x H x W x C, C = (d_in - 1) / 9, bf16); its A
+    # factor then comes from kfac_conv_factors instead of a patch matrix
+    image: Optional[Tuple[int, int]] = None
 
 
 def layer_groups(layers: Sequence[LayerSpec], n_groups: int):
@@ -98,7 +104,15 @@ class KFACStep:
         for L in self.layers:
             if L.rows % P:
                 raise ValueError("rows must split into P equal shards")
-            self.a.append(torch.zeros((L.rows, _pad(L.d_in, vec)), dtype=tdt, device=dev))
+            if L.image is not None:
+                H, W = L.image
+                C = (L.d_in - 1) // 9
+                if in_dtype != "bf16" or 9 * C + 1 != L.d_in or C % 64 or H * W != L.hw or L.rows != L.batch * L.hw:
+                    raise ValueError("a layer given by its image needs bf16, d_in = 9 C + 1 with C % 64 == 0 "
+                                     "and rows = batch * H * W")
+                self.a.append(torch.zeros((L.batch, H, W, C), dtype=tdt, device=dev))
+            else:
+                self.a.append(torch.zeros((L.rows, _pad(L.d_in, vec)), dtype=tdt, device=dev))
             self.g.append(torch.zeros((L.rows, _pad(L.d_out, vec)), dtype=tdt, device=dev))
             if L.hw > 1:
                 if L.batch % P:
@@ -137,8 +151,17 @@ class KFACStep:
     def _build_args(self):
         P = self.P
         fa_main, fa_fp32 = [], []   # factors from a (dtype of a), factors from fp32 spatial sums
+        self._fac_conv = {}         # layer -> A factor from NHWC activations
+        self._main_index = {}       # ("A" | "G", layer) -> index in fa_main
         for li, L in enumerate(self.layers):
             A = self.fa[li]
+            if L.image is not None:
+                B, H, W, C = self.a[li].shape
+                self._fac_conv[li] = capi.kfac_conv_factor_args(self.a[li].data_ptr(), B, H, W, C,
+                                                                A.shards.data_ptr(), A.ld, A.stride,
+                                                                1.0 / (L.rows // P))
+                continue
+            self._main_index[("A", li)] = len(fa_main)
             fa_main.append(capi.kfac_factor_args(self.a[li].data_ptr(), L.rows, L.d_in, self.a[li].shape[1],
                                                  A.shards.data_ptr(), A.ld, A.stride, 1.0 / (L.rows // P)))
         for li, L in enumerate(self.layers):
@@ -148,6 +171,7 @@ class KFACStep:
                 fa_fp32.append(capi.kfac_factor_args(gs.data_ptr(), L.batch, L.d_out, gs.shape[1],
                                                      G.shards.data_ptr(), G.ld, G.stride, 1.0 / (L.batch // P)))
             else:
+                self._main_index[("G", li)] = len(fa_main)
                 fa_main.append(capi.kfac_factor_args(self.g[li].data_ptr(), L.rows, L.d_out, self.g[li].shape[1],
                                                      G.shards.data_ptr(), G.ld, G.stride, 1.0 / (L.rows // P)))
         self._fac_main = fa_main
@@ -182,11 +206,12 @@ class KFACStep:
         self._groups = []
         for b, e in layer_groups(self.layers, n_groups):
             lis = range(b, e)
-            main = [self._fac_main[li] for li in lis]  # A factors
-            main += [self._fac_main[nl + li - self._n_conv_before(li)] for li in lis if self.layers[li].hw == 1]
+            main = [self._fac_main[self._main_index[(side, li)]] for side in ("A", "G") for li in lis
+                    if (side, li) in self._main_index]
             fp32 = [self._fac_fp32[self._n_conv_before(li)] for li in lis if self.layers[li].hw > 1]
+            conv = [self._fac_conv[li] for li in lis if li in self._fac_conv]
             run = [self._run_args[li] for li in lis] + [self._run_args[nl + li] for li in lis]
-            self._groups.append((list(lis), main, fp32, run))
+            self._groups.append((list(lis), main, fp32, conv, run))
 
     def _n_conv_before(self, li: int) -> int:
         return sum(1 for L in self.layers[:li] if L.hw > 1)
@@ -194,9 +219,13 @@ class KFACStep:
     # ------------------------------------------------------------------ inputs
     def set_layer_inputs(self, li: int, a: torch.Tensor, g: torch.Tensor, grad: torch.Tensor,
                          non_blocking: bool = False):
-        """Copy one layer's inputs (any device) into the padded device buffers."""
+        """Copy one layer's inputs (any device) into the padded device buffers;
+        `a` is the NHWC activation tensor for a layer given by its image."""
         L = self.layers[li]
-        self.a[li][:, :L.d_in].copy_(a, non_blocking=non_blocking)
+        if L.image is not None:
+            self.a[li].copy_(a, non_blocking=non_blocking)
+        else:
+            self.a[li][:, :L.d_in].copy_(a, non_blocking=non_blocking)
         self.g[li][:, :L.d_out].copy_(g, non_blocking=non_blocking)
         self.grad[li][:, :L.d_in].copy_(grad, non_blocking=non_blocking)
 
@@ -214,6 +243,8 @@ class KFACStep:
                                       self.g[li].shape[1], gs.data_ptr(), gs.shape[1], stream)
         if self._fac_main:
             capi.kfac_factors(self._fac_main, self.kdt, P, 0, stream)
+        if self._fac_conv:
+            capi.kfac_conv_factors(list(self._fac_conv.values()), P, 0, stream)
         if self._fac_fp32:
             capi.kfac_factors(self._fac_fp32, capi.KFAC_FP32, P, 0, stream)
 
@@ -237,7 +268,7 @@ class KFACStep:
         ms, ss = main.cuda_stream, self._side.cuda_stream
         decay = 0.0 if first_step else self.decay
         self._side.wait_stream(main)  # the side stream's earlier work must not overtake the inputs
-        for (lis, fmain, ffp32, run), ev in zip(self._groups, self._ev_fac):
+        for (lis, fmain, ffp32, fconv, run), ev in zip(self._groups, self._ev_fac):
             for li in lis:
                 L = self.layers[li]
                 if L.hw > 1:
@@ -246,6 +277,8 @@ class KFACStep:
                                           self.g[li].shape[1], gs.data_ptr(), gs.shape[1], ms)
             if fmain:
                 capi.kfac_factors(fmain, self.kdt, self.P, 0, ms)
+            if fconv:
+                capi.kfac_conv_factors(fconv, self.P, 0, ms)
             if ffp32:
                 capi.kfac_factors(ffp32, capi.KFAC_FP32, self.P, 0, ms)
             ev.record(main)

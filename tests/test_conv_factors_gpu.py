@@ -135,3 +135,61 @@ def test_conv_factors_resnet_full_size_sampled_workers(layer_index):
     x = synth.conv_activations(shape, (cfg.key, 0, layer_index))
     res = run_conv(x, P, ld_extra=0)
     check_upper(res, x, P, shards=(0, P - 1))
+
+
+def test_step_with_conv_layers_given_by_their_images():
+    # KFACStep on two 3 x 3 conv layers given as NHWC activations and one
+    # linear layer, two steps.  Worker factors against the oracle on the patch
+    # matrices (oracle.im2col3x3) of the same activations; each later stage
+    # against the oracle fed the GPU's previous stage, as in the config tests
+    from infra_fac_factors_gb300.step import KFACStep, LayerSpec
+    from gpu_util import residual
+
+    P, batch, gamma, decay = 4, 8, 1e-3, 0.9
+    convs = [((batch, 6, 6, 64), 64), ((batch, 3, 5, 128), 96)]  # (NHWC, d_out)
+    specs = [LayerSpec(9 * C + 1, d_out, B * H * W, B, H * W, image=(H, W)) for (B, H, W, C), d_out in convs]
+    specs.append(LayerSpec(129, 80, 64, 64))
+    step = KFACStep(specs, P, gamma, decay, "bf16", refine=capi.KFAC_REFINE_AUTO, n_groups=2)
+    prevR = {}
+    for t in range(2):
+        data = []
+        for li, L in enumerate(specs):
+            rng = np.random.default_rng(100 * t + li)
+            g = synth.round_bf16((rng.standard_normal((L.rows, L.d_out)) * 1e-2).astype(np.float32))
+            if L.image is not None:
+                x = synth.conv_activations(convs[li][0], ("step", t, li))
+                a, src = oracle.im2col3x3(x), torch.from_numpy(x)
+                gsrc = oracle.spatial_sum(g, L.batch, L.hw)
+            else:
+                a = synth.round_bf16(rng.standard_normal((L.rows, L.d_in)).astype(np.float32))
+                a[:, -1] = 1.0
+                src, gsrc = torch.from_numpy(a), g
+            grad = (g.astype(np.float64).T @ a.astype(np.float64) / L.batch).astype(np.float32)
+            data.append((a, gsrc, grad))
+            step.set_layer_inputs(li, src, torch.from_numpy(g), torch.from_numpy(grad))
+        step.step(first_step=(t == 0))
+        sync()
+        assert (step.info.cpu().numpy() == 0).all()
+        for li, L in enumerate(specs):
+            a, gsrc, grad = data[li]
+            X = {}
+            for name, F, src in (("A", step.fa[li], a), ("G", step.fg[li], gsrc)):
+                d = F.d
+                m = upper_tile_mask(d)
+                S = F.shards.cpu().numpy()[:, :, :d].astype(np.float64)
+                for p, ref in enumerate(oracle.shard_factors(src, P)):
+                    assert rel_fro(S[p], ref, m) <= 1e-5, (t, li, name, p, rel_fro(S[p], ref, m))
+                R = oracle.update_running(oracle.aggregate(list(S)), prevR.get((li, name)), decay, t == 0)
+                Rg = F.running.cpu().numpy()[:, :d].astype(np.float64)
+                assert rel_fro(Rg, R, m) <= 1e-6
+                Rg[~m] = 0
+                prevR[(li, name)] = Rg
+                Dg = F.damped.cpu().numpy()[:, :d].astype(np.float64)
+                assert rel_fro(Dg, oracle.damp(R, gamma), m) <= 1e-6
+                Dsym = np.triu(Dg) + np.triu(Dg, 1).T
+                X[name] = F.inv.cpu().numpy()[:, :d]
+                Xref, info = oracle.spd_inverse(Dsym)
+                assert info == 0
+                assert residual(X[name], Dsym) <= 1e-3 and rel_fro(X[name], Xref) <= 1e-3, (t, li, name)
+            V = step.out[li].cpu().numpy()[:, :L.d_in]
+            assert rel_fro(V, oracle.precondition(X["G"], grad, X["A"])) <= 2e-3, (t, li)
