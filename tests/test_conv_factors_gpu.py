@@ -137,27 +137,24 @@ def test_conv_factors_resnet_full_size_sampled_workers(layer_index):
     check_upper(res, x, P, shards=(0, P - 1))
 
 
-def test_step_with_conv_layers_given_by_their_images():
-    # KFACStep on two 3 x 3 conv layers given as NHWC activations and one
-    # linear layer, two steps.  Worker factors against the oracle on the patch
-    # matrices (oracle.im2col3x3) of the same activations; each later stage
-    # against the oracle fed the GPU's previous stage, as in the config tests
-    from infra_fac_factors_gb300.step import KFACStep, LayerSpec
+def run_step_and_check(specs, images, P, gamma, decay, steps, g_sigma, seed):
+    """Run KFACStep for `steps` steps on `specs` (conv layers given by their
+    NHWC activations of shape images[li], linear layers by a) and check every
+    stage: worker factors against the oracle on the patch matrices
+    (oracle.im2col3x3) of the same activations, each later stage against the
+    oracle fed the GPU's previous stage, as in the config tests."""
+    from infra_fac_factors_gb300.step import KFACStep
     from gpu_util import residual
 
-    P, batch, gamma, decay = 4, 8, 1e-3, 0.9
-    convs = [((batch, 6, 6, 64), 64), ((batch, 3, 5, 128), 96)]  # (NHWC, d_out)
-    specs = [LayerSpec(9 * C + 1, d_out, B * H * W, B, H * W, image=(H, W)) for (B, H, W, C), d_out in convs]
-    specs.append(LayerSpec(129, 80, 64, 64))
     step = KFACStep(specs, P, gamma, decay, "bf16", refine=capi.KFAC_REFINE_AUTO, n_groups=2)
     prevR = {}
-    for t in range(2):
+    for t in range(steps):
         data = []
         for li, L in enumerate(specs):
-            rng = np.random.default_rng(100 * t + li)
-            g = synth.round_bf16((rng.standard_normal((L.rows, L.d_out)) * 1e-2).astype(np.float32))
+            rng = np.random.default_rng((seed, t, li))
+            g = synth.round_bf16((rng.standard_normal((L.rows, L.d_out)) * g_sigma).astype(np.float32))
             if L.image is not None:
-                x = synth.conv_activations(convs[li][0], ("step", t, li))
+                x = synth.conv_activations(images[li], (seed, t, li))
                 a, src = oracle.im2col3x3(x), torch.from_numpy(x)
                 gsrc = oracle.spatial_sum(g, L.batch, L.hw)
             else:
@@ -180,6 +177,7 @@ def test_step_with_conv_layers_given_by_their_images():
                 for p, ref in enumerate(oracle.shard_factors(src, P)):
                     assert rel_fro(S[p], ref, m) <= 1e-5, (t, li, name, p, rel_fro(S[p], ref, m))
                 R = oracle.update_running(oracle.aggregate(list(S)), prevR.get((li, name)), decay, t == 0)
+                del S
                 Rg = F.running.cpu().numpy()[:, :d].astype(np.float64)
                 assert rel_fro(Rg, R, m) <= 1e-6
                 Rg[~m] = 0
@@ -190,6 +188,34 @@ def test_step_with_conv_layers_given_by_their_images():
                 X[name] = F.inv.cpu().numpy()[:, :d]
                 Xref, info = oracle.spd_inverse(Dsym)
                 assert info == 0
-                assert residual(X[name], Dsym) <= 1e-3 and rel_fro(X[name], Xref) <= 1e-3, (t, li, name)
+                err, res = rel_fro(X[name], Xref), residual(X[name], Dsym)
+                assert err <= 1e-3 and res <= 1e-3, (t, li, name, err, res)
             V = step.out[li].cpu().numpy()[:, :L.d_in]
             assert rel_fro(V, oracle.precondition(X["G"], grad, X["A"])) <= 2e-3, (t, li)
+
+
+def test_step_with_conv_layers_given_by_their_images():
+    # two 3 x 3 conv layers given as NHWC activations and one linear layer, two steps
+    from infra_fac_factors_gb300.step import LayerSpec
+
+    P, batch = 4, 8
+    images = [(batch, 6, 6, 64), (batch, 3, 5, 128), None]
+    d_outs = [64, 96]
+    specs = [LayerSpec(9 * C + 1, d_out, B * H * W, B, H * W, image=(H, W))
+             for (B, H, W, C), d_out in zip(images[:2], d_outs)]
+    specs.append(LayerSpec(129, 80, 64, 64))
+    run_step_and_check(specs, images, P, 1e-3, 0.9, 2, 1e-2, seed=1)
+
+
+def test_step_resnet_conv_workload_from_images():
+    # the ResNet-50 3 x 3 conv workload at full size (batch 32, P = 8) with its
+    # factor A formed from NHWC activations, one step, every stage checked
+    from infra_fac_factors_gb300.step import LayerSpec
+
+    cfg = synth.config("resnet_conv")
+    images, specs = [], []
+    for layer in cfg.layers:
+        B, H, W, C = synth.conv_shape(cfg, layer)
+        images.append((B, H, W, C))
+        specs.append(LayerSpec(layer.d_in, layer.d_out, cfg.rows(layer), cfg.batch, layer.hw, image=(H, W)))
+    run_step_and_check(specs, images, cfg.P, cfg.gamma, 0.0, 1, cfg.g_sigma, seed=2)
