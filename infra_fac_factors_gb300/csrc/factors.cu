@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "factor_epilogue.cuh"
+#include "conv_geom.cuh"
 #include "launch.h"
 #include "simt.cuh"
 #include "tilemap.cuh"
@@ -74,13 +75,9 @@ struct SyLinear {};
 // ... or the 3 x 3 patches of NHWC activations (conv layers, implicit im2col):
 // one problem per worker, its tensor map an im2col map over the worker's
 // images; the bias column and the columns past d come from `ones`.
-struct SyConvGeom {
-  int c64, H, W;     // channels / 64, image height and width
-  int sw, sh, sn;    // 64 positions = sn images + sh rows + sw columns
-};
 struct SyConv {
   CUtensorMap ones;  // {64, 128} bf16: rows 0-63 = (1, 0, ..., 0), rows 64-127 = 0; box 64 x 64
-  SyConvGeom g[kSyMaxProbs];
+  ConvGeom g[kSyMaxProbs];
 };
 
 template <class In>
@@ -122,25 +119,6 @@ __device__ __forceinline__ SyUnit sy_decode(const SyParams<In>& prm, long long u
   return r;
 }
 
-// Source of column box q (patch columns 64q .. 64q + 63) of a conv problem.
-// With C % 64 == 0 a box is 64 channels (from c0) of one tap (dh, dw); box
-// 9C/64 holds the bias column and later boxes are past d.
-struct SyConvBox {
-  int c0, dw, dh;
-  int kind;  // 0 tap, 1 bias column, 2 zeros
-};
-__device__ __forceinline__ SyConvBox sy_conv_box_source(const SyConvGeom& g, int q) {
-  SyConvBox b{0, 0, 0, q == 9 * g.c64 ? 1 : 2};
-  if (q < 9 * g.c64) {
-    const int tap = q / g.c64;
-    b.dh = tap / 3;
-    b.dw = tap - 3 * b.dh;
-    b.c0 = (q - tap * g.c64) * 64;
-    b.kind = 0;
-  }
-  return b;
-}
-
 // One box of the 64 patch rows that start at output position (n, h, w) of the
 // worker's images, `rem` of them inside the worker's rows.  A tap box is an
 // im2col load from (w - 1, h - 1) (the map's bounding box starts one pixel
@@ -148,7 +126,7 @@ __device__ __forceinline__ SyConvBox sy_conv_box_source(const SyConvGeom& g, int
 // fall outside the map and read zero.  The bias box reads rows 0-63 of
 // `ones` (from row 64 - rem for a tail), a box past d rows 64-127.
 template <bool MC>
-__device__ __forceinline__ void sy_conv_load(const SyParams<SyConv>& prm, int e, const SyConvBox& b, int n, int h,
+__device__ __forceinline__ void sy_conv_load(const SyParams<SyConv>& prm, int e, const ConvBox& b, int n, int h,
                                              int w, int rem, void* dst, uint64_t* bar) {
   if (b.kind == 0) {
     if (MC)
@@ -216,15 +194,15 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
         const int half = (nb + 1) / 2, q0 = rank == 0 ? 0 : half, q1 = rank == 0 ? half : nb;
         // conv: the unit's box sources (at most two column boxes per CTA) and the
         // output position (n, h, w) of the k-block's first patch row, stepped by 64
-        SyConvBox bx[4];
-        SyConvGeom g{};
+        ConvBox bx[4];
+        ConvGeom g{};
         int n = 0, h = 0, w = 0;
         if constexpr (kConv) {
           g = prm.in.g[un.prob];
-          bx[0] = sy_conv_box_source(g, un.i * 2);
-          bx[1] = sy_conv_box_source(g, un.i * 2 + 1);
-          bx[2] = sy_conv_box_source(g, (int)(un.j0 / 64) + q0);
-          bx[3] = sy_conv_box_source(g, (int)(un.j0 / 64) + q0 + 1);
+          bx[0] = conv_box_source(g, un.i * 2);
+          bx[1] = conv_box_source(g, un.i * 2 + 1);
+          bx[2] = conv_box_source(g, (int)(un.j0 / 64) + q0);
+          bx[3] = conv_box_source(g, (int)(un.j0 / 64) + q0 + 1);
         }
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
@@ -238,17 +216,7 @@ __global__ void __launch_bounds__(192, 1) syrk_tc_kernel(const __grid_constant__
             if (q1 > q0) sy_conv_load<true>(prm, un.prob, bx[2], n, h, w, rem, sb + q0 * kSyBox, &full[stage]);
             if (q1 > q0 + 1)
               sy_conv_load<true>(prm, un.prob, bx[3], n, h, w, rem, sb + (q0 + 1) * kSyBox, &full[stage]);
-            w += g.sw;
-            if (w >= g.W) {
-              w -= g.W;
-              ++h;
-            }
-            h += g.sh;
-            if (h >= g.H) {
-              h -= g.H;
-              ++n;
-            }
-            n += g.sn;
+            conv_step(g, n, h, w);
           } else {
             tma_load_3d(sa, map, un.i * 128, kb * kSyBK, un.p, &full[stage]);
             tma_load_3d(sa + kSyBox, map, un.i * 128 + 64, kb * kSyBK, un.p, &full[stage]);
@@ -620,9 +588,7 @@ int launch_conv_factors(int n, const kfac_conv_factor_args* args, int P, int mir
       const int st = sy_set_output(enc, &prm.omaps[k], prm.probs[k], a.out + (long long)p * a.stride_out, d,
                                    a.ld_out, 0, 1, rows_p, a.scale, units);
       if (st != KFAC_OK) return st;
-      const int steps_w = (int)(kSyBK / a.W);  // 64 = sn H W + sh W + sw
-      prm.in.g[k] = SyConvGeom{(int)(a.C / 64), (int)a.H,       (int)a.W, (int)(kSyBK % a.W),
-                               (int)(steps_w % a.H), (int)(steps_w / a.H)};
+      prm.in.g[k] = make_conv_geom((int)a.C, (int)a.H, (int)a.W, kSyBK);
       work += 2.0 * (double)rows_p * (double)d * ((double)d + 1.0) / 2.0;
     }
     prm.n_probs = cnt;

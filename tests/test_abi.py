@@ -8,6 +8,7 @@ import re
 import subprocess
 import tempfile
 
+import numpy as np
 import pytest
 
 import oracle
@@ -269,3 +270,88 @@ def test_profile_api_without_launches():
     capi.kfac_profile(False)
     with pytest.raises(capi.KFACError):
         capi.kfac_profile_read(len(capi.KERNEL_KINDS))
+
+
+def _run_host_program(src):
+    csrc = os.path.join(ROOT, "infra_fac_factors_gb300", "csrc")
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "t.cpp")
+        exe = os.path.join(td, "t")
+        open(c, "w").write(src)
+        subprocess.run(["g++", "-O2", "-std=c++17", "-D__host__=", "-D__device__=", "-I", csrc, c, "-o", exe],
+                       check=True)
+        return subprocess.run([exe], capture_output=True, text=True, check=True).stdout
+
+
+def test_conv_kblock_positions_equal_division():
+    # the conv factor kernel steps each k-block's first output position by 64
+    # with carries; it must equal (n, h, w) = divmod of the row index, for every
+    # image size up to 70 x 70 and a few wide / tall ones, over 40 k-blocks past
+    # a worker's last image
+    src = r"""
+#include <cstdio>
+#include "conv_geom.cuh"
+using namespace kfac;
+int main() {
+  long long bad = 0, n_checked = 0;
+  auto check = [&](int H, int W) {
+    const ConvGeom g = make_conv_geom(64, H, W, 64);
+    int n = 0, h = 0, w = 0;
+    const long long hw = (long long)H * W;
+    const long long blocks = (3 * hw + 63) / 64 + 40;
+    for (long long kb = 0; kb < blocks; ++kb, ++n_checked) {
+      const long long lp = kb * 64;
+      bad += (n != lp / hw || h != (lp % hw) / W || w != lp % W);
+      conv_step(g, n, h, w);
+    }
+  };
+  for (int H = 1; H <= 70; ++H)
+    for (int W = 1; W <= 70; ++W) check(H, W);
+  const int odd[][2] = {{1, 1000}, {1000, 1}, {3, 4097}, {224, 224}, {2, 63}, {2, 65}};
+  for (auto& s : odd) check(s[0], s[1]);
+  printf("%lld %lld\n", n_checked, bad);
+  return 0;
+}
+"""
+    n, bad = map(int, _run_host_program(src).split())
+    assert n > 100000 and bad == 0
+
+
+@pytest.mark.parametrize("C", [64, 128, 192, 512])
+def test_conv_box_sources_follow_the_oracle_patch_columns(C):
+    # box q of the patch matrix: the (tap, first channel) the kernel loads for
+    # it, checked column by column against oracle.im2col3x3 on an image whose
+    # every pixel value encodes its (h, w, c)
+    src = r"""
+#include <cstdio>
+#include "conv_geom.cuh"
+using namespace kfac;
+int main() {
+  const int C = %d;
+  const ConvGeom g = make_conv_geom(C, 1, 1, 64);
+  for (int q = 0; q < 9 * C / 64 + 3; ++q) {
+    const ConvBox b = conv_box_source(g, q);
+    printf("%%d %%d %%d %%d %%d\n", q, b.kind, b.dh, b.dw, b.c0);
+  }
+  return 0;
+}
+""" % C
+    boxes = [tuple(map(int, l.split())) for l in _run_host_program(src).strip().splitlines()]
+    H = W = 3
+    x = np.zeros((1, H, W, C))
+    for h in range(H):
+        for w in range(W):
+            x[0, h, w, :] = 1 + (h * W + w) * C + np.arange(C)  # distinct, non-zero
+    X = oracle.im2col3x3(x)[H * W // 2]  # the centre position sees all nine taps inside the image
+    d = 9 * C + 1
+    for q, kind, dh, dw, c0 in boxes:
+        for j in range(64):
+            col = 64 * q + j
+            if kind == 0:
+                assert col < 9 * C
+                want = x[0, 1 + dh - 1, 1 + dw - 1, c0 + j]
+                assert X[col] == want, (q, j)
+            elif kind == 1:
+                assert 64 * q == 9 * C and (X[col] == 1.0 if j == 0 else col >= d)
+            else:
+                assert 64 * q > 9 * C
