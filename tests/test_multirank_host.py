@@ -61,3 +61,14 @@ def test_single_process_without_group_is_identity():
     assert not dist.is_initialized()
     assert bench.max_over_ranks(3.25) == 3.25
     assert bench.job_ms_per_step(8.0, 1) == 8.0
+
+
+def test_bench_tables_cover_every_profiled_kernel_kind():
+    # the bench reads every kind of the library's launch profile: each needs a
+    # kernel name for the roofline line and, if tensor-bound, its MMA count
+    sys.path.insert(0, ROOT)
+    import bench
+    from infra_fac_factors_gb300 import capi
+
+    assert set(bench.KERNEL_NAMES) == set(capi.KERNEL_KINDS)
+    assert set(bench.ISSUED_PER_ALGORITHMIC) == set(capi.KERNEL_KINDS) - {"running"}
