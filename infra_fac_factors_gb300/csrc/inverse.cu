@@ -185,14 +185,14 @@ __global__ void __launch_bounds__(256) inv_panel_kernel(InvCtx c, int k) {
         T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
         Opnd<T> A{Lrk, np, 1, 128};
         Opnd<T> B{winv, np, 1, 128};
-        simt_tile<T, T, T>(acc, A, B, 128, smem);
+        simt_tile_df(acc, A, B, 128, smem);
         tile_store(Lrk, np, acc, 0);
       } else {
         const int cc = q - nr;
         T* Ckc = W + (long long)k * 128 * np + (long long)cc * 128;
         Opnd<T> A{winv, np, 1, 128};
         Opnd<T> B{Ckc, 1, np, 128};
-        simt_tile<T, T, T>(acc, A, B, 128, smem);
+        simt_tile_df(acc, A, B, 128, smem);
         tile_store(Ckc, np, acc, 0);
       }
     }
@@ -221,11 +221,11 @@ __global__ void __launch_bounds__(256) inv_update_kernel(InvCtx c, int k) {
       Opnd<T> A{Lrk, np, 1, 128};
       if (cc > k) {
         Opnd<T> B{L + (long long)cc * 128 * np + (long long)k * 128, np, 1, 128};
-        simt_tile<T, T, T>(acc, A, B, 128, smem);
+        simt_tile_df(acc, A, B, 128, smem);
         tile_store(L + (long long)r * 128 * np + (long long)cc * 128, np, acc, 1);
       } else {
         Opnd<T> B{W + (long long)k * 128 * np + (long long)cc * 128, 1, np, 128};
-        simt_tile<T, T, T>(acc, A, B, 128, smem);
+        simt_tile_df(acc, A, B, 128, smem);
         tile_store(W + (long long)r * 128 * np + (long long)cc * 128, np, acc, cc == k ? 2 : 1);
       }
     }
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
       zero_acc(acc);
       Opnd<T> A{W + (long long)j * 128 * np + (long long)i * 128, 1, np, 128};
       Opnd<T> B{W + (long long)j * 128 * np + (long long)j * 128, 1, np, 128};
-      simt_tile<T, T, T>(acc, A, B, (int)(np - (long long)j * 128), smem);
+      simt_tile_df(acc, A, B, (int)(np - (long long)j * 128), smem);
 #pragma unroll
       for (int a = 0; a < 8; ++a) {
         const int mm = ty * 8 + a;

@@ -163,4 +163,104 @@ __device__ void simt_tile(T (&acc)[8][8], const Opnd<TinA>& A, const Opnd<TinB>&
   __syncthreads();
 }
 
+// out = A Bᵀ for fp64 operands, in double-float arithmetic on the fp32 pipes
+// (the part's fp64 rate is a small fraction of its fp32 rate).  Operands are
+// staged as (hi, lo) float pairs, hi = fl32(x), lo = fl32(x - hi) (about 48
+// significant bits); each multiply-add keeps the exact error of the product
+// hi_a hi_b (an FMA, after Dekker's two-product) and of its addition to the
+// running sum (Knuth's two-sum), and adds the cross terms hi_a lo_b + lo_a hi_b
+// to the low word.  The error grows like K 2^-48 relative to the largest
+// term, against K 2^-53 in fp64: ample for the inverse's fp64 pass, whose
+// target is a residual of 1e-3 at condition numbers near 1e6.
+// smem: simt_smem_bytes<double>() bytes.  All 256 threads must call.
+__device__ __forceinline__ float2 df_split(double x) {
+  const float hi = (float)x;
+  return make_float2(hi, (float)(x - (double)hi));
+}
+
+__device__ __forceinline__ void df_fetch(float2 (&reg)[(SimtCfg<double>::KC * 128) / 256], const Opnd<double>& o,
+                                         int k0, int K) {
+  double v[(SimtCfg<double>::KC * 128) / 256];
+  fetch_slab<double, double>(v, o, k0, K);
+#pragma unroll
+  for (int j = 0; j < (SimtCfg<double>::KC * 128) / 256; ++j) reg[j] = df_split(v[j]);
+}
+
+__device__ __forceinline__ void df_store(float2* S, const float2 (&reg)[(SimtCfg<double>::KC * 128) / 256],
+                                         const Opnd<double>& o) {
+  constexpr int KC = SimtCfg<double>::KC;
+  constexpr int PITCH = SimtCfg<double>::PITCH;
+  constexpr int EPT = (KC * 128) / 256;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    const int e = tid + 256 * j;
+    if (o.sk == 1)
+      S[(e % KC) * PITCH + e / KC] = reg[j];
+    else
+      S[(e / 128) * PITCH + e % 128] = reg[j];
+  }
+}
+
+__device__ __forceinline__ void lds8_df(const float2* p, float2 (&v)[8]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 x = *reinterpret_cast<const float4*>(p + 2 * q);
+    v[2 * q] = make_float2(x.x, x.y);
+    v[2 * q + 1] = make_float2(x.z, x.w);
+  }
+}
+
+__device__ inline void simt_tile_df(double (&out)[8][8], const Opnd<double>& A, const Opnd<double>& B, int K, double* smem) {
+  constexpr int KC = SimtCfg<double>::KC;
+  constexpr int PITCH = SimtCfg<double>::PITCH;
+  constexpr int EPT = (KC * 128) / 256;
+  float2* SA = reinterpret_cast<float2*>(smem);
+  float2* SB = SA + KC * PITCH;
+  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  float hi[8][8], lo[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) hi[i][j] = lo[i][j] = 0.f;
+  float2 ra[EPT], rb[EPT];
+  if (K > 0) {
+    df_fetch(ra, A, 0, K);
+    df_fetch(rb, B, 0, K);
+  }
+  for (int k0 = 0; k0 < K; k0 += KC) {
+    __syncthreads();
+    df_store(SA, ra, A);
+    df_store(SB, rb, B);
+    __syncthreads();
+    if (k0 + KC < K) {
+      df_fetch(ra, A, k0 + KC, K);
+      df_fetch(rb, B, k0 + KC, K);
+    }
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      float2 a[8], b[8];
+      lds8_df(SA + k * PITCH + ty * 8, a);
+      lds8_df(SB + k * PITCH + tx * 8, b);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float p = a[i].x * b[j].x;
+          const float pe = fmaf(a[i].x, b[j].x, -p);  // hi_a hi_b - p, exactly
+          const float s = hi[i][j] + p;
+          const float bb = s - hi[i][j];
+          const float e = (hi[i][j] - (s - bb)) + (p - bb);  // hi + p - s, exactly
+          hi[i][j] = s;
+          lo[i][j] += e + fmaf(a[i].x, b[j].y, fmaf(a[i].y, b[j].x, pe));
+        }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) out[i][j] = (double)hi[i][j] + (double)lo[i][j];
+}
+
 }  // namespace kfac
