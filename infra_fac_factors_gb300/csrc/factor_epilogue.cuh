@@ -1,5 +1,5 @@
-// Epilogue of the tensor-core factor kernels (the linear-layer SYRK in
-// factors.cu and the implicit-im2col conv variant in conv_factors.cu).
+// Epilogue of the tensor-core factor SYRK (factors.cu: both its linear-layer
+// and its implicit-im2col conv instantiation).
 //
 // One epilogue warp owns TMEM lane quarter q, i.e. rows i*128 + 32q .. +31 of
 // a work unit (row block i, columns [j0, j0 + w) of the tile map in
