@@ -145,12 +145,12 @@ __global__ void __launch_bounds__(256, 1) inv_diag_kernel(InvCtx c, int k) {
 
 // ------------------------------------------------------------------ tile epilogues
 template <typename T>
-__device__ __forceinline__ void tile_store(T* dst, long long ld, const T (&acc)[8][8], int mode) {
-  // mode 0: dst = acc, 1: dst -= acc, 2: dst = -acc
+__device__ __forceinline__ void tile_store(T* dst, long long ld, const T (&acc)[4][8], int mode) {
+  // mode 0: dst = acc, 1: dst -= acc, 2: dst = -acc (simt_tile_df's thread layout)
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
 #pragma unroll
-  for (int a = 0; a < 8; ++a) {
-    T* row = dst + (long long)(ty * 8 + a) * ld + tx * 8;
+  for (int a = 0; a < 4; ++a) {
+    T* row = dst + (long long)(ty * 4 + a) * ld + tx * 8;
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       if (mode == 0)
@@ -165,7 +165,7 @@ __device__ __forceinline__ void tile_store(T* dst, long long ld, const T (&acc)[
 
 // ------------------------------------------------------------------ fp64 pass: panel
 template <typename T>
-__global__ void __launch_bounds__(256) inv_panel_kernel(InvCtx c, int k) {
+__global__ void __launch_bounds__(kDfThreads) inv_panel_kernel(InvCtx c, int k) {
   __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
   const int nf = *c.nflagged;
   for (int f = 0; f < nf; ++f) {
@@ -178,8 +178,7 @@ __global__ void __launch_bounds__(256) inv_panel_kernel(InvCtx c, int k) {
     T* W = wbuf<T>(c, m);
     const T* winv = W + (long long)k * 128 * np + (long long)k * 128;
     for (int q = blockIdx.x; q < nr + k; q += gridDim.x) {
-      T acc[8][8];
-      zero_acc(acc);
+      T acc[4][8];
       if (q < nr) {
         const int r = k + 1 + q;
         T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
@@ -201,7 +200,7 @@ __global__ void __launch_bounds__(256) inv_panel_kernel(InvCtx c, int k) {
 
 // ------------------------------------------------------------------ fp64 pass: trailing update
 template <typename T>
-__global__ void __launch_bounds__(256) inv_update_kernel(InvCtx c, int k) {
+__global__ void __launch_bounds__(kDfThreads) inv_update_kernel(InvCtx c, int k) {
   __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
   const int nf = *c.nflagged;
   for (int f = 0; f < nf; ++f) {
@@ -216,8 +215,7 @@ __global__ void __launch_bounds__(256) inv_update_kernel(InvCtx c, int k) {
       const int r = tri_root(qq);
       const int cc = (int)(qq - tri(r));
       const T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
-      T acc[8][8];
-      zero_acc(acc);
+      T acc[4][8];
       Opnd<T> A{Lrk, np, 1, 128};
       if (cc > k) {
         Opnd<T> B{L + (long long)cc * 128 * np + (long long)k * 128, np, 1, 128};
@@ -234,7 +232,7 @@ __global__ void __launch_bounds__(256) inv_update_kernel(InvCtx c, int k) {
 
 // ------------------------------------------------------------------ fp64 pass: X = W^T W
 template <typename T>
-__global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
+__global__ void __launch_bounds__(kDfThreads) inv_lauum_kernel(InvCtx c) {
   __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
   const int nf = *c.nflagged;
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
@@ -247,14 +245,13 @@ __global__ void __launch_bounds__(256) inv_lauum_kernel(InvCtx c) {
     for (long long q = blockIdx.x; q < tri(m.T); q += gridDim.x) {
       const int j = tri_root(q);
       const int i = (int)(q - tri(j));  // i <= j
-      T acc[8][8];
-      zero_acc(acc);
+      T acc[4][8];
       Opnd<T> A{W + (long long)j * 128 * np + (long long)i * 128, 1, np, 128};
       Opnd<T> B{W + (long long)j * 128 * np + (long long)j * 128, 1, np, 128};
       simt_tile_df(acc, A, B, (int)(np - (long long)j * 128), smem);
 #pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        const int mm = ty * 8 + a;
+      for (int a = 0; a < 4; ++a) {
+        const int mm = ty * 4 + a;
         const long long row = (long long)i * 128 + mm;
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
@@ -392,15 +389,15 @@ static int run_fp64_pass(const InvCtx& ctx, int Tmax, cudaStream_t stream) {
     inv_diag_kernel<double><<<sms, 256, dsm, stream>>>(ctx, k);
     count_launch();
     if (Tmax > 1) {
-      inv_panel_kernel<double><<<sms, 256, 0, stream>>>(ctx, k);
+      inv_panel_kernel<double><<<sms, kDfThreads, 0, stream>>>(ctx, k);
       count_launch();
       if (k + 1 < Tmax) {
-        inv_update_kernel<double><<<sms, 256, 0, stream>>>(ctx, k);
+        inv_update_kernel<double><<<sms, kDfThreads, 0, stream>>>(ctx, k);
         count_launch();
       }
     }
   }
-  inv_lauum_kernel<double><<<sms, 256, 0, stream>>>(ctx);
+  inv_lauum_kernel<double><<<sms, kDfThreads, 0, stream>>>(ctx);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }

@@ -172,29 +172,38 @@ __device__ void simt_tile(T (&acc)[8][8], const Opnd<TinA>& A, const Opnd<TinB>&
 // to the low word.  The error grows like K 2^-48 relative to the largest
 // term, against K 2^-53 in fp64: ample for the inverse's fp64 pass, whose
 // target is a residual of 1e-3 at condition numbers near 1e6.
-// smem: simt_smem_bytes<double>() bytes.  All 256 threads must call.
+// kDfThreads threads; thread (ty, tx) = (tid / 16, tid % 16) owns rows
+// ty*4 .. ty*4+3 and columns tx*8 .. tx*8+7 of the tile (two words per value
+// double the accumulator registers, so each thread holds half the values of
+// simt_tile's and twice as many warps share an SM).
+// smem: simt_smem_bytes<double>() bytes.  All kDfThreads threads must call.
+constexpr int kDfThreads = 512;
+constexpr int kDfEpt = (SimtCfg<double>::KC * 128) / kDfThreads;  // staged values per thread and operand
+
 __device__ __forceinline__ float2 df_split(double x) {
   const float hi = (float)x;
   return make_float2(hi, (float)(x - (double)hi));
 }
 
-__device__ __forceinline__ void df_fetch(float2 (&reg)[(SimtCfg<double>::KC * 128) / 256], const Opnd<double>& o,
-                                         int k0, int K) {
-  double v[(SimtCfg<double>::KC * 128) / 256];
-  fetch_slab<double, double>(v, o, k0, K);
-#pragma unroll
-  for (int j = 0; j < (SimtCfg<double>::KC * 128) / 256; ++j) reg[j] = df_split(v[j]);
-}
-
-__device__ __forceinline__ void df_store(float2* S, const float2 (&reg)[(SimtCfg<double>::KC * 128) / 256],
-                                         const Opnd<double>& o) {
+__device__ __forceinline__ void df_fetch(float2 (&reg)[kDfEpt], const Opnd<double>& o, int k0, int K) {
   constexpr int KC = SimtCfg<double>::KC;
-  constexpr int PITCH = SimtCfg<double>::PITCH;
-  constexpr int EPT = (KC * 128) / 256;
   const int tid = threadIdx.x;
 #pragma unroll
-  for (int j = 0; j < EPT; ++j) {
-    const int e = tid + 256 * j;
+  for (int j = 0; j < kDfEpt; ++j) {
+    const int e = tid + kDfThreads * j;
+    const int k = o.sk == 1 ? e % KC : e / 128, m = o.sk == 1 ? e / KC : e % 128;
+    const int kk = k0 + k;
+    reg[j] = df_split((m < o.mv && kk < K) ? o.p[(int64_t)m * o.sm + (int64_t)kk * o.sk] : 0.0);
+  }
+}
+
+__device__ __forceinline__ void df_store(float2* S, const float2 (&reg)[kDfEpt], const Opnd<double>& o) {
+  constexpr int KC = SimtCfg<double>::KC;
+  constexpr int PITCH = SimtCfg<double>::PITCH;
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < kDfEpt; ++j) {
+    const int e = tid + kDfThreads * j;
     if (o.sk == 1)
       S[(e % KC) * PITCH + e / KC] = reg[j];
     else
@@ -202,28 +211,29 @@ __device__ __forceinline__ void df_store(float2* S, const float2 (&reg)[(SimtCfg
   }
 }
 
-__device__ __forceinline__ void lds8_df(const float2* p, float2 (&v)[8]) {
+template <int N>
+__device__ __forceinline__ void lds_df(const float2* p, float2 (&v)[N]) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < N / 2; ++q) {
     const float4 x = *reinterpret_cast<const float4*>(p + 2 * q);
     v[2 * q] = make_float2(x.x, x.y);
     v[2 * q + 1] = make_float2(x.z, x.w);
   }
 }
 
-__device__ inline void simt_tile_df(double (&out)[8][8], const Opnd<double>& A, const Opnd<double>& B, int K, double* smem) {
+__device__ inline void simt_tile_df(double (&out)[4][8], const Opnd<double>& A, const Opnd<double>& B, int K,
+                                    double* smem) {
   constexpr int KC = SimtCfg<double>::KC;
   constexpr int PITCH = SimtCfg<double>::PITCH;
-  constexpr int EPT = (KC * 128) / 256;
   float2* SA = reinterpret_cast<float2*>(smem);
   float2* SB = SA + KC * PITCH;
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-  float hi[8][8], lo[8][8];
+  float hi[4][8], lo[4][8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) hi[i][j] = lo[i][j] = 0.f;
-  float2 ra[EPT], rb[EPT];
+  float2 ra[kDfEpt], rb[kDfEpt];
   if (K > 0) {
     df_fetch(ra, A, 0, K);
     df_fetch(rb, B, 0, K);
@@ -239,11 +249,11 @@ __device__ inline void simt_tile_df(double (&out)[8][8], const Opnd<double>& A, 
     }
 #pragma unroll
     for (int k = 0; k < KC; ++k) {
-      float2 a[8], b[8];
-      lds8_df(SA + k * PITCH + ty * 8, a);
-      lds8_df(SB + k * PITCH + tx * 8, b);
+      float2 a[4], b[8];
+      lds_df<4>(SA + k * PITCH + ty * 4, a);
+      lds_df<8>(SB + k * PITCH + tx * 8, b);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float p = a[i].x * b[j].x;
@@ -258,7 +268,7 @@ __device__ inline void simt_tile_df(double (&out)[8][8], const Opnd<double>& A, 
   }
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 8; ++j) out[i][j] = (double)hi[i][j] + (double)lo[i][j];
 }
