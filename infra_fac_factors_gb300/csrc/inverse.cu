@@ -242,7 +242,13 @@ __global__ void __launch_bounds__(kDfThreads) inv_lauum_kernel(InvCtx c) {
     if (c.st[mi].failed) continue;
     const long long np = (long long)m.T * 128;
     const T* W = wbuf<T>(c, m);
-    for (long long q = blockIdx.x; q < tri(m.T); q += gridDim.x) {
+    // Jobs come longest first (K = np - 128 j falls with j); CTA b takes job b
+    // of even rounds and job G - 1 - b of odd ones, so that long and short
+    // jobs pair up on each CTA.
+    const long long G = gridDim.x, njobs = tri(m.T);
+    for (long long round = 0; round * G < njobs; ++round) {
+      const long long q = round * G + ((round & 1) ? G - 1 - blockIdx.x : blockIdx.x);
+      if (q >= njobs) continue;
       const int j = tri_root(q);
       const int i = (int)(q - tri(j));  // i <= j
       T acc[4][8];
