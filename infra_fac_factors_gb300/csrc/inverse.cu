@@ -199,8 +199,10 @@ __global__ void __launch_bounds__(kDfThreads) inv_panel_kernel(InvCtx c, int k) 
 }
 
 // ------------------------------------------------------------------ fp64 pass: trailing update
+// part 0: every job; part 1: the jobs step k + 1 reads (block row k + 1 of W
+// and of L, block column k + 1 of L: m.T jobs); part 2: the others.
 template <typename T>
-__global__ void __launch_bounds__(kDfThreads) inv_update_kernel(InvCtx c, int k) {
+__global__ void __launch_bounds__(kDfThreads) inv_update_kernel(InvCtx c, int k, int part) {
   __shared__ __align__(16) T smem[simt_smem_bytes<T>() / sizeof(T)];
   const int nf = *c.nflagged;
   for (int f = 0; f < nf; ++f) {
@@ -210,10 +212,18 @@ __global__ void __launch_bounds__(kDfThreads) inv_update_kernel(InvCtx c, int k)
     const long long np = (long long)m.T * 128;
     T* L = lbuf<T>(c, m);
     T* W = wbuf<T>(c, m);
-    for (long long q = blockIdx.x; q < tri(m.T) - tri(k + 1); q += gridDim.x) {
-      const long long qq = q + tri(k + 1);
-      const int r = tri_root(qq);
-      const int cc = (int)(qq - tri(r));
+    const long long njobs = part == 1 ? m.T : tri(m.T) - tri(k + 1);
+    for (long long q = blockIdx.x; q < njobs; q += gridDim.x) {
+      int r, cc;
+      if (part == 1) {
+        r = q <= k + 1 ? k + 1 : (int)q;
+        cc = q <= k + 1 ? (int)q : k + 1;
+      } else {
+        const long long qq = q + tri(k + 1);
+        r = tri_root(qq);
+        cc = (int)(qq - tri(r));
+        if (part == 2 && (r == k + 1 || cc == k + 1)) continue;
+      }
       const T* Lrk = L + (long long)r * 128 * np + (long long)k * 128;
       T acc[4][8];
       Opnd<T> A{Lrk, np, 1, 128};
@@ -391,17 +401,46 @@ static int run_fp64_pass(const InvCtx& ctx, int Tmax, cudaStream_t stream) {
   if (!ensure_smem_attr(dev, (const void*)inv_diag_kernel<double>, dsm)) return KFAC_ERR_CUDA;
   inv_load_kernel<double><<<sms, 256, 0, stream>>>(ctx);
   count_launch();
+  // Look-ahead: step k's chain (diagonal block, panel, and the part of the
+  // trailing update that step k + 1 reads) runs on the high-priority stream;
+  // the rest of the update runs on the caller's stream, one job per CTA so
+  // that SMs come free for the chain, beside the next steps' chain.
+  cudaStream_t chain = nullptr;
+  cudaEvent_t ev[4];
+  const bool split = Tmax > 2 && fp64_chain_stream(dev, stream, &chain, ev);
+  if (split) {
+    if (cudaEventRecord(ev[0], stream) != cudaSuccess || cudaStreamWaitEvent(chain, ev[0], 0) != cudaSuccess)
+      return KFAC_ERR_CUDA;
+  }
+  cudaStream_t cs = split ? chain : stream;
   for (int k = 0; k < Tmax; ++k) {
-    inv_diag_kernel<double><<<sms, 256, dsm, stream>>>(ctx, k);
+    inv_diag_kernel<double><<<sms, 256, dsm, cs>>>(ctx, k);
     count_launch();
     if (Tmax > 1) {
-      inv_panel_kernel<double><<<sms, kDfThreads, 0, stream>>>(ctx, k);
+      inv_panel_kernel<double><<<sms, kDfThreads, 0, cs>>>(ctx, k);
       count_launch();
       if (k + 1 < Tmax) {
-        inv_update_kernel<double><<<sms, kDfThreads, 0, stream>>>(ctx, k);
+        if (!split) {
+          inv_update_kernel<double><<<sms, kDfThreads, 0, stream>>>(ctx, k, 0);
+          count_launch();
+          continue;
+        }
+        // the far update of step k - 1 has written block row and column k + 1
+        if (k > 0 && cudaStreamWaitEvent(chain, ev[2], 0) != cudaSuccess) return KFAC_ERR_CUDA;
+        inv_update_kernel<double><<<Tmax, kDfThreads, 0, chain>>>(ctx, k, 1);
         count_launch();
+        if (cudaEventRecord(ev[1], chain) != cudaSuccess || cudaStreamWaitEvent(stream, ev[1], 0) != cudaSuccess)
+          return KFAC_ERR_CUDA;
+        const long long far = tri(Tmax) - tri(k + 1);
+        inv_update_kernel<double><<<(unsigned)(far > 0 ? far : 1), kDfThreads, 0, stream>>>(ctx, k, 2);
+        count_launch();
+        if (cudaEventRecord(ev[2], stream) != cudaSuccess) return KFAC_ERR_CUDA;
       }
     }
+  }
+  if (split) {
+    if (cudaEventRecord(ev[3], chain) != cudaSuccess || cudaStreamWaitEvent(stream, ev[3], 0) != cudaSuccess)
+      return KFAC_ERR_CUDA;
   }
   inv_lauum_kernel<double><<<sms, kDfThreads, 0, stream>>>(ctx);
   count_launch();

@@ -1004,6 +1004,17 @@ static bool aux_stream(int dev, cudaStream_t caller, AuxStream* out) {
   return true;
 }
 
+bool fp64_chain_stream(int dev, cudaStream_t caller, cudaStream_t* chain, cudaEvent_t (&ev)[4]) {
+  AuxStream aux;
+  if (!aux_stream(dev, caller, &aux)) return false;
+  *chain = aux.hi;
+  ev[0] = aux.start;
+  ev[1] = aux.fork;
+  ev[2] = aux.join;
+  ev[3] = aux.end;
+  return true;
+}
+
 // Jobs per CTA of a far update: its CTAs retire every few jobs, so that the
 // higher-priority chain on the other stream finds SMs within tens of us.
 constexpr int kFarJobsPerCta = 4;

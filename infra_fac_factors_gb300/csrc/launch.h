@@ -44,6 +44,10 @@ int launch_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw, int6
 int launch_update_running(int n, const kfac_running_args* args, int P, float decay, float gamma, int first_step,
                           cudaStream_t stream);
 size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine);
+// The high-priority stream of the caller's auxiliary set (the fp32 sweep's)
+// and four of its events, for the fp64 pass that follows the fp32 pass in
+// the same call on the same caller stream.
+bool fp64_chain_stream(int dev, cudaStream_t caller, cudaStream_t* chain, cudaEvent_t (&ev)[4]);
 int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra, int refine, int* info, int* route,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 size_t precondition_workspace(int n, const kfac_precond_args* args);
