@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "dfloat.cuh"
 
 namespace kfac {
 
