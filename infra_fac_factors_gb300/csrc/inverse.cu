@@ -108,12 +108,10 @@ __global__ void __launch_bounds__(256) inv_load_kernel(InvCtx c) {
 }
 
 // ------------------------------------------------------------------ fp64 pass: diagonal block
-// The block is factored in double-float arithmetic (DF, on the fp32 pipes);
-// the buffers stay fp64.
 template <typename T>
 __global__ void __launch_bounds__(256, 1) inv_diag_kernel(InvCtx c, int k) {
   extern __shared__ __align__(16) uint8_t diag_smem[];
-  DF* a = reinterpret_cast<DF*>(diag_smem);
+  T* a = reinterpret_cast<T*>(diag_smem);
   const int nf = *c.nflagged;
   const int t = threadIdx.x;
   for (int f = blockIdx.x; f < nf; f += gridDim.x) {
@@ -124,11 +122,11 @@ __global__ void __launch_bounds__(256, 1) inv_diag_kernel(InvCtx c, int k) {
     const T* src = lbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
     for (int e = t; e < 128 * 128; e += blockDim.x) {
       const int r = e / 128, col = e % 128;
-      a[r * kDiagPitch + col] = DF((col <= r) ? (double)src[(long long)r * np + col] : 0.0);
+      a[r * kDiagPitch + col] = (col <= r) ? src[(long long)r * np + col] : T(0);
     }
     __syncthreads();
-    DF min_piv;
-    const int fail = block_chol_inv<DF>(a, m.d - k * 128, min_piv);
+    T min_piv;
+    const int fail = block_chol_inv<T>(a, m.d - k * 128, min_piv);
     if (fail >= 0) {
       if (t == 0) {
         c.st[mi].failed = 1;
@@ -138,7 +136,7 @@ __global__ void __launch_bounds__(256, 1) inv_diag_kernel(InvCtx c, int k) {
       T* dst = wbuf<T>(c, m) + (long long)k * 128 * np + (long long)k * 128;
       for (int e = t; e < 128 * 128; e += blockDim.x) {
         const int r = e / 128, col = e % 128;
-        dst[(long long)r * np + col] = (col <= r) ? (T)(double)a[r * kDiagPitch + col] : T(0);
+        dst[(long long)r * np + col] = (col <= r) ? a[r * kDiagPitch + col] : T(0);
       }
     }
     __syncthreads();

@@ -5,7 +5,6 @@
 #include <stdint.h>
 
 #include "common.cuh"
-#include "dfloat.cuh"
 
 namespace kfac {
 
