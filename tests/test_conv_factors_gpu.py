@@ -219,3 +219,23 @@ def test_step_resnet_conv_workload_from_images():
         images.append((B, H, W, C))
         specs.append(LayerSpec(layer.d_in, layer.d_out, cfg.rows(layer), cfg.batch, layer.hw, image=(H, W)))
     run_step_and_check(specs, images, cfg.P, cfg.gamma, 0.0, 1, cfg.g_sigma, seed=2)
+
+
+def test_conv_factors_more_problems_than_one_launch_holds():
+    # 13 layers x 8 workers = 104 (layer, worker) problems: two launches
+    P = 8
+    shapes = [(8, 2 + k % 3, 3 + k % 2, 64 * (1 + k % 2)) for k in range(13)]
+    xs, outs, args = [], [], []
+    for k, sh in enumerate(shapes):
+        x = synth.conv_activations(sh, ("many", k))
+        d = 9 * sh[3] + 1
+        ldo = pad(d, 4)
+        xt = torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+        out = torch.full((P, d, ldo), float("nan"), dtype=torch.float32, device="cuda")
+        xs.append((x, xt))
+        outs.append(out)
+        args.append(conv_args(xt, sh, out, ldo, P))
+    capi.kfac_conv_factors(args, P, 0, stream())
+    sync()
+    for (x, _), out in zip(xs, outs):
+        check_upper(out.cpu().numpy(), x, P)
