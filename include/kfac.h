@@ -14,8 +14,11 @@
  *
  * Conventions shared by every call
  *   - All matrices are row-major.  "ld" is the leading dimension in elements.
- *   - Every data pointer is a DEVICE pointer, 16-byte aligned.  Every array of
- *     argument structs is a HOST array that is read during the call only.
+ *   - Every data pointer is a DEVICE pointer into memory of the CURRENT
+ *     device (cudaMemoryTypeDevice), 16-byte aligned; host, host-mapped,
+ *     managed and peer pointers are refused with KFAC_ERR_INVALID_ARG before
+ *     any launch.  Every array of argument structs is a HOST array that is
+ *     read during the call only.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream), never synchronise the host, and never
  *     allocate device memory.  Scratch memory is caller-provided ("workspace")
@@ -231,9 +234,10 @@ int kfac_update_running(int n, const kfac_running_args* args, int P,
  * from `stream` after the work already queued there and joined back into
  * `stream` before the call returns, so ordering on `stream` is as for a
  * single-stream call.  Each caller stream gets its own set (up to four per
- * device; further caller streams share the first set), so inverses issued on
- * different streams overlap.  A set is not meant for concurrent calls from
- * several host threads on the same caller stream.                           */
+ * device), so inverses issued on different streams overlap; calls on further
+ * caller streams run on their own stream alone (the same results, without the
+ * look-ahead).  A set is not meant for concurrent calls from several host
+ * threads on the same caller stream.                                         */
 enum kfac_refine { KFAC_REFINE_NONE = 0, KFAC_REFINE_AUTO = 1, KFAC_REFINE_ALWAYS = 2 };
 
 typedef struct {
@@ -308,7 +312,9 @@ int kfac_precondition(int n, const kfac_precond_args* args, int precision, int* 
  * loads the library until the process exits.  A call whose
  * kfac_precondition_workspace() exceeds it returns KFAC_ERR_WORKSPACE before
  * any launch.  The first call on a device looks up the array's address on
- * that device (cudaGetSymbolAddress), so make it before any stream capture.
+ * that device (cudaGetSymbolAddress), so make it before any stream capture;
+ * the address is kept for the process, so do not call this entry point on a
+ * device after cudaDeviceReset of that device.
  * All calls share the array and it keeps the last call's contents; calls that
  * overlap on the GPU (e.g. on two streams at once) race.  Otherwise as
  * kfac_precondition.                                                         */

@@ -4,6 +4,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 
 #include "common.cuh"
@@ -84,6 +85,30 @@ static int check_device() {
   }
   return g_cc_ok[dev] == 1 ? KFAC_OK : KFAC_ERR_UNSUPPORTED;
 }
+
+// Every data pointer of a call must lie in device memory of the current device:
+// the tensor maps the kernels load through (some with cluster multicast) must
+// cover this GPU's own memory only, and no kernel may touch host-mapped,
+// managed or peer memory.  Checked on the host before any launch.
+static bool on_device(const void* p, int dev) {
+  if (!p) return true;  // optional pointers; required ones are checked for NULL before
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // do not leave the query's error behind for the launch checks
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+static int check_pointers(std::initializer_list<const void*> ptrs) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  for (const void* p : ptrs)
+    if (!on_device(p, dev)) return KFAC_ERR_INVALID_ARG;
+  return KFAC_OK;
+}
+
+int supported_device() { return check_device(); }
 
 int* device_status_ptr();
 
@@ -180,6 +205,10 @@ int kfac_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirr
   if (n == 0) return KFAC_OK;
   const int dc = check_device();
   if (dc != KFAC_OK) return dc;
+  for (int i = 0; i < n; ++i) {
+    const int pc = check_pointers({args[i].x, args[i].out});
+    if (pc != KFAC_OK) return pc;
+  }
   return launch_factors(n, args, dtype, P, mirror, static_cast<cudaStream_t>(stream));
 }
 
@@ -200,6 +229,10 @@ int kfac_conv_factors(int n, const kfac_conv_factor_args* args, int P, int mirro
   if (n == 0) return KFAC_OK;
   const int dc = check_device();
   if (dc != KFAC_OK) return dc;
+  for (int i = 0; i < n; ++i) {
+    const int pc = check_pointers({args[i].x, args[i].out});
+    if (pc != KFAC_OK) return pc;
+  }
   return launch_conv_factors(n, args, P, mirror, static_cast<cudaStream_t>(stream));
 }
 
@@ -212,6 +245,8 @@ int kfac_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw, int64_
   if (ld_g < C || ld_g % vec != 0 || ld_gs < C || ld_gs % 4 != 0) return KFAC_ERR_INVALID_ARG;
   const int dc = check_device();
   if (dc != KFAC_OK) return dc;
+  const int pc = check_pointers({g, gs});
+  if (pc != KFAC_OK) return pc;
   return launch_spatial_sum(g, dtype, batch, hw, C, ld_g, gs, ld_gs, static_cast<cudaStream_t>(stream));
 }
 
@@ -232,6 +267,10 @@ int kfac_update_running(int n, const kfac_running_args* args, int P, float decay
   if (n == 0) return KFAC_OK;
   const int dc = check_device();
   if (dc != KFAC_OK) return dc;
+  for (int i = 0; i < n; ++i) {
+    const int pc = check_pointers({args[i].shards, args[i].running, args[i].damped});
+    if (pc != KFAC_OK) return pc;
+  }
   return launch_update_running(n, args, P, decay, gamma, first_step, static_cast<cudaStream_t>(stream));
 }
 
@@ -264,6 +303,9 @@ int kfac_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra,
   if (workspace_bytes < inverse_workspace(n, args, refine)) return KFAC_ERR_WORKSPACE;
   const int dc = check_device();
   if (dc != KFAC_OK) return dc;
+  int pc = check_pointers({info, route, workspace});
+  for (int i = 0; i < n && pc == KFAC_OK; ++i) pc = check_pointers({args[i].damped, args[i].inv});
+  if (pc != KFAC_OK) return pc;
   return launch_damped_inverse(n, args, gamma_extra, refine, info, route, workspace, workspace_bytes,
                                static_cast<cudaStream_t>(stream));
 }
@@ -306,6 +348,10 @@ int kfac_precondition(int n, const kfac_precond_args* args, int precision, int* 
   if (workspace_bytes < precondition_workspace(n, args)) return KFAC_ERR_WORKSPACE;
   const int dc = check_device();
   if (dc != KFAC_OK) return dc;
+  int pc = check_pointers({route, workspace});
+  for (int i = 0; i < n && pc == KFAC_OK; ++i)
+    pc = check_pointers({args[i].inv_g, args[i].grad, args[i].inv_a, args[i].out, args[i].weight});
+  if (pc != KFAC_OK) return pc;
   return launch_precondition(n, args, precision, route, workspace, workspace_bytes,
                              static_cast<cudaStream_t>(stream));
 }

@@ -76,7 +76,10 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
 }
 // The same box into the same shared-memory offset of every CTA of the cluster
 // in `mask`; each destination's mbarrier at `bar`'s offset receives the bytes
-// that land in that CTA.
+// that land in that CTA.  Every multicast load reads this GPU's own memory:
+// the entry points refuse any operand that is not device memory of the
+// current device before a tensor map is encoded, and the library runs in
+// one-GPU processes only.
 __device__ __forceinline__ void tma_load_3d_mc(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2,
                                                uint64_t* bar, uint16_t mask) {
   asm volatile(

@@ -958,8 +958,10 @@ struct AuxStream {
               lodone = nullptr, prep0 = nullptr, prep1 = nullptr;
 };
 // One set per (device, caller's stream), up to kAuxSets per device, so that
-// inverses issued on different streams run concurrently; further callers share
-// the first set (their work is then ordered one after the other).
+// inverses issued on different streams run concurrently.  A further caller
+// stream gets no set (false): its calls run on that stream alone, without the
+// look-ahead, since sharing a set's events between two callers would let one
+// call wait on the other's event records.
 constexpr int kAuxSets = 4;
 static bool aux_stream(int dev, cudaStream_t caller, AuxStream* out) {
   static std::mutex mu;
@@ -975,7 +977,7 @@ static bool aux_stream(int dev, cudaStream_t caller, AuxStream* out) {
       slot = i;
       owner[dev][i] = caller;
     }
-  if (slot < 0) slot = 0;
+  if (slot < 0) return false;
   AuxStream& t = table[dev][slot];
   if (!t.hi) {
     int least = 0, greatest = 0;

@@ -11,6 +11,9 @@
 namespace kfac {
 
 int device_sm_count(int dev);
+// KFAC_OK when the current device is an sm_103 part, else KFAC_ERR_UNSUPPORTED
+// (or KFAC_ERR_CUDA when the runtime cannot tell).
+int supported_device();
 int* device_status_ptr();
 // Counts every kernel launch of the library (reported by kfac_launch_count).
 void count_launch();

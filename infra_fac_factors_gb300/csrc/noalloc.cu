@@ -12,7 +12,10 @@
 // variable: every GPU that loads the library holds it until the process exits.
 // Its device address is looked up once per device (cudaGetSymbolAddress, with
 // that device current) by the first call on that device; that first call
-// should therefore come before any stream capture.  Every call shares the
+// should therefore come before any stream capture.  The address is kept for
+// the life of the process: after cudaDeviceReset the library's module is
+// loaded again and the kept address no longer holds, so a process that resets
+// a device must not call this entry point on it afterwards.  Every call shares the
 // array and it keeps the previous call's contents (nothing in it has to start
 // at zero: each call writes its scratch before reading it), so calls that
 // overlap on the GPU (for example on two streams at once) race.
@@ -57,6 +60,8 @@ int kfac_precondition_static(int n, const kfac_precond_args* args, int precision
   const size_t need = kfac_precondition_workspace(n, args);
   if (need == 0) return KFAC_ERR_INVALID_ARG;  // the query rejects invalid arguments
   if (need > kfac::kStaticScratchBytes) return KFAC_ERR_WORKSPACE;
+  const int dc = kfac::supported_device();  // before the symbol lookup: a non-sm_103 device has no kernels
+  if (dc != KFAC_OK) return dc;
   void* scratch = kfac::scratch_address();
   if (!scratch) return KFAC_ERR_CUDA;
   return kfac_precondition(n, args, precision, route, scratch, kfac::kStaticScratchBytes, stream);
