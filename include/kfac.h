@@ -322,6 +322,35 @@ size_t kfac_precondition_static_capacity(void);
 int kfac_precondition_static(int n, const kfac_precond_args* args, int precision,
                              int* route, void* stream);
 
+/* --------------------------------------------------- packed upper triangles
+ * A symmetric factor or inverse travels as its d(d+1)/2 upper-triangle
+ * elements, and small factors are fused into one message (§III-A: the
+ * communicated elements of a symmetric Kronecker factor, tensor fusion of
+ * factors, Eq. (14)/(15), Fig. 4; §IV: only the upper triangle of the
+ * symmetric inverse is sent).  Layout: row-major packed upper triangle,
+ *     packed[r*d - r*(r-1)/2 + (c - r)] = M[r][c]      0 <= r <= c < d,
+ * i.e. row r holds the d - r elements M[r][r..d-1].
+ * kfac_pack_upper   packed <- upper triangle of mat (reads c >= r only);
+ * kfac_unpack_upper upper triangle of mat <- packed; with mirror != 0 the
+ *                   strict lower triangle of mat too (M[c][r] = M[r][c]), so
+ *                   mat becomes the full symmetric matrix.  Other elements of
+ *                   mat (padding columns) are not touched.
+ * All matrices of a call are moved by one launch (the fused pass; give
+ * consecutive `packed` pointers, e.g. base + prefix sums of d(d+1)/2, to get one
+ * contiguous buffer).  mat: device fp32 d x d, ld >= d, ld % 4 == 0, 16-byte
+ * aligned; packed: device fp32, d(d+1)/2 elements, 4-byte aligned, not
+ * overlapping mat.  n <= 4096, 1 <= d <= 65536.  Errors: KFAC_ERR_INVALID_ARG
+ * before any launch.  Asynchronous on stream.                               */
+typedef struct {
+  float* mat;      /* device, d x d fp32 (read by pack, written by unpack)  */
+  int64_t d;
+  int64_t ld;      /* leading dimension of mat (elements)                   */
+  float* packed;   /* device, d(d+1)/2 fp32 (written by pack, read by unpack) */
+} kfac_pack_args;
+
+int kfac_pack_upper(int n, const kfac_pack_args* args, void* stream);
+int kfac_unpack_upper(int n, const kfac_pack_args* args, int mirror, void* stream);
+
 /* ------------------------------------------------------------- index tables
  * The work units kfac_factors uses to cover the upper tiles of a d x d factor
  * on the tensor-core path (one per CTA of a CTA pair): row blocks 2s and

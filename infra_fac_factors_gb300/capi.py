@@ -21,7 +21,7 @@ __all__ = [
     "kfac_factors", "kfac_conv_factor_args", "kfac_conv_factors", "kfac_spatial_sum", "kfac_update_running",
     "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
-    "kfac_precondition_static", "kfac_factor_tile_map",
+    "kfac_precondition_static", "kfac_pack_args", "kfac_pack_upper", "kfac_unpack_upper", "kfac_factor_tile_map",
 ]
 
 KFAC_OK, KFAC_ERR_INVALID_ARG, KFAC_ERR_NOT_SPD, KFAC_ERR_CUDA = 0, 1, 2, 3
@@ -62,12 +62,16 @@ class kfac_precond_args(C.Structure):
                 ("weight", C.c_void_p), ("ld_weight", C.c_int64), ("lr", C.c_float)]
 
 
+class kfac_pack_args(C.Structure):
+    _fields_ = [("mat", C.c_void_p), ("d", C.c_int64), ("ld", C.c_int64), ("packed", C.c_void_p)]
+
+
 exported_symbols = (
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
     "kfac_profile", "kfac_profile_read", "kfac_factors", "kfac_conv_factors", "kfac_spatial_sum",
     "kfac_update_running", "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
-    "kfac_precondition_static", "kfac_factor_tile_map",
+    "kfac_precondition_static", "kfac_pack_upper", "kfac_unpack_upper", "kfac_factor_tile_map",
 )
 
 _lib = None
@@ -106,6 +110,8 @@ def lib() -> C.CDLL:
                                         C.c_void_p]),
         "kfac_precondition_static_capacity": (C.c_size_t, []),
         "kfac_precondition_static": (C.c_int, [C.c_int, P(kfac_precond_args), C.c_int, C.c_void_p, C.c_void_p]),
+        "kfac_pack_upper": (C.c_int, [C.c_int, P(kfac_pack_args), C.c_void_p]),
+        "kfac_unpack_upper": (C.c_int, [C.c_int, P(kfac_pack_args), C.c_int, C.c_void_p]),
         "kfac_factor_tile_map": (C.c_int, [C.c_int64, C.c_int64, P(C.c_int32), P(C.c_int64), P(C.c_int32),
                                            P(C.c_int64)]),
     }
@@ -232,6 +238,20 @@ def kfac_precondition_static(args, precision: int, route: int, stream: int = 0, 
     n, a = _arr(kfac_precond_args, args)
     st = lib().kfac_precondition_static(n, a, precision, route, stream)
     return _check("kfac_precondition_static", st) if check else st
+
+
+def kfac_pack_upper(args, stream: int = 0, check: bool = True) -> int:
+    """Packed upper triangles of every matrix of `args`, one launch."""
+    n, a = _arr(kfac_pack_args, args)
+    st = lib().kfac_pack_upper(n, a, stream)
+    return _check("kfac_pack_upper", st) if check else st
+
+
+def kfac_unpack_upper(args, mirror: bool = False, stream: int = 0, check: bool = True) -> int:
+    """Upper triangles (with `mirror` the full symmetric matrices) from packed ones, one launch."""
+    n, a = _arr(kfac_pack_args, args)
+    st = lib().kfac_unpack_upper(n, a, int(bool(mirror)), stream)
+    return _check("kfac_unpack_upper", st) if check else st
 
 
 def kfac_factor_tile_map(d: int):

@@ -2,6 +2,7 @@
 // launchers.  Nothing here allocates device memory or synchronises the host
 // (except kfac_device_status, which documents its synchronisation).
 #include <math.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <initializer_list>
@@ -110,6 +111,20 @@ static int check_pointers(std::initializer_list<const void*> ptrs) {
 
 int supported_device() { return check_device(); }
 
+// An NVTX range around the host side of one call, named after the time
+// categories the pages break an iteration into (FactorComp: the Kronecker
+// factors; InverseComp: the inverses; and, on one GPU, EMAReduce for the shard
+// mean that stands in for the factor all-reduce, with the running average and
+// damping, and Precond for the preconditioned gradient).  Profilers show the
+// launches of the call under it; without a profiler attached it costs a
+// branch.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 int* device_status_ptr();
 
 static std::atomic<unsigned long long> g_launches{0};
@@ -209,6 +224,7 @@ int kfac_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirr
     const int pc = check_pointers({args[i].x, args[i].out});
     if (pc != KFAC_OK) return pc;
   }
+  NvtxRange range("FactorComp");
   return launch_factors(n, args, dtype, P, mirror, static_cast<cudaStream_t>(stream));
 }
 
@@ -233,6 +249,7 @@ int kfac_conv_factors(int n, const kfac_conv_factor_args* args, int P, int mirro
     const int pc = check_pointers({args[i].x, args[i].out});
     if (pc != KFAC_OK) return pc;
   }
+  NvtxRange range("FactorComp");
   return launch_conv_factors(n, args, P, mirror, static_cast<cudaStream_t>(stream));
 }
 
@@ -247,6 +264,7 @@ int kfac_spatial_sum(const void* g, int dtype, int64_t batch, int64_t hw, int64_
   if (dc != KFAC_OK) return dc;
   const int pc = check_pointers({g, gs});
   if (pc != KFAC_OK) return pc;
+  NvtxRange range("FactorComp");
   return launch_spatial_sum(g, dtype, batch, hw, C, ld_g, gs, ld_gs, static_cast<cudaStream_t>(stream));
 }
 
@@ -271,6 +289,7 @@ int kfac_update_running(int n, const kfac_running_args* args, int P, float decay
     const int pc = check_pointers({args[i].shards, args[i].running, args[i].damped});
     if (pc != KFAC_OK) return pc;
   }
+  NvtxRange range("EMAReduce");
   return launch_update_running(n, args, P, decay, gamma, first_step, static_cast<cudaStream_t>(stream));
 }
 
@@ -306,6 +325,7 @@ int kfac_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra,
   int pc = check_pointers({info, route, workspace});
   for (int i = 0; i < n && pc == KFAC_OK; ++i) pc = check_pointers({args[i].damped, args[i].inv});
   if (pc != KFAC_OK) return pc;
+  NvtxRange range("InverseComp");
   return launch_damped_inverse(n, args, gamma_extra, refine, info, route, workspace, workspace_bytes,
                                static_cast<cudaStream_t>(stream));
 }
@@ -352,8 +372,38 @@ int kfac_precondition(int n, const kfac_precond_args* args, int precision, int* 
   for (int i = 0; i < n && pc == KFAC_OK; ++i)
     pc = check_pointers({args[i].inv_g, args[i].grad, args[i].inv_a, args[i].out, args[i].weight});
   if (pc != KFAC_OK) return pc;
+  NvtxRange range("Precond");
   return launch_precondition(n, args, precision, route, workspace, workspace_bytes,
                              static_cast<cudaStream_t>(stream));
+}
+
+static int packed_call(int n, const kfac_pack_args* args, int unpack, int mirror, void* stream) {
+  if (n < 0 || n > 4096 || (n > 0 && !args)) return KFAC_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const kfac_pack_args& a = args[i];
+    if (!a.mat || !a.packed || !aligned16(a.mat) || (reinterpret_cast<uintptr_t>(a.packed) & 3))
+      return KFAC_ERR_INVALID_ARG;
+    if (a.d < 1 || a.d > 65536 || a.ld < a.d || a.ld % 4 != 0) return KFAC_ERR_INVALID_ARG;
+    // the two buffers must not overlap: [mat, mat + (d-1) ld + d) and [packed, packed + d(d+1)/2)
+    const uintptr_t m0 = reinterpret_cast<uintptr_t>(a.mat), p0 = reinterpret_cast<uintptr_t>(a.packed);
+    const uintptr_t m1 = m0 + (uintptr_t)((a.d - 1) * a.ld + a.d) * 4, p1 = p0 + (uintptr_t)(a.d * (a.d + 1) / 2) * 4;
+    if (m0 < p1 && p0 < m1) return KFAC_ERR_INVALID_ARG;
+  }
+  if (n == 0) return KFAC_OK;
+  const int dc = check_device();
+  if (dc != KFAC_OK) return dc;
+  for (int i = 0; i < n; ++i) {
+    const int pc = check_pointers({args[i].mat, args[i].packed});
+    if (pc != KFAC_OK) return pc;
+  }
+  NvtxRange range(unpack ? "UnpackUpper" : "PackUpper");
+  return launch_packed(n, args, unpack, mirror, static_cast<cudaStream_t>(stream));
+}
+
+int kfac_pack_upper(int n, const kfac_pack_args* args, void* stream) { return packed_call(n, args, 0, 0, stream); }
+
+int kfac_unpack_upper(int n, const kfac_pack_args* args, int mirror, void* stream) {
+  return packed_call(n, args, 1, mirror != 0, stream);
 }
 
 int kfac_factor_tile_map(int64_t d, int64_t capacity, int32_t* row_block, int64_t* col_start, int32_t* width,

@@ -53,6 +53,7 @@ size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine);
 bool fp64_chain_stream(int dev, cudaStream_t caller, cudaStream_t* chain, cudaEvent_t (&ev)[4]);
 int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra, int refine, int* info, int* route,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int launch_packed(int n, const kfac_pack_args* args, int unpack, int mirror, cudaStream_t stream);
 size_t precondition_workspace(int n, const kfac_precond_args* args);
 int launch_precondition(int n, const kfac_precond_args* args, int precision, int* route, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream);

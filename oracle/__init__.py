@@ -17,5 +17,5 @@ from .kfac import (  # noqa: F401
     cholesky_lower, lower_tri_inverse, spd_inverse, damped_inverse,
     precondition, spatial_sum, factor_tile_units, upper_tiles,
     packed_index, kron_precondition_bruteforce, kfac_step, weight_step, stored_part,
-    im2col3x3,
+    im2col3x3, pack_upper, unpack_upper,
 )

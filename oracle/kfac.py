@@ -249,6 +249,33 @@ def packed_index(i: int, j: int, d: int) -> int:
     return i * d - i * (i - 1) // 2 + (j - i)
 
 
+def pack_upper(M: np.ndarray) -> np.ndarray:
+    """The d(d+1)/2 upper-triangle elements of a symmetric d x d matrix, row
+    by row: row r contributes M[r, r:] (§III-A: a symmetric factor is
+    communicated as its upper triangle; §IV: so is the symmetric inverse)."""
+    M = np.asarray(M)
+    d = M.shape[0]
+    return np.concatenate([M[r, r:] for r in range(d)])
+
+
+def unpack_upper(p: np.ndarray, d: int, mirror: bool = True) -> np.ndarray:
+    """The matrix whose upper triangle ``p`` packs (``pack_upper``'s layout);
+    with ``mirror`` the strict lower triangle is filled from it, else it is
+    left NaN."""
+    p = np.asarray(p)
+    if p.shape[0] != d * (d + 1) // 2:
+        raise ValueError("packed length is not d(d+1)/2")
+    M = np.full((d, d), np.nan, dtype=p.dtype)
+    start = 0
+    for r in range(d):
+        M[r, r:] = p[start:start + d - r]
+        start += d - r
+    if mirror:
+        il = np.tril_indices(d, -1)
+        M[il] = M.T[il]
+    return M
+
+
 # ---------------------------------------------------------------- one step
 def kfac_step(layer_data, P: int, gamma: float, decay: float, first_step: bool,
               running=None, conv=None):

@@ -32,7 +32,7 @@ def declared_functions():
 
 def test_exports_every_declared_function():
     names = declared_functions()
-    assert len(names) == 18
+    assert len(names) == 20
     out = subprocess.run(["nm", "-D", "--defined-only", capi.library_path], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (kfac_[a-z_0-9]+)$", out, flags=re.M))
     for n in names:
@@ -55,6 +55,7 @@ int main(void) {
   S(kfac_precond_args) O(kfac_precond_args, out) O(kfac_precond_args, d_in)
   S(kfac_conv_factor_args) O(kfac_conv_factor_args, C) O(kfac_conv_factor_args, out)
   O(kfac_conv_factor_args, scale)
+  S(kfac_pack_args) O(kfac_pack_args, ld) O(kfac_pack_args, packed)
   return 0;
 }
 """
@@ -67,7 +68,8 @@ int main(void) {
     got = dict(l.split() for l in lines if l)
     for name, st in (("kfac_factor_args", capi.kfac_factor_args), ("kfac_running_args", capi.kfac_running_args),
                      ("kfac_inverse_args", capi.kfac_inverse_args), ("kfac_precond_args", capi.kfac_precond_args),
-                     ("kfac_conv_factor_args", capi.kfac_conv_factor_args)):
+                     ("kfac_conv_factor_args", capi.kfac_conv_factor_args),
+                     ("kfac_pack_args", capi.kfac_pack_args)):
         assert int(got[name]) == C.sizeof(st), name
         for key, val in got.items():
             if key.startswith(name + "."):
@@ -212,6 +214,17 @@ def test_spatial_sum_rejects_invalid():
     assert f(A16, 0, 2, 4, 8, 4, A16, 8, check=False) == capi.KFAC_ERR_INVALID_ARG
     assert f(A16, 0, 0, 4, 8, 8, A16, 8, check=False) == capi.KFAC_ERR_INVALID_ARG
     assert f(A16, 1, 2, 4, 8, 8, A16, 6, check=False) == capi.KFAC_ERR_INVALID_ARG
+
+
+def test_pack_unpack_reject_invalid():
+    pk = lambda **kw: capi.kfac_pack_args(**{**dict(mat=A16, d=10, ld=12, packed=A16 * 64), **kw})
+    for bad in (pk(mat=0), pk(packed=0), pk(mat=A16 + 4), pk(packed=A16 * 64 + 2), pk(d=0), pk(d=65537),
+                pk(ld=9), pk(ld=14), pk(packed=A16 + 40),  # packed overlapping mat
+                pk(packed=A16 - 16)):                        # mat overlapping packed's tail
+        assert capi.kfac_pack_upper([bad], check=False) == capi.KFAC_ERR_INVALID_ARG
+        assert capi.kfac_unpack_upper([bad], True, check=False) == capi.KFAC_ERR_INVALID_ARG
+    assert capi.kfac_pack_upper([], check=False) == capi.KFAC_OK
+    assert capi.kfac_unpack_upper([], check=False) == capi.KFAC_OK
 
 
 def test_wait_selftest_rejects_limits_outside_the_kernels_range():

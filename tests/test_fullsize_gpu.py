@@ -73,6 +73,20 @@ def test_sampled_factor_entries(run):
                 assert abs(S[p, r, c] - ref) <= 1e-5 * norm, (li, p, r, c, S[p, r, c], ref)
 
 
+def test_whole_shard_factor_per_layer_kind(run):
+    # one whole worker factor of each layer kind (a different worker each),
+    # every upper-tile element against the oracle
+    P = CFG.P
+    for k, li in enumerate(LAYERS):
+        for x, S in ((run["inputs"][li]["a"], run["shards"][li][0]), (run["inputs"][li]["g"], run["shards"][li][1])):
+            rows, d = x.shape
+            rp = rows // P
+            p = (3 * k + 1) % P
+            ref = oracle.factor(x[p * rp:(p + 1) * rp], 1.0 / rp)
+            m = upper_tile_mask(d)
+            assert rel_fro(S[p][:, :d], ref, m) <= 1e-5, (li, p, d)
+
+
 def test_running_average_and_damping_properties(run):
     for li in LAYERS:
         S = run["shards"][li][0]

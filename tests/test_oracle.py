@@ -345,6 +345,28 @@ def test_packed_index_enumeration():
         oracle.packed_index(2, 1, 4)
 
 
+def test_pack_upper_follows_the_enumerated_index_and_round_trips():
+    rng = np.random.default_rng(3)
+    for d in (1, 2, 5, 33):
+        M = rng.standard_normal((d, d))
+        M = M + M.T
+        p = oracle.pack_upper(M)
+        assert p.shape == (d * (d + 1) // 2,)
+        for i in range(d):
+            for j in range(i, d):
+                assert p[oracle.packed_index(i, j, d)] == M[i, j]
+        assert np.array_equal(oracle.unpack_upper(p, d), M)
+        U = oracle.unpack_upper(p, d, mirror=False)
+        assert np.array_equal(np.triu(U), np.triu(M)) and np.isnan(U[np.tril_indices(d, -1)]).all()
+    # the packed form holds exactly the upper triangle: an asymmetric matrix
+    # packs its upper part only, so unpacking gives the symmetrised upper part
+    A = np.arange(16.0).reshape(4, 4)
+    assert list(oracle.pack_upper(A)) == [0, 1, 2, 3, 5, 6, 7, 10, 11, 15]
+    assert np.array_equal(oracle.unpack_upper(oracle.pack_upper(A), 4), np.triu(A) + np.triu(A, 1).T)
+    with pytest.raises(ValueError):
+        oracle.unpack_upper(np.zeros(5), 3)
+
+
 # ------------------------------------------------------------------ page pin: ResNet-50 sizes
 def _resnet50_layers():
     """(kernel, C_in, C_out) of the 53 convolutions of ResNet-50, then the fc."""

@@ -473,8 +473,11 @@ def test_config_resnet_conv_one_step():
     check_config("resnet_conv", 1)
 
 
-def test_config_bert_layer_three_steps():
-    check_config("bert_layer", 3, inv_steps=(0, 2))
+def test_config_bert_layer_twenty_steps():
+    # the workload's 20 running-average steps: every step's worker factors,
+    # running and damped factors against the oracle; inverses and
+    # preconditioned gradients on the first and the last step
+    check_config("bert_layer", 20, inv_steps=(0, 19))
 
 
 def test_step_applies_the_weight_step_after_routing():
