@@ -95,15 +95,27 @@ int kfac_device_status(int* status_out, int clear, void* stream);
  *   KFAC_K_GEMM16      preconditioning GEMMs, 16-bit   work: 2 M N K per problem
  *   KFAC_K_GEMM24      preconditioning GEMMs, 24-bit   work: 2 M N K per problem run
  *   KFAC_K_CONV_SYRK   conv factor SYRK (implicit im2col) work: as KFAC_K_SYRK, rows = patch rows
+ *   KFAC_K_INV_DIAG    inverse: 128 x 128 diagonal blocks (CUDA cores)  work: 0
+ *   KFAC_K_INV_PREP    inverse: block-column slicing (CUDA cores)       work: 0
+ *   KFAC_K_INV_AUX     inverse: load, operand width, norms, residual probe, flags (CUDA cores)  work: 0
  * Recording holds at most 65536 launches (later ones are not recorded).
- * Invalid kind: KFAC_ERR_INVALID_ARG.                                        */
+ * Invalid kind: KFAC_ERR_INVALID_ARG.
+ * kfac_profile_count gives the number of recorded launches and
+ * kfac_profile_launch the i-th of them (in the order they were issued): its
+ * kind, its start and end (ms after the start of the first recorded launch,
+ * so launches on concurrent streams line up on one time axis) and its work;
+ * both synchronise on the recorded events.  i out of range:
+ * KFAC_ERR_INVALID_ARG.                                                      */
 typedef enum {
   KFAC_K_SYRK = 0, KFAC_K_RUNNING = 1, KFAC_K_INV_PANEL = 2, KFAC_K_INV_UPDATE = 3,
   KFAC_K_INV_LAUUM = 4, KFAC_K_GEMM16 = 5, KFAC_K_GEMM24 = 6, KFAC_K_CONV_SYRK = 7,
-  KFAC_K_COUNT = 8
+  KFAC_K_INV_DIAG = 8, KFAC_K_INV_PREP = 9, KFAC_K_INV_AUX = 10,
+  KFAC_K_COUNT = 11
 } kfac_kernel_kind;
 int kfac_profile(int enable);
 int kfac_profile_read(int kind, int64_t* launches, double* ms, double* work);
+int kfac_profile_count(int64_t* count);
+int kfac_profile_launch(int64_t i, int* kind, double* start_ms, double* end_ms, double* work);
 
 /* Failure-detection self-test (no counterpart on the pages; a property of the
  * library): launches one CTA that waits, with the same bounded wait every
@@ -215,9 +227,14 @@ int kfac_update_running(int n, const kfac_running_args* args, int P,
  * exactly symmetric matrix (§IV: the inverse of a symmetric factor is
  * symmetric).  Matrices may have different sizes.
  *
- * refine: KFAC_REFINE_NONE   fp32 arithmetic for every matrix;
- *         KFAC_REFINE_AUTO   fp32, then a matrix is recomputed in fp64 when
- *                            its residual ||inv D - I||_F / sqrt(d), estimated
+ * refine: KFAC_REFINE_NONE   fp32 arithmetic for every matrix (tile products
+ *                            on tensor cores with 24-bit operands: three bf16
+ *                            slices, six MMAs per multiply-add);
+ *         KFAC_REFINE_AUTO   fp32, with 16-bit operands (two slices, three
+ *                            MMAs) for a matrix whose Gershgorin discs bound its
+ *                            condition number by 16 and 24-bit ones otherwise;
+ *                            then a matrix is recomputed in fp64 when its
+ *                            residual ||inv D - I||_F / sqrt(d), estimated
  *                            with four random +-1 probes, exceeds 2.5e-4, when
  *                            ||D||_1 / min_j L_jj^2 exceeds 3e5, or when its
  *                            fp32 factorisation failed;
@@ -225,7 +242,8 @@ int kfac_update_running(int n, const kfac_running_args* args, int P,
  * info: device int[n]; info[i] = 0 on success, k > 0 when the k-th pivot
  *       (1-based) is not positive (LAPACK potrf convention); inv_i is then
  *       unspecified.  route (device int[n], may be NULL): 0 when inv_i came
- *       from the fp32 pass, 1 from the fp64 pass.
+ *       from the fp32 pass with 24-bit operands, 2 with 16-bit operands, 1
+ *       from the fp64 pass.
  * ld_in, ld_out % 4 == 0.  n <= 4096, 1 <= d <= 65536.
  * Workspace: kfac_damped_inverse_workspace(n, args, refine) bytes, 256-byte
  * aligned, fully overwritten (no initialisation needed).

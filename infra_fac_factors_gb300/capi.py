@@ -17,7 +17,7 @@ __all__ = [
     "kfac_factor_args", "kfac_running_args", "kfac_inverse_args", "kfac_precond_args",
     "KFACError", "lib", "library_path", "exported_symbols", "KERNEL_KINDS",
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
-    "kfac_profile", "kfac_profile_read",
+    "kfac_profile", "kfac_profile_read", "kfac_profile_count", "kfac_profile_launch", "kfac_profile_timeline",
     "kfac_factors", "kfac_conv_factor_args", "kfac_conv_factors", "kfac_spatial_sum", "kfac_update_running",
     "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
@@ -29,7 +29,8 @@ KFAC_ERR_UNSUPPORTED, KFAC_ERR_TIMEOUT, KFAC_ERR_WORKSPACE = 4, 5, 6
 KFAC_BF16, KFAC_FP32 = 0, 1
 KFAC_REFINE_NONE, KFAC_REFINE_AUTO, KFAC_REFINE_ALWAYS = 0, 1, 2
 KFAC_PRECOND_FP32, KFAC_PRECOND_AUTO = 0, 1
-KERNEL_KINDS = ("syrk", "running", "inv_panel", "inv_update", "inv_lauum", "gemm16", "gemm24", "conv_syrk")
+KERNEL_KINDS = ("syrk", "running", "inv_panel", "inv_update", "inv_lauum", "gemm16", "gemm24", "conv_syrk",
+                "inv_diag", "inv_prep", "inv_aux")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libkfac_gb300.so")
@@ -68,7 +69,8 @@ class kfac_pack_args(C.Structure):
 
 exported_symbols = (
     "kfac_status_string", "kfac_version", "kfac_launch_count", "kfac_device_status", "kfac_wait_selftest",
-    "kfac_profile", "kfac_profile_read", "kfac_factors", "kfac_conv_factors", "kfac_spatial_sum",
+    "kfac_profile", "kfac_profile_read", "kfac_profile_count", "kfac_profile_launch", "kfac_factors",
+    "kfac_conv_factors", "kfac_spatial_sum",
     "kfac_update_running", "kfac_damped_inverse_workspace", "kfac_damped_inverse",
     "kfac_precondition_workspace", "kfac_precondition", "kfac_precondition_static_capacity",
     "kfac_precondition_static", "kfac_pack_upper", "kfac_unpack_upper", "kfac_factor_tile_map",
@@ -96,6 +98,8 @@ def lib() -> C.CDLL:
         "kfac_wait_selftest": (C.c_int, [C.c_int64, C.c_void_p]),
         "kfac_profile": (C.c_int, [C.c_int]),
         "kfac_profile_read": (C.c_int, [C.c_int, P(C.c_int64), P(C.c_double), P(C.c_double)]),
+        "kfac_profile_count": (C.c_int, [P(C.c_int64)]),
+        "kfac_profile_launch": (C.c_int, [C.c_int64, P(C.c_int), P(C.c_double), P(C.c_double), P(C.c_double)]),
         "kfac_factors": (C.c_int, [C.c_int, P(kfac_factor_args), C.c_int, C.c_int, C.c_int, C.c_void_p]),
         "kfac_conv_factors": (C.c_int, [C.c_int, P(kfac_conv_factor_args), C.c_int, C.c_int, C.c_void_p]),
         "kfac_spatial_sum": (C.c_int, [C.c_void_p, C.c_int, C.c_int64, C.c_int64, C.c_int64, C.c_int64,
@@ -177,6 +181,25 @@ def kfac_profile_read(kind) -> dict:
     n, ms, w = C.c_int64(0), C.c_double(0.0), C.c_double(0.0)
     _check("kfac_profile_read", lib().kfac_profile_read(k, C.byref(n), C.byref(ms), C.byref(w)))
     return {"launches": int(n.value), "ms": float(ms.value), "work": float(w.value)}
+
+
+def kfac_profile_count() -> int:
+    n = C.c_int64(0)
+    _check("kfac_profile_count", lib().kfac_profile_count(C.byref(n)))
+    return int(n.value)
+
+
+def kfac_profile_launch(i: int) -> dict:
+    """The i-th recorded launch: kind name, start and end (ms on a common axis), work."""
+    k, a, b, w = C.c_int(0), C.c_double(0.0), C.c_double(0.0), C.c_double(0.0)
+    _check("kfac_profile_launch", lib().kfac_profile_launch(i, C.byref(k), C.byref(a), C.byref(b), C.byref(w)))
+    return {"kind": KERNEL_KINDS[k.value], "start_ms": float(a.value), "end_ms": float(b.value),
+            "work": float(w.value)}
+
+
+def kfac_profile_timeline() -> list:
+    """Every recorded launch, in issue order."""
+    return [kfac_profile_launch(i) for i in range(kfac_profile_count())]
 
 
 def kfac_factors(args, dtype: int, P: int, mirror: int = 0, stream: int = 0, check: bool = True) -> int:

@@ -53,6 +53,7 @@ __global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, InvCtx c)
     s.kappa = 0.f;
     s.xnorm2 = 0.f;
     s.est_res = 0.f;
+    s.slices = 3;
     c.st[e] = s;
     c.flagged[e] = (int)e;
   }
@@ -333,12 +334,12 @@ __global__ void inv_finish_kernel(InvCtx c, int n, int* info, int* route) {
   if (i >= n) return;
   const InvState s = c.st[i];
   info[i] = s.use64 ? s.info64 : s.info32;
-  if (route) route[i] = s.use64;
+  if (route) route[i] = s.use64 ? 1 : (s.slices == 2 ? 2 : 0);
 }
 
 // ------------------------------------------------------------------ host side
 struct InvLayout {
-  size_t mats_off, st_off, flag_off, rowsum_off, probe_off, region_off, total;
+  size_t mats_off, st_off, flag_off, rowsum_off, probe_off, gpart_off, region_off, total;
   TcLayout tc;
 };
 
@@ -351,21 +352,25 @@ static InvLayout inv_layout(int n, const kfac_inverse_args* args, int refine, lo
   L.st_off = align256(sizeof(InvMat) * (size_t)n);
   L.flag_off = L.st_off + align256(sizeof(InvState) * (size_t)n);
   L.rowsum_off = L.flag_off + align256(sizeof(int) * (size_t)(n + 1));
-  long long rs = 0;
+  long long rs = 0, gp = 0;
   int Ts[kInvMaxGroup];
   for (int i = 0; i < n; ++i) {
+    Ts[i] = (int)((args[i].d + 127) / 128);
     if (mats) {
       mats[i].off_rowsum = rs;
       mats[i].off_probe = 2 * kProbes * rs;
       mats[i].row_off = rs;
+      mats[i].off_gpart = gp;
     }
-    Ts[i] = (int)((args[i].d + 127) / 128);
     rs += (long long)Ts[i] * 128;
+    gp += (long long)Ts[i] * Ts[i] * 128;
   }
   *rowsum_total = rs;
   *probe_total = 2 * kProbes * rs;
   L.probe_off = L.rowsum_off + align256(sizeof(float) * (size_t)rs);
-  L.region_off = L.probe_off + align256(sizeof(float2) * (size_t)(2 * kProbes * rs));
+  L.gpart_off = L.probe_off + align256(sizeof(float2) * (size_t)(2 * kProbes * rs));
+  const size_t gpart_bytes = refine == KFAC_REFINE_AUTO ? align256(sizeof(float) * (size_t)gp) : 0;
+  L.region_off = L.gpart_off + gpart_bytes;
   // the fp32 tensor-core pass and the fp64 pass run one after the other and
   // share the work region
   size_t fp64 = 0;
@@ -483,6 +488,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
     ctx.nflagged = ctx.flagged + cnt;
     ctx.rowsum = reinterpret_cast<float*>(ws + L.rowsum_off);
     ctx.probe = reinterpret_cast<float2*>(ws + L.probe_off);
+    ctx.gpart = refine == KFAC_REFINE_AUTO ? reinterpret_cast<float*>(ws + L.gpart_off) : nullptr;
     ctx.region = ws + L.region_off;
     ctx.gamma_extra = gamma_extra;
     ctx.want_rowsum = refine == KFAC_REFINE_AUTO;
@@ -500,7 +506,10 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
       if (rc != KFAC_OK) return rc;
     }
     if (refine == KFAC_REFINE_AUTO) {
+      ProfMark pm;
+      prof_begin(stream, pm);
       inv_flag_kernel<<<cnt, 128, 0, stream>>>(ctx);
+      prof_end(KFAC_K_INV_AUX, stream, pm, 0.0);
       count_launch();
     }
     if (refine != KFAC_REFINE_NONE) {

@@ -12,6 +12,13 @@ constexpr int kInvMaxGroup = 256;
 constexpr float kAutoKappa = 3e5f;
 constexpr double kAutoResidual = 2.5e-4;
 constexpr int kProbes = 4;
+// AUTO: a matrix whose Gershgorin discs bound its condition number by this
+// ratio runs the fp32 pass with 16-bit operands (two bf16 slices, three MMAs
+// per multiply-add).  Emulated on the host, two slices left a residual
+// ||X D - I||_F / sqrt(d) of about 3e-6 times the condition number
+// (2e-7 at 1, 1e-5 at 4, 1.2e-3 at 4e3); at 16 that is under 5e-5, five times
+// below the residual bar that sends a matrix to the fp64 pass.
+constexpr float kSlices16Kappa = 16.f;
 
 struct InvMat {
   const float* D;
@@ -21,6 +28,7 @@ struct InvMat {
   long long off_rowsum;  // float index of this matrix's row sums
   long long off_probe;   // double index of this matrix's probe vectors w, y
   long long row_off;     // first row of this matrix in the stacked fp32 work buffers
+  long long off_gpart;   // float index of this matrix's partial off-diagonal row sums (T x T x 128)
   int d, T;
 };
 
@@ -28,6 +36,7 @@ struct InvState {
   int info32, info64, failed, use64;
   float min_piv, kappa;
   float xnorm2, est_res;  // ||X||_F^2 and the estimated residual of the fp32 pass
+  int slices;             // bf16 slices per operand in the fp32 pass: 3 (24-bit) or 2 (16-bit)
 };
 
 // Rademacher probe entry v_p(i) in {-1, +1} (splitmix64 finaliser of (i, p)).
@@ -50,6 +59,7 @@ struct InvCtx {
   const InvMat* mats;
   InvState* st;
   float* rowsum;
+  float* gpart;     // AUTO: per matrix, partial sums of |D_rc| (c != r) over each 128-column block
   float2* probe;    // per matrix: w[kProbes][n_pad] then y[kProbes][n_pad], double-float (hi, lo)
   int* flagged;     // indices of the matrices the fp64 pass inverts
   int* nflagged;    // their count

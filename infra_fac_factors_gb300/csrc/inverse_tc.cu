@@ -42,6 +42,11 @@ constexpr int kItThreads = 320;
 // 16-wide k-steps accumulated in one TMEM accumulator between two drains into
 // the epilogue's round-to-nearest fp32 sums
 constexpr int kItDrain = 2;
+// the same with 16-bit operands (two slices, three MMAs per k-step): their
+// slicing error (2^-16 of a product) dominates the accumulator's, so the
+// accumulator is drained every eight k-steps, as in the 16-bit GEMM of the
+// preconditioning
+constexpr int kItDrain16 = 8;
 constexpr int kLoadSmem = 128 * 129 * 4;
 constexpr int kNormsXch = 1 + 2 * kProbes;
 constexpr int kNormsSmem = (128 * 129 + kProbes * 128 + 128 * kNormsXch) * 4;
@@ -111,7 +116,11 @@ struct ItJob {
   int a_y, a_x0, b_y, b_x0, b_box, K, n_mma;
   int o_y, o_x, mode;  // output rows/cols; panel: 0 -> Lp, 1 -> U; update: 0 add, 1 store
   int i, j;            // X tile (i, j) of the pair j, j+1 (lauum)
+  int ns;              // bf16 slices per operand for this matrix: 3 (24-bit) or 2 (16-bit)
 };
+
+// k-steps of one accumulator drain for operands of `ns` slices
+__device__ __forceinline__ int it_drain(int ns) { return ns == 2 ? kItDrain16 : kItDrain; }
 
 // jobs of the update at step k for a matrix of T block rows: rows r > k pair
 // their columns c in (k, r]; columns c <= k pair their rows r > k
@@ -177,6 +186,7 @@ __device__ ItJob it_decode(const ItParams& prm, long long u) {
   const int k = prm.k;
   J.m = m;
   J.valid = !prm.st[m].failed;
+  J.ns = prm.st[m].slices == 2 ? 2 : kSlices;
   J.i = J.j = 0;
   J.mode = 0;
   if (KIND == kItPanel) {
@@ -334,13 +344,14 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
       for (long long u = blockIdx.x; u < prm.total_jobs && !*abort_flag; u += gridDim.x) {
         const ItJob J = it_decode<KIND>(prm, u);
         if (!J.valid) continue;
-        const uint32_t bytes = kSlices * (kItA + J.b_box * kItBK * 2);
+        const uint32_t bytes = J.ns * (kItA + J.b_box * kItBK * 2);
         for (int kb = 0; kb < J.K / kItBK; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, prm.status)) break;
           uint8_t* s0 = smem + stage * Cfg::stage;
           mbar_arrive_expect_tx(&full[stage], bytes);
 #pragma unroll
           for (int s = 0; s < kSlices; ++s) {
+            if (s >= J.ns) break;
             tma_load_3d(s0 + s * kItA, J.ma, J.a_x0 + kb * kItBK, J.a_y, s, &full[stage]);
             tma_load_3d(s0 + kSlices * kItA + s * Cfg::b_slice, J.mb, J.b_x0 + kb * kItBK, J.b_y, s, &full[stage]);
           }
@@ -360,6 +371,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         if (!J.valid) continue;
         const uint32_t idesc = idesc_bf16_f32(J.n_mma, false, false);
         const int n16 = J.K / 16;  // 16-wide k-steps of the job
+        const int dr = it_drain(J.ns);
         int st16 = 0;
         for (int kb = 0; kb < J.K / kItBK && ok; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, prm.status)) {
@@ -370,8 +382,8 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
           const uint32_t b0 = a0 + kSlices * kItA;
 #pragma unroll
           for (int kk = 0; kk < kItBK / 16; ++kk, ++st16) {
-            const bool gfirst = st16 % kItDrain == 0;
-            const bool glast = st16 % kItDrain == kItDrain - 1 || st16 == n16 - 1;
+            const bool gfirst = st16 % dr == 0;
+            const bool glast = st16 % dr == dr - 1 || st16 == n16 - 1;
             if (gfirst) {
               if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, prm.status)) {
                 ok = false;
@@ -387,12 +399,15 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
               da[s] = it_desc(a0 + s * kItA + off);
               db[s] = it_desc(b0 + s * Cfg::b_slice + off);
             }
+            // hi*hi, hi*mid, mid*hi (16-bit operands); and hi*lo, lo*hi, mid*mid (24-bit)
             tc_mma_bf16(d_tmem, da[0], db[0], idesc, gfirst ? 0u : 1u);
             tc_mma_bf16(d_tmem, da[0], db[1], idesc, 1u);
             tc_mma_bf16(d_tmem, da[1], db[0], idesc, 1u);
-            tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
-            tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
-            tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
+            if (J.ns == kSlices) {
+              tc_mma_bf16(d_tmem, da[0], db[2], idesc, 1u);
+              tc_mma_bf16(d_tmem, da[2], db[0], idesc, 1u);
+              tc_mma_bf16(d_tmem, da[1], db[1], idesc, 1u);
+            }
             if (glast) {
               tc_commit(&acc_full[acc]);
               acc ^= 1;
@@ -423,7 +438,7 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
       float run[128];
 #pragma unroll
       for (int t = 0; t < 128; ++t) run[t] = 0.f;
-      const int nsteps = (J.K / 16 + kItDrain - 1) / kItDrain;
+      const int nsteps = (J.K / 16 + it_drain(J.ns) - 1) / it_drain(J.ns);
       for (int st = 0; st < nsteps; ++st) {
         if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, prm.status)) {
           ok = false;
@@ -561,6 +576,37 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
     d[3] = v.w;
   }
   __syncthreads();
+  if (c.gpart) {
+    // AUTO: partial sums of |D_rc| over the tile for the Gershgorin bound of
+    // the 16-bit route (tc_route_kernel), without the diagonal: rows of block
+    // C along the tile's rows, rows of block R down its columns (the mirror);
+    // on a diagonal tile only its upper triangle counts, for both
+    // (columns of the tile at or past d hold whatever the float4 loads brought
+    // from the padding: they are left out; rows past d were loaded as zero)
+    float* gp = c.gpart + m.off_gpart;
+    const long long cleft = m.d - (long long)R * 128;
+    const int jmax = cleft < 128 ? (int)cleft : 128;
+    if (R == C) {
+      if (t < 128) {
+        float s = 0.f;
+        if (t < jmax) {
+          for (int j = t + 1; j < jmax; ++j) s += fabsf(sub[t * 129 + j]);
+          for (int i = 0; i < t; ++i) s += fabsf(sub[i * 129 + t]);
+        }
+        gp[((long long)C * m.T + C) * 128 + t] = s;
+      }
+    } else if (t < 128) {
+      float s = 0.f;
+      for (int j = 0; j < jmax; ++j) s += fabsf(sub[t * 129 + j]);
+      gp[((long long)C * m.T + R) * 128 + t] = s;
+    } else {
+      const int j = t - 128;
+      float s = 0.f;
+      if (j < jmax)
+        for (int i = 0; i < 128; ++i) s += fabsf(sub[i * 129 + j]);
+      gp[((long long)R * m.T + C) * 128 + j] = s;
+    }
+  }
   // write the lower tile (R, C) of the work buffer along its rows: element
   // (R*128 + j, C*128 + i) = D(C*128 + i, R*128 + j); identity past d, zero
   // above the diagonal, gamma_extra on it
@@ -592,6 +638,50 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
       for (int s = 0; s < kSlices; ++s) *reinterpret_cast<uint4*>(dst + s * ss) = make_uint4(0, 0, 0, 0);
     }
   }
+}
+
+// ------------------------------------------------------------------ operand width (AUTO)
+// The Gershgorin discs of D + gamma_extra I hold every eigenvalue in
+// [min_r (D_rr - s_r), max_r (D_rr + s_r)], s_r = sum_{c != r} |D_rc| (the
+// partial sums of tc_load_kernel).  When the lower end is positive and the
+// ratio is at most kSlices16Kappa, the matrix is that well conditioned and its
+// fp32 pass runs with 16-bit operands (two slices); else with 24-bit ones.
+// The residual probe checks the result either way.
+__global__ void __launch_bounds__(128) tc_route_kernel(InvCtx c) {
+  const int mi = blockIdx.x;
+  if (!inv_active(c, mi, false)) return;
+  const InvMat m = c.mats[mi];
+  const float* gp = c.gpart + m.off_gpart;
+  __shared__ float slo[128], shi[128];
+  __shared__ int sbad;
+  if (threadIdx.x == 0) sbad = 0;
+  __syncthreads();
+  float lo = 3.0e38f, hi = 0.f;
+  bool bad = false;
+  for (long long r = threadIdx.x; r < m.d; r += 128) {
+    const long long b = r / 128;
+    const int i = (int)(r % 128);
+    float off = 0.f;
+    for (int cb = 0; cb < m.T; ++cb) off += gp[(b * m.T + cb) * 128 + i];
+    const float dg = m.D[r * m.ld_in + r] + c.gamma_extra;
+    const float l = dg - off, h = dg + off;
+    if (!isfinite(l) || !isfinite(h)) bad = true;
+    lo = fminf(lo, l);
+    hi = fmaxf(hi, h);
+  }
+  if (bad) sbad = 1;
+  slo[threadIdx.x] = lo;
+  shi[threadIdx.x] = hi;
+  __syncthreads();
+  for (int s = 64; s > 0; s >>= 1) {
+    if (threadIdx.x < s) {
+      slo[threadIdx.x] = fminf(slo[threadIdx.x], slo[threadIdx.x + s]);
+      shi[threadIdx.x] = fmaxf(shi[threadIdx.x], shi[threadIdx.x + s]);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0)
+    c.st[mi].slices = (!sbad && slo[0] > 0.f && shi[0] <= kSlices16Kappa * slo[0]) ? 2 : kSlices;
 }
 
 // ------------------------------------------------------------------ ||D||_1 and w = D v (AUTO)
@@ -1017,6 +1107,17 @@ bool fp64_chain_stream(int dev, cudaStream_t caller, cudaStream_t* chain, cudaEv
   return true;
 }
 
+// A CUDA-core launch of the inverse, timed as `kind` while the launch profile
+// records (kfac_profile).
+template <typename F>
+static void timed_launch(int kind, cudaStream_t stream, F&& launch) {
+  ProfMark pm;
+  prof_begin(stream, pm);
+  launch();
+  prof_end(kind, stream, pm, 0.0);
+  count_launch();
+}
+
 // Jobs per CTA of a far update: its CTAs retire every few jobs, so that the
 // higher-priority chain on the other stream finds SMs within tens of us.
 constexpr int kFarJobsPerCta = 4;
@@ -1099,14 +1200,16 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
     main = aux.hi;
   }
   if (rc == KFAC_OK) {
-    tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, kLoadSmem, main>>>(ctx, b);
-    count_launch();
+    timed_launch(KFAC_K_INV_AUX, main,
+                 [&] { tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, kLoadSmem, main>>>(ctx, b); });
+    if (ctx.gpart) {
+      timed_launch(KFAC_K_INV_AUX, main, [&] { tc_route_kernel<<<n, 128, 0, main>>>(ctx); });
+    }
     if (ctx.want_rowsum) {  // reads the caller's matrices only: beside the sweep, at lowest priority
       norms_forked = fork_ok;
       cudaStream_t ns = fork_ok ? aux.lo : stream;
       if (fork_ok && cudaStreamWaitEvent(aux.lo, aux.start, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
-      tc_norms_kernel<<<dim3((unsigned)Tmax, n), 256, kNormsSmem, ns>>>(ctx);
-      count_launch();
+      timed_launch(KFAC_K_INV_AUX, ns, [&] { tc_norms_kernel<<<dim3((unsigned)Tmax, n), 256, kNormsSmem, ns>>>(ctx); });
       if (fork_ok && cudaEventRecord(aux.norms, aux.lo) != cudaSuccess) rc = KFAC_ERR_CUDA;
     }
   }
@@ -1127,8 +1230,8 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       rc = launch_it<kItLauum>(prm, Ts, n, 0, (int)((lj + 1) / 2), aux.lo, kUpdInner, k);
       if (rc != KFAC_OK) break;
       if (ctx.want_rowsum) {
-        tc_probe_kernel<<<dim3((unsigned)(k * 128 / kPrRows), n), 256, 0, aux.lo>>>(ctx, k);
-        count_launch();
+        timed_launch(KFAC_K_INV_AUX, aux.lo,
+                     [&] { tc_probe_kernel<<<dim3((unsigned)(k * 128 / kPrRows), n), 256, 0, aux.lo>>>(ctx, k); });
       }
       early_any = true;
     }
@@ -1141,11 +1244,10 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       rc = KFAC_ERR_CUDA;
       break;
     }
-    tc_diag_kernel<<<n, 256, diag_smem_bytes<float>(), main>>>(ctx, b, k);
-    count_launch();
+    timed_launch(KFAC_K_INV_DIAG, main, [&] { tc_diag_kernel<<<n, 256, diag_smem_bytes<float>(), main>>>(ctx, b, k); });
     if (Tmax > 1) {
-      tc_prep_kernel<<<dim3((unsigned)(Tmax - 1), n), 256, 0, fork_prep ? aux.hi2 : main>>>(ctx, b, k);
-      count_launch();
+      cudaStream_t ps = fork_prep ? aux.hi2 : main;
+      timed_launch(KFAC_K_INV_PREP, ps, [&] { tc_prep_kernel<<<dim3((unsigned)(Tmax - 1), n), 256, 0, ps>>>(ctx, b, k); });
     }
     if (fork_prep && (cudaEventRecord(aux.prep1, aux.hi2) != cudaSuccess ||
                       cudaStreamWaitEvent(main, aux.prep1, 0) != cudaSuccess)) {
@@ -1191,8 +1293,8 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   if (rc == KFAC_OK && ctx.want_rowsum) {
     // y = X w needs the norms' w
     if (fork_ok && cudaStreamWaitEvent(main, aux.norms, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
-    tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, main>>>(ctx, t_last);
-    count_launch();
+    timed_launch(KFAC_K_INV_AUX, main,
+                 [&] { tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, main>>>(ctx, t_last); });
   }
   // the early X = U U^T and probes on the lowest-priority stream
   if (early_any && (cudaEventRecord(aux.lodone, aux.lo) != cudaSuccess ||

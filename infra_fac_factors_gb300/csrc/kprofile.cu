@@ -101,4 +101,32 @@ int kfac_profile_read(int kind, int64_t* launches, double* ms, double* work) {
   return KFAC_OK;
 }
 
+int kfac_profile_count(int64_t* count) {
+  if (!count) return KFAC_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(kfac::g_prof_mu);
+  for (const kfac::ProfRec& r : kfac::g_prof)
+    if (cudaEventSynchronize(r.end) != cudaSuccess) return KFAC_ERR_CUDA;
+  *count = (int64_t)kfac::g_prof.size();
+  return KFAC_OK;
+}
+
+int kfac_profile_launch(int64_t i, int* kind, double* start_ms, double* end_ms, double* work) {
+  if (!kind || !start_ms || !end_ms || !work) return KFAC_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(kfac::g_prof_mu);
+  if (i < 0 || i >= (int64_t)kfac::g_prof.size()) return KFAC_ERR_INVALID_ARG;
+  const kfac::ProfRec& first = kfac::g_prof[0];
+  const kfac::ProfRec& r = kfac::g_prof[(size_t)i];
+  if (cudaEventSynchronize(r.end) != cudaSuccess || cudaEventSynchronize(first.start) != cudaSuccess)
+    return KFAC_ERR_CUDA;
+  float a = 0.f, b = 0.f;
+  if (cudaEventElapsedTime(&a, first.start, r.start) != cudaSuccess ||
+      cudaEventElapsedTime(&b, first.start, r.end) != cudaSuccess)
+    return KFAC_ERR_CUDA;
+  *kind = r.kind;
+  *start_ms = a;
+  *end_ms = b;
+  *work = r.work;
+  return KFAC_OK;
+}
+
 }  // extern "C"

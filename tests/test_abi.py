@@ -32,7 +32,7 @@ def declared_functions():
 
 def test_exports_every_declared_function():
     names = declared_functions()
-    assert len(names) == 20
+    assert len(names) == 22
     out = subprocess.run(["nm", "-D", "--defined-only", capi.library_path], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (kfac_[a-z_0-9]+)$", out, flags=re.M))
     for n in names:
@@ -280,9 +280,12 @@ def test_profile_api_without_launches():
     capi.kfac_profile(True)
     for kind in capi.KERNEL_KINDS:
         assert capi.kfac_profile_read(kind) == {"launches": 0, "ms": 0.0, "work": 0.0}
+    assert capi.kfac_profile_count() == 0 and capi.kfac_profile_timeline() == []
     capi.kfac_profile(False)
     with pytest.raises(capi.KFACError):
         capi.kfac_profile_read(len(capi.KERNEL_KINDS))
+    with pytest.raises(capi.KFACError):
+        capi.kfac_profile_launch(0)
 
 
 def _run_host_program(src):

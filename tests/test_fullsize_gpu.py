@@ -51,8 +51,15 @@ def run():
 def test_all_inverses_succeeded_in_fp32(run):
     st = run["step"]
     assert (st.info.cpu().numpy() == 0).all()
-    # the BERT-large factors are well conditioned: AUTO keeps all of them in fp32
-    assert (st.route.cpu().numpy() == 0).all()
+    # the BERT-large factors are well conditioned: AUTO keeps all of them in the
+    # fp32 pass; the G factors (gamma I plus a factor about 1e-5 of it) have
+    # Gershgorin bounds near 1 and take 16-bit operands, the A factors 24-bit
+    route = st.route.cpu().numpy()
+    facs = st.factor_list()
+    for i, r in enumerate(route):
+        F = facs[st.inv_order[i]]
+        is_g = st.inv_order[i] >= len(st.layers)
+        assert r == (2 if is_g else 0), (i, F.d, r)
 
 
 def test_sampled_factor_entries(run):

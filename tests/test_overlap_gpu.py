@@ -82,3 +82,12 @@ def test_kernel_profile_counts_the_step_work():
     # the 16-bit GEMMs carry the layer's 2 M N K products; the 24-bit re-run picks its layers on the device
     assert abs(prof["gemm16"]["work"] - work["precond_flops"]) <= 1e-9 * work["precond_flops"]
     assert prof["gemm24"]["work"] == 0.0
+    for k in ("inv_diag", "inv_prep", "inv_aux"):  # the inverse's CUDA-core launches, timed without work
+        assert prof[k]["launches"] > 0 and prof[k]["work"] == 0.0, (k, prof[k])
+    # the timeline lists the same launches on one time axis
+    tl = capi.kfac_profile_timeline()
+    assert len(tl) == sum(p["launches"] for p in prof.values())
+    assert tl[0]["start_ms"] == 0.0 and all(0.0 <= e["start_ms"] <= e["end_ms"] for e in tl)
+    for k in capi.KERNEL_KINDS:
+        got = sum(e["end_ms"] - e["start_ms"] for e in tl if e["kind"] == k)
+        assert abs(got - prof[k]["ms"]) <= 1e-3 * max(prof[k]["ms"], 1.0), k

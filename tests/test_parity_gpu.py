@@ -196,7 +196,7 @@ def test_damped_inverse_batched_variable_sizes(refine):
     Xs, info, route = run_inverse(Ds, refine)
     assert (info == 0).all()
     if refine == capi.KFAC_REFINE_AUTO:
-        assert set(route.tolist()) <= {0, 1}, route
+        assert set(route.tolist()) <= {0, 1, 2}, route
     else:
         assert (route == (1 if refine == capi.KFAC_REFINE_ALWAYS else 0)).all(), route
     for D, X in zip(Ds, Xs):
@@ -229,6 +229,46 @@ def test_damped_inverse_auto_routes_ill_conditioned_to_fp64():
         ref, _ = oracle.spd_inverse(D.astype(np.float64))
         assert rel_fro(X, ref) <= 1e-3
         assert residual(X, D) <= 1e-3
+
+
+def gershgorin_ratio(D):
+    D = np.asarray(D, np.float64)
+    off = np.abs(D).sum(1) - np.abs(np.diag(D))
+    lo, hi = (np.diag(D) - off).min(), (np.diag(D) + off).max()
+    return hi / lo if lo > 0 else np.inf
+
+
+def test_damped_inverse_auto_takes_16bit_operands_when_gershgorin_allows():
+    # AUTO runs the fp32 pass with two-slice (16-bit) operands for a matrix whose
+    # Gershgorin discs bound its condition number by 16, and with three slices
+    # otherwise; the residual probe still checks both
+    rng = np.random.default_rng(31)
+    cases = []
+    for d in (1, 130, 640, 1025):  # G-like: gamma I plus a tiny factor (kappa ~ 1)
+        g = rng.standard_normal((256, d)) * 1e-4
+        cases.append(((g.T @ g / 256) + 1e-3 * np.eye(d)).astype(np.float32))
+    for scale, d in ((0.6, 300), (0.88, 300), (0.95, 300)):  # diagonally dominant: bounds ~4, ~15.7, ~39
+        M = rng.standard_normal((d, d))
+        M = (M + M.T) / 2
+        np.fill_diagonal(M, 0.0)
+        M *= scale / np.abs(M).sum(1).max()
+        cases.append((np.eye(d) + M).astype(np.float32))
+    cases.append(spd_case(257, rng))  # Wishart with rows ~ d: no Gershgorin bound
+    want = [2 if gershgorin_ratio(D) <= 16 else 0 for D in cases]
+    assert want == [2, 2, 2, 2, 2, 2, 0, 0]
+    Xs, info, route = run_inverse(cases, capi.KFAC_REFINE_AUTO)
+    assert (info == 0).all()
+    assert list(route) == want, route
+    Xn, _, route_n = run_inverse(cases, capi.KFAC_REFINE_NONE)
+    assert (route_n == 0).all()  # NONE keeps 24-bit operands for every matrix
+    for D, X, X24, r in zip(cases, Xs, Xn, route):
+        ref, _ = oracle.spd_inverse(D.astype(np.float64))
+        assert np.array_equal(X, X.T)
+        if r == 2:
+            assert rel_fro(X, ref) <= 1e-4 and residual(X, D) <= 1e-4, (D.shape, rel_fro(X, ref), residual(X, D))
+        else:
+            assert np.array_equal(X, X24)  # the 24-bit route is the NONE pass, bit for bit
+            assert rel_fro(X, ref) <= 1e-3 and residual(X, D) <= 1e-3
 
 
 def test_damped_inverse_reports_first_bad_pivot():
