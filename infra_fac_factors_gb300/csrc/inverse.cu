@@ -54,6 +54,10 @@ __global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, InvCtx c)
     s.xnorm2 = 0.f;
     s.est_res = 0.f;
     s.slices = 3;
+    s.glo = 0xffffffffu;
+    s.ghi = 0u;
+    s.gbad = 0;
+    s.gdone = 0;
     c.st[e] = s;
     c.flagged[e] = (int)e;
   }

@@ -37,6 +37,11 @@ struct InvState {
   float min_piv, kappa;
   float xnorm2, est_res;  // ||X||_F^2 and the estimated residual of the fp32 pass
   int slices;             // bf16 slices per operand in the fp32 pass: 3 (24-bit) or 2 (16-bit)
+  // AUTO's Gershgorin bound, gathered over the row blocks (tc_route_kernel):
+  // ordered bits of the smallest disc end and of the largest, a non-finite
+  // flag and the number of row blocks done
+  unsigned glo, ghi;
+  int gbad, gdone;
 };
 
 // Rademacher probe entry v_p(i) in {-1, +1} (splitmix64 finaliser of (i, p)).

@@ -64,13 +64,16 @@ enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
 // drained accumulator 35 % of the time instead of 4 %: the lanes' rows are
 // 128 B apart, so each reduction instruction touches 32 lines.)
 constexpr int kItOutBlock = 4096;  // one 32 x 32 fp32 block
+// The panel's epilogue warps pass their 32 rows through shared memory in
+// 64-column halves (32 x 64 fp32 each) on the way to the bf16 slice stores.
+constexpr int kItPanelStage = 32 * 64 * 4;
 template <int KIND>
 struct ItCfg {
   static constexpr int b_rows = KIND == kItPanel ? 128 : 256;
   static constexpr int stages = KIND == kItUpdate ? 2 : KIND == kItPanel ? 4 : 3;
   static constexpr int b_slice = b_rows * kItBK * 2;
   static constexpr int stage = kSlices * (kItA + b_slice);
-  static constexpr int out = KIND == kItUpdate ? 8 * 2 * kItOutBlock : 0;
+  static constexpr int out = KIND == kItUpdate ? 8 * 2 * kItOutBlock : KIND == kItPanel ? 4 * kItPanelStage : 0;
   static constexpr int smem = stages * stage + out + 1024 + 256;
 };
 
@@ -106,6 +109,7 @@ struct ItParams {
   long long total_jobs;
   int n, k;
   int upd_mode;  // update launches: kUpdInner / kUpdFull / kUpdNear / kUpdFar
+  int use_route; // 1 once the operand widths of AUTO are decided (before: three slices for all)
   int lp_off;    // first row of the current outer panel's Lp buffer (0 or R)
 };
 
@@ -186,7 +190,7 @@ __device__ ItJob it_decode(const ItParams& prm, long long u) {
   const int k = prm.k;
   J.m = m;
   J.valid = !prm.st[m].failed;
-  J.ns = prm.st[m].slices == 2 ? 2 : kSlices;
+  J.ns = (prm.use_route && prm.st[m].slices == 2) ? 2 : kSlices;
   J.i = J.j = 0;
   J.mode = 0;
   if (KIND == kItPanel) {
@@ -465,22 +469,40 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
       if (!ok || !mine) continue;
       const int mrow = q * 32 + lane;  // row of the 128-row output tile
       if (KIND == kItPanel) {
-        // L_rk (r > k) into Lp, or U_rk (r < k) into U, as three bf16 slices
-        uint16_t* dst;
-        long long sstride;
+        // L_rk (r > k) into Lp, or U_rk (r < k) into U, as three bf16 slices.
+        // The warp's 32 rows go through shared memory in two 64-column halves
+        // (16-byte chunks XOR-swizzled by row: conflict-free both ways), so
+        // that each store instruction writes four whole 128-byte row
+        // segments instead of 32 pieces of 32 different rows.
+        uint16_t* dst0;
+        long long sstride, ld;
         if (J.mode == 0) {
-          dst = prm.b.lp + (long long)(prm.lp_off + J.o_y + mrow) * kLpW + (long long)((J.o_x / 128) % kOuter) * 128;
+          dst0 = prm.b.lp + (long long)(prm.lp_off + J.o_y + q * 32) * kLpW + (long long)((J.o_x / 128) % kOuter) * 128;
           sstride = 2 * prm.b.R * kLpW;
+          ld = kLpW;
         } else {
-          dst = prm.b.u + (long long)(J.o_y + mrow) * prm.b.LD + J.o_x;
+          dst0 = prm.b.u + (long long)(J.o_y + q * 32) * prm.b.LD + J.o_x;
           sstride = prm.b.R * prm.b.LD;
+          ld = prm.b.LD;
         }
+        float* stg = reinterpret_cast<float*>(out_stage + e * kItPanelStage);
 #pragma unroll
-        for (int t = 0; t < 128; t += 8) {
-          float x8[8];
+        for (int hc = 0; hc < 2; ++hc) {
+          __syncwarp();  // the previous half has been read
 #pragma unroll
-          for (int e8 = 0; e8 < 8; ++e8) x8[e8] = run[t + e8];
-          split8_store(x8, dst + t, sstride);
+          for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<float4*>(stg + lane * 64 + ((j ^ (lane & 7)) << 2)) =
+                make_float4(run[hc * 64 + 4 * j], run[hc * 64 + 4 * j + 1], run[hc * 64 + 4 * j + 2],
+                            run[hc * 64 + 4 * j + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int r = it * 4 + lane / 8, k2 = 2 * (lane % 8);
+            const float4 v0 = *reinterpret_cast<const float4*>(stg + r * 64 + ((k2 ^ (r & 7)) << 2));
+            const float4 v1 = *reinterpret_cast<const float4*>(stg + r * 64 + (((k2 + 1) ^ (r & 7)) << 2));
+            const float x8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            split8_store(x8, dst0 + (long long)r * ld + hc * 64 + k2 * 4, sstride);
+          }
         }
       } else if (KIND == kItUpdate) {
         // -acc into Acc through 32 x 32 TMA add-reductions (or stores, first time)
@@ -550,13 +572,22 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
 }
 
 // ------------------------------------------------------------------ D -> Acc (lower blocks)
-__global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
+// Lower tiles counted column by column: block column C starts at tile
+// C T - C (C - 1) / 2 (T - C tiles each).
+__host__ __device__ inline long long load_col_start(long long C, long long T) { return C * T - C * (C - 1) / 2; }
+
+// The lower tiles of block columns [c_begin, c_end) of every matrix.
+__global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_begin, int c_end) {
   const int mi = blockIdx.y;
   if (!inv_active(c, mi, false)) return;
   const InvMat m = c.mats[mi];
-  const long long q = blockIdx.x;
-  if (q >= tri(m.T)) return;
-  const int R = tri_root(q), C = (int)(q - tri(R));  // lower tile (R, C), R >= C
+  const int ce = c_end < m.T ? c_end : m.T;
+  if (c_begin >= ce) return;
+  const long long q = load_col_start(c_begin, m.T) + blockIdx.x;
+  if (q >= load_col_start(ce, m.T)) return;
+  int C = c_begin;
+  while (load_col_start(C + 1, m.T) <= q) ++C;
+  const int R = C + (int)(q - load_col_start(C, m.T));  // lower tile (R, C), R >= C
   float* A = b.acc + m.row_off * b.LD;
   extern __shared__ __align__(16) uint8_t load_smem[];
   float* sub = reinterpret_cast<float*>(load_smem);  // 128 x 129: sub[i][j] = D[C*128 + i][R*128 + j]
@@ -647,29 +678,39 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b) {
 // ratio is at most kSlices16Kappa, the matrix is that well conditioned and its
 // fp32 pass runs with 16-bit operands (two slices); else with 24-bit ones.
 // The residual probe checks the result either way.
+__device__ __forceinline__ unsigned ordered_bits(float x) {  // monotone float -> unsigned map
+  const unsigned b = __float_as_uint(x);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float from_ordered_bits(unsigned u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+// One CTA per (128-row block, matrix): its rows' disc ends, reduced over the
+// CTA, then into the matrix's running min / max (exact, so the order of the
+// CTAs does not matter); the matrix's last CTA to finish takes the decision.
 __global__ void __launch_bounds__(128) tc_route_kernel(InvCtx c) {
-  const int mi = blockIdx.x;
+  const int mi = blockIdx.y;
   if (!inv_active(c, mi, false)) return;
   const InvMat m = c.mats[mi];
-  const float* gp = c.gpart + m.off_gpart;
+  const int b = blockIdx.x;
+  if (b >= m.T) return;
+  const float* gp = c.gpart + m.off_gpart + (long long)b * m.T * 128;
   __shared__ float slo[128], shi[128];
-  __shared__ int sbad;
+  __shared__ int sbad, slast;
   if (threadIdx.x == 0) sbad = 0;
   __syncthreads();
+  const long long r = (long long)b * 128 + threadIdx.x;
   float lo = 3.0e38f, hi = 0.f;
-  bool bad = false;
-  for (long long r = threadIdx.x; r < m.d; r += 128) {
-    const long long b = r / 128;
-    const int i = (int)(r % 128);
+  if (r < m.d) {
     float off = 0.f;
-    for (int cb = 0; cb < m.T; ++cb) off += gp[(b * m.T + cb) * 128 + i];
+#pragma unroll 8
+    for (int cb = 0; cb < m.T; ++cb) off += gp[(long long)cb * 128 + threadIdx.x];
     const float dg = m.D[r * m.ld_in + r] + c.gamma_extra;
-    const float l = dg - off, h = dg + off;
-    if (!isfinite(l) || !isfinite(h)) bad = true;
-    lo = fminf(lo, l);
-    hi = fmaxf(hi, h);
+    lo = dg - off;
+    hi = dg + off;
+    if (!isfinite(lo) || !isfinite(hi)) sbad = 1;
   }
-  if (bad) sbad = 1;
   slo[threadIdx.x] = lo;
   shi[threadIdx.x] = hi;
   __syncthreads();
@@ -680,8 +721,23 @@ __global__ void __launch_bounds__(128) tc_route_kernel(InvCtx c) {
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0)
-    c.st[mi].slices = (!sbad && slo[0] > 0.f && shi[0] <= kSlices16Kappa * slo[0]) ? 2 : kSlices;
+  if (threadIdx.x == 0) {
+    InvState& st = c.st[mi];
+    if (sbad) atomicOr(&st.gbad, 1);
+    atomicMin(&st.glo, ordered_bits(slo[0]));
+    atomicMax(&st.ghi, ordered_bits(shi[0]));
+    __threadfence();
+    slast = atomicAdd(&st.gdone, 1) == m.T - 1;
+  }
+  __syncthreads();
+  if (slast && threadIdx.x == 0) {
+    InvState& st = c.st[mi];
+    __threadfence();
+    const float glo = from_ordered_bits(atomicOr(&st.glo, 0u));
+    const float ghi = from_ordered_bits(atomicOr(&st.ghi, 0u));
+    const int bad = atomicOr(&st.gbad, 0);
+    st.slices = (!bad && glo > 0.f && ghi <= kSlices16Kappa * glo) ? 2 : kSlices;
+  }
 }
 
 // ------------------------------------------------------------------ ||D||_1 and w = D v (AUTO)
@@ -1039,13 +1095,14 @@ static int launch_it(ItParams* prm, const int* Ts, int n, int k, int grid_cap, c
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
 
-// Three streams of this library per device, two of highest and one of lowest
+// Five streams of this library per device, three of highest and two of lowest
 // priority, and the events that fork work from the caller's stream onto them
 // and join it back (created once, kept until exit).
 struct AuxStream {
-  cudaStream_t hi = nullptr, hi2 = nullptr, lo = nullptr;
+  cudaStream_t hi = nullptr, hi2 = nullptr, hi3 = nullptr, lo = nullptr, lo2 = nullptr;
   cudaEvent_t start = nullptr, fork = nullptr, join = nullptr, end = nullptr, norms = nullptr, early = nullptr,
-              lodone = nullptr, prep0 = nullptr, prep1 = nullptr;
+              lodone = nullptr, prep0 = nullptr, prep1 = nullptr, early2 = nullptr, lodone2 = nullptr,
+              loaded = nullptr;
 };
 // One set per (device, caller's stream), up to kAuxSets per device, so that
 // inverses issued on different streams run concurrently.  A further caller
@@ -1072,14 +1129,21 @@ static bool aux_stream(int dev, cudaStream_t caller, AuxStream* out) {
   if (!t.hi) {
     int least = 0, greatest = 0;
     if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
-    cudaEvent_t ev[9];
-    for (int i = 0; i < 9; ++i)
+    cudaEvent_t ev[12];
+    for (int i = 0; i < 12; ++i)
       if (cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) != cudaSuccess) return false;
-    cudaStream_t st, st2, sl;
+    cudaStream_t st, st2, st3, sl, sl2;
+    if (cudaStreamCreateWithPriority(&st3, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
     if (cudaStreamCreateWithPriority(&sl, cudaStreamNonBlocking, least) != cudaSuccess) return false;
+    if (cudaStreamCreateWithPriority(&sl2, cudaStreamNonBlocking, least) != cudaSuccess) return false;
     if (cudaStreamCreateWithPriority(&st2, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
     if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, greatest) != cudaSuccess) return false;
     t.lo = sl;
+    t.lo2 = sl2;
+    t.hi3 = st3;
+    t.early2 = ev[9];
+    t.lodone2 = ev[10];
+    t.loaded = ev[11];
     t.hi2 = st2;
     t.start = ev[0];
     t.fork = ev[1];
@@ -1199,12 +1263,41 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       rc = KFAC_ERR_CUDA;
     main = aux.hi;
   }
+  // D into the work buffer: the first outer panel's block columns on the
+  // sweep's stream, the rest (and AUTO's operand-width decision, which needs
+  // every row sum) on a third highest-priority stream beside the first steps
+  // of the sweep, which only touch the first outer panel; the sweep waits for
+  // them before its first outer update.  Until then every matrix runs with
+  // three slices.
+  bool split_load = false;
+  prm->use_route = ctx.gpart ? 0 : 1;
   if (rc == KFAC_OK) {
-    timed_launch(KFAC_K_INV_AUX, main,
-                 [&] { tc_load_kernel<<<dim3((unsigned)tri(Tmax), n), 256, kLoadSmem, main>>>(ctx, b); });
-    if (ctx.gpart) {
-      timed_launch(KFAC_K_INV_AUX, main, [&] { tc_route_kernel<<<n, 128, 0, main>>>(ctx); });
+    const int c_split = fork_ok && Tmax > kOuter ? kOuter : Tmax;
+    split_load = c_split < Tmax;
+    long long cnt_a = 0, cnt_b = 0;
+    for (int i = 0; i < n; ++i) {
+      const int ci = c_split < Ts[i] ? c_split : Ts[i];
+      const long long a = load_col_start(ci, Ts[i]);
+      cnt_a = a > cnt_a ? a : cnt_a;
+      const long long bb = tri(Ts[i]) - a;
+      cnt_b = bb > cnt_b ? bb : cnt_b;
     }
+    timed_launch(KFAC_K_INV_AUX, main, [&] {
+      tc_load_kernel<<<dim3((unsigned)cnt_a, n), 256, kLoadSmem, main>>>(ctx, b, 0, c_split);
+    });
+    cudaStream_t rs = main;  // where the rest of D and the decision go
+    if (split_load) {
+      rs = aux.hi3;
+      if (cudaStreamWaitEvent(rs, aux.start, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
+      timed_launch(KFAC_K_INV_AUX, rs, [&] {
+        tc_load_kernel<<<dim3((unsigned)cnt_b, n), 256, kLoadSmem, rs>>>(ctx, b, c_split, Tmax);
+      });
+      if (cudaEventRecord(aux.fork, main) != cudaSuccess || cudaStreamWaitEvent(rs, aux.fork, 0) != cudaSuccess)
+        rc = KFAC_ERR_CUDA;
+    }
+    if (ctx.gpart) timed_launch(KFAC_K_INV_AUX, rs, [&] { tc_route_kernel<<<dim3((unsigned)Tmax, n), 128, 0, rs>>>(ctx); });
+    if (split_load && (cudaEventRecord(aux.loaded, rs) != cudaSuccess)) rc = KFAC_ERR_CUDA;
+    if (!split_load) prm->use_route = 1;
     if (ctx.want_rowsum) {  // reads the caller's matrices only: beside the sweep, at lowest priority
       norms_forked = fork_ok;
       cudaStream_t ns = fork_ok ? aux.lo : stream;
@@ -1216,9 +1309,18 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   bool pending = false;  // a far update in flight on `stream`
   bool early_any = false;
   for (int k = 0; k < Tmax && rc == KFAC_OK; ++k) {
+    if (split_load && k == kOuter - 1) {
+      // the rest of D is in the work buffer and the operand widths are known
+      if (cudaStreamWaitEvent(main, aux.loaded, 0) != cudaSuccess) {
+        rc = KFAC_ERR_CUDA;
+        break;
+      }
+      prm->use_route = 1;
+    }
     // matrices of k block rows finished their sweep at step k - 1: their
     // X = U U^T and residual probe run now, at lowest priority, in CTAs of
-    // two jobs, beside the larger matrices' sweep
+    // two jobs, beside the larger matrices' sweep; the probes on a stream of
+    // their own, so that the next group's X = U U^T need not wait for them
     bool ends_here = false;
     for (int i = 0; i < n; ++i) ends_here = ends_here || Ts[i] == k;
     if (fork_ok && k > 0 && ends_here) {
@@ -1230,8 +1332,13 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       rc = launch_it<kItLauum>(prm, Ts, n, 0, (int)((lj + 1) / 2), aux.lo, kUpdInner, k);
       if (rc != KFAC_OK) break;
       if (ctx.want_rowsum) {
-        timed_launch(KFAC_K_INV_AUX, aux.lo,
-                     [&] { tc_probe_kernel<<<dim3((unsigned)(k * 128 / kPrRows), n), 256, 0, aux.lo>>>(ctx, k); });
+        if (cudaEventRecord(aux.early2, aux.lo) != cudaSuccess ||
+            cudaStreamWaitEvent(aux.lo2, aux.early2, 0) != cudaSuccess) {
+          rc = KFAC_ERR_CUDA;
+          break;
+        }
+        timed_launch(KFAC_K_INV_AUX, aux.lo2,
+                     [&] { tc_probe_kernel<<<dim3((unsigned)(k * 128 / kPrRows), n), 256, 0, aux.lo2>>>(ctx, k); });
       }
       early_any = true;
     }
@@ -1298,7 +1405,9 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   }
   // the early X = U U^T and probes on the lowest-priority stream
   if (early_any && (cudaEventRecord(aux.lodone, aux.lo) != cudaSuccess ||
-                    cudaStreamWaitEvent(main, aux.lodone, 0) != cudaSuccess))
+                    cudaStreamWaitEvent(main, aux.lodone, 0) != cudaSuccess ||
+                    cudaEventRecord(aux.lodone2, aux.lo2) != cudaSuccess ||
+                    cudaStreamWaitEvent(main, aux.lodone2, 0) != cudaSuccess))
     rc = KFAC_ERR_CUDA;
   // everything is ordered on the caller's stream again, also after an error
   if (fork_ok && (cudaEventRecord(aux.end, main) != cudaSuccess || cudaStreamWaitEvent(stream, aux.end, 0) != cudaSuccess))
