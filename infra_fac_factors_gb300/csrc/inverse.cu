@@ -22,8 +22,9 @@
 // refine = AUTO: the fp32 pass measures its own residual.  With kProbes
 // Rademacher vectors v (+-1 entries), w = D v and then y = X w are formed in
 // double-float arithmetic (fp32 pairs, ~48 bits), so ||y - v||^2 averaged over
-// the probes is an unbiased estimate of ||X D - I||_F^2 (inverse_tc.cu:
-// tc_norms_kernel, tc_probe_kernel).  Matrices whose estimated
+// the probes is an unbiased estimate of ||X D - I||_F^2 (inverse_tc.cu: w
+// from the partial sums tc_load_kernel leaves per tile, added up by
+// tc_route_kernel; y in tc_probe_kernel).  Matrices whose estimated
 // residual ||X D - I||_F / sqrt(d) exceeds 2.5e-4 (four times below the 1e-3
 // target), whose ||D||_1 / min L_jj^2 exceeds 3e5 (a guard on the relative
 // error), or whose fp32 factorisation failed, are redone in fp64; the fp64
@@ -343,7 +344,7 @@ __global__ void inv_finish_kernel(InvCtx c, int n, int* info, int* route) {
 
 // ------------------------------------------------------------------ host side
 struct InvLayout {
-  size_t mats_off, st_off, flag_off, rowsum_off, probe_off, gpart_off, region_off, total;
+  size_t mats_off, st_off, flag_off, rowsum_off, probe_off, gpart_off, wpart_off, region_off, total;
   TcLayout tc;
 };
 
@@ -374,7 +375,9 @@ static InvLayout inv_layout(int n, const kfac_inverse_args* args, int refine, lo
   L.probe_off = L.rowsum_off + align256(sizeof(float) * (size_t)rs);
   L.gpart_off = L.probe_off + align256(sizeof(float2) * (size_t)(2 * kProbes * rs));
   const size_t gpart_bytes = refine == KFAC_REFINE_AUTO ? align256(sizeof(float) * (size_t)gp) : 0;
-  L.region_off = L.gpart_off + gpart_bytes;
+  L.wpart_off = L.gpart_off + gpart_bytes;
+  const size_t wpart_bytes = refine == KFAC_REFINE_AUTO ? align256(sizeof(float2) * (size_t)gp * kProbes) : 0;
+  L.region_off = L.wpart_off + wpart_bytes;
   // the fp32 tensor-core pass and the fp64 pass run one after the other and
   // share the work region
   size_t fp64 = 0;
@@ -493,6 +496,7 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
     ctx.rowsum = reinterpret_cast<float*>(ws + L.rowsum_off);
     ctx.probe = reinterpret_cast<float2*>(ws + L.probe_off);
     ctx.gpart = refine == KFAC_REFINE_AUTO ? reinterpret_cast<float*>(ws + L.gpart_off) : nullptr;
+    ctx.wpart = refine == KFAC_REFINE_AUTO ? reinterpret_cast<float2*>(ws + L.wpart_off) : nullptr;
     ctx.region = ws + L.region_off;
     ctx.gamma_extra = gamma_extra;
     ctx.want_rowsum = refine == KFAC_REFINE_AUTO;

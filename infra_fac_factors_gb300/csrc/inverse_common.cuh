@@ -65,6 +65,7 @@ struct InvCtx {
   InvState* st;
   float* rowsum;
   float* gpart;     // AUTO: per matrix, partial sums of |D_rc| (c != r) over each 128-column block
+  float2* wpart;    // AUTO: per matrix, the same blocks' double-float partial sums of (D v_p)_r
   float2* probe;    // per matrix: w[kProbes][n_pad] then y[kProbes][n_pad], double-float (hi, lo)
   int* flagged;     // indices of the matrices the fp64 pass inverts
   int* nflagged;    // their count

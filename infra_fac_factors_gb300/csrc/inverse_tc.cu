@@ -47,9 +47,7 @@ constexpr int kItDrain = 2;
 // accumulator is drained every eight k-steps, as in the 16-bit GEMM of the
 // preconditioning
 constexpr int kItDrain16 = 8;
-constexpr int kLoadSmem = 128 * 129 * 4;
-constexpr int kNormsXch = 1 + 2 * kProbes;
-constexpr int kNormsSmem = (128 * 129 + kProbes * 128 + 128 * kNormsXch) * 4;
+constexpr int kLoadSmem = (128 * 129 + 2 * kProbes * 128) * 4;  // the tile, and the probe signs of its two blocks
 
 enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
 
@@ -608,34 +606,78 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_
   }
   __syncthreads();
   if (c.gpart) {
-    // AUTO: partial sums of |D_rc| over the tile for the Gershgorin bound of
-    // the 16-bit route (tc_route_kernel), without the diagonal: rows of block
-    // C along the tile's rows, rows of block R down its columns (the mirror);
-    // on a diagonal tile only its upper triangle counts, for both
-    // (columns of the tile at or past d hold whatever the float4 loads brought
-    // from the padding: they are left out; rows past d were loaded as zero)
+    // AUTO: per tile, for the rows of block C along the tile's rows and for
+    // the rows of block R down its columns (the mirror), the partial sums of
+    //   |D_rc| (c != r)      -> gpart: Gershgorin radii (tc_route_kernel) and ||D||_1
+    //   D_rc v_p(c)          -> wpart: w = D v for the residual probes
+    // with v_p the Rademacher probes (the products are exact, the sums
+    // double-float).  On a diagonal tile only its upper triangle counts, and
+    // the diagonal itself (with gamma_extra) goes into w only.  Columns of the
+    // tile at or past d hold whatever the float4 loads brought from the
+    // padding: they are left out; rows past d were loaded as zero.
+    float* vr = sub + 128 * 129;        // kProbes x 128 probe signs of block R's indices
+    float* vc = vr + kProbes * 128;     // and of block C's
+    for (int e = t; e < kProbes * 128; e += 256) {
+      const int p = e / 128, ii = e % 128;
+      vr[e] = (float)probe_sign((long long)R * 128 + ii, p);
+      vc[e] = (float)probe_sign((long long)C * 128 + ii, p);
+    }
+    __syncthreads();
     float* gp = c.gpart + m.off_gpart;
+    float2* wp = c.wpart + m.off_gpart * kProbes;
     const long long cleft = m.d - (long long)R * 128;
     const int jmax = cleft < 128 ? (int)cleft : 128;
+    float s = 0.f, whi[kProbes], wlo[kProbes];
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) whi[p] = wlo[p] = 0.f;
+    long long slot = -1;  // (row block, column block) of this thread's sums
+    int row = 0;
     if (R == C) {
       if (t < 128) {
-        float s = 0.f;
+        row = t;
+        slot = (long long)C * m.T + C;
         if (t < jmax) {
-          for (int j = t + 1; j < jmax; ++j) s += fabsf(sub[t * 129 + j]);
-          for (int i = 0; i < t; ++i) s += fabsf(sub[i * 129 + t]);
+          for (int j = t + 1; j < jmax; ++j) {
+            const float x = sub[t * 129 + j];
+            s += fabsf(x);
+#pragma unroll
+            for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vr[p * 128 + j]);
+          }
+          for (int i2 = 0; i2 < t; ++i2) {
+            const float x = sub[i2 * 129 + t];
+            s += fabsf(x);
+#pragma unroll
+            for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vc[p * 128 + i2]);
+          }
+          const float dg = sub[t * 129 + t] + c.gamma_extra;
+#pragma unroll
+          for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], dg * vc[p * 128 + t]);
         }
-        gp[((long long)C * m.T + C) * 128 + t] = s;
       }
     } else if (t < 128) {
-      float s = 0.f;
-      for (int j = 0; j < jmax; ++j) s += fabsf(sub[t * 129 + j]);
-      gp[((long long)C * m.T + R) * 128 + t] = s;
+      row = t;
+      slot = (long long)C * m.T + R;
+      for (int j = 0; j < jmax; ++j) {
+        const float x = sub[t * 129 + j];
+        s += fabsf(x);
+#pragma unroll
+        for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vr[p * 128 + j]);
+      }
     } else {
-      const int j = t - 128;
-      float s = 0.f;
-      if (j < jmax)
-        for (int i = 0; i < 128; ++i) s += fabsf(sub[i * 129 + j]);
-      gp[((long long)R * m.T + C) * 128 + j] = s;
+      row = t - 128;
+      slot = (long long)R * m.T + C;
+      if (row < jmax)
+        for (int i2 = 0; i2 < 128; ++i2) {
+          const float x = sub[i2 * 129 + row];
+          s += fabsf(x);
+#pragma unroll
+          for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vc[p * 128 + i2]);
+        }
+    }
+    if (slot >= 0) {
+      gp[slot * 128 + row] = s;
+#pragma unroll
+      for (int p = 0; p < kProbes; ++p) wp[(slot * kProbes + p) * 128 + row] = make_float2(whi[p], wlo[p]);
     }
   }
   // write the lower tile (R, C) of the work buffer along its rows: element
@@ -710,6 +752,20 @@ __global__ void __launch_bounds__(128) tc_route_kernel(InvCtx c) {
     lo = dg - off;
     hi = dg + off;
     if (!isfinite(lo) || !isfinite(hi)) sbad = 1;
+    // ||D||_1 row sum, and w = D v for the residual probes, from the load's partial sums
+    c.rowsum[m.off_rowsum + r] = off + fabsf(dg);
+    const float2* wp = c.wpart + (m.off_gpart + (long long)b * m.T * 128) * kProbes;
+    const long long np = (long long)m.T * 128;
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) {
+      float whi = 0.f, wlo = 0.f;
+      for (int cb = 0; cb < m.T; ++cb) {
+        const float2 v = wp[((long long)cb * kProbes + p) * 128 + threadIdx.x];
+        df_add(whi, wlo, v.x);
+        wlo += v.y;
+      }
+      c.probe[m.off_probe + p * np + r] = df_pack(whi, wlo);
+    }
   }
   slo[threadIdx.x] = lo;
   shi[threadIdx.x] = hi;
@@ -737,94 +793,6 @@ __global__ void __launch_bounds__(128) tc_route_kernel(InvCtx c) {
     const float ghi = from_ordered_bits(atomicOr(&st.ghi, 0u));
     const int bad = atomicOr(&st.gbad, 0);
     st.slices = (!bad && glo > 0.f && ghi <= kSlices16Kappa * glo) ? 2 : kSlices;
-  }
-}
-
-// ------------------------------------------------------------------ ||D||_1 and w = D v (AUTO)
-// One CTA per 128-row block R of a matrix, straight from the upper triangle of
-// the caller's damped matrix plus gamma_extra on the diagonal, so that it can
-// run beside the sweep: the rows of R gather their
-// sums from the tiles (R, C >= R) row-wise and from the tiles (C < R, R)
-// column-wise, and no atomics are needed.  Each row is split between two
-// threads (64 columns of every tile each); the probe sums w = D v are
-// double-float (the products with v = +-1 are exact).
-__global__ void __launch_bounds__(256) tc_norms_kernel(InvCtx c) {
-  const int mi = blockIdx.y;
-  if (!inv_active(c, mi, false)) return;
-  const InvMat m = c.mats[mi];
-  const int R = blockIdx.x;
-  if (R >= m.T) return;
-  extern __shared__ __align__(16) uint8_t norms_smem[];
-  float* tile = reinterpret_cast<float*>(norms_smem);  // 128 x 129
-  float* vs = tile + 128 * 129;                        // kProbes x 128 probe signs of the tile's columns
-  float* xch = vs + kProbes * 128;                     // 128 x kNormsXch sums of the second half of the threads
-  const int t = threadIdx.x, row = t % 128, half = t / 128;
-  float asum = 0.f;  // row abs sum (a norm for a threshold: plain fp32)
-  float whi[kProbes], wlo[kProbes];
-#pragma unroll
-  for (int p = 0; p < kProbes; ++p) whi[p] = wlo[p] = 0.f;
-  const long long r = (long long)R * 128 + row;
-  for (int C = 0; C < m.T; ++C) {
-    const bool rowwise = C >= R;  // tile (R, C) read along rows; else tile (C, R) along columns
-    const long long sr = (long long)(rowwise ? R : C) * 128, sc = (long long)(rowwise ? C : R) * 128;
-    __syncthreads();
-    for (int e = t; e < 128 * 32; e += 256) {  // 128 rows x 32 float4; ld_in % 4 == 0 keeps them in the row
-      const int rr = e / 32, c4 = (e % 32) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      const long long gr = sr + rr, gc = sc + c4;
-      if (gr < m.d && gc < m.d) {
-        v = *reinterpret_cast<const float4*>(m.D + gr * m.ld_in + gc);
-        if (gc + 1 >= m.d) v.y = 0.f;
-        if (gc + 2 >= m.d) v.z = 0.f;
-        if (gc + 3 >= m.d) v.w = 0.f;
-      }
-      float* dst = tile + rr * 129 + c4;
-      dst[0] = v.x;
-      dst[1] = v.y;
-      dst[2] = v.z;
-      dst[3] = v.w;
-    }
-    for (int e = t; e < kProbes * 128; e += 256) {
-      const int p = e / 128, i = e % 128;
-      vs[p * 128 + i] = (float)probe_sign((long long)C * 128 + i, p);
-    }
-    __syncthreads();
-    const long long left = m.d - ((long long)C * 128 + 64 * half);  // columns of this half inside d
-    const int iend = left < 0 ? 0 : (left < 64 ? (int)left : 64);
-    if (r < m.d) {
-#pragma unroll 4
-      for (int ii = 0; ii < iend; ++ii) {
-        const int i = 64 * half + ii;
-        // the caller's matrix is read on and above the diagonal only: the
-        // diagonal tile's lower part comes from its mirror
-        float x = (rowwise && !(C == R && i < row)) ? tile[row * 129 + i] : tile[i * 129 + row];
-        if (C == R && i == row) x += c.gamma_extra;
-        asum += fabsf(x);
-#pragma unroll
-        for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vs[p * 128 + i]);  // exact products
-      }
-    }
-  }
-  __syncthreads();
-  if (half == 1) {
-    xch[row * kNormsXch] = asum;
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) {
-      xch[row * kNormsXch + 1 + 2 * p] = whi[p];
-      xch[row * kNormsXch + 2 + 2 * p] = wlo[p];
-    }
-  }
-  __syncthreads();
-  if (half == 0 && r < m.d) {
-    asum += xch[row * kNormsXch];
-    c.rowsum[m.off_rowsum + r] = asum;
-    const long long np = (long long)m.T * 128;
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) {
-      df_add(whi[p], wlo[p], xch[row * kNormsXch + 1 + 2 * p]);
-      wlo[p] += xch[row * kNormsXch + 2 + 2 * p];
-      c.probe[m.off_probe + p * np + r] = df_pack(whi[p], wlo[p]);
-    }
   }
 }
 
@@ -1198,7 +1166,6 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItUpdate>, ItCfg<kItUpdate>::smem) ||
       !ensure_smem_attr(dev, (const void*)inv_tc_kernel<kItLauum>, ItCfg<kItLauum>::smem) ||
       !ensure_smem_attr(dev, (const void*)tc_diag_kernel, diag_smem_bytes<float>()) ||
-      !ensure_smem_attr(dev, (const void*)tc_norms_kernel, kNormsSmem) ||
       !ensure_smem_attr(dev, (const void*)tc_load_kernel, kLoadSmem))
     return KFAC_ERR_CUDA;
   int* status = device_status_ptr();
@@ -1257,7 +1224,6 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   AuxStream aux;
   const bool fork_ok = aux_stream(dev, stream, &aux);
   cudaStream_t main = stream;  // the sweep's stream
-  bool norms_forked = false;
   if (fork_ok) {
     if (cudaEventRecord(aux.start, stream) != cudaSuccess || cudaStreamWaitEvent(aux.hi, aux.start, 0) != cudaSuccess)
       rc = KFAC_ERR_CUDA;
@@ -1287,24 +1253,24 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
     });
     cudaStream_t rs = main;  // where the rest of D and the decision go
     if (split_load) {
+      // the rest of D at lowest priority (its CTAs take the SMs the first
+      // steps leave free), the decision at highest once both parts are in
       rs = aux.hi3;
-      if (cudaStreamWaitEvent(rs, aux.start, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
-      timed_launch(KFAC_K_INV_AUX, rs, [&] {
-        tc_load_kernel<<<dim3((unsigned)cnt_b, n), 256, kLoadSmem, rs>>>(ctx, b, c_split, Tmax);
+      if (cudaStreamWaitEvent(aux.lo, aux.start, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
+      timed_launch(KFAC_K_INV_AUX, aux.lo, [&] {
+        tc_load_kernel<<<dim3((unsigned)cnt_b, n), 256, kLoadSmem, aux.lo>>>(ctx, b, c_split, Tmax);
       });
-      if (cudaEventRecord(aux.fork, main) != cudaSuccess || cudaStreamWaitEvent(rs, aux.fork, 0) != cudaSuccess)
+      if (cudaEventRecord(aux.norms, aux.lo) != cudaSuccess || cudaStreamWaitEvent(rs, aux.norms, 0) != cudaSuccess ||
+          cudaEventRecord(aux.fork, main) != cudaSuccess || cudaStreamWaitEvent(rs, aux.fork, 0) != cudaSuccess)
         rc = KFAC_ERR_CUDA;
     }
     if (ctx.gpart) timed_launch(KFAC_K_INV_AUX, rs, [&] { tc_route_kernel<<<dim3((unsigned)Tmax, n), 128, 0, rs>>>(ctx); });
-    if (split_load && (cudaEventRecord(aux.loaded, rs) != cudaSuccess)) rc = KFAC_ERR_CUDA;
+    // the residual probes read the decision kernel's w = D v: the early ones
+    // (on lo2) may be issued before the sweep has waited for it
+    if (split_load && (cudaEventRecord(aux.loaded, rs) != cudaSuccess ||
+                       cudaStreamWaitEvent(aux.lo2, aux.loaded, 0) != cudaSuccess))
+      rc = KFAC_ERR_CUDA;
     if (!split_load) prm->use_route = 1;
-    if (ctx.want_rowsum) {  // reads the caller's matrices only: beside the sweep, at lowest priority
-      norms_forked = fork_ok;
-      cudaStream_t ns = fork_ok ? aux.lo : stream;
-      if (fork_ok && cudaStreamWaitEvent(aux.lo, aux.start, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
-      timed_launch(KFAC_K_INV_AUX, ns, [&] { tc_norms_kernel<<<dim3((unsigned)Tmax, n), 256, kNormsSmem, ns>>>(ctx); });
-      if (fork_ok && cudaEventRecord(aux.norms, aux.lo) != cudaSuccess) rc = KFAC_ERR_CUDA;
-    }
   }
   bool pending = false;  // a far update in flight on `stream`
   bool early_any = false;
@@ -1398,8 +1364,7 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   const int t_last = early_any ? Tmax : 0;
   if (rc == KFAC_OK) rc = launch_it<kItLauum>(prm, Ts, n, 0, sms, main, kUpdInner, t_last);
   if (rc == KFAC_OK && ctx.want_rowsum) {
-    // y = X w needs the norms' w
-    if (fork_ok && cudaStreamWaitEvent(main, aux.norms, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
+    // y = X w (w = D v from the decision kernel, ordered before on this stream)
     timed_launch(KFAC_K_INV_AUX, main,
                  [&] { tc_probe_kernel<<<dim3((unsigned)(Tmax * 128 / kPrRows), n), 256, 0, main>>>(ctx, t_last); });
   }
@@ -1412,7 +1377,6 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
   // everything is ordered on the caller's stream again, also after an error
   if (fork_ok && (cudaEventRecord(aux.end, main) != cudaSuccess || cudaStreamWaitEvent(stream, aux.end, 0) != cudaSuccess))
     rc = KFAC_ERR_CUDA;
-  if (norms_forked && cudaStreamWaitEvent(stream, aux.norms, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
   delete prm;
   if (rc == KFAC_OK && cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
   return rc;
