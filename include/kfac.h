@@ -98,6 +98,7 @@ int kfac_device_status(int* status_out, int clear, void* stream);
  *   KFAC_K_INV_DIAG    inverse: 128 x 128 diagonal blocks (CUDA cores)  work: 0
  *   KFAC_K_INV_PREP    inverse: block-column slicing (CUDA cores)       work: 0
  *   KFAC_K_INV_AUX     inverse: load, operand width, norms, residual probe, flags (CUDA cores)  work: 0
+ *   KFAC_K_INV_NEWTON  inverse: the Newton step of AUTO (slicing, exact products, symmetrisation)  work: 0
  * Recording holds at most 65536 launches (later ones are not recorded).
  * Invalid kind: KFAC_ERR_INVALID_ARG.
  * kfac_profile_count gives the number of recorded launches and
@@ -109,8 +110,8 @@ int kfac_device_status(int* status_out, int clear, void* stream);
 typedef enum {
   KFAC_K_SYRK = 0, KFAC_K_RUNNING = 1, KFAC_K_INV_PANEL = 2, KFAC_K_INV_UPDATE = 3,
   KFAC_K_INV_LAUUM = 4, KFAC_K_GEMM16 = 5, KFAC_K_GEMM24 = 6, KFAC_K_CONV_SYRK = 7,
-  KFAC_K_INV_DIAG = 8, KFAC_K_INV_PREP = 9, KFAC_K_INV_AUX = 10,
-  KFAC_K_COUNT = 11
+  KFAC_K_INV_DIAG = 8, KFAC_K_INV_PREP = 9, KFAC_K_INV_AUX = 10, KFAC_K_INV_NEWTON = 11,
+  KFAC_K_COUNT = 12
 } kfac_kernel_kind;
 int kfac_profile(int enable);
 int kfac_profile_read(int kind, int64_t* launches, double* ms, double* work);
@@ -233,17 +234,21 @@ int kfac_update_running(int n, const kfac_running_args* args, int P,
  *         KFAC_REFINE_AUTO   fp32, with 16-bit operands (two slices, three
  *                            MMAs) for a matrix whose Gershgorin discs bound its
  *                            condition number by 16 and 24-bit ones otherwise;
- *                            then a matrix is recomputed in fp64 when its
- *                            residual ||inv D - I||_F / sqrt(d), estimated
- *                            with four random +-1 probes, exceeds 2.5e-4, when
- *                            ||D||_1 / min_j L_jj^2 exceeds 3e5, or when its
+ *                            a matrix whose residual ||inv D - I||_F / sqrt(d),
+ *                            estimated with four random +-1 probes, exceeds
+ *                            2.5e-4, or whose ||D||_1 / min_j L_jj^2 exceeds
+ *                            3e5, then gets one Newton step
+ *                            inv + inv (I - D inv) on tensor cores, its
+ *                            residual formed exactly (error-free bf16 slices),
+ *                            and is recomputed in fp64 when the step's
+ *                            estimated residual still exceeds 5e-4 or when its
  *                            fp32 factorisation failed;
  *         KFAC_REFINE_ALWAYS fp64 arithmetic for every matrix.
  * info: device int[n]; info[i] = 0 on success, k > 0 when the k-th pivot
  *       (1-based) is not positive (LAPACK potrf convention); inv_i is then
  *       unspecified.  route (device int[n], may be NULL): 0 when inv_i came
- *       from the fp32 pass with 24-bit operands, 2 with 16-bit operands, 1
- *       from the fp64 pass.
+ *       from the fp32 pass with 24-bit operands, 2 with 16-bit operands, 3
+ *       from the Newton step after it, 1 from the fp64 pass.
  * ld_in, ld_out % 4 == 0.  n <= 4096, 1 <= d <= 65536.
  * Workspace: kfac_damped_inverse_workspace(n, args, refine) bytes, 256-byte
  * aligned, fully overwritten (no initialisation needed).

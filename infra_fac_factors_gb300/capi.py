@@ -30,7 +30,7 @@ KFAC_BF16, KFAC_FP32 = 0, 1
 KFAC_REFINE_NONE, KFAC_REFINE_AUTO, KFAC_REFINE_ALWAYS = 0, 1, 2
 KFAC_PRECOND_FP32, KFAC_PRECOND_AUTO = 0, 1
 KERNEL_KINDS = ("syrk", "running", "inv_panel", "inv_update", "inv_lauum", "gemm16", "gemm24", "conv_syrk",
-                "inv_diag", "inv_prep", "inv_aux")
+                "inv_diag", "inv_prep", "inv_aux", "inv_newton")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libkfac_gb300.so")

@@ -59,6 +59,8 @@ __global__ void inv_setup_kernel(const __grid_constant__ InvSetup prm, InvCtx c)
     s.ghi = 0u;
     s.gbad = 0;
     s.gdone = 0;
+    s.refine = 0;
+    s.refined = 0;
     c.st[e] = s;
     c.flagged[e] = (int)e;
   }
@@ -339,7 +341,7 @@ __global__ void inv_finish_kernel(InvCtx c, int n, int* info, int* route) {
   if (i >= n) return;
   const InvState s = c.st[i];
   info[i] = s.use64 ? s.info64 : s.info32;
-  if (route) route[i] = s.use64 ? 1 : (s.slices == 2 ? 2 : 0);
+  if (route) route[i] = s.use64 ? 1 : s.refined ? 3 : (s.slices == 2 ? 2 : 0);
 }
 
 // ------------------------------------------------------------------ host side
@@ -389,7 +391,17 @@ static InvLayout inv_layout(int n, const kfac_inverse_args* args, int refine, lo
     }
   L.tc = tc_layout(n, Ts);
   const size_t fp32 = refine != KFAC_REFINE_ALWAYS ? L.tc.bytes : 0;
-  L.total = L.region_off + (fp64 > fp32 ? fp64 : fp32);
+  // AUTO: the tensor-core Newton step (refine.cu) runs between the fp32 pass
+  // and the fp64 pass, on the same region, with its own per-matrix buffers
+  size_t ref = 0;
+  if (refine == KFAC_REFINE_AUTO)
+    for (int i = 0; i < n; ++i) {
+      if (mats) mats[i].off_ref = (long long)ref;
+      ref += align256(refine_bytes((long long)Ts[i] * 128));
+    }
+  size_t region = fp64 > fp32 ? fp64 : fp32;
+  if (ref > region) region = ref;
+  L.total = L.region_off + region;
   return L;
 }
 
@@ -519,6 +531,10 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
       inv_flag_kernel<<<cnt, 128, 0, stream>>>(ctx);
       prof_end(KFAC_K_INV_AUX, stream, pm, 0.0);
       count_launch();
+      // the flagged matrices first get one Newton step on tensor cores; those
+      // it settles leave the fp64 pass's list
+      rc = run_refine_pass(ctx, cnt, Tmax, stream);
+      if (rc != KFAC_OK) return rc;
     }
     if (refine != KFAC_REFINE_NONE) {
       ctx.pass64 = 1;

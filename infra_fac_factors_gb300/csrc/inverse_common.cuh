@@ -29,6 +29,7 @@ struct InvMat {
   long long off_probe;   // double index of this matrix's probe vectors w, y
   long long row_off;     // first row of this matrix in the stacked fp32 work buffers
   long long off_gpart;   // float index of this matrix's partial off-diagonal row sums (T x T x 128)
+  long long off_ref;     // byte offset of the refinement buffers in the work region (AUTO)
   int d, T;
 };
 
@@ -42,6 +43,8 @@ struct InvState {
   // flag and the number of row blocks done
   unsigned glo, ghi;
   int gbad, gdone;
+  int refine;   // AUTO sent it away from the fp32 pass and its fp32 factorisation succeeded
+  int refined;  // its inverse came from the tensor-core Newton step (refine.cu)
 };
 
 // Rademacher probe entry v_p(i) in {-1, +1} (splitmix64 finaliser of (i, p)).
@@ -347,6 +350,11 @@ struct TcLayout {
   size_t bytes;
 };
 TcLayout tc_layout(int n, const int* T);
+// refine.cu: bytes of one matrix's refinement buffers (np = 128 T), and the pass
+size_t refine_bytes(long long np);
+int run_refine_pass(const InvCtx& ctx, int n, int Tmax, cudaStream_t stream);
+// inverse_tc.cu: the residual probe y = X w over the refinement candidates
+int run_refined_probe(const InvCtx& ctx, int sms, cudaStream_t stream);
 int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, const int* Ts, const TcLayout& L,
                 cudaStream_t stream);
 

@@ -895,13 +895,13 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(InvCtx c, TcBufs b, int k)
 // rows of its warp, so w is read once per strip.  Double-float products and sums.
 constexpr int kPrWarpRows = 4;
 constexpr int kPrRows = 8 * kPrWarpRows;
-__global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c, int t_only) {
-  const int mi = blockIdx.y;
-  if (!inv_active(c, mi, true)) return;
+// y = X w over one strip of kPrRows rows of matrix mi (each warp its own
+// kPrWarpRows rows; no block-wide synchronisation); ||X||_F^2 of the strip is
+// added to the matrix's state when count_norm is set.
+__device__ void probe_strip(const InvCtx& c, int mi, long long strip, bool count_norm) {
   const InvMat m = c.mats[mi];
-  if (t_only && m.T != t_only) return;  // only the matrices of T block rows
-  const long long rw = (long long)blockIdx.x * kPrRows + (threadIdx.x / 32) * kPrWarpRows;  // the warp's first row
-  if ((long long)blockIdx.x * kPrRows >= m.d) return;
+  const long long rw = strip * kPrRows + (threadIdx.x / 32) * kPrWarpRows;  // the warp's first row
+  if (strip * kPrRows >= m.d) return;
   const int lane = threadIdx.x % 32;
   const long long np = (long long)m.T * 128;
   const float2* w = c.probe + m.off_probe;
@@ -951,11 +951,32 @@ __global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c, int t_only) {
     }
   }
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-  if (lane == 0 && nrow > 0) atomicAdd(&c.st[mi].xnorm2, sq);
+  if (lane == 0 && nrow > 0 && count_norm) atomicAdd(&c.st[mi].xnorm2, sq);
+}
+
+__global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c, int t_only) {
+  const int mi = blockIdx.y;
+  if (!inv_active(c, mi, true)) return;
+  if (t_only && c.mats[mi].T != t_only) return;  // only the matrices of T block rows
+  probe_strip(c, mi, blockIdx.x, true);
+}
+
+// The same over the Newton step's candidates (refine.cu), a persistent grid
+// over the flagged list: nothing runs when no matrix is flagged.
+__global__ void __launch_bounds__(256) rf_probe_kernel(InvCtx c) {
+  const int nf = *c.nflagged;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = c.flagged[f];
+    if (!c.st[mi].refine) continue;
+    for (long long strip = blockIdx.x; strip * kPrRows < c.mats[mi].d; strip += gridDim.x)
+      probe_strip(c, mi, strip, false);
+  }
 }
 
 // ------------------------------------------------------------------ host side
 static size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+
+
 
 TcLayout tc_layout(int n, const int* T) {
   TcLayout L;
@@ -1148,6 +1169,11 @@ static void timed_launch(int kind, cudaStream_t stream, F&& launch) {
   launch();
   prof_end(kind, stream, pm, 0.0);
   count_launch();
+}
+
+int run_refined_probe(const InvCtx& ctx, int sms, cudaStream_t stream) {
+  timed_launch(KFAC_K_INV_AUX, stream, [&] { rf_probe_kernel<<<4 * sms, 256, 0, stream>>>(ctx); });
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
 
 // Jobs per CTA of a far update: its CTAs retire every few jobs, so that the

@@ -1,0 +1,517 @@
+// Refinement, on tensor cores, of the inverses that AUTO does not accept from
+// the fp32 pass (SPD-KFAC §IV: the inverse of each damped factor; its accuracy
+// is this library's own concern).  One Newton step
+//
+//     X1 = X0 + X0 (I - D X0),      D symmetric, X0 the fp32 pass's inverse,
+//
+// halves the number of correct digits lost to D's conditioning, provided the
+// residual I - D X0 is formed well beyond fp32 accuracy: its entries are
+// differences of products that are up to kappa(D) times larger than they are.
+// The products are therefore taken exactly, in the error-free split of Ozaki,
+// Ogita, Oishi and Rump (fixed-point slices that share one exponent per row,
+// so that every bf16 x bf16 tensor-core product of two slices is an integer
+// multiple of one power of two and a short sum of them is exact in fp32):
+//
+//   split   x_rc = 2^e_r (sum_{s=1..6} q_s(r, c) 2^(-8 s)),  q_s integers, |q_s| <= 256,
+//           e_r the exponent of the largest |x_r.| (each slice a bf16 value
+//           q_s 2^(-8 s), exact);
+//   product (A B^T)_ij = 2^(e_i + f_j) sum_{s,t} sum_k a_s(i, k) b_t(j, k),
+//           the pairs grouped by level L = s + t: every product of one level
+//           is an integer multiple of 2^(-8 L), so the sum of the level's
+//           pairs over one 32-wide k-block (at most four pairs below level 5,
+//           |q q'| <= 2^16) stays below 2^24 and is exact in a tensor-core
+//           fp32 accumulator.  Levels 2, 3 and 4 get an accumulator each;
+//           levels 5 to 7 share one (their rounding error is below 2^-48 of the
+//           products).  Each k-block's accumulators are drained into
+//           double-float sums (fp32 pairs) by the epilogue warps.
+//
+// Host emulation on the ResNet-50 C = 512 conv factor (d = 4609,
+// kappa = 7.4e5): six slices with the pairs up to level 7 (21 MMAs per 16-wide
+// k-step) form the residual to 1.4e-9 (RMS) and the step lands on the fp32
+// storage floor of the inverse, ||X1 D - I||_F / sqrt(d) = 2.3e-4 (1.0e-3
+// before), relative error 8.5e-8; pairs up to level 6 leave 4.5e-7 in the
+// residual and 2.0e-3 after the step.  The correction X0 (I - D X0) needs
+// only three slices and the pairs up to level 4 (six MMAs).
+//
+// Steps, all on the device and only for the matrices AUTO flagged whose fp32
+// factorisation succeeded (the others exit at once):
+//   rf_split_kernel   D (upper triangle, + gamma_extra) and X0 into slices
+//   rf_gemm_kernel    S = I - X0 D = (I - D X0)^T   (levels up to 7)
+//   rf_split_kernel   S into slices
+//   rf_gemm_kernel    T = X0 S^T = X0 (I - D X0)    (levels up to 4)
+//   rf_sym_kernel     X1 = X0 + (T + T^T) / 2, written over X0 (exactly symmetric)
+// then the residual probe runs on X1 and a matrix whose estimate meets the
+// refined bar keeps X1; the others go on to the fp64 pass.
+#include "common.cuh"
+#include "inverse_common.cuh"
+#include "launch.h"
+
+namespace kfac {
+
+constexpr int kRfSlices = 6;
+constexpr int kRfBK = 32;                              // k of one stage (one drain)
+constexpr int kRfM = 128, kRfN = 64;                   // output tile
+constexpr int kRfA = kRfM * kRfBK * 2;                 // one A slice of a stage: 8 KB
+constexpr int kRfB = kRfN * kRfBK * 2;                 // one B slice: 4 KB
+constexpr int kRfStage = kRfSlices * (kRfA + kRfB);    // 72 KB
+constexpr int kRfStages = 3;
+constexpr int kRfProducers = 128;                      // warps 0-3 fill the stages (cp.async)
+constexpr int kRfThreads = kRfProducers + 32 + 256;    // + MMA warp + eight epilogue warps
+constexpr int kRfSmem = kRfStages * kRfStage + 1024 + 256;
+constexpr int kRfAcc = 4;                              // accumulators: levels 2, 3, 4, 5-7
+
+// Per-matrix refinement buffers, at m.off_ref in the work region (np = 128 T):
+//   xs  bf16 [6][np][np]   slices of X0
+//   bs  bf16 [6][np][np]   slices of D, then of S
+//   st  fp32 [np][np]      S, then T
+//   ex, eb  int [np]       row exponents of xs and bs
+struct RfBufs {
+  uint16_t* xs;
+  uint16_t* bs;
+  float* st;
+  int* ex;
+  int* eb;
+};
+__host__ __device__ inline size_t rf_bytes(long long np) {
+  return (size_t)np * np * (2 * kRfSlices * 2 + 4) + (size_t)np * 8;
+}
+__device__ __forceinline__ RfBufs rf_bufs(const InvCtx& c, const InvMat& m) {
+  const long long np = (long long)m.T * 128;
+  uint8_t* base = c.region + m.off_ref;
+  RfBufs b;
+  b.xs = reinterpret_cast<uint16_t*>(base);
+  b.bs = b.xs + (size_t)kRfSlices * np * np;
+  b.st = reinterpret_cast<float*>(b.bs + (size_t)kRfSlices * np * np);
+  b.ex = reinterpret_cast<int*>(b.st + (size_t)np * np);
+  b.eb = b.ex + np;
+  return b;
+}
+
+// the f-th matrix of the flagged list, when it is a refinement candidate
+__device__ __forceinline__ int rf_matrix(const InvCtx& c, int f) {
+  if (f >= *c.nflagged) return -1;
+  const int mi = c.flagged[f];
+  return c.st[mi].refine ? mi : -1;
+}
+
+// ------------------------------------------------------------------ candidates
+// Matrices AUTO sends away from the fp32 pass whose fp32 factorisation succeeded.
+__global__ void rf_mark_kernel(InvCtx c, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  InvState& s = c.st[i];
+  s.refine = (s.use64 && s.info32 == 0) ? 1 : 0;
+  s.refined = 0;
+}
+
+// ------------------------------------------------------------------ split
+// One warp per row: the largest |x_r.| gives the row exponent, then the six
+// slices of every column (zero past d, and for the padding rows).
+//   op 0: D (upper triangle read; the lower part by symmetry; gamma_extra on the diagonal)
+//   op 1: X0 (the fp32 pass's full symmetric inverse in m.X)
+//   op 2: S (fp32, in the refinement buffers)
+__device__ void rf_split_block(const InvCtx& c, int mi, int rbk, int op) {
+  const InvMat m = c.mats[mi];
+  const RfBufs rb = rf_bufs(c, m);
+  const long long np = (long long)m.T * 128;
+  uint16_t* dst = op == 1 ? rb.xs : rb.bs;
+  int* ex = op == 1 ? rb.ex : rb.eb;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  auto get = [&](long long r, long long col) -> float {
+    if (op == 0) {
+      const float v = col >= r ? m.D[r * m.ld_in + col] : m.D[col * m.ld_in + r];
+      return col == r ? v + c.gamma_extra : v;
+    }
+    if (op == 1) return m.X[r * m.ld_out + col];
+    return rb.st[r * np + col];
+  };
+  for (int i = warp; i < 128; i += 8) {
+    const long long r = (long long)rbk * 128 + i;
+    float mx = 0.f;
+    if (r < m.d)
+      for (long long col = lane; col < m.d; col += 32) mx = fmaxf(mx, fabsf(get(r, col)));
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    int e = 0;
+    if (mx > 0.f && isfinite(mx)) frexpf(mx, &e);  // mx = f 2^e, f in [0.5, 1): |x / 2^e| < 1
+    if (lane == 0) ex[r] = e;
+    for (long long col = lane; col < np; col += 32) {
+      float x = (r < m.d && col < m.d) ? ldexpf(get(r, col), -e) : 0.f;
+#pragma unroll
+      for (int s = 0; s < kRfSlices; ++s) {
+        const float q = rintf(x * 256.f);  // |q| <= 256: exact in bf16
+        x = x * 256.f - q;                 // exact
+        const float v = ldexpf(q, -8 * (s + 1));
+        dst[((long long)s * np + r) * np + col] = (uint16_t)(__float_as_uint(v) >> 16);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) rf_split_kernel(InvCtx c, int op_base) {
+  const int nf = *c.nflagged;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = rf_matrix(c, f);
+    if (mi < 0) continue;
+    for (int rbk = blockIdx.x; rbk < c.mats[mi].T; rbk += gridDim.x) rf_split_block(c, mi, rbk, op_base + (int)blockIdx.y);
+  }
+}
+
+// ------------------------------------------------------------------ exact product
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// K-major shared-memory descriptor, 64-byte swizzle (rows of 64 B, 8-row groups 512 B apart)
+__device__ __forceinline__ uint64_t rf_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)(16 >> 4) << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
+// accumulator of the slice pair (s, t) (0-based): levels 2, 3, 4, then 5-7 together
+__device__ __forceinline__ int rf_slot(int s, int t) { return s + t < 3 ? s + t : 3; }
+
+// C = A B^T over the flagged candidates, A = xs (rows of X0), B = bs (rows of
+// D, or of S); tiles of 128 x 64, jobs dealt round-robin over a persistent
+// grid.  lmax: highest level taken (7 for the residual, 4 for the correction).
+// mode 0: st = I - 2^(e_i + f_j) C  (the residual S);  mode 1: st = 2^(e_i + f_j) C  (T).
+__global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n, int lmax, int mode, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRfStages * kRfStage);
+  uint64_t* empty = full + kRfStages;
+  uint64_t* acc_full = empty + kRfStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* done_bar = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int nf = *c.nflagged;
+  bool any = false;
+  for (int f = 0; f < nf && !any; ++f) any = rf_matrix(c, f) >= 0;
+  if (!any) return;  // uniform over the grid: nothing to refine
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRfStages; ++s) {
+      mbar_init(&full[s], kRfProducers);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 8);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) tc_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < 4) {
+    // ---------------- producers: cp.async of 32 k-columns of all slices per stage
+    const int p = threadIdx.x;
+    uint32_t stage = 0, phase = 0;
+    int pending = -1;  // stage whose copies are in flight and not yet signalled
+    bool ok = true;
+    for (int f = 0; f < nf && ok; ++f) {
+      const int mi = rf_matrix(c, f);
+      if (mi < 0) continue;
+      const InvMat m = c.mats[mi];
+      const RfBufs rb = rf_bufs(c, m);
+      const long long np = (long long)m.T * 128;
+      const long long tn = np / kRfN, jobs = (long long)m.T * tn;
+      for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
+        const long long i0 = (u / tn) * kRfM, j0 = (u % tn) * kRfN;
+        for (long long kb = 0; kb < np / kRfBK; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t s0 = smem_u32(smem + stage * kRfStage);
+          // A: 6 slices x 128 rows x 4 chunks of 16 B; B: 6 x 64 x 4
+          for (int idx = p; idx < kRfSlices * (kRfM + kRfN) * 4; idx += kRfProducers) {
+            const bool isa = idx < kRfSlices * kRfM * 4;
+            const int j = isa ? idx : idx - kRfSlices * kRfM * 4;
+            const int rows = isa ? kRfM : kRfN;
+            const int s = j / (rows * 4), row = (j / 4) % rows, ch = j % 4;
+            const uint16_t* src = (isa ? rb.xs + ((long long)s * np + i0 + row) * np
+                                       : rb.bs + ((long long)s * np + j0 + row) * np) +
+                                  kb * kRfBK + ch * 8;
+            const uint32_t dst = s0 + (isa ? s * kRfA : kRfSlices * kRfA + s * kRfB) + row * 64 +
+                                 ((ch ^ ((row >> 1) & 3)) << 4);
+            cp_async16(dst, src);
+          }
+          cp_async_commit();
+          if (pending >= 0) {
+            cp_async_wait<1>();          // the previous stage's copies are done
+            fence_proxy_async_smem();    // and visible to the tensor cores
+            mbar_arrive(&full[pending]);
+          }
+          pending = (int)stage;
+          if (++stage == kRfStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (pending >= 0) mbar_arrive(&full[pending]);
+  } else if (warp == 4) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kRfN, false, false);
+      uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
+      bool ok = true;
+      for (int f = 0; f < nf && ok; ++f) {
+        const int mi = rf_matrix(c, f);
+        if (mi < 0) continue;
+        const long long np = (long long)c.mats[mi].T * 128;
+        const long long tn = np / kRfN, jobs = (long long)c.mats[mi].T * tn;
+        for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
+          for (long long kb = 0; kb < np / kRfBK && ok; ++kb) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, status) ||
+                !mbar_wait(&acc_empty[abuf], aphase ^ 1, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(smem + stage * kRfStage);
+            const uint32_t b0 = a0 + kRfSlices * kRfA;
+            bool started[kRfAcc] = {false, false, false, false};
+#pragma unroll
+            for (int kk = 0; kk < kRfBK / 16; ++kk) {
+#pragma unroll
+              for (int s = 0; s < kRfSlices; ++s) {
+#pragma unroll
+                for (int t = 0; t < kRfSlices; ++t) {
+                  if (s + t + 2 > lmax) continue;
+                  const int a = rf_slot(s, t);
+                  tc_mma_bf16(tmem_base + abuf * 256 + a * kRfN, rf_desc(a0 + s * kRfA + kk * 32),
+                              rf_desc(b0 + t * kRfB + kk * 32), idesc, started[a] ? 1u : 0u);
+                  started[a] = true;
+                }
+              }
+            }
+            tc_commit(&empty[stage]);
+            tc_commit(&acc_full[abuf]);
+            if (++stage == kRfStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+            abuf ^= 1;
+            if (abuf == 0) aphase ^= 1;
+          }
+        }
+      }
+      tc_commit(done_bar);
+      mbar_wait(done_bar, 0, abort_flag, status);
+    }
+  } else {
+    // ---------------- epilogue: warp e holds TMEM lanes 32 q.. and 32 columns of half h
+    const int e = warp - 5;
+    const int q = warp & 3;
+    const int h = e / 4;
+    const int nacc = lmax - 1 < kRfAcc ? lmax - 1 : kRfAcc;
+    uint32_t abuf = 0, aphase = 0;
+    bool ok = true;
+    for (int f = 0; f < nf && ok; ++f) {
+      const int mi = rf_matrix(c, f);
+      if (mi < 0) continue;
+      const InvMat m = c.mats[mi];
+      const RfBufs rb = rf_bufs(c, m);
+      const long long np = (long long)m.T * 128;
+      const long long tn = np / kRfN, jobs = (long long)m.T * tn;
+      for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
+        const long long i0 = (u / tn) * kRfM, j0 = (u % tn) * kRfN;
+        float hi[32], lo[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) hi[t] = lo[t] = 0.f;
+        for (long long kb = 0; kb < np / kRfBK; ++kb) {
+          if (!mbar_wait(&acc_full[abuf], aphase, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int a = 0; a < nacc; ++a) {
+            uint32_t v[32];
+            tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + abuf * 256 + a * kRfN + h * 32, v);
+            tc_wait_ld();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) df_add(hi[t], lo[t], __uint_as_float(v[t]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[abuf]);
+          abuf ^= 1;
+          if (abuf == 0) aphase ^= 1;
+        }
+        if (!ok) break;
+        const long long row = i0 + q * 32 + lane;
+        const int er = rb.ex[row];
+        float* out = rb.st + row * np + j0 + h * 32;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const long long col = j0 + h * 32 + t;
+          const int sc = er + rb.eb[col];
+          const float vh = ldexpf(hi[t], sc), vl = ldexpf(lo[t], sc);
+          out[t] = mode == 0 ? ((row == col ? 1.f : 0.f) - vh) - vl : vh + vl;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tc_dealloc(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------------------------ X1 = X0 + (T + T^T) / 2
+// One CTA per upper tile (I, J) of a candidate: reads X0(I, J), T(I, J) and
+// T(J, I) (through shared memory, transposed), writes X1(I, J) and its mirror.
+__device__ void rf_sym_tile(const InvCtx& c, int mi, long long q) {
+  const InvMat m = c.mats[mi];
+  const int J = tri_root(q), I = (int)(q - tri(J));  // I <= J
+  const RfBufs rb = rf_bufs(c, m);
+  const long long np = (long long)m.T * 128;
+  __shared__ float tt[32][33];  // a 32 x 32 block of T(J, I), transposed
+  __shared__ float xx[32][33];  // the 32 x 32 block of X1(I, J) for the mirror
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+  for (int bi = 0; bi < 4; ++bi)
+    for (int bj = 0; bj < 4; ++bj) {
+      const long long r0 = (long long)I * 128 + bi * 32, c0 = (long long)J * 128 + bj * 32;
+      __syncthreads();
+      for (int yy = ty; yy < 32; yy += 8) tt[tx][yy] = rb.st[(c0 + yy) * np + r0 + tx];  // T(c0+yy, r0+tx)
+      __syncthreads();
+      for (int yy = ty; yy < 32; yy += 8) {
+        const long long r = r0 + yy, col = c0 + tx;
+        float v = 0.f;
+        if (r < m.d && col < m.d) {
+          const float x0 = m.X[r * m.ld_out + col];
+          v = x0 + 0.5f * (rb.st[r * np + col] + tt[yy][tx]);
+          m.X[r * m.ld_out + col] = v;
+        }
+        xx[yy][tx] = v;
+      }
+      __syncthreads();
+      // the mirror (a diagonal tile is written whole above: its formula is
+      // symmetric in (r, col), bit for bit)
+      if (I != J)
+        for (int yy = ty; yy < 32; yy += 8) {
+          const long long r = c0 + yy, col = r0 + tx;  // X1(c0+yy, r0+tx) = X1(r0+tx, c0+yy)
+          if (r < m.d && col < m.d) m.X[r * m.ld_out + col] = xx[tx][yy];
+        }
+    }
+  __syncthreads();  // tt and xx are free for the next tile
+}
+
+__global__ void __launch_bounds__(256) rf_sym_kernel(InvCtx c) {
+  const int nf = *c.nflagged;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = rf_matrix(c, f);
+    if (mi < 0) continue;
+    for (long long q = blockIdx.x; q < tri(c.mats[mi].T); q += gridDim.x) rf_sym_tile(c, mi, q);
+  }
+}
+
+// ------------------------------------------------------------------ decision after the step
+// The refined estimate (the probe kernel has formed y = X1 w for the
+// candidates): accepted at most kRefinedResidual (twice the 2.5e-4 of the fp32
+// pass: a matrix refined to its fp32 storage floor sits near 2.5e-4, and the
+// fp64 pass, whose result is stored in fp32 as well, cannot do better there).
+constexpr double kRefinedResidual = 5.0e-4;
+
+__global__ void __launch_bounds__(128) rf_decide_kernel(InvCtx c) {
+  const int mi = rf_matrix(c, blockIdx.x);
+  if (mi < 0) return;
+  const InvMat m = c.mats[mi];
+  const long long np = (long long)m.T * 128;
+  const float2* y = c.probe + m.off_probe + (long long)kProbes * np;
+  __shared__ double red[128];
+  double e2 = 0.0;
+  for (long long r = threadIdx.x; r < m.d; r += 128)
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) {
+      const float2 yv = y[p * np + r];
+      const double dv = df_value(yv.x, yv.y) - probe_sign(r, p);
+      e2 += dv * dv;
+    }
+  red[threadIdx.x] = e2;
+  __syncthreads();
+  for (int s = 64; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double est = sqrt(red[0] / kProbes / (double)m.d);
+    InvState& s = c.st[mi];
+    s.est_res = (float)est;
+    if (est <= kRefinedResidual) {  // false for NaN
+      s.use64 = 0;
+      s.refined = 1;
+    }
+  }
+}
+
+// the fp64 pass's list: the flagged matrices the step did not settle
+__global__ void rf_relist_kernel(InvCtx c) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const int nf = *c.nflagged;
+  int k = 0;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = c.flagged[f];
+    if (c.st[mi].use64) c.flagged[k++] = mi;
+  }
+  *c.nflagged = k;
+}
+
+size_t refine_bytes(long long np) { return rf_bytes(np); }
+
+int run_refine_pass(const InvCtx& ctx, int n, int Tmax, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return KFAC_ERR_CUDA;
+  if (!ensure_smem_attr(dev, (const void*)rf_gemm_kernel, kRfSmem)) return KFAC_ERR_CUDA;
+  int* status = device_status_ptr();
+  if (!status) return KFAC_ERR_CUDA;
+  // persistent grids over the flagged list: with nothing flagged every launch ends at once
+  auto timed = [&](auto&& launch) {
+    ProfMark pm;
+    prof_begin(stream, pm);
+    launch();
+    prof_end(KFAC_K_INV_NEWTON, stream, pm, 0.0);
+    count_launch();
+  };
+  rf_mark_kernel<<<(n + 127) / 128, 128, 0, stream>>>(ctx, n);
+  count_launch();
+  timed([&] { rf_split_kernel<<<dim3((unsigned)(2 * sms), 2), 256, 0, stream>>>(ctx, 0); });  // D and X0
+  timed([&] { rf_gemm_kernel<<<sms, kRfThreads, kRfSmem, stream>>>(ctx, n, 7, 0, status); });
+  timed([&] { rf_split_kernel<<<dim3((unsigned)(2 * sms), 1), 256, 0, stream>>>(ctx, 2); });  // S
+  timed([&] { rf_gemm_kernel<<<sms, kRfThreads, kRfSmem, stream>>>(ctx, n, 4, 1, status); });
+  timed([&] { rf_sym_kernel<<<4 * sms, 256, 0, stream>>>(ctx); });
+  (void)Tmax;
+  int rc = run_refined_probe(ctx, sms, stream);
+  if (rc != KFAC_OK) return rc;
+  rf_decide_kernel<<<n, 128, 0, stream>>>(ctx);
+  rf_relist_kernel<<<1, 32, 0, stream>>>(ctx);
+  count_launch();
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
+}  // namespace kfac

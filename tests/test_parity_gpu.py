@@ -217,18 +217,69 @@ def test_damped_inverse_gamma_extra():
     assert info[0] == 0 and rel_fro(X, ref) <= 1e-5
 
 
-def test_damped_inverse_auto_routes_ill_conditioned_to_fp64():
+def test_damped_inverse_auto_sends_ill_conditioned_away_from_the_fp32_pass():
     rng = np.random.default_rng(9)
-    # rank-deficient ReLU factor (rows < d) with tiny damping: kappa ~ 1e6
+    # rank-deficient ReLU factor (rows < d) with tiny damping: kappa ~ 1e6; AUTO
+    # does not keep its fp32 result: the tensor-core Newton step (route 3) or,
+    # failing that, the fp64 pass (route 1) gives it
     D_bad = spd_case(640, rng, gamma=1e-4, rows=200, relu=True)
     D_ok = spd_case(200, rng)
     Xs, info, route = run_inverse([D_bad, D_ok], capi.KFAC_REFINE_AUTO)
     assert list(info) == [0, 0]
-    assert list(route) == [1, 0]
+    assert route[0] in (1, 3) and route[1] == 0, route
     for D, X in zip((D_bad, D_ok), Xs):
         ref, _ = oracle.spd_inverse(D.astype(np.float64))
         assert rel_fro(X, ref) <= 1e-3
         assert residual(X, D) <= 1e-3
+        assert np.array_equal(X, X.T)
+
+
+def conv_like_factor(d, rows, gamma, rng):
+    """A damped factor shaped like a conv layer's A: ReLU patches with a ones
+    column, rows < d (rank-deficient), so kappa ~ max eigenvalue / gamma."""
+    a = np.maximum(rng.standard_normal((rows, d)), 0.0)
+    a[:, -1] = 1.0
+    a = synth.round_bf16(a.astype(np.float32)).astype(np.float64)
+    return (a.T @ a / rows + gamma * np.eye(d)).astype(np.float32)
+
+
+@pytest.mark.parametrize("d,rows", [(385, 200), (1153, 784), (2305, 1024)])
+def test_damped_inverse_newton_step_on_tensor_cores(d, rows):
+    # kappa ~ 1e5 .. 1e6: the fp32 pass alone misses the AUTO bar; one Newton
+    # step with the residual formed exactly (error-free slices on tensor cores)
+    # lands at the fp32 storage floor of the inverse
+    rng = np.random.default_rng(d)
+    D = conv_like_factor(d, rows, 1e-3, rng)
+    (X,), info, route = run_inverse([D], capi.KFAC_REFINE_AUTO)
+    (X32,), _, _ = run_inverse([D], capi.KFAC_REFINE_NONE)
+    Dd = D.astype(np.float64)
+    ref, _ = oracle.spd_inverse(Dd)
+    assert info[0] == 0
+    r32, r = residual(X32, Dd), residual(X, Dd)
+    assert route[0] in (1, 3), (route, r32)
+    assert np.array_equal(X, X.T)
+    assert r <= 1e-3 and rel_fro(X, ref) <= 1e-3, (r, rel_fro(X, ref))
+    if route[0] == 3:
+        # the step gains what fp32 storage allows: the residual drops below the
+        # fp32 pass's and the error against the oracle far below it
+        assert r <= 5e-4 and r < r32, (r, r32)
+        assert rel_fro(X, ref) <= 0.1 * rel_fro(X32, ref), (rel_fro(X, ref), rel_fro(X32, ref))
+
+
+def test_newton_step_matrices_among_well_conditioned_ones():
+    # candidates and the rest in one batch: only the candidates change
+    rng = np.random.default_rng(77)
+    Ds = [spd_case(300, rng), conv_like_factor(577, 300, 1e-3, rng), spd_case(129, rng),
+          conv_like_factor(1025, 600, 1e-3, rng)]
+    Xs, info, route = run_inverse(Ds, capi.KFAC_REFINE_AUTO)
+    Xn, _, _ = run_inverse(Ds, capi.KFAC_REFINE_NONE)
+    assert (info == 0).all()
+    for D, X, X24, r in zip(Ds, Xs, Xn, route):
+        ref, _ = oracle.spd_inverse(D.astype(np.float64))
+        assert rel_fro(X, ref) <= 1e-3 and residual(X, D) <= 1e-3, (D.shape, r)
+        if r == 0:
+            assert np.array_equal(X, X24)
+    assert route[0] == 0 and route[2] == 0 and route[1] in (1, 3) and route[3] in (1, 3), route
 
 
 def gershgorin_ratio(D):
