@@ -41,7 +41,9 @@
 //   rf_gemm_kernel    T = X0 S^T = X0 (I - D X0)    (levels up to 4)
 //   rf_sym_kernel     X1 = X0 + (T + T^T) / 2, written over X0 (exactly symmetric)
 // then the residual probe runs on X1 and a matrix whose estimate meets the
-// refined bar keeps X1; the others go on to the fp64 pass.
+// refined bar keeps X1; the others take a second step from X1 (the D slices
+// are taken again: their buffer held S), and those it does not settle go on
+// to the fp64 pass.
 #include "common.cuh"
 #include "inverse_common.cuh"
 #include "launch.h"
@@ -49,22 +51,32 @@
 namespace kfac {
 
 constexpr int kRfSlices = 6;
-constexpr int kRfBK = 32;                              // k of one stage (one drain)
+constexpr int kRfBK = 32;                              // k of one stage
+constexpr int kRfDrain = 4;                            // stages per accumulator drain (128 k)
 constexpr int kRfM = 128, kRfN = 64;                   // output tile
 constexpr int kRfA = kRfM * kRfBK * 2;                 // one A slice of a stage: 8 KB
 constexpr int kRfB = kRfN * kRfBK * 2;                 // one B slice: 4 KB
 constexpr int kRfStage = kRfSlices * (kRfA + kRfB);    // 72 KB
 constexpr int kRfStages = 3;
-constexpr int kRfProducers = 128;                      // warps 0-3 fill the stages (cp.async)
-constexpr int kRfThreads = kRfProducers + 32 + 256;    // + MMA warp + eight epilogue warps
+constexpr int kRfThreads = 64 + 256;                   // producer warp, MMA warp, eight epilogue warps
 constexpr int kRfSmem = kRfStages * kRfStage + 1024 + 256;
 constexpr int kRfAcc = 4;                              // accumulators: levels 2, 3, 4, 5-7
 
+// Slices are stored tile by tile, each tile the byte image of the K-major,
+// 64-byte-swizzled shared-memory layout the tensor cores read: tile (rb, kb)
+// of a slice is 128 rows x 32 k of bf16, 8 KB contiguous, row r at 64 r
+// bytes, its 16-byte chunk c (k = 8c .. 8c + 7) at chunk position
+// c ^ ((r / 2) % 4); one bulk copy moves a stage's tile of a slice (the first
+// or second 64 rows of a tile are its first or second 4 KB).
+__host__ __device__ inline long long rf_tile_off(long long T, int s, long long rb, long long kb) {
+  return (((long long)s * T + rb) * (4 * T) + kb) * (kRfM * kRfBK);
+}
+
 // Per-matrix refinement buffers, at m.off_ref in the work region (np = 128 T):
-//   xs  bf16 [6][np][np]   slices of X0
-//   bs  bf16 [6][np][np]   slices of D, then of S
-//   st  fp32 [np][np]      S, then T
-//   ex, eb  int [np]       row exponents of xs and bs
+//   xs  bf16 [6][T][4T] tiles   slices of X0
+//   bs  bf16 [6][T][4T] tiles   slices of D, then of S
+//   st  fp32 [np][np]           S, then T
+//   ex, eb  int [np]            row exponents of xs and bs
 struct RfBufs {
   uint16_t* xs;
   uint16_t* bs;
@@ -105,68 +117,134 @@ __global__ void rf_mark_kernel(InvCtx c, int n) {
 }
 
 // ------------------------------------------------------------------ split
-// One warp per row: the largest |x_r.| gives the row exponent, then the six
-// slices of every column (zero past d, and for the padding rows).
+// One CTA per 128-row block: the rows' largest |x| over all column tiles
+// (through shared memory: a tile of D left of the diagonal is read from its
+// mirror in the upper triangle and transposed), then the six slices of each
+// tile, written tile by tile in the tensor cores' layout.
 //   op 0: D (upper triangle read; the lower part by symmetry; gamma_extra on the diagonal)
 //   op 1: X0 (the fp32 pass's full symmetric inverse in m.X)
 //   op 2: S (fp32, in the refinement buffers)
-__device__ void rf_split_block(const InvCtx& c, int mi, int rbk, int op) {
+constexpr int kRfPitch = 129;
+__device__ void rf_load_tile(const InvCtx& c, const InvMat& m, const RfBufs& rb, int op, int rbk, int cb, float* t) {
+  const long long np = (long long)m.T * 128;
+  const bool mirror = op == 0 && cb < rbk;  // a tile of D left of the diagonal: its mirror, transposed
+  const long long r0 = (long long)(mirror ? cb : rbk) * 128, c0 = (long long)(mirror ? rbk : cb) * 128;
+  const float* src = op == 0 ? m.D : op == 1 ? m.X : rb.st;
+  const long long ld = op == 0 ? m.ld_in : op == 1 ? m.ld_out : np;
+  __syncthreads();
+  // 16 float4 per thread, all loads issued before the stores (rows are
+  // 16-byte multiples long, so a float4 starting inside a row stays in it)
+  float4 v[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int e = threadIdx.x + 256 * k, a = e / 32, b4 = (e % 32) * 4;
+    const long long gr = r0 + a, gc = c0 + b4;
+    v[k] = (gr < m.d && gc < m.d) ? *reinterpret_cast<const float4*>(src + gr * ld + gc) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int e = threadIdx.x + 256 * k, a = e / 32, b4 = (e % 32) * 4;
+    const long long gc = c0 + b4;
+    const float x[4] = {v[k].x, gc + 1 < m.d ? v[k].y : 0.f, gc + 2 < m.d ? v[k].z : 0.f, gc + 3 < m.d ? v[k].w : 0.f};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (mirror)
+        t[(b4 + u) * kRfPitch + a] = x[u];
+      else
+        t[a * kRfPitch + b4 + u] = x[u];
+    }
+  }
+  __syncthreads();
+  if (op == 0 && cb == rbk) {
+    // the diagonal tile of D: its lower part by symmetry (whatever the caller
+    // keeps below the diagonal is not read), gamma_extra on the diagonal
+    for (int e = threadIdx.x; e < 128 * 128; e += 256) {
+      const int a = e / 128, b = e % 128;
+      if (b < a) t[a * kRfPitch + b] = t[b * kRfPitch + a];
+    }
+    __syncthreads();
+    if (threadIdx.x < 128 && r0 + threadIdx.x < m.d) t[threadIdx.x * kRfPitch + threadIdx.x] += c.gamma_extra;
+    __syncthreads();
+  }
+}
+
+__device__ void rf_split_block(const InvCtx& c, int mi, int rbk, int op, float* t, int* rowexp) {
   const InvMat m = c.mats[mi];
   const RfBufs rb = rf_bufs(c, m);
-  const long long np = (long long)m.T * 128;
   uint16_t* dst = op == 1 ? rb.xs : rb.bs;
   int* ex = op == 1 ? rb.ex : rb.eb;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  auto get = [&](long long r, long long col) -> float {
-    if (op == 0) {
-      const float v = col >= r ? m.D[r * m.ld_in + col] : m.D[col * m.ld_in + r];
-      return col == r ? v + c.gamma_extra : v;
-    }
-    if (op == 1) return m.X[r * m.ld_out + col];
-    return rb.st[r * np + col];
-  };
-  for (int i = warp; i < 128; i += 8) {
-    const long long r = (long long)rbk * 128 + i;
-    float mx = 0.f;
-    if (r < m.d)
-      for (long long col = lane; col < m.d; col += 32) mx = fmaxf(mx, fabsf(get(r, col)));
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  // pass 1: row maxima (two threads per row, 64 columns of each tile each)
+  const int row = threadIdx.x % 128, half = threadIdx.x / 128;
+  float mx = 0.f;
+  for (int cb = 0; cb < m.T; ++cb) {
+    rf_load_tile(c, m, rb, op, rbk, cb, t);
+    for (int b = 64 * half; b < 64 * half + 64; ++b) mx = fmaxf(mx, fabsf(t[row * kRfPitch + b]));
+  }
+  __syncthreads();
+  if (half == 1) rowexp[row] = __float_as_int(mx);
+  __syncthreads();
+  if (half == 0) {
+    mx = fmaxf(mx, __int_as_float(rowexp[row]));
     int e = 0;
     if (mx > 0.f && isfinite(mx)) frexpf(mx, &e);  // mx = f 2^e, f in [0.5, 1): |x / 2^e| < 1
-    if (lane == 0) ex[r] = e;
-    for (long long col = lane; col < np; col += 32) {
-      float x = (r < m.d && col < m.d) ? ldexpf(get(r, col), -e) : 0.f;
+    rowexp[row] = e;
+    ex[(long long)rbk * 128 + row] = e;
+  }
+  // pass 2: slices; each thread takes 16-byte chunks (8 values of one row),
+  // consecutive threads along a row's four chunks, then the next rows: a warp
+  // writes 512 contiguous bytes of a tile per slice
+  for (int cb = 0; cb < m.T; ++cb) {
+    rf_load_tile(c, m, rb, op, rbk, cb, t);  // (its first barrier also publishes rowexp)
+    for (int qq = threadIdx.x; qq < 2048; qq += 256) {
+      const int kbl = qq / 512, rr = (qq / 4) % 128, ck = qq % 4;
+      const int k0 = kbl * 32 + ck * 8;
+      const int e = rowexp[rr];
+      float x[8];
 #pragma unroll
-      for (int s = 0; s < kRfSlices; ++s) {
-        const float q = rintf(x * 256.f);  // |q| <= 256: exact in bf16
-        x = x * 256.f - q;                 // exact
-        const float v = ldexpf(q, -8 * (s + 1));
-        dst[((long long)s * np + r) * np + col] = (uint16_t)(__float_as_uint(v) >> 16);
+      for (int u = 0; u < 8; ++u) x[u] = ldexpf(t[rr * kRfPitch + k0 + u], -e);
+      const long long within = (long long)rr * 32 + ((ck ^ ((rr >> 1) & 3)) * 8);
+#pragma unroll
+      for (int sl = 0; sl < kRfSlices; ++sl) {
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 8; u += 2) {
+          const float q0 = rintf(x[u] * 256.f), q1 = rintf(x[u + 1] * 256.f);  // |q| <= 256: exact in bf16
+          x[u] = x[u] * 256.f - q0;                                           // exact
+          x[u + 1] = x[u + 1] * 256.f - q1;
+          const uint32_t b0 = __float_as_uint(ldexpf(q0, -8 * (sl + 1))) >> 16;
+          const uint32_t b1 = __float_as_uint(ldexpf(q1, -8 * (sl + 1))) >> 16;
+          w[u / 2] = b0 | (b1 << 16);
+        }
+        uint16_t* tile = dst + rf_tile_off(m.T, sl, rbk, (long long)cb * 4 + kbl);
+        *reinterpret_cast<uint4*>(tile + within) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   }
 }
 
 __global__ void __launch_bounds__(256) rf_split_kernel(InvCtx c, int op_base) {
+  extern __shared__ __align__(16) uint8_t rf_split_smem[];
+  float* t = reinterpret_cast<float*>(rf_split_smem);  // 128 x kRfPitch
+  int* rowexp = reinterpret_cast<int*>(t + 128 * kRfPitch);
   const int nf = *c.nflagged;
   for (int f = 0; f < nf; ++f) {
     const int mi = rf_matrix(c, f);
     if (mi < 0) continue;
-    for (int rbk = blockIdx.x; rbk < c.mats[mi].T; rbk += gridDim.x) rf_split_block(c, mi, rbk, op_base + (int)blockIdx.y);
+    for (int rbk = blockIdx.x; rbk < c.mats[mi].T; rbk += gridDim.x)
+      rf_split_block(c, mi, rbk, op_base + (int)blockIdx.y, t, rowexp);
   }
 }
+constexpr int kRfSplitSmem = (128 * kRfPitch + 128) * 4;
 
 // ------------------------------------------------------------------ exact product
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+               "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
-// K-major shared-memory descriptor, 64-byte swizzle (rows of 64 B, 8-row groups 512 B apart)
+// K-major shared-memory descriptor, 64-byte swizzle (rows of 64 B, 8-row
+// groups 512 B apart, layout type 4)
 __device__ __forceinline__ uint64_t rf_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
@@ -177,14 +255,55 @@ __device__ __forceinline__ uint64_t rf_desc(uint32_t saddr) {
   return d;
 }
 
+// Job u of a matrix with T row blocks -> (A row block ib, B half-block jn):
+// bands of kRfBand row blocks, column-major inside a band, so that the grid's
+// concurrent jobs share few operand panels (about kRfBand A panels and
+// gridDim / kRfBand B panels, which L2 holds).
+constexpr int kRfBand = 8;
+__device__ __forceinline__ void rf_job(long long u, long long T, long long& ib, long long& jn) {
+  const long long tn = 2 * T, per_band = (long long)kRfBand * tn;
+  const long long band = u / per_band, w = u % per_band;
+  const long long rows = (band + 1) * kRfBand <= T ? kRfBand : T - band * kRfBand;
+  ib = band * kRfBand + w % rows;
+  jn = w / rows;
+}
+
 // accumulator of the slice pair (s, t) (0-based): levels 2, 3, 4, then 5-7 together
-__device__ __forceinline__ int rf_slot(int s, int t) { return s + t < 3 ? s + t : 3; }
+__host__ __device__ constexpr int rf_slot(int s, int t) { return s + t < 3 ? s + t : 3; }
+
+// The MMAs of one stage (two 16-wide k-steps): every slice pair up to level
+// LMAX, each into its level's accumulator.  All indices are static; the first
+// pair of each accumulator, (0, slot), overwrites it at the start of a drain
+// period (`first`).
+template <int LMAX>
+__device__ __forceinline__ void rf_issue(uint32_t tmem_acc, uint32_t a0, uint32_t b0, uint32_t idesc, bool first) {
+  const uint64_t da0 = rf_desc(a0), db0 = rf_desc(b0);  // the address field is linear in the address
+#pragma unroll
+  for (int kk = 0; kk < kRfBK / 16; ++kk) {
+#pragma unroll
+    for (int s = 0; s < kRfSlices; ++s) {
+#pragma unroll
+      for (int t = 0; t < kRfSlices; ++t) {
+        if (s + t + 2 > LMAX) continue;
+        const int a = rf_slot(s, t);
+        const uint64_t da = da0 + (uint64_t)((s * kRfA + kk * 32) >> 4);
+        const uint64_t db = db0 + (uint64_t)((t * kRfB + kk * 32) >> 4);
+        const bool opens = kk == 0 && s == 0 && t == a;
+        tc_mma_bf16(tmem_acc + a * kRfN, da, db, idesc, (opens && first) ? 0u : 1u);
+      }
+    }
+  }
+}
 
 // C = A B^T over the flagged candidates, A = xs (rows of X0), B = bs (rows of
 // D, or of S); tiles of 128 x 64, jobs dealt round-robin over a persistent
-// grid.  lmax: highest level taken (7 for the residual, 4 for the correction).
+// grid.  LMAX: highest level taken (7 for the residual, 4 for the correction).
 // mode 0: st = I - 2^(e_i + f_j) C  (the residual S);  mode 1: st = 2^(e_i + f_j) C  (T).
-__global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n, int lmax, int mode, int* status) {
+// The accumulators are drained every kRfDrain stages (128 k: every level up to
+// 4 stays below 2^24 of its unit, |q_1| <= 256 and |q_s| <= 128 after it).
+template <int LMAX>
+__global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n, int mode, int* status) {
+  constexpr int lmax = LMAX;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRfStages * kRfStage);
@@ -198,11 +317,12 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
   bool any = false;
   for (int f = 0; f < nf && !any; ++f) any = rf_matrix(c, f) >= 0;
   if (!any) return;  // uniform over the grid: nothing to refine
+  (void)n;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRfStages; ++s) {
-      mbar_init(&full[s], kRfProducers);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -213,64 +333,51 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) tc_alloc(tmem_slot, 512);
+  if (warp == 1) tc_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < 4) {
-    // ---------------- producers: cp.async of 32 k-columns of all slices per stage
-    const int p = threadIdx.x;
-    uint32_t stage = 0, phase = 0;
-    int pending = -1;  // stage whose copies are in flight and not yet signalled
-    bool ok = true;
-    for (int f = 0; f < nf && ok; ++f) {
-      const int mi = rf_matrix(c, f);
-      if (mi < 0) continue;
-      const InvMat m = c.mats[mi];
-      const RfBufs rb = rf_bufs(c, m);
-      const long long np = (long long)m.T * 128;
-      const long long tn = np / kRfN, jobs = (long long)m.T * tn;
-      for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
-        const long long i0 = (u / tn) * kRfM, j0 = (u % tn) * kRfN;
-        for (long long kb = 0; kb < np / kRfBK; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t s0 = smem_u32(smem + stage * kRfStage);
-          // A: 6 slices x 128 rows x 4 chunks of 16 B; B: 6 x 64 x 4
-          for (int idx = p; idx < kRfSlices * (kRfM + kRfN) * 4; idx += kRfProducers) {
-            const bool isa = idx < kRfSlices * kRfM * 4;
-            const int j = isa ? idx : idx - kRfSlices * kRfM * 4;
-            const int rows = isa ? kRfM : kRfN;
-            const int s = j / (rows * 4), row = (j / 4) % rows, ch = j % 4;
-            const uint16_t* src = (isa ? rb.xs + ((long long)s * np + i0 + row) * np
-                                       : rb.bs + ((long long)s * np + j0 + row) * np) +
-                                  kb * kRfBK + ch * 8;
-            const uint32_t dst = s0 + (isa ? s * kRfA : kRfSlices * kRfA + s * kRfB) + row * 64 +
-                                 ((ch ^ ((row >> 1) & 3)) << 4);
-            cp_async16(dst, src);
-          }
-          cp_async_commit();
-          if (pending >= 0) {
-            cp_async_wait<1>();          // the previous stage's copies are done
-            fence_proxy_async_smem();    // and visible to the tensor cores
-            mbar_arrive(&full[pending]);
-          }
-          pending = (int)stage;
-          if (++stage == kRfStages) {
-            stage = 0;
-            phase ^= 1;
+  if (warp == 0) {
+    // ---------------- producer: one bulk copy per slice tile of a stage (the
+    // slices the level cap reaches: s <= lmax - 2)
+    if (lane == 0) {
+      const int nsl = lmax - 1 < kRfSlices ? lmax - 1 : kRfSlices;
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int f = 0; f < nf && ok; ++f) {
+        const int mi = rf_matrix(c, f);
+        if (mi < 0) continue;
+        const InvMat m = c.mats[mi];
+        const RfBufs rb = rf_bufs(c, m);
+        const long long T = m.T, tn = 2 * T, jobs = T * tn;
+        for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
+          long long ib, jn;  // A row block; B row block jn / 2, half jn % 2
+          rf_job(u, T, ib, jn);
+          for (long long kb = 0; kb < 4 * T; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            uint8_t* s0 = smem + stage * kRfStage;
+            mbar_arrive_expect_tx(&full[stage], nsl * (kRfA + kRfB));
+#pragma unroll
+            for (int sl = 0; sl < kRfSlices; ++sl) {
+              if (sl >= nsl) break;
+              bulk_load(smem_u32(s0 + sl * kRfA), rb.xs + rf_tile_off(T, sl, ib, kb), kRfA, &full[stage]);
+              bulk_load(smem_u32(s0 + kRfSlices * kRfA + sl * kRfB),
+                        rb.bs + rf_tile_off(T, sl, jn / 2, kb) + (jn % 2) * (kRfN * kRfBK), kRfB, &full[stage]);
+            }
+            if (++stage == kRfStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
       }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (pending >= 0) mbar_arrive(&full[pending]);
-  } else if (warp == 4) {
+  } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kRfN, false, false);
@@ -279,41 +386,28 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
       for (int f = 0; f < nf && ok; ++f) {
         const int mi = rf_matrix(c, f);
         if (mi < 0) continue;
-        const long long np = (long long)c.mats[mi].T * 128;
-        const long long tn = np / kRfN, jobs = (long long)c.mats[mi].T * tn;
+        const long long T = c.mats[mi].T, jobs = T * 2 * T;
         for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
-          for (long long kb = 0; kb < np / kRfBK && ok; ++kb) {
+          for (long long kb = 0; kb < 4 * T && ok; ++kb) {
+            const bool first = kb % kRfDrain == 0, last = kb % kRfDrain == kRfDrain - 1;
             if (!mbar_wait(&full[stage], phase, abort_flag, status) ||
-                !mbar_wait(&acc_empty[abuf], aphase ^ 1, abort_flag, status)) {
+                (first && !mbar_wait(&acc_empty[abuf], aphase ^ 1, abort_flag, status))) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t a0 = smem_u32(smem + stage * kRfStage);
-            const uint32_t b0 = a0 + kRfSlices * kRfA;
-            bool started[kRfAcc] = {false, false, false, false};
-#pragma unroll
-            for (int kk = 0; kk < kRfBK / 16; ++kk) {
-#pragma unroll
-              for (int s = 0; s < kRfSlices; ++s) {
-#pragma unroll
-                for (int t = 0; t < kRfSlices; ++t) {
-                  if (s + t + 2 > lmax) continue;
-                  const int a = rf_slot(s, t);
-                  tc_mma_bf16(tmem_base + abuf * 256 + a * kRfN, rf_desc(a0 + s * kRfA + kk * 32),
-                              rf_desc(b0 + t * kRfB + kk * 32), idesc, started[a] ? 1u : 0u);
-                  started[a] = true;
-                }
-              }
-            }
+            rf_issue<LMAX>(tmem_base + abuf * 256, a0, a0 + kRfSlices * kRfA, idesc, first);
             tc_commit(&empty[stage]);
-            tc_commit(&acc_full[abuf]);
+            if (last) {
+              tc_commit(&acc_full[abuf]);
+              abuf ^= 1;
+              if (abuf == 0) aphase ^= 1;
+            }
             if (++stage == kRfStages) {
               stage = 0;
               phase ^= 1;
             }
-            abuf ^= 1;
-            if (abuf == 0) aphase ^= 1;
           }
         }
       }
@@ -322,7 +416,7 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
     }
   } else {
     // ---------------- epilogue: warp e holds TMEM lanes 32 q.. and 32 columns of half h
-    const int e = warp - 5;
+    const int e = warp - 2;
     const int q = warp & 3;
     const int h = e / 4;
     const int nacc = lmax - 1 < kRfAcc ? lmax - 1 : kRfAcc;
@@ -336,11 +430,13 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
       const long long np = (long long)m.T * 128;
       const long long tn = np / kRfN, jobs = (long long)m.T * tn;
       for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
-        const long long i0 = (u / tn) * kRfM, j0 = (u % tn) * kRfN;
+        long long ib, jn;
+        rf_job(u, m.T, ib, jn);
+        const long long i0 = ib * kRfM, j0 = jn * kRfN;
         float hi[32], lo[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) hi[t] = lo[t] = 0.f;
-        for (long long kb = 0; kb < np / kRfBK; ++kb) {
+        for (long long kd = 0; kd < 4 * m.T / kRfDrain; ++kd) {
           if (!mbar_wait(&acc_full[abuf], aphase, abort_flag, status)) {
             ok = false;
             break;
@@ -374,7 +470,7 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
     }
   }
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 1) {
     tc_fence_after();
     tc_dealloc(tmem_base, 512);
   }
@@ -434,6 +530,10 @@ __global__ void __launch_bounds__(256) rf_sym_kernel(InvCtx c) {
 // pass: a matrix refined to its fp32 storage floor sits near 2.5e-4, and the
 // fp64 pass, whose result is stored in fp32 as well, cannot do better there).
 constexpr double kRefinedResidual = 5.0e-4;
+// Newton steps at most: the fp32 pass leaves the 4609-wide ResNet-50 conv
+// factor at a residual near 6e-3 (about 1e-3 in the host emulation), which one
+// step takes to about 2e-3 and a second one to the storage floor.
+constexpr int kRfSteps = 2;
 
 __global__ void __launch_bounds__(128) rf_decide_kernel(InvCtx c) {
   const int mi = rf_matrix(c, blockIdx.x);
@@ -463,6 +563,7 @@ __global__ void __launch_bounds__(128) rf_decide_kernel(InvCtx c) {
     if (est <= kRefinedResidual) {  // false for NaN
       s.use64 = 0;
       s.refined = 1;
+      s.refine = 0;  // settled: later steps skip it
     }
   }
 }
@@ -486,7 +587,10 @@ int run_refine_pass(const InvCtx& ctx, int n, int Tmax, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return KFAC_ERR_CUDA;
-  if (!ensure_smem_attr(dev, (const void*)rf_gemm_kernel, kRfSmem)) return KFAC_ERR_CUDA;
+  if (!ensure_smem_attr(dev, (const void*)rf_gemm_kernel<7>, kRfSmem) ||
+      !ensure_smem_attr(dev, (const void*)rf_gemm_kernel<4>, kRfSmem) ||
+      !ensure_smem_attr(dev, (const void*)rf_split_kernel, kRfSplitSmem))
+    return KFAC_ERR_CUDA;
   int* status = device_status_ptr();
   if (!status) return KFAC_ERR_CUDA;
   // persistent grids over the flagged list: with nothing flagged every launch ends at once
@@ -499,17 +603,21 @@ int run_refine_pass(const InvCtx& ctx, int n, int Tmax, cudaStream_t stream) {
   };
   rf_mark_kernel<<<(n + 127) / 128, 128, 0, stream>>>(ctx, n);
   count_launch();
-  timed([&] { rf_split_kernel<<<dim3((unsigned)(2 * sms), 2), 256, 0, stream>>>(ctx, 0); });  // D and X0
-  timed([&] { rf_gemm_kernel<<<sms, kRfThreads, kRfSmem, stream>>>(ctx, n, 7, 0, status); });
-  timed([&] { rf_split_kernel<<<dim3((unsigned)(2 * sms), 1), 256, 0, stream>>>(ctx, 2); });  // S
-  timed([&] { rf_gemm_kernel<<<sms, kRfThreads, kRfSmem, stream>>>(ctx, n, 4, 1, status); });
-  timed([&] { rf_sym_kernel<<<4 * sms, 256, 0, stream>>>(ctx); });
   (void)Tmax;
-  int rc = run_refined_probe(ctx, sms, stream);
-  if (rc != KFAC_OK) return rc;
-  rf_decide_kernel<<<n, 128, 0, stream>>>(ctx);
+  // up to kRfSteps steps; a matrix whose estimate meets the bar after a step
+  // leaves the candidates (the ones that follow skip it)
+  for (int step = 0; step < kRfSteps; ++step) {
+    timed([&] { rf_split_kernel<<<dim3((unsigned)(2 * sms), 2), 256, kRfSplitSmem, stream>>>(ctx, 0); });  // D, X
+    timed([&] { rf_gemm_kernel<7><<<sms, kRfThreads, kRfSmem, stream>>>(ctx, n, 0, status); });
+    timed([&] { rf_split_kernel<<<dim3((unsigned)(2 * sms), 1), 256, kRfSplitSmem, stream>>>(ctx, 2); });  // S
+    timed([&] { rf_gemm_kernel<4><<<sms, kRfThreads, kRfSmem, stream>>>(ctx, n, 1, status); });
+    timed([&] { rf_sym_kernel<<<4 * sms, 256, 0, stream>>>(ctx); });
+    const int rc = run_refined_probe(ctx, sms, stream);
+    if (rc != KFAC_OK) return rc;
+    rf_decide_kernel<<<n, 128, 0, stream>>>(ctx);
+    count_launch();
+  }
   rf_relist_kernel<<<1, 32, 0, stream>>>(ctx);
-  count_launch();
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
 }
