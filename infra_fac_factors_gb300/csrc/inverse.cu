@@ -16,8 +16,9 @@
 // Two passes run these steps:
 //   * fp32 on tcgen05 tensor cores (inverse_tc.cu): every tile product with
 //     three-slice bf16 operands, drained per k-step into fp32;
-//   * fp64 on CUDA cores (this file), for the matrices the fp32 pass routes
-//     to it (refine = AUTO) or for all of them (refine = ALWAYS).
+//   * fp64 on CUDA cores (this file), for the matrices that neither the
+//     fp32 pass nor the Newton step after it settles (refine = AUTO) or for
+//     all of them (refine = ALWAYS).
 //
 // refine = AUTO: the fp32 pass measures its own residual.  With kProbes
 // Rademacher vectors v (+-1 entries), w = D v and then y = X w are formed in
@@ -27,8 +28,10 @@
 // tc_route_kernel; y in tc_probe_kernel).  Matrices whose estimated
 // residual ||X D - I||_F / sqrt(d) exceeds 2.5e-4 (four times below the 1e-3
 // target), whose ||D||_1 / min L_jj^2 exceeds 3e5 (a guard on the relative
-// error), or whose fp32 factorisation failed, are redone in fp64; the fp64
-// kernels of the other matrices exit at once.
+// error), or whose fp32 factorisation failed, are flagged.  A flagged matrix
+// whose factorisation succeeded first gets up to two Newton steps on the
+// tensor cores (refine.cu); what is still flagged after them is redone in
+// fp64, and the fp64 kernels of the other matrices exit at once.
 #include <math.h>
 
 #include "common.cuh"
