@@ -47,7 +47,7 @@ constexpr int kItDrain = 2;
 // accumulator is drained every eight k-steps, as in the 16-bit GEMM of the
 // preconditioning
 constexpr int kItDrain16 = 8;
-constexpr int kLoadSmem = (128 * 129 + 2 * kProbes * 128) * 4;  // the tile, and the probe signs of its two blocks
+constexpr int kLoadSmem = (128 * 129 + 2 * 128) * 4;  // the tile, and the probe signs s() of its two blocks
 
 enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
 
@@ -590,19 +590,27 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_
   extern __shared__ __align__(16) uint8_t load_smem[];
   float* sub = reinterpret_cast<float*>(load_smem);  // 128 x 129: sub[i][j] = D[C*128 + i][R*128 + j]
   const int t = threadIdx.x;
-  // read the upper tile (C, R) of D along its rows, 16 float4 per thread (ld_in % 4 == 0
-  // keeps a float4 that starts inside the row inside it)
-#pragma unroll 4
-  for (int e = t; e < 128 * 32; e += 256) {
-    const int i = e / 32, j4 = (e % 32) * 4;
-    const long long gc = (long long)C * 128 + i, gr = (long long)R * 128 + j4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (gc < m.d && gr < m.d) v = *reinterpret_cast<const float4*>(m.D + gc * m.ld_in + gr);
-    float* d = sub + i * 129 + j4;
-    d[0] = v.x;
-    d[1] = v.y;
-    d[2] = v.z;
-    d[3] = v.w;
+  // read the upper tile (C, R) of D along its rows, 16 float4 per thread, all
+  // issued before the first shared-memory store (ld_in % 4 == 0 keeps a
+  // float4 that starts inside the row inside it)
+  {
+    float4 v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int e = t + 256 * u, i = e / 32, j4 = (e % 32) * 4;
+      const long long gc = (long long)C * 128 + i, gr = (long long)R * 128 + j4;
+      v[u] = (gc < m.d && gr < m.d) ? *reinterpret_cast<const float4*>(m.D + gc * m.ld_in + gr)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int e = t + 256 * u, i = e / 32, j4 = (e % 32) * 4;
+      float* d = sub + i * 129 + j4;
+      d[0] = v[u].x;
+      d[1] = v[u].y;
+      d[2] = v[u].z;
+      d[3] = v[u].w;
+    }
   }
   __syncthreads();
   if (c.gpart) {
@@ -610,26 +618,25 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_
     // the rows of block R down its columns (the mirror), the partial sums of
     //   |D_rc| (c != r)      -> gpart: Gershgorin radii (tc_route_kernel) and ||D||_1
     //   D_rc v_p(c)          -> wpart: w = D v for the residual probes
-    // with v_p the Rademacher probes (the products are exact, the sums
-    // double-float).  On a diagonal tile only its upper triangle counts, and
-    // the diagonal itself (with gamma_extra) goes into w only.  Columns of the
+    // With v_p(c) = s(c) H4[p][c mod 4] (inverse_common.cuh), the four sums
+    // come from one double-float sum of s(c) D_rc per residue class of c
+    // (the sign flips are exact), combined by a 4-point Hadamard transform at
+    // the end.  On a diagonal tile only its upper triangle counts, and the
+    // diagonal itself (with gamma_extra) goes into w only.  Columns of the
     // tile at or past d hold whatever the float4 loads brought from the
     // padding: they are left out; rows past d were loaded as zero.
-    float* vr = sub + 128 * 129;        // kProbes x 128 probe signs of block R's indices
-    float* vc = vr + kProbes * 128;     // and of block C's
-    for (int e = t; e < kProbes * 128; e += 256) {
-      const int p = e / 128, ii = e % 128;
-      vr[e] = (float)probe_sign((long long)R * 128 + ii, p);
-      vc[e] = (float)probe_sign((long long)C * 128 + ii, p);
+    float* sr = sub + 128 * 129;  // s() of block R's indices
+    float* sc = sr + 128;         // and of block C's
+    for (int e = t; e < 128; e += 256) {
+      sr[e] = probe_base_sign((long long)R * 128 + e);
+      sc[e] = probe_base_sign((long long)C * 128 + e);
     }
     __syncthreads();
     float* gp = c.gpart + m.off_gpart;
     float2* wp = c.wpart + m.off_gpart * kProbes;
     const long long cleft = m.d - (long long)R * 128;
     const int jmax = cleft < 128 ? (int)cleft : 128;
-    float s = 0.f, whi[kProbes], wlo[kProbes];
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p) whi[p] = wlo[p] = 0.f;
+    float s = 0.f, yhi[4] = {0.f, 0.f, 0.f, 0.f}, ylo[4] = {0.f, 0.f, 0.f, 0.f};  // residue-class sums
     long long slot = -1;  // (row block, column block) of this thread's sums
     int row = 0;
     if (R == C) {
@@ -640,44 +647,73 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_
           for (int j = t + 1; j < jmax; ++j) {
             const float x = sub[t * 129 + j];
             s += fabsf(x);
-#pragma unroll
-            for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vr[p * 128 + j]);
+            df_add(yhi[j & 3], ylo[j & 3], x * sr[j]);
           }
           for (int i2 = 0; i2 < t; ++i2) {
             const float x = sub[i2 * 129 + t];
             s += fabsf(x);
-#pragma unroll
-            for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vc[p * 128 + i2]);
+            df_add(yhi[i2 & 3], ylo[i2 & 3], x * sc[i2]);
           }
           const float dg = sub[t * 129 + t] + c.gamma_extra;
-#pragma unroll
-          for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], dg * vc[p * 128 + t]);
+          df_add(yhi[t & 3], ylo[t & 3], dg * sc[t]);
         }
       }
     } else if (t < 128) {
       row = t;
       slot = (long long)C * m.T + R;
-      for (int j = 0; j < jmax; ++j) {
+      // unrolled by the residue class, so that each sum stays in registers
+      int j = 0;
+      for (; j + 4 <= jmax; j += 4) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float x = sub[t * 129 + j + b];
+          s += fabsf(x);
+          df_add(yhi[b], ylo[b], x * sr[j + b]);
+        }
+      }
+      for (; j < jmax; ++j) {
         const float x = sub[t * 129 + j];
         s += fabsf(x);
-#pragma unroll
-        for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vr[p * 128 + j]);
+        df_add(yhi[j & 3], ylo[j & 3], x * sr[j]);
       }
     } else {
       row = t - 128;
       slot = (long long)R * m.T + C;
       if (row < jmax)
-        for (int i2 = 0; i2 < 128; ++i2) {
-          const float x = sub[i2 * 129 + row];
-          s += fabsf(x);
+        for (int i2 = 0; i2 < 128; i2 += 4) {
 #pragma unroll
-          for (int p = 0; p < kProbes; ++p) df_add(whi[p], wlo[p], x * vc[p * 128 + i2]);
+          for (int b = 0; b < 4; ++b) {
+            const float x = sub[(i2 + b) * 129 + row];
+            s += fabsf(x);
+            df_add(yhi[b], ylo[b], x * sc[i2 + b]);
+          }
         }
     }
     if (slot >= 0) {
       gp[slot * 128 + row] = s;
-#pragma unroll
-      for (int p = 0; p < kProbes; ++p) wp[(slot * kProbes + p) * 128 + row] = make_float2(whi[p], wlo[p]);
+      // w_p = sum_b H4[p][b] Y_b (double-float butterflies)
+      float ah = yhi[0], al = ylo[0], bh = yhi[0], bl = ylo[0], ch = yhi[2], cl = ylo[2], dh = yhi[2], dl = ylo[2];
+      df_add(ah, al, yhi[1]);
+      al += ylo[1];
+      df_add(bh, bl, -yhi[1]);
+      bl -= ylo[1];
+      df_add(ch, cl, yhi[3]);
+      cl += ylo[3];
+      df_add(dh, dl, -yhi[3]);
+      dl -= ylo[3];
+      float w0h = ah, w0l = al, w2h = ah, w2l = al, w1h = bh, w1l = bl, w3h = bh, w3l = bl;
+      df_add(w0h, w0l, ch);  // Y0 + Y1 + Y2 + Y3
+      w0l += cl;
+      df_add(w2h, w2l, -ch);  // Y0 + Y1 - Y2 - Y3
+      w2l -= cl;
+      df_add(w1h, w1l, dh);  // Y0 - Y1 + Y2 - Y3
+      w1l += dl;
+      df_add(w3h, w3l, -dh);  // Y0 - Y1 - Y2 + Y3
+      w3l -= dl;
+      wp[(slot * kProbes + 0) * 128 + row] = make_float2(w0h, w0l);
+      wp[(slot * kProbes + 1) * 128 + row] = make_float2(w1h, w1l);
+      wp[(slot * kProbes + 2) * 128 + row] = make_float2(w2h, w2l);
+      wp[(slot * kProbes + 3) * 128 + row] = make_float2(w3h, w3l);
     }
   }
   // write the lower tile (R, C) of the work buffer along its rows: element
@@ -890,50 +926,76 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(InvCtx c, TcBufs b, int k)
 
 // ------------------------------------------------------------------ residual probe y = X w, ||X||_F^2 (AUTO)
 // A CTA per strip of kPrRows rows of X (full symmetric, as written by the
-// X = U U^T step), columns in chunks of 128: lane l owns columns 4l..4l+3 of
-// the chunk and keeps their w (all probes) in registers for the kPrWarpRows
-// rows of its warp, so w is read once per strip.  Double-float products and sums.
+// X = U U^T step), columns in chunks of 128: the CTA stages the chunk's w (all
+// probes) in shared memory, lane l of each warp takes columns 4l..4l+3 of the
+// chunk for the kPrWarpRows rows of its warp, and the next chunk's X and w are
+// fetched while the current one is summed.  Double-float products and sums.
 constexpr int kPrWarpRows = 4;
 constexpr int kPrRows = 8 * kPrWarpRows;
 // y = X w over one strip of kPrRows rows of matrix mi (each warp its own
-// kPrWarpRows rows; no block-wide synchronisation); ||X||_F^2 of the strip is
-// added to the matrix's state when count_norm is set.
+// kPrWarpRows rows); ||X||_F^2 of the strip is added to the matrix's state
+// when count_norm is set.  Called by all threads of the block alike.
 __device__ void probe_strip(const InvCtx& c, int mi, long long strip, bool count_norm) {
+  __shared__ __align__(16) float2 ws[2][kProbes * 128];  // w of a chunk, [probe][column], double-buffered
   const InvMat m = c.mats[mi];
-  const long long rw = strip * kPrRows + (threadIdx.x / 32) * kPrWarpRows;  // the warp's first row
   if (strip * kPrRows >= m.d) return;
-  const int lane = threadIdx.x % 32;
+  const int t = threadIdx.x, lane = t % 32;
+  const long long rw = strip * kPrRows + (t / 32) * kPrWarpRows;  // the warp's first row
   const long long np = (long long)m.T * 128;
   const float2* w = c.probe + m.off_probe;
   float2* y = c.probe + m.off_probe + (long long)kProbes * np;
   const int nrow = rw >= m.d ? 0 : (int)(m.d - rw < kPrWarpRows ? m.d - rw : kPrWarpRows);
+  const int nchunk = (int)((m.d + 127) / 128);
+  float2 wn[2];                // this thread's share of the next chunk's w
+  float4 xn[kPrWarpRows];      // and of its X (columns past d are masked when summed)
+  auto fetch = [&](int ch) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e = t + 256 * h;
+      const long long col = (long long)ch * 128 + e % 128;
+      wn[h] = col < m.d ? w[(e / 128) * np + col] : make_float2(0.f, 0.f);
+    }
+    const long long col = (long long)ch * 128 + 4 * lane;  // float4 reads of columns col..col+3 stay inside the row (ld_out % 4 == 0)
+#pragma unroll
+    for (int q = 0; q < kPrWarpRows; ++q)
+      xn[q] = (q < nrow && col < m.d) ? *reinterpret_cast<const float4*>(m.X + (rw + q) * m.ld_out + col)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
   float hi[kPrWarpRows][kProbes], lo[kPrWarpRows][kProbes];
 #pragma unroll
   for (int q = 0; q < kPrWarpRows; ++q)
 #pragma unroll
     for (int p = 0; p < kProbes; ++p) hi[q][p] = lo[q][p] = 0.f;
   float sq = 0.f;
-  for (long long c0 = 0; c0 < m.d && nrow > 0; c0 += 128) {
-    const long long col = c0 + 4 * lane;
-    const bool any = col < m.d;  // float4 reads of columns col..col+3 stay inside the row (ld_out % 4 == 0)
-    float2 wv[kProbes][4];
-#pragma unroll
-    for (int p = 0; p < kProbes; ++p)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) wv[p][e] = (col + e < m.d) ? w[p * np + col + e] : make_float2(0.f, 0.f);
+  fetch(0);
+  for (int ch = 0; ch < nchunk; ++ch) {
+    float2* wb = ws[ch & 1];
+    wb[t] = wn[0];
+    wb[t + 256] = wn[1];
+    __syncthreads();  // (the other buffer was last read before the previous barrier)
+    const long long col = (long long)ch * 128 + 4 * lane;
+    float xs[kPrWarpRows][4];
 #pragma unroll
     for (int q = 0; q < kPrWarpRows; ++q) {
-      if (q < nrow && any) {
-        const float4 x4 = *reinterpret_cast<const float4*>(m.X + (rw + q) * m.ld_out + col);
-        const float xs[4] = {x4.x, col + 1 < m.d ? x4.y : 0.f, col + 2 < m.d ? x4.z : 0.f,
-                             col + 3 < m.d ? x4.w : 0.f};
+      xs[q][0] = col < m.d ? xn[q].x : 0.f;
+      xs[q][1] = col + 1 < m.d ? xn[q].y : 0.f;
+      xs[q][2] = col + 2 < m.d ? xn[q].z : 0.f;
+      xs[q][3] = col + 3 < m.d ? xn[q].w : 0.f;
+    }
+    if (ch + 1 < nchunk) fetch(ch + 1);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          sq += xs[e] * xs[e];
+    for (int q = 0; q < kPrWarpRows; ++q)
 #pragma unroll
-          for (int p = 0; p < kProbes; ++p) df_add_prod(hi[q][p], lo[q][p], xs[e], wv[p][e].x, wv[p][e].y);
-        }
-      }
+      for (int e = 0; e < 4; ++e) sq += xs[q][e] * xs[q][e];
+#pragma unroll
+    for (int p = 0; p < kProbes; ++p) {
+      const float4 w01 = *reinterpret_cast<const float4*>(wb + p * 128 + 4 * lane);
+      const float4 w23 = *reinterpret_cast<const float4*>(wb + p * 128 + 4 * lane + 2);
+      const float wh[4] = {w01.x, w01.z, w23.x, w23.z}, wl[4] = {w01.y, w01.w, w23.y, w23.w};
+#pragma unroll
+      for (int q = 0; q < kPrWarpRows; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) df_add_prod(hi[q][p], lo[q][p], xs[q][e], wh[e], wl[e]);
     }
   }
 #pragma unroll
@@ -952,9 +1014,10 @@ __device__ void probe_strip(const InvCtx& c, int mi, long long strip, bool count
   }
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
   if (lane == 0 && nrow > 0 && count_norm) atomicAdd(&c.st[mi].xnorm2, sq);
+  __syncthreads();  // the next strip of this block (persistent callers) rewrites ws
 }
 
-__global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c, int t_only) {
+__global__ void __launch_bounds__(256, 2) tc_probe_kernel(InvCtx c, int t_only) {
   const int mi = blockIdx.y;
   if (!inv_active(c, mi, true)) return;
   if (t_only && c.mats[mi].T != t_only) return;  // only the matrices of T block rows
@@ -963,7 +1026,7 @@ __global__ void __launch_bounds__(256) tc_probe_kernel(InvCtx c, int t_only) {
 
 // The same over the Newton step's candidates (refine.cu), a persistent grid
 // over the flagged list: nothing runs when no matrix is flagged.
-__global__ void __launch_bounds__(256) rf_probe_kernel(InvCtx c) {
+__global__ void __launch_bounds__(256, 2) rf_probe_kernel(InvCtx c) {
   const int nf = *c.nflagged;
   for (int f = 0; f < nf; ++f) {
     const int mi = c.flagged[f];

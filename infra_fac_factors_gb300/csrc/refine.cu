@@ -53,14 +53,20 @@ namespace kfac {
 constexpr int kRfSlices = 6;
 constexpr int kRfBK = 32;                              // k of one stage
 constexpr int kRfDrain = 4;                            // stages per accumulator drain (128 k)
-constexpr int kRfM = 128, kRfN = 64;                   // output tile
-constexpr int kRfA = kRfM * kRfBK * 2;                 // one A slice of a stage: 8 KB
-constexpr int kRfB = kRfN * kRfBK * 2;                 // one B slice: 4 KB
-constexpr int kRfStage = kRfSlices * (kRfA + kRfB);    // 72 KB
-constexpr int kRfStages = 3;
-constexpr int kRfThreads = 64 + 256;                   // producer warp, MMA warp, eight epilogue warps
+constexpr int kRfM = 128, kRfN = 128;                  // output tile
+constexpr int kRfA = kRfM * kRfBK * 2;                 // one A slice of a stage: 8 KB (a whole slice tile)
+constexpr int kRfB = kRfN * kRfBK * 2;                 // one B slice: 8 KB
+constexpr int kRfStage = kRfSlices * (kRfA + kRfB);    // 96 KB
+constexpr int kRfStages = 2;
+constexpr int kRfEpiWarps = 16;                        // epilogue warps: four per TMEM lane quarter
+constexpr int kRfThreads = 64 + 32 * kRfEpiWarps;      // producer warp, MMA warp, epilogue warps
 constexpr int kRfSmem = kRfStages * kRfStage + 1024 + 256;
 constexpr int kRfAcc = 4;                              // accumulators: levels 2, 3, 4, 5-7
+// sets of the four accumulators in the 512 TMEM columns: with 128-wide tiles
+// one set, drained in place (the MMAs of the next 128 k wait for the drain)
+constexpr int kRfBufs = 512 / (kRfAcc * kRfN);
+constexpr int kRfHalves = kRfM / kRfN;                 // B tiles per slice tile
+static_assert(kRfBufs >= 1 && kRfHalves >= 1, "tile shape");
 
 // Slices are stored tile by tile, each tile the byte image of the K-major,
 // 64-byte-swizzled shared-memory layout the tensor cores read: tile (rb, kb)
@@ -255,17 +261,24 @@ __device__ __forceinline__ uint64_t rf_desc(uint32_t saddr) {
   return d;
 }
 
-// Job u of a matrix with T row blocks -> (A row block ib, B half-block jn):
+// Job u of a matrix with T row blocks -> (A row block ib, B column tile jn):
 // bands of kRfBand row blocks, column-major inside a band, so that the grid's
 // concurrent jobs share few operand panels (about kRfBand A panels and
 // gridDim / kRfBand B panels, which L2 holds).
 constexpr int kRfBand = 8;
 __device__ __forceinline__ void rf_job(long long u, long long T, long long& ib, long long& jn) {
-  const long long tn = 2 * T, per_band = (long long)kRfBand * tn;
+  const long long tn = kRfHalves * T, per_band = (long long)kRfBand * tn;
   const long long band = u / per_band, w = u % per_band;
   const long long rows = (band + 1) * kRfBand <= T ? kRfBand : T - band * kRfBand;
   ib = band * kRfBand + w % rows;
   jn = w / rows;
+}
+
+// x 2^k for |k| <= 252: two exact power-of-two factors built from their
+// IEEE-754 exponent fields (each in [-126, 127])
+__device__ __forceinline__ float scale_pow2(float x, int k) {
+  const int k1 = k / 2, k2 = k - k1;
+  return x * __int_as_float((127 + k1) << 23) * __int_as_float((127 + k2) << 23);
 }
 
 // accumulator of the slice pair (s, t) (0-based): levels 2, 3, 4, then 5-7 together
@@ -296,7 +309,7 @@ __device__ __forceinline__ void rf_issue(uint32_t tmem_acc, uint32_t a0, uint32_
 }
 
 // C = A B^T over the flagged candidates, A = xs (rows of X0), B = bs (rows of
-// D, or of S); tiles of 128 x 64, jobs dealt round-robin over a persistent
+// D, or of S); tiles of 128 x 128, jobs dealt round-robin over a persistent
 // grid.  LMAX: highest level taken (7 for the residual, 4 for the correction).
 // mode 0: st = I - 2^(e_i + f_j) C  (the residual S);  mode 1: st = 2^(e_i + f_j) C  (T).
 // The accumulators are drained every kRfDrain stages (128 k: every level up to
@@ -327,7 +340,7 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 8);
+      mbar_init(&acc_empty[a], kRfEpiWarps);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -351,9 +364,9 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
         if (mi < 0) continue;
         const InvMat m = c.mats[mi];
         const RfBufs rb = rf_bufs(c, m);
-        const long long T = m.T, tn = 2 * T, jobs = T * tn;
+        const long long T = m.T, tn = kRfHalves * T, jobs = T * tn;
         for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
-          long long ib, jn;  // A row block; B row block jn / 2, half jn % 2
+          long long ib, jn;  // A row block; B rows: tile jn / kRfHalves, part jn % kRfHalves
           rf_job(u, T, ib, jn);
           for (long long kb = 0; kb < 4 * T; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, status)) {
@@ -367,7 +380,8 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
               if (sl >= nsl) break;
               bulk_load(smem_u32(s0 + sl * kRfA), rb.xs + rf_tile_off(T, sl, ib, kb), kRfA, &full[stage]);
               bulk_load(smem_u32(s0 + kRfSlices * kRfA + sl * kRfB),
-                        rb.bs + rf_tile_off(T, sl, jn / 2, kb) + (jn % 2) * (kRfN * kRfBK), kRfB, &full[stage]);
+                        rb.bs + rf_tile_off(T, sl, jn / kRfHalves, kb) + (jn % kRfHalves) * (kRfN * kRfBK), kRfB,
+                        &full[stage]);
             }
             if (++stage == kRfStages) {
               stage = 0;
@@ -386,7 +400,7 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
       for (int f = 0; f < nf && ok; ++f) {
         const int mi = rf_matrix(c, f);
         if (mi < 0) continue;
-        const long long T = c.mats[mi].T, jobs = T * 2 * T;
+        const long long T = c.mats[mi].T, jobs = T * kRfHalves * T;
         for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
           for (long long kb = 0; kb < 4 * T && ok; ++kb) {
             const bool first = kb % kRfDrain == 0, last = kb % kRfDrain == kRfDrain - 1;
@@ -397,12 +411,14 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
             }
             tc_fence_after();
             const uint32_t a0 = smem_u32(smem + stage * kRfStage);
-            rf_issue<LMAX>(tmem_base + abuf * 256, a0, a0 + kRfSlices * kRfA, idesc, first);
+            rf_issue<LMAX>(tmem_base + abuf * (kRfAcc * kRfN), a0, a0 + kRfSlices * kRfA, idesc, first);
             tc_commit(&empty[stage]);
             if (last) {
               tc_commit(&acc_full[abuf]);
-              abuf ^= 1;
-              if (abuf == 0) aphase ^= 1;
+              if (++abuf == kRfBufs) {
+                abuf = 0;
+                aphase ^= 1;
+              }
             }
             if (++stage == kRfStages) {
               stage = 0;
@@ -415,7 +431,7 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
       mbar_wait(done_bar, 0, abort_flag, status);
     }
   } else {
-    // ---------------- epilogue: warp e holds TMEM lanes 32 q.. and 32 columns of half h
+    // ---------------- epilogue: warp e holds TMEM lanes 32 q.. and the kCols columns of group h
     const int e = warp - 2;
     const int q = warp & 3;
     const int h = e / 4;
@@ -425,46 +441,63 @@ __global__ void __launch_bounds__(kRfThreads, 1) rf_gemm_kernel(InvCtx c, int n,
     for (int f = 0; f < nf && ok; ++f) {
       const int mi = rf_matrix(c, f);
       if (mi < 0) continue;
-      const InvMat m = c.mats[mi];
-      const RfBufs rb = rf_bufs(c, m);
-      const long long np = (long long)m.T * 128;
-      const long long tn = np / kRfN, jobs = (long long)m.T * tn;
-      for (long long u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
-        long long ib, jn;
-        rf_job(u, m.T, ib, jn);
-        const long long i0 = ib * kRfM, j0 = jn * kRfN;
-        float hi[32], lo[32];
+      const int T = c.mats[mi].T;
+      const int np = T * 128, jobs = T * (np / kRfN);  // 32-bit: few registers beside the sums
+      for (int u = blockIdx.x; u < jobs && ok; u += gridDim.x) {
+        long long ib64, jn64;
+        rf_job(u, T, ib64, jn64);
+        const int i0 = (int)ib64 * kRfM, j0 = (int)jn64 * kRfN;
+        constexpr int kCols = kRfN / (kRfEpiWarps / 4);  // this warp's columns
+        float hi[kCols], lo[kCols];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) hi[t] = lo[t] = 0.f;
-        for (long long kd = 0; kd < 4 * m.T / kRfDrain; ++kd) {
+        for (int t = 0; t < kCols; ++t) hi[t] = lo[t] = 0.f;
+        for (int kd = 0; kd < 4 * T / kRfDrain; ++kd) {
           if (!mbar_wait(&acc_full[abuf], aphase, abort_flag, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          for (int a = 0; a < nacc; ++a) {
-            uint32_t v[32];
-            tc_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + abuf * 256 + a * kRfN + h * 32, v);
-            tc_wait_ld();
 #pragma unroll
-            for (int t = 0; t < 32; ++t) df_add(hi[t], lo[t], __uint_as_float(v[t]));
+          for (int a = 0; a < kRfAcc; ++a) {
+            if (a >= nacc) break;
+#pragma unroll
+            for (int g = 0; g < kCols / 8; ++g) {  // eight columns at a time: few registers beside the sums
+              uint32_t v[8];
+              tc_ld_32x32b_x8(tmem_base + ((uint32_t)(q * 32) << 16) + abuf * (kRfAcc * kRfN) + a * kRfN + h * kCols +
+                                  g * 8,
+                              v);
+              tc_wait_ld();
+#pragma unroll
+              for (int t = 0; t < 8; ++t) df_add(hi[g * 8 + t], lo[g * 8 + t], __uint_as_float(v[t]));
+            }
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[abuf]);
-          abuf ^= 1;
-          if (abuf == 0) aphase ^= 1;
+          if (++abuf == kRfBufs) {
+            abuf = 0;
+            aphase ^= 1;
+          }
         }
         if (!ok) break;
-        const long long row = i0 + q * 32 + lane;
+        const RfBufs rb = rf_bufs(c, c.mats[mi]);
+        const int row = i0 + q * 32 + lane;
         const int er = rb.ex[row];
-        float* out = rb.st + row * np + j0 + h * 32;
+        float* out = rb.st + (long long)row * np + j0 + h * kCols;
+        const int* ebc = rb.eb + j0 + h * kCols;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const long long col = j0 + h * 32 + t;
-          const int sc = er + rb.eb[col];
-          const float vh = ldexpf(hi[t], sc), vl = ldexpf(lo[t], sc);
-          out[t] = mode == 0 ? ((row == col ? 1.f : 0.f) - vh) - vl : vh + vl;
+        for (int t4 = 0; t4 < kCols; t4 += 4) {  // four columns at a time (16-byte loads and stores)
+          const int4 e4 = *reinterpret_cast<const int4*>(ebc + t4);
+          const int ecs[4] = {e4.x, e4.y, e4.z, e4.w};
+          float o[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int col = j0 + h * kCols + t4 + u;
+            const int sc = er + ecs[u];
+            const float vh = scale_pow2(hi[t4 + u], sc), vl = scale_pow2(lo[t4 + u], sc);
+            o[u] = mode == 0 ? ((row == col ? 1.f : 0.f) - vh) - vl : vh + vl;
+          }
+          *reinterpret_cast<float4*>(out + t4) = make_float4(o[0], o[1], o[2], o[3]);
         }
       }
     }
