@@ -153,6 +153,16 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  if (prm.flags != nullptr) {
+    // a re-run over the flagged problems: nothing to do when none is flagged
+    // (the same answer in every CTA, so whole clusters leave together)
+    bool any = false;
+    for (int i = 0; i < prm.n_probs && !any; ++i) {
+      const int f = prm.probs[i].flag_idx;
+      any = f < 0 || prm.flags[f] != 0;
+    }
+    if (!any) return;
+  }
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGtStages; ++s) {
@@ -397,7 +407,16 @@ template <int NP>
 __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitParams prm) {
   // warp unit = 256 consecutive columns of one row (8 per lane); chunks of
   // kSplitChunk units never straddle two matrices, so the matrix lookup is
-  // block-uniform
+  // block-uniform.  Each warp fetches its next unit's row segment while it
+  // slices the current one.
+  if (prm.flags != nullptr) {  // a re-run over the flagged matrices: none flagged, nothing to do
+    bool any = false;
+    for (int i = 0; i < prm.n && !any; ++i) {
+      const int f = prm.items[i].flag_idx;
+      any = f < 0 || prm.flags[f] != 0;
+    }
+    if (!any) return;
+  }
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (long long ch = blockIdx.x; ch < prm.total_items; ch += gridDim.x) {
     int lo = 0, hi = prm.n;  // matrix with item_begin (in chunks) <= ch
@@ -413,10 +432,11 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
     const long long segs = (it.cols + kSplitSeg - 1) / kSplitSeg;
     const long long work = it.rows * segs;
     const long long w0 = (ch - it.item_begin) * kSplitChunk;
-    for (long long unit = w0 + warp; unit < w0 + kSplitChunk && unit < work; unit += 8) {
-      const long long r = unit / segs;
-      const long long c0 = (unit - r * segs) * kSplitSeg + lane * 8;
-      float x[8];
+    const long long w_end = w0 + kSplitChunk < work ? w0 + kSplitChunk : work;
+    // the lane's 8 values of unit u (zero past the row's end)
+    auto fetch = [&](long long u, float (&x)[8]) {
+      const long long r = u / segs;
+      const long long c0 = (u - r * segs) * kSplitSeg + lane * 8;
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = 0.f;
       if (c0 < it.cols) {
@@ -430,8 +450,19 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = (c0 + e < it.cols) ? src[e] : 0.f;
         }
-        split8_store<NP>(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
       }
+    };
+    long long unit = w0 + warp;
+    float xn[8];
+    if (unit < w_end) fetch(unit, xn);
+    for (; unit < w_end; unit += 8) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = xn[e];
+      if (unit + 8 < w_end) fetch(unit + 8, xn);
+      const long long r = unit / segs;
+      const long long c0 = (unit - r * segs) * kSplitSeg + lane * 8;
+      if (c0 < it.cols) split8_store<NP>(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
       if (it.probe != nullptr) {  // warp-uniform
         float p[8];
         probe8(x, c0, it.probe_shift, p);

@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(256) pc_check_kernel(const __grid_constant__ P
     }
     float acc4[4] = {0.f, 0.f, 0.f, 0.f};
     const long long r_end = (rg + 1) * kChkRows < it.d_out ? (rg + 1) * kChkRows : it.d_out;
-    for (long long r = rg * kChkRows; r < r_end; ++r) {
-      float g8[8], o8[8];
+    // this lane's 8 columns of row r of grad and out (zero past d_in)
+    auto fetch = [&](long long r, float (&g8)[8], float (&o8)[8]) {
       if (c0 + 8 <= it.d_in) {
         const float4 a = *reinterpret_cast<const float4*>(it.grad + r * it.ld_grad + c0);
         const float4 b = *reinterpret_cast<const float4*>(it.grad + r * it.ld_grad + c0 + 4);
@@ -192,6 +192,18 @@ __global__ void __launch_bounds__(256) pc_check_kernel(const __grid_constant__ P
           o8[e] = in ? it.out[r * it.ld_out + c0 + e] : 0.f;
         }
       }
+    };
+    // the next row is fetched while the current one is reduced
+    float gn[8], on[8];
+    if (rg * kChkRows < r_end) fetch(rg * kChkRows, gn, on);
+    for (long long r = rg * kChkRows; r < r_end; ++r) {
+      float g8[8], o8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        g8[e] = gn[e];
+        o8[e] = on[e];
+      }
+      if (r + 1 < r_end) fetch(r + 1, gn, on);
       float v[16], q[8];
       right_probe8(o8, c0, q);
 #pragma unroll
