@@ -370,7 +370,6 @@ TcLayout tc_layout(int n, const int* T);
 size_t refine_bytes(long long np);
 int run_refine_pass(const InvCtx& ctx, int n, int Tmax, cudaStream_t stream);
 // inverse_tc.cu: the residual probe y = X w over the refinement candidates
-int run_refined_probe(const InvCtx& ctx, int sms, cudaStream_t stream);
 int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, const int* Ts, const TcLayout& L,
                 cudaStream_t stream);
 

@@ -1024,18 +1024,6 @@ __global__ void __launch_bounds__(256, 2) tc_probe_kernel(InvCtx c, int t_only) 
   probe_strip(c, mi, blockIdx.x, true);
 }
 
-// The same over the Newton step's candidates (refine.cu), a persistent grid
-// over the flagged list: nothing runs when no matrix is flagged.
-__global__ void __launch_bounds__(256, 2) rf_probe_kernel(InvCtx c) {
-  const int nf = *c.nflagged;
-  for (int f = 0; f < nf; ++f) {
-    const int mi = c.flagged[f];
-    if (!c.st[mi].refine) continue;
-    for (long long strip = blockIdx.x; strip * kPrRows < c.mats[mi].d; strip += gridDim.x)
-      probe_strip(c, mi, strip, false);
-  }
-}
-
 // ------------------------------------------------------------------ host side
 static size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -1234,10 +1222,6 @@ static void timed_launch(int kind, cudaStream_t stream, F&& launch) {
   count_launch();
 }
 
-int run_refined_probe(const InvCtx& ctx, int sms, cudaStream_t stream) {
-  timed_launch(KFAC_K_INV_AUX, stream, [&] { rf_probe_kernel<<<4 * sms, 256, 0, stream>>>(ctx); });
-  return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
-}
 
 // Jobs per CTA of a far update: its CTAs retire every few jobs, so that the
 // higher-priority chain on the other stream finds SMs within tens of us.

@@ -40,10 +40,10 @@
 //   rf_split_kernel   S into slices
 //   rf_gemm_kernel    T = X0 S^T = X0 (I - D X0)    (levels up to 4)
 //   rf_sym_kernel     X1 = X0 + (T + T^T) / 2, written over X0 (exactly symmetric)
-// then the residual probe runs on X1 and a matrix whose estimate meets the
-// refined bar keeps X1; the others take a second step from X1 (the D slices
-// are taken again: their buffer held S), and those it does not settle go on
-// to the fp64 pass.
+// then sixteen probes of its own (rf_w16_kernel, once; rf_y16_kernel) estimate
+// the residual of X1, and a matrix whose estimate meets the refined bar keeps
+// X1; the others take a second step from X1 (the D slices are taken again:
+// their buffer held S), and those it does not settle go on to the fp64 pass.
 #include "common.cuh"
 #include "inverse_common.cuh"
 #include "launch.h"
@@ -78,20 +78,38 @@ __host__ __device__ inline long long rf_tile_off(long long T, int s, long long r
   return (((long long)s * T + rb) * (4 * T) + kb) * (kRfM * kRfBK);
 }
 
+// Probes of the decision after a step: kRfProbes of them,
+//   v_p(i) = s'(i) H16[p][i mod 16],  H16[p][b] = (-1)^popcount(p & b),
+// s'(i) = +-1 from the splitmix64 finaliser of i offset by 2^40 (a sign
+// stream apart from the fp32 pass's probes).  Each is a Rademacher vector;
+// their mean squared residual sums over the same-residue pairs mod 16, so
+// for a residual close to rank one (what a Newton step leaves: I - X1 D =
+// (I - X0 D)^2 up to rounding) it has the spread of sixteen independent
+// probes: an estimate below half the true residual has a probability near
+// 1e-3, against near 0.09 with four.
+constexpr int kRfProbes = 16;
+__device__ __forceinline__ float rf_sign(long long i) { return probe_base_sign(i + (1LL << 40)); }
+__device__ __forceinline__ float hadamard16(int p, int b) {
+  return (__popc((unsigned)(p & b & 15)) & 1) ? -1.f : 1.f;
+}
+
 // Per-matrix refinement buffers, at m.off_ref in the work region (np = 128 T):
 //   xs  bf16 [6][T][4T] tiles   slices of X0
 //   bs  bf16 [6][T][4T] tiles   slices of D, then of S
 //   st  fp32 [np][np]           S, then T
 //   ex, eb  int [np]            row exponents of xs and bs
+//   w16, y16  double-float [kRfProbes][np]   D v and X1 D v for the decision's probes
 struct RfBufs {
   uint16_t* xs;
   uint16_t* bs;
   float* st;
   int* ex;
   int* eb;
+  float2* w16;
+  float2* y16;
 };
 __host__ __device__ inline size_t rf_bytes(long long np) {
-  return (size_t)np * np * (2 * kRfSlices * 2 + 4) + (size_t)np * 8;
+  return (size_t)np * np * (2 * kRfSlices * 2 + 4) + (size_t)np * 8 + (size_t)np * kRfProbes * 2 * sizeof(float2);
 }
 __device__ __forceinline__ RfBufs rf_bufs(const InvCtx& c, const InvMat& m) {
   const long long np = (long long)m.T * 128;
@@ -102,6 +120,8 @@ __device__ __forceinline__ RfBufs rf_bufs(const InvCtx& c, const InvMat& m) {
   b.st = reinterpret_cast<float*>(b.bs + (size_t)kRfSlices * np * np);
   b.ex = reinterpret_cast<int*>(b.st + (size_t)np * np);
   b.eb = b.ex + np;
+  b.w16 = reinterpret_cast<float2*>(b.eb + np);  // np is a multiple of 128: 512-byte aligned
+  b.y16 = b.w16 + (size_t)kRfProbes * np;
   return b;
 }
 
@@ -557,15 +577,114 @@ __global__ void __launch_bounds__(256) rf_sym_kernel(InvCtx c) {
   }
 }
 
+// ------------------------------------------------------------------ probes of the decision
+// w = D v for the kRfProbes probes of each candidate, once (D does not change
+// over the steps).  A warp per row r, D read by symmetry from its upper
+// triangle (the row segment from r on, the column segment above r), with
+// gamma_extra on the diagonal: lane l meets only columns of residue l mod 16,
+// so each lane keeps one double-float sum Y_b (s'(c) D_rc over c = b mod 16);
+// then w_p = sum_b H16[p][b] Y_b.
+__global__ void __launch_bounds__(256) rf_w16_kernel(InvCtx c) {
+  const int nf = *c.nflagged;
+  const int lane = threadIdx.x % 32;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const long long nw = (long long)gridDim.x * blockDim.x / 32;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = rf_matrix(c, f);
+    if (mi < 0) continue;
+    const InvMat m = c.mats[mi];
+    const RfBufs rb = rf_bufs(c, m);
+    const long long np = (long long)m.T * 128;
+    for (long long r = gw; r < m.d; r += nw) {
+      float hi = 0.f, lo = 0.f;
+      for (long long col = lane; col < m.d; col += 32) {
+        float x = col >= r ? m.D[r * m.ld_in + col] : m.D[col * m.ld_in + r];
+        if (col == r) x += c.gamma_extra;
+        df_add(hi, lo, x * rf_sign(col));  // exact: a sign flip
+      }
+      {  // lanes l and l + 16 hold the same residue class
+        const float oh = __shfl_xor_sync(0xffffffffu, hi, 16), ol = __shfl_xor_sync(0xffffffffu, lo, 16);
+        df_add(hi, lo, oh);
+        lo += ol;
+      }
+      float wh = 0.f, wl = 0.f;  // lane p < 16: w_p
+      for (int b = 0; b < 16; ++b) {
+        const float yh = __shfl_sync(0xffffffffu, hi, b), yl = __shfl_sync(0xffffffffu, lo, b);
+        const float sg = hadamard16(lane & 15, b);
+        df_add(wh, wl, sg * yh);
+        wl += sg * yl;
+      }
+      if (lane < kRfProbes) rb.w16[lane * np + r] = df_pack(wh, wl);
+    }
+  }
+}
+
+// y = X1 w for the kRfProbes probes of each candidate: a CTA per 8 rows (a
+// warp per row), columns in chunks of 128 with the chunk's w staged in shared
+// memory; double-float products and sums.
+__global__ void __launch_bounds__(256) rf_y16_kernel(InvCtx c) {
+  __shared__ __align__(16) float2 ws[kRfProbes * 128];
+  const int nf = *c.nflagged;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int f = 0; f < nf; ++f) {
+    const int mi = rf_matrix(c, f);
+    if (mi < 0) continue;  // uniform over the grid
+    const InvMat m = c.mats[mi];
+    const RfBufs rb = rf_bufs(c, m);
+    const long long np = (long long)m.T * 128;
+    for (long long r0 = (long long)blockIdx.x * 8; r0 < m.d; r0 += (long long)gridDim.x * 8) {  // uniform over the block
+      const long long r = r0 + warp;
+      float hi[kRfProbes], lo[kRfProbes];
+#pragma unroll
+      for (int p = 0; p < kRfProbes; ++p) hi[p] = lo[p] = 0.f;
+      for (long long c0 = 0; c0 < m.d; c0 += 128) {
+        __syncthreads();  // the previous chunk's w has been read
+        for (int e = threadIdx.x; e < kRfProbes * 128; e += 256) {
+          const long long col = c0 + e % 128;
+          ws[e] = col < m.d ? rb.w16[(e / 128) * np + col] : make_float2(0.f, 0.f);
+        }
+        __syncthreads();
+        const long long col = c0 + 4 * lane;  // float4 reads stay inside the row (ld_out % 4 == 0)
+        if (r < m.d && col < m.d) {
+          const float4 x4 = *reinterpret_cast<const float4*>(m.X + r * m.ld_out + col);
+          const float xs[4] = {x4.x, col + 1 < m.d ? x4.y : 0.f, col + 2 < m.d ? x4.z : 0.f,
+                               col + 3 < m.d ? x4.w : 0.f};
+#pragma unroll
+          for (int p = 0; p < kRfProbes; ++p) {
+            const float4 w01 = *reinterpret_cast<const float4*>(ws + p * 128 + 4 * lane);
+            const float4 w23 = *reinterpret_cast<const float4*>(ws + p * 128 + 4 * lane + 2);
+            df_add_prod(hi[p], lo[p], xs[0], w01.x, w01.y);
+            df_add_prod(hi[p], lo[p], xs[1], w01.z, w01.w);
+            df_add_prod(hi[p], lo[p], xs[2], w23.x, w23.y);
+            df_add_prod(hi[p], lo[p], xs[3], w23.z, w23.w);
+          }
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < kRfProbes; ++p) {
+        float h = hi[p], l = lo[p];
+        for (int o = 16; o > 0; o >>= 1) {
+          const float oh = __shfl_xor_sync(0xffffffffu, h, o), ol = __shfl_xor_sync(0xffffffffu, l, o);
+          df_add(h, l, oh);
+          l += ol;
+        }
+        if (lane == 0 && r < m.d) rb.y16[p * np + r] = df_pack(h, l);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ decision after the step
-// The refined estimate (the probe kernel has formed y = X1 w for the
-// candidates): accepted at most kRefinedResidual (twice the 2.5e-4 of the fp32
-// pass: a matrix refined to its fp32 storage floor sits near 2.5e-4, and the
-// fp64 pass, whose result is stored in fp32 as well, cannot do better there).
+// The refined estimate from the kRfProbes probes (y = X1 w formed by
+// rf_y16_kernel): accepted at most kRefinedResidual (twice the 2.5e-4 of the
+// fp32 pass: a matrix refined to its fp32 storage floor sits near 2.5e-4, and
+// the fp64 pass, whose result is stored in fp32 as well, cannot do better
+// there).
 constexpr double kRefinedResidual = 5.0e-4;
 // Newton steps at most: the fp32 pass leaves the 4609-wide ResNet-50 conv
-// factor at a residual near 6e-3 (about 1e-3 in the host emulation), which one
-// step takes to about 2e-3 and a second one to the storage floor.
+// factor at a residual near 6e-3, which one step takes to about 7e-4 (inside
+// the 1e-3 bar, not inside the 5e-4 acceptance) and a second one to the fp32
+// storage floor.
 constexpr int kRfSteps = 2;
 
 __global__ void __launch_bounds__(128) rf_decide_kernel(InvCtx c) {
@@ -573,16 +692,18 @@ __global__ void __launch_bounds__(128) rf_decide_kernel(InvCtx c) {
   if (mi < 0) return;
   const InvMat m = c.mats[mi];
   const long long np = (long long)m.T * 128;
-  const float2* y = c.probe + m.off_probe + (long long)kProbes * np;
+  const float2* y = rf_bufs(c, m).y16;
   __shared__ double red[128];
   double e2 = 0.0;
-  for (long long r = threadIdx.x; r < m.d; r += 128)
+  for (long long r = threadIdx.x; r < m.d; r += 128) {
+    const float sr = rf_sign(r);
 #pragma unroll
-    for (int p = 0; p < kProbes; ++p) {
+    for (int p = 0; p < kRfProbes; ++p) {
       const float2 yv = y[p * np + r];
-      const double dv = df_value(yv.x, yv.y) - probe_sign(r, p);
+      const double dv = df_value(yv.x, yv.y) - (double)(sr * hadamard16(p, (int)(r & 15)));
       e2 += dv * dv;
     }
+  }
   red[threadIdx.x] = e2;
   __syncthreads();
   for (int s = 64; s > 0; s >>= 1) {
@@ -590,7 +711,7 @@ __global__ void __launch_bounds__(128) rf_decide_kernel(InvCtx c) {
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    const double est = sqrt(red[0] / kProbes / (double)m.d);
+    const double est = sqrt(red[0] / kRfProbes / (double)m.d);
     InvState& s = c.st[mi];
     s.est_res = (float)est;
     if (est <= kRefinedResidual) {  // false for NaN
@@ -637,6 +758,7 @@ int run_refine_pass(const InvCtx& ctx, int n, int Tmax, cudaStream_t stream) {
   rf_mark_kernel<<<(n + 127) / 128, 128, 0, stream>>>(ctx, n);
   count_launch();
   (void)Tmax;
+  timed([&] { rf_w16_kernel<<<4 * sms, 256, 0, stream>>>(ctx); });
   // up to kRfSteps steps; a matrix whose estimate meets the bar after a step
   // leaves the candidates (the ones that follow skip it)
   for (int step = 0; step < kRfSteps; ++step) {
@@ -645,8 +767,7 @@ int run_refine_pass(const InvCtx& ctx, int n, int Tmax, cudaStream_t stream) {
     timed([&] { rf_split_kernel<<<dim3((unsigned)(2 * sms), 1), 256, kRfSplitSmem, stream>>>(ctx, 2); });  // S
     timed([&] { rf_gemm_kernel<4><<<sms, kRfThreads, kRfSmem, stream>>>(ctx, n, 1, status); });
     timed([&] { rf_sym_kernel<<<4 * sms, 256, 0, stream>>>(ctx); });
-    const int rc = run_refined_probe(ctx, sms, stream);
-    if (rc != KFAC_OK) return rc;
+    timed([&] { rf_y16_kernel<<<4 * sms, 256, 0, stream>>>(ctx); });
     rf_decide_kernel<<<n, 128, 0, stream>>>(ctx);
     count_launch();
   }
