@@ -694,17 +694,20 @@ __global__ void __launch_bounds__(128) rf_decide_kernel(InvCtx c) {
   const long long np = (long long)m.T * 128;
   const float2* y = rf_bufs(c, m).y16;
   __shared__ double red[128];
-  double e2 = 0.0;
+  // (y - v) in fp32: y_hi - v is exact while y is within a factor two of v
+  // (a residual far below one), and larger differences need no precision;
+  // per-thread sums in fp32 (a few hundred terms), the block's in fp64
+  float e2 = 0.f;
   for (long long r = threadIdx.x; r < m.d; r += 128) {
     const float sr = rf_sign(r);
 #pragma unroll
     for (int p = 0; p < kRfProbes; ++p) {
       const float2 yv = y[p * np + r];
-      const double dv = df_value(yv.x, yv.y) - (double)(sr * hadamard16(p, (int)(r & 15)));
-      e2 += dv * dv;
+      const float dv = (yv.x - sr * hadamard16(p, (int)(r & 15))) + yv.y;
+      e2 = fmaf(dv, dv, e2);
     }
   }
-  red[threadIdx.x] = e2;
+  red[threadIdx.x] = (double)e2;
   __syncthreads();
   for (int s = 64; s > 0; s >>= 1) {
     if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
