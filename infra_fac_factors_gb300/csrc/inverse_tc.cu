@@ -53,8 +53,8 @@ enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
 
 // Shared-memory ring of each kind: a stage holds one 32-wide k-block of all
 // three slices of A (128 rows) and B.  The panel's B is the 128-row diagonal
-// inverse and its epilogue stores straight to global memory: four 48 KB
-// stages.  X = U U^T (B of 256 rows) also stores straight from registers
+// inverse; its eight epilogue warps pass their 32 x 64 blocks through
+// shared memory (64 KB): three 48 KB stages.  X = U U^T (B of 256 rows) also stores straight from registers
 // (row stores of X and of its mirror): three 72 KB stages.  The updates add
 // into the work buffer through 32 x 32 TMA reductions staged in shared memory
 // (64 KB): two 72 KB stages.  (Vector reductions straight from registers,
@@ -68,10 +68,10 @@ constexpr int kItPanelStage = 32 * 64 * 4;
 template <int KIND>
 struct ItCfg {
   static constexpr int b_rows = KIND == kItPanel ? 128 : 256;
-  static constexpr int stages = KIND == kItUpdate ? 2 : KIND == kItPanel ? 4 : 3;
+  static constexpr int stages = KIND == kItUpdate ? 2 : 3;
   static constexpr int b_slice = b_rows * kItBK * 2;
   static constexpr int stage = kSlices * (kItA + b_slice);
-  static constexpr int out = KIND == kItUpdate ? 8 * 2 * kItOutBlock : KIND == kItPanel ? 4 * kItPanelStage : 0;
+  static constexpr int out = KIND == kItUpdate ? 8 * 2 * kItOutBlock : KIND == kItPanel ? 8 * kItPanelStage : 0;
   static constexpr int smem = stages * stage + out + 1024 + 256;
 };
 
@@ -429,14 +429,17 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
   } else {
     const int e = warp - 2;
     const int q = warp & 3;  // TMEM lane quarter
-    const int h = e / 4;     // column half of the 256-wide tile
+    const int h = e / 4;     // column half of the 256-wide tile (of the panel's 128-wide one)
+    // first column of this warp's share: 128 wide, or 64 wide on the panel's tile
+    const int col0w = KIND == kItPanel ? h * 64 : h * 128;
+    constexpr int kDrainGroups = KIND == kItPanel ? 2 : 4;  // 32-column TMEM loads per drain
     uint32_t acc = 0, acc_phase = 0;
     int obuf = 0;
     bool ok = true;
     for (long long u = blockIdx.x; u < prm.total_jobs && ok; u += gridDim.x) {
       const ItJob J = it_decode<KIND>(prm, u);
       if (!J.valid) continue;
-      const bool mine = h * 128 < J.n_mma;  // this warp's 128 columns exist
+      const bool mine = col0w < J.n_mma;  // this warp's columns exist
       float run[128];
 #pragma unroll
       for (int t = 0; t < 128; ++t) run[t] = 0.f;
@@ -448,9 +451,9 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         }
         tc_fence_after();
         if (mine) {
-          const uint32_t base = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + h * 128;
+          const uint32_t base = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256 + col0w;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 0; g < kDrainGroups; ++g) {
             uint32_t v[32];
             tc_ld_32x32b_x32(base + g * 32, v);
             tc_wait_ld();
@@ -468,10 +471,10 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
       const int mrow = q * 32 + lane;  // row of the 128-row output tile
       if (KIND == kItPanel) {
         // L_rk (r > k) into Lp, or U_rk (r < k) into U, as three bf16 slices.
-        // The warp's 32 rows go through shared memory in two 64-column halves
-        // (16-byte chunks XOR-swizzled by row: conflict-free both ways), so
-        // that each store instruction writes four whole 128-byte row
-        // segments instead of 32 pieces of 32 different rows.
+        // The two warps of a lane quarter take 64 columns each; a warp's 32
+        // rows go through shared memory (16-byte chunks XOR-swizzled by row:
+        // conflict-free both ways), so that each store instruction writes four
+        // whole 128-byte row segments instead of 32 pieces of 32 different rows.
         uint16_t* dst0;
         long long sstride, ld;
         if (J.mode == 0) {
@@ -484,23 +487,19 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
           ld = prm.b.LD;
         }
         float* stg = reinterpret_cast<float*>(out_stage + e * kItPanelStage);
+        __syncwarp();  // the previous job's rows have been read
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-          __syncwarp();  // the previous half has been read
+        for (int j = 0; j < 16; ++j)
+          *reinterpret_cast<float4*>(stg + lane * 64 + ((j ^ (lane & 7)) << 2)) =
+              make_float4(run[4 * j], run[4 * j + 1], run[4 * j + 2], run[4 * j + 3]);
+        __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            *reinterpret_cast<float4*>(stg + lane * 64 + ((j ^ (lane & 7)) << 2)) =
-                make_float4(run[hc * 64 + 4 * j], run[hc * 64 + 4 * j + 1], run[hc * 64 + 4 * j + 2],
-                            run[hc * 64 + 4 * j + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int r = it * 4 + lane / 8, k2 = 2 * (lane % 8);
-            const float4 v0 = *reinterpret_cast<const float4*>(stg + r * 64 + ((k2 ^ (r & 7)) << 2));
-            const float4 v1 = *reinterpret_cast<const float4*>(stg + r * 64 + (((k2 + 1) ^ (r & 7)) << 2));
-            const float x8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            split8_store(x8, dst0 + (long long)r * ld + hc * 64 + k2 * 4, sstride);
-          }
+        for (int it = 0; it < 8; ++it) {
+          const int r = it * 4 + lane / 8, k2 = 2 * (lane % 8);
+          const float4 v0 = *reinterpret_cast<const float4*>(stg + r * 64 + ((k2 ^ (r & 7)) << 2));
+          const float4 v1 = *reinterpret_cast<const float4*>(stg + r * 64 + (((k2 + 1) ^ (r & 7)) << 2));
+          const float x8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          split8_store(x8, dst0 + (long long)r * ld + col0w + k2 * 4, sstride);
         }
       } else if (KIND == kItUpdate) {
         // -acc into Acc through 32 x 32 TMA add-reductions (or stores, first time)
