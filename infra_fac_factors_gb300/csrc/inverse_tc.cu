@@ -834,7 +834,7 @@ __global__ void __launch_bounds__(128) tc_route_kernel(InvCtx c) {
 // ------------------------------------------------------------------ step k: diagonal block
 // Cholesky and inverse of the diagonal block k: Winv_k rows (the panel's B
 // operand) and U_kk = Winv_k^T, as bf16 slices.
-__global__ void __launch_bounds__(256, 1) tc_diag_kernel(InvCtx c, TcBufs b, int k) {
+__global__ void __launch_bounds__(256, 2) tc_diag_kernel(InvCtx c, TcBufs b, int k) {
   const int mi = blockIdx.x;
   if (!inv_active(c, mi, true)) return;
   const InvMat m = c.mats[mi];
