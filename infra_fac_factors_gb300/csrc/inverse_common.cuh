@@ -369,7 +369,7 @@ TcLayout tc_layout(int n, const int* T);
 // refine.cu: bytes of one matrix's refinement buffers (np = 128 T), and the pass
 size_t refine_bytes(long long np);
 int run_refine_pass(const InvCtx& ctx, int n, int Tmax, cudaStream_t stream);
-// inverse_tc.cu: the residual probe y = X w over the refinement candidates
+// inverse_tc.cu: the fp32 pass on tensor cores (with AUTO's residual probes)
 int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, const int* Ts, const TcLayout& L,
                 cudaStream_t stream);
 
