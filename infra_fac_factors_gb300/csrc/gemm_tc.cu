@@ -384,11 +384,11 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
 constexpr int kSplitSeg = 256;   // columns of one warp unit (32 lanes x 8)
 constexpr int kSplitChunk = 64;  // warp units per block iteration (8 warps x 8)
 
-// p[k] = sum_e z_k[c0 + e] x[e] for eight Rademacher probes z_k: z_k[c] is
-// H8[k][c % 8] times the sign in bit (c % 8) + shift of probe_hash(c / 8),
-// H8 the 8 x 8 Sylvester-Hadamard matrix
+// p[k] = sum_e z_k[c0 + e] x[e] for the eight probes z_k of gemm_tc.h
+// (c0 a multiple of 8; bit offset `shift`)
 __device__ __forceinline__ void probe8(const float (&x)[8], long long c0, int shift, float (&p)[8]) {
-  const uint32_t h = probe_hash((uint32_t)(c0 >> 3)) >> shift;
+  const uint32_t hh = probe_hash((uint32_t)(c0 >> 3)), h = hh >> shift;
+  const int t = probe_class_offset(hh, shift);
 #pragma unroll
   for (int e = 0; e < 8; ++e) p[e] = ((h >> e) & 1u) ? -x[e] : x[e];
   // 8-point Walsh-Hadamard transform: p[k] = sum_e (-1)^popcount(k & e) p[e]
@@ -401,6 +401,8 @@ __device__ __forceinline__ void probe8(const float (&x)[8], long long c0, int sh
         p[e] = a + b;
         p[e + len] = a - b;
       }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) p[k] *= hadamard8(k, t);  // the class offset t
 }
 
 template <int NP>

@@ -52,6 +52,16 @@ struct SplitParams {
 };
 
 // Probes of the preconditioning check: eight Rademacher vectors on each side.
+// Entry k of the probes at index i (8 g + e):
+//   z_k(i) = H8[k][e ^ t(g)] * (sign from bit e + shift of probe_hash(g)),
+// H8 the 8 x 8 Sylvester-Hadamard matrix, shift 0 for the right probes and 8
+// for the left ones, and t(g) a 3-bit class offset per group of eight (bits
+// 16-18 of the hash for the right probes, 19-21 for the left).  Each z_k is a
+// Rademacher vector; the mean of the 8 x 8 bilinear forms keeps the pairs
+// of equal class, and the class offset stops a residual concentrated on
+// every eighth index from falling into one class.  Since
+// H8[k][e ^ t] = H8[k][e] H8[k][t], a group's eight projections are its
+// 8-point Walsh-Hadamard transform with probe k's result times H8[k][t].
 constexpr int kProbeN = 8;
 
 // sign (+1 / -1) of probe k at index i: bit k + shift of a 32-bit integer
@@ -63,6 +73,16 @@ __host__ __device__ __forceinline__ uint32_t probe_hash(uint32_t x) {
   x *= 0x846ca68bU;
   x ^= x >> 16;
   return x;
+}
+
+// t(g) of the probes with bit offset `shift` (0 or 8), from probe_hash(g)
+__host__ __device__ __forceinline__ int probe_class_offset(uint32_t hash, int shift) {
+  return (int)((hash >> (16 + 3 * (shift / 8))) & 7u);
+}
+// H8[k][b] = (-1)^popcount(k & b)
+__host__ __device__ __forceinline__ float hadamard8(int k, int b) {
+  const int kb = k & b & 7;
+  return ((kb ^ (kb >> 1) ^ (kb >> 2)) & 1) ? -1.f : 1.f;
 }
 
 // `planes` bf16 slices per fp32 value (2 or 3).  Items whose flag_idx >= 0 run

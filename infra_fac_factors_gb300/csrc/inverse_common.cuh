@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "probes.cuh"
 
 namespace kfac {
 
@@ -47,30 +48,9 @@ struct InvState {
   int refined;  // its inverse came from the tensor-core Newton step (refine.cu)
 };
 
-// Probe vectors v_p (p < kProbes = 4) of the residual check:
-//   v_p(i) = s(i) H4[p][i mod 4],  H4[p][b] = (-1)^popcount(p & b)  (Sylvester-Hadamard),
-// with s(i) in {-1, +1} from the splitmix64 finaliser of i.  Each v_p alone
-// has independent +-1 entries (a Rademacher vector, so E||E v_p||^2 =
-// ||E||_F^2); together, sum_p v_p(i) v_p(j) / 4 is s(i) s(j) when i = j mod 4
-// and zero otherwise, so the four squared norms average to a sum over the
-// same-residue pairs alone (no worse than four independent vectors when the
-// residual is close to rank one).  The structure lets D v_p be formed from
-// four sums of s(j) D_ij, one per residue class of j.
-__host__ __device__ __forceinline__ float probe_base_sign(long long i) {
-  unsigned long long z = (unsigned long long)i + 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  z ^= z >> 31;
-  return (z & 1ull) ? 1.f : -1.f;
-}
-__host__ __device__ __forceinline__ float hadamard4(int p, int b) {
-  const int pb = p & b & 3;
-  return ((pb ^ (pb >> 1)) & 1) ? -1.f : 1.f;
-}
-static_assert(kProbes == 4, "the probes are the four rows of H4");
-__device__ __forceinline__ double probe_sign(long long i, int p) {
-  return (double)(probe_base_sign(i) * hadamard4(p, (int)(i & 3)));
-}
+static_assert(kProbes == 4, "the fp32 pass's probes are the four rows of H4 (probes.cuh)");
+// v_p(i) of the fp32 pass's residual check (probes.cuh)
+__device__ __forceinline__ double probe_sign(long long i, int p) { return (double)probe4(i, p); }
 
 struct InvSetup {
   InvMat mats[kInvMaxGroup];

@@ -47,7 +47,9 @@ constexpr int kItDrain = 2;
 // accumulator is drained every eight k-steps, as in the 16-bit GEMM of the
 // preconditioning
 constexpr int kItDrain16 = 8;
-constexpr int kLoadSmem = (128 * 129 + 2 * 128) * 4;  // the tile, and the probe signs s() of its two blocks
+// the tile; the probe signs s() of its two blocks, their indices in class
+// order and the four class starts of each
+constexpr int kLoadSmem = (128 * 129 + 2 * 128) * 4 + (2 * 128 + 2 * 8) * 4;
 
 enum { kItPanel = 0, kItUpdate = 1, kItLauum = 2 };
 
@@ -617,25 +619,58 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_
     // the rows of block R down its columns (the mirror), the partial sums of
     //   |D_rc| (c != r)      -> gpart: Gershgorin radii (tc_route_kernel) and ||D||_1
     //   D_rc v_p(c)          -> wpart: w = D v for the residual probes
-    // With v_p(c) = s(c) H4[p][c mod 4] (inverse_common.cuh), the four sums
-    // come from one double-float sum of s(c) D_rc per residue class of c
-    // (the sign flips are exact), combined by a 4-point Hadamard transform at
-    // the end.  On a diagonal tile only its upper triangle counts, and the
-    // diagonal itself (with gamma_extra) goes into w only.  Columns of the
-    // tile at or past d hold whatever the float4 loads brought from the
-    // padding: they are left out; rows past d were loaded as zero.
+    // With v_p(c) = s(c) H4[p][class(c)] (probes.cuh), the four sums come
+    // from one double-float sum of s(c) D_rc per class of c (the sign flips
+    // are exact), combined by a 4-point Hadamard transform at the end; each
+    // thread walks its columns (or rows) class by class, in index order within
+    // a class (so that the sums do not depend on scheduling).  On a diagonal
+    // tile only its upper triangle counts, and the diagonal itself (with
+    // gamma_extra) goes into w only.  Columns of the tile at or past d hold
+    // whatever the float4 loads brought from the padding: they are left out;
+    // rows past d were loaded as zero.
     float* sr = sub + 128 * 129;  // s() of block R's indices
     float* sc = sr + 128;         // and of block C's
-    for (int e = t; e < 128; e += 256) {
-      sr[e] = probe_base_sign((long long)R * 128 + e);
-      sc[e] = probe_base_sign((long long)C * 128 + e);
+    int* lr = reinterpret_cast<int*>(sc + 128);  // block R's indices 0..127 in class order
+    int* lc = lr + 128;                           // block C's
+    int* orr = lc + 128;                          // class starts in lr (4, then the warps' counts)
+    int* occ = orr + 8;                           // and in lc
+    {
+      // threads 0-127 sort block R's indices by class, 128-255 block C's:
+      // each warp counts its indices of each class with a ballot, then every
+      // index lands at (class start) + (the class's count in earlier warps) +
+      // (its rank among the warp's indices of the class)
+      const int half = t / 128, e = t % 128, wq = e / 32, ln = e % 32;
+      const long long gi = (long long)(half ? C : R) * 128 + e;
+      (half ? sc : sr)[e] = probe_base_sign(gi);
+      const int cls = probe_class(gi);
+      __shared__ int wcnt[2][4][4];  // [half][warp][class]
+      unsigned masks[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        masks[b] = __ballot_sync(0xffffffffu, cls == b);
+        if (ln == 0) wcnt[half][wq][b] = __popc(masks[b]);
+      }
+      __syncthreads();
+      int start = 0;
+      for (int b = 0; b < cls; ++b)
+        for (int w = 0; w < 4; ++w) start += wcnt[half][w][b];
+      for (int w = 0; w < wq; ++w) start += wcnt[half][w][cls];
+      const unsigned mk = cls == 0 ? masks[0] : cls == 1 ? masks[1] : cls == 2 ? masks[2] : masks[3];
+      start += __popc(mk & ((1u << ln) - 1u));
+      (half ? lc : lr)[start] = e;
+      if (e < 5) {  // class starts 0..4
+        int o = 0;
+        for (int b = 0; b < e; ++b)
+          for (int w = 0; w < 4; ++w) o += wcnt[half][w][b];
+        (half ? occ : orr)[e] = o;
+      }
     }
     __syncthreads();
     float* gp = c.gpart + m.off_gpart;
     float2* wp = c.wpart + m.off_gpart * kProbes;
     const long long cleft = m.d - (long long)R * 128;
     const int jmax = cleft < 128 ? (int)cleft : 128;
-    float s = 0.f, yhi[4] = {0.f, 0.f, 0.f, 0.f}, ylo[4] = {0.f, 0.f, 0.f, 0.f};  // residue-class sums
+    float s = 0.f, yhi[4] = {0.f, 0.f, 0.f, 0.f}, ylo[4] = {0.f, 0.f, 0.f, 0.f};  // class sums
     long long slot = -1;  // (row block, column block) of this thread's sums
     int row = 0;
     if (R == C) {
@@ -643,50 +678,55 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_
         row = t;
         slot = (long long)C * m.T + C;
         if (t < jmax) {
-          for (int j = t + 1; j < jmax; ++j) {
-            const float x = sub[t * 129 + j];
-            s += fabsf(x);
-            df_add(yhi[j & 3], ylo[j & 3], x * sr[j]);
-          }
-          for (int i2 = 0; i2 < t; ++i2) {
-            const float x = sub[i2 * 129 + t];
-            s += fabsf(x);
-            df_add(yhi[i2 & 3], ylo[i2 & 3], x * sc[i2]);
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            for (int q = orr[b]; q < orr[b + 1]; ++q) {
+              const int j = lr[q];
+              if (j <= t || j >= jmax) continue;
+              const float x = sub[t * 129 + j];
+              s += fabsf(x);
+              df_add(yhi[b], ylo[b], x * sr[j]);
+            }
+            for (int q = occ[b]; q < occ[b + 1]; ++q) {
+              const int i2 = lc[q];
+              if (i2 >= t) continue;
+              const float x = sub[i2 * 129 + t];
+              s += fabsf(x);
+              df_add(yhi[b], ylo[b], x * sc[i2]);
+            }
           }
           const float dg = sub[t * 129 + t] + c.gamma_extra;
-          df_add(yhi[t & 3], ylo[t & 3], dg * sc[t]);
+          const int bt = probe_class((long long)C * 128 + t);
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (b == bt) df_add(yhi[b], ylo[b], dg * sc[t]);
         }
       }
     } else if (t < 128) {
       row = t;
       slot = (long long)C * m.T + R;
-      // unrolled by the residue class, so that each sum stays in registers
-      int j = 0;
-      for (; j + 4 <= jmax; j += 4) {
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const float x = sub[t * 129 + j + b];
+      for (int b = 0; b < 4; ++b)
+        for (int q = orr[b]; q < orr[b + 1]; ++q) {
+          const int j = lr[q];
+          if (j >= jmax) continue;
+          const float x = sub[t * 129 + j];
           s += fabsf(x);
-          df_add(yhi[b], ylo[b], x * sr[j + b]);
+          df_add(yhi[b], ylo[b], x * sr[j]);
         }
-      }
-      for (; j < jmax; ++j) {
-        const float x = sub[t * 129 + j];
-        s += fabsf(x);
-        df_add(yhi[j & 3], ylo[j & 3], x * sr[j]);
-      }
     } else {
       row = t - 128;
       slot = (long long)R * m.T + C;
-      if (row < jmax)
-        for (int i2 = 0; i2 < 128; i2 += 4) {
+      if (row < jmax) {
 #pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const float x = sub[(i2 + b) * 129 + row];
+        for (int b = 0; b < 4; ++b)
+          for (int q = occ[b]; q < occ[b + 1]; ++q) {
+            const int i2 = lc[q];
+            const float x = sub[i2 * 129 + row];
             s += fabsf(x);
-            df_add(yhi[b], ylo[b], x * sc[i2 + b]);
+            df_add(yhi[b], ylo[b], x * sc[i2]);
           }
-        }
+      }
     }
     if (slot >= 0) {
       gp[slot * 128 + row] = s;

@@ -113,16 +113,18 @@ struct PcChkParams {
   int n;
 };
 
-// sign of left probe l at row r (the probes of probe8 with bit offset 8)
+// left probe l at row r (the probes of gemm_tc.h with bit offset 8)
 __device__ __forceinline__ float left_sign(long long r, int l) {
-  const uint32_t h = probe_hash((uint32_t)(r >> 3)) >> 8;
+  const uint32_t hh = probe_hash((uint32_t)(r >> 3)), h = hh >> 8;
   const int e = (int)(r & 7);
-  return ((__popc(l & e) + (int)((h >> e) & 1u)) & 1) ? -1.f : 1.f;
+  const int b = e ^ probe_class_offset(hh, 8);
+  return ((__popc(l & b) + (int)((h >> e) & 1u)) & 1) ? -1.f : 1.f;
 }
 
 // p[k] = sum_e z_k[c0 + e] x[e]: the right probes (bit offset 0)
 __device__ __forceinline__ void right_probe8(const float (&x)[8], long long c0, float (&p)[8]) {
   const uint32_t h = probe_hash((uint32_t)(c0 >> 3));
+  const int t = probe_class_offset(h, 0);
 #pragma unroll
   for (int e = 0; e < 8; ++e) p[e] = ((h >> e) & 1u) ? -x[e] : x[e];
 #pragma unroll
@@ -134,6 +136,8 @@ __device__ __forceinline__ void right_probe8(const float (&x)[8], long long c0, 
         p[e] = a + b;
         p[e + len] = a - b;
       }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) p[k] *= hadamard8(k, t);  // the class offset t
 }
 
 // Warp unit: one 256-column segment (8 columns per lane) of kChkRows rows.

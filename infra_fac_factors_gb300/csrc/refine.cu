@@ -40,10 +40,11 @@
 //   rf_split_kernel   S into slices
 //   rf_gemm_kernel    T = X0 S^T = X0 (I - D X0)    (levels up to 4)
 //   rf_sym_kernel     X1 = X0 + (T + T^T) / 2, written over X0 (exactly symmetric)
-// then sixteen probes of its own (rf_w16_kernel, once; rf_y16_kernel) estimate
-// the residual of X1, and a matrix whose estimate meets the refined bar keeps
-// X1; the others take a second step from X1 (the D slices are taken again:
-// their buffer held S), and those it does not settle go on to the fp64 pass.
+// then sixteen independent probes of its own (rf_w16_kernel, once;
+// rf_y16_kernel) estimate the residual of X1, and a matrix whose estimate
+// meets the refined bar keeps X1; the others take a second step from X1 (the
+// D slices are taken again: their buffer held S), and those it does not
+// settle go on to the fp64 pass.
 #include "common.cuh"
 #include "inverse_common.cuh"
 #include "launch.h"
@@ -78,20 +79,13 @@ __host__ __device__ inline long long rf_tile_off(long long T, int s, long long r
   return (((long long)s * T + rb) * (4 * T) + kb) * (kRfM * kRfBK);
 }
 
-// Probes of the decision after a step: kRfProbes of them,
-//   v_p(i) = s'(i) H16[p][i mod 16],  H16[p][b] = (-1)^popcount(p & b),
-// s'(i) = +-1 from the splitmix64 finaliser of i offset by 2^40 (a sign
-// stream apart from the fp32 pass's probes).  Each is a Rademacher vector;
-// their mean squared residual sums over the same-residue pairs mod 16, so
-// for a residual close to rank one (what a Newton step leaves: I - X1 D =
-// (I - X0 D)^2 up to rounding) it has the spread of sixteen independent
-// probes: an estimate below half the true residual has a probability near
-// 1e-3, against near 0.09 with four.
-constexpr int kRfProbes = 16;
-__device__ __forceinline__ float rf_sign(long long i) { return probe_base_sign(i + (1LL << 40)); }
-__device__ __forceinline__ float hadamard16(int p, int b) {
-  return (__popc((unsigned)(p & b & 15)) & 1) ? -1.f : 1.f;
-}
+// Probes of the decision after a step: kRfProbes independent Rademacher
+// vectors (probe16 in probes.cuh).  A Newton step leaves I - X1 D =
+// (I - X0 D)^2 up to rounding, a residual close to rank one: the mean of
+// sixteen squared projections then gives an estimate below half the true
+// residual with a probability near 1e-3 (chi-square with sixteen degrees of
+// freedom below four), against near 0.09 with four.
+constexpr int kRfProbes = kProbes16;
 
 // Per-matrix refinement buffers, at m.off_ref in the work region (np = 128 T):
 //   xs  bf16 [6][T][4T] tiles   slices of X0
@@ -581,9 +575,8 @@ __global__ void __launch_bounds__(256) rf_sym_kernel(InvCtx c) {
 // w = D v for the kRfProbes probes of each candidate, once (D does not change
 // over the steps).  A warp per row r, D read by symmetry from its upper
 // triangle (the row segment from r on, the column segment above r), with
-// gamma_extra on the diagonal: lane l meets only columns of residue l mod 16,
-// so each lane keeps one double-float sum Y_b (s'(c) D_rc over c = b mod 16);
-// then w_p = sum_b H16[p][b] Y_b.
+// gamma_extra on the diagonal; each lane keeps the double-float sums of all
+// probes over its columns, and the warp adds them up.
 __global__ void __launch_bounds__(256) rf_w16_kernel(InvCtx c) {
   const int nf = *c.nflagged;
   const int lane = threadIdx.x % 32;
@@ -596,25 +589,26 @@ __global__ void __launch_bounds__(256) rf_w16_kernel(InvCtx c) {
     const RfBufs rb = rf_bufs(c, m);
     const long long np = (long long)m.T * 128;
     for (long long r = gw; r < m.d; r += nw) {
-      float hi = 0.f, lo = 0.f;
+      float hi[kRfProbes], lo[kRfProbes];
+#pragma unroll
+      for (int p = 0; p < kRfProbes; ++p) hi[p] = lo[p] = 0.f;
       for (long long col = lane; col < m.d; col += 32) {
         float x = col >= r ? m.D[r * m.ld_in + col] : m.D[col * m.ld_in + r];
         if (col == r) x += c.gamma_extra;
-        df_add(hi, lo, x * rf_sign(col));  // exact: a sign flip
+        const uint32_t sb = probe16_bits(col);  // bit p: sign of probe p at col
+#pragma unroll
+        for (int p = 0; p < kRfProbes; ++p) df_add(hi[p], lo[p], ((sb >> p) & 1u) ? x : -x);  // exact
       }
-      {  // lanes l and l + 16 hold the same residue class
-        const float oh = __shfl_xor_sync(0xffffffffu, hi, 16), ol = __shfl_xor_sync(0xffffffffu, lo, 16);
-        df_add(hi, lo, oh);
-        lo += ol;
+#pragma unroll
+      for (int p = 0; p < kRfProbes; ++p) {
+        float h = hi[p], l = lo[p];
+        for (int o = 16; o > 0; o >>= 1) {
+          const float oh = __shfl_xor_sync(0xffffffffu, h, o), ol = __shfl_xor_sync(0xffffffffu, l, o);
+          df_add(h, l, oh);
+          l += ol;
+        }
+        if (lane == 0) rb.w16[p * np + r] = df_pack(h, l);
       }
-      float wh = 0.f, wl = 0.f;  // lane p < 16: w_p
-      for (int b = 0; b < 16; ++b) {
-        const float yh = __shfl_sync(0xffffffffu, hi, b), yl = __shfl_sync(0xffffffffu, lo, b);
-        const float sg = hadamard16(lane & 15, b);
-        df_add(wh, wl, sg * yh);
-        wl += sg * yl;
-      }
-      if (lane < kRfProbes) rb.w16[lane * np + r] = df_pack(wh, wl);
     }
   }
 }
@@ -699,11 +693,11 @@ __global__ void __launch_bounds__(128) rf_decide_kernel(InvCtx c) {
   // per-thread sums in fp32 (a few hundred terms), the block's in fp64
   float e2 = 0.f;
   for (long long r = threadIdx.x; r < m.d; r += 128) {
-    const float sr = rf_sign(r);
+    const uint32_t sb = probe16_bits(r);
 #pragma unroll
     for (int p = 0; p < kRfProbes; ++p) {
       const float2 yv = y[p * np + r];
-      const float dv = (yv.x - sr * hadamard16(p, (int)(r & 15))) + yv.y;
+      const float dv = (yv.x - (((sb >> p) & 1u) ? 1.f : -1.f)) + yv.y;
       e2 = fmaf(dv, dv, e2);
     }
   }

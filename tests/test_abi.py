@@ -371,3 +371,97 @@ int main() {
                 assert 64 * q == 9 * C and (X[col] == 1.0 if j == 0 else col >= d)
             else:
                 assert 64 * q > 9 * C
+
+
+def test_residual_probes_algebra_and_spread():
+    # The inverse's four probes v_p(i) = s(i) H4[p][c(i)] (probes.cuh): the
+    # mean over p of v_p(i) v_p(j) is s(i) s(j) when the hashed classes agree,
+    # else zero; classes and signs are balanced.  For a rank-one residual
+    # u u^T, the estimate's square over the truth is mean_p (u.v_p)^2 / |u|^2;
+    # with u on every 4th index (a periodic pattern that would put all of u in
+    # one class if the class were i mod 4: chi-square with one degree of
+    # freedom, an estimate below half the truth 38 % of the time) it must
+    # behave like four independent probes (chi2_4 / 4 < 1/4: 9.0 %).  The
+    # Newton step's sixteen independent probes: chi2_16 / 16 < 1/4: 0.11 %.
+    # The preconditioning check's right probes (gemm_tc.h), u on every 8th
+    # index: chi2_8 / 8 < 1/4: 1.9 % (i mod 8 classes would give 38 %).
+    src = r"""
+#include <cuda_runtime.h>
+#include <cstdio>
+#include <random>
+#include "probes.cuh"
+#include "gemm_tc.h"
+using namespace kfac;
+static float zright(long long i, int k) {  // right probe k of the preconditioning check, by its definition
+  const unsigned hh = probe_hash((unsigned)(i >> 3));
+  const int e = (int)(i & 7);
+  const float sg = ((hh >> e) & 1u) ? -1.f : 1.f;
+  return sg * hadamard8(k, e ^ probe_class_offset(hh, 0));
+}
+int main() {
+  long long bad = 0;
+  for (long long i = 0; i < 2048; ++i)
+    for (long long j = 0; j < 2048; j += 7) {
+      float a = 0.f;
+      for (int p = 0; p < 4; ++p) a += probe4(i, p) * probe4(j, p);
+      const float want = probe_class(i) == probe_class(j) ? 4.f * probe_base_sign(i) * probe_base_sign(j) : 0.f;
+      bad += a != want;
+      for (int p = 0; p < 4; ++p) bad += probe4(i, p) * probe4(i, p) != 1.f;
+    }
+  long long cls[4] = {0, 0, 0, 0}, pos = 0;
+  for (long long i = 0; i < 1000000; ++i) {
+    ++cls[probe_class(i)];
+    pos += probe_base_sign(i) > 0.f;
+  }
+  std::mt19937_64 rng(12345);
+  std::normal_distribution<double> n01;
+  const int d = 1024, trials = 20000;
+  long long u4 = 0, u16 = 0, u8 = 0;
+  std::vector<double> u(d);
+  for (int t = 0; t < trials; ++t) {
+    double n2 = 0.0;
+    for (int i = 0; i < d; ++i) {
+      u[i] = (i % 4 == 0) ? n01(rng) : 0.0;
+      n2 += u[i] * u[i];
+    }
+    double e4 = 0.0, e16 = 0.0;
+    for (int p = 0; p < 4; ++p) {
+      double s = 0.0;
+      for (int i = 0; i < d; i += 4) s += u[i] * probe4(i, p);
+      e4 += s * s;
+    }
+    for (int p = 0; p < 16; ++p) {
+      double s = 0.0;
+      for (int i = 0; i < d; i += 4) s += u[i] * probe16(i, p);
+      e16 += s * s;
+    }
+    u4 += e4 / 4.0 / n2 < 0.25;
+    u16 += e16 / 16.0 / n2 < 0.25;
+    double m2 = 0.0, e8 = 0.0;
+    for (int i = 0; i < d; i += 8) m2 += u[i] * u[i];
+    for (int k = 0; k < 8; ++k) {
+      double s = 0.0;
+      for (int i = 0; i < d; i += 8) s += u[i] * zright(i, k);
+      e8 += s * s;
+    }
+    u8 += e8 / 8.0 / m2 < 0.25;
+  }
+  printf("%lld %lld %lld %lld %lld %lld %lld %lld %lld\n", bad, cls[0], cls[1], cls[2], cls[3], pos, u4, u16, u8);
+  return 0;
+}
+"""
+    csrc = os.path.join(ROOT, "infra_fac_factors_gb300", "csrc")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "t.cpp")
+        exe = os.path.join(td, "t")
+        open(c, "w").write(src)
+        subprocess.run(["g++", "-O2", "-std=c++17", "-I", csrc, "-I", cuda_inc, c, "-o", exe], check=True)
+        out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()
+    bad, c0, c1, c2, c3, pos, u4, u16, u8 = map(int, out)
+    assert bad == 0
+    assert all(abs(cnt - 250000) < 2500 for cnt in (c0, c1, c2, c3)) and abs(pos - 500000) < 2500
+    trials = 20000
+    assert 0.075 < u4 / trials < 0.106, u4        # chi2_4 / 4 < 1/4: 0.0902
+    assert u16 / trials < 0.004, u16              # chi2_16 / 16 < 1/4: 0.0011
+    assert u8 / trials < 0.035, u8                # chi2_8 / 8 < 1/4: 0.019
