@@ -381,8 +381,14 @@ __global__ void __launch_bounds__(kGtThreads, 1) gemm_tc_kernel(const __grid_con
 }
 
 // ------------------------------------------------------------------ fp32 -> bf16 slices
-constexpr int kSplitSeg = 256;   // columns of one warp unit (32 lanes x 8)
-constexpr int kSplitChunk = 64;  // warp units per block iteration (8 warps x 8)
+constexpr int kSplitSeg = 256;  // columns of one warp unit (32 lanes x 8)
+// Two shapes of the split: eight warps per block over a grid of eight blocks
+// per SM (the split running alone), or four warps per block with one block
+// per chunk, small enough (128 threads, 8 K registers) to run beside a
+// preconditioning GEMM block on the same SM.  A block iteration takes a chunk
+// of kSplitUnits warp units per warp.
+constexpr int kSplitUnits = 8;
+__host__ __device__ constexpr int split_chunk(int nw) { return nw * kSplitUnits; }
 
 // p[k] = sum_e z_k[c0 + e] x[e] for the eight probes z_k of gemm_tc.h
 // (c0 a multiple of 8; bit offset `shift`)
@@ -405,10 +411,10 @@ __device__ __forceinline__ void probe8(const float (&x)[8], long long c0, int sh
   for (int k = 0; k < 8; ++k) p[k] *= hadamard8(k, t);  // the class offset t
 }
 
-template <int NP>
-__global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ SplitParams prm) {
+template <int NP, int NW>
+__global__ void __launch_bounds__(NW * 32, 32 / NW) split_kernel(const __grid_constant__ SplitParams prm) {
   // warp unit = 256 consecutive columns of one row (8 per lane); chunks of
-  // kSplitChunk units never straddle two matrices, so the matrix lookup is
+  // split_chunk(NW) units never straddle two matrices, so the matrix lookup is
   // block-uniform.  Each warp fetches its next unit's row segment while it
   // slices the current one.
   if (prm.flags != nullptr) {  // a re-run over the flagged matrices: none flagged, nothing to do
@@ -433,8 +439,8 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
     if (prm.flags != nullptr && it.flag_idx >= 0 && prm.flags[it.flag_idx] == 0) continue;
     const long long segs = (it.cols + kSplitSeg - 1) / kSplitSeg;
     const long long work = it.rows * segs;
-    const long long w0 = (ch - it.item_begin) * kSplitChunk;
-    const long long w_end = w0 + kSplitChunk < work ? w0 + kSplitChunk : work;
+    const long long w0 = (ch - it.item_begin) * split_chunk(NW);
+    const long long w_end = w0 + split_chunk(NW) < work ? w0 + split_chunk(NW) : work;
     // the lane's 8 values of unit u (zero past the row's end)
     auto fetch = [&](long long u, float (&x)[8]) {
       const long long r = u / segs;
@@ -457,28 +463,40 @@ __global__ void __launch_bounds__(256) split_kernel(const __grid_constant__ Spli
     long long unit = w0 + warp;
     float xn[8];
     if (unit < w_end) fetch(unit, xn);
-    for (; unit < w_end; unit += 8) {
+    for (; unit < w_end; unit += NW) {
       float x[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = xn[e];
-      if (unit + 8 < w_end) fetch(unit + 8, xn);
+      if (unit + NW < w_end) fetch(unit + NW, xn);
       const long long r = unit / segs;
       const long long c0 = (unit - r * segs) * kSplitSeg + lane * 8;
       if (c0 < it.cols) split8_store<NP>(x, it.dst + r * it.ld_dst + c0, it.slice_stride);
       if (it.probe != nullptr) {  // warp-uniform
         float p[8];
         probe8(x, c0, it.probe_shift, p);
+        // reduce-scatter over the warp: offsets 16, 8, 4 halve the values
+        // held, offsets 2 and 1 complete the sum; lane 4k + j then holds
+        // probe k's sum over the unit
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) p[k] += __shfl_xor_sync(0xffffffffu, p[k], o);
-        if (lane < kProbeN) {
-          float v = p[0];
-#pragma unroll
-          for (int k = 1; k < 8; ++k)
-            if (lane == k) v = p[k];
-          atomicAdd(it.probe + r * kProbeN + lane, v);
+        for (int i = 0; i < 4; ++i) {
+          const bool up = lane & 16;
+          const float send = up ? p[i] : p[i + 4], keep = up ? p[i + 4] : p[i];
+          p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
         }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const bool up = lane & 8;
+          const float send = up ? p[i] : p[i + 2], keep = up ? p[i + 2] : p[i];
+          p[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        }
+        {
+          const bool up = lane & 4;
+          const float send = up ? p[0] : p[1], keep = up ? p[1] : p[0];
+          p[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+        p[0] += __shfl_xor_sync(0xffffffffu, p[0], 2);
+        p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
+        if ((lane & 3) == 0) atomicAdd(it.probe + r * kProbeN + (lane >> 2), p[0]);
       }
     }
   }
@@ -497,11 +515,12 @@ static bool encode_slices(EncodeTiledFn enc, CUtensorMap* map, const uint16_t* b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int launch_split(const SplitItem* items, int n, int planes, const int* flags, cudaStream_t stream) {
+int launch_split(const SplitItem* items, int n, int planes, const int* flags, cudaStream_t stream, bool compact) {
   if (planes != 2 && planes != 3) return KFAC_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
+  const int nw = compact ? 4 : 8;
   for (int base = 0; base < n; base += kSplitMax) {
     const int cnt = n - base < kSplitMax ? n - base : kSplitMax;
     SplitParams prm;
@@ -509,21 +528,29 @@ int launch_split(const SplitItem* items, int n, int planes, const int* flags, cu
     long long total = 0;
     for (int i = 0; i < cnt; ++i) {
       prm.items[i] = items[base + i];
-      prm.items[i].item_begin = total;  // in chunks of kSplitChunk warp units
+      prm.items[i].item_begin = total;  // in chunks of split_chunk(nw) warp units
       const long long work = prm.items[i].rows * ((prm.items[i].cols + kSplitSeg - 1) / kSplitSeg);
-      total += (work + kSplitChunk - 1) / kSplitChunk;
+      total += (work + split_chunk(nw) - 1) / split_chunk(nw);
     }
     prm.n = cnt;
     prm.flags = flags;
     prm.planes = planes;
     prm.total_items = total;
     if (total == 0) continue;
-    const long long cap = (long long)sms * 8;
-    const unsigned grid = (unsigned)(total < cap ? total : cap);
-    if (planes == 3)
-      split_kernel<3><<<grid, 256, 0, stream>>>(prm);
-    else
-      split_kernel<2><<<grid, 256, 0, stream>>>(prm);
+    if (compact) {  // one block per chunk: blocks come and go beside the GEMM's
+      const unsigned grid = (unsigned)total;
+      if (planes == 3)
+        split_kernel<3, 4><<<grid, 128, 0, stream>>>(prm);
+      else
+        split_kernel<2, 4><<<grid, 128, 0, stream>>>(prm);
+    } else {
+      const long long cap = (long long)sms * 8;
+      const unsigned grid = (unsigned)(total < cap ? total : cap);
+      if (planes == 3)
+        split_kernel<3, 8><<<grid, 256, 0, stream>>>(prm);
+      else
+        split_kernel<2, 8><<<grid, 256, 0, stream>>>(prm);
+    }
     count_launch();
     if (cudaGetLastError() != cudaSuccess) return KFAC_ERR_CUDA;
   }

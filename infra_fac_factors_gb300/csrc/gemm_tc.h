@@ -87,7 +87,10 @@ __host__ __device__ __forceinline__ float hadamard8(int k, int b) {
 
 // `planes` bf16 slices per fp32 value (2 or 3).  Items whose flag_idx >= 0 run
 // only when flags[flag_idx] != 0 (flags may be null: every item runs).
-int launch_split(const SplitItem* items, int n, int planes, const int* flags, cudaStream_t stream);
+// compact: small blocks, one per chunk of rows, that fit beside a GEMM block
+// on one SM (for a split that overlaps the GEMMs of other matrices).
+int launch_split(const SplitItem* items, int n, int planes, const int* flags, cudaStream_t stream,
+                 bool compact = false);
 // ns = operand slices read per product: 3 (six MMAs per multiply-add, all 24
 // bits) or 2 (three MMAs: hi*hi + hi*mid + mid*hi, 16 bits).  Split outputs
 // are written with ns slices.  Problems whose flag_idx >= 0 run only when

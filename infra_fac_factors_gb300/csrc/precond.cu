@@ -35,6 +35,8 @@
 // bits in pc_weight_kernel, from the stored out, after the check.
 // inv_a and inv_g are symmetric, so their rows serve as the K-major operands,
 // and s = inv_g Z' = (Z'^T inv_g)^T.
+#include <mutex>
+
 #include "common.cuh"
 #include "gemm_tc.h"
 #include "launch.h"
@@ -145,12 +147,16 @@ __device__ __forceinline__ void right_probe8(const float (&x)[8], long long c0, 
 // (16 values) are reduce-scattered in 16 shuffles; lane pairs (2j, 2j + 1)
 // then hold value j (q_0..7 for j < 8, w_0..7 after) and multiply it by
 // z'_l[r] (for q) or s_l[r] (for w), each lane of the pair for four l.
-__global__ void __launch_bounds__(256) pc_check_kernel(const __grid_constant__ PcChkParams prm) {
+// NW warps per block: eight (the check running alone) or two (one block per
+// NW units, 64 threads and 8 K registers: it fits beside a preconditioning
+// GEMM block on one SM).
+template <int NW>
+__global__ void __launch_bounds__(NW * 32, 16 / NW) pc_check_kernel(const __grid_constant__ PcChkParams prm) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // value this lane holds after the reduce-scatter: bits 4..1 of the lane
   const int j = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
   const int is_w = j >> 3, kj = j & 7, l0 = (lane & 1) * 4;
-  for (long long u = (long long)blockIdx.x * 8 + warp; u < prm.total_units; u += (long long)gridDim.x * 8) {
+  for (long long u = (long long)blockIdx.x * NW + warp; u < prm.total_units; u += (long long)gridDim.x * NW) {
     int lo = 0, hi = prm.n;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -364,7 +370,7 @@ __global__ void pc_route_fill_kernel(int* route, int n, int v) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) route[i] = v;
 }
 
-static int launch_check(int n, const PcChkItem* items, cudaStream_t stream) {
+static int launch_check(int n, const PcChkItem* items, cudaStream_t stream, bool compact = false) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
   const int sms = device_sm_count(dev);
@@ -381,12 +387,145 @@ static int launch_check(int n, const PcChkItem* items, cudaStream_t stream) {
     }
     prm->n = cnt;
     prm->total_units = total;
-    const long long blocks = (total + 7) / 8, cap = (long long)sms * 8;
-    pc_check_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, stream>>>(*prm);
+    if (total == 0) continue;
+    if (compact) {
+      pc_check_kernel<2><<<(unsigned)((total + 1) / 2), 64, 0, stream>>>(*prm);
+    } else {
+      const long long blocks = (total + 7) / 8, cap = (long long)sms * 8;
+      pc_check_kernel<8><<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, stream>>>(*prm);
+    }
     count_launch();
     if (cudaGetLastError() != cudaSuccess) rc = KFAC_ERR_CUDA;
   }
   delete prm;
+  return rc;
+}
+
+// ------------------------------------------------------------------ layer groups
+// A large AUTO call runs its layers in groups (contiguous, of about equal GEMM
+// work): the GEMMs of group g on a highest-priority stream of the library
+// while the split of group g + 1 and the check of group g - 1 run on two
+// lowest-priority streams, in blocks small enough to share an SM with a GEMM
+// block (the GEMMs are bound by the tensor pipe, the split and the check by
+// memory).  Only the first group's split and the last group's check run alone.
+constexpr int kPcMaxGroups = 8;
+constexpr double kPcGroupWork = 7.0e11;  // GEMM flops (2 M N K) per group, about
+
+struct PcStreams {
+  cudaStream_t hi = nullptr, lo = nullptr, lo2 = nullptr;
+  cudaEvent_t fork = nullptr, split_done[kPcMaxGroups] = {}, gemm_done[kPcMaxGroups] = {}, hi_done = nullptr,
+              chk_done = nullptr;
+};
+
+// The streams and events of the caller stream's set, created once (up to four
+// caller streams per device); false when no set is free: the call then runs
+// in one group on the caller's stream.  A set is not meant for concurrent
+// calls from several host threads on the same caller stream.
+static bool pc_streams(int dev, cudaStream_t caller, PcStreams* out) {
+  constexpr int kSets = 4;
+  static std::mutex mu;
+  static PcStreams table[64][kSets];
+  static cudaStream_t owner[64][kSets];
+  if (dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  int slot = -1;
+  for (int i = 0; i < kSets && slot < 0; ++i)
+    if (table[dev][i].hi && owner[dev][i] == caller) slot = i;
+  for (int i = 0; i < kSets && slot < 0; ++i)
+    if (!table[dev][i].hi) slot = i;
+  if (slot < 0) return false;
+  PcStreams& t = table[dev][slot];
+  if (!t.hi) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return false;
+    PcStreams n;
+    cudaEvent_t* evs[] = {&n.fork, &n.hi_done, &n.chk_done};
+    for (cudaEvent_t* e : evs)
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+    for (int g = 0; g < kPcMaxGroups; ++g)
+      if (cudaEventCreateWithFlags(&n.split_done[g], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&n.gemm_done[g], cudaEventDisableTiming) != cudaSuccess)
+        return false;
+    if (cudaStreamCreateWithPriority(&n.lo, cudaStreamNonBlocking, least) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&n.lo2, cudaStreamNonBlocking, least) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&n.hi, cudaStreamNonBlocking, greatest) != cudaSuccess)
+      return false;
+    t = n;
+    owner[dev][slot] = caller;
+  }
+  *out = t;
+  return true;
+}
+
+// Group boundaries: first[g] .. first[g + 1] - 1; returns the group count.
+static int pc_groups(int n, const kfac_precond_args* args, int (&first)[kPcMaxGroups + 1]) {
+  double total = 0.0;
+  for (int i = 0; i < n; ++i)
+    total += 2.0 * (double)args[i].d_in * args[i].d_out * (double)(args[i].d_in + args[i].d_out);
+  int G = (int)(total / kPcGroupWork + 0.5);
+  G = G < 1 ? 1 : G > kPcMaxGroups ? kPcMaxGroups : G;
+  if (G > n) G = n;
+  first[0] = 0;
+  int g = 1;
+  double run = 0.0;
+  for (int i = 0; i < n && g < G; ++i) {
+    run += 2.0 * (double)args[i].d_in * args[i].d_out * (double)(args[i].d_in + args[i].d_out);
+    if (run >= total * g / G && i + 1 < n) first[g++] = i + 1;
+  }
+  G = g;
+  first[G] = n;
+  return G;
+}
+
+// The 16-bit pass of AUTO (split with probes, both GEMMs, check) in groups;
+// on return everything is ordered before the caller's stream's next work.
+static int pc_auto_pass_grouped(int G, const int (&first)[kPcMaxGroups + 1], const SplitItem* items,
+                                const GtOperand* g1, const GtOperand* g2, const PcChkItem* chk,
+                                const PcStreams& ps, cudaStream_t stream) {
+  int rc = KFAC_OK;
+  auto ok = [&](cudaError_t e) {
+    if (e != cudaSuccess && rc == KFAC_OK) rc = KFAC_ERR_CUDA;
+    return rc == KFAC_OK;
+  };
+  if (!ok(cudaEventRecord(ps.fork, stream))) return rc;
+  ok(cudaStreamWaitEvent(ps.hi, ps.fork, 0));
+  ok(cudaStreamWaitEvent(ps.lo, ps.fork, 0));
+  ok(cudaStreamWaitEvent(ps.lo2, ps.fork, 0));
+  // the first group's split alone, on the GEMM stream
+  if (rc == KFAC_OK) rc = launch_split(items, 3 * first[1], 2, nullptr, ps.hi);
+  ok(cudaEventRecord(ps.split_done[0], ps.hi));
+  // the other groups' splits, from the first GEMM on
+  ok(cudaStreamWaitEvent(ps.lo, ps.split_done[0], 0));
+  for (int g = 1; g < G && rc == KFAC_OK; ++g) {
+    rc = launch_split(items + 3 * first[g], 3 * (first[g + 1] - first[g]), 2, nullptr, ps.lo, true);
+    ok(cudaEventRecord(ps.split_done[g], ps.lo));
+  }
+  // GEMM launches: GEMM 1 of group 0; then GEMM 2 of group g - 1 together
+  // with GEMM 1 of group g (independent problems, one persistent grid); last,
+  // GEMM 2 of the last group.  The check of group g follows GEMM 2 of group g.
+  GtOperand* ops = new GtOperand[first[G] > 0 ? first[G] : 1];
+  for (int g = 0; g <= G && rc == KFAC_OK; ++g) {
+    int cnt = 0;
+    if (g > 0)
+      for (int i = first[g - 1]; i < first[g]; ++i) ops[cnt++] = g2[i];
+    if (g < G) {
+      for (int i = first[g]; i < first[g + 1]; ++i) ops[cnt++] = g1[i];
+      if (g > 0) ok(cudaStreamWaitEvent(ps.hi, ps.split_done[g], 0));
+    }
+    if (rc == KFAC_OK) rc = launch_gemm_tc(ops, cnt, 2, nullptr, ps.hi);
+    if (g > 0) {
+      ok(cudaEventRecord(ps.gemm_done[g - 1], ps.hi));
+      ok(cudaStreamWaitEvent(ps.lo2, ps.gemm_done[g - 1], 0));
+      const int a = first[g - 1];
+      if (rc == KFAC_OK) rc = launch_check(first[g] - a, chk + a, ps.lo2, g < G);
+    }
+  }
+  delete[] ops;
+  // join (also on failure, so that no side stream is left forked)
+  cudaEventRecord(ps.hi_done, ps.hi);
+  cudaEventRecord(ps.chk_done, ps.lo2);
+  cudaStreamWaitEvent(stream, ps.hi_done, 0);
+  cudaStreamWaitEvent(stream, ps.chk_done, 0);
   return rc;
 }
 
@@ -449,10 +588,18 @@ int launch_precondition(int n, const kfac_precond_args* args, int precision, int
     }
   } else {
     if (cudaMemsetAsync(ws + PL.begin, 0, PL.flags - PL.begin, stream) != cudaSuccess) rc = KFAC_ERR_CUDA;
-    if (rc == KFAC_OK) rc = launch_split(items, 3 * n, 2, nullptr, stream);
-    if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, 2, nullptr, stream);
-    if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, 2, nullptr, stream);
-    if (rc == KFAC_OK) rc = launch_check(n, chk, stream);
+    int first[kPcMaxGroups + 1];
+    const int G = pc_groups(n, args, first);
+    int dev = 0;
+    PcStreams ps;
+    if (rc == KFAC_OK && G > 1 && cudaGetDevice(&dev) == cudaSuccess && pc_streams(dev, stream, &ps)) {
+      rc = pc_auto_pass_grouped(G, first, items, g1, g2, chk, ps, stream);
+    } else {
+      if (rc == KFAC_OK) rc = launch_split(items, 3 * n, 2, nullptr, stream);
+      if (rc == KFAC_OK) rc = launch_gemm_tc(g1, n, 2, nullptr, stream);
+      if (rc == KFAC_OK) rc = launch_gemm_tc(g2, n, 2, nullptr, stream);
+      if (rc == KFAC_OK) rc = launch_check(n, chk, stream);
+    }
     if (rc == KFAC_OK) {
       pc_flag_kernel<<<(n + 127) / 128, 128, 0, stream>>>(acc, n, kPcAutoTol, flags, route);
       count_launch();
