@@ -260,7 +260,15 @@ int kfac_update_running(int n, const kfac_running_args* args, int P,
  * device), so inverses issued on different streams overlap; calls on further
  * caller streams run on their own stream alone (the same results, without the
  * look-ahead).  A set is not meant for concurrent calls from several host
- * threads on the same caller stream.                                         */
+ * threads on the same caller stream.
+ * Graphs: with KFAC_REFINE_AUTO the Newton step and the fp64 pass are
+ * launched as one CUDA graph whose conditional nodes skip them when no matrix
+ * is flagged (device-side decision, no host synchronisation).  The library
+ * builds it on the first call for a given batch size, largest block count and
+ * workspace address, and keeps it for the process (up to 64 such graphs per
+ * process; further calls, calls while kfac_profile records, and calls on a
+ * stream that is being captured launch the passes one by one, with the same
+ * results).                                                                  */
 enum kfac_refine { KFAC_REFINE_NONE = 0, KFAC_REFINE_AUTO = 1, KFAC_REFINE_ALWAYS = 2 };
 
 typedef struct {

@@ -34,6 +34,9 @@
 // fp64, and the fp64 kernels of the other matrices exit at once.
 #include <math.h>
 
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 #include "inverse_common.cuh"
 #include "launch.h"
@@ -420,7 +423,7 @@ size_t inverse_workspace(int n, const kfac_inverse_args* args, int refine) {
   return best;
 }
 
-static int run_fp64_pass(const InvCtx& ctx, int Tmax, cudaStream_t stream) {
+static int run_fp64_pass(const InvCtx& ctx, int Tmax, cudaStream_t stream, bool lookahead = true) {
   const int dsm = diag_smem_bytes<double>();
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KFAC_ERR_CUDA;
@@ -434,7 +437,7 @@ static int run_fp64_pass(const InvCtx& ctx, int Tmax, cudaStream_t stream) {
   // that SMs come free for the chain, beside the next steps' chain.
   cudaStream_t chain = nullptr;
   cudaEvent_t ev[4];
-  const bool split = Tmax > 2 && fp64_chain_stream(dev, stream, &chain, ev);
+  const bool split = lookahead && Tmax > 2 && fp64_chain_stream(dev, stream, &chain, ev);
   if (split) {
     if (cudaEventRecord(ev[0], stream) != cudaSuccess || cudaStreamWaitEvent(chain, ev[0], 0) != cudaSuccess)
       return KFAC_ERR_CUDA;
@@ -472,6 +475,129 @@ static int run_fp64_pass(const InvCtx& ctx, int Tmax, cudaStream_t stream) {
   inv_lauum_kernel<double><<<sms, kDfThreads, 0, stream>>>(ctx);
   count_launch();
   return cudaGetLastError() == cudaSuccess ? KFAC_OK : KFAC_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ AUTO's later passes, skipped when idle
+// The Newton step and the fp64 pass are persistent grids over the flagged
+// list, about 150 launches for the largest factors, each ending at once when
+// nothing is flagged.  A call of AUTO instead launches them as one cached
+// CUDA graph: a one-thread kernel sets a conditional handle from the flagged
+// count, the Newton step runs inside an IF node, a second such kernel reads
+// the count the Newton step left, and the fp64 pass (without its look-ahead
+// stream) runs inside a second IF node.  With nothing flagged the call costs
+// two tiny launches.  The graph is kept per (device, batch, work buffers), so
+// a caller that repeats a call on the same buffers builds it once.
+__global__ void inv_gate_kernel(cudaGraphConditionalHandle h, const int* nflagged) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) cudaGraphSetConditional(h, *nflagged > 0 ? 1u : 0u);
+}
+
+namespace {
+constexpr int kGateKey = 16;
+constexpr size_t kMaxGateGraphs = 64;  // built graphs kept for the process; more calls run the plain launches
+struct GateGraph {
+  unsigned long long key[kGateKey];
+  cudaGraphExec_t exec;
+};
+std::mutex g_gate_mu;
+std::vector<GateGraph> g_gate;
+cudaStream_t g_capture[64];  // a private stream per device to record the bodies on
+
+void gate_key(const InvCtx& c, int n, int Tmax, int dev, unsigned long long (&k)[kGateKey]) {
+  unsigned int gbits = 0;
+  memcpy(&gbits, &c.gamma_extra, sizeof(gbits));
+  const unsigned long long v[kGateKey] = {
+      (unsigned long long)dev, (unsigned long long)n, (unsigned long long)Tmax, (unsigned long long)gbits,
+      (unsigned long long)(uintptr_t)c.ws, (unsigned long long)(uintptr_t)c.mats,
+      (unsigned long long)(uintptr_t)c.st, (unsigned long long)(uintptr_t)c.rowsum,
+      (unsigned long long)(uintptr_t)c.gpart, (unsigned long long)(uintptr_t)c.wpart,
+      (unsigned long long)(uintptr_t)c.probe, (unsigned long long)(uintptr_t)c.flagged,
+      (unsigned long long)(uintptr_t)c.nflagged, (unsigned long long)(uintptr_t)c.region,
+      (unsigned long long)c.want_rowsum, 0ull};
+  memcpy(k, v, sizeof(k));
+}
+
+bool add_gate(cudaGraph_t g, const cudaGraphNode_t* dep, int ndep, cudaGraphConditionalHandle h, const int* nflagged,
+              cudaGraphNode_t* node) {
+  void* argv[2] = {&h, const_cast<int**>(&nflagged)};
+  cudaKernelNodeParams kp = {};
+  kp.func = (void*)inv_gate_kernel;
+  kp.gridDim = dim3(1);
+  kp.blockDim = dim3(32);
+  kp.kernelParams = argv;
+  return cudaGraphAddKernelNode(node, g, dep, (size_t)ndep, &kp) == cudaSuccess;
+}
+
+bool add_if(cudaGraph_t g, cudaGraphNode_t dep, cudaGraphConditionalHandle h, cudaGraphNode_t* node,
+            cudaGraph_t* body) {
+  cudaGraphNodeParams np = {};
+  np.type = cudaGraphNodeTypeConditional;
+  np.conditional.handle = h;
+  np.conditional.type = cudaGraphCondTypeIf;
+  np.conditional.size = 1;
+  if (cudaGraphAddNode(node, g, &dep, nullptr, 1, &np) != cudaSuccess) return false;
+  *body = np.conditional.phGraph_out[0];
+  return true;
+}
+}  // namespace
+
+// The executable graph for (ctx, n, Tmax) on the current device, built on
+// first use; nullptr when it cannot be built (the caller then launches the
+// passes directly).
+static cudaGraphExec_t gated_passes(const InvCtx& ctx, int n, int Tmax) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  unsigned long long key[kGateKey];
+  gate_key(ctx, n, Tmax, dev, key);
+  std::lock_guard<std::mutex> lk(g_gate_mu);
+  for (const GateGraph& e : g_gate)
+    if (memcmp(e.key, key, sizeof(key)) == 0) return e.exec;
+  if (g_gate.size() >= kMaxGateGraphs) return nullptr;
+  if (!g_capture[dev] && cudaStreamCreateWithFlags(&g_capture[dev], cudaStreamNonBlocking) != cudaSuccess) {
+    g_capture[dev] = nullptr;
+    return nullptr;
+  }
+  const cudaStream_t cs = g_capture[dev];
+  cudaGraph_t g = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  bool ok = cudaGraphCreate(&g, 0) == cudaSuccess;
+  cudaGraphConditionalHandle h1 = 0, h2 = 0;
+  ok = ok && cudaGraphConditionalHandleCreate(&h1, g, 0, cudaGraphCondAssignDefault) == cudaSuccess &&
+       cudaGraphConditionalHandleCreate(&h2, g, 0, cudaGraphCondAssignDefault) == cudaSuccess;
+  cudaGraphNode_t g1 = nullptr, c1 = nullptr, g2 = nullptr, c2 = nullptr;
+  cudaGraph_t b1 = nullptr, b2 = nullptr;
+  ok = ok && add_gate(g, nullptr, 0, h1, ctx.nflagged, &g1) && add_if(g, g1, h1, &c1, &b1);
+  if (ok) {  // body 1: the Newton step
+    ok = cudaStreamBeginCaptureToGraph(cs, b1, nullptr, nullptr, 0, cudaStreamCaptureModeRelaxed) == cudaSuccess;
+    if (ok) {
+      const int rc = run_refine_pass(ctx, n, Tmax, cs);
+      cudaGraph_t got = nullptr;
+      ok = cudaStreamEndCapture(cs, &got) == cudaSuccess && rc == KFAC_OK;
+    }
+  }
+  ok = ok && add_gate(g, &c1, 1, h2, ctx.nflagged, &g2) && add_if(g, g2, h2, &c2, &b2);
+  if (ok) {  // body 2: the fp64 pass
+    InvCtx c64 = ctx;
+    c64.pass64 = 1;
+    c64.want_rowsum = 0;
+    ok = cudaStreamBeginCaptureToGraph(cs, b2, nullptr, nullptr, 0, cudaStreamCaptureModeRelaxed) == cudaSuccess;
+    if (ok) {
+      const int rc = run_fp64_pass(c64, Tmax, cs, false);
+      cudaGraph_t got = nullptr;
+      ok = cudaStreamEndCapture(cs, &got) == cudaSuccess && rc == KFAC_OK;
+    }
+  }
+  ok = ok && cudaGraphInstantiate(&exec, g, 0) == cudaSuccess;
+  if (g) cudaGraphDestroy(g);
+  if (!ok) {
+    if (exec) cudaGraphExecDestroy(exec);
+    cudaGetLastError();  // a failed build leaves no error behind: the plain launches follow
+    return nullptr;
+  }
+  GateGraph e;
+  memcpy(e.key, key, sizeof(key));
+  e.exec = exec;
+  g_gate.push_back(e);
+  return exec;
 }
 
 int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra, int refine, int* info, int* route,
@@ -535,11 +661,26 @@ int launch_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extr
       prof_end(KFAC_K_INV_AUX, stream, pm, 0.0);
       count_launch();
       // the flagged matrices first get one Newton step on tensor cores; those
-      // it settles leave the fp64 pass's list
-      rc = run_refine_pass(ctx, cnt, Tmax, stream);
-      if (rc != KFAC_OK) return rc;
-    }
-    if (refine != KFAC_REFINE_NONE) {
+      // it settles leave the fp64 pass's list.  Both passes run from the
+      // gated graph unless the launch profile records (its events would not
+      // be captured) or the caller's stream is itself being captured.
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      const bool gated = !prof_recording() && cudaStreamIsCapturing(stream, &cap) == cudaSuccess &&
+                         cap == cudaStreamCaptureStatusNone;
+      cudaGraphExec_t exec = gated ? gated_passes(ctx, cnt, Tmax) : nullptr;
+      if (exec) {
+        if (cudaGraphLaunch(exec, stream) != cudaSuccess) return KFAC_ERR_CUDA;
+        count_launch();
+        count_launch();
+      } else {
+        rc = run_refine_pass(ctx, cnt, Tmax, stream);
+        if (rc != KFAC_OK) return rc;
+        ctx.pass64 = 1;
+        ctx.want_rowsum = 0;
+        rc = run_fp64_pass(ctx, Tmax, stream);
+        if (rc != KFAC_OK) return rc;
+      }
+    } else if (refine == KFAC_REFINE_ALWAYS) {
       ctx.pass64 = 1;
       ctx.want_rowsum = 0;
       rc = run_fp64_pass(ctx, Tmax, stream);

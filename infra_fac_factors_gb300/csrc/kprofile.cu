@@ -43,6 +43,11 @@ void recycle_all() {
 
 }  // namespace
 
+bool prof_recording() {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  return g_prof_on;
+}
+
 void prof_begin(cudaStream_t stream, ProfMark& m) {
   m.start = nullptr;
   std::lock_guard<std::mutex> lk(g_prof_mu);

@@ -38,6 +38,8 @@ struct ProfMark {
   cudaEvent_t start = nullptr;
 };
 void prof_begin(cudaStream_t stream, ProfMark& m);
+// Whether kfac_profile is recording (its events cannot be captured in a graph).
+bool prof_recording();
 void prof_end(int kind, cudaStream_t stream, const ProfMark& m, double work);
 
 int launch_factors(int n, const kfac_factor_args* args, int dtype, int P, int mirror, cudaStream_t stream);

@@ -321,6 +321,33 @@ def test_damped_inverse_auto_takes_16bit_operands_when_gershgorin_allows():
             assert rel_fro(X, ref) <= 1e-3 and residual(X, D) <= 1e-3
 
 
+def test_auto_refinement_graph_matches_direct_launches():
+    # AUTO runs its Newton step and its fp64 pass from a cached CUDA graph whose
+    # IF nodes skip them when nothing is flagged; while the launch profile
+    # records, the same passes are launched one by one.  Both give the same
+    # bits, with nothing flagged, with a matrix the Newton step settles, and
+    # with one that goes on to the fp64 pass (a negative pivot fails there too).
+    rng = np.random.default_rng(77)
+    bad = spd_case(300, rng)
+    bad[200, 200] = -1.0
+    newton = conv_like_factor(385, 200, 1e-3, rng)
+    ok = spd_case(200, rng)
+    for batch in ([ok], [bad, newton, ok]):
+        capi.kfac_profile(1)
+        try:
+            Xp, infop, routep = run_inverse(batch, capi.KFAC_REFINE_AUTO)
+        finally:
+            capi.kfac_profile(0)
+        Xg, infog, routeg = run_inverse(batch, capi.KFAC_REFINE_AUTO)
+        Xg2, infog2, routeg2 = run_inverse(batch, capi.KFAC_REFINE_AUTO)  # the graph again, built once
+        assert list(infop) == list(infog) == list(infog2)
+        assert list(routep) == list(routeg) == list(routeg2)
+        for a, b, c, i in zip(Xp, Xg, Xg2, infop):
+            if i == 0:
+                assert np.array_equal(a, b) and np.array_equal(b, c)
+    assert list(routep) == [1, 3, 0] and infop[0] > 0 and infop[1] == 0 and infop[2] == 0, (routep, infop)
+
+
 def test_damped_inverse_reports_first_bad_pivot():
     rng = np.random.default_rng(4)
     D = spd_case(300, rng)
