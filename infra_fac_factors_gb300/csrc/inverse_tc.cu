@@ -535,6 +535,8 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
         const InvMat mt = prm.mats[J.m];
         const int jt = J.j + h;
         const long long row = (long long)J.i * 128 + q * 32 + lane;
+        // rows 32-byte aligned: each lane writes whole sectors of its row
+        const bool v8 = (mt.ld_out % 8) == 0 && (reinterpret_cast<uintptr_t>(mt.X) & 31) == 0;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const long long col0 = (long long)jt * 128 + g * 32;
@@ -547,10 +549,17 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
           if (row < mt.d) {
             float* xr = mt.X + row * mt.ld_out + col0;
             if (col0 + 32 <= mt.d && (J.i != jt || mrow <= g * 32)) {
+              if (v8) {
 #pragma unroll
-              for (int t = 0; t < 32; t += 4)
-                *reinterpret_cast<float4*>(xr + t) =
-                    make_float4(run[g * 32 + t], run[g * 32 + t + 1], run[g * 32 + t + 2], run[g * 32 + t + 3]);
+                for (int t = 0; t < 32; t += 8)
+                  st_global_v8(xr + t, run[g * 32 + t], run[g * 32 + t + 1], run[g * 32 + t + 2], run[g * 32 + t + 3],
+                               run[g * 32 + t + 4], run[g * 32 + t + 5], run[g * 32 + t + 6], run[g * 32 + t + 7]);
+              } else {
+#pragma unroll
+                for (int t = 0; t < 32; t += 4)
+                  *reinterpret_cast<float4*>(xr + t) =
+                      make_float4(run[g * 32 + t], run[g * 32 + t + 1], run[g * 32 + t + 2], run[g * 32 + t + 3]);
+              }
             } else {
 #pragma unroll
               for (int t = 0; t < 32; ++t)
