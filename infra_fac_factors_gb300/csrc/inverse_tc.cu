@@ -585,7 +585,10 @@ __global__ void __launch_bounds__(kItThreads, 1) inv_tc_kernel(const __grid_cons
 __host__ __device__ inline long long load_col_start(long long C, long long T) { return C * T - C * (C - 1) / 2; }
 
 // The lower tiles of block columns [c_begin, c_end) of every matrix.
-__global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_begin, int c_end) {
+// mode: kLoadCopy (the tiles into the work buffer), kLoadSums (AUTO's partial
+// sums only), or both
+constexpr int kLoadCopy = 1, kLoadSums = 2;
+__global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_begin, int c_end, int mode) {
   const int mi = blockIdx.y;
   if (!inv_active(c, mi, false)) return;
   const InvMat m = c.mats[mi];
@@ -623,7 +626,7 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_
     }
   }
   __syncthreads();
-  if (c.gpart) {
+  if (c.gpart && (mode & kLoadSums)) {
     // AUTO: per tile, for the rows of block C along the tile's rows and for
     // the rows of block R down its columns (the mirror), the partial sums of
     //   |D_rc| (c != r)      -> gpart: Gershgorin radii (tc_route_kernel) and ||D||_1
@@ -767,6 +770,7 @@ __global__ void __launch_bounds__(256) tc_load_kernel(InvCtx c, TcBufs b, int c_
   // write the lower tile (R, C) of the work buffer along its rows: element
   // (R*128 + j, C*128 + i) = D(C*128 + i, R*128 + j); identity past d, zero
   // above the diagonal, gamma_extra on it
+  if (!(mode & kLoadCopy)) return;
 #pragma unroll 4
   for (int e = t; e < 128 * 32; e += 256) {
     const int j = e / 32, i4 = (e % 32) * 4;
@@ -1369,8 +1373,12 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       const long long bb = tri(Ts[i]) - a;
       cnt_b = bb > cnt_b ? bb : cnt_b;
     }
+    // with the load split, the first outer panel is only copied on the
+    // sweep's stream (the first diagonal block waits for it); its partial
+    // sums are formed beside the sweep with the rest of D
+    const int mode_a = split_load && ctx.gpart ? kLoadCopy : kLoadCopy | kLoadSums;
     timed_launch(KFAC_K_INV_AUX, main, [&] {
-      tc_load_kernel<<<dim3((unsigned)cnt_a, n), 256, kLoadSmem, main>>>(ctx, b, 0, c_split);
+      tc_load_kernel<<<dim3((unsigned)cnt_a, n), 256, kLoadSmem, main>>>(ctx, b, 0, c_split, mode_a);
     });
     cudaStream_t rs = main;  // where the rest of D and the decision go
     if (split_load) {
@@ -1378,8 +1386,13 @@ int run_tc_pass(const InvCtx& ctx, const InvMat* host_mats, int n, int Tmax, con
       // steps leave free), the decision at highest once both parts are in
       rs = aux.hi3;
       if (cudaStreamWaitEvent(aux.lo, aux.start, 0) != cudaSuccess) rc = KFAC_ERR_CUDA;
+      if (ctx.gpart)
+        timed_launch(KFAC_K_INV_AUX, aux.lo, [&] {
+          tc_load_kernel<<<dim3((unsigned)cnt_a, n), 256, kLoadSmem, aux.lo>>>(ctx, b, 0, c_split, kLoadSums);
+        });
       timed_launch(KFAC_K_INV_AUX, aux.lo, [&] {
-        tc_load_kernel<<<dim3((unsigned)cnt_b, n), 256, kLoadSmem, aux.lo>>>(ctx, b, c_split, Tmax);
+        tc_load_kernel<<<dim3((unsigned)cnt_b, n), 256, kLoadSmem, aux.lo>>>(ctx, b, c_split, Tmax,
+                                                                             kLoadCopy | kLoadSums);
       });
       if (cudaEventRecord(aux.norms, aux.lo) != cudaSuccess || cudaStreamWaitEvent(rs, aux.norms, 0) != cudaSuccess ||
           cudaEventRecord(aux.fork, main) != cudaSuccess || cudaStreamWaitEvent(rs, aux.fork, 0) != cudaSuccess)
