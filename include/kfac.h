@@ -305,7 +305,14 @@ int kfac_damped_inverse(int n, const kfac_inverse_args* args, float gamma_extra,
  *                      4e-4, or is not finite, is recomputed as with FP32.
  * route: NULL, or a device int[n] receiving, per layer, the MMAs per
  * multiply-add its result came from (3 or 6).  Invalid precision, or a route
- * pointer not 4-byte aligned, returns KFAC_ERR_INVALID_ARG.                   */
+ * pointer not 4-byte aligned, returns KFAC_ERR_INVALID_ARG.
+ * Streams: an AUTO call with more than about 1 TFLOP of GEMM work runs its
+ * 16-bit pass in groups of layers on three streams that the library creates
+ * once per caller stream (up to four caller streams per device; further ones
+ * run the call on `stream` alone), forked from `stream` and joined back into
+ * it before the call returns: ordering on `stream` is as for a single-stream
+ * call.  A set is not meant for concurrent calls from several host threads on
+ * the same caller stream.                                                    */
 typedef struct {
   const float* inv_g;  int64_t ld_g;
   const float* grad;   int64_t ld_grad;
