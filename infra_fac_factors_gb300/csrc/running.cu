@@ -48,6 +48,12 @@ __global__ void __launch_bounds__(256) update_running_kernel(const __grid_consta
     for (long long cb = c_begin + lane * 4; cb < c_vec_end; cb += 256) {
       float4 f2[2];
       const bool two = cb + 128 < c_vec_end;
+      // the running factor's values, loaded with the shards' (not after their sum)
+      float4 old2[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+      if (!prm.first_step) {
+        old2[0] = *reinterpret_cast<const float4*>(pr.running + off_row + cb);
+        if (two) old2[1] = *reinterpret_cast<const float4*>(pr.running + off_row + cb + 128);
+      }
       {
         float4 v[16];
 #pragma unroll
@@ -86,7 +92,7 @@ __global__ void __launch_bounds__(256) update_running_kernel(const __grid_consta
         if (prm.first_step) {
           rn = f;
         } else {
-          const float4 old = *reinterpret_cast<const float4*>(pr.running + off);
+          const float4 old = old2[h];
           rn.x = fmaf(decay, old.x, keep * f.x);
           rn.y = fmaf(decay, old.y, keep * f.y);
           rn.z = fmaf(decay, old.z, keep * f.z);
